@@ -1,0 +1,196 @@
+"""float64 CPU oracle for the selective state space scan (S6).
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package. The CUDA library and
+its Python binding never import it, and it imports nothing from them.
+
+The arithmetic lives in ``ssm_oracle.c`` (plain float64 C, compiled with gcc
+``-O2`` and no fast-math). This module only compiles it, marshals numpy
+float64 arrays through ctypes, and returns numpy arrays. It adds no arithmetic
+of its own.
+
+What it computes (page title, section):
+  * "State Space Models -- Mamba, S4, and Beyond", "Mamba (S6 -- Selective
+    State Space)", ``_selective_scan``: dA = exp(delta*A), dB = delta*B, the
+    sequential loop h = dA*h + dB*u, y = C.h, plus D*u.
+  * "Mamba: State Space Models Challenge Transformers", "Selective Scan
+    Algorithm" and "Mamba's Innovation: Selection": A of shape [D, N],
+    delta = softplus(delta), gate y * silu(z).
+  * "State-space models (Mamba, S4)", "Training vs Inference Modes": the
+    O(1)-per-token recurrent step on a cached state.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssm_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libssm_oracle.so")
+_lock = threading.Lock()
+_default = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_i64 = ctypes.c_int64
+
+
+def compile_source(src: str, out_path: str) -> str:
+    """Compile an oracle C source into a shared library with gcc (no fast-math,
+    no FMA contraction)."""
+    tmp = out_path + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+           "-ffp-contract=off", "-pthread", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out_path)
+    return out_path
+
+
+def build(force: bool = False) -> str:
+    """Compile ssm_oracle.c into oracle/libssm_oracle.so (only when stale)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    return compile_source(_SRC, _LIB_PATH)
+
+
+def _bind(lib):
+    lib.oracle_softplus.restype = ctypes.c_double
+    lib.oracle_softplus.argtypes = [ctypes.c_double]
+    lib.oracle_silu.restype = ctypes.c_double
+    lib.oracle_silu.argtypes = [ctypes.c_double]
+    lib.oracle_recurrence.restype = None
+    lib.oracle_recurrence.argtypes = [_i64, _i64, _dp, _dp, _dp, _dp, _dp, _dp]
+    lib.oracle_selective_scan.restype = ctypes.c_int
+    lib.oracle_selective_scan.argtypes = (
+        [_i64] * 4 + [_dp] * 8 + [ctypes.c_int] + [_dp] * 3 + [ctypes.c_int])
+    lib.oracle_state_update.restype = ctypes.c_int
+    lib.oracle_state_update.argtypes = (
+        [_i64] * 3 + [_dp] * 9 + [ctypes.c_int] + [_dp])
+    return lib
+
+
+def _f64(a, shape=None):
+    """Contiguous float64 copy (or view) of a, checked against shape."""
+    if a is None:
+        return None
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    if shape is not None and tuple(arr.shape) != tuple(shape):
+        raise ValueError("expected shape %s, got %s" % (tuple(shape), arr.shape))
+    return arr
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_dp)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+class Oracle:
+    """ctypes front end of one compiled oracle library."""
+
+    def __init__(self, lib_path: str):
+        self.path = lib_path
+        self._lib = _bind(ctypes.CDLL(lib_path))
+
+    def softplus(self, v: float) -> float:
+        return self._lib.oracle_softplus(float(v))
+
+    def silu(self, z: float) -> float:
+        return self._lib.oracle_silu(float(z))
+
+    def recurrence(self, Abar, Bbar, C, x, h0):
+        """Discretized recurrence for one channel.
+
+        Abar, Bbar, C: [L, N]; x: [L]; h0: [N]. Returns (y [L], h_L [N]).
+        """
+        Abar = _f64(Abar)
+        L, N = Abar.shape
+        Bbar, C = _f64(Bbar, (L, N)), _f64(C, (L, N))
+        x, h = _f64(x, (L,)), _f64(h0, (N,)).copy()
+        y = np.zeros(L, dtype=np.float64)
+        self._lib.oracle_recurrence(L, N, _ptr(Abar), _ptr(Bbar), _ptr(C), _ptr(x), _ptr(h), _ptr(y))
+        return y, h
+
+    def selective_scan(self, x, delta, A, B, C, D=None, z=None, delta_bias=None,
+                       delta_softplus=False, h0=None, nthreads=None):
+        """Selective scan over [batch, L, dim] with a [dim, N] diagonal A.
+
+        Returns (out [batch, L, dim], final_state [batch, dim, N]), both float64.
+        """
+        x = _f64(x)
+        batch, L, dim = x.shape
+        A = _f64(A)
+        N = A.shape[1]
+        delta = _f64(delta, (batch, L, dim))
+        A = _f64(A, (dim, N))
+        B, C = _f64(B, (batch, L, N)), _f64(C, (batch, L, N))
+        D = _f64(D, (dim,))
+        z = _f64(z, (batch, L, dim))
+        delta_bias = _f64(delta_bias, (dim,))
+        h0 = _f64(h0, (batch, dim, N))
+        out = np.zeros((batch, L, dim), dtype=np.float64)
+        fs = np.zeros((batch, dim, N), dtype=np.float64)
+        rc = self._lib.oracle_selective_scan(
+            batch, L, dim, N, _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+            _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(out),
+            _ptr(fs), int(nthreads or default_threads()))
+        if rc != 0:
+            raise RuntimeError("oracle_selective_scan failed (%d)" % rc)
+        return out, fs
+
+    def state_update(self, state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
+                     delta_softplus=False):
+        """One recurrent step. state: [batch, dim, N] (not modified; a new array is
+        returned). x, delta, z: [batch, dim]; B, C: [batch, N].
+
+        Returns (out [batch, dim], new_state [batch, dim, N]).
+        """
+        st = _f64(state).copy()
+        batch, dim, N = st.shape
+        x, delta = _f64(x, (batch, dim)), _f64(delta, (batch, dim))
+        A = _f64(A, (dim, N))
+        B, C = _f64(B, (batch, N)), _f64(C, (batch, N))
+        D, z = _f64(D, (dim,)), _f64(z, (batch, dim))
+        delta_bias = _f64(delta_bias, (dim,))
+        out = np.zeros((batch, dim), dtype=np.float64)
+        rc = self._lib.oracle_state_update(
+            batch, dim, N, _ptr(st), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+            _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(out))
+        if rc != 0:
+            raise RuntimeError("oracle_state_update failed (%d)" % rc)
+        return out, st
+
+
+def default() -> Oracle:
+    """The oracle built from ssm_oracle.c (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def softplus(v):
+    return default().softplus(v)
+
+
+def silu(z):
+    return default().silu(z)
+
+
+def recurrence(*a, **k):
+    return default().recurrence(*a, **k)
+
+
+def selective_scan(*a, **k):
+    return default().selective_scan(*a, **k)
+
+
+def state_update(*a, **k):
+    return default().state_update(*a, **k)

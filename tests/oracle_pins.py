@@ -1,0 +1,344 @@
+"""Checks that pin the float64 oracle to facts the pages and mathematics fix.
+
+Each ``pin_*`` function takes a compiled oracle (``oracle.Oracle``) and raises
+AssertionError when the oracle disagrees with a fact that does not come from
+the oracle itself: a value printed on the pages, a closed form, a library
+routine, or an invariant of the recurrence. ``test_oracle_pins.py`` runs them
+on the real oracle; ``test_oracle_mutants.py`` runs them on copies of the
+oracle with planted mistakes and requires that every mistake trips one.
+
+Sources (page title, section):
+  * "State-space models (Mamba, S4)", "Worked Example: 2D SSM Step" (the
+    printed 2-D step) and "The Convolution View" (time-invariant case: y is the
+    causal convolution of x with K = (C Bbar, C Abar Bbar, C Abar^2 Bbar, ...),
+    from h_0 = 0).
+  * "State Space Models -- Mamba, S4, and Beyond", "Mamba (S6 -- Selective
+    State Space)" (dA = exp(delta A), dB = delta B, y + D u) and its
+    "Verification Checklist" (recurrent inference must reproduce the scan).
+  * "Mamba: State Space Models Challenge Transformers", "Mamba's Innovation:
+    Selection" (softplus on delta, output gate y * silu(z)).
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+from scipy.special import expit
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def load_golden(name="worked_example_2d.txt"):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split("=", 1)
+            vals[k.strip()] = np.array([float(t) for t in v.split()], dtype=np.float64)
+    return vals
+
+
+def _rng(seed):
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def _close(a, b, rtol, atol=0.0, what=""):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    assert a.shape == b.shape, (what, a.shape, b.shape)
+    err = np.abs(a - b)
+    lim = atol + rtol * np.abs(b)
+    assert np.all(err <= lim), "%s: max err %.3e (worst at %s)" % (
+        what, float(err.max()), np.unravel_index(int(np.argmax(err - lim)), err.shape))
+
+
+# --------------------------------------------------------------------------
+# 1. the worked example
+# --------------------------------------------------------------------------
+def pin_worked_example_core(orc):
+    g = load_golden()
+    N = int(g["N"][0])
+    y, h = orc.recurrence(g["Abar"].reshape(1, N), g["Bbar"].reshape(1, N),
+                          g["C"].reshape(1, N), g["x1"], g["h0"])
+    _close(h, g["h1"], 0, 1e-12, "h1")
+    _close(y, g["y1"], 0, 1e-12, "y1")
+    # the page's intermediate terms: Abar h0 alone (x = 0), Bbar x alone (h0 = 0)
+    _, h_a = orc.recurrence(g["Abar"].reshape(1, N), g["Bbar"].reshape(1, N),
+                            g["C"].reshape(1, N), [0.0], g["h0"])
+    _close(h_a, g["Abar_h0"], 0, 1e-12, "Abar h0")
+    _, h_b = orc.recurrence(g["Abar"].reshape(1, N), g["Bbar"].reshape(1, N),
+                            g["C"].reshape(1, N), g["x1"], np.zeros(N))
+    _close(h_b, g["Bbar_x1"], 0, 1e-12, "Bbar x1")
+
+
+def pin_worked_example_selective_path(orc):
+    """The same step through the full selective path: delta = 1 and
+    A = [ln 0.9, ln 0.5] give Abar = exp(delta A) = diag(0.9, 0.5) and
+    Bbar = delta B = B; no D, no gate."""
+    g = load_golden()
+    N = int(g["N"][0])
+    x = g["x1"].reshape(1, 1, 1)
+    delta = np.ones((1, 1, 1))
+    A = np.log(g["Abar"]).reshape(1, N)
+    B = g["Bbar"].reshape(1, 1, N)
+    C = g["C"].reshape(1, 1, N)
+    out, fs = orc.selective_scan(x, delta, A, B, C, h0=g["h0"].reshape(1, 1, N))
+    _close(fs.reshape(N), g["h1"], 0, 1e-12, "h1 (selective path)")
+    _close(out.reshape(1), g["y1"], 0, 1e-12, "y1 (selective path)")
+    # as a decode step from the same cached state
+    o2, st = orc.state_update(g["h0"].reshape(1, 1, N), g["x1"].reshape(1, 1),
+                              np.ones((1, 1)), A, g["Bbar"].reshape(1, N),
+                              g["C"].reshape(1, N))
+    _close(st.reshape(N), g["h1"], 0, 1e-12, "h1 (decode step)")
+    _close(o2.reshape(1), g["y1"], 0, 1e-12, "y1 (decode step)")
+
+
+# --------------------------------------------------------------------------
+# 2. time-invariant case == causal convolution with K
+# --------------------------------------------------------------------------
+def pin_lti_convolution(orc, seed=11):
+    r = _rng(seed)
+    batch, L, dim, N = 2, 48, 3, 5
+    A = -np.exp(r.standard_normal((dim, N)) * 0.5)
+    dd = np.exp(r.uniform(np.log(1e-2), np.log(0.5), dim))      # one step per channel
+    B0, C0 = r.standard_normal(N), r.standard_normal(N)
+    D = r.uniform(0.5, 1.5, dim)
+    x = r.standard_normal((batch, L, dim))
+    delta = np.broadcast_to(dd, (batch, L, dim)).copy()
+    B = np.broadcast_to(B0, (batch, L, N)).copy()
+    C = np.broadcast_to(C0, (batch, L, N)).copy()
+    out, _ = orc.selective_scan(x, delta, A, B, C, D=D)
+    k = np.arange(L)
+    for d in range(dim):
+        Abar = np.exp(dd[d] * A[d])                                   # [N]
+        Bbar = dd[d] * B0
+        K = (C0[None, :] * Abar[None, :] ** k[:, None] * Bbar[None, :]).sum(1)  # [L]
+        for b in range(batch):
+            ref = np.convolve(x[b, :, d], K)[:L] + D[d] * x[b, :, d]
+            _close(out[b, :, d], ref, 1e-12, 1e-12, "LTI conv (b=%d, d=%d)" % (b, d))
+
+
+# --------------------------------------------------------------------------
+# 3. selective case == brute-force unrolled sum
+# --------------------------------------------------------------------------
+def _unrolled(x, delta, A, B, C, D, z, bias, softplus, h0):
+    """y_k = sum_{i<=k} C_k (prod_{j=i+1..k} Abar_j) Bbar_i x_i
+             + C_k (prod_{j<=k} Abar_j) h0 + D x_k, gated by silu(z_k).
+    Independent of the oracle's loop: explicit products, one term at a time."""
+    batch, L, dim = x.shape
+    N = A.shape[1]
+    dt = delta + (bias if bias is not None else 0.0)
+    if softplus:
+        dt = np.logaddexp(0.0, dt)                        # log(1 + e^v)
+    Abar = np.exp(dt[..., None] * A[None, None])          # [b, L, d, N]
+    Bbar = dt[..., None] * B[:, :, None, :]               # [b, L, d, N]
+    y = np.zeros((batch, L, dim))
+    hL = np.zeros((batch, dim, N))
+    for b in range(batch):
+        for d in range(dim):
+            for kk in range(L):
+                s = np.zeros(N)
+                for i in range(kk + 1):
+                    p = np.ones(N)
+                    for j in range(i + 1, kk + 1):
+                        p = p * Abar[b, j, d]
+                    s = s + p * Bbar[b, i, d] * x[b, i, d]
+                p0 = np.ones(N)
+                for j in range(kk + 1):
+                    p0 = p0 * Abar[b, j, d]
+                h = s + (p0 * h0[b, d] if h0 is not None else 0.0)
+                yk = float(np.dot(C[b, kk], h))
+                if D is not None:
+                    yk += D[d] * x[b, kk, d]
+                if z is not None:
+                    yk *= z[b, kk, d] * expit(z[b, kk, d])
+                y[b, kk, d] = yk
+                if kk == L - 1:
+                    hL[b, d] = h
+    return y, hL
+
+
+def pin_unrolled_sum(orc, seed=12):
+    r = _rng(seed)
+    batch, L, dim, N = 2, 9, 3, 3
+    x = r.standard_normal((batch, L, dim))
+    u = r.standard_normal((batch, L, dim)) * 0.5
+    bias = np.log(np.expm1(np.exp(r.uniform(np.log(1e-2), np.log(0.5), dim))))
+    A = -np.exp(r.standard_normal((dim, N)) * 0.5)
+    A[0, 0] = 0.3                                  # one growing mode: sign matters
+    B = r.standard_normal((batch, L, N))
+    C = r.standard_normal((batch, L, N))
+    D = r.uniform(0.5, 1.5, dim)
+    z = r.standard_normal((batch, L, dim))
+    h0 = r.standard_normal((batch, dim, N))
+    for softplus in (True, False):
+        d_in = u if softplus else np.abs(u) * 0.2
+        out, fs = orc.selective_scan(x, d_in, A, B, C, D=D, z=z, delta_bias=bias,
+                                     delta_softplus=softplus, h0=h0)
+        ry, rh = _unrolled(x, d_in, A, B, C, D, z, bias, softplus, h0)
+        _close(out, ry, 1e-11, 1e-12, "unrolled y (softplus=%s)" % softplus)
+        _close(fs, rh, 1e-11, 1e-12, "unrolled h_L (softplus=%s)" % softplus)
+    # without D / z / bias / h0
+    out, fs = orc.selective_scan(x, np.abs(u) * 0.2, A, B, C)
+    ry, rh = _unrolled(x, np.abs(u) * 0.2, A, B, C, None, None, None, False, None)
+    _close(out, ry, 1e-11, 1e-12, "unrolled y (bare)")
+    _close(fs, rh, 1e-11, 1e-12, "unrolled h_L (bare)")
+
+
+# --------------------------------------------------------------------------
+# 4. invariants
+# --------------------------------------------------------------------------
+def _random_case(r, batch=2, L=32, dim=4, N=6):
+    return dict(
+        x=r.standard_normal((batch, L, dim)),
+        delta=np.exp(r.uniform(np.log(1e-3), np.log(1e-1), (batch, L, dim))),
+        A=-np.exp(r.standard_normal((dim, N)) * 0.5),
+        B=r.standard_normal((batch, L, N)),
+        C=r.standard_normal((batch, L, N)),
+        D=r.uniform(0.5, 1.5, dim),
+        z=r.standard_normal((batch, L, dim)),
+    )
+
+
+def pin_linearity(orc, seed=13):
+    """Delta, B, C, z fixed: y is linear in x (the gate multiplies y by a
+    factor that does not depend on x; D x is linear)."""
+    r = _rng(seed)
+    c = _random_case(r)
+    x1, x2 = c.pop("x"), r.standard_normal(c["delta"].shape)
+    a, b = 0.7, -1.9
+    y1, h1 = orc.selective_scan(x1, **c)
+    y2, h2 = orc.selective_scan(x2, **c)
+    y3, h3 = orc.selective_scan(a * x1 + b * x2, **c)
+    _close(y3, a * y1 + b * y2, 1e-12, 1e-12, "linearity y")
+    _close(h3, a * h1 + b * h2, 1e-12, 1e-12, "linearity h")
+    # homogeneity alone also fixes that nothing in y is independent of x
+    y0, h0 = orc.selective_scan(np.zeros_like(x1), **c)
+    assert np.all(y0 == 0.0) and np.all(h0 == 0.0), "x = 0 must give y = 0, h = 0"
+
+
+def pin_delta_zero(orc, seed=14):
+    """delta = 0: Abar = 1, Bbar = 0, so h stays h0 exactly and
+    y = (C h0 + D x) * silu(z)."""
+    r = _rng(seed)
+    c = _random_case(r)
+    batch, L, dim = c["x"].shape
+    N = c["A"].shape[1]
+    h0 = r.standard_normal((batch, dim, N))
+    c["delta"] = np.zeros_like(c["delta"])
+    out, fs = orc.selective_scan(h0=h0, **c)
+    assert np.array_equal(fs, h0), "delta = 0 must leave the state bit-identical"
+    ref = (np.einsum("btn,bdn->btd", c["C"], h0) + c["D"] * c["x"]) * (c["z"] * expit(c["z"]))
+    _close(out, ref, 1e-12, 1e-12, "delta = 0 output")
+
+
+def pin_delta_large(orc, seed=15):
+    """delta -> infinity with A < 0: Abar -> 0 (exactly 0 in float64 for
+    delta A < -745), so the state resets every step: h_t = delta B_t x_t."""
+    r = _rng(seed)
+    c = _random_case(r)
+    c["delta"] = np.full_like(c["delta"], 1e4)
+    c["A"] = -np.abs(c["A"]) - 0.1
+    out, fs = orc.selective_scan(**c)
+    ht = c["delta"][..., None] * c["B"][:, :, None, :] * c["x"][..., None]   # [b,L,d,N]
+    _close(fs, ht[:, -1], 1e-14, 0, "reset state")
+    ref = ((c["C"][:, :, None, :] * ht).sum(-1) + c["D"] * c["x"]) * (c["z"] * expit(c["z"]))
+    _close(out, ref, 1e-12, 1e-9, "reset output")
+
+
+def pin_n1_closed_form(orc, seed=16):
+    """N = 1, constant delta, B, x: a = e^{delta A}, c = delta B x and
+    h_L = a^L h0 + c (1 - a^L) / (1 - a) (geometric series)."""
+    r = _rng(seed)
+    L = 300
+    for dt, Aval, Bv, xv, h0 in [(0.01, -1.0, 0.8, 1.3, 0.4), (0.2, -3.0, -1.1, 0.5, -2.0),
+                                 (0.05, 0.5, 0.3, -0.7, 1.0)]:
+        x = np.full((1, L, 1), xv)
+        delta = np.full((1, L, 1), dt)
+        A = np.array([[Aval]])
+        B = np.full((1, L, 1), Bv)
+        C = np.full((1, L, 1), 1.0)
+        out, fs = orc.selective_scan(x, delta, A, B, C, h0=np.array([[[h0]]]))
+        a, c = np.exp(dt * Aval), dt * Bv * xv
+        t = np.arange(1, L + 1)
+        ref = a ** t * h0 + c * (1 - a ** t) / (1 - a)
+        _close(out.reshape(L), ref, 1e-11, 1e-13, "geometric series")
+        _close(fs.reshape(1), ref[-1:], 1e-11, 1e-13, "geometric series h_L")
+    del r
+
+
+def pin_split_resume(orc, seed=17):
+    """scan over [0, L) == scan over [L1, L) started from the state that the
+    scan over [0, L1) ends in (the chunk-carry identity)."""
+    r = _rng(seed)
+    c = _random_case(r, L=40)
+    c["delta_bias"] = r.standard_normal(c["A"].shape[0]) * 0.1
+    full, fs = orc.selective_scan(delta_softplus=True, **c)
+    L1 = 17
+    head = {k: (v[:, :L1] if k in ("x", "delta", "B", "C", "z") else v) for k, v in c.items()}
+    tail = {k: (v[:, L1:] if k in ("x", "delta", "B", "C", "z") else v) for k, v in c.items()}
+    y1, h1 = orc.selective_scan(delta_softplus=True, **head)
+    y2, h2 = orc.selective_scan(delta_softplus=True, h0=h1, **tail)
+    assert np.array_equal(np.concatenate([y1, y2], axis=1), full), "split output"
+    assert np.array_equal(h2, fs), "split final state"
+
+
+def pin_decode_equals_scan(orc, seed=18):
+    """Recurrent inference (one step per token on a cached state) reproduces
+    the scan token by token, from the same initial state."""
+    r = _rng(seed)
+    c = _random_case(r, L=12)
+    batch, L, dim = c["x"].shape
+    N = c["A"].shape[1]
+    h0 = r.standard_normal((batch, dim, N))
+    bias = r.standard_normal(dim) * 0.1
+    full, fs = orc.selective_scan(h0=h0, delta_bias=bias, delta_softplus=True, **c)
+    st = h0
+    for t in range(L):
+        y, st = orc.state_update(st, c["x"][:, t], c["delta"][:, t], c["A"], c["B"][:, t],
+                                 c["C"][:, t], D=c["D"], z=c["z"][:, t], delta_bias=bias,
+                                 delta_softplus=True)
+        _close(y, full[:, t], 1e-14, 1e-14, "decode step %d" % t)
+    _close(st, fs, 1e-14, 1e-14, "decode final state")
+
+
+def pin_softplus_silu(orc):
+    """softplus and silu against library routines at float64."""
+    vs = [-800.0, -40.0, -20.0, -3.0, -1e-3, 0.0, 1e-8, 0.5, 3.0, 20.0, 40.0, 700.0]
+    for v in vs:
+        ref = float(np.logaddexp(0.0, v))
+        got = orc.softplus(v)
+        assert abs(got - ref) <= 1e-15 * max(1.0, abs(ref)) + 1e-300, ("softplus", v, got, ref)
+        refs = v * float(expit(v))
+        gots = orc.silu(v)
+        assert abs(gots - refs) <= 1e-15 * max(1.0, abs(refs)) + 1e-300, ("silu", v, gots, refs)
+    # very negative arguments: softplus(v) = e^v - e^{2v}/2 + O(e^{3v}); the
+    # relative accuracy there is what keeps small steps exact
+    for v in (-30.0, -50.0, -300.0):
+        ev = np.exp(v)
+        assert abs(orc.softplus(v) / (ev - ev * ev / 2) - 1.0) < 1e-15, v
+
+
+def pin_thread_invariance(orc, seed=19):
+    r = _rng(seed)
+    c = _random_case(r, batch=3, L=20, dim=7)
+    y1, h1 = orc.selective_scan(nthreads=1, **c)
+    y8, h8 = orc.selective_scan(nthreads=8, **c)
+    assert np.array_equal(y1, y8) and np.array_equal(h1, h8)
+
+
+ALL_PINS = [
+    pin_worked_example_core,
+    pin_worked_example_selective_path,
+    pin_lti_convolution,
+    pin_unrolled_sum,
+    pin_linearity,
+    pin_delta_zero,
+    pin_delta_large,
+    pin_n1_closed_form,
+    pin_split_resume,
+    pin_decode_equals_scan,
+    pin_softplus_silu,
+    pin_thread_invariance,
+]

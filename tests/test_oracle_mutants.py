@@ -1,0 +1,66 @@
+"""Planted mistakes in the oracle must each trip at least one pin.
+
+Every case copies ``oracle/ssm_oracle.c``, applies one plausible slip (a
+dropped term, a wrong sign or index, a swapped operand, a wrong activation),
+compiles the copy with gcc into a temporary directory and runs the pins on it.
+A mutant that passes every pin would mean the pins cannot see that mistake.
+The real oracle source is never modified.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                   "oracle", "ssm_oracle.c")
+
+# (name, text in the oracle source, replacement)
+MUTANTS = [
+    ("drop_D_skip", "if (j->D) y += j->D[d] * xv;", ""),
+    ("wrong_sign_in_exp", "exp(dt * j->A[d * N + n])", "exp(-dt * j->A[d * N + n])"),
+    ("transposed_A", "exp(dt * j->A[d * N + n])", "exp(dt * j->A[n * j->dim + d])"),
+    ("Bbar_without_delta", "const double dBx = dt * j->B[", "const double dBx = j->B["),
+    ("B_time_index_off_by_one", "j->B[(b * L + t) * N + n]",
+     "j->B[(b * L + (t > 0 ? t - 1 : 0)) * N + n]"),
+    ("C_reads_B", "acc += j->C[(b * L + t) * N + n] * h[n];",
+     "acc += j->B[(b * L + t) * N + n] * h[n];"),
+    ("y_reads_state_before_update",
+     "h[n] = dA * h[n] + dBx;\n            acc += j->C[(b * L + t) * N + n] * h[n];",
+     "acc += j->C[(b * L + t) * N + n] * h[n];\n            h[n] = dA * h[n] + dBx;"),
+    ("drop_delta_bias", "if (j->delta_bias) dt += j->delta_bias[d];", ""),
+    ("bias_after_softplus",
+     "if (j->delta_bias) dt += j->delta_bias[d];\n        if (j->delta_softplus) dt = oracle_softplus(dt);",
+     "if (j->delta_softplus) dt = oracle_softplus(dt);\n        if (j->delta_bias) dt += j->delta_bias[d];"),
+    ("softplus_wrong_sign", "log1p(exp(-fabs(v)))", "log1p(exp(fabs(v)))"),
+    ("gate_sigmoid_not_silu", "return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
+    ("gate_before_D", "if (j->D) y += j->D[d] * xv;\n        if (j->z) y *= oracle_silu(j->z[e]);",
+     "if (j->z) y *= oracle_silu(j->z[e]);\n        if (j->D) y += j->D[d] * xv;"),
+    ("h0_ignored", "h[n] = j->h0 ? j->h0[(b * dim + d) * N + n] : 0.0;", "h[n] = 0.0;"),
+    ("final_state_index_transposed", "j->final_state[(b * dim + d) * N + n] = h[n];",
+     "j->final_state[(b * dim + d) + n * (j->batch * dim)] = h[n];"),
+    ("decode_drops_delta_in_exp", "*h = exp(dt * A[d * N + n]) * (*h)",
+     "*h = exp(A[d * N + n]) * (*h)"),
+    ("decode_wrong_B_row", "dt * B[b * N + n] * xv", "dt * B[n] * xv"),
+    ("core_recurrence_drops_state", "h[n] = Abar[t * N + n] * h[n] + Bbar[t * N + n] * x[t];",
+     "h[n] = Abar[t * N + n] + Bbar[t * N + n] * x[t];"),
+    ("core_readout_drops_C", "acc += C[t * N + n] * h[n];", "acc += h[n];"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, "mutation anchor not found exactly once: %s" % name
+    path = tmp_path / ("mut_%s.c" % name)
+    path.write_text(src.replace(old, new))
+    lib = oracle.compile_source(str(path), str(tmp_path / ("libmut_%s.so" % name)))
+    orc = oracle.Oracle(lib)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, RuntimeError, ValueError, FloatingPointError):
+            failed.append(pin.__name__)
+    assert failed, "mutant %s passed every pin" % name
