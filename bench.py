@@ -1,0 +1,529 @@
+#!/usr/bin/env python
+"""Benchmark of the selective scan (Mamba S6) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one ssm_selective_scan_fwd call over one batch of the workload
+(default: bf16, batch 4, L 2048, d_inner 1536, d_state 16, softplus(delta +
+bias), gate), i.e. every step of the scan path. Rank 0 prints one JSON line.
+
+* value: elements (batch * L * dim) per second over the K timed steps, inputs
+  resident in HBM; the K steps rotate over several input sets whose total is
+  larger than twice the L2 cache, so every step reads its inputs from HBM.
+* e2e: the same metric through the same C-ABI call with host buffers:
+  pinned host -> device copies of the step's inputs and a device -> host copy
+  of its output inside the timed region.
+* roofline: algorithmic bytes per call / average call time, against the
+  measured HBM copy bandwidth of this GPU model.
+* decode: the recurrent step ssm_state_update on the decode workload (batch
+  256, dim 5120, N 16), rotating over several cached states.
+* cpu_baseline: the float64 CPU oracle timed on this host (rank 0, N = 1).
+
+N > 1 (torchrun): every rank runs its own replica of the workload on its own
+GPU (the scan has no cross-channel exchange: weak scaling, no collective on
+the data path); the timed region is bracketed by a barrier and the time is
+the maximum over ranks. ``--impl reference`` times the float64 CPU oracle on
+the same workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan elems/s (B·L·D) and achieved HBM GB/s vs B300 peak, 1 GPU"
+DEFAULT_WORKLOAD = "scan_bf16_b4_L2048_d1536_softplus"
+DECODE_WORKLOAD = "decode_bf16_b256_d5120_x64"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_HBM_GBS = 6400.0
+
+
+# ---------------------------------------------------------------------------
+# small utilities (host side)
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(value: float, group=None) -> float:
+    """Maximum of a per-rank float over the process group (identity at N = 1)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return value
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def reduce_sum(value: float, group=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return value
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item())
+
+
+def aggregate(units_this_rank: float, seconds_this_rank: float, group=None):
+    """Whole-job throughput: units of all ranks / slowest rank's time."""
+    total_units = reduce_sum(units_this_rank, group)
+    slowest = reduce_max(seconds_this_rank, group)
+    return total_units / slowest, slowest
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML in a thread."""
+
+    REASONS = {
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+        0x100: "display_clock_setting",
+    }
+
+    def __init__(self, index: int, period_s: float = 0.02):
+        self.index, self.period = index, period_s
+        self.samples = []
+        self.sm_max = None
+        self._stop = threading.Event()
+        self._thread = None
+        self.ok = False
+
+    def start(self):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            self.sm_max = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            return self
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+        return self
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                sm = nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM)
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                self.samples.append((time.time(), sm, r))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def stop(self):
+        self._stop.set()
+        if self._thread:
+            self._thread.join(timeout=2)
+
+    def summary(self, t0=None, t1=None):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        s = [x for x in self.samples if (t0 is None or x[0] >= t0) and (t1 is None or x[0] <= t1)]
+        window = "timed"
+        if len(s) < 3:
+            s, window = self.samples, "warmup+timed"
+        reasons = set()
+        for _, _, r in s:
+            for bit, name in self.REASONS.items():
+                if r & bit and name != "gpu_idle":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median([x[1] for x in s]) if s else None,
+                "sm_max_mhz": self.sm_max, "reasons": sorted(reasons), "samples": len(s),
+                "window": window}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def _upload(arr, dev):
+    import numpy as np
+    import torch
+    if arr is None:
+        return None
+    if arr.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(arr)).to(dev)
+
+
+def _vp(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def bench_scan(args, rank, world, local):
+    import torch
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    spec = I.WORKLOADS[args.workload]
+    inp = I.make_scan_inputs(spec)
+    io = libssm.SSM_BF16 if spec.io == "bf16" else libssm.SSM_F32
+    elems = spec.elements
+    alg_bytes = I.algorithmic_bytes_scan(spec)
+
+    # input sets, rotated so that no step finds its inputs in L2
+    per_set = alg_bytes
+    nsets = max(2, min(16, math.ceil(2 * L2_BYTES / per_set) + 1))
+    base = {k: _upload(v, dev) for k, v in inp.items()}
+    sets = []
+    for i in range(nsets):
+        s = {k: (None if base[k] is None else (base[k] if k in ("A", "D", "delta_bias")
+                                                else base[k].clone()))
+             for k in base}
+        s["out"] = torch.empty_like(base["x"])
+        s["fs"] = (torch.empty((spec.batch, spec.dim, spec.N), dtype=torch.float32, device=dev)
+                   if spec.final_state else None)
+        sets.append(s)
+    plan = libssm.ssm_scan_plan(spec.batch, spec.L, spec.dim, spec.N, io)
+    ws = libssm.alloc_workspace(spec.batch, spec.L, spec.dim, spec.N, io, dev)
+    dims = libssm.make_dims(spec.batch, spec.L, spec.dim, spec.N, io,
+                            None if ws is None else ws.data_ptr(),
+                            0 if ws is None else ws.numel())
+    stream = torch.cuda.current_stream(dev)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    fn = libssm.lib.ssm_selective_scan_fwd
+    call_args = [(_vp(s["x"]), _vp(s["delta"]), _vp(s["A"]), _vp(s["B"]), _vp(s["C"]),
+                  _vp(s["D"]), _vp(s["z"]), _vp(s["delta_bias"]), 1 if spec.delta_softplus else 0,
+                  _vp(s["out"]), _vp(s["fs"]), ctypes.byref(dims), sptr) for s in sets]
+
+    def step(i):
+        rc = fn(*call_args[i % nsets])
+        if rc != 0:
+            raise libssm.SSMError(rc, "ssm_selective_scan_fwd")
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local).start()
+    import torch.distributed as dist
+    if dist.is_initialized():
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist.is_initialized():
+        dist.barrier()
+    clocks.stop()
+    sec = e0.elapsed_time(e1) / 1e3
+    value, slowest = aggregate(elems * args.steps, sec)
+    status = libssm.ssm_get_device_status(spec.batch, spec.L, spec.dim, spec.N, io, ws)
+    if status != 0:
+        raise libssm.SSMError(status, "device status")
+
+    per_call = sec / args.steps
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / per_call / 1e9
+    res = {
+        "value": value, "ms_per_step": slowest / args.steps * 1e3,
+        "gbps": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "ssm_selective_scan_fwd call (%d kernel%s)"
+                               % (plan["kernels"], "s" if plan["kernels"] > 1 else ""),
+                     "algorithmic_bytes_per_call": alg_bytes},
+        "gpu_launches": args.steps * plan["kernels"],
+        "clocks": clocks.summary(t_wall0, t_wall1),
+        "plan": plan,
+        "input_sets": nsets,
+    }
+
+    # end to end: pinned host buffers, copies inside the timed region
+    host = {k: (None if base[k] is None else base[k].cpu().pin_memory())
+            for k in ("x", "delta", "z", "B", "C")}
+    s0 = sets[0]
+    h_out = torch.empty(s0["out"].shape, dtype=s0["out"].dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = h_out.numel() * h_out.element_size()
+    k_e2e = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        for k, t in host.items():
+            if t is not None:
+                s0[k].copy_(t, non_blocking=True)
+        step(0)
+        h_out.copy_(s0["out"], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist.is_initialized():
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(k_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_sec = e0.elapsed_time(e1) / 1e3
+    e2e_value, _ = aggregate(elems * k_e2e, e2e_sec)
+    res["e2e"] = {"value": e2e_value, "unit": "elems/s", "h2d_bytes_per_step": h2d,
+                  "d2h_bytes_per_step": d2h, "steps": k_e2e}
+
+    # quick self-check of the timed output against the oracle on a few channels
+    res["check"] = parity_probe(spec, inp, sets[0]["out"]) if rank == 0 else None
+    del sets
+    torch.cuda.empty_cache()
+    if not args.no_decode:
+        res["decode"] = bench_decode(args, dev, stream)
+    return res, spec
+
+
+def parity_probe(spec, inp, out):
+    """Compare 8 channels of the last timed output with the oracle."""
+    import numpy as np
+    import torch
+    import oracle
+    from selective_state_space_119_b300 import inputs as I
+    dsel = np.linspace(0, spec.dim - 1, 8).astype(np.int64)
+    ry, _ = oracle.selective_scan(
+        I.widen(inp["x"][:, :, dsel]), I.widen(inp["delta"][:, :, dsel]), inp["A"][dsel],
+        I.widen(inp["B"]), I.widen(inp["C"]),
+        D=None if inp["D"] is None else inp["D"][dsel],
+        z=None if inp["z"] is None else I.widen(inp["z"][:, :, dsel]),
+        delta_bias=None if inp["delta_bias"] is None else inp["delta_bias"][dsel],
+        delta_softplus=spec.delta_softplus)
+    y = out[:, :, torch.as_tensor(dsel, device=out.device)].float().cpu().numpy().astype(np.float64)
+    rel = float(np.linalg.norm(y - ry) / np.linalg.norm(ry))
+    mx = float(np.max(np.abs(y - ry) / (1 + np.abs(ry))))
+    return {"channels": len(dsel), "rel_l2": rel, "max_scaled_err": mx}
+
+
+def bench_decode(args, dev, stream):
+    import torch
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+
+    spec = I.WORKLOADS[DECODE_WORKLOAD]
+    small = I.DecodeSpec(spec.batch, spec.dim, steps=4, seed=spec.seed)
+    inp = I.make_decode_inputs(small)
+    io = libssm.SSM_BF16 if spec.io == "bf16" else libssm.SSM_F32
+    state_bytes = spec.batch * spec.dim * spec.N * 4
+    nstates = max(2, min(8, math.ceil(2 * L2_BYTES / state_bytes) + 1))
+    st0 = _upload(inp["state0"], dev)
+    states = [st0.clone() for _ in range(nstates)]
+    tok = [{k: _upload(inp[k][t], dev) for k in ("x", "delta", "z", "B", "C")} for t in range(4)]
+    A, D = _upload(inp["A"], dev), _upload(inp["D"], dev)
+    outs = [torch.empty_like(tok[0]["x"]) for _ in range(4)]
+    dims = libssm.make_dims(spec.batch, 1, spec.dim, spec.N, io)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    fn = libssm.lib.ssm_state_update
+
+    def step(i):
+        t = tok[i % 4]
+        rc = fn(_vp(states[i % nstates]), _vp(t["x"]), _vp(t["delta"]), _vp(A), _vp(t["B"]),
+                _vp(t["C"]), _vp(D), _vp(t["z"]), None, 0, _vp(outs[i % 4]), ctypes.byref(dims),
+                sptr)
+        if rc != 0:
+            raise libssm.SSMError(rc, "ssm_state_update")
+
+    n = max(64, min(args.steps, 2000))
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3 / n
+    alg = I.algorithmic_bytes_decode_step(spec)
+    peak, kind = measured_peaks()
+    gbs = alg / sec / 1e9
+    return {"workload": DECODE_WORKLOAD, "metric": "decode elems/s (B*D per step)",
+            "value": spec.batch * spec.dim / sec, "unit": "elems/s", "us_per_step": sec * 1e6,
+            "us_per_64_steps": sec * 64 * 1e6, "states_rotated": nstates, "timed_steps": n,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "traffic": None, "peak_kind": kind,
+                         "algorithmic_bytes_per_call": alg}}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle arm
+# ---------------------------------------------------------------------------
+def cpu_oracle_rate(spec, inp, min_seconds: float, max_passes: int = 100):
+    """Time the float64 oracle over whole passes of the workload on every host
+    thread until min_seconds have passed (at least one pass)."""
+    import oracle
+    from selective_state_space_119_b300 import inputs as I
+    threads = oracle.default_threads()
+    args = (I.widen(inp["x"]), I.widen(inp["delta"]), inp["A"], I.widen(inp["B"]),
+            I.widen(inp["C"]))
+    kw = dict(D=inp["D"], z=I.widen(inp["z"]), delta_bias=inp["delta_bias"],
+              delta_softplus=spec.delta_softplus, nthreads=threads)
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.selective_scan(*args, **kw)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or passes >= max_passes:
+            break
+    return spec.elements * passes / el, threads, passes, el
+
+
+def run_reference(args, rank, world, budget_s: float = 120.0):
+    """The float64 CPU oracle as the reference arm. One step = the oracle over
+    every token and batch row of a rotating subset of channels, the subset
+    sized so that warm-up + K steps stay within about budget_s seconds."""
+    import numpy as np
+    import oracle
+    from selective_state_space_119_b300 import inputs as I
+    if rank != 0:
+        return
+    spec = I.WORKLOADS[args.workload]
+    inp = I.make_scan_inputs(spec)
+    threads = oracle.default_threads()
+    B, C = I.widen(inp["B"]), I.widen(inp["C"])
+
+    def run(dsel):
+        oracle.selective_scan(
+            I.widen(inp["x"][:, :, dsel]), I.widen(inp["delta"][:, :, dsel]), inp["A"][dsel],
+            B, C, D=None if inp["D"] is None else inp["D"][dsel],
+            z=None if inp["z"] is None else I.widen(inp["z"][:, :, dsel]),
+            delta_bias=None if inp["delta_bias"] is None else inp["delta_bias"][dsel],
+            delta_softplus=spec.delta_softplus, nthreads=threads)
+        return spec.batch * spec.L * len(dsel)
+
+    probe = np.arange(0, spec.dim, max(1, spec.dim // 64))
+    t0 = time.perf_counter()
+    n = run(probe)
+    per_elem = (time.perf_counter() - t0) / n
+    nsteps = args.steps + args.warmup
+    per_step = max(1, int(budget_s / nsteps / per_elem / (spec.batch * spec.L)))
+    per_step = min(spec.dim, per_step)
+    for w in range(args.warmup):
+        run(np.arange(w * per_step, (w + 1) * per_step) % spec.dim)
+    done, t0 = 0, time.perf_counter()
+    for k in range(args.steps):
+        done += run(np.arange(k * per_step, (k + 1) * per_step) % spec.dim)
+    el = time.perf_counter() - t0
+    rate = done / el
+    sample = ("per step: %d of %d channels (rotating), every batch row and token; "
+              "float64 oracle on %d host threads" % (per_step, spec.dim, threads))
+    line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": "elems/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(spec),
+            "cpu_baseline": {"value": rate, "unit": "elems/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": rate, "unit": "elems/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(spec):
+    return {"workload": _name_of(spec),
+            "batch": spec.batch, "seqlen": spec.L, "dim": spec.dim, "dstate": spec.N,
+            "io": spec.io, "delta": "softplus(u + bias)" if spec.delta_softplus else
+            "log-uniform [%g, %g]" % (spec.delta_lo, spec.delta_hi),
+            "A": spec.A_kind, "D": spec.D_kind, "gate": spec.gate,
+            "final_state": spec.final_state,
+            "l2": "rotating input sets, total > 2x the 126 MB L2 (no L2 reuse between steps)"}
+
+
+def _name_of(spec):
+    from selective_state_space_119_b300 import inputs as I
+    for k, v in I.WORKLOADS.items():
+        if v == spec:
+            return k
+    return "custom"
+
+
+# ---------------------------------------------------------------------------
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+                    help="minimum wall time of the CPU oracle baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from selective_state_space_119_b300 import build
+    if rank == 0 or world == 1:
+        build.build(quiet=True)
+    if world > 1:
+        dist.barrier()
+
+    res, spec = bench_scan(args, rank, world, local)
+    if rank == 0:
+        line = {"metric": METRIC, "value": res["value"], "unit": "elems/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "io_dtype": spec.io, "data": "synthetic",
+                "config": workload_config(spec), "gbps": res["gbps"],
+                "roofline": res["roofline"], "e2e": res["e2e"],
+                "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
+                "plan": res["plan"], "check": res["check"]}
+        if "decode" in res:
+            line["decode"] = res["decode"]
+        if world == 1:
+            from selective_state_space_119_b300 import inputs as I
+            inp = I.make_scan_inputs(spec)
+            rate, threads, passes, el = cpu_oracle_rate(spec, inp, args.cpu_seconds)
+            line["cpu_baseline"] = {
+                "value": rate, "unit": "elems/s", "cores": threads, "kind": "oracle",
+                "sample": "whole workload (%d x %d x %d), %d pass(es), %.1f s, all host threads"
+                          % (spec.batch, spec.L, spec.dim, passes, el)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+/*
+ * ssm.h -- C ABI of libssm, the selective state space scan (Mamba S6) for
+ * NVIDIA B300 (sm_103a).
+ *
+ * What the library computes. For every batch row b and channel d (d < dim),
+ * with an N-wide diagonal state h (N = dstate) that starts at zero:
+ *
+ *     dt_t   = delta[b,t,d] (+ delta_bias[d])  (then softplus, if asked)
+ *     Abar_t = exp(dt_t * A[d,:])                 -- N values
+ *     h_t    = Abar_t * h_{t-1} + dt_t * B[b,t,:] * x[b,t,d]
+ *     y_t    = sum_n C[b,t,n] * h_t[n]  + D[d] * x[b,t,d]
+ *     out    = y_t * silu(z[b,t,d])                (when z is given)
+ *
+ * Sources (page title, section):
+ *  - "State Space Models -- Mamba, S4, and Beyond", "Mamba (S6 -- Selective
+ *    State Space)", method _selective_scan: the per-token discretization
+ *    exp(delta * A) and delta * B, the recurrence, C . h and the D skip.
+ *  - "Mamba: State Space Models Challenge Transformers", "Selective Scan
+ *    Algorithm": the call selective_scan(x, delta, A, B, C, D), x [B, L, D],
+ *    A [D, N], D [D]; "Mamba's Innovation: Selection": softplus on delta and
+ *    the output gate y * silu(z).
+ *  - "State-space models (Mamba, S4)", "The Convolution View" (h_0 = 0; y
+ *    reads the updated state) and "Training vs Inference Modes" (the O(1)
+ *    recurrent step of generation, ssm_state_update below).
+ *  - "State Space Models and Mamba", "Mamba: Selective State Spaces"
+ *    (Delta_t = softplus(Linear(x_t))).
+ *
+ * Conventions for every entry point:
+ *  - All tensors are contiguous, row-major, in DEVICE memory, caller-owned.
+ *    The library never allocates, frees or keeps pointers past a call.
+ *  - I/O tensors (x, delta, z, B, C, out) are fp32 or bf16 (dims->io_dtype);
+ *    A, D, delta_bias, final_state and state are always fp32. All arithmetic
+ *    is fp32; bf16 outputs are rounded to nearest even.
+ *  - Every device pointer must be 16-byte aligned, and dim must be a multiple
+ *    of 8 for bf16 I/O and of 4 for fp32 I/O (128-bit accesses along d).
+ *  - Calls only enqueue work on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and return; they never synchronize. Arguments are fully
+ *    validated on the host before anything is enqueued; on error nothing is
+ *    enqueued and a negative SSM_ERR_* code is returned.
+ *  - `out` and `final_state` must not overlap any input (SSM_ERR_ALIAS).
+ *  - Calls that share a workspace must not run concurrently.
+ */
+#ifndef LIBSSM_SSM_H
+#define LIBSSM_SSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so that the header needs no CUDA
+ * include. */
+struct CUstream_st;
+typedef struct CUstream_st* ssm_stream_t;
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+/* Return codes. 0 is success; every error is negative. */
+enum {
+    SSM_OK = 0,
+    SSM_ERR_NULL = -1,      /* a required pointer is NULL                         */
+    SSM_ERR_DIMS = -2,      /* a size is negative, too large, or dstate unsupported */
+    SSM_ERR_DTYPE = -3,     /* io_dtype is not SSM_F32 / SSM_BF16                 */
+    SSM_ERR_ALIGN = -4,     /* pointer not 16-byte aligned, or dim not a multiple
+                               of 8 (bf16) / 4 (fp32)                             */
+    SSM_ERR_WORKSPACE = -5, /* workspace NULL or smaller than ssm_scan_workspace_bytes */
+    SSM_ERR_CUDA = -6,      /* a CUDA launch or query failed (see ssm_last_cuda_error) */
+    SSM_ERR_TIMEOUT = -7,   /* device side: a bounded wait on another CTA gave up  */
+    SSM_ERR_ALIAS = -8      /* an output overlaps an input                         */
+};
+
+/* Problem sizes and the caller-owned workspace.
+ *   batch   : b >= 0
+ *   seqlen  : L >= 0 (ignored by ssm_state_update)
+ *   dim     : d_inner >= 0 (channels)
+ *   dstate  : N, one of 1, 2, 4, 8, 16 (16 is the production size)
+ *   io_dtype: ssm_dtype of x, delta, z, B, C, out
+ *   workspace, workspace_bytes: device scratch for ssm_selective_scan_fwd (see
+ *     ssm_scan_workspace_bytes); may be NULL when that size is 0. Must be
+ *     zero-filled once before its first use; the library leaves it in a state
+ *     that the next call accepts. Ignored by ssm_state_update. */
+typedef struct {
+    int64_t batch, seqlen, dim, dstate;
+    int32_t io_dtype;
+    int32_t chunk_len_hint; /* 0: library's choice; else tokens per L-chunk of the
+                               scan (rounded up to a multiple of 16; the
+                               workspace size follows it)                 */
+    void* workspace;
+    size_t workspace_bytes;
+} ssm_dims;
+
+/*
+ * ssm_selective_scan_fwd -- the selective scan over a whole sequence.
+ *
+ *   x, delta, z, out : [batch, seqlen, dim]  io dtype (z may be NULL: no gate)
+ *   A                : [dim, dstate] fp32 (any sign; < 0 for a stable scan)
+ *   B, C             : [batch, seqlen, dstate] io dtype, shared by all channels
+ *   D                : [dim] fp32, or NULL (no skip term)
+ *   delta_bias       : [dim] fp32, or NULL; added to delta before softplus
+ *   delta_softplus   : nonzero -> dt = softplus(delta + bias)
+ *   final_state      : [batch, dim, dstate] fp32 state after the last token,
+ *                      or NULL
+ * The scan starts from h = 0. seqlen == 0 writes zeros to final_state.
+ */
+int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A,
+                           const void* B, const void* C, const float* D,
+                           const void* z, const float* delta_bias, int delta_softplus,
+                           void* out, float* final_state, const ssm_dims* dims,
+                           ssm_stream_t stream);
+
+/*
+ * ssm_state_update -- one token of recurrent generation on a cached state
+ * ("State-space models (Mamba, S4)", "Training vs Inference Modes"). Exactly
+ * one step of the scan above, with the state updated in place:
+ *
+ *   state            : [batch, dim, dstate] fp32, read and overwritten
+ *   x, delta, z, out : [batch, dim] io dtype (z may be NULL)
+ *   B, C             : [batch, dstate] io dtype
+ *   A, D, delta_bias, delta_softplus : as for the scan
+ * dims->seqlen and the workspace fields are ignored.
+ */
+int ssm_state_update(float* state, const void* x, const void* delta, const float* A,
+                     const void* B, const void* C, const float* D, const void* z,
+                     const float* delta_bias, int delta_softplus, void* out,
+                     const ssm_dims* dims, ssm_stream_t stream);
+
+/* Bytes of workspace ssm_selective_scan_fwd needs for these sizes (0 when the
+ * scan runs in one pass). Depends only on batch, seqlen, dim, dstate and
+ * chunk_len_hint; returns 0 for invalid sizes. */
+size_t ssm_scan_workspace_bytes(const ssm_dims* dims);
+
+/* Launch plan the scan will use for these sizes (for benchmarks and tests). */
+typedef struct {
+    int64_t chunk_len;      /* tokens per L-chunk                       */
+    int64_t nchunks;        /* L-chunks per channel                     */
+    int64_t channels_per_cta;
+    int64_t ctas;           /* CTAs of the main (output) kernel         */
+    int32_t kernels;        /* kernel launches per call                 */
+    int32_t reserved;
+} ssm_plan;
+int ssm_scan_plan(const ssm_dims* dims, ssm_plan* plan);
+
+/* Synchronizes `stream`, then reads the device-side status word of the
+ * workspace: SSM_OK, or SSM_ERR_TIMEOUT when a bounded wait gave up, which
+ * the next call clears. Returns SSM_OK when the plan uses no workspace. */
+int ssm_get_device_status(const ssm_dims* dims, ssm_stream_t stream);
+
+/* Human-readable text for a return code (static storage). */
+const char* ssm_strerror(int code);
+
+/* The last CUDA error code (cudaError_t as int) seen by this thread, 0 if none. */
+int ssm_last_cuda_error(void);
+
+/* Library ABI version: (major << 16) | minor. */
+int ssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LIBSSM_SSM_H */

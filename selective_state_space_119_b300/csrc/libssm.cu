@@ -1,0 +1,270 @@
+// libssm.cu -- the C ABI of libssm: argument validation, launch planning and
+// dispatch. Declarations and the contract of every entry point are in
+// include/ssm.h. No entry point allocates, frees, or synchronizes (except
+// ssm_get_device_status, which is documented to synchronize).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+
+#include "ssm.h"
+#include "ssm_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+constexpr int64_t kMaxDim = int64_t(1) << 31;     // per-axis limit
+constexpr int64_t kMaxElems = int64_t(1) << 40;   // batch * seqlen * dim limit
+// Enough resident CTAs to fill a B300 (148 SMs) about four deep; the chunk
+// count of the scan is chosen to reach it.
+constexpr int64_t kTargetCtas = 148 * 4;
+constexpr int64_t kMinChunk = 64;
+
+int set_cuda(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t io_size(int32_t io) { return io == SSM_BF16 ? 2 : 4; }
+
+bool valid_dstate(int64_t n) { return n == 1 || n == 2 || n == 4 || n == 8 || n == 16; }
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+int check_dims(const ssm_dims* d, bool scan) {
+    if (!d) return SSM_ERR_NULL;
+    if (d->io_dtype != SSM_F32 && d->io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
+    if (d->batch < 0 || d->dim < 0 || (scan && d->seqlen < 0)) return SSM_ERR_DIMS;
+    if (!valid_dstate(d->dstate)) return SSM_ERR_DIMS;
+    if (d->batch >= kMaxDim || d->dim >= kMaxDim || (scan && d->seqlen >= kMaxDim))
+        return SSM_ERR_DIMS;
+    if (scan && d->chunk_len_hint < 0) return SSM_ERR_DIMS;
+    const int64_t L = scan ? d->seqlen : 1;
+    if (d->batch > 0 && d->dim > 0 && L > 0 &&
+        (d->batch > kMaxElems / d->dim || d->batch * d->dim > kMaxElems / L))
+        return SSM_ERR_DIMS;
+    const int64_t vec = d->io_dtype == SSM_BF16 ? 8 : 4;
+    if (d->dim % vec != 0) return SSM_ERR_ALIGN;
+    return SSM_OK;
+}
+
+int make_plan(const ssm_dims* d, ssm::ScanPlan* p) {
+    *p = ssm::ScanPlan{};
+    const int64_t batch = d->batch, L = d->seqlen, dim = d->dim, N = d->dstate;
+    p->channels_per_cta = int64_t(ssm::kScanThreads) * ssm::kScanCPT;
+    if (batch == 0 || L == 0 || dim == 0) return SSM_OK;
+    p->tiles = (dim + p->channels_per_cta - 1) / p->channels_per_cta;
+    const int64_t per_chunk = p->tiles * batch;
+    int64_t chunk;
+    if (d->chunk_len_hint > 0) {
+        chunk = d->chunk_len_hint;
+    } else {
+        int64_t nck = std::max<int64_t>(1, (kTargetCtas + per_chunk - 1) / per_chunk);
+        nck = std::min(nck, std::max<int64_t>(1, (L + kMinChunk - 1) / kMinChunk));
+        chunk = (L + nck - 1) / nck;
+    }
+    chunk = std::max<int64_t>(16, (chunk + 15) / 16 * 16);
+    chunk = std::min(chunk, (L + 15) / 16 * 16);
+    p->chunk_len = chunk;
+    p->nchunks = (L + chunk - 1) / chunk;
+    p->ctas = per_chunk * p->nchunks;
+    if (p->ctas >= (int64_t(1) << 31)) return SSM_ERR_DIMS;
+    p->kernels = p->nchunks > 1 ? 3 : 1;
+    if (p->nchunks > 1) {
+        const size_t carries = size_t(batch) * size_t(p->nchunks - 1) * size_t(dim);
+        p->ws_off_H = ssm::kWsHeaderBytes;
+        p->ws_off_S = p->ws_off_H + align256(carries * size_t(N) * sizeof(float));
+        p->ws_bytes = p->ws_off_S + align256(carries * sizeof(float));
+    }
+    return SSM_OK;
+}
+
+struct Range {
+    const void* p;
+    size_t bytes;
+};
+
+bool overlap(const Range& a, const Range& b) {
+    if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+template <size_t NI, size_t NO>
+int check_alias(const Range (&in)[NI], const Range (&out)[NO]) {
+    for (size_t i = 0; i < NO; ++i) {
+        for (size_t j = 0; j < NI; ++j)
+            if (overlap(out[i], in[j])) return SSM_ERR_ALIAS;
+        for (size_t j = i + 1; j < NO; ++j)
+            if (overlap(out[i], out[j])) return SSM_ERR_ALIAS;
+    }
+    return SSM_OK;
+}
+
+template <size_t K>
+int check_aligned(const void* const (&ptrs)[K]) {
+    for (size_t i = 0; i < K; ++i)
+        if (ptrs[i] && !aligned16(ptrs[i])) return SSM_ERR_ALIGN;
+    return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_version(void) { return (1 << 16) | 0; }
+
+int ssm_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* ssm_strerror(int code) {
+    switch (code) {
+        case SSM_OK: return "success";
+        case SSM_ERR_NULL: return "a required pointer is NULL";
+        case SSM_ERR_DIMS: return "invalid sizes (negative, too large, or unsupported dstate)";
+        case SSM_ERR_DTYPE: return "io_dtype must be SSM_F32 or SSM_BF16";
+        case SSM_ERR_ALIGN:
+            return "pointer not 16-byte aligned, or dim not a multiple of 8 (bf16) / 4 (fp32)";
+        case SSM_ERR_WORKSPACE: return "workspace missing or smaller than ssm_scan_workspace_bytes";
+        case SSM_ERR_CUDA: return "a CUDA call failed (see ssm_last_cuda_error)";
+        case SSM_ERR_TIMEOUT: return "device-side bounded wait gave up";
+        case SSM_ERR_ALIAS: return "an output buffer overlaps an input";
+        default: return "unknown libssm error code";
+    }
+}
+
+int ssm_scan_plan(const ssm_dims* dims, ssm_plan* plan) {
+    if (!plan) return SSM_ERR_NULL;
+    int rc = check_dims(dims, true);
+    if (rc != SSM_OK) return rc;
+    ssm::ScanPlan p;
+    rc = make_plan(dims, &p);
+    if (rc != SSM_OK) return rc;
+    plan->chunk_len = p.chunk_len;
+    plan->nchunks = p.nchunks;
+    plan->channels_per_cta = p.channels_per_cta;
+    plan->ctas = p.ctas;
+    plan->kernels = p.kernels;
+    plan->reserved = 0;
+    return SSM_OK;
+}
+
+size_t ssm_scan_workspace_bytes(const ssm_dims* dims) {
+    if (check_dims(dims, true) != SSM_OK) return 0;
+    ssm::ScanPlan p;
+    if (make_plan(dims, &p) != SSM_OK) return 0;
+    return p.ws_bytes;
+}
+
+int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z,
+                           const float* delta_bias, int delta_softplus, void* out,
+                           float* final_state, const ssm_dims* dims, ssm_stream_t stream) {
+    int rc = check_dims(dims, true);
+    if (rc != SSM_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // Empty problems: nothing to read (empty tensors may carry NULL pointers).
+    if (dims->batch == 0 || dims->dim == 0) return SSM_OK;
+    if (dims->seqlen == 0) {
+        if (!final_state) return SSM_OK;
+        if (!aligned16(final_state)) return SSM_ERR_ALIGN;
+        return set_cuda(cudaMemsetAsync(
+            final_state, 0, size_t(dims->batch) * dims->dim * dims->dstate * 4, s));
+    }
+    if (!x || !delta || !A || !B || !C || !out) return SSM_ERR_NULL;
+    {
+        const void* const ptrs[] = {x, delta, A, B, C, D, z, delta_bias, out, final_state,
+                                    dims->workspace};
+        rc = check_aligned(ptrs);
+        if (rc != SSM_OK) return rc;
+    }
+    ssm::ScanPlan p;
+    rc = make_plan(dims, &p);
+    if (rc != SSM_OK) return rc;
+    if (p.ws_bytes > 0 && (!dims->workspace || dims->workspace_bytes < p.ws_bytes))
+        return SSM_ERR_WORKSPACE;
+
+    const int64_t batch = dims->batch, L = dims->seqlen, dim = dims->dim, N = dims->dstate;
+    const size_t es = io_size(dims->io_dtype);
+    const size_t elems = size_t(batch) * size_t(L) * size_t(dim);
+    const size_t rows = size_t(batch) * size_t(L) * size_t(N);
+    {
+        const Range in[] = {{x, elems * es},      {delta, elems * es},
+                            {z, elems * es},      {B, rows * es},
+                            {C, rows * es},       {A, size_t(dim) * N * 4},
+                            {D, size_t(dim) * 4}, {delta_bias, size_t(dim) * 4},
+                            {dims->workspace, p.ws_bytes}};
+        const Range outs[] = {{out, elems * es},
+                              {final_state, size_t(batch) * dim * N * 4}};
+        rc = check_alias(in, outs);
+        if (rc != SSM_OK) return rc;
+    }
+
+    ssm::ScanArgs a{};
+    a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
+    a.delta_bias = delta_bias; a.softplus = delta_softplus ? 1 : 0;
+    a.out = out; a.final_state = final_state;
+    a.batch = batch; a.L = L; a.dim = dim;
+    a.chunk_len = p.chunk_len; a.nchunks = p.nchunks; a.tiles = p.tiles;
+    if (p.ws_bytes > 0) {
+        char* ws = static_cast<char*>(dims->workspace);
+        a.ws_H = reinterpret_cast<float*>(ws + p.ws_off_H);
+        a.ws_S = reinterpret_cast<float*>(ws + p.ws_off_S);
+    }
+    return set_cuda(ssm::launch_scan(a, p, dims->io_dtype, static_cast<int>(N), s));
+}
+
+int ssm_state_update(float* state, const void* x, const void* delta, const float* A,
+                     const void* B, const void* C, const float* D, const void* z,
+                     const float* delta_bias, int delta_softplus, void* out,
+                     const ssm_dims* dims, ssm_stream_t stream) {
+    int rc = check_dims(dims, false);
+    if (rc != SSM_OK) return rc;
+    if (dims->batch == 0 || dims->dim == 0) return SSM_OK;   // nothing to update
+    if (!state || !x || !delta || !A || !B || !C || !out) return SSM_ERR_NULL;
+    {
+        const void* const ptrs[] = {state, x, delta, A, B, C, D, z, delta_bias, out};
+        rc = check_aligned(ptrs);
+        if (rc != SSM_OK) return rc;
+    }
+    const int64_t batch = dims->batch, dim = dims->dim, N = dims->dstate;
+    const size_t es = io_size(dims->io_dtype);
+    const size_t bd = size_t(batch) * size_t(dim);
+    {
+        const Range in[] = {{x, bd * es},          {delta, bd * es},
+                            {z, bd * es},          {B, size_t(batch) * N * es},
+                            {C, size_t(batch) * N * es}, {A, size_t(dim) * N * 4},
+                            {D, size_t(dim) * 4},  {delta_bias, size_t(dim) * 4}};
+        const Range outs[] = {{out, bd * es}, {state, bd * N * 4}};
+        rc = check_alias(in, outs);
+        if (rc != SSM_OK) return rc;
+    }
+    ssm::StepArgs a{};
+    a.state = state; a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
+    a.delta_bias = delta_bias; a.softplus = delta_softplus ? 1 : 0; a.out = out;
+    a.batch = batch; a.dim = dim;
+    return set_cuda(ssm::launch_state_update(a, dims->io_dtype, static_cast<int>(N),
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ssm_get_device_status(const ssm_dims* dims, ssm_stream_t stream) {
+    int rc = check_dims(dims, true);
+    if (rc != SSM_OK) return rc;
+    ssm::ScanPlan p;
+    rc = make_plan(dims, &p);
+    if (rc != SSM_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    rc = set_cuda(cudaStreamSynchronize(s));
+    if (rc != SSM_OK) return rc;
+    if (p.ws_bytes == 0) return SSM_OK;
+    if (!dims->workspace || dims->workspace_bytes < p.ws_bytes) return SSM_ERR_WORKSPACE;
+    uint32_t status = 0;
+    rc = set_cuda(cudaMemcpy(&status, dims->workspace, sizeof(status), cudaMemcpyDeviceToHost));
+    if (rc != SSM_OK) return rc;
+    return status == 0 ? SSM_OK : -static_cast<int>(status);
+}
+
+}  // extern "C"

@@ -1,0 +1,255 @@
+"""Python binding of libssm (ctypes). Argument marshalling only.
+
+Every step of the scan and of the decode step runs in the CUDA kernels of
+``libssm.so``; PyTorch only supplies device memory, the current stream and
+the output allocations. Importing this module fails loudly when the library
+has not been built (``python -m selective_state_space_119_b300.build``); there
+is no CPU fallback.
+
+The functions carry the C names (``ssm_selective_scan_fwd``,
+``ssm_state_update``, ``ssm_scan_workspace_bytes``, ``ssm_scan_plan``,
+``ssm_get_device_status``, ``ssm_strerror``) and take torch tensors. The raw
+ctypes handle is ``lib`` for callers that hold plain device pointers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "lib", "libssm.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        "libssm.so is not built (%s); run `python -m selective_state_space_119_b300.build`"
+        % LIB_PATH)
+
+lib = ctypes.CDLL(LIB_PATH)
+
+SSM_F32, SSM_BF16 = 0, 1
+SSM_OK = 0
+SSM_ERR_NULL = -1
+SSM_ERR_DIMS = -2
+SSM_ERR_DTYPE = -3
+SSM_ERR_ALIGN = -4
+SSM_ERR_WORKSPACE = -5
+SSM_ERR_CUDA = -6
+SSM_ERR_TIMEOUT = -7
+SSM_ERR_ALIAS = -8
+
+# Every symbol include/ssm.h declares.
+EXPORTED = ("ssm_selective_scan_fwd", "ssm_state_update", "ssm_scan_workspace_bytes",
+            "ssm_scan_plan", "ssm_get_device_status", "ssm_strerror", "ssm_last_cuda_error",
+            "ssm_version")
+
+
+class ssm_dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("dim", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("io_dtype", ctypes.c_int32),
+                ("chunk_len_hint", ctypes.c_int32), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+class ssm_plan(ctypes.Structure):
+    _fields_ = [("chunk_len", ctypes.c_int64), ("nchunks", ctypes.c_int64),
+                ("channels_per_cta", ctypes.c_int64), ("ctas", ctypes.c_int64),
+                ("kernels", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+_vp = ctypes.c_void_p
+_dims_p = ctypes.POINTER(ssm_dims)
+lib.ssm_selective_scan_fwd.restype = ctypes.c_int
+lib.ssm_selective_scan_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
+                                       _vp, _vp, _dims_p, _vp]
+lib.ssm_state_update.restype = ctypes.c_int
+lib.ssm_state_update.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
+                                 _vp, _dims_p, _vp]
+lib.ssm_scan_workspace_bytes.restype = ctypes.c_size_t
+lib.ssm_scan_workspace_bytes.argtypes = [_dims_p]
+lib.ssm_scan_plan.restype = ctypes.c_int
+lib.ssm_scan_plan.argtypes = [_dims_p, ctypes.POINTER(ssm_plan)]
+lib.ssm_get_device_status.restype = ctypes.c_int
+lib.ssm_get_device_status.argtypes = [_dims_p, _vp]
+lib.ssm_strerror.restype = ctypes.c_char_p
+lib.ssm_strerror.argtypes = [ctypes.c_int]
+lib.ssm_last_cuda_error.restype = ctypes.c_int
+lib.ssm_last_cuda_error.argtypes = []
+lib.ssm_version.restype = ctypes.c_int
+lib.ssm_version.argtypes = []
+
+
+class SSMError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = "%s: %s (%d)" % (where, ssm_strerror(code), code)
+        if code == SSM_ERR_CUDA:
+            msg += ", cudaError %d" % lib.ssm_last_cuda_error()
+        super().__init__(msg)
+
+
+def ssm_strerror(code: int) -> str:
+    return lib.ssm_strerror(int(code)).decode()
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != SSM_OK:
+        raise SSMError(rc, where)
+
+
+def make_dims(batch, seqlen, dim, dstate, io, workspace=None, workspace_bytes=0,
+              chunk_len_hint=0) -> ssm_dims:
+    io_code = io if isinstance(io, int) else (SSM_BF16 if str(io) in ("bf16", "torch.bfloat16") else SSM_F32)
+    return ssm_dims(int(batch), int(seqlen), int(dim), int(dstate), io_code, int(chunk_len_hint),
+                    workspace, int(workspace_bytes))
+
+
+def ssm_scan_workspace_bytes(batch, seqlen, dim, dstate, io, chunk_len_hint=0) -> int:
+    d = make_dims(batch, seqlen, dim, dstate, io, chunk_len_hint=chunk_len_hint)
+    return int(lib.ssm_scan_workspace_bytes(ctypes.byref(d)))
+
+
+def ssm_scan_plan(batch, seqlen, dim, dstate, io, chunk_len_hint=0) -> dict:
+    d = make_dims(batch, seqlen, dim, dstate, io, chunk_len_hint=chunk_len_hint)
+    p = ssm_plan()
+    _check(lib.ssm_scan_plan(ctypes.byref(d), ctypes.byref(p)), "ssm_scan_plan")
+    return {k: getattr(p, k) for k, _ in ssm_plan._fields_ if k != "reserved"}
+
+
+# ---------------------------------------------------------------------------
+# torch front end
+# ---------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _io_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return SSM_BF16
+    if t.dtype == torch.float32:
+        return SSM_F32
+    raise TypeError("I/O tensors must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _ptr(t, name, dtype=None, shape=None, device=None) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    return t.data_ptr()
+
+
+def _stream(device, stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def alloc_workspace(batch, seqlen, dim, dstate, io, device, chunk_len_hint=0):
+    """Zero-filled workspace tensor (uint8) of the size the scan needs, or None."""
+    torch = _torch()
+    n = ssm_scan_workspace_bytes(batch, seqlen, dim, dstate, io, chunk_len_hint)
+    if n == 0:
+        return None
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
+                           delta_softplus=False, out=None, final_state=None,
+                           return_final_state=True, workspace=None, chunk_len_hint=0,
+                           stream=None) -> Tuple[object, Optional[object]]:
+    """Selective scan over x [batch, L, dim] (see include/ssm.h).
+
+    Returns (out, final_state); final_state is None when not requested.
+    ``out`` / ``final_state`` may be passed preallocated; ``workspace`` is a
+    zero-initialised uint8 CUDA tensor of at least ssm_scan_workspace_bytes
+    (allocated per call when omitted).
+    """
+    torch = _torch()
+    batch, L, dim = x.shape
+    N = A.shape[1]
+    io = x.dtype
+    dev = x.device
+    if out is None:
+        out = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(batch, L, dim, N, _io_code(x), dev, chunk_len_hint)
+    ws_ptr = _ptr(workspace, "workspace", torch.uint8, device=dev)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    dims = make_dims(batch, L, dim, N, _io_code(x), ws_ptr, ws_bytes, chunk_len_hint)
+    args = (
+        _ptr(x, "x", io, (batch, L, dim), dev),
+        _ptr(delta, "delta", io, (batch, L, dim), dev),
+        _ptr(A, "A", torch.float32, (dim, N), dev),
+        _ptr(B, "B", io, (batch, L, N), dev),
+        _ptr(C, "C", io, (batch, L, N), dev),
+        _ptr(D, "D", torch.float32, (dim,), dev),
+        _ptr(z, "z", io, (batch, L, dim), dev),
+        _ptr(delta_bias, "delta_bias", torch.float32, (dim,), dev),
+        1 if delta_softplus else 0,
+        _ptr(out, "out", io, (batch, L, dim), dev),
+        _ptr(final_state, "final_state", torch.float32, (batch, dim, N), dev),
+    )
+    with torch.cuda.device(dev):
+        rc = lib.ssm_selective_scan_fwd(*args, ctypes.byref(dims), _stream(dev, stream))
+    _check(rc, "ssm_selective_scan_fwd")
+    return out, final_state
+
+
+def ssm_state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
+                     delta_softplus=False, out=None, stream=None):
+    """One recurrent step; ``state`` [batch, dim, N] fp32 is updated in place.
+    x, delta, z: [batch, dim]; B, C: [batch, N]. Returns out [batch, dim]."""
+    torch = _torch()
+    batch, dim, N = state.shape
+    io = x.dtype
+    dev = x.device
+    if out is None:
+        out = torch.empty_like(x)
+    dims = make_dims(batch, 1, dim, N, _io_code(x))
+    args = (
+        _ptr(state, "state", torch.float32, (batch, dim, N), dev),
+        _ptr(x, "x", io, (batch, dim), dev),
+        _ptr(delta, "delta", io, (batch, dim), dev),
+        _ptr(A, "A", torch.float32, (dim, N), dev),
+        _ptr(B, "B", io, (batch, N), dev),
+        _ptr(C, "C", io, (batch, N), dev),
+        _ptr(D, "D", torch.float32, (dim,), dev),
+        _ptr(z, "z", io, (batch, dim), dev),
+        _ptr(delta_bias, "delta_bias", torch.float32, (dim,), dev),
+        1 if delta_softplus else 0,
+        _ptr(out, "out", io, (batch, dim), dev),
+    )
+    with torch.cuda.device(dev):
+        rc = lib.ssm_state_update(*args, ctypes.byref(dims), _stream(dev, stream))
+    _check(rc, "ssm_state_update")
+    return out
+
+
+def ssm_get_device_status(batch, seqlen, dim, dstate, io, workspace, chunk_len_hint=0,
+                          stream=None) -> int:
+    """Synchronize the stream and return the workspace's device status code."""
+    torch = _torch()
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    dims = make_dims(batch, seqlen, dim, dstate, io, ws_ptr, ws_bytes, chunk_len_hint)
+    dev = workspace.device if workspace is not None else torch.device("cuda")
+    with torch.cuda.device(dev):
+        return int(lib.ssm_get_device_status(ctypes.byref(dims), _stream(dev, stream)))
+
+
+# Short aliases.
+selective_scan_fwd = ssm_selective_scan_fwd
+state_update = ssm_state_update

@@ -1,0 +1,130 @@
+"""The C-ABI library on a host without a GPU: it loads, exports every symbol
+include/ssm.h declares, sizes workspaces and plans, and rejects bad arguments
+with the documented codes before touching CUDA (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_119_b300 import build
+
+build.build(quiet=True)
+from selective_state_space_119_b300 import libssm as L  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ssm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssm_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    names = declared_functions()
+    assert set(names) == set(L.EXPORTED), names
+    for n in names:
+        assert hasattr(L.lib, n), n
+
+
+def test_version_and_strerror():
+    assert L.lib.ssm_version() >> 16 == 1
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
+        assert L.ssm_strerror(code) and "unknown" not in L.ssm_strerror(code)
+    assert "unknown" in L.ssm_strerror(-99)
+
+
+def test_struct_layout_matches_header():
+    # int64 x4, int32 x2, pointer, size_t
+    assert ctypes.sizeof(L.ssm_dims) == 4 * 8 + 2 * 4 + 8 + 8
+    assert ctypes.sizeof(L.ssm_plan) == 4 * 8 + 2 * 4
+
+
+def test_workspace_and_plan():
+    # one chunk -> no workspace
+    assert L.ssm_scan_workspace_bytes(1, 64, 256, 16, "bf16", chunk_len_hint=64) == 0
+    p = L.ssm_scan_plan(1, 64, 256, 16, "bf16", chunk_len_hint=64)
+    assert p["nchunks"] == 1 and p["kernels"] == 1
+    # several chunks -> header + carries
+    p = L.ssm_scan_plan(2, 1000, 512, 16, "bf16", chunk_len_hint=100)
+    assert p["chunk_len"] == 112 and p["nchunks"] == 9 and p["kernels"] == 3
+    ws = L.ssm_scan_workspace_bytes(2, 1000, 512, 16, "bf16", chunk_len_hint=100)
+    carries = 2 * 8 * 512
+    assert ws >= 256 + carries * 16 * 4 + carries * 4
+    # automatic plan fills the GPU for the long-sequence workload
+    p = L.ssm_scan_plan(1, 131072, 5120, 16, "bf16")
+    assert p["ctas"] >= 148 and p["chunk_len"] % 16 == 0
+    # invalid sizes
+    assert L.ssm_scan_workspace_bytes(1, 64, 256, 3, "bf16") == 0
+    with pytest.raises(L.SSMError) as e:
+        L.ssm_scan_plan(1, 64, 256, 32, "bf16")
+    assert e.value.code == L.SSM_ERR_DIMS
+    with pytest.raises(L.SSMError) as e:
+        L.ssm_scan_plan(1, 64, 12, 16, "bf16")       # dim not a multiple of 8
+    assert e.value.code == L.SSM_ERR_ALIGN
+    with pytest.raises(L.SSMError) as e:
+        L.ssm_scan_plan(-1, 64, 256, 16, "f32")
+    assert e.value.code == L.SSM_ERR_DIMS
+
+
+FAKE = 0x7f0000000000   # never dereferenced: every call below fails validation
+
+
+def _scan(dims, x=FAKE, delta=FAKE + 4096, A=FAKE + 8192, B=FAKE + 12288, C=FAKE + 16384,
+          D=None, z=None, bias=None, out=FAKE + (1 << 30), fs=None):
+    return L.lib.ssm_selective_scan_fwd(x, delta, A, B, C, D, z, bias, 0, out, fs,
+                                        ctypes.byref(dims), None)
+
+
+def test_scan_rejects_bad_arguments_before_launch():
+    d = L.make_dims(1, 4, 8, 16, "bf16")
+    assert _scan(d, x=None) == L.SSM_ERR_NULL
+    assert _scan(d, out=None) == L.SSM_ERR_NULL
+    assert L.lib.ssm_selective_scan_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, 0,
+                                        FAKE, None, None, None) == L.SSM_ERR_NULL
+    assert _scan(L.make_dims(1, 4, 8, 5, "bf16")) == L.SSM_ERR_DIMS
+    assert _scan(L.make_dims(1, -4, 8, 16, "bf16")) == L.SSM_ERR_DIMS
+    bad = L.make_dims(1, 4, 8, 16, "bf16")
+    bad.io_dtype = 7
+    assert _scan(bad) == L.SSM_ERR_DTYPE
+    assert _scan(L.make_dims(1, 4, 12, 16, "bf16")) == L.SSM_ERR_ALIGN
+    assert _scan(L.make_dims(1, 4, 6, 16, "f32")) == L.SSM_ERR_ALIGN
+    assert _scan(d, x=FAKE + 2) == L.SSM_ERR_ALIGN
+    assert _scan(d, z=FAKE + 8) == L.SSM_ERR_ALIGN
+    # out overlapping x
+    assert _scan(d, out=FAKE + 16) == L.SSM_ERR_ALIAS
+    # final_state overlapping out
+    assert _scan(d, fs=FAKE + (1 << 30) + 16) == L.SSM_ERR_ALIAS
+    # workspace needed but missing / too small
+    dw = L.make_dims(1, 4096, 8, 16, "bf16", chunk_len_hint=64)
+    assert L.ssm_scan_workspace_bytes(1, 4096, 8, 16, "bf16", chunk_len_hint=64) > 0
+    assert _scan(dw) == L.SSM_ERR_WORKSPACE
+    dw.workspace = FAKE + (1 << 32)
+    dw.workspace_bytes = 256
+    assert _scan(dw) == L.SSM_ERR_WORKSPACE
+
+
+def test_state_update_rejects_bad_arguments_before_launch():
+    d = L.make_dims(2, 1, 8, 16, "bf16")
+    f = L.lib.ssm_state_update
+
+    def call(state=FAKE, x=FAKE + (1 << 20), out=FAKE + (2 << 20), dims=d):
+        return f(state, x, FAKE + (3 << 20), FAKE + (4 << 20), FAKE + (5 << 20), FAKE + (6 << 20), None,
+                 None, None, 0, out, ctypes.byref(dims) if dims is not None else None, None)
+
+    assert call(state=None) == L.SSM_ERR_NULL
+    assert call(dims=None) == L.SSM_ERR_NULL
+    assert call(x=FAKE + (1 << 20) + 4) == L.SSM_ERR_ALIGN
+    assert call(out=FAKE + 16) == L.SSM_ERR_ALIAS          # out inside the state
+    assert call(dims=L.make_dims(2, 1, 8, 7, "bf16")) == L.SSM_ERR_DIMS
+
+
+def test_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 4, 8, dtype=torch.bfloat16)
+    A = torch.zeros(8, 16)
+    with pytest.raises(ValueError):
+        L.ssm_selective_scan_fwd(x, x, A, torch.zeros(1, 4, 16, dtype=torch.bfloat16),
+                                 torch.zeros(1, 4, 16, dtype=torch.bfloat16),
+                                 out=torch.empty_like(x), return_final_state=False)

@@ -1,0 +1,239 @@
+"""GPU parity of ssm_selective_scan_fwd (through the C ABI) against the float64
+oracle on the same seeded inputs.
+
+Covered: the fp32 workload in full; bf16 cases spanning several channel tiles
+and L-chunks with ragged tails; every optional argument on and off; dstate
+1..16; empty, single-token and minimum-width inputs; delta = 0 and very large
+delta; long-memory carries across many chunks (no D, no gate, so nothing masks
+a broken carry); an impulse that must travel through every chunk boundary;
+the three full-size bf16 workloads on sampled channels (all tokens); bitwise
+determinism; guard bands around the outputs; and argument errors.
+"""
+import numpy as np
+import pytest
+
+import gpu_util as G
+from selective_state_space_119_b300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    t = pytest.importorskip("torch")
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from selective_state_space_119_b300 import build
+    build.build(quiet=True)
+    return t
+
+
+def _small(batch=2, L=300, dim=520, N=16, io="bf16", seed=7, **kw):
+    spec = I.ScanSpec(batch, L, dim, N=N, io=io, seed=seed, **kw)
+    return spec, I.make_scan_inputs(spec)
+
+
+def _check(spec, inp, hint=0, final=True, **override):
+    out, fs = G.gpu_scan(inp, spec.delta_softplus, final_state=final, chunk_len_hint=hint,
+                         **override)
+    ry, rh = G.oracle_scan(inp, spec.delta_softplus, **override)
+    st = G.parity(G.host64(out), ry, spec.io, "y (hint %d)" % hint)
+    if final:
+        G.parity(G.host64(fs), rh, "state", "final_state (hint %d)" % hint)
+    return st
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("hint", [0, 16, 64, 256])
+def test_f32_workload_full(torch, hint):
+    spec = I.WORKLOADS["scan_f32_b2_L256_d16"]
+    _check(spec, I.make_scan_inputs(spec), hint)
+
+
+@pytest.mark.parametrize("hint", [0, 16, 48, 112, 320])
+def test_bf16_ragged_tiles_and_chunks(torch, hint):
+    # dim 520 = two full 256-channel tiles + an 8-channel tail; L = 300 is
+    # ragged against every chunk length and the 64-token staging.
+    spec, inp = _small(delta_kind="softplus_bias", A_kind="lognormal", D_kind="uniform")
+    _check(spec, inp, hint)
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+@pytest.mark.parametrize("z_on,D_on,bias_on,softplus,final", [
+    (False, False, False, False, False),
+    (True, False, False, False, True),
+    (False, True, False, False, True),
+    (False, False, True, False, True),
+    (False, False, True, True, True),
+    (True, True, True, True, False),
+])
+def test_optional_arguments(torch, io, z_on, D_on, bias_on, softplus, final):
+    spec, inp = _small(batch=1, L=130, dim=64, io=io,
+                       delta_kind="softplus_bias" if softplus else "loguniform",
+                       D_kind="uniform" if D_on else "none", gate=z_on)
+    if bias_on and not softplus:
+        inp["delta_bias"] = np.linspace(0.0, 0.01, 64).astype(np.float32)
+    if not bias_on:
+        inp["delta_bias"] = None
+    out, fs = G.gpu_scan(inp, softplus, final_state=final, chunk_len_hint=32)
+    ry, rh = G.oracle_scan(inp, softplus)
+    G.parity(G.host64(out), ry, io, "y")
+    if final:
+        G.parity(G.host64(fs), rh, "state", "final_state")
+    else:
+        assert fs is None
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_dstate(torch, N, io):
+    spec, inp = _small(batch=2, L=77, dim=24, N=N, io=io, A_kind="lognormal")
+    _check(spec, inp, 32)
+
+
+def test_single_token_and_minimum_width(torch):
+    spec, inp = _small(batch=1, L=1, dim=8)
+    _check(spec, inp)
+    spec, inp = _small(batch=3, L=5, dim=8, io="f32")
+    _check(spec, inp)
+
+
+def test_empty_inputs(torch):
+    from selective_state_space_119_b300 import libssm
+    t = torch
+    A = t.full((8, 16), -1.0, device="cuda")
+    # L = 0: nothing to scan, the final state is the initial (zero) state
+    x = t.zeros((2, 0, 8), dtype=t.bfloat16, device="cuda")
+    BC = t.zeros((2, 0, 16), dtype=t.bfloat16, device="cuda")
+    fs = t.full((2, 8, 16), 7.0, device="cuda")
+    out, fs = libssm.ssm_selective_scan_fwd(x, x, A, BC, BC, final_state=fs)
+    assert out.shape == (2, 0, 8) and t.count_nonzero(fs).item() == 0
+    # batch = 0 and dim = 0: nothing happens, no error
+    x0 = t.zeros((0, 5, 8), dtype=t.bfloat16, device="cuda")
+    libssm.ssm_selective_scan_fwd(x0, x0, A, t.zeros((0, 5, 16), dtype=t.bfloat16, device="cuda"),
+                                  t.zeros((0, 5, 16), dtype=t.bfloat16, device="cuda"))
+    xd = t.zeros((1, 5, 0), dtype=t.bfloat16, device="cuda")
+    libssm.ssm_selective_scan_fwd(xd, xd, t.zeros((0, 16), device="cuda"),
+                                  t.zeros((1, 5, 16), dtype=t.bfloat16, device="cuda"),
+                                  t.zeros((1, 5, 16), dtype=t.bfloat16, device="cuda"))
+    t.cuda.synchronize()
+
+
+def test_delta_zero_keeps_state(torch):
+    spec, inp = _small(batch=2, L=100, dim=32, D_kind="uniform")
+    inp["delta"] = np.zeros_like(inp["delta"])
+    out, fs = G.gpu_scan(inp, False, chunk_len_hint=32)
+    assert torch.count_nonzero(fs).item() == 0            # h stays exactly 0
+    ry, _ = G.oracle_scan(inp, False)
+    G.parity(G.host64(out), ry, "bf16", "y (delta = 0)")
+
+
+def test_delta_large_resets_state(torch):
+    spec, inp = _small(batch=1, L=64, dim=16, io="f32")
+    inp["delta"] = np.full_like(inp["delta"], 1e4)
+    _check(spec, inp, 16)
+
+
+def test_all_zero_inputs(torch):
+    spec, inp = _small(batch=1, L=50, dim=16)
+    for k in ("x", "z", "B", "C"):
+        inp[k] = np.zeros_like(inp[k])
+    out, fs = G.gpu_scan(inp, False, chunk_len_hint=16)
+    assert torch.count_nonzero(out).item() == 0 and torch.count_nonzero(fs).item() == 0
+
+
+@pytest.mark.parametrize("hint", [16, 64, 2048])
+def test_long_memory_carries(torch, hint):
+    """No D, no gate, slow decay (delta in [1e-4, 1e-2]): y is pure scan
+    output and depends on state carried across every chunk boundary."""
+    spec, inp = _small(batch=2, L=2048, dim=64, delta_lo=1e-4, delta_hi=1e-2,
+                       D_kind="none", gate=False)
+    _check(spec, inp, hint)
+
+
+def test_impulse_crosses_every_chunk(torch):
+    spec, inp = _small(batch=1, L=1024, dim=16, io="f32", delta_lo=1e-4, delta_hi=1e-3,
+                       D_kind="none", gate=False)
+    x = np.zeros_like(inp["x"])
+    x[:, 0, :] = 1.0
+    inp["x"] = x
+    out, fs = G.gpu_scan(inp, False, chunk_len_hint=16)
+    ry, rh = G.oracle_scan(inp, False)
+    y = G.host64(out)
+    G.parity(y, ry, "f32", "impulse response")
+    G.parity(G.host64(fs), rh, "state", "impulse final state")
+    # the response is still alive in the last chunk
+    assert np.abs(ry[:, -16:]).max() > 1e-4
+
+
+@pytest.mark.parametrize("name", ["scan_bf16_b4_L2048_d1536_softplus",
+                                  "scan_bf16_b8_L4096_d2048",
+                                  "scan_bf16_b1_L131072_d5120"])
+def test_full_size_workloads_sampled(torch, name):
+    """Full sizes in the launch configuration the benchmark times (automatic
+    plan); every token of 40 sampled channels, plus the final state."""
+    spec = I.WORKLOADS[name]
+    inp = I.make_scan_inputs(spec)
+    out, fs = G.gpu_scan(inp, spec.delta_softplus, final_state=True)
+    rng = np.random.default_rng(5)
+    dsel = np.unique(np.concatenate([[0, 1, 255, 256, spec.dim - 1],
+                                     rng.choice(spec.dim, 35, replace=False)]))
+    ry, rh = G.oracle_scan(inp, spec.delta_softplus, dsel=dsel)
+    y = out[:, :, torch.as_tensor(dsel, device="cuda")]
+    G.parity(G.host64(y), ry, spec.io, name)
+    G.parity(G.host64(fs[:, torch.as_tensor(dsel, device="cuda")]), rh, "state", name + " state")
+    del out, fs
+    torch.cuda.empty_cache()
+
+
+def test_deterministic(torch):
+    spec, inp = _small(delta_kind="softplus_bias", A_kind="lognormal")
+    a, fa = G.gpu_scan(inp, True, chunk_len_hint=48)
+    b, fb = G.gpu_scan(inp, True, chunk_len_hint=48)
+    assert torch.equal(a, b) and torch.equal(fa, fb)
+
+
+def test_guard_bands_untouched(torch):
+    from selective_state_space_119_b300 import libssm
+    spec, inp = _small(batch=2, L=200, dim=40)
+    n_out = 2 * 200 * 40
+    n_fs = 2 * 40 * 16
+    pad = 4096
+    big = torch.full((pad + n_out + pad,), 12345.0, dtype=torch.bfloat16, device="cuda")
+    fbig = torch.full((pad + n_fs + pad,), -777.0, dtype=torch.float32, device="cuda")
+    out = big[pad:pad + n_out].view(2, 200, 40)
+    fs = fbig[pad:pad + n_fs].view(2, 40, 16)
+    libssm.ssm_selective_scan_fwd(G.dev(inp["x"]), G.dev(inp["delta"]), G.dev(inp["A"]),
+                                  G.dev(inp["B"]), G.dev(inp["C"]), D=G.dev(inp["D"]),
+                                  z=G.dev(inp["z"]), out=out, final_state=fs, chunk_len_hint=32)
+    torch.cuda.synchronize()
+    assert torch.all(big[:pad] == 12345.0) and torch.all(big[pad + n_out:] == 12345.0)
+    assert torch.all(fbig[:pad] == -777.0) and torch.all(fbig[pad + n_fs:] == -777.0)
+    ry, rh = G.oracle_scan(inp, False)
+    G.parity(G.host64(out), ry, "bf16", "y in guarded buffer")
+
+
+def test_argument_errors(torch):
+    from selective_state_space_119_b300 import libssm
+    spec, inp = _small(batch=1, L=40, dim=16)
+    x, dl, A, B, C = (G.dev(inp[k]) for k in ("x", "delta", "A", "B", "C"))
+    with pytest.raises(libssm.SSMError) as e:
+        libssm.ssm_selective_scan_fwd(x, dl, A, B, C, out=x)
+    assert e.value.code == libssm.SSM_ERR_ALIAS
+    buf = torch.zeros(1 * 40 * 16 + 1, dtype=torch.bfloat16, device="cuda")
+    mis = buf[1:].view(1, 40, 16)                       # 2-byte offset
+    with pytest.raises(libssm.SSMError) as e:
+        libssm.ssm_selective_scan_fwd(x, dl, A, B, C, out=mis)
+    assert e.value.code == libssm.SSM_ERR_ALIGN
+    small_ws = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(libssm.SSMError) as e:
+        libssm.ssm_selective_scan_fwd(x, dl, A, B, C, chunk_len_hint=16, workspace=small_ws)
+    assert e.value.code == libssm.SSM_ERR_WORKSPACE
+
+
+def test_device_status_ok_after_calls(torch):
+    from selective_state_space_119_b300 import libssm
+    spec, inp = _small(batch=1, L=256, dim=16)
+    ws = libssm.alloc_workspace(1, 256, 16, 16, "bf16", "cuda", chunk_len_hint=16)
+    G.gpu_scan(inp, False, chunk_len_hint=16, workspace=ws)
+    assert libssm.ssm_get_device_status(1, 256, 16, 16, "bf16", ws, chunk_len_hint=16) == 0
