@@ -126,6 +126,41 @@ int ssm_state_update(float* state, const void* x, const void* delta, const float
                      const float* delta_bias, int delta_softplus, void* out,
                      const ssm_dims* dims, ssm_stream_t stream);
 
+/* Size of the library-owned scratch used by ssm_selective_scan_fwd_static. */
+#define SSM_STATIC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * ssm_selective_scan_fwd_static -- ssm_selective_scan_fwd for callers that
+ * cannot allocate device memory. The pages have no counterpart: this entry
+ * point is a library convenience, not part of the method.
+ *
+ * Who needs it: plain C hosts and plugins inside another runtime that are
+ * handed only their inputs and outputs and have no allocator, and callers that
+ * must not call cudaMalloc on the hot path (it can synchronize the device and
+ * can fail under memory pressure at an arbitrary point).
+ *
+ * Arguments, layouts, validation and results are those of
+ * ssm_selective_scan_fwd; dims->workspace and dims->workspace_bytes are
+ * ignored. The scan's scratch is a fixed array of SSM_STATIC_SCRATCH_BYTES
+ * (16 MiB) inside the library, which every GPU that loads the library holds
+ * until the process exits. When ssm_scan_workspace_bytes(dims) exceeds that
+ * size the call returns SSM_ERR_WORKSPACE and enqueues nothing (use
+ * ssm_selective_scan_fwd with a workspace, or a larger chunk_len_hint, which
+ * needs fewer carries). The call allocates nothing.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture. Every call on a device shares the one array, which keeps the last
+ * call's contents (nothing in it has to start at zero): calls that can overlap
+ * on the GPU -- on different streams, or from different host threads -- race
+ * on it and must be serialized by the caller.
+ */
+int ssm_selective_scan_fwd_static(const void* x, const void* delta, const float* A,
+                                  const void* B, const void* C, const float* D,
+                                  const void* z, const float* delta_bias, int delta_softplus,
+                                  void* out, float* final_state, const ssm_dims* dims,
+                                  ssm_stream_t stream);
+
 /* Bytes of workspace ssm_selective_scan_fwd needs for these sizes (0 when the
  * scan runs in one pass). Depends only on batch, seqlen, dim, dstate and
  * chunk_len_hint; returns 0 for invalid sizes. */

@@ -41,7 +41,10 @@ SSM_ERR_ALIAS = -8
 # Every symbol include/ssm.h declares.
 EXPORTED = ("ssm_selective_scan_fwd", "ssm_state_update", "ssm_scan_workspace_bytes",
             "ssm_scan_plan", "ssm_get_device_status", "ssm_strerror", "ssm_last_cuda_error",
-            "ssm_version")
+            "ssm_version", "ssm_selective_scan_fwd_static")
+
+# Size of the library-owned scratch of ssm_selective_scan_fwd_static (include/ssm.h).
+SSM_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class ssm_dims(ctypes.Structure):
@@ -62,6 +65,8 @@ _dims_p = ctypes.POINTER(ssm_dims)
 lib.ssm_selective_scan_fwd.restype = ctypes.c_int
 lib.ssm_selective_scan_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
                                        _vp, _vp, _dims_p, _vp]
+lib.ssm_selective_scan_fwd_static.restype = ctypes.c_int
+lib.ssm_selective_scan_fwd_static.argtypes = list(lib.ssm_selective_scan_fwd.argtypes)
 lib.ssm_state_update.restype = ctypes.c_int
 lib.ssm_state_update.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
                                  _vp, _dims_p, _vp]
@@ -205,6 +210,41 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
     with torch.cuda.device(dev):
         rc = lib.ssm_selective_scan_fwd(*args, ctypes.byref(dims), _stream(dev, stream))
     _check(rc, "ssm_selective_scan_fwd")
+    return out, final_state
+
+
+def ssm_selective_scan_fwd_static(x, delta, A, B, C, D=None, z=None, delta_bias=None,
+                                  delta_softplus=False, out=None, final_state=None,
+                                  return_final_state=True, chunk_len_hint=0, stream=None):
+    """ssm_selective_scan_fwd without a workspace: the scan's scratch is the
+    library's own fixed array (include/ssm.h), for callers that cannot allocate.
+    Calls that overlap on the GPU share that array and must be serialized."""
+    torch = _torch()
+    batch, L, dim = x.shape
+    N = A.shape[1]
+    io = x.dtype
+    dev = x.device
+    if out is None:
+        out = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+    dims = make_dims(batch, L, dim, N, _io_code(x), None, 0, chunk_len_hint)
+    args = (
+        _ptr(x, "x", io, (batch, L, dim), dev),
+        _ptr(delta, "delta", io, (batch, L, dim), dev),
+        _ptr(A, "A", torch.float32, (dim, N), dev),
+        _ptr(B, "B", io, (batch, L, N), dev),
+        _ptr(C, "C", io, (batch, L, N), dev),
+        _ptr(D, "D", torch.float32, (dim,), dev),
+        _ptr(z, "z", io, (batch, L, dim), dev),
+        _ptr(delta_bias, "delta_bias", torch.float32, (dim,), dev),
+        1 if delta_softplus else 0,
+        _ptr(out, "out", io, (batch, L, dim), dev),
+        _ptr(final_state, "final_state", torch.float32, (batch, dim, N), dev),
+    )
+    with torch.cuda.device(dev):
+        rc = lib.ssm_selective_scan_fwd_static(*args, ctypes.byref(dims), _stream(dev, stream))
+    _check(rc, "ssm_selective_scan_fwd_static")
     return out, final_state
 
 
