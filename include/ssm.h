@@ -78,9 +78,11 @@ enum {
  *   dstate  : N, one of 1, 2, 4, 8, 16 (16 is the production size)
  *   io_dtype: ssm_dtype of x, delta, z, B, C, out
  *   workspace, workspace_bytes: device scratch for ssm_selective_scan_fwd (see
- *     ssm_scan_workspace_bytes); may be NULL when that size is 0. Must be
- *     zero-filled once before its first use; the library leaves it in a state
- *     that the next call accepts. Ignored by ssm_state_update. */
+ *     ssm_scan_workspace_bytes: a 256-byte header with the status word, plus
+ *     the chunk carries when the sequence is split); may be NULL only for
+ *     empty problems. Must be zero-filled once before its first use; the
+ *     library leaves it in a state that the next call accepts. Ignored by
+ *     ssm_state_update. */
 typedef struct {
     int64_t batch, seqlen, dim, dstate;
     int32_t io_dtype;
@@ -89,6 +91,10 @@ typedef struct {
                                workspace size follows it)                 */
     void* workspace;
     size_t workspace_bytes;
+    int32_t tile_config_hint; /* 0: library's choice; 1..4: force tile configuration
+                                 0..3 of the scan (1, 2, 4 or 8 threads per channel;
+                                 dstate 16 only, ignored otherwise)           */
+    int32_t reserved;         /* must be 0 */
 } ssm_dims;
 
 /*
@@ -161,9 +167,10 @@ int ssm_selective_scan_fwd_static(const void* x, const void* delta, const float*
                                   void* out, float* final_state, const ssm_dims* dims,
                                   ssm_stream_t stream);
 
-/* Bytes of workspace ssm_selective_scan_fwd needs for these sizes (0 when the
- * scan runs in one pass). Depends only on batch, seqlen, dim, dstate and
- * chunk_len_hint; returns 0 for invalid sizes. */
+/* Bytes of workspace ssm_selective_scan_fwd needs for these sizes (256 when
+ * the scan runs in one pass, 0 for empty problems). Depends only on batch,
+ * seqlen, dim, dstate, io_dtype, chunk_len_hint and tile_config_hint; returns
+ * 0 for invalid sizes. */
 size_t ssm_scan_workspace_bytes(const ssm_dims* dims);
 
 /* Launch plan the scan will use for these sizes (for benchmarks and tests). */
@@ -173,13 +180,15 @@ typedef struct {
     int64_t channels_per_cta;
     int64_t ctas;           /* CTAs of the main (output) kernel         */
     int32_t kernels;        /* kernel launches per call                 */
-    int32_t reserved;
+    int32_t tile_config;    /* tile configuration id (0..3)             */
 } ssm_plan;
 int ssm_scan_plan(const ssm_dims* dims, ssm_plan* plan);
 
 /* Synchronizes `stream`, then reads the device-side status word of the
- * workspace: SSM_OK, or SSM_ERR_TIMEOUT when a bounded wait gave up, which
- * the next call clears. Returns SSM_OK when the plan uses no workspace. */
+ * workspace: SSM_OK, or SSM_ERR_TIMEOUT when a bounded wait inside a scan
+ * kernel gave up since the word was last read (the affected outputs are then
+ * undefined). The word is sticky across calls; reading a nonzero word clears
+ * it. Returns SSM_OK for empty problems. */
 int ssm_get_device_status(const ssm_dims* dims, ssm_stream_t stream);
 
 /* Human-readable text for a return code (static storage). */

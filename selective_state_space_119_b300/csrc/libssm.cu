@@ -17,10 +17,14 @@ thread_local int g_last_cuda_error = 0;
 
 constexpr int64_t kMaxDim = int64_t(1) << 31;     // per-axis limit
 constexpr int64_t kMaxElems = int64_t(1) << 40;   // batch * seqlen * dim limit
-// Enough resident CTAs to fill a B300 (148 SMs) about four deep; the chunk
-// count of the scan is chosen to reach it.
-constexpr int64_t kTargetCtas = 148 * 4;
-constexpr int64_t kMinChunk = 64;
+// Planning. The scan is ALU-bound (16 exponentials per element), so the plan
+// first looks for enough threads: about kTargetThreads resident threads
+// (148 SMs x 512) keep every SM's pipes fed. It takes the cheapest tile
+// configuration (fewest threads per channel) that reaches the target from the
+// channels alone, and splits L into chunks only if even 8 threads per channel
+// fall short. Chunks are never shorter than kMinChunk tokens.
+constexpr int64_t kTargetThreads = 148 * 512;
+constexpr int64_t kMinChunk = 512;
 
 int set_cuda(cudaError_t e) {
     g_last_cuda_error = static_cast<int>(e);
@@ -43,6 +47,8 @@ int check_dims(const ssm_dims* d, bool scan) {
     if (d->batch >= kMaxDim || d->dim >= kMaxDim || (scan && d->seqlen >= kMaxDim))
         return SSM_ERR_DIMS;
     if (scan && d->chunk_len_hint < 0) return SSM_ERR_DIMS;
+    if (scan && (d->tile_config_hint < 0 || d->tile_config_hint > ssm::kScanTileConfigs))
+        return SSM_ERR_DIMS;
     const int64_t L = scan ? d->seqlen : 1;
     if (d->batch > 0 && d->dim > 0 && L > 0 &&
         (d->batch > kMaxElems / d->dim || d->batch * d->dim > kMaxElems / L))
@@ -52,28 +58,42 @@ int check_dims(const ssm_dims* d, bool scan) {
     return SSM_OK;
 }
 
+int choose_tile_cfg(int64_t channels, int64_t N, int32_t hint) {
+    if (N != 16) return 1;
+    if (hint > 0) return hint - 1;
+    for (int c = 0; c < ssm::kScanTileConfigs; ++c)
+        if (channels * ssm::scan_threads_per_channel(c) >= kTargetThreads) return c;
+    return ssm::kScanTileConfigs - 1;
+}
+
 int make_plan(const ssm_dims* d, ssm::ScanPlan* p) {
     *p = ssm::ScanPlan{};
     const int64_t batch = d->batch, L = d->seqlen, dim = d->dim, N = d->dstate;
-    p->channels_per_cta = int64_t(ssm::kScanThreads) * ssm::kScanCPT;
+    const int64_t TS = ssm::kScanStageTokens;
     if (batch == 0 || L == 0 || dim == 0) return SSM_OK;
+    p->tile_cfg = choose_tile_cfg(batch * dim, N, d->tile_config_hint);
+    p->channels_per_cta = ssm::scan_tile_channels(p->tile_cfg);
     p->tiles = (dim + p->channels_per_cta - 1) / p->channels_per_cta;
     const int64_t per_chunk = p->tiles * batch;
+    const int64_t threads = batch * dim * ssm::scan_threads_per_channel(p->tile_cfg);
     int64_t chunk;
     if (d->chunk_len_hint > 0) {
         chunk = d->chunk_len_hint;
     } else {
-        int64_t nck = std::max<int64_t>(1, (kTargetCtas + per_chunk - 1) / per_chunk);
-        nck = std::min(nck, std::max<int64_t>(1, (L + kMinChunk - 1) / kMinChunk));
+        int64_t nck = std::max<int64_t>(1, (kTargetThreads + threads - 1) / threads);
+        nck = std::min(nck, std::max<int64_t>(1, L / kMinChunk));
         chunk = (L + nck - 1) / nck;
     }
-    chunk = std::max<int64_t>(16, (chunk + 15) / 16 * 16);
-    chunk = std::min(chunk, (L + 15) / 16 * 16);
+    // whole pipeline stages per chunk, so that only the sequence end is ragged
+    chunk = std::max<int64_t>(TS, (chunk + TS - 1) / TS * TS);
+    chunk = std::min(chunk, (L + TS - 1) / TS * TS);
     p->chunk_len = chunk;
     p->nchunks = (L + chunk - 1) / chunk;
     p->ctas = per_chunk * p->nchunks;
     if (p->ctas >= (int64_t(1) << 31)) return SSM_ERR_DIMS;
     p->kernels = p->nchunks > 1 ? 3 : 1;
+    // header (status word) always; chunk carries when the sequence is split
+    p->ws_bytes = ssm::kWsHeaderBytes;
     if (p->nchunks > 1) {
         const size_t carries = size_t(batch) * size_t(p->nchunks - 1) * size_t(dim);
         p->ws_off_H = ssm::kWsHeaderBytes;
@@ -148,7 +168,7 @@ int ssm_scan_plan(const ssm_dims* dims, ssm_plan* plan) {
     plan->channels_per_cta = p.channels_per_cta;
     plan->ctas = p.ctas;
     plan->kernels = p.kernels;
-    plan->reserved = 0;
+    plan->tile_config = p.tile_cfg;
     return SSM_OK;
 }
 
@@ -209,8 +229,9 @@ int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, con
     a.out = out; a.final_state = final_state;
     a.batch = batch; a.L = L; a.dim = dim;
     a.chunk_len = p.chunk_len; a.nchunks = p.nchunks; a.tiles = p.tiles;
-    if (p.ws_bytes > 0) {
-        char* ws = static_cast<char*>(dims->workspace);
+    char* ws = static_cast<char*>(dims->workspace);
+    a.status = reinterpret_cast<unsigned int*>(ws);
+    if (p.nchunks > 1) {
         a.ws_H = reinterpret_cast<float*>(ws + p.ws_off_H);
         a.ws_S = reinterpret_cast<float*>(ws + p.ws_off_S);
     }
@@ -260,10 +281,15 @@ int ssm_get_device_status(const ssm_dims* dims, ssm_stream_t stream) {
     rc = set_cuda(cudaStreamSynchronize(s));
     if (rc != SSM_OK) return rc;
     if (p.ws_bytes == 0) return SSM_OK;
-    if (!dims->workspace || dims->workspace_bytes < p.ws_bytes) return SSM_ERR_WORKSPACE;
+    if (!dims->workspace || dims->workspace_bytes < sizeof(uint32_t)) return SSM_ERR_WORKSPACE;
     uint32_t status = 0;
     rc = set_cuda(cudaMemcpy(&status, dims->workspace, sizeof(status), cudaMemcpyDeviceToHost));
     if (rc != SSM_OK) return rc;
+    if (status != 0) {
+        // the word is sticky: clear it now that it has been reported
+        rc = set_cuda(cudaMemset(dims->workspace, 0, sizeof(status)));
+        if (rc != SSM_OK) return rc;
+    }
     return status == 0 ? SSM_OK : -static_cast<int>(status);
 }
 

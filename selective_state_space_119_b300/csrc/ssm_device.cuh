@@ -25,10 +25,25 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// softplus(v) = log(1 + e^v). Above 20, log(1 + e^v) and v agree to within
-// e^-20 relative, below float resolution.
+constexpr float kLn2 = 0.6931471805599453f;
+
+// log2(x) with the SFU (PTX lg2.approx.ftz.f32).
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// softplus(v) = log(1 + e^v) with two SFU operations. w = e^v; for w < 2^-7
+// the rounding of 1 + w would dominate log(1 + w), so the Taylor series
+// w - w^2/2 + w^3/3 - w^4/4 is used there (truncation error below w^5/5,
+// under 2^-28 relative). Above v = 20, log(1 + e^v) equals v to within e^-20.
 __device__ __forceinline__ float softplus(float v) {
-    return v > 20.f ? v : log1pf(__expf(v));
+    const float w = ex2(v * kLog2e);
+    const float series = w * fmaf(w, fmaf(w, fmaf(w, -0.25f, 1.f / 3.f), -0.5f), 1.f);
+    const float logged = lg2(1.f + w) * kLn2;
+    const float r = w < 0.0078125f ? series : logged;
+    return v > 20.f ? v : r;
 }
 
 // silu(z) = z * sigmoid(z) = z / (1 + e^-z). For z < -88, e^-z overflows to
@@ -73,6 +88,16 @@ template <int CPT> struct Vec<float, CPT> {
             v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
         }
     }
+    // shared-memory pair access (CPT == 2)
+    __device__ __forceinline__ static void lds(const float* p, float (&v)[CPT]) {
+        static_assert(CPT == 2, "pairs");
+        const float2 u = *reinterpret_cast<const float2*>(p);
+        v[0] = u.x; v[1] = u.y;
+    }
+    __device__ __forceinline__ static void sts(float* p, const float (&v)[CPT]) {
+        static_assert(CPT == 2, "pairs");
+        *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+    }
     __device__ __forceinline__ static void st(float* p, const float (&v)[CPT]) {
         if constexpr (CPT == 1) {
             *p = v[0];
@@ -107,6 +132,15 @@ template <int CPT> struct Vec<__nv_bfloat16, CPT> {
             unpack(u.x, v[0], v[1]); unpack(u.y, v[2], v[3]);
             unpack(u.z, v[4], v[5]); unpack(u.w, v[6], v[7]);
         }
+    }
+    // shared-memory pair access (CPT == 2)
+    __device__ __forceinline__ static void lds(const __nv_bfloat16* p, float (&v)[CPT]) {
+        static_assert(CPT == 2, "pairs");
+        unpack(*reinterpret_cast<const uint32_t*>(p), v[0], v[1]);
+    }
+    __device__ __forceinline__ static void sts(__nv_bfloat16* p, const float (&v)[CPT]) {
+        static_assert(CPT == 2, "pairs");
+        *reinterpret_cast<uint32_t*>(p) = pack(v[0], v[1]);
     }
     __device__ __forceinline__ static void st(__nv_bfloat16* p, const float (&v)[CPT]) {
         if constexpr (CPT == 1) {

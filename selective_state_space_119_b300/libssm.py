@@ -51,13 +51,14 @@ class ssm_dims(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("dim", ctypes.c_int64),
                 ("dstate", ctypes.c_int64), ("io_dtype", ctypes.c_int32),
                 ("chunk_len_hint", ctypes.c_int32), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("tile_config_hint", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class ssm_plan(ctypes.Structure):
     _fields_ = [("chunk_len", ctypes.c_int64), ("nchunks", ctypes.c_int64),
                 ("channels_per_cta", ctypes.c_int64), ("ctas", ctypes.c_int64),
-                ("kernels", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("kernels", ctypes.c_int32), ("tile_config", ctypes.c_int32)]
 
 
 _vp = ctypes.c_void_p
@@ -103,22 +104,25 @@ def _check(rc: int, where: str) -> None:
 
 
 def make_dims(batch, seqlen, dim, dstate, io, workspace=None, workspace_bytes=0,
-              chunk_len_hint=0) -> ssm_dims:
+              chunk_len_hint=0, tile_config_hint=0) -> ssm_dims:
     io_code = io if isinstance(io, int) else (SSM_BF16 if str(io) in ("bf16", "torch.bfloat16") else SSM_F32)
     return ssm_dims(int(batch), int(seqlen), int(dim), int(dstate), io_code, int(chunk_len_hint),
-                    workspace, int(workspace_bytes))
+                    workspace, int(workspace_bytes), int(tile_config_hint), 0)
 
 
-def ssm_scan_workspace_bytes(batch, seqlen, dim, dstate, io, chunk_len_hint=0) -> int:
-    d = make_dims(batch, seqlen, dim, dstate, io, chunk_len_hint=chunk_len_hint)
+def ssm_scan_workspace_bytes(batch, seqlen, dim, dstate, io, chunk_len_hint=0,
+                             tile_config_hint=0) -> int:
+    d = make_dims(batch, seqlen, dim, dstate, io, chunk_len_hint=chunk_len_hint,
+                  tile_config_hint=tile_config_hint)
     return int(lib.ssm_scan_workspace_bytes(ctypes.byref(d)))
 
 
-def ssm_scan_plan(batch, seqlen, dim, dstate, io, chunk_len_hint=0) -> dict:
-    d = make_dims(batch, seqlen, dim, dstate, io, chunk_len_hint=chunk_len_hint)
+def ssm_scan_plan(batch, seqlen, dim, dstate, io, chunk_len_hint=0, tile_config_hint=0) -> dict:
+    d = make_dims(batch, seqlen, dim, dstate, io, chunk_len_hint=chunk_len_hint,
+                  tile_config_hint=tile_config_hint)
     p = ssm_plan()
     _check(lib.ssm_scan_plan(ctypes.byref(d), ctypes.byref(p)), "ssm_scan_plan")
-    return {k: getattr(p, k) for k, _ in ssm_plan._fields_ if k != "reserved"}
+    return {k: getattr(p, k) for k, _ in ssm_plan._fields_}
 
 
 # ---------------------------------------------------------------------------
@@ -160,10 +164,10 @@ def _stream(device, stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def alloc_workspace(batch, seqlen, dim, dstate, io, device, chunk_len_hint=0):
+def alloc_workspace(batch, seqlen, dim, dstate, io, device, chunk_len_hint=0, tile_config_hint=0):
     """Zero-filled workspace tensor (uint8) of the size the scan needs, or None."""
     torch = _torch()
-    n = ssm_scan_workspace_bytes(batch, seqlen, dim, dstate, io, chunk_len_hint)
+    n = ssm_scan_workspace_bytes(batch, seqlen, dim, dstate, io, chunk_len_hint, tile_config_hint)
     if n == 0:
         return None
     return torch.zeros(n, dtype=torch.uint8, device=device)
@@ -172,7 +176,7 @@ def alloc_workspace(batch, seqlen, dim, dstate, io, device, chunk_len_hint=0):
 def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
                            delta_softplus=False, out=None, final_state=None,
                            return_final_state=True, workspace=None, chunk_len_hint=0,
-                           stream=None) -> Tuple[object, Optional[object]]:
+                           tile_config_hint=0, stream=None) -> Tuple[object, Optional[object]]:
     """Selective scan over x [batch, L, dim] (see include/ssm.h).
 
     Returns (out, final_state); final_state is None when not requested.
@@ -190,10 +194,12 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
     if final_state is None and return_final_state:
         final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
     if workspace is None:
-        workspace = alloc_workspace(batch, L, dim, N, _io_code(x), dev, chunk_len_hint)
+        workspace = alloc_workspace(batch, L, dim, N, _io_code(x), dev, chunk_len_hint,
+                                    tile_config_hint)
     ws_ptr = _ptr(workspace, "workspace", torch.uint8, device=dev)
     ws_bytes = workspace.numel() if workspace is not None else 0
-    dims = make_dims(batch, L, dim, N, _io_code(x), ws_ptr, ws_bytes, chunk_len_hint)
+    dims = make_dims(batch, L, dim, N, _io_code(x), ws_ptr, ws_bytes, chunk_len_hint,
+                     tile_config_hint)
     args = (
         _ptr(x, "x", io, (batch, L, dim), dev),
         _ptr(delta, "delta", io, (batch, L, dim), dev),
@@ -215,7 +221,8 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
 
 def ssm_selective_scan_fwd_static(x, delta, A, B, C, D=None, z=None, delta_bias=None,
                                   delta_softplus=False, out=None, final_state=None,
-                                  return_final_state=True, chunk_len_hint=0, stream=None):
+                                  return_final_state=True, chunk_len_hint=0,
+                                  tile_config_hint=0, stream=None):
     """ssm_selective_scan_fwd without a workspace: the scan's scratch is the
     library's own fixed array (include/ssm.h), for callers that cannot allocate.
     Calls that overlap on the GPU share that array and must be serialized."""
@@ -228,7 +235,7 @@ def ssm_selective_scan_fwd_static(x, delta, A, B, C, D=None, z=None, delta_bias=
         out = torch.empty_like(x)
     if final_state is None and return_final_state:
         final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
-    dims = make_dims(batch, L, dim, N, _io_code(x), None, 0, chunk_len_hint)
+    dims = make_dims(batch, L, dim, N, _io_code(x), None, 0, chunk_len_hint, tile_config_hint)
     args = (
         _ptr(x, "x", io, (batch, L, dim), dev),
         _ptr(delta, "delta", io, (batch, L, dim), dev),
@@ -279,12 +286,13 @@ def ssm_state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
 
 
 def ssm_get_device_status(batch, seqlen, dim, dstate, io, workspace, chunk_len_hint=0,
-                          stream=None) -> int:
+                          stream=None, tile_config_hint=0) -> int:
     """Synchronize the stream and return the workspace's device status code."""
     torch = _torch()
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() if workspace is not None else 0
-    dims = make_dims(batch, seqlen, dim, dstate, io, ws_ptr, ws_bytes, chunk_len_hint)
+    dims = make_dims(batch, seqlen, dim, dstate, io, ws_ptr, ws_bytes, chunk_len_hint,
+                     tile_config_hint)
     dev = workspace.device if workspace is not None else torch.device("cuda")
     with torch.cuda.device(dev):
         return int(lib.ssm_get_device_status(ctypes.byref(dims), _stream(dev, stream)))

@@ -63,7 +63,8 @@ def parity(got, ref, io, what=""):
     return stats
 
 
-def gpu_scan(inp, softplus, final_state=True, chunk_len_hint=0, workspace=None, **override):
+def gpu_scan(inp, softplus, final_state=True, chunk_len_hint=0, workspace=None, tile_config_hint=0,
+             **override):
     """Run ssm_selective_scan_fwd on stored inputs; returns (out tensor, fs tensor)."""
     from selective_state_space_119_b300 import libssm
     a = dict(inp)
@@ -72,7 +73,7 @@ def gpu_scan(inp, softplus, final_state=True, chunk_len_hint=0, workspace=None, 
         dev(a["x"]), dev(a["delta"]), dev(a["A"]), dev(a["B"]), dev(a["C"]),
         D=dev(a.get("D")), z=dev(a.get("z")), delta_bias=dev(a.get("delta_bias")),
         delta_softplus=softplus, return_final_state=final_state,
-        chunk_len_hint=chunk_len_hint, workspace=workspace)
+        chunk_len_hint=chunk_len_hint, workspace=workspace, tile_config_hint=tile_config_hint)
     return out, fs
 
 

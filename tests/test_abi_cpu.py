@@ -36,25 +36,35 @@ def test_version_and_strerror():
 
 
 def test_struct_layout_matches_header():
-    # int64 x4, int32 x2, pointer, size_t
-    assert ctypes.sizeof(L.ssm_dims) == 4 * 8 + 2 * 4 + 8 + 8
+    # int64 x4, int32 x2, pointer, size_t, int32 x2
+    assert ctypes.sizeof(L.ssm_dims) == 4 * 8 + 2 * 4 + 8 + 8 + 2 * 4
     assert ctypes.sizeof(L.ssm_plan) == 4 * 8 + 2 * 4
 
 
 def test_workspace_and_plan():
-    # one chunk -> no workspace
-    assert L.ssm_scan_workspace_bytes(1, 64, 256, 16, "bf16", chunk_len_hint=64) == 0
+    # one chunk -> only the 256-byte header (status word)
+    assert L.ssm_scan_workspace_bytes(1, 64, 256, 16, "bf16", chunk_len_hint=64) == 256
+    assert L.ssm_scan_workspace_bytes(0, 64, 256, 16, "bf16") == 0      # empty problem
     p = L.ssm_scan_plan(1, 64, 256, 16, "bf16", chunk_len_hint=64)
     assert p["nchunks"] == 1 and p["kernels"] == 1
-    # several chunks -> header + carries
+    # several chunks -> header + carries; chunks are whole 16-token stages
     p = L.ssm_scan_plan(2, 1000, 512, 16, "bf16", chunk_len_hint=100)
     assert p["chunk_len"] == 112 and p["nchunks"] == 9 and p["kernels"] == 3
+    for cfg, ch in ((1, 64), (2, 64), (3, 32), (4, 16)):
+        p = L.ssm_scan_plan(2, 1000, 512, 16, "bf16", tile_config_hint=cfg)
+        assert p["tile_config"] == cfg - 1 and p["channels_per_cta"] == ch
+    assert L.ssm_scan_plan(2, 1000, 512, 8, "bf16", tile_config_hint=4)["tile_config"] == 1
+    with pytest.raises(L.SSMError):
+        L.ssm_scan_plan(2, 1000, 512, 16, "bf16", tile_config_hint=5)
     ws = L.ssm_scan_workspace_bytes(2, 1000, 512, 16, "bf16", chunk_len_hint=100)
     carries = 2 * 8 * 512
     assert ws >= 256 + carries * 16 * 4 + carries * 4
     # automatic plan fills the GPU for the long-sequence workload
     p = L.ssm_scan_plan(1, 131072, 5120, 16, "bf16")
     assert p["ctas"] >= 148 and p["chunk_len"] % 16 == 0
+    # a channel-rich workload needs one thread per channel and no L-split
+    p = L.ssm_scan_plan(64, 2048, 2048, 16, "bf16")
+    assert p["tile_config"] == 0 and p["nchunks"] == 1
     # invalid sizes
     assert L.ssm_scan_workspace_bytes(1, 64, 256, 3, "bf16") == 0
     with pytest.raises(L.SSMError) as e:
@@ -78,7 +88,7 @@ def _scan(dims, x=FAKE, delta=FAKE + 4096, A=FAKE + 8192, B=FAKE + 12288, C=FAKE
 
 
 def test_scan_rejects_bad_arguments_before_launch():
-    d = L.make_dims(1, 4, 8, 16, "bf16")
+    d = L.make_dims(1, 4, 8, 16, "bf16", workspace=FAKE + (1 << 34), workspace_bytes=1 << 20)
     assert _scan(d, x=None) == L.SSM_ERR_NULL
     assert _scan(d, out=None) == L.SSM_ERR_NULL
     assert L.lib.ssm_selective_scan_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, 0,
@@ -96,7 +106,8 @@ def test_scan_rejects_bad_arguments_before_launch():
     assert _scan(d, out=FAKE + 16) == L.SSM_ERR_ALIAS
     # final_state overlapping out
     assert _scan(d, fs=FAKE + (1 << 30) + 16) == L.SSM_ERR_ALIAS
-    # workspace needed but missing / too small
+    # workspace missing / too small
+    assert _scan(L.make_dims(1, 4, 8, 16, "bf16")) == L.SSM_ERR_WORKSPACE
     dw = L.make_dims(1, 4096, 8, 16, "bf16", chunk_len_hint=64)
     assert L.ssm_scan_workspace_bytes(1, 4096, 8, 16, "bf16", chunk_len_hint=64) > 0
     assert _scan(dw) == L.SSM_ERR_WORKSPACE

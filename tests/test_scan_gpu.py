@@ -33,29 +33,34 @@ def _small(batch=2, L=300, dim=520, N=16, io="bf16", seed=7, **kw):
     return spec, I.make_scan_inputs(spec)
 
 
-def _check(spec, inp, hint=0, final=True, **override):
+def _check(spec, inp, hint=0, final=True, tile=0, **override):
     out, fs = G.gpu_scan(inp, spec.delta_softplus, final_state=final, chunk_len_hint=hint,
-                         **override)
+                         tile_config_hint=tile, **override)
     ry, rh = G.oracle_scan(inp, spec.delta_softplus, **override)
-    st = G.parity(G.host64(out), ry, spec.io, "y (hint %d)" % hint)
+    st = G.parity(G.host64(out), ry, spec.io, "y (chunk hint %d, tile %d)" % (hint, tile))
     if final:
-        G.parity(G.host64(fs), rh, "state", "final_state (hint %d)" % hint)
+        G.parity(G.host64(fs), rh, "state", "final_state (chunk hint %d, tile %d)" % (hint, tile))
     return st
 
 
+TILES = [0, 1, 2, 3, 4]   # 0 = library's choice; k = tile configuration k - 1
+
+
 # ---------------------------------------------------------------------------
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("hint", [0, 16, 64, 256])
-def test_f32_workload_full(torch, hint):
+def test_f32_workload_full(torch, hint, tile):
     spec = I.WORKLOADS["scan_f32_b2_L256_d16"]
-    _check(spec, I.make_scan_inputs(spec), hint)
+    _check(spec, I.make_scan_inputs(spec), hint, tile=tile)
 
 
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("hint", [0, 16, 48, 112, 320])
-def test_bf16_ragged_tiles_and_chunks(torch, hint):
-    # dim 520 = two full 256-channel tiles + an 8-channel tail; L = 300 is
-    # ragged against every chunk length and the 64-token staging.
+def test_bf16_ragged_tiles_and_chunks(torch, hint, tile):
+    # dim 520 is ragged against every channel tile (16, 32, 64); L = 300 is
+    # ragged against every chunk length and the 16-token stages.
     spec, inp = _small(delta_kind="softplus_bias", A_kind="lognormal", D_kind="uniform")
-    _check(spec, inp, hint)
+    _check(spec, inp, hint, tile=tile)
 
 
 @pytest.mark.parametrize("io", ["bf16", "f32"])
@@ -142,13 +147,14 @@ def test_all_zero_inputs(torch):
     assert torch.count_nonzero(out).item() == 0 and torch.count_nonzero(fs).item() == 0
 
 
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("hint", [16, 64, 2048])
-def test_long_memory_carries(torch, hint):
+def test_long_memory_carries(torch, hint, tile):
     """No D, no gate, slow decay (delta in [1e-4, 1e-2]): y is pure scan
     output and depends on state carried across every chunk boundary."""
     spec, inp = _small(batch=2, L=2048, dim=64, delta_lo=1e-4, delta_hi=1e-2,
                        D_kind="none", gate=False)
-    _check(spec, inp, hint)
+    _check(spec, inp, hint, tile=tile)
 
 
 def test_impulse_crosses_every_chunk(torch):
@@ -175,6 +181,22 @@ def test_full_size_workloads_sampled(torch, name):
     spec = I.WORKLOADS[name]
     inp = I.make_scan_inputs(spec)
     out, fs = G.gpu_scan(inp, spec.delta_softplus, final_state=True)
+    _sampled_parity(torch, spec, inp, out, fs, name)
+    del out, fs
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("tile", [1, 2, 3, 4])
+def test_benchmark_workload_every_tile(torch, tile):
+    spec = I.WORKLOADS["scan_bf16_b4_L2048_d1536_softplus"]
+    inp = I.make_scan_inputs(spec)
+    for hint in (0, 512):
+        out, fs = G.gpu_scan(inp, True, final_state=True, tile_config_hint=tile,
+                             chunk_len_hint=hint)
+        _sampled_parity(torch, spec, inp, out, fs, "tile %d chunk hint %d" % (tile, hint))
+
+
+def _sampled_parity(torch, spec, inp, out, fs, name):
     rng = np.random.default_rng(5)
     dsel = np.unique(np.concatenate([[0, 1, 255, 256, spec.dim - 1],
                                      rng.choice(spec.dim, 35, replace=False)]))
@@ -182,8 +204,6 @@ def test_full_size_workloads_sampled(torch, name):
     y = out[:, :, torch.as_tensor(dsel, device="cuda")]
     G.parity(G.host64(y), ry, spec.io, name)
     G.parity(G.host64(fs[:, torch.as_tensor(dsel, device="cuda")]), rh, "state", name + " state")
-    del out, fs
-    torch.cuda.empty_cache()
 
 
 def test_deterministic(torch):
