@@ -87,13 +87,14 @@ typedef struct {
     int64_t batch, seqlen, dim, dstate;
     int32_t io_dtype;
     int32_t chunk_len_hint; /* 0: library's choice; else tokens per L-chunk of the
-                               scan (rounded up to a multiple of 16; the
+                               scan (rounded up to a multiple of 32; the
                                workspace size follows it)                 */
     void* workspace;
     size_t workspace_bytes;
     int32_t tile_config_hint; /* 0: library's choice; 1..4: force tile configuration
-                                 0..3 of the scan (1, 2, 4 or 8 threads per channel;
-                                 dstate 16 only, ignored otherwise)           */
+                                 0..3 of the scan: lanes sharing one channel's
+                                 states x warps per CTA = 4x4, 8x4, 4x2, 2x4
+                                 (fewer lanes when dstate is smaller)        */
     int32_t reserved;         /* must be 0 */
 } ssm_dims;
 

@@ -18,12 +18,12 @@ thread_local int g_last_cuda_error = 0;
 constexpr int64_t kMaxDim = int64_t(1) << 31;     // per-axis limit
 constexpr int64_t kMaxElems = int64_t(1) << 40;   // batch * seqlen * dim limit
 // Planning. The scan is ALU-bound (16 exponentials per element), so the plan
-// first looks for enough threads: about kTargetThreads resident threads
-// (148 SMs x 512) keep every SM's pipes fed. It takes the cheapest tile
-// configuration (fewest threads per channel) that reaches the target from the
-// channels alone, and splits L into chunks only if even 8 threads per channel
-// fall short. Chunks are never shorter than kMinChunk tokens.
-constexpr int64_t kTargetThreads = 148 * 512;
+// looks for enough warps to keep every SM sub-partition issuing: about
+// kTargetThreads resident threads (148 SMs x 4 sub-partitions x 2 warps). The
+// channels alone usually provide them (a channel is shared by 4 lanes); the
+// sequence is split into chunks only when they fall short, since every chunk
+// but the last is scanned twice. Chunks are never shorter than kMinChunk.
+constexpr int64_t kTargetThreads = 148 * 4 * 2 * 32;
 constexpr int64_t kMinChunk = 512;
 
 int set_cuda(cudaError_t e) {
@@ -58,12 +58,10 @@ int check_dims(const ssm_dims* d, bool scan) {
     return SSM_OK;
 }
 
-int choose_tile_cfg(int64_t channels, int64_t N, int32_t hint) {
-    if (N != 16) return 1;
+int choose_tile_cfg(int64_t N, int32_t hint) {
+    (void)N;
     if (hint > 0) return hint - 1;
-    for (int c = 0; c < ssm::kScanTileConfigs; ++c)
-        if (channels * ssm::scan_threads_per_channel(c) >= kTargetThreads) return c;
-    return ssm::kScanTileConfigs - 1;
+    return 0;
 }
 
 int make_plan(const ssm_dims* d, ssm::ScanPlan* p) {
@@ -71,11 +69,11 @@ int make_plan(const ssm_dims* d, ssm::ScanPlan* p) {
     const int64_t batch = d->batch, L = d->seqlen, dim = d->dim, N = d->dstate;
     const int64_t TS = ssm::kScanStageTokens;
     if (batch == 0 || L == 0 || dim == 0) return SSM_OK;
-    p->tile_cfg = choose_tile_cfg(batch * dim, N, d->tile_config_hint);
-    p->channels_per_cta = ssm::scan_tile_channels(p->tile_cfg);
+    p->tile_cfg = choose_tile_cfg(N, d->tile_config_hint);
+    p->channels_per_cta = ssm::scan_tile_channels(p->tile_cfg, N);
     p->tiles = (dim + p->channels_per_cta - 1) / p->channels_per_cta;
     const int64_t per_chunk = p->tiles * batch;
-    const int64_t threads = batch * dim * ssm::scan_threads_per_channel(p->tile_cfg);
+    const int64_t threads = batch * dim * ssm::scan_lanes_per_channel(p->tile_cfg, N);
     int64_t chunk;
     if (d->chunk_len_hint > 0) {
         chunk = d->chunk_len_hint;

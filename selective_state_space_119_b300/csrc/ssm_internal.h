@@ -8,22 +8,28 @@
 
 namespace ssm {
 
-// Scan tiling shared by the planner and the kernels. A tile configuration
-// fixes the channels per CTA and how many threads share one channel:
-//   id 0: 64 channels, 1 thread per channel      id 1: 64 channels, 2 per channel
-//   id 2: 32 channels, 4 per channel             id 3: 16 channels, 8 per channel
-// (dstate 16; smaller dstate always uses id 1). Tokens stream through shared
-// memory in stages of kScanStageTokens; L-chunks are a whole number of stages
-// so that only the sequence end is ragged.
-constexpr int kScanStageTokens = 16;
+// Scan tiling shared by the planner and the kernels. A CTA has SW "state"
+// warps, which run the recurrence, and RW "row" warps, which stage the inputs,
+// compute dt and write the gated output. NS lanes of a state warp share one
+// channel's N states (each holds N / NS of them), so a state warp covers
+// 32 / NS channels and a CTA SW * 32 / NS channels:
+//   id 0: NS 4, SW 4, RW 2   id 1: NS 8, SW 4, RW 2
+//   id 2: NS 4, SW 2, RW 1   id 3: NS 2, SW 4, RW 2
+// For N < NS the lanes per channel drop to N, and a CTA keeps at most 64
+// channels. Tokens stream through shared memory in stages of kScanStageTokens;
+// L-chunks are a whole number of stages so that only the sequence end is
+// ragged.
+constexpr int kScanStageTokens = 32;
 constexpr int kScanTileConfigs = 4;
-inline int scan_tile_channels(int cfg) {
-    static const int ch[kScanTileConfigs] = {64, 64, 32, 16};
-    return ch[cfg];
+inline int scan_lanes_per_channel(int cfg, int64_t N) {
+    static const int ns[kScanTileConfigs] = {4, 8, 4, 2};
+    return ns[cfg] < N ? ns[cfg] : static_cast<int>(N);
 }
-inline int scan_threads_per_channel(int cfg) {
-    static const int t[kScanTileConfigs] = {1, 2, 4, 8};
-    return t[cfg];
+inline int scan_tile_channels(int cfg, int64_t N) {
+    static const int sw[kScanTileConfigs] = {4, 4, 2, 4};
+    const int cpw = 32 / scan_lanes_per_channel(cfg, N);
+    const int warps = sw[cfg] * cpw <= 64 ? sw[cfg] : (64 / cpw > 0 ? 64 / cpw : 1);
+    return warps * cpw;
 }
 
 // Host-side plan of one scan call (pure function of the sizes and hints).
