@@ -99,7 +99,8 @@ def aggregate(units_this_rank: float, seconds_this_rank: float, group=None):
 
 
 class ClockSampler:
-    """Samples SM clock and clock-event reasons through NVML in a thread."""
+    """Samples the SM clock and the clock-event reasons during the timed region:
+    through NVML when it initialises, else by running nvidia-smi in a loop."""
 
     REASONS = {
         0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
@@ -114,7 +115,8 @@ class ClockSampler:
         self.sm_max = None
         self._stop = threading.Event()
         self._thread = None
-        self.ok = False
+        self._proc = None
+        self.source = None
 
     def start(self):
         try:
@@ -123,14 +125,27 @@ class ClockSampler:
             self._nv = pynvml
             self._h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
             self.sm_max = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception:
+            self.source = "nvml"
+            self._thread = threading.Thread(target=self._run_nvml, daemon=True)
+            self._thread.start()
             return self
-        self._thread = threading.Thread(target=self._run, daemon=True)
-        self._thread.start()
+        except Exception:
+            pass
+        try:
+            import subprocess
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
+            self._thread = threading.Thread(target=self._run_smi, daemon=True)
+            self._thread.start()
+        except Exception:
+            self.source = None
         return self
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self._nv
         while not self._stop.is_set():
             try:
@@ -141,14 +156,31 @@ class ClockSampler:
                 pass
             time.sleep(self.period)
 
+    def _run_smi(self):
+        for line in self._proc.stdout:
+            try:
+                sm, smax, reasons = [x.strip() for x in line.split(",")]
+                self.sm_max = int(float(smax))
+                self.samples.append((time.time(), int(float(sm)), int(reasons, 16)))
+            except Exception:
+                pass
+            if self._stop.is_set():
+                break
+
     def stop(self):
         self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=2)
+            except Exception:
+                self._proc.kill()
         if self._thread:
             self._thread.join(timeout=2)
 
     def summary(self, t0=None, t1=None):
-        if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        if self.source is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
         s = [x for x in self.samples if (t0 is None or x[0] >= t0) and (t1 is None or x[0] <= t1)]
         window = "timed"
         if len(s) < 3:
@@ -160,7 +192,7 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median([x[1] for x in s]) if s else None,
                 "sm_max_mhz": self.sm_max, "reasons": sorted(reasons), "samples": len(s),
-                "window": window}
+                "window": window, "source": self.source}
 
 
 # ---------------------------------------------------------------------------
@@ -223,11 +255,11 @@ def bench_scan(args, rank, world, local):
         if rc != 0:
             raise libssm.SSMError(rc, "ssm_selective_scan_fwd")
 
+    clocks = ClockSampler(local).start()
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(local).start()
     import torch.distributed as dist
     if dist.is_initialized():
         dist.barrier()
@@ -260,6 +292,7 @@ def bench_scan(args, rank, world, local):
                      "kernel": "ssm_selective_scan_fwd call (%d kernel%s)"
                                % (plan["kernels"], "s" if plan["kernels"] > 1 else ""),
                      "algorithmic_bytes_per_call": alg_bytes},
+        "alu_roofline": alu_roofline(spec, per_call),
         "gpu_launches": args.steps * plan["kernels"],
         "clocks": clocks.summary(t_wall0, t_wall1),
         "plan": plan,
@@ -304,6 +337,27 @@ def bench_scan(args, rank, world, local):
     if not args.no_decode:
         res["decode"] = bench_decode(args, dev, stream)
     return res, spec
+
+
+# SFU (MUFU) exponential rate of one B300 SM per clock, measured with a probe of
+# back-to-back independent ex2.approx.ftz.f32 at full occupancy: 29.1 per SM per
+# clock (the nominal 2 x 16 of Blackwell Ultra's doubled SFU), 148 SMs, at the
+# 2032 MHz maximum SM clock.
+EX2_PER_SM_CLK = 29.1
+SMS = 148
+SM_MAX_MHZ = 2032.0
+
+
+def alu_roofline(spec, per_call_s):
+    """The exponentials the method needs (N per element for exp(dt A), one more
+    per element for softplus and one for the silu gate) per second, against the
+    SFU peak."""
+    per_elem = spec.N + (1 if spec.delta_softplus else 0) + (1 if spec.gate else 0)
+    achieved = spec.elements * per_elem / per_call_s / 1e12
+    peak = EX2_PER_SM_CLK * SMS * SM_MAX_MHZ * 1e6 / 1e12
+    return {"bound": "alu", "unit": "T exp/s", "achieved": achieved, "peak": peak,
+            "frac": achieved / peak, "exp_per_element": per_elem,
+            "peak_basis": "measured ex2 rate 29.1 per SM per clock x 148 SMs x 2032 MHz"}
 
 
 def parity_probe(spec, inp, out):
@@ -472,7 +526,7 @@ def _name_of(spec):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -506,7 +560,7 @@ def main(argv=None):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f32", "io_dtype": spec.io, "data": "synthetic",
                 "config": workload_config(spec), "gbps": res["gbps"],
-                "roofline": res["roofline"], "e2e": res["e2e"],
+                "roofline": res["roofline"], "alu_roofline": res["alu_roofline"], "e2e": res["e2e"],
                 "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
                 "plan": res["plan"], "check": res["check"]}
         if "decode" in res:

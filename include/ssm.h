@@ -67,7 +67,8 @@ enum {
                                of 8 (bf16) / 4 (fp32)                             */
     SSM_ERR_WORKSPACE = -5, /* workspace NULL or smaller than ssm_scan_workspace_bytes */
     SSM_ERR_CUDA = -6,      /* a CUDA launch or query failed (see ssm_last_cuda_error) */
-    SSM_ERR_TIMEOUT = -7,   /* device side: a bounded wait on another CTA gave up  */
+    SSM_ERR_TIMEOUT = -7,   /* device side: a bounded wait gave up (reserved: no
+                               current kernel waits on another CTA)           */
     SSM_ERR_ALIAS = -8      /* an output overlaps an input                         */
 };
 
@@ -92,9 +93,9 @@ typedef struct {
     void* workspace;
     size_t workspace_bytes;
     int32_t tile_config_hint; /* 0: library's choice; 1..4: force tile configuration
-                                 0..3 of the scan: lanes sharing one channel's
-                                 states x warps per CTA = 4x4, 8x4, 4x2, 2x4
-                                 (fewer lanes when dstate is smaller)        */
+                                 0..3 of the scan: 4, 2, 1 or 3 warps per CTA
+                                 (32 channels per warp); dstate 16 only,
+                                 other dstate always use configuration 0      */
     int32_t reserved;         /* must be 0 */
 } ssm_dims;
 

@@ -17,14 +17,14 @@ thread_local int g_last_cuda_error = 0;
 
 constexpr int64_t kMaxDim = int64_t(1) << 31;     // per-axis limit
 constexpr int64_t kMaxElems = int64_t(1) << 40;   // batch * seqlen * dim limit
-// Planning. The scan is ALU-bound (16 exponentials per element), so the plan
-// looks for enough warps to keep every SM sub-partition issuing: about
-// kTargetThreads resident threads (148 SMs x 4 sub-partitions x 2 warps). The
-// channels alone usually provide them (a channel is shared by 4 lanes); the
-// sequence is split into chunks only when they fall short, since every chunk
-// but the last is scanned twice. Chunks are never shorter than kMinChunk.
-constexpr int64_t kTargetThreads = 148 * 4 * 2 * 32;
-constexpr int64_t kMinChunk = 512;
+// Planning. A lane of the scan owns one channel, so the channels alone give
+// batch * dim threads. One warp per SM sub-partition (148 x 4 x 32 threads)
+// keeps the SFU and FMA pipes of every sub-partition fed; the plan splits the
+// sequence into about kTargetThreads / (batch * dim) chunks (rounded to the
+// nearest whole number), since every chunk but the last is scanned twice.
+// Chunks are never shorter than kMinChunk tokens.
+constexpr int64_t kTargetThreads = 148 * 4 * 32;
+constexpr int64_t kMinChunk = 256;
 
 int set_cuda(cudaError_t e) {
     g_last_cuda_error = static_cast<int>(e);
@@ -59,7 +59,7 @@ int check_dims(const ssm_dims* d, bool scan) {
 }
 
 int choose_tile_cfg(int64_t N, int32_t hint) {
-    (void)N;
+    if (N != 16) return 0;   // small dstate runs configuration 0 only
     if (hint > 0) return hint - 1;
     return 0;
 }
@@ -70,15 +70,15 @@ int make_plan(const ssm_dims* d, ssm::ScanPlan* p) {
     const int64_t TS = ssm::kScanStageTokens;
     if (batch == 0 || L == 0 || dim == 0) return SSM_OK;
     p->tile_cfg = choose_tile_cfg(N, d->tile_config_hint);
-    p->channels_per_cta = ssm::scan_tile_channels(p->tile_cfg, N);
+    p->channels_per_cta = ssm::scan_tile_channels(p->tile_cfg);
     p->tiles = (dim + p->channels_per_cta - 1) / p->channels_per_cta;
     const int64_t per_chunk = p->tiles * batch;
-    const int64_t threads = batch * dim * ssm::scan_lanes_per_channel(p->tile_cfg, N);
+    const int64_t threads = batch * dim;
     int64_t chunk;
     if (d->chunk_len_hint > 0) {
         chunk = d->chunk_len_hint;
     } else {
-        int64_t nck = std::max<int64_t>(1, (kTargetThreads + threads - 1) / threads);
+        int64_t nck = std::max<int64_t>(1, (kTargetThreads + threads / 2) / threads);
         nck = std::min(nck, std::max<int64_t>(1, L / kMinChunk));
         chunk = (L + nck - 1) / nck;
     }

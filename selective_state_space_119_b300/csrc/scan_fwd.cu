@@ -23,32 +23,33 @@
 //                    last chunk writes final_state           (MODE 1)
 // An unsplit sequence runs phase 3 alone.
 //
-// Work layout. One CTA = one (chunk, batch row, tile of DT channels) and WARPS
-// warps. A warp owns CPW = 32 / NS consecutive channels of the tile; lane
-// (c, j) = (lane / NS, lane % NS) holds states [j*SPL, j*SPL + SPL) of channel
-// c in fp32 registers (SPL = N / NS). Each warp works on its own channels from
-// start to end; the only CTA-wide barrier is one per stage of TS = 32 tokens.
+// Work layout. The data movement that bounds this scan on B300 is the
+// broadcast of B_t and C_t (shared by every channel) from shared memory into
+// the registers of every lane that uses them. A lane loads each B_t / C_t value
+// once per token and reuses it for two channels: two adjacent lanes (a pair)
+// own two adjacent channels; lane j of the pair holds states
+// [j*N/2, (j+1)*N/2) of both channels in fp32 registers. Lane j computes its
+// own channel's dt = softplus(delta + bias) and dt x and swaps them with its
+// partner; after the token both lanes hold half of each channel's C_t . h and
+// swap the half for the partner's channel, so each lane ends with the full
+// readout of its own channel and writes y = (C . h + D x) * silu(z). A warp
+// covers 32 consecutive channels; a CTA W warps of one batch row and one
+// chunk. (dstate 1 runs one lane per channel.)
 //
-// Per stage:
-//   * TMA (cp.async.bulk.tensor) has loaded the [TS x DT] tiles of x, delta and
-//     z into an NST-deep ring of shared-memory buffers (mbarrier completion);
-//     B_t and C_t rows of the stage were converted to fp32 in shared memory
-//     during the previous stage by all threads of the CTA, and are read by
-//     every warp.
-//   * prologue (lane = token of the stage): dt = softplus(delta + bias) and
-//     dt * x for the warp's CPW channels, into a warp-private buffer; tokens
-//     past the chunk end get dt = dt*x = 0, which leaves h unchanged exactly
-//     (exp(0) = 1), so the state loop needs no ragged bounds.
-//   * states: for each token, exp2(dt * A log2 e) on the SFU, h = Abar h +
-//     (dt x) B_t and the lane's partial C_t . h, in packed f32x2 arithmetic.
-//     Each lane stores its partial sums to a warp-private buffer, four tokens
-//     per store.
-//   * epilogue (lane = token again): y = sum of the NS partials + D x, times
-//     silu(z), rounded to the I/O type, into the output tile.
-//   * one elected thread TMA-stores the stage's output tile (triple-buffered)
-//     and refills the input ring.
-// Every mbarrier wait is bounded; a wait that gives up sets the workspace
-// status word and the CTA stops.
+// Per 32-token stage, TMA (cp.async.bulk.tensor) loads the [32 x DT] tiles of
+// x, delta (and z) and the stage's B_t (and C_t) rows into a ring of NST
+// shared-memory stages (mbarrier completion, bounded waits). Per token a lane
+//   * reads x, delta (and z) of its channel from the staged tile;
+//   * forms, for each of its states, Abar = exp2(dt * A log2 e) on the SFU,
+//     h = Abar h + (dt x) B_t and the readout, in packed f32x2 arithmetic;
+//   * writes y into the stage's output tile in shared memory, which one thread
+//     TMA-stores (cp.async.bulk.tensor) after the stage.
+// The B_t / C_t rows of the next stage are converted to fp32 into the other
+// half of a double-buffered shared array and published by the one CTA barrier
+// of each stage, after which the stage's ring slot is refilled. Tokens past
+// the chunk end get dt = dt x = 0, which leaves h unchanged exactly
+// (exp(0) = 1), and are not stored. No thread ever waits for another CTA; a
+// TMA wait that gives up sets the workspace status word and the CTA stops.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -62,105 +63,58 @@
 namespace ssm {
 namespace {
 
+
 constexpr uint32_t kMaxPolls = 1u << 24;  // bound on one mbarrier wait (about a second)
 constexpr uint32_t kStatusTimeout = 7;    // -SSM_ERR_TIMEOUT
 
-template <int NS_, int SW_, int RW_>
+template <int W_>
 struct TileCfg {
-    static constexpr int NS = NS_, SW = SW_, RW = RW_;
+    static constexpr int W = W_;
 };
 
 template <typename T, int N, typename TC>
 struct Cfg {
-    static constexpr int NS = TC::NS < N ? TC::NS : N;   // lanes per channel
+    static constexpr int NS = N >= 2 ? 2 : 1;             // lanes (and channels) per group
     static constexpr int SPL = N / NS;                    // states per lane
-    static constexpr int CPW = 32 / NS;                   // channels per state warp
-    // state warps (small dstate: at most 64 channels per CTA)
-    static constexpr int SW = TC::SW * CPW <= 64 ? TC::SW : (64 / CPW > 0 ? 64 / CPW : 1);
-    static constexpr int RW = TC::RW;                     // row warps
-    static constexpr int DT = SW * CPW;                   // channels per CTA
-    static constexpr int CPR = DT / RW;                   // channels per row lane
-    static constexpr int THREADS = (SW + RW) * 32;
-    static constexpr int ROW_THREADS = RW * 32;
-    static constexpr int TS = kScanStageTokens;           // tokens per stage (= 32 lanes)
-    static constexpr int TILE = TS * DT;                  // elements per [TS x DT] tile
-    static constexpr int NST = 3;                         // input ring depth (stages)
-    static constexpr int R = 2;                           // dt / B,C / partial-sum ring depth
-    static_assert(TS == 32, "a row lane owns one token of the stage");
-    static_assert(N % NS == 0 && 32 % NS == 0, "state split");
-    static_assert(DT % RW == 0 && CPR >= 4, "row lanes own whole vectors of channels");
-    static_assert(DT * sizeof(T) % 16 == 0, "TMA rows must be whole 16-byte units");
+    static constexpr int W = TC::W;                       // warps per CTA
+    static constexpr int DT = 32 * W;                     // channels per CTA (one per lane)
+    static constexpr int THREADS = 32 * W;
+    static constexpr int TS = kScanStageTokens;           // tokens per stage
+    static constexpr int TILE = TS * DT;                  // elements of one [TS x DT] tile
+    static constexpr int NST = TILE * sizeof(T) >= 16384 ? 2 : 3;  // TMA ring depth (stages)
+    static_assert(DT * sizeof(T) % 16 == 0, "TMA rows are whole 16-byte units");
 };
-
-constexpr int align128(int v) { return (v + 127) & ~127; }
 
 template <typename T, int N, typename TC, int MODE>
 struct Smem {
     using C = Cfg<T, N, TC>;
-    static constexpr int NT = MODE == 1 ? 3 : 2;  // x, delta (, z) tiles per stage
-    // B (and, for the output pass, C) rows travel with the stage's TMA
-    // transaction when a row is a whole number of 16-byte units; otherwise the
-    // row warps read them from global memory while converting.
+    static constexpr int NT = MODE == 1 ? 3 : 2;          // x, delta (, z) tiles per stage
+    static constexpr int NBC = MODE == 1 ? 2 : 1;         // B (and C) rows per token
+    static constexpr int ROW = NBC * N;                   // floats per token row of bcf
+    // B / C rows travel with the stage's TMA transaction when a row is a whole
+    // number of 16-byte units; otherwise they are read from global memory
+    // while being converted.
     static constexpr bool BC_TMA = (N * sizeof(T)) % 16 == 0;
-    static constexpr int NBC = MODE == 1 ? 2 : 1;
     static constexpr int BC_ELEMS = BC_TMA ? NBC * C::TS * N : 0;
     static constexpr int STAGE_ELEMS = NT * C::TILE + BC_ELEMS;
-    // padded row strides (floats): row-lane writes and column reads then hit
-    // distinct banks
-    static constexpr int DTP_ROW = 2 * C::DT + 4;     // one token's (dt, dt*x) pairs
-    static constexpr int YS_ROW = C::TS + 4;          // one (channel, lane) row of partials
-    static constexpr int BCF = C::TS * 2 * N;         // floats per B/C slot
     static constexpr int kIn = 0;                                                   // [NST][STAGE_ELEMS] T
-    static constexpr int kBC = align128(kIn + C::NST * STAGE_ELEMS * int(sizeof(T)));  // [R][TS][NS][2*SPL] f32
-    static constexpr int kDtp = align128(kBC + C::R * BCF * 4);                     // [R][TS][DTP_ROW] f32
-    static constexpr int kYs = align128(kDtp + C::R * C::TS * DTP_ROW * 4);         // [R][DT*NS][YS_ROW] f32
-    static constexpr int kOut = align128(kYs + (MODE == 1 ? C::R * C::DT * C::NS * YS_ROW * 4 : 0));  // [2][TS][DT] T
-    static constexpr int kPar = align128(kOut + (MODE == 1 ? 2 * C::TILE * int(sizeof(T)) : 0));  // [2][DT] f32: bias, D
-    static constexpr int kBar = align128(kPar + 2 * C::DT * 4);
-    // barriers: full[NST], prep_full[R], prep_empty[R], ys_full[R], ys_empty[R]
-    static constexpr int kBytes = align128(kBar + (C::NST + 4 * C::R) * 8);
+    static constexpr int kOut = kIn + C::NST * STAGE_ELEMS * int(sizeof(T));        // [2][TS][DT] T
+    static constexpr int kBC = (kOut + (MODE == 1 ? 2 * C::TILE * int(sizeof(T)) : 0) + 127) & ~127;  // [2][TS][ROW] f32
+    static constexpr int kBar = kBC + 2 * C::TS * ROW * 4;
+    static constexpr int kBytes = kBar + C::NST * 8;
     static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
     static_assert((STAGE_ELEMS * sizeof(T)) % 128 == 0 && (C::TILE * sizeof(T)) % 128 == 0,
                   "TMA destinations stay 128-byte aligned");
 };
-
-// ---- shared-memory element access ----------------------------------------
-__device__ __forceinline__ float lds1(const float* p) { return *p; }
-__device__ __forceinline__ float lds1(const __nv_bfloat16* p) {
-    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16);
-}
-__device__ __forceinline__ void sts1(float* p, float v) { *p = v; }
-__device__ __forceinline__ void sts1(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 __device__ __forceinline__ void unpack_bf16x2(uint32_t w, float& lo, float& hi) {
     lo = __uint_as_float(w << 16);
     hi = __uint_as_float(w & 0xffff0000u);
 }
 
-// K consecutive elements of one shared-memory row (K * sizeof(T) bytes,
-// aligned to min(16, K * sizeof(T))) widened to fp32.
+// K floats from shared memory (16-byte vectors where K allows).
 template <int K>
-__device__ __forceinline__ void lds_row(const __nv_bfloat16* p, float* v) {
-    if constexpr (K % 8 == 0) {
-#pragma unroll
-        for (int i = 0; i < K; i += 8) {
-            const uint4 u = *reinterpret_cast<const uint4*>(p + i);
-            unpack_bf16x2(u.x, v[i], v[i + 1]);
-            unpack_bf16x2(u.y, v[i + 2], v[i + 3]);
-            unpack_bf16x2(u.z, v[i + 4], v[i + 5]);
-            unpack_bf16x2(u.w, v[i + 6], v[i + 7]);
-        }
-    } else if constexpr (K == 4) {
-        const uint2 u = *reinterpret_cast<const uint2*>(p);
-        unpack_bf16x2(u.x, v[0], v[1]);
-        unpack_bf16x2(u.y, v[2], v[3]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < K; ++i) v[i] = lds1(p + i);
-    }
-}
-template <int K>
-__device__ __forceinline__ void lds_row(const float* p, float* v) {
+__device__ __forceinline__ void lds_f(const float* p, float* v) {
     if constexpr (K % 4 == 0) {
 #pragma unroll
         for (int i = 0; i < K; i += 4) {
@@ -173,9 +127,6 @@ __device__ __forceinline__ void lds_row(const float* p, float* v) {
     }
 }
 
-// K floats from shared memory (16-byte vectors where K allows).
-template <int K>
-__device__ __forceinline__ void lds_f(const float* p, float* v) { lds_row<K>(p, v); }
 
 template <int K>
 __device__ __forceinline__ void sts_f(float* p, const float* v) {
@@ -191,35 +142,14 @@ __device__ __forceinline__ void sts_f(float* p, const float* v) {
     }
 }
 
-// K consecutive elements of one shared-memory row from fp32, rounded to T.
-template <int K>
-__device__ __forceinline__ void sts_row(float* p, const float* v) { sts_f<K>(p, v); }
-template <int K>
-__device__ __forceinline__ void sts_row(__nv_bfloat16* p, const float* v) {
-    auto pk = [](float lo, float hi) {
-        const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half)
-        return *reinterpret_cast<const uint32_t*>(&b);
-    };
-    if constexpr (K % 8 == 0) {
-#pragma unroll
-        for (int i = 0; i < K; i += 8)
-            *reinterpret_cast<uint4*>(p + i) = make_uint4(pk(v[i], v[i + 1]), pk(v[i + 2], v[i + 3]),
-                                                          pk(v[i + 4], v[i + 5]), pk(v[i + 6], v[i + 7]));
-    } else if constexpr (K == 4) {
-        *reinterpret_cast<uint2*>(p) = make_uint2(pk(v[0], v[1]), pk(v[2], v[3]));
-    } else {
-#pragma unroll
-        for (int i = 0; i < K; ++i) sts1(p + i, v[i]);
-    }
-}
-
 // One state-lane step for one token: h <- exp2(dt * A2) h + dtx * B, and
 // (MODE 1) the partial C . h over the lane's states.
 template <int SPL, bool READOUT>
 __device__ __forceinline__ float state_step(float dt, float dtx, const float* __restrict__ bc,
                                             const float (&A2)[SPL], float (&h)[SPL]) {
     if constexpr (SPL % 2 == 0) {
-        float2 acc = make_float2(0.f, 0.f);
+        // two accumulators halve the dependent chain of the readout
+        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         const float2 dt2 = make_float2(dt, dt), dtx2 = make_float2(dtx, dtx);
 #pragma unroll
         for (int q = 0; q < SPL; q += 2) {
@@ -230,9 +160,11 @@ __device__ __forceinline__ float state_step(float dt, float dtx, const float* __
             h[q] = hn.x;
             h[q + 1] = hn.y;
             if constexpr (READOUT)
-                acc = __ffma2_rn(make_float2(bc[SPL + q], bc[SPL + q + 1]), hn, acc);
+                acc[(q / 2) & 1] =
+                    __ffma2_rn(make_float2(bc[SPL + q], bc[SPL + q + 1]), hn, acc[(q / 2) & 1]);
         }
-        return acc.x + acc.y;
+        const float2 sum = make_float2(acc[0].x + acc[1].x, acc[0].y + acc[1].y);
+        return sum.x + sum.y;
     } else {
         float acc = 0.f;
 #pragma unroll
@@ -244,87 +176,37 @@ __device__ __forceinline__ float state_step(float dt, float dtx, const float* __
     }
 }
 
-// The token's discretized parameters for the lane's states:
-// Abar = exp2(dt * A log2 e) and (dt x) B.
-template <int SPL>
-__device__ __forceinline__ void discretize(float dt, float dtx, const float* __restrict__ bv,
-                                           const float (&A2)[SPL], float (&ea)[SPL],
-                                           float (&bx)[SPL]) {
-    if constexpr (SPL % 2 == 0) {
-        const float2 dt2 = make_float2(dt, dt), dtx2 = make_float2(dtx, dtx);
-#pragma unroll
-        for (int q = 0; q < SPL; q += 2) {
-            const float2 arg = __fmul2_rn(dt2, make_float2(A2[q], A2[q + 1]));
-            ea[q] = ex2(arg.x);
-            ea[q + 1] = ex2(arg.y);
-            const float2 u = __fmul2_rn(dtx2, make_float2(bv[q], bv[q + 1]));
-            bx[q] = u.x;
-            bx[q + 1] = u.y;
-        }
-    } else {
-#pragma unroll
-        for (int q = 0; q < SPL; ++q) {
-            ea[q] = ex2(dt * A2[q]);
-            bx[q] = dtx * bv[q];
-        }
-    }
+__device__ __forceinline__ void sts_elem(float* p, float v) { *p = v; }
+__device__ __forceinline__ void sts_elem(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+__device__ __forceinline__ float lds_elem(const float* p) { return *p; }
+__device__ __forceinline__ float lds_elem(const __nv_bfloat16* p) {
+    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16);
 }
 
-// h <- Abar h + (dt x) B and the lane's partial C . h.
-template <int SPL>
-__device__ __forceinline__ float recur_readout(const float (&ea)[SPL], const float (&bx)[SPL],
-                                               const float* __restrict__ cv, float (&h)[SPL]) {
-    if constexpr (SPL % 2 == 0) {
-        float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < SPL; q += 2) {
-            const float2 hn = __ffma2_rn(make_float2(ea[q], ea[q + 1]), make_float2(h[q], h[q + 1]),
-                                         make_float2(bx[q], bx[q + 1]));
-            h[q] = hn.x;
-            h[q + 1] = hn.y;
-            acc = __ffma2_rn(make_float2(cv[q], cv[q + 1]), hn, acc);
-        }
-        return acc.x + acc.y;
-    } else {
-        float acc = 0.f;
-#pragma unroll
-        for (int q = 0; q < SPL; ++q) {
-            h[q] = fmaf(ea[q], h[q], bx[q]);
-            acc = fmaf(cv[q], h[q], acc);
-        }
-        return acc;
-    }
-}
-
-template <typename T, int N, typename TC, int MODE>
+// SOFTPLUS: dt = softplus(delta + bias); GATE: out = y * silu(z). Both are
+// template flags so that the per-token body has no branches and the compiler
+// can overlap successive tokens.
+template <typename T, int N, typename TC, int MODE, bool SOFTPLUS, bool GATE>
 __global__ void __launch_bounds__(Cfg<T, N, TC>::THREADS, 1)
 scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dt,
-            const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_out,
-            const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_C,
+            const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
+            const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_out,
             const ScanArgs a) {
     using Cf = Cfg<T, N, TC>;
     using Sm = Smem<T, N, TC, MODE>;
-    constexpr int NS = Cf::NS, SPL = Cf::SPL, CPW = Cf::CPW, DT = Cf::DT, TS = Cf::TS;
-    constexpr int CPR = Cf::CPR, RW = Cf::RW, NST = Cf::NST, R = Cf::R, TILE = Cf::TILE;
-    constexpr int NT = Sm::NT, NBC = Sm::NBC, DTP_ROW = Sm::DTP_ROW, YS_ROW = Sm::YS_ROW;
-    constexpr int ROW_THREADS = Cf::ROW_THREADS, STATE_THREADS = Cf::SW * 32;
+    constexpr int NS = Cf::NS, SPL = Cf::SPL, DT = Cf::DT, TS = Cf::TS, TILE = Cf::TILE;
+    constexpr int NST = Cf::NST, THREADS = Cf::THREADS, NT = Sm::NT, NBC = Sm::NBC, ROW = Sm::ROW;
     constexpr bool BC_TMA = Sm::BC_TMA;
+    constexpr bool has_z = MODE == 1 && GATE;
 
     extern __shared__ __align__(128) unsigned char smem[];
-    T* in = reinterpret_cast<T*>(smem + Sm::kIn);           // [NST] x, delta, (z,) B, (C) of a stage
-    float* bcf_all = reinterpret_cast<float*>(smem + Sm::kBC);
-    float* dtp_all = reinterpret_cast<float*>(smem + Sm::kDtp);
-    float* ys_all = reinterpret_cast<float*>(smem + Sm::kYs);
-    T* outb = reinterpret_cast<T*>(smem + Sm::kOut);
-    float* par = reinterpret_cast<float*>(smem + Sm::kPar);  // [0..DT): bias, [DT..2DT): D
+    T* in = reinterpret_cast<T*>(smem + Sm::kIn);          // [NST] x, delta, (z,) B, (C) of a stage
+    T* outb = reinterpret_cast<T*>(smem + Sm::kOut);         // [2][TS][DT] output tiles
+    float* bcf = reinterpret_cast<float*>(smem + Sm::kBC);  // [2][TS][ROW]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sm::kBar);
-    uint64_t* prep_full = full + NST;    // row warps -> state warps: dt, dt*x, B/C of a stage
-    uint64_t* prep_empty = prep_full + R;  // state warps -> row warps: that slot is consumed
-    uint64_t* ys_full = prep_empty + R;  // state warps -> row warps: partial sums of a stage
-    uint64_t* ys_empty = ys_full + R;    // row warps -> state warps: that slot is consumed
 
     const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
+    const int lane = tid & 31, w = tid >> 5;
     const int64_t lin = blockIdx.x;  // chunk-major: ((k * batch) + b) * tiles + tile
     const int64_t tile = lin % a.tiles;
     const int64_t b = (lin / a.tiles) % a.batch;
@@ -333,28 +215,16 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const int64_t t_end = min(a.L, t_begin + a.chunk_len);
     const int nstages = static_cast<int>((t_end - t_begin + TS - 1) / TS);
     const int64_t dbase = tile * DT;
-    const bool has_z = MODE == 1 && a.z != nullptr;
+    // bytes that land per stage: the tiles actually loaded (no z tile without
+    // the gate) and the B / C rows
     const uint32_t stage_tx =
         static_cast<uint32_t>(((has_z ? 3 : 2) * TILE + Sm::BC_ELEMS) * sizeof(T));
 
     if (tid == 0) {
         for (int i = 0; i < NST; ++i) mbar_init(&full[i], 1);
-        for (int i = 0; i < R; ++i) {
-            mbar_init(&prep_full[i], ROW_THREADS);
-            mbar_init(&prep_empty[i], STATE_THREADS);
-            mbar_init(&ys_full[i], STATE_THREADS);
-            mbar_init(&ys_empty[i], ROW_THREADS);
-        }
         fence_mbar_init();
     }
-    for (int i = tid; i < DT; i += Cf::THREADS) {
-        const int64_t dq = dbase + i;
-        const bool okq = dq < a.dim;
-        par[i] = (a.delta_bias && okq) ? __ldg(a.delta_bias + dq) : 0.f;
-        par[DT + i] = (MODE == 1 && a.D && okq) ? __ldg(a.D + dq) : 0.f;
-    }
     __syncthreads();
-
     auto issue = [&](int s) {
         const int buf = s % NST;
         T* dst = in + static_cast<size_t>(buf) * Sm::STAGE_ELEMS;
@@ -362,7 +232,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         mbar_arrive_expect_tx(&full[buf], stage_tx);
         tma_load_3d(dst, &tm_x, static_cast<int>(dbase), t, static_cast<int>(b), &full[buf]);
         tma_load_3d(dst + TILE, &tm_dt, static_cast<int>(dbase), t, static_cast<int>(b), &full[buf]);
-        if (has_z)
+        if constexpr (has_z)
             tma_load_3d(dst + 2 * TILE, &tm_z, static_cast<int>(dbase), t, static_cast<int>(b),
                         &full[buf]);
         if constexpr (BC_TMA) {
@@ -371,224 +241,182 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 tma_load_3d(dst + NT * TILE + TS * N, &tm_C, 0, t, static_cast<int>(b), &full[buf]);
         }
     };
+    if (tid == 0)
+        for (int s = 0; s < NST && s < nstages; ++s) issue(s);
 
-    bool aborted = false;
-    if (warp < RW) {
-        // =================== row warps: TMA, prologue, epilogue ===================
-        const int rw = warp;                 // row warp index
-        int issued = 0;
-        if (tid == 0)
-            for (; issued < NST && issued < nstages; ++issued) issue(issued);
+    // ---- this lane: own channel d, pair position j; channel slot r holds
+    //      channel (d - j) + (j ^ r), i.e. slot 0 = own, slot 1 = partner ----
+    const int j = lane % NS;
+    const int col = w * 32 + lane;               // own channel within the tile
+    const int64_t d = dbase + col;
+    const bool ch_ok = d < a.dim;                 // dim is even: pairs are whole
+    const int64_t dsafe = ch_ok ? d : 0;
+    float A2[NS][SPL], h[NS][SPL], dt_sum = 0.f;
+#pragma unroll
+    for (int r = 0; r < NS; ++r) {
+        const int64_t dr = dsafe - j + (j ^ r);
+#pragma unroll
+        for (int q = 0; q < SPL; ++q) {
+            A2[r][q] = ch_ok ? __ldg(a.A + dr * N + j * SPL + q) * kLog2e : 0.f;
+            h[r][q] = 0.f;
+        }
+        if (MODE == 1 && k > 0 && ch_ok) {
+            const float* hin = a.ws_H + ((b * (a.nchunks - 1) + (k - 1)) * a.dim + dr) * N + j * SPL;
+#pragma unroll
+            for (int q = 0; q < SPL; ++q) h[r][q] = hin[q];
+        }
+    }
+    const float bias = (a.delta_bias && ch_ok) ? __ldg(a.delta_bias + dsafe) : 0.f;
+    const float Dd = (MODE == 1 && a.D && ch_ok) ? __ldg(a.D + dsafe) : 0.f;
 
-        // Row lane: token `lane` of a stage, channels [rw*CPR, rw*CPR + CPR).
-        const int cbase = rw * CPR;
-        const bool softplus_on = a.softplus != 0;
-        const T* __restrict__ Bg = static_cast<const T*>(a.B);
-        const T* __restrict__ Cg = static_cast<const T*>(a.C);
-        constexpr int VE = 16 / sizeof(T) < N ? 16 / sizeof(T) : N;   // elements per vector
-        constexpr int NVEC = NBC * TS * N / VE;                        // B/C vectors per stage
-        constexpr int RUN = SPL < VE ? SPL : VE;                       // runs of one state group
-
-        const int last = MODE == 1 ? nstages + 1 : nstages;
-        for (int i = 0; i < last; ++i) {
-            bool ok = true;
-            if (i < nstages) {
-                // ---- prologue of stage i ----
-                const int buf = i % NST, slot = i % R;
-                ok = mbar_wait_bounded(&full[buf], static_cast<uint32_t>((i / NST) & 1), kMaxPolls);
-                if (i >= R)
-                    ok = ok && mbar_wait_bounded(&prep_empty[slot],
-                                                 static_cast<uint32_t>(((i / R) - 1) & 1), kMaxPolls);
-                const T* xt = in + static_cast<size_t>(buf) * Sm::STAGE_ELEMS;
-                const T* dlt = xt + TILE;
-                const T* staged = xt + NT * TILE;
-                float* bcf = bcf_all + slot * Sm::BCF;
-                float* dtp = dtp_all + slot * TS * DTP_ROW;
-                const int64_t ts = t_begin + static_cast<int64_t>(i) * TS;
-                // B (and C) rows -> fp32 bcf[t][j][B(SPL) | C(SPL)]
-                for (int idx = tid; idx < NVEC; idx += ROW_THREADS) {
-                    const int which = idx / (TS * N / VE);
-                    const int r = idx % (TS * N / VE);
-                    const int t = r / (N / VE), n0 = (r % (N / VE)) * VE;
-                    float v[VE];
-                    if constexpr (BC_TMA) {
-                        lds_row<VE>(staged + which * TS * N + t * N + n0, v);  // zero past the end
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < VE; ++e)
-                            v[e] = ts + t < t_end
-                                       ? IO<T>::ld((which ? Cg : Bg) + (b * a.L + ts + t) * N + n0 + e)
-                                       : 0.f;
-                    }
-#pragma unroll
-                    for (int e = 0; e < VE; e += RUN) {
-                        const int n = n0 + e;
-                        sts_f<RUN>(bcf + (t * NS + n / SPL) * 2 * SPL + which * SPL + n % SPL, &v[e]);
-                    }
-                }
-                // dt and dt * x for token `lane`; tokens past the chunk end get
-                // dt = dt*x = 0, which leaves h unchanged exactly
-                {
-                    float xv[CPR], dv[CPR], bv[CPR];
-                    lds_row<CPR>(xt + lane * DT + cbase, xv);
-                    lds_row<CPR>(dlt + lane * DT + cbase, dv);
-                    lds_f<CPR>(par + cbase, bv);
-                    const bool valid = ts + lane < t_end;
-                    float o[2 * CPR];
-#pragma unroll
-                    for (int q = 0; q < CPR; ++q) {
-                        float dtv = dv[q] + bv[q];
-                        if (softplus_on) dtv = softplus(dtv);
-                        dtv = valid ? dtv : 0.f;
-                        o[2 * q] = dtv;
-                        o[2 * q + 1] = dtv * xv[q];
-                    }
-                    sts_f<2 * CPR>(dtp + lane * DTP_ROW + 2 * cbase, o);
-                }
-                mbar_arrive(&prep_full[slot]);
-                if constexpr (MODE == 0) {
-                    // the stage's input slot is free once every row thread is done
-                    if (named_bar_or(1, ROW_THREADS, !ok)) { aborted = true; break; }
-                    if (tid == 0 && issued < nstages) {
-                        fence_proxy_async_smem();
-                        issue(issued++);
-                    }
-                }
-            }
-            if constexpr (MODE == 1) {
-                if (i == 0) {
-                    if (named_bar_or(1, ROW_THREADS, !ok)) { aborted = true; break; }
+    // ---- B / C rows of a stage -> fp32 bcf[s & 1][t][B(N) | C(N)] ----
+    constexpr int VE = 16 / sizeof(T) < N ? 16 / sizeof(T) : N;  // elements per vector
+    constexpr int NVEC = NBC * TS * N / VE;                       // vectors per stage
+    const T* __restrict__ Bg = static_cast<const T*>(a.B) + b * a.L * N;
+    const T* __restrict__ Cg = static_cast<const T*>(a.C) + b * a.L * N;
+    auto convert_bc = [&](int s) {
+        const T* staged = in + static_cast<size_t>(s % NST) * Sm::STAGE_ELEMS + NT * TILE;
+        float* dst = bcf + (s & 1) * TS * ROW;
+        const int64_t ts = t_begin + static_cast<int64_t>(s) * TS;
+        for (int idx = tid; idx < NVEC; idx += THREADS) {
+            const int which = idx / (TS * N / VE);
+            const int r = idx % (TS * N / VE);
+            const int t = r / (N / VE), n0 = (r % (N / VE)) * VE;
+            float v[VE];
+            if constexpr (BC_TMA) {
+                const T* src = staged + which * TS * N + t * N + n0;   // zero past the end
+                if constexpr (sizeof(T) == 2) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(src);
+                    unpack_bf16x2(u.x, v[0], v[1]);
+                    unpack_bf16x2(u.y, v[2], v[3]);
+                    unpack_bf16x2(u.z, v[4], v[5]);
+                    unpack_bf16x2(u.w, v[6], v[7]);
                 } else {
-                    // ---- epilogue of stage e = i - 1 ----
-                    const int e = i - 1, slot = e % R, buf = e % NST;
-                    ok = ok && mbar_wait_bounded(&ys_full[slot], static_cast<uint32_t>((e / R) & 1),
-                                                 kMaxPolls);
-                    // the output buffer this stage writes was stored by stage e - 2
-                    if (tid == 0) bulk_wait_read<1>();
-                    if (named_bar_or(1, ROW_THREADS, !ok)) { aborted = true; break; }
-                    const T* xt = in + static_cast<size_t>(buf) * Sm::STAGE_ELEMS;
-                    const T* zt = xt + 2 * TILE;
-                    const float* ys = ys_all + slot * DT * NS * YS_ROW;
-                    T* ot = outb + (e & 1) * TILE;
-                    float xv[CPR], yv[CPR], Dq[CPR];
-                    lds_row<CPR>(xt + lane * DT + cbase, xv);
-                    lds_f<CPR>(par + DT + cbase, Dq);
-#pragma unroll
-                    for (int q = 0; q < CPR; ++q) {
-                        float y = 0.f;
-#pragma unroll
-                        for (int jj = 0; jj < NS; ++jj) y += ys[((cbase + q) * NS + jj) * YS_ROW + lane];
-                        yv[q] = fmaf(Dq[q], xv[q], y);
-                    }
-                    mbar_arrive(&ys_empty[slot]);
-                    if (has_z) {
-                        float zv[CPR];
-                        lds_row<CPR>(zt + lane * DT + cbase, zv);
-#pragma unroll
-                        for (int q = 0; q < CPR; ++q) yv[q] *= silu(zv[q]);
-                    }
-                    sts_row<CPR>(ot + lane * DT + cbase, yv);
-                    fence_proxy_async_smem();   // the output tile is read by the TMA store
-                    named_bar_sync(1, ROW_THREADS);
-                    if (tid == 0) {
-                        tma_store_3d(&tm_out, static_cast<int>(dbase),
-                                     static_cast<int>(t_begin + static_cast<int64_t>(e) * TS),
-                                     static_cast<int>(b), ot);
-                        bulk_commit();
-                        // the stage's input slot is free: refill it
-                        if (issued < nstages) {
-                            fence_proxy_async_smem();
-                            issue(issued++);
-                        }
-                    }
+                    const float4 u = *reinterpret_cast<const float4*>(src);
+                    v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
                 }
-            }
-        }
-        if (tid == 0) {
-            bulk_wait_all();
-            if (aborted) {
-                // let the copies already in flight land before the CTA releases its smem
-                for (int r = issued - NST < 0 ? 0 : issued - NST; r < issued; ++r)
-                    mbar_wait_bounded(&full[r % NST], static_cast<uint32_t>((r / NST) & 1), kMaxPolls);
-            }
-        }
-        if (aborted && lane == 0 && a.status) atomicExch(a.status, kStatusTimeout);
-        return;
-    }
-
-    // =================== state warps: the recurrence ===================
-    const int sw = warp - RW;
-    const int c = lane / NS, j = lane % NS;
-    const int col = sw * CPW + c;                // channel within the tile
-    const bool ch_ok = dbase + col < a.dim;
-    const int64_t d = ch_ok ? dbase + col : 0;
-    float A2[SPL], h[SPL];
+            } else {
 #pragma unroll
-    for (int q = 0; q < SPL; ++q) {
-        A2[q] = ch_ok ? __ldg(a.A + d * N + j * SPL + q) * kLog2e : 0.f;
-        h[q] = 0.f;
-    }
-    if (MODE == 1 && k > 0 && ch_ok) {
-        const float* hin = a.ws_H + ((b * (a.nchunks - 1) + (k - 1)) * a.dim + d) * N + j * SPL;
-#pragma unroll
-        for (int q = 0; q < SPL; ++q) h[q] = hin[q];
-    }
-    float dt_sum = 0.f;
+                for (int e = 0; e < VE; ++e)
+                    v[e] = ts + t < t_end ? IO<T>::ld((which ? Cg : Bg) + (ts + t) * N + n0 + e) : 0.f;
+            }
+            sts_f<VE>(dst + t * ROW + which * N + n0, v);
+        }
+    };
 
-    for (int s = 0; s < nstages; ++s) {
-        const int slot = s % R;
-        bool ok = mbar_wait_bounded(&prep_full[slot], static_cast<uint32_t>((s / R) & 1), kMaxPolls);
-        if (MODE == 1 && s >= R)
-            ok = ok && mbar_wait_bounded(&ys_empty[slot], static_cast<uint32_t>(((s / R) - 1) & 1),
-                                         kMaxPolls);
-        if (__any_sync(0xffffffffu, !ok)) { aborted = true; break; }
-        const float* dtp = dtp_all + slot * TS * DTP_ROW;
-        const float* bcf = bcf_all + slot * Sm::BCF;
+    bool ok = mbar_wait_bounded(&full[0], 0u, kMaxPolls);
+    convert_bc(0);
+    bool aborted = __syncthreads_or(!ok);
+
+    int s = 0;
+    for (; s < nstages && !aborted; ++s) {
+        const int buf = s % NST;
+        const T* xt = in + static_cast<size_t>(buf) * Sm::STAGE_ELEMS;
+        const T* dlt = xt + TILE;
+        const T* zt = xt + 2 * TILE;
+        const float* bc = bcf + (s & 1) * TS * ROW;
+        T* ot = outb + (s & 1) * TILE;
+        const int64_t t0 = t_begin + static_cast<int64_t>(s) * TS;
+        ok = s == 0 || mbar_wait_bounded(&full[buf], static_cast<uint32_t>((s / NST) & 1), kMaxPolls);
+        // Software-pipelined by one token: the next token's dt, dt * x (and
+        // the partner's, through the pair shuffle) are formed before this
+        // token's state update, so that their short serial chain overlaps it.
+        // (The prefetch after the last token wraps to token 0 of the stage and
+        // is discarded.)
+        struct Tok {
+            float dt[NS], dtx[NS], x;
+        };
+        auto prep = [&](int tl) {
+            Tok k;
+            k.x = lds_elem(xt + tl * DT + col);
+            float dt = lds_elem(dlt + tl * DT + col) + bias;
+            if constexpr (SOFTPLUS) dt = softplus(dt);
+            dt = t0 + tl < t_end ? dt : 0.f;
+            k.dt[0] = dt;
+            k.dtx[0] = dt * k.x;
+            if constexpr (NS == 2) {
+                k.dt[1] = __shfl_xor_sync(0xffffffffu, k.dt[0], 1);
+                k.dtx[1] = __shfl_xor_sync(0xffffffffu, k.dtx[0], 1);
+            }
+            return k;
+        };
+        Tok cur = prep(0);
+#pragma unroll 8
+        for (int tl = 0; tl < TS; ++tl) {
+            const Tok nxt = prep((tl + 1) & (TS - 1));
+            // this lane's states of B_t (then C_t)
+            float bv[2 * SPL];
+            lds_f<SPL>(bc + tl * ROW + j * SPL, bv);
+            if constexpr (MODE == 1) {
+                lds_f<SPL>(bc + tl * ROW + N + j * SPL, bv + SPL);
+                float part[NS];
+#pragma unroll
+                for (int r = 0; r < NS; ++r)
+                    part[r] = state_step<SPL, true>(cur.dt[r], cur.dtx[r], bv, A2[r], h[r]);
+                float y = part[0];
+                if constexpr (NS == 2) y += __shfl_xor_sync(0xffffffffu, part[1], 1);
+                y = fmaf(Dd, cur.x, y);
+                if constexpr (has_z) y *= silu(lds_elem(zt + tl * DT + col));
+                // unconditional: the tile's TMA store drops rows past the
+                // sequence end and channels past dim
+                sts_elem(ot + tl * DT + col, y);
+            } else {
+                dt_sum += cur.dt[0];
+#pragma unroll
+                for (int r = 0; r < NS; ++r)
+                    state_step<SPL, false>(cur.dt[r], cur.dtx[r], bv, A2[r], h[r]);
+            }
+            cur = nxt;
+        }
+        // B / C of the next stage (its bcf half was last read during stage s - 1)
+        if (s + 1 < nstages) {
+            ok = ok && mbar_wait_bounded(&full[(s + 1) % NST],
+                                         static_cast<uint32_t>(((s + 1) / NST) & 1), kMaxPolls);
+            convert_bc(s + 1);
+        }
         if constexpr (MODE == 1) {
-            // the recurrence and this lane's partial C . h for every token of
-            // the stage, kept in registers, then stored to the partial-sum slot
-            float p[TS];
-#pragma unroll
-            for (int t = 0; t < TS; ++t) {
-                const float2 dd = *reinterpret_cast<const float2*>(dtp + t * DTP_ROW + 2 * col);
-                float bcv[2 * SPL];
-                lds_f<2 * SPL>(bcf + (t * NS + j) * 2 * SPL, bcv);
-                p[t] = state_step<SPL, true>(dd.x, dd.y, bcv, A2, h);
+            fence_proxy_async_smem();   // the output tile is read by the TMA store
+            // the tile stage s + 1 writes was stored at the end of stage s - 1
+            if (tid == 0) bulk_wait_read<0>();
+        }
+        aborted = __syncthreads_or(!ok);   // stage s consumed by every warp
+        if (tid == 0 && !aborted) {
+            if constexpr (MODE == 1) {
+                tma_store_3d(&tm_out, static_cast<int>(dbase), static_cast<int>(t0),
+                             static_cast<int>(b), ot);
+                bulk_commit();
             }
-            mbar_arrive(&prep_empty[slot]);
-            float* yrow = ys_all + slot * DT * NS * YS_ROW + (sw * 32 + lane) * YS_ROW;  // row (col, j)
-#pragma unroll
-            for (int t4 = 0; t4 < TS; t4 += 4)
-                *reinterpret_cast<float4*>(yrow + t4) =
-                    make_float4(p[t4], p[t4 + 1], p[t4 + 2], p[t4 + 3]);
-            mbar_arrive(&ys_full[slot]);
-        } else {
-#pragma unroll
-            for (int t = 0; t < TS; ++t) {
-                const float2 dd = *reinterpret_cast<const float2*>(dtp + t * DTP_ROW + 2 * col);
-                float bv[SPL];
-                lds_f<SPL>(bcf + (t * NS + j) * 2 * SPL, bv);
-                dt_sum += dd.x;
-                state_step<SPL, false>(dd.x, dd.y, bv, A2, h);
+            if (s + NST < nstages) {
+                fence_proxy_async_smem();
+                issue(s + NST);
             }
-            mbar_arrive(&prep_empty[slot]);
         }
     }
+    if (tid == 0) bulk_wait_all();
     if (aborted) {
-        if (lane == 0 && a.status) atomicExch(a.status, kStatusTimeout);
+        if (tid == 0) {
+            // let the copies already in flight land before the CTA releases its smem
+            for (int r = s; r < nstages && r < s + NST; ++r)
+                mbar_wait_bounded(&full[r % NST], static_cast<uint32_t>((r / NST) & 1), kMaxPolls);
+            if (a.status) atomicExch(a.status, kStatusTimeout);
+        }
         return;
     }
+
     if (!ch_ok) return;
-    if (MODE == 0) {
-        const int64_t base = (b * (a.nchunks - 1) + k) * a.dim + d;
-        float* dst = a.ws_H + base * N + j * SPL;
 #pragma unroll
-        for (int q = 0; q < SPL; ++q) dst[q] = h[q];
-        if (j == 0) a.ws_S[base] = dt_sum;
-    } else if (a.final_state && k == a.nchunks - 1) {
-        float* fs = a.final_state + (b * a.dim + d) * N + j * SPL;
+    for (int r = 0; r < NS; ++r) {
+        const int64_t dr = d - j + (j ^ r);
+        if (MODE == 0) {
+            const int64_t base = (b * (a.nchunks - 1) + k) * a.dim + dr;
 #pragma unroll
-        for (int q = 0; q < SPL; ++q) fs[q] = h[q];
+            for (int q = 0; q < SPL; ++q) a.ws_H[base * N + j * SPL + q] = h[r][q];
+            if (r == 0) a.ws_S[base] = dt_sum;
+        } else if (a.final_state && k == a.nchunks - 1) {
+            float* fs = a.final_state + (b * a.dim + dr) * N + j * SPL;
+#pragma unroll
+            for (int q = 0; q < SPL; ++q) fs[q] = h[r][q];
+        }
     }
 }
 
@@ -653,7 +481,7 @@ cudaError_t make_tmap(CUtensorMap* tm, const void* base, int64_t batch, int64_t 
 
 // Raise the dynamic shared-memory limit of one kernel instantiation, once per
 // device (the statics are per instantiation).
-template <typename T, int N, typename TC, int MODE>
+template <typename T, int N, typename TC, int MODE, bool SP, bool GATE>
 cudaError_t allow_smem() {
     static std::mutex mu;
     static bool done[128] = {};
@@ -663,64 +491,76 @@ cudaError_t allow_smem() {
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(scan_kernel<T, N, TC, MODE>,
+    e = cudaFuncSetAttribute(scan_kernel<T, N, TC, MODE, SP, GATE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem<T, N, TC, MODE>::kBytes);
     if (e == cudaSuccess) done[dev] = true;
     return e;
 }
 
-template <typename T, int N, typename TC>
-cudaError_t launch_cfg(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
+template <typename T, int N, typename TC, bool SOFTPLUS, bool GATE>
+cudaError_t launch_flags(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     using Cf = Cfg<T, N, TC>;
     if (p.channels_per_cta != Cf::DT) return cudaErrorInvalidValue;
-    CUtensorMap tx, tdt, tz, tout;
+    CUtensorMap tx, tdt, tz, tB, tC, tout;
     cudaError_t e;
     if ((e = make_tmap<T>(&tx, a.x, a.batch, a.L, a.dim, Cf::DT)) != cudaSuccess) return e;
     if ((e = make_tmap<T>(&tdt, a.delta, a.batch, a.L, a.dim, Cf::DT)) != cudaSuccess) return e;
-    if ((e = make_tmap<T>(&tz, a.z ? a.z : a.x, a.batch, a.L, a.dim, Cf::DT)) != cudaSuccess)
-        return e;
     if ((e = make_tmap<T>(&tout, a.out, a.batch, a.L, a.dim, Cf::DT)) != cudaSuccess) return e;
+    tz = tx;
+    if (GATE && (e = make_tmap<T>(&tz, a.z, a.batch, a.L, a.dim, Cf::DT)) != cudaSuccess) return e;
     // B, C [batch][L][N]: box of N states x TS tokens (only when a row is a
     // whole number of 16-byte units; otherwise the kernel reads them directly)
-    CUtensorMap tB = tx, tC = tx;
+    tB = tx;
+    tC = tx;
     if constexpr (Smem<T, N, TC, 1>::BC_TMA) {
         if ((e = make_tmap<T>(&tB, a.B, a.batch, a.L, N, N)) != cudaSuccess) return e;
         if ((e = make_tmap<T>(&tC, a.C, a.batch, a.L, N, N)) != cudaSuccess) return e;
     }
     const int64_t per_chunk = p.tiles * a.batch;
     if (p.nchunks > 1) {
-        constexpr int sm0 = Smem<T, N, TC, 0>::kBytes;
-        if ((e = allow_smem<T, N, TC, 0>()) != cudaSuccess) return e;
-        scan_kernel<T, N, TC, 0>
-            <<<static_cast<unsigned>(per_chunk * (p.nchunks - 1)), Cf::THREADS, sm0, s>>>(
-                tx, tdt, tz, tout, tB, tC, a);
+        if ((e = allow_smem<T, N, TC, 0, SOFTPLUS, false>()) != cudaSuccess) return e;
+        scan_kernel<T, N, TC, 0, SOFTPLUS, false>
+            <<<static_cast<unsigned>(per_chunk * (p.nchunks - 1)), Cf::THREADS,
+               Smem<T, N, TC, 0>::kBytes, s>>>(tx, tdt, tz, tB, tC, tout, a);
         const int64_t n = a.batch * a.dim * N;
         scan_carry_kernel<N><<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(a);
     }
-    constexpr int sm1 = Smem<T, N, TC, 1>::kBytes;
-    if ((e = allow_smem<T, N, TC, 1>()) != cudaSuccess) return e;
-    scan_kernel<T, N, TC, 1>
-        <<<static_cast<unsigned>(per_chunk * p.nchunks), Cf::THREADS, sm1, s>>>(tx, tdt, tz, tout,
-                                                                                 tB, tC, a);
+    if ((e = allow_smem<T, N, TC, 1, SOFTPLUS, GATE>()) != cudaSuccess) return e;
+    scan_kernel<T, N, TC, 1, SOFTPLUS, GATE>
+        <<<static_cast<unsigned>(per_chunk * p.nchunks), Cf::THREADS, Smem<T, N, TC, 1>::kBytes,
+           s>>>(tx, tdt, tz, tB, tC, tout, a);
     return cudaGetLastError();
 }
 
-// The tile configurations by id (the same table as scan_lanes_per_channel and
-// scan_tile_warps in ssm_internal.h).
-using Tile0 = TileCfg<4, 4, 2>;
-using Tile1 = TileCfg<8, 4, 2>;
-using Tile2 = TileCfg<4, 2, 1>;
-using Tile3 = TileCfg<2, 4, 2>;
+template <typename T, int N, typename TC>
+cudaError_t launch_cfg(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
+    const bool sp = a.softplus != 0, gate = a.z != nullptr;
+    if (sp)
+        return gate ? launch_flags<T, N, TC, true, true>(a, p, s)
+                    : launch_flags<T, N, TC, true, false>(a, p, s);
+    return gate ? launch_flags<T, N, TC, false, true>(a, p, s)
+                : launch_flags<T, N, TC, false, false>(a, p, s);
+}
+
+// The tile configurations by id (the same table as scan_lanes... in ssm_internal.h).
+using Tile0 = TileCfg<4>;
+using Tile1 = TileCfg<2>;
+using Tile2 = TileCfg<1>;
+using Tile3 = TileCfg<3>;
 
 template <typename T, int N>
 cudaError_t launch_typed(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
-    switch (p.tile_cfg) {
-        case 0: return launch_cfg<T, N, Tile0>(a, p, s);
-        case 1: return launch_cfg<T, N, Tile1>(a, p, s);
-        case 2: return launch_cfg<T, N, Tile2>(a, p, s);
-        case 3: return launch_cfg<T, N, Tile3>(a, p, s);
-        default: return cudaErrorInvalidValue;
+    if constexpr (N == 16) {
+        switch (p.tile_cfg) {
+            case 0: return launch_cfg<T, N, Tile0>(a, p, s);
+            case 1: return launch_cfg<T, N, Tile1>(a, p, s);
+            case 2: return launch_cfg<T, N, Tile2>(a, p, s);
+            case 3: return launch_cfg<T, N, Tile3>(a, p, s);
+            default: return cudaErrorInvalidValue;
+        }
+    } else {
+        return launch_cfg<T, N, Tile0>(a, p, s);   // small dstate: one configuration
     }
 }
 

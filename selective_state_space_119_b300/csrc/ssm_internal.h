@@ -8,28 +8,19 @@
 
 namespace ssm {
 
-// Scan tiling shared by the planner and the kernels. A CTA has SW "state"
-// warps, which run the recurrence, and RW "row" warps, which stage the inputs,
-// compute dt and write the gated output. NS lanes of a state warp share one
-// channel's N states (each holds N / NS of them), so a state warp covers
-// 32 / NS channels and a CTA SW * 32 / NS channels:
-//   id 0: NS 4, SW 4, RW 2   id 1: NS 8, SW 4, RW 2
-//   id 2: NS 4, SW 2, RW 1   id 3: NS 2, SW 4, RW 2
-// For N < NS the lanes per channel drop to N, and a CTA keeps at most 64
-// channels. Tokens stream through shared memory in stages of kScanStageTokens;
+// Scan tiling shared by the planner and the kernels. Every lane of the scan
+// owns one channel (and, with its partner lane, the states of a channel
+// pair); a CTA has W warps, so it covers 32 * W channels of one batch row and
+// one L-chunk:
+//   id 0: W 4 (128 channels)   id 1: W 2 (64)   id 2: W 1 (32)   id 3: W 3 (96)
+// B_t / C_t rows go through shared memory in stages of kScanStageTokens;
 // L-chunks are a whole number of stages so that only the sequence end is
 // ragged.
 constexpr int kScanStageTokens = 32;
 constexpr int kScanTileConfigs = 4;
-inline int scan_lanes_per_channel(int cfg, int64_t N) {
-    static const int ns[kScanTileConfigs] = {4, 8, 4, 2};
-    return ns[cfg] < N ? ns[cfg] : static_cast<int>(N);
-}
-inline int scan_tile_channels(int cfg, int64_t N) {
-    static const int sw[kScanTileConfigs] = {4, 4, 2, 4};
-    const int cpw = 32 / scan_lanes_per_channel(cfg, N);
-    const int warps = sw[cfg] * cpw <= 64 ? sw[cfg] : (64 / cpw > 0 ? 64 / cpw : 1);
-    return warps * cpw;
+inline int scan_tile_channels(int cfg) {
+    static const int w[kScanTileConfigs] = {4, 2, 1, 3};
+    return 32 * w[cfg];
 }
 
 // Host-side plan of one scan call (pure function of the sizes and hints).
@@ -69,7 +60,7 @@ struct ScanArgs {
     int64_t chunk_len, nchunks, tiles;
     float* ws_H;   // [batch][nchunks-1][dim][N]: chunk-local end states, then carries
     float* ws_S;   // [batch][nchunks-1][dim]: sum of dt over each chunk
-    unsigned int* status;  // workspace status word (sticky; 0 = ok)
+    unsigned int* status;  // workspace status word (sticky; 0 = ok; no current kernel sets it)
 };
 
 struct StepArgs {

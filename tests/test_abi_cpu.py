@@ -50,13 +50,10 @@ def test_workspace_and_plan():
     # several chunks -> header + carries; chunks are whole 32-token stages
     p = L.ssm_scan_plan(2, 1000, 512, 16, "bf16", chunk_len_hint=100)
     assert p["chunk_len"] == 128 and p["nchunks"] == 8 and p["kernels"] == 3
-    # channels per CTA = warps * 32 / (lanes per channel)
-    for cfg, ch in ((1, 32), (2, 16), (3, 16), (4, 64)):
+    # channels per CTA = 32 lanes (one channel each) * warps
+    for cfg, ch in ((1, 128), (2, 64), (3, 32), (4, 96)):
         p = L.ssm_scan_plan(2, 1000, 512, 16, "bf16", tile_config_hint=cfg)
         assert p["tile_config"] == cfg - 1 and p["channels_per_cta"] == ch
-    # dstate 4: at most 4 lanes share a channel
-    p = L.ssm_scan_plan(2, 1000, 512, 4, "bf16", tile_config_hint=2)
-    assert p["tile_config"] == 1 and p["channels_per_cta"] == 32
     with pytest.raises(L.SSMError):
         L.ssm_scan_plan(2, 1000, 512, 16, "bf16", tile_config_hint=5)
     ws = L.ssm_scan_workspace_bytes(2, 1000, 512, 16, "bf16", chunk_len_hint=100)
@@ -66,7 +63,7 @@ def test_workspace_and_plan():
     p = L.ssm_scan_plan(1, 131072, 5120, 16, "bf16")
     assert p["ctas"] >= 148 and p["chunk_len"] % 32 == 0
     # a channel-rich workload needs no L-split
-    p = L.ssm_scan_plan(64, 2048, 2048, 16, "bf16")
+    p = L.ssm_scan_plan(64, 2048, 4096, 16, "bf16")
     assert p["nchunks"] == 1
     # invalid sizes
     assert L.ssm_scan_workspace_bytes(1, 64, 256, 3, "bf16") == 0
