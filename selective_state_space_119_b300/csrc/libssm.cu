@@ -17,14 +17,34 @@ thread_local int g_last_cuda_error = 0;
 
 constexpr int64_t kMaxDim = int64_t(1) << 31;     // per-axis limit
 constexpr int64_t kMaxElems = int64_t(1) << 40;   // batch * seqlen * dim limit
-// Planning. A lane of the scan owns one channel, so the channels alone give
-// batch * dim threads. One warp per SM sub-partition (148 x 4 x 32 threads)
-// keeps the SFU and FMA pipes of every sub-partition fed; the plan splits the
-// sequence into about kTargetThreads / (batch * dim) chunks (rounded to the
-// nearest whole number), since every chunk but the last is scanned twice.
-// Chunks are never shorter than kMinChunk tokens.
-constexpr int64_t kTargetThreads = 148 * 4 * 32;
-constexpr int64_t kMinChunk = 256;
+// Planning. A CTA of the scan covers channels_per_cta channels of one batch
+// row over one L-chunk, and a B300 SM keeps kResidentCtas of them (shared
+// memory bounds it). Splitting the sequence into K chunks multiplies the CTAs
+// by K, which fills more of the 148 SMs, at the price of scanning every chunk
+// but the last twice (the chunk-state pass costs about kStatePassCost of the
+// output pass per token). The plan takes the K of least modelled time:
+//   time ~ chunk_len * (wave_cost(output CTAs) + kStatePassCost * wave_cost(state CTAs))
+// where wave_cost(n) sums, over the waves of n CTAs on 148 SMs, the cost of
+// the busiest SM of the wave: 1 for one CTA, kTwoCtaCost for two (two CTAs
+// share an SM's pipes at better than half speed each), plus kSplitCost for
+// the two extra launches a split needs (one token of a lone CTA takes about
+// 0.1 us; a launch about 3 us). The constants come from timing the bf16
+// N = 16 workloads (chunk counts 1..64) on a B300.
+constexpr int64_t kSms = 148;
+constexpr int64_t kResidentCtas = 2;
+constexpr double kTwoCtaCost = 1.44;
+constexpr double kStatePassCost = 0.7;
+constexpr double kSplitCost = 60.0;
+constexpr int64_t kMinChunk = 128;
+constexpr int64_t kMaxChunks = 256;
+
+double wave_cost(int64_t ctas) {
+    const int64_t per_wave = kSms * kResidentCtas;
+    const int64_t full = ctas / per_wave, rem = ctas % per_wave;
+    double c = double(full) * (kResidentCtas > 1 ? kTwoCtaCost : 1.0);
+    if (rem > 0) c += rem > kSms ? kTwoCtaCost : 1.0;
+    return c;
+}
 
 int set_cuda(cudaError_t e) {
     g_last_cuda_error = static_cast<int>(e);
@@ -73,14 +93,25 @@ int make_plan(const ssm_dims* d, ssm::ScanPlan* p) {
     p->channels_per_cta = ssm::scan_tile_channels(p->tile_cfg);
     p->tiles = (dim + p->channels_per_cta - 1) / p->channels_per_cta;
     const int64_t per_chunk = p->tiles * batch;
-    const int64_t threads = batch * dim;
     int64_t chunk;
     if (d->chunk_len_hint > 0) {
         chunk = d->chunk_len_hint;
     } else {
-        int64_t nck = std::max<int64_t>(1, (kTargetThreads + threads / 2) / threads);
-        nck = std::min(nck, std::max<int64_t>(1, L / kMinChunk));
-        chunk = (L + nck - 1) / nck;
+        // modelled time of every chunk count (see the planning note above)
+        chunk = (L + TS - 1) / TS * TS;
+        double best = double(chunk) * wave_cost(per_chunk);
+        const int64_t kmax = std::min<int64_t>(kMaxChunks, std::max<int64_t>(1, L / kMinChunk));
+        for (int64_t k = 2; k <= kmax; ++k) {
+            const int64_t c = ((L + k - 1) / k + TS - 1) / TS * TS;
+            const int64_t nk = (L + c - 1) / c;
+            const double t = double(c) * (wave_cost(per_chunk * nk) +
+                                          kStatePassCost * wave_cost(per_chunk * (nk - 1))) +
+                             kSplitCost;
+            if (t < best) {
+                best = t;
+                chunk = c;
+            }
+        }
     }
     // whole pipeline stages per chunk, so that only the sequence end is ragged
     chunk = std::max<int64_t>(TS, (chunk + TS - 1) / TS * TS);

@@ -8,10 +8,15 @@
 // y = C . h + D x, out = y * silu(z); the fp32 state is updated in place.
 //
 // The step is bound by HBM traffic on the state (N fp32 read + written per
-// channel). L = N / kNPL lanes share a channel, each holding kNPL = 4 states
+// channel). LANES = N / NPL lanes share a channel, each holding NPL = 4 states
 // (one 128-bit load and store), so a warp reads and writes 512 contiguous
-// bytes of state per instruction. The partial C . h sums meet through
-// butterfly shuffles; lane 0 of each group writes y.
+// bytes of state per instruction; the state is streamed (read once, written
+// once) with evict-first cache hints. A CTA covers one batch row (the grid's
+// y index) and kItems * CH_PER_CTA channels; each thread handles kItems
+// channel groups that lie CH_PER_CTA channels apart, with all their loads
+// issued before any arithmetic, to keep enough bytes in flight per SM. The
+// partial C . h sums meet through butterfly shuffles; lane 0 of each group
+// writes y.
 #include <cuda_bf16.h>
 
 #include "ssm_device.cuh"
@@ -21,6 +26,26 @@ namespace ssm {
 namespace {
 
 constexpr int kStepThreads = 256;
+constexpr int kItems = 2;
+
+// NPL consecutive I/O elements widened to fp32 (NPL <= 4; 8-byte aligned for
+// bf16 x 4 and 16-byte aligned for fp32 x 4).
+template <typename T, int NPL>
+__device__ __forceinline__ void ld_vec(const T* p, float (&v)[NPL]) {
+    if constexpr (NPL == 4 && sizeof(T) == 2) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+        v[0] = __uint_as_float(u.x << 16);
+        v[1] = __uint_as_float(u.x & 0xffff0000u);
+        v[2] = __uint_as_float(u.y << 16);
+        v[3] = __uint_as_float(u.y & 0xffff0000u);
+    } else if constexpr (NPL == 4 && sizeof(T) == 4) {
+        const float4 u = __ldg(reinterpret_cast<const float4*>(p));
+        v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < NPL; ++j) v[j] = IO<T>::ld(p + j);
+    }
+}
 
 template <typename T, int N>
 __global__ void __launch_bounds__(kStepThreads) state_update_kernel(const StepArgs a) {
@@ -29,60 +54,81 @@ __global__ void __launch_bounds__(kStepThreads) state_update_kernel(const StepAr
     constexpr int CH_PER_CTA = kStepThreads / LANES;
 
     const int lane_in_ch = threadIdx.x % LANES;
-    const int64_t ch = static_cast<int64_t>(blockIdx.x) * CH_PER_CTA + threadIdx.x / LANES;
-    const int64_t nch = a.batch * a.dim;
-    // Whole groups of LANES lanes share the same `ch`, so the shuffle below
-    // always runs with every participant present.
-    const bool active = ch < nch;
-    const int64_t b = active ? ch / a.dim : 0;
-    const int64_t d = active ? ch % a.dim : 0;
     const int n0 = lane_in_ch * NPL;
-
+    const int64_t b = blockIdx.y;              // batch row (2-D grid: no index division)
     const T* __restrict__ x = static_cast<const T*>(a.x);
     const T* __restrict__ delta = static_cast<const T*>(a.delta);
     const T* __restrict__ Bg = static_cast<const T*>(a.B);
     const T* __restrict__ Cg = static_cast<const T*>(a.C);
     const T* __restrict__ z = static_cast<const T*>(a.z);
 
-    float y = 0.f, xv = 0.f;
-    if (active) {
-        xv = IO<T>::ld(x + ch);
-        float dt = IO<T>::ld(delta + ch);
-        if (a.delta_bias) dt += __ldg(a.delta_bias + d);
-        if (a.softplus) dt = softplus(dt);
-        const float dtx = dt * xv;
-
-        float h[NPL], A2[NPL];
-        float* st = a.state + ch * N + n0;
+    // ---- loads of every item first ----
+    int64_t ch[kItems];
+    bool active[kItems];
+    float xv[kItems], dt[kItems], zv[kItems], h[kItems][NPL], A2[kItems][NPL], Bv[kItems][NPL],
+        Cv[kItems][NPL];
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+        // Whole groups of LANES lanes share the same channel, so the shuffles
+        // below always run with every participant present.
+        const int64_t dd = (static_cast<int64_t>(blockIdx.x) * kItems + it) * CH_PER_CTA +
+                           threadIdx.x / LANES;
+        active[it] = dd < a.dim;
+        const int64_t d = active[it] ? dd : 0;
+        ch[it] = b * a.dim + d;
+        const int64_t c = ch[it];
+        xv[it] = IO<T>::ld(x + c);
+        dt[it] = IO<T>::ld(delta + c);
+        zv[it] = z ? IO<T>::ld(z + c) : 0.f;
+        const float* st = a.state + c * N + n0;
         if constexpr (NPL == 4) {
-            const float4 hv = *reinterpret_cast<const float4*>(st);
-            h[0] = hv.x; h[1] = hv.y; h[2] = hv.z; h[3] = hv.w;
+            const float4 hv = __ldcs(reinterpret_cast<const float4*>(st));
+            h[it][0] = hv.x; h[it][1] = hv.y; h[it][2] = hv.z; h[it][3] = hv.w;
             const float4 av = __ldg(reinterpret_cast<const float4*>(a.A + d * N + n0));
-            A2[0] = av.x; A2[1] = av.y; A2[2] = av.z; A2[3] = av.w;
+            A2[it][0] = av.x; A2[it][1] = av.y; A2[it][2] = av.z; A2[it][3] = av.w;
         } else {
 #pragma unroll
-            for (int j = 0; j < NPL; ++j) { h[j] = st[j]; A2[j] = __ldg(a.A + d * N + n0 + j); }
+            for (int j = 0; j < NPL; ++j) {
+                h[it][j] = __ldcs(st + j);
+                A2[it][j] = __ldg(a.A + d * N + n0 + j);
+            }
         }
+        ld_vec<T, NPL>(Bg + b * N + n0, Bv[it]);
+        ld_vec<T, NPL>(Cg + b * N + n0, Cv[it]);
+        if (a.delta_bias) dt[it] += __ldg(a.delta_bias + d);
+    }
+
+    // ---- arithmetic and stores ----
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+        const int64_t c = ch[it];
+        const int64_t d = c - b * a.dim;
+        float dtv = dt[it];
+        if (a.softplus) dtv = softplus(dtv);
+        const float dtx = dtv * xv[it];
+        float y = 0.f;
 #pragma unroll
         for (int j = 0; j < NPL; ++j) {
-            const float Bn = IO<T>::ld(Bg + b * N + n0 + j);
-            const float Cn = IO<T>::ld(Cg + b * N + n0 + j);
-            h[j] = fmaf(ex2(dt * (A2[j] * kLog2e)), h[j], dtx * Bn);
-            y = fmaf(Cn, h[j], y);
+            h[it][j] = fmaf(ex2(dtv * (A2[it][j] * kLog2e)), h[it][j], dtx * Bv[it][j]);
+            y = fmaf(Cv[it][j], h[it][j], y);
         }
-        if constexpr (NPL == 4) {
-            *reinterpret_cast<float4*>(st) = make_float4(h[0], h[1], h[2], h[3]);
-        } else {
+        if (active[it]) {
+            float* st = a.state + c * N + n0;
+            if constexpr (NPL == 4) {
+                __stcs(reinterpret_cast<float4*>(st),
+                       make_float4(h[it][0], h[it][1], h[it][2], h[it][3]));
+            } else {
 #pragma unroll
-            for (int j = 0; j < NPL; ++j) st[j] = h[j];
+                for (int j = 0; j < NPL; ++j) __stcs(st + j, h[it][j]);
+            }
         }
-    }
 #pragma unroll
-    for (int off = 1; off < LANES; off <<= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
-    if (active && lane_in_ch == 0) {
-        if (a.D) y = fmaf(__ldg(a.D + d), xv, y);
-        if (z) y *= silu(IO<T>::ld(z + ch));
-        IO<T>::st(static_cast<T*>(a.out) + ch, y);
+        for (int off = 1; off < LANES; off <<= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
+        if (active[it] && lane_in_ch == 0) {
+            if (a.D) y = fmaf(__ldg(a.D + d), xv[it], y);
+            if (z) y *= silu(zv[it]);
+            IO<T>::st(static_cast<T*>(a.out) + c, y);
+        }
     }
 }
 
@@ -90,9 +136,24 @@ template <typename T, int N>
 cudaError_t launch_typed(const StepArgs& a, cudaStream_t s) {
     constexpr int NPL = N >= 4 ? 4 : N;
     constexpr int CH_PER_CTA = kStepThreads / (N / NPL);
-    const int64_t nch = a.batch * a.dim;
-    const int64_t grid = (nch + CH_PER_CTA - 1) / CH_PER_CTA;
-    state_update_kernel<T, N><<<static_cast<unsigned>(grid), kStepThreads, 0, s>>>(a);
+    constexpr int64_t kMaxGridY = 65535;
+    const int64_t per_cta = int64_t(CH_PER_CTA) * kItems;
+    // batch rows go on the grid's y axis, in slices of at most 65535 rows
+    for (int64_t b0 = 0; b0 < a.batch; b0 += kMaxGridY) {
+        StepArgs p = a;
+        p.batch = a.batch - b0 < kMaxGridY ? a.batch - b0 : kMaxGridY;
+        const int64_t e = b0 * a.dim;      // elements before the slice
+        p.state = a.state + e * N;
+        p.x = static_cast<const T*>(a.x) + e;
+        p.delta = static_cast<const T*>(a.delta) + e;
+        p.z = a.z ? static_cast<const T*>(a.z) + e : nullptr;
+        p.out = static_cast<T*>(a.out) + e;
+        p.B = static_cast<const T*>(a.B) + b0 * N;
+        p.C = static_cast<const T*>(a.C) + b0 * N;
+        const dim3 grid(static_cast<unsigned>((a.dim + per_cta - 1) / per_cta),
+                        static_cast<unsigned>(p.batch));
+        state_update_kernel<T, N><<<grid, kStepThreads, 0, s>>>(p);
+    }
     return cudaGetLastError();
 }
 
