@@ -119,6 +119,27 @@ int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A,
                            ssm_stream_t stream);
 
 /*
+ * ssm_selective_scan_fwd_from_state -- the same scan started from a given
+ * state instead of zero, so that a sequence can be continued: prefill a prompt
+ * in several pieces, or hand a generation state back to the scan. The pages
+ * write the recurrence from an arbitrary h_{t-1} ("State-space models (Mamba,
+ * S4)", "Worked Example: 2D SSM Step" starts from h_0 != 0; "Training vs
+ * Inference Modes" keeps h between tokens); the scan above is this call with
+ * h0 = 0.
+ *
+ *   h0 : [batch, dim, dstate] fp32, the state before the first token; read
+ *        only, must not overlap out or final_state (SSM_ERR_ALIAS)
+ * Every other argument is as for ssm_selective_scan_fwd. seqlen == 0 copies
+ * h0 to final_state. h0 == NULL with a non-empty problem is SSM_ERR_NULL.
+ */
+int ssm_selective_scan_fwd_from_state(const void* x, const void* delta, const float* A,
+                                      const void* B, const void* C, const float* D,
+                                      const void* z, const float* delta_bias,
+                                      int delta_softplus, const float* h0, void* out,
+                                      float* final_state, const ssm_dims* dims,
+                                      ssm_stream_t stream);
+
+/*
  * ssm_state_update -- one token of recurrent generation on a cached state
  * ("State-space models (Mamba, S4)", "Training vs Inference Modes"). Exactly
  * one step of the scan above, with the state updated in place:

@@ -27,14 +27,14 @@ constexpr int64_t kMaxElems = int64_t(1) << 40;   // batch * seqlen * dim limit
 // where wave_cost(n) sums, over the waves of n CTAs on 148 SMs, the cost of
 // the busiest SM of the wave: 1 for one CTA, kTwoCtaCost for two (two CTAs
 // share an SM's pipes at better than half speed each), plus kSplitCost for
-// the two extra launches a split needs (one token of a lone CTA takes about
-// 0.1 us; a launch about 3 us). The constants come from timing the bf16
+// the extra launch a split needs (one token of a lone CTA takes about 0.1 us;
+// a launch about 3 us). The constants come from timing the bf16
 // N = 16 workloads (chunk counts 1..64) on a B300.
 constexpr int64_t kSms = 148;
 constexpr int64_t kResidentCtas = 2;
 constexpr double kTwoCtaCost = 1.44;
 constexpr double kStatePassCost = 0.7;
-constexpr double kSplitCost = 60.0;
+constexpr double kSplitCost = 30.0;
 constexpr int64_t kMinChunk = 128;
 constexpr int64_t kMaxChunks = 256;
 
@@ -120,7 +120,7 @@ int make_plan(const ssm_dims* d, ssm::ScanPlan* p) {
     p->nchunks = (L + chunk - 1) / chunk;
     p->ctas = per_chunk * p->nchunks;
     if (p->ctas >= (int64_t(1) << 31)) return SSM_ERR_DIMS;
-    p->kernels = p->nchunks > 1 ? 3 : 1;
+    p->kernels = p->nchunks > 1 ? 2 : 1;
     // header (status word) always; chunk carries when the sequence is split
     p->ws_bytes = ssm::kWsHeaderBytes;
     if (p->nchunks > 1) {
@@ -208,24 +208,34 @@ size_t ssm_scan_workspace_bytes(const ssm_dims* dims) {
     return p.ws_bytes;
 }
 
-int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, const void* B,
-                           const void* C, const float* D, const void* z,
-                           const float* delta_bias, int delta_softplus, void* out,
-                           float* final_state, const ssm_dims* dims, ssm_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The scan behind both scan entry points; h0 (state before the first token)
+// may be NULL for h = 0.
+int scan_impl(const void* x, const void* delta, const float* A, const void* B, const void* C,
+              const float* D, const void* z, const float* delta_bias, int delta_softplus,
+              const float* h0, void* out, float* final_state, const ssm_dims* dims,
+              ssm_stream_t stream) {
     int rc = check_dims(dims, true);
     if (rc != SSM_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // Empty problems: nothing to read (empty tensors may carry NULL pointers).
     if (dims->batch == 0 || dims->dim == 0) return SSM_OK;
+    const size_t state_bytes = size_t(dims->batch) * dims->dim * dims->dstate * 4;
     if (dims->seqlen == 0) {
+        // no token: the final state is the initial state
         if (!final_state) return SSM_OK;
-        if (!aligned16(final_state)) return SSM_ERR_ALIGN;
-        return set_cuda(cudaMemsetAsync(
-            final_state, 0, size_t(dims->batch) * dims->dim * dims->dstate * 4, s));
+        if (!aligned16(final_state) || (h0 && !aligned16(h0))) return SSM_ERR_ALIGN;
+        if (h0 && overlap({h0, state_bytes}, {final_state, state_bytes})) return SSM_ERR_ALIAS;
+        return set_cuda(h0 ? cudaMemcpyAsync(final_state, h0, state_bytes,
+                                             cudaMemcpyDeviceToDevice, s)
+                           : cudaMemsetAsync(final_state, 0, state_bytes, s));
     }
     if (!x || !delta || !A || !B || !C || !out) return SSM_ERR_NULL;
     {
-        const void* const ptrs[] = {x, delta, A, B, C, D, z, delta_bias, out, final_state,
+        const void* const ptrs[] = {x, delta, A, B, C, D, z, delta_bias, h0, out, final_state,
                                     dims->workspace};
         rc = check_aligned(ptrs);
         if (rc != SSM_OK) return rc;
@@ -245,7 +255,7 @@ int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, con
                             {z, elems * es},      {B, rows * es},
                             {C, rows * es},       {A, size_t(dim) * N * 4},
                             {D, size_t(dim) * 4}, {delta_bias, size_t(dim) * 4},
-                            {dims->workspace, p.ws_bytes}};
+                            {h0, state_bytes},    {dims->workspace, p.ws_bytes}};
         const Range outs[] = {{out, elems * es},
                               {final_state, size_t(batch) * dim * N * 4}};
         rc = check_alias(in, outs);
@@ -255,6 +265,7 @@ int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, con
     ssm::ScanArgs a{};
     a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
     a.delta_bias = delta_bias; a.softplus = delta_softplus ? 1 : 0;
+    a.h0 = h0;
     a.out = out; a.final_state = final_state;
     a.batch = batch; a.L = L; a.dim = dim;
     a.chunk_len = p.chunk_len; a.nchunks = p.nchunks; a.tiles = p.tiles;
@@ -265,6 +276,29 @@ int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, con
         a.ws_S = reinterpret_cast<float*>(ws + p.ws_off_S);
     }
     return set_cuda(ssm::launch_scan(a, p, dims->io_dtype, static_cast<int>(N), s));
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z,
+                           const float* delta_bias, int delta_softplus, void* out,
+                           float* final_state, const ssm_dims* dims, ssm_stream_t stream) {
+    return scan_impl(x, delta, A, B, C, D, z, delta_bias, delta_softplus, nullptr, out,
+                     final_state, dims, stream);
+}
+
+int ssm_selective_scan_fwd_from_state(const void* x, const void* delta, const float* A,
+                                      const void* B, const void* C, const float* D,
+                                      const void* z, const float* delta_bias,
+                                      int delta_softplus, const float* h0, void* out,
+                                      float* final_state, const ssm_dims* dims,
+                                      ssm_stream_t stream) {
+    if (!h0 && dims && dims->batch > 0 && dims->dim > 0) return SSM_ERR_NULL;
+    return scan_impl(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, out,
+                     final_state, dims, stream);
 }
 
 int ssm_state_update(float* state, const void* x, const void* delta, const float* A,

@@ -14,14 +14,16 @@
 // scan ("State Space Models -- Mamba, S4, and Beyond", "Hardware-Efficient
 // Scan (for Training)"; "State-space models (Mamba, S4)", "Training vs
 // Inference Modes"). For a chunk P = prod_t exp(dt_t A) = exp(A sum_t dt_t), so
-// only the sum of dt is kept. When a sequence is split, three stream-ordered
-// phases run (no CTA ever waits for another CTA):
+// only the sum of dt is kept. When a sequence is split, two stream-ordered
+// passes run (no CTA ever waits for another CTA):
 //   1. chunk state : every chunk but the last runs from h = 0 and stores its
 //                    end state H and S = sum(dt)            (MODE 0)
-//   2. carry       : per (b, d, n), h_in(k+1) = exp(A S_k) h_in(k) + H_k
-//   3. output      : every chunk runs from its entering state, writes y; the
-//                    last chunk writes final_state           (MODE 1)
-// An unsplit sequence runs phase 3 alone.
+//   2. output      : chunk k starts from the initial state (zero, or h0)
+//                    and composes the maps of chunks 0 .. k-1,
+//                    h_in = exp(A S_i) h_in + H_i in order, then runs from
+//                    h_in and writes y; the last chunk writes final_state
+//                    (MODE 1)
+// An unsplit sequence runs pass 2 alone.
 //
 // Work layout. The data movement that bounds this scan on B300 is the
 // broadcast of B_t and C_t (shared by every channel) from shared memory into
@@ -260,10 +262,22 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             A2[r][q] = ch_ok ? __ldg(a.A + dr * N + j * SPL + q) * kLog2e : 0.f;
             h[r][q] = 0.f;
         }
-        if (MODE == 1 && k > 0 && ch_ok) {
-            const float* hin = a.ws_H + ((b * (a.nchunks - 1) + (k - 1)) * a.dim + dr) * N + j * SPL;
+        // The state entering chunk k composes the maps of chunks 0 .. k-1 in
+        // order: h <- exp(A S_i) h + H_i (S_i = sum of dt over chunk i, H_i its
+        // end state from 0, both stored by the chunk-state pass).
+        if (MODE == 1 && a.h0 && ch_ok) {
+            const float* hs = a.h0 + (b * a.dim + dr) * N + j * SPL;
 #pragma unroll
-            for (int q = 0; q < SPL; ++q) h[r][q] = hin[q];
+            for (int q = 0; q < SPL; ++q) h[r][q] = hs[q];
+        }
+        if (MODE == 1 && k > 0 && ch_ok) {
+            for (int64_t i = 0; i < k; ++i) {
+                const int64_t idx = (b * (a.nchunks - 1) + i) * a.dim + dr;
+                const float S = a.ws_S[idx];
+                const float* Hi = a.ws_H + idx * N + j * SPL;
+#pragma unroll
+                for (int q = 0; q < SPL; ++q) h[r][q] = fmaf(ex2(A2[r][q] * S), h[r][q], Hi[q]);
+            }
         }
     }
     const float bias = (a.delta_bias && ch_ok) ? __ldg(a.delta_bias + dsafe) : 0.f;
@@ -420,24 +434,6 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     }
 }
 
-// Phase 2: one thread per (b, d, n). h_in(0) = 0 and
-// h_in(k+1) = exp(A S_k) h_in(k) + H_k, written over H_k.
-template <int N>
-__global__ void __launch_bounds__(256) scan_carry_kernel(const ScanArgs a) {
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i >= a.batch * a.dim * N) return;
-    const int64_t n = i % N;
-    const int64_t d = (i / N) % a.dim;
-    const int64_t b = i / (N * a.dim);
-    const float A2 = __ldg(a.A + d * N + n) * kLog2e;
-    float h = 0.f;
-    for (int64_t k = 0; k + 1 < a.nchunks; ++k) {
-        const int64_t idx = (b * (a.nchunks - 1) + k) * a.dim + d;
-        h = fmaf(ex2(A2 * a.ws_S[idx]), h, a.ws_H[idx * N + n]);
-        a.ws_H[idx * N + n] = h;
-    }
-}
-
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -523,8 +519,6 @@ cudaError_t launch_flags(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
         scan_kernel<T, N, TC, 0, SOFTPLUS, false>
             <<<static_cast<unsigned>(per_chunk * (p.nchunks - 1)), Cf::THREADS,
                Smem<T, N, TC, 0>::kBytes, s>>>(tx, tdt, tz, tB, tC, tout, a);
-        const int64_t n = a.batch * a.dim * N;
-        scan_carry_kernel<N><<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(a);
     }
     if ((e = allow_smem<T, N, TC, 1, SOFTPLUS, GATE>()) != cudaSuccess) return e;
     scan_kernel<T, N, TC, 1, SOFTPLUS, GATE>

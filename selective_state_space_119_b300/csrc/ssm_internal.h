@@ -58,7 +58,8 @@ struct ScanArgs {
     float* final_state;
     int64_t batch, L, dim;
     int64_t chunk_len, nchunks, tiles;
-    float* ws_H;   // [batch][nchunks-1][dim][N]: chunk-local end states, then carries
+    const float* h0;  // [batch][dim][N] state before the first token, or NULL (zero)
+    float* ws_H;   // [batch][nchunks-1][dim][N]: chunk-local end states (from h = 0)
     float* ws_S;   // [batch][nchunks-1][dim]: sum of dt over each chunk
     unsigned int* status;  // workspace status word (sticky; 0 = ok; no current kernel sets it)
 };

@@ -41,7 +41,7 @@ SSM_ERR_ALIAS = -8
 # Every symbol include/ssm.h declares.
 EXPORTED = ("ssm_selective_scan_fwd", "ssm_state_update", "ssm_scan_workspace_bytes",
             "ssm_scan_plan", "ssm_get_device_status", "ssm_strerror", "ssm_last_cuda_error",
-            "ssm_version", "ssm_selective_scan_fwd_static")
+            "ssm_version", "ssm_selective_scan_fwd_static", "ssm_selective_scan_fwd_from_state")
 
 # Size of the library-owned scratch of ssm_selective_scan_fwd_static (include/ssm.h).
 SSM_STATIC_SCRATCH_BYTES = 16 << 20
@@ -66,6 +66,9 @@ _dims_p = ctypes.POINTER(ssm_dims)
 lib.ssm_selective_scan_fwd.restype = ctypes.c_int
 lib.ssm_selective_scan_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
                                        _vp, _vp, _dims_p, _vp]
+lib.ssm_selective_scan_fwd_from_state.restype = ctypes.c_int
+lib.ssm_selective_scan_fwd_from_state.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                                  ctypes.c_int, _vp, _vp, _vp, _dims_p, _vp]
 lib.ssm_selective_scan_fwd_static.restype = ctypes.c_int
 lib.ssm_selective_scan_fwd_static.argtypes = list(lib.ssm_selective_scan_fwd.argtypes)
 lib.ssm_state_update.restype = ctypes.c_int
@@ -176,13 +179,15 @@ def alloc_workspace(batch, seqlen, dim, dstate, io, device, chunk_len_hint=0, ti
 def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
                            delta_softplus=False, out=None, final_state=None,
                            return_final_state=True, workspace=None, chunk_len_hint=0,
-                           tile_config_hint=0, stream=None) -> Tuple[object, Optional[object]]:
+                           tile_config_hint=0, stream=None, h0=None) -> Tuple[object, Optional[object]]:
     """Selective scan over x [batch, L, dim] (see include/ssm.h).
 
     Returns (out, final_state); final_state is None when not requested.
     ``out`` / ``final_state`` may be passed preallocated; ``workspace`` is a
     zero-initialised uint8 CUDA tensor of at least ssm_scan_workspace_bytes
-    (allocated per call when omitted).
+    (allocated per call when omitted). ``h0`` ([batch, dim, N] fp32), when
+    given, is the state before the first token
+    (ssm_selective_scan_fwd_from_state); otherwise the scan starts from zero.
     """
     torch = _torch()
     batch, L, dim = x.shape
@@ -214,8 +219,13 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
         _ptr(final_state, "final_state", torch.float32, (batch, dim, N), dev),
     )
     with torch.cuda.device(dev):
-        rc = lib.ssm_selective_scan_fwd(*args, ctypes.byref(dims), _stream(dev, stream))
-    _check(rc, "ssm_selective_scan_fwd")
+        if h0 is None:
+            rc = lib.ssm_selective_scan_fwd(*args, ctypes.byref(dims), _stream(dev, stream))
+        else:
+            h0p = _ptr(h0, "h0", torch.float32, (batch, dim, N), dev)
+            rc = lib.ssm_selective_scan_fwd_from_state(*args[:9], h0p, *args[9:],
+                                                       ctypes.byref(dims), _stream(dev, stream))
+    _check(rc, "ssm_selective_scan_fwd" if h0 is None else "ssm_selective_scan_fwd_from_state")
     return out, final_state
 
 

@@ -49,7 +49,7 @@ def test_workspace_and_plan():
     assert p["nchunks"] == 1 and p["kernels"] == 1
     # several chunks -> header + carries; chunks are whole 32-token stages
     p = L.ssm_scan_plan(2, 1000, 512, 16, "bf16", chunk_len_hint=100)
-    assert p["chunk_len"] == 128 and p["nchunks"] == 8 and p["kernels"] == 3
+    assert p["chunk_len"] == 128 and p["nchunks"] == 8 and p["kernels"] == 2
     # channels per CTA = 32 lanes (one channel each) * warps
     for cfg, ch in ((1, 128), (2, 64), (3, 32), (4, 96)):
         p = L.ssm_scan_plan(2, 1000, 512, 16, "bf16", tile_config_hint=cfg)
@@ -139,3 +139,16 @@ def test_binding_refuses_cpu_tensors():
         L.ssm_selective_scan_fwd(x, x, A, torch.zeros(1, 4, 16, dtype=torch.bfloat16),
                                  torch.zeros(1, 4, 16, dtype=torch.bfloat16),
                                  out=torch.empty_like(x), return_final_state=False)
+
+
+def test_from_state_rejects_bad_arguments_before_launch():
+    f = L.lib.ssm_selective_scan_fwd_from_state
+    d = L.make_dims(1, 4, 8, 16, "bf16", workspace=FAKE + (1 << 34), workspace_bytes=1 << 20)
+
+    def call(h0=FAKE + (1 << 31), fs=None, dims=d):
+        return f(FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288, FAKE + 16384, None, None, None, 0,
+                 h0, FAKE + (1 << 30), fs, ctypes.byref(dims), None)
+
+    assert call(h0=None) == L.SSM_ERR_NULL                     # the state is required
+    assert call(h0=FAKE + (1 << 31) + 4) == L.SSM_ERR_ALIGN
+    assert call(fs=FAKE + (1 << 31)) == L.SSM_ERR_ALIAS         # final state over h0
