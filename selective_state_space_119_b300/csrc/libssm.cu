@@ -35,7 +35,7 @@ constexpr int64_t kResidentCtas = 2;
 constexpr double kTwoCtaCost = 1.44;
 constexpr double kStatePassCost = 0.7;
 constexpr double kSplitCost = 30.0;
-constexpr int64_t kMinChunk = 128;
+constexpr int64_t kMinChunk = 256;
 constexpr int64_t kMaxChunks = 256;
 
 double wave_cost(int64_t ctas) {
