@@ -150,8 +150,7 @@ template <int SPL, bool READOUT>
 __device__ __forceinline__ float state_step(float dt, float dtx, const float* __restrict__ bc,
                                             const float (&A2)[SPL], float (&h)[SPL]) {
     if constexpr (SPL % 2 == 0) {
-        // two accumulators halve the dependent chain of the readout
-        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        float2 acc = make_float2(0.f, 0.f);
         const float2 dt2 = make_float2(dt, dt), dtx2 = make_float2(dtx, dtx);
 #pragma unroll
         for (int q = 0; q < SPL; q += 2) {
@@ -162,11 +161,9 @@ __device__ __forceinline__ float state_step(float dt, float dtx, const float* __
             h[q] = hn.x;
             h[q + 1] = hn.y;
             if constexpr (READOUT)
-                acc[(q / 2) & 1] =
-                    __ffma2_rn(make_float2(bc[SPL + q], bc[SPL + q + 1]), hn, acc[(q / 2) & 1]);
+                acc = __ffma2_rn(make_float2(bc[SPL + q], bc[SPL + q + 1]), hn, acc);
         }
-        const float2 sum = make_float2(acc[0].x + acc[1].x, acc[0].y + acc[1].y);
-        return sum.x + sum.y;
+        return acc.x + acc.y;
     } else {
         float acc = 0.f;
 #pragma unroll
@@ -340,12 +337,13 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         struct Tok {
             float dt[NS], dtx[NS], x;
         };
+        const int lim = static_cast<int>(t_end - t0 < TS ? t_end - t0 : TS);  // valid tokens
         auto prep = [&](int tl) {
             Tok k;
             k.x = lds_elem(xt + tl * DT + col);
             float dt = lds_elem(dlt + tl * DT + col) + bias;
             if constexpr (SOFTPLUS) dt = softplus(dt);
-            dt = t0 + tl < t_end ? dt : 0.f;
+            dt = tl < lim ? dt : 0.f;
             k.dt[0] = dt;
             k.dtx[0] = dt * k.x;
             if constexpr (NS == 2) {
