@@ -70,6 +70,8 @@ def _bind(lib):
     lib.oracle_state_update.restype = ctypes.c_int
     lib.oracle_state_update.argtypes = (
         [_i64] * 3 + [_dp] * 9 + [ctypes.c_int] + [_dp])
+    lib.oracle_causal_conv1d_silu.restype = None
+    lib.oracle_causal_conv1d_silu.argtypes = [_i64] * 4 + [_dp] * 4
     return lib
 
 
@@ -167,6 +169,23 @@ class Oracle:
         return out, st
 
 
+def _conv_method(self, x, w, bias=None):
+    """Causal depthwise conv1d + SiLU. x: [batch, L, dim]; w: [dim, K];
+    bias: [dim] or None. Returns u [batch, L, dim] float64."""
+    x = _f64(x)
+    batch, L, dim = x.shape
+    w = _f64(w)
+    K = w.shape[1]
+    w = _f64(w, (dim, K))
+    bias = _f64(bias, (dim,))
+    u = np.zeros((batch, L, dim), dtype=np.float64)
+    self._lib.oracle_causal_conv1d_silu(batch, L, dim, K, _ptr(x), _ptr(w), _ptr(bias), _ptr(u))
+    return u
+
+
+Oracle.causal_conv1d_silu = _conv_method
+
+
 def default() -> Oracle:
     """The oracle built from ssm_oracle.c (compiled on first use)."""
     global _default
@@ -194,3 +213,7 @@ def selective_scan(*a, **k):
 
 def state_update(*a, **k):
     return default().state_update(*a, **k)
+
+
+def causal_conv1d_silu(*a, **k):
+    return default().causal_conv1d_silu(*a, **k)

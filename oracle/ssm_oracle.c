@@ -201,3 +201,30 @@ int oracle_state_update(int64_t batch, int64_t dim, int64_t N, double* state,
     }
     return 0;
 }
+
+/*
+ * Causal depthwise 1-D convolution followed by SiLU: the input stage of the
+ * Mamba block ("State Space Models -- Mamba, S4, and Beyond", section "Mamba
+ * (S6 -- Selective State Space)", MambaBlock: nn.Conv1d with kernel_size =
+ * d_conv, padding = d_conv - 1, groups = d_inner, the output cut to seq_len,
+ * then silu; "State-space models (Mamba, S4)", the block diagram's
+ * "Conv1D + SiLU"). Conv1d is a cross-correlation over the left-padded input,
+ * so for every batch row b, channel d and token t:
+ *   pre[t] = bias[d] + sum_{k=0..K-1} w[d,k] * x[t - (K-1) + k]   (x = 0 before t = 0)
+ *   u[t]   = silu(pre[t])
+ * Layouts: x, u [batch, L, dim]; w [dim, K]; bias [dim] or NULL (zero).
+ */
+void oracle_causal_conv1d_silu(int64_t batch, int64_t L, int64_t dim, int64_t K,
+                               const double* x, const double* w, const double* bias, double* u)
+{
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t t = 0; t < L; ++t)
+            for (int64_t d = 0; d < dim; ++d) {
+                double pre = bias ? bias[d] : 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    const int64_t s = t - (K - 1) + k;
+                    if (s >= 0) pre += w[d * K + k] * x[(b * L + s) * dim + d];
+                }
+                u[(b * L + t) * dim + d] = oracle_silu(pre);
+            }
+}

@@ -328,7 +328,72 @@ def pin_thread_invariance(orc, seed=19):
     assert np.array_equal(y1, y8) and np.array_equal(h1, h8)
 
 
+def _conv_case(r, K, batch=2, L=40, dim=5):
+    x = r.standard_normal((batch, L, dim))
+    w = r.standard_normal((dim, K))
+    bias = r.standard_normal(dim)
+    return x, w, bias
+
+
+def _silu(v):
+    return v * expit(v)
+
+
+def pin_conv_library(orc, seed=21):
+    """Causal depthwise conv1d + SiLU ("State Space Models -- Mamba, S4, and
+    Beyond", MambaBlock: nn.Conv1d(kernel_size=d_conv, padding=d_conv - 1,
+    groups=d_inner) cut to seq_len, then silu): the pre-activation of channel d
+    is numpy's full convolution of x[:, d] with the reversed kernel (Conv1d is
+    a cross-correlation), truncated to the first L outputs, plus the bias."""
+    r = _rng(seed)
+    for K in (1, 2, 3, 4):
+        x, w, bias = _conv_case(r, K)
+        got = orc.causal_conv1d_silu(x, w, bias)
+        batch, L, dim = x.shape
+        for b in range(batch):
+            for d in range(dim):
+                pre = np.convolve(x[b, :, d], w[d, ::-1])[:L] + bias[d]
+                _close(got[b, :, d], _silu(pre), 1e-13, 1e-14, "conv K=%d b=%d d=%d" % (K, b, d))
+
+
+def pin_conv_taps(orc, seed=22):
+    """Single-tap kernels: the last tap is the identity (u = silu(x + bias));
+    the first tap of a width-4 kernel delays by three tokens, with zeros
+    (silu(bias)) before the sequence start -- the causal left padding."""
+    r = _rng(seed)
+    x, _, bias = _conv_case(r, 4)
+    w = np.zeros((x.shape[2], 4))
+    w[:, 3] = 1.0
+    _close(orc.causal_conv1d_silu(x, w, bias), _silu(x + bias), 1e-15, 1e-15, "identity tap")
+    w = np.zeros((x.shape[2], 4))
+    w[:, 0] = 1.0
+    want = np.empty_like(x)
+    want[:, :3] = _silu(bias)
+    want[:, 3:] = _silu(x[:, :-3] + bias)
+    _close(orc.causal_conv1d_silu(x, w, bias), want, 1e-15, 1e-15, "delay tap")
+    nob = np.zeros_like(x)                  # no bias: silu(0) = 0 before the start
+    nob[:, 3:] = _silu(x[:, :-3])
+    _close(orc.causal_conv1d_silu(x, w), nob, 1e-15, 1e-15, "delay tap, no bias")
+
+
+def pin_conv_causal(orc, seed=23):
+    """Changing x at token t0 changes no output before t0 and, for a width-K
+    kernel, none after t0 + K - 1."""
+    r = _rng(seed)
+    x, w, bias = _conv_case(r, 4, batch=1, L=30, dim=3)
+    base = orc.causal_conv1d_silu(x, w, bias)
+    x2 = x.copy()
+    x2[0, 12] += 1.0
+    moved = orc.causal_conv1d_silu(x2, w, bias)
+    assert np.array_equal(moved[0, :12], base[0, :12]), "conv reads the future"
+    assert np.array_equal(moved[0, 16:], base[0, 16:]), "conv reaches beyond its width"
+    assert np.all(moved[0, 12:16] != base[0, 12:16]), "conv misses a tap"
+
+
 ALL_PINS = [
+    pin_conv_library,
+    pin_conv_taps,
+    pin_conv_causal,
     pin_worked_example_core,
     pin_worked_example_selective_path,
     pin_lti_convolution,

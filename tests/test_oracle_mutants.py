@@ -46,6 +46,12 @@ MUTANTS = [
     ("core_recurrence_drops_state", "h[n] = Abar[t * N + n] * h[n] + Bbar[t * N + n] * x[t];",
      "h[n] = Abar[t * N + n] + Bbar[t * N + n] * x[t];"),
     ("core_readout_drops_C", "acc += C[t * N + n] * h[n];", "acc += h[n];"),
+    ("conv_kernel_flipped", "pre += w[d * K + k] * x[(b * L + s) * dim + d];",
+     "pre += w[d * K + (K - 1 - k)] * x[(b * L + s) * dim + d];"),
+    ("conv_shift_off_by_one", "const int64_t s = t - (K - 1) + k;", "const int64_t s = t - K + k;"),
+    ("conv_drops_bias", "double pre = bias ? bias[d] : 0.0;", "double pre = 0.0;"),
+    ("conv_without_silu", "u[(b * L + t) * dim + d] = oracle_silu(pre);",
+     "u[(b * L + t) * dim + d] = pre;"),
 ]
 
 
