@@ -17,6 +17,8 @@ bias), gate), i.e. every step of the scan path. Rank 0 prints one JSON line.
   measured HBM copy bandwidth of this GPU model.
 * decode: the recurrent step ssm_state_update on the decode workload (batch
   256, dim 5120, N 16), rotating over several cached states.
+* input_stage: the causal conv1d + SiLU (width 4) alone, fused in front of
+  the scan, and as two calls (conv, then the scan on its output).
 * cpu_baseline: the float64 CPU oracle timed on this host (rank 0, N = 1).
 
 N > 1 (torchrun): every rank runs its own replica of the workload on its own
@@ -336,6 +338,8 @@ def bench_scan(args, rank, world, local):
     torch.cuda.empty_cache()
     if not args.no_decode:
         res["decode"] = bench_decode(args, dev, stream)
+    if not args.no_input_stage:
+        res["input_stage"] = bench_input_stage(args, spec, dev, stream)
     return res, spec
 
 
@@ -428,6 +432,96 @@ def bench_decode(args, dev, stream):
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                          "frac": gbs / peak, "traffic": None, "peak_kind": kind,
                          "algorithmic_bytes_per_call": alg}}
+
+
+def bench_input_stage(args, spec, dev, stream):
+    """The Mamba block's input stage on the scan workload: the standalone
+    causal conv1d + SiLU (width 4, with bias), the scan with that stage fused
+    in front, and the two-call path (conv, then scan on its output), each over
+    rotating input sets larger than twice the L2 cache."""
+    import torch
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+
+    K = 4
+    inp = I.make_scan_inputs(spec)
+    w, b = I.make_conv_weights(spec.dim, K, True, seed=spec.seed + 7)
+    io = libssm.SSM_BF16 if spec.io == "bf16" else libssm.SSM_F32
+    conv_bytes = I.algorithmic_bytes_conv(spec.batch, spec.L, spec.dim, K, spec.io)
+    scan_bytes = I.algorithmic_bytes_scan(spec)
+    nsets = max(2, min(16, math.ceil(2 * L2_BYTES / scan_bytes) + 1))
+    base = {k: _upload(v, dev) for k, v in inp.items()}
+    wt, bt = _upload(w, dev), _upload(b, dev)
+    sets = []
+    for _ in range(nsets):
+        st = {k: (None if base[k] is None else (base[k] if k in ("A", "D", "delta_bias")
+                                                 else base[k].clone())) for k in base}
+        st["u"] = torch.empty_like(base["x"])
+        st["out"] = torch.empty_like(base["x"])
+        sets.append(st)
+    ws = libssm.alloc_workspace(spec.batch, spec.L, spec.dim, spec.N, io, dev)
+    dims = libssm.make_dims(spec.batch, spec.L, spec.dim, spec.N, io,
+                            None if ws is None else ws.data_ptr(),
+                            0 if ws is None else ws.numel())
+    plan = libssm.ssm_scan_plan(spec.batch, spec.L, spec.dim, spec.N, io)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    sp = 1 if spec.delta_softplus else 0
+
+    def conv(i):
+        st = sets[i % nsets]
+        rc = libssm.lib.ssm_causal_conv1d_silu(_vp(st["x"]), _vp(wt), _vp(bt), K, _vp(st["u"]),
+                                               ctypes.byref(dims), sptr)
+        if rc != 0:
+            raise libssm.SSMError(rc, "ssm_causal_conv1d_silu")
+
+    def scan_args(st, xkey):
+        return (_vp(st[xkey]), _vp(st["delta"]), _vp(st["A"]), _vp(st["B"]), _vp(st["C"]),
+                _vp(st["D"]), _vp(st["z"]), _vp(st["delta_bias"]), sp, _vp(st["out"]), None,
+                ctypes.byref(dims), sptr)
+
+    def fused(i):
+        a = scan_args(sets[i % nsets], "x")
+        rc = libssm.lib.ssm_selective_scan_fwd_conv(a[0], _vp(wt), _vp(bt), K, *a[1:])
+        if rc != 0:
+            raise libssm.SSMError(rc, "ssm_selective_scan_fwd_conv")
+
+    def two_calls(i):
+        conv(i)
+        rc = libssm.lib.ssm_selective_scan_fwd(*scan_args(sets[i % nsets], "u"))
+        if rc != 0:
+            raise libssm.SSMError(rc, "ssm_selective_scan_fwd")
+
+    def timed(fn, n):
+        for i in range(max(args.warmup, 3)):
+            fn(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    n = max(64, min(args.steps, 2000))
+    t_conv = timed(conv, n)
+    t_fused = timed(fused, n)
+    t_two = timed(two_calls, n)
+    status = libssm.ssm_get_device_status(spec.batch, spec.L, spec.dim, spec.N, io, ws)
+    if status != 0:
+        raise libssm.SSMError(status, "device status")
+    peak, kind = measured_peaks()
+    gbs = conv_bytes / t_conv / 1e9
+    elems = spec.elements
+    return {"conv_width": K, "timed_calls": n, "input_sets": nsets,
+            "conv": {"us_per_call": t_conv * 1e6, "value": elems / t_conv, "unit": "elems/s",
+                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                                  "frac": gbs / peak, "traffic": None, "peak_kind": kind,
+                                  "algorithmic_bytes_per_call": conv_bytes}},
+            "fused_scan": {"us_per_call": t_fused * 1e6, "value": elems / t_fused,
+                           "unit": "elems/s", "kernels_per_call": plan["kernels"]},
+            "conv_then_scan": {"us_per_call": t_two * 1e6, "value": elems / t_two,
+                               "unit": "elems/s", "kernels_per_call": plan["kernels"] + 1}}
 
 
 # ---------------------------------------------------------------------------
@@ -531,6 +625,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-input-stage", action="store_true",
+                    help="skip the conv1d + SiLU input-stage timings")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,
                     help="minimum wall time of the CPU oracle baseline")
     args = ap.parse_args(argv)
@@ -565,6 +661,8 @@ def main(argv=None):
                 "plan": res["plan"], "check": res["check"]}
         if "decode" in res:
             line["decode"] = res["decode"]
+        if "input_stage" in res:
+            line["input_stage"] = res["input_stage"]
         if world == 1:
             from selective_state_space_119_b300 import inputs as I
             inp = I.make_scan_inputs(spec)

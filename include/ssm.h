@@ -140,6 +140,52 @@ int ssm_selective_scan_fwd_from_state(const void* x, const void* delta, const fl
                                       ssm_stream_t stream);
 
 /*
+ * The Mamba block's input stage: a causal depthwise conv1d of width conv_k
+ * followed by SiLU ("State Space Models -- Mamba, S4, and Beyond", "Mamba (S6
+ * -- Selective State Space)", MambaBlock: Conv1d with kernel_size = d_conv,
+ * groups = d_inner, padding = d_conv - 1, the output cut to seq_len, then
+ * F.silu; "State-space models (Mamba, S4)", "The Mamba Architecture Block"
+ * draws a Conv1D + SiLU step too). Conv1d is a cross-correlation, so with x = 0 before
+ * the first token:
+ *
+ *     u[b,t,d] = silu(conv_b[d] + sum_{k < conv_k} conv_w[d,k] * x[b, t-conv_k+1+k, d])
+ *
+ *   x, u    : [batch, seqlen, dim] io dtype
+ *   conv_w  : [dim, conv_k] fp32 (the depthwise weight [dim, 1, conv_k]
+ *             without its middle axis); conv_k in 1 .. 4 (d_conv = 4 on the
+ *             pages), else SSM_ERR_DIMS
+ *   conv_b  : [dim] fp32 or NULL (no bias; the pages' block has bias=False)
+ */
+
+/*
+ * ssm_causal_conv1d_silu -- the input stage alone: writes u. In the pages'
+ * block x_proj forms delta, B and C from u, so u is needed in memory before
+ * the scan; this is the call that makes it. u must not overlap x, conv_w or
+ * conv_b (SSM_ERR_ALIAS; the op is not in-place). Only batch, seqlen, dim and
+ * io_dtype of dims are read; dstate, the hints and the workspace are ignored.
+ */
+int ssm_causal_conv1d_silu(const void* x, const float* conv_w, const float* conv_b, int conv_k,
+                           void* u, const ssm_dims* dims, ssm_stream_t stream);
+
+/*
+ * ssm_selective_scan_fwd_conv -- the scan of ssm_selective_scan_fwd with the
+ * input stage fused in front: every x of the scan (the B * x input and the
+ * D * x skip) is replaced by u computed on the fly from x, and u is never
+ * written. Results equal ssm_causal_conv1d_silu followed by
+ * ssm_selective_scan_fwd on u (up to the rounding of u to the io dtype, which
+ * the fused call skips). For callers that form delta, B and C without u, or
+ * that recompute u rather than keep it resident. Arguments are those of
+ * ssm_selective_scan_fwd plus conv_w, conv_b and conv_k as above; with
+ * dstate 16, tile_config_hint must be 0 or 1 (SSM_ERR_DIMS otherwise), and the
+ * workspace is sized by ssm_scan_workspace_bytes as usual.
+ */
+int ssm_selective_scan_fwd_conv(const void* x, const float* conv_w, const float* conv_b,
+                                int conv_k, const void* delta, const float* A, const void* B,
+                                const void* C, const float* D, const void* z,
+                                const float* delta_bias, int delta_softplus, void* out,
+                                float* final_state, const ssm_dims* dims, ssm_stream_t stream);
+
+/*
  * ssm_state_update -- one token of recurrent generation on a cached state
  * ("State-space models (Mamba, S4)", "Training vs Inference Modes"). Exactly
  * one step of the scan above, with the state updated in place:

@@ -212,14 +212,23 @@ size_t ssm_scan_workspace_bytes(const ssm_dims* dims) {
 
 namespace {
 
-// The scan behind both scan entry points; h0 (state before the first token)
-// may be NULL for h = 0.
+// The conv taps of the fused input stage (NULL conv_w: no input stage).
+struct ConvIn {
+    const float* w = nullptr;
+    const float* b = nullptr;
+    int k = 0;
+};
+
+// The scan behind every scan entry point; h0 (state before the first token)
+// may be NULL for h = 0; cv.w non-NULL puts the causal conv1d + SiLU in front.
 int scan_impl(const void* x, const void* delta, const float* A, const void* B, const void* C,
               const float* D, const void* z, const float* delta_bias, int delta_softplus,
               const float* h0, void* out, float* final_state, const ssm_dims* dims,
-              ssm_stream_t stream) {
+              ssm_stream_t stream, const ConvIn& cv = ConvIn{}) {
     int rc = check_dims(dims, true);
     if (rc != SSM_OK) return rc;
+    // the fused input stage runs tile configuration 0 only
+    if (cv.w && dims->dstate == 16 && dims->tile_config_hint > 1) return SSM_ERR_DIMS;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // Empty problems: nothing to read (empty tensors may carry NULL pointers).
     if (dims->batch == 0 || dims->dim == 0) return SSM_OK;
@@ -236,7 +245,7 @@ int scan_impl(const void* x, const void* delta, const float* A, const void* B, c
     if (!x || !delta || !A || !B || !C || !out) return SSM_ERR_NULL;
     {
         const void* const ptrs[] = {x, delta, A, B, C, D, z, delta_bias, h0, out, final_state,
-                                    dims->workspace};
+                                    dims->workspace, cv.w, cv.b};
         rc = check_aligned(ptrs);
         if (rc != SSM_OK) return rc;
     }
@@ -255,7 +264,9 @@ int scan_impl(const void* x, const void* delta, const float* A, const void* B, c
                             {z, elems * es},      {B, rows * es},
                             {C, rows * es},       {A, size_t(dim) * N * 4},
                             {D, size_t(dim) * 4}, {delta_bias, size_t(dim) * 4},
-                            {h0, state_bytes},    {dims->workspace, p.ws_bytes}};
+                            {h0, state_bytes},    {dims->workspace, p.ws_bytes},
+                            {cv.w, size_t(dim) * size_t(cv.k) * 4},
+                            {cv.b, size_t(dim) * 4}};
         const Range outs[] = {{out, elems * es},
                               {final_state, size_t(batch) * dim * N * 4}};
         rc = check_alias(in, outs);
@@ -266,6 +277,7 @@ int scan_impl(const void* x, const void* delta, const float* A, const void* B, c
     a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
     a.delta_bias = delta_bias; a.softplus = delta_softplus ? 1 : 0;
     a.h0 = h0;
+    a.conv_w = cv.w; a.conv_b = cv.b; a.conv_k = cv.k;
     a.out = out; a.final_state = final_state;
     a.batch = batch; a.L = L; a.dim = dim;
     a.chunk_len = p.chunk_len; a.nchunks = p.nchunks; a.tiles = p.tiles;
@@ -299,6 +311,52 @@ int ssm_selective_scan_fwd_from_state(const void* x, const void* delta, const fl
     if (!h0 && dims && dims->batch > 0 && dims->dim > 0) return SSM_ERR_NULL;
     return scan_impl(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, out,
                      final_state, dims, stream);
+}
+
+int ssm_selective_scan_fwd_conv(const void* x, const float* conv_w, const float* conv_b,
+                                int conv_k, const void* delta, const float* A, const void* B,
+                                const void* C, const float* D, const void* z,
+                                const float* delta_bias, int delta_softplus, void* out,
+                                float* final_state, const ssm_dims* dims, ssm_stream_t stream) {
+    if (conv_k < 1 || conv_k > ssm::kMaxConvK) return SSM_ERR_DIMS;
+    if (!conv_w && dims && dims->batch > 0 && dims->dim > 0 && dims->seqlen > 0)
+        return SSM_ERR_NULL;
+    ConvIn cv;
+    cv.w = conv_w; cv.b = conv_b; cv.k = conv_k;
+    return scan_impl(x, delta, A, B, C, D, z, delta_bias, delta_softplus, nullptr, out,
+                     final_state, dims, stream, cv);
+}
+
+int ssm_causal_conv1d_silu(const void* x, const float* conv_w, const float* conv_b, int conv_k,
+                           void* u, const ssm_dims* dims, ssm_stream_t stream) {
+    if (!dims) return SSM_ERR_NULL;
+    if (conv_k < 1 || conv_k > ssm::kMaxConvK) return SSM_ERR_DIMS;
+    // only the [batch, seqlen, dim] sizes and io_dtype matter here
+    ssm_dims d = *dims;
+    d.dstate = 16; d.chunk_len_hint = 0; d.tile_config_hint = 0;
+    int rc = check_dims(&d, true);
+    if (rc != SSM_OK) return rc;
+    if (d.batch == 0 || d.seqlen == 0 || d.dim == 0) return SSM_OK;
+    if (!x || !conv_w || !u) return SSM_ERR_NULL;
+    {
+        const void* const ptrs[] = {x, conv_w, conv_b, u};
+        rc = check_aligned(ptrs);
+        if (rc != SSM_OK) return rc;
+    }
+    const size_t elems = size_t(d.batch) * size_t(d.seqlen) * size_t(d.dim);
+    {
+        const Range in[] = {{x, elems * io_size(d.io_dtype)},
+                            {conv_w, size_t(d.dim) * size_t(conv_k) * 4},
+                            {conv_b, size_t(d.dim) * 4}};
+        const Range outs[] = {{u, elems * io_size(d.io_dtype)}};
+        rc = check_alias(in, outs);
+        if (rc != SSM_OK) return rc;
+    }
+    ssm::ConvArgs a{};
+    a.x = x; a.w = conv_w; a.b = conv_b; a.u = u;
+    a.batch = d.batch; a.L = d.seqlen; a.dim = d.dim; a.k = conv_k;
+    return set_cuda(ssm::launch_conv1d_silu(a, d.io_dtype,
+                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int ssm_state_update(float* state, const void* x, const void* delta, const float* A,

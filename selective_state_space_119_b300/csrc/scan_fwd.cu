@@ -87,10 +87,17 @@ struct Cfg {
     static_assert(DT * sizeof(T) % 16 == 0, "TMA rows are whole 16-byte units");
 };
 
-template <typename T, int N, typename TC, int MODE>
+// CONV: the x tile carries kConvHalo extra rows before the stage (the causal
+// conv1d window of the fused input stage).
+constexpr int kConvMaxK = kMaxConvK;
+constexpr int kConvHalo = kConvMaxK - 1;
+
+template <typename T, int N, typename TC, int MODE, bool CONV = false>
 struct Smem {
     using C = Cfg<T, N, TC>;
     static constexpr int NT = MODE == 1 ? 3 : 2;          // x, delta (, z) tiles per stage
+    static constexpr int XR = C::TS + (CONV ? kConvHalo : 0);  // rows of the x tile
+    static constexpr int XT = XR * C::DT;                 // elements of the x tile
     static constexpr int NBC = MODE == 1 ? 2 : 1;         // B (and C) rows per token
     static constexpr int ROW = NBC * N;                   // floats per token row of bcf
     // B / C rows travel with the stage's TMA transaction when a row is a whole
@@ -98,14 +105,19 @@ struct Smem {
     // while being converted.
     static constexpr bool BC_TMA = (N * sizeof(T)) % 16 == 0;
     static constexpr int BC_ELEMS = BC_TMA ? NBC * C::TS * N : 0;
-    static constexpr int STAGE_ELEMS = NT * C::TILE + BC_ELEMS;
+    // stage layout: x [XR][DT], delta [TS][DT], (z [TS][DT],) B rows, (C rows)
+    static constexpr int STAGE_ELEMS = XT + (NT - 1) * C::TILE + BC_ELEMS;
+    static constexpr int kDelta = XT;                     // element offsets in a stage
+    static constexpr int kZ = XT + C::TILE;
+    static constexpr int kStagedBC = XT + (NT - 1) * C::TILE;
     static constexpr int kIn = 0;                                                   // [NST][STAGE_ELEMS] T
     static constexpr int kOut = kIn + C::NST * STAGE_ELEMS * int(sizeof(T));        // [2][TS][DT] T
     static constexpr int kBC = (kOut + (MODE == 1 ? 2 * C::TILE * int(sizeof(T)) : 0) + 127) & ~127;  // [2][TS][ROW] f32
     static constexpr int kBar = kBC + 2 * C::TS * ROW * 4;
     static constexpr int kBytes = kBar + C::NST * 8;
     static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
-    static_assert((STAGE_ELEMS * sizeof(T)) % 128 == 0 && (C::TILE * sizeof(T)) % 128 == 0,
+    static_assert((STAGE_ELEMS * sizeof(T)) % 128 == 0 && (C::TILE * sizeof(T)) % 128 == 0 &&
+                      (XT * sizeof(T)) % 128 == 0,
                   "TMA destinations stay 128-byte aligned");
 };
 
@@ -182,19 +194,22 @@ __device__ __forceinline__ float lds_elem(const __nv_bfloat16* p) {
     return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16);
 }
 
-// SOFTPLUS: dt = softplus(delta + bias); GATE: out = y * silu(z). Both are
-// template flags so that the per-token body has no branches and the compiler
-// can overlap successive tokens.
-template <typename T, int N, typename TC, int MODE, bool SOFTPLUS, bool GATE>
+// SOFTPLUS: dt = softplus(delta + bias); GATE: out = y * silu(z); CONV: the
+// scan input is u = silu(conv_b + sum_k conv_w[k] x[t - 3 + k]) (the fused
+// causal depthwise conv1d + SiLU) instead of x. They are template flags so
+// that the per-token body has no branches and the compiler can overlap
+// successive tokens.
+template <typename T, int N, typename TC, int MODE, bool SOFTPLUS, bool GATE, bool CONV>
 __global__ void __launch_bounds__(Cfg<T, N, TC>::THREADS, 1)
 scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dt,
             const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
             const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_out,
             const ScanArgs a) {
     using Cf = Cfg<T, N, TC>;
-    using Sm = Smem<T, N, TC, MODE>;
+    using Sm = Smem<T, N, TC, MODE, CONV>;
     constexpr int NS = Cf::NS, SPL = Cf::SPL, DT = Cf::DT, TS = Cf::TS, TILE = Cf::TILE;
-    constexpr int NST = Cf::NST, THREADS = Cf::THREADS, NT = Sm::NT, NBC = Sm::NBC, ROW = Sm::ROW;
+    constexpr int XH = CONV ? kConvHalo : 0;   // halo rows before the stage in the x tile
+    constexpr int NST = Cf::NST, THREADS = Cf::THREADS, NBC = Sm::NBC, ROW = Sm::ROW;
     constexpr bool BC_TMA = Sm::BC_TMA;
     constexpr bool has_z = MODE == 1 && GATE;
 
@@ -217,7 +232,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     // bytes that land per stage: the tiles actually loaded (no z tile without
     // the gate) and the B / C rows
     const uint32_t stage_tx =
-        static_cast<uint32_t>(((has_z ? 3 : 2) * TILE + Sm::BC_ELEMS) * sizeof(T));
+        static_cast<uint32_t>((Sm::XT + (has_z ? 2 : 1) * TILE + Sm::BC_ELEMS) * sizeof(T));
 
     if (tid == 0) {
         for (int i = 0; i < NST; ++i) mbar_init(&full[i], 1);
@@ -229,15 +244,19 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         T* dst = in + static_cast<size_t>(buf) * Sm::STAGE_ELEMS;
         const int t = static_cast<int>(t_begin + static_cast<int64_t>(s) * TS);
         mbar_arrive_expect_tx(&full[buf], stage_tx);
-        tma_load_3d(dst, &tm_x, static_cast<int>(dbase), t, static_cast<int>(b), &full[buf]);
-        tma_load_3d(dst + TILE, &tm_dt, static_cast<int>(dbase), t, static_cast<int>(b), &full[buf]);
+        // the x tile starts XH tokens early (negative rows read as zero: the
+        // conv's causal padding)
+        tma_load_3d(dst, &tm_x, static_cast<int>(dbase), t - XH, static_cast<int>(b), &full[buf]);
+        tma_load_3d(dst + Sm::kDelta, &tm_dt, static_cast<int>(dbase), t, static_cast<int>(b),
+                    &full[buf]);
         if constexpr (has_z)
-            tma_load_3d(dst + 2 * TILE, &tm_z, static_cast<int>(dbase), t, static_cast<int>(b),
+            tma_load_3d(dst + Sm::kZ, &tm_z, static_cast<int>(dbase), t, static_cast<int>(b),
                         &full[buf]);
         if constexpr (BC_TMA) {
-            tma_load_3d(dst + NT * TILE, &tm_B, 0, t, static_cast<int>(b), &full[buf]);
+            tma_load_3d(dst + Sm::kStagedBC, &tm_B, 0, t, static_cast<int>(b), &full[buf]);
             if constexpr (MODE == 1)
-                tma_load_3d(dst + NT * TILE + TS * N, &tm_C, 0, t, static_cast<int>(b), &full[buf]);
+                tma_load_3d(dst + Sm::kStagedBC + TS * N, &tm_C, 0, t, static_cast<int>(b),
+                            &full[buf]);
         }
     };
     if (tid == 0)
@@ -279,6 +298,17 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     }
     const float bias = (a.delta_bias && ch_ok) ? __ldg(a.delta_bias + dsafe) : 0.f;
     const float Dd = (MODE == 1 && a.D && ch_ok) ? __ldg(a.D + dsafe) : 0.f;
+    // conv taps of the own channel, right-aligned in a width-4 window (the
+    // last tap multiplies the current token)
+    float cw[kConvMaxK], cb = 0.f;
+    if constexpr (CONV) {
+#pragma unroll
+        for (int q = 0; q < kConvMaxK; ++q) {
+            const int kk = q - (kConvMaxK - a.conv_k);
+            cw[q] = (kk >= 0 && ch_ok) ? __ldg(a.conv_w + dsafe * a.conv_k + kk) : 0.f;
+        }
+        cb = (a.conv_b && ch_ok) ? __ldg(a.conv_b + dsafe) : 0.f;
+    }
 
     // ---- B / C rows of a stage -> fp32 bcf[s & 1][t][B(N) | C(N)] ----
     constexpr int VE = 16 / sizeof(T) < N ? 16 / sizeof(T) : N;  // elements per vector
@@ -286,7 +316,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const T* __restrict__ Bg = static_cast<const T*>(a.B) + b * a.L * N;
     const T* __restrict__ Cg = static_cast<const T*>(a.C) + b * a.L * N;
     auto convert_bc = [&](int s) {
-        const T* staged = in + static_cast<size_t>(s % NST) * Sm::STAGE_ELEMS + NT * TILE;
+        const T* staged = in + static_cast<size_t>(s % NST) * Sm::STAGE_ELEMS + Sm::kStagedBC;
         float* dst = bcf + (s & 1) * TS * ROW;
         const int64_t ts = t_begin + static_cast<int64_t>(s) * TS;
         for (int idx = tid; idx < NVEC; idx += THREADS) {
@@ -322,9 +352,9 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     int s = 0;
     for (; s < nstages && !aborted; ++s) {
         const int buf = s % NST;
-        const T* xt = in + static_cast<size_t>(buf) * Sm::STAGE_ELEMS;
-        const T* dlt = xt + TILE;
-        const T* zt = xt + 2 * TILE;
+        const T* xt = in + static_cast<size_t>(buf) * Sm::STAGE_ELEMS;  // row XH = first token
+        const T* dlt = xt + Sm::kDelta;
+        const T* zt = xt + Sm::kZ;
         const float* bc = bcf + (s & 1) * TS * ROW;
         T* ot = outb + (s & 1) * TILE;
         const int64_t t0 = t_begin + static_cast<int64_t>(s) * TS;
@@ -340,7 +370,15 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         const int lim = static_cast<int>(t_end - t0 < TS ? t_end - t0 : TS);  // valid tokens
         auto prep = [&](int tl) {
             Tok k;
-            k.x = lds_elem(xt + tl * DT + col);
+            if constexpr (CONV) {
+                float pre = cb;
+#pragma unroll
+                for (int q = 0; q < kConvMaxK; ++q)
+                    pre = fmaf(cw[q], lds_elem(xt + (tl + q) * DT + col), pre);
+                k.x = silu(pre);
+            } else {
+                k.x = lds_elem(xt + tl * DT + col);
+            }
             float dt = lds_elem(dlt + tl * DT + col) + bias;
             if constexpr (SOFTPLUS) dt = softplus(dt);
             dt = tl < lim ? dt : 0.f;
@@ -453,17 +491,18 @@ EncodeTiled encode_fn() {
     return fn;
 }
 
-// [batch][L][dim] tensor, box of `box_channels` channels x TS tokens x 1 batch
-// row (elements past the sequence end or the last channel read as zero).
+// [batch][L][dim] tensor, box of `box_channels` channels x `box_rows` tokens x
+// 1 batch row (elements before the sequence start, past its end or past the
+// last channel read as zero).
 template <typename T>
 cudaError_t make_tmap(CUtensorMap* tm, const void* base, int64_t batch, int64_t L, int64_t dim,
-                      int box_channels) {
+                      int box_channels, int box_rows = kScanStageTokens) {
     EncodeTiled fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     const cuuint64_t es = sizeof(T);
     const cuuint64_t gdim[3] = {cuuint64_t(dim), cuuint64_t(L), cuuint64_t(batch)};
     const cuuint64_t gstride[2] = {cuuint64_t(dim) * es, cuuint64_t(L) * cuuint64_t(dim) * es};
-    const cuuint32_t box[3] = {cuuint32_t(box_channels), cuuint32_t(kScanStageTokens), 1};
+    const cuuint32_t box[3] = {cuuint32_t(box_channels), cuuint32_t(box_rows), 1};
     const cuuint32_t estride[3] = {1, 1, 1};
     const CUresult r = fn(tm, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
@@ -475,7 +514,7 @@ cudaError_t make_tmap(CUtensorMap* tm, const void* base, int64_t batch, int64_t 
 
 // Raise the dynamic shared-memory limit of one kernel instantiation, once per
 // device (the statics are per instantiation).
-template <typename T, int N, typename TC, int MODE, bool SP, bool GATE>
+template <typename T, int N, typename TC, int MODE, bool SP, bool GATE, bool CONV>
 cudaError_t allow_smem() {
     static std::mutex mu;
     static bool done[128] = {};
@@ -485,20 +524,22 @@ cudaError_t allow_smem() {
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(scan_kernel<T, N, TC, MODE, SP, GATE>,
+    e = cudaFuncSetAttribute(scan_kernel<T, N, TC, MODE, SP, GATE, CONV>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Smem<T, N, TC, MODE>::kBytes);
+                             Smem<T, N, TC, MODE, CONV>::kBytes);
     if (e == cudaSuccess) done[dev] = true;
     return e;
 }
 
-template <typename T, int N, typename TC, bool SOFTPLUS, bool GATE>
+template <typename T, int N, typename TC, bool SOFTPLUS, bool GATE, bool CONV>
 cudaError_t launch_flags(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     using Cf = Cfg<T, N, TC>;
     if (p.channels_per_cta != Cf::DT) return cudaErrorInvalidValue;
     CUtensorMap tx, tdt, tz, tB, tC, tout;
     cudaError_t e;
-    if ((e = make_tmap<T>(&tx, a.x, a.batch, a.L, a.dim, Cf::DT)) != cudaSuccess) return e;
+    if ((e = make_tmap<T>(&tx, a.x, a.batch, a.L, a.dim, Cf::DT,
+                          Smem<T, N, TC, 1, CONV>::XR)) != cudaSuccess)
+        return e;
     if ((e = make_tmap<T>(&tdt, a.delta, a.batch, a.L, a.dim, Cf::DT)) != cudaSuccess) return e;
     if ((e = make_tmap<T>(&tout, a.out, a.batch, a.L, a.dim, Cf::DT)) != cudaSuccess) return e;
     tz = tx;
@@ -513,26 +554,26 @@ cudaError_t launch_flags(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     }
     const int64_t per_chunk = p.tiles * a.batch;
     if (p.nchunks > 1) {
-        if ((e = allow_smem<T, N, TC, 0, SOFTPLUS, false>()) != cudaSuccess) return e;
-        scan_kernel<T, N, TC, 0, SOFTPLUS, false>
+        if ((e = allow_smem<T, N, TC, 0, SOFTPLUS, false, CONV>()) != cudaSuccess) return e;
+        scan_kernel<T, N, TC, 0, SOFTPLUS, false, CONV>
             <<<static_cast<unsigned>(per_chunk * (p.nchunks - 1)), Cf::THREADS,
-               Smem<T, N, TC, 0>::kBytes, s>>>(tx, tdt, tz, tB, tC, tout, a);
+               Smem<T, N, TC, 0, CONV>::kBytes, s>>>(tx, tdt, tz, tB, tC, tout, a);
     }
-    if ((e = allow_smem<T, N, TC, 1, SOFTPLUS, GATE>()) != cudaSuccess) return e;
-    scan_kernel<T, N, TC, 1, SOFTPLUS, GATE>
-        <<<static_cast<unsigned>(per_chunk * p.nchunks), Cf::THREADS, Smem<T, N, TC, 1>::kBytes,
-           s>>>(tx, tdt, tz, tB, tC, tout, a);
+    if ((e = allow_smem<T, N, TC, 1, SOFTPLUS, GATE, CONV>()) != cudaSuccess) return e;
+    scan_kernel<T, N, TC, 1, SOFTPLUS, GATE, CONV>
+        <<<static_cast<unsigned>(per_chunk * p.nchunks), Cf::THREADS,
+           Smem<T, N, TC, 1, CONV>::kBytes, s>>>(tx, tdt, tz, tB, tC, tout, a);
     return cudaGetLastError();
 }
 
-template <typename T, int N, typename TC>
+template <typename T, int N, typename TC, bool CONV>
 cudaError_t launch_cfg(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     const bool sp = a.softplus != 0, gate = a.z != nullptr;
     if (sp)
-        return gate ? launch_flags<T, N, TC, true, true>(a, p, s)
-                    : launch_flags<T, N, TC, true, false>(a, p, s);
-    return gate ? launch_flags<T, N, TC, false, true>(a, p, s)
-                : launch_flags<T, N, TC, false, false>(a, p, s);
+        return gate ? launch_flags<T, N, TC, true, true, CONV>(a, p, s)
+                    : launch_flags<T, N, TC, true, false, CONV>(a, p, s);
+    return gate ? launch_flags<T, N, TC, false, true, CONV>(a, p, s)
+                : launch_flags<T, N, TC, false, false, CONV>(a, p, s);
 }
 
 // The tile configurations by id (the same table as scan_lanes... in ssm_internal.h).
@@ -543,16 +584,20 @@ using Tile3 = TileCfg<3>;
 
 template <typename T, int N>
 cudaError_t launch_typed(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
+    // the fused conv input stage is built for tile configuration 0 only (the
+    // planner never picks another one for it)
+    if (a.conv_w) return p.tile_cfg == 0 ? launch_cfg<T, N, Tile0, true>(a, p, s)
+                                         : cudaErrorInvalidValue;
     if constexpr (N == 16) {
         switch (p.tile_cfg) {
-            case 0: return launch_cfg<T, N, Tile0>(a, p, s);
-            case 1: return launch_cfg<T, N, Tile1>(a, p, s);
-            case 2: return launch_cfg<T, N, Tile2>(a, p, s);
-            case 3: return launch_cfg<T, N, Tile3>(a, p, s);
+            case 0: return launch_cfg<T, N, Tile0, false>(a, p, s);
+            case 1: return launch_cfg<T, N, Tile1, false>(a, p, s);
+            case 2: return launch_cfg<T, N, Tile2, false>(a, p, s);
+            case 3: return launch_cfg<T, N, Tile3, false>(a, p, s);
             default: return cudaErrorInvalidValue;
         }
     } else {
-        return launch_cfg<T, N, Tile0>(a, p, s);   // small dstate: one configuration
+        return launch_cfg<T, N, Tile0, false>(a, p, s);   // small dstate: one configuration
     }
 }
 

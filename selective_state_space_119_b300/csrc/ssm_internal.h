@@ -59,6 +59,9 @@ struct ScanArgs {
     int64_t batch, L, dim;
     int64_t chunk_len, nchunks, tiles;
     const float* h0;  // [batch][dim][N] state before the first token, or NULL (zero)
+    const float* conv_w;  // [dim][conv_k] causal conv taps of the fused input stage, or NULL
+    const float* conv_b;  // [dim] conv bias, or NULL
+    int conv_k;           // conv width (1 .. 4) when conv_w is given
     float* ws_H;   // [batch][nchunks-1][dim][N]: chunk-local end states (from h = 0)
     float* ws_S;   // [batch][nchunks-1][dim]: sum of dt over each chunk
     unsigned int* status;  // workspace status word (sticky; 0 = ok; no current kernel sets it)
@@ -79,9 +82,23 @@ struct StepArgs {
     int64_t batch, dim;
 };
 
+// Widest causal conv of the Mamba block's input stage (d_conv = 4 on the pages).
+constexpr int kMaxConvK = 4;
+
+struct ConvArgs {
+    const void* x;          // [batch][L][dim]
+    const float* w;         // [dim][k]
+    const float* b;         // [dim] or NULL
+    void* u;                // [batch][L][dim]
+    int64_t batch, L, dim;
+    int k;
+};
+
 // Enqueue one full scan (all phases). io: 0 = fp32, 1 = bf16.
 cudaError_t launch_scan(const ScanArgs& a, const ScanPlan& p, int io, int N, cudaStream_t s);
 // Enqueue one decode step.
 cudaError_t launch_state_update(const StepArgs& a, int io, int N, cudaStream_t s);
+// Enqueue the standalone causal depthwise conv1d + SiLU.
+cudaError_t launch_conv1d_silu(const ConvArgs& a, int io, cudaStream_t s);
 
 }  // namespace ssm

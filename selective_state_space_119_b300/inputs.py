@@ -30,7 +30,7 @@ turns any stored array back into float64 exactly.
 from __future__ import annotations
 
 import dataclasses
-from typing import Dict, Optional
+from typing import Dict, Optional, Tuple
 
 import numpy as np
 
@@ -253,6 +253,26 @@ def make_decode_inputs(spec: DecodeSpec, seed: Optional[int] = None) -> Dict[str
     else:
         out["state0"] = np.zeros((b, d, N), dtype=np.float32)
     return out
+
+
+def make_conv_weights(dim: int, K: int = 4, bias: bool = True,
+                      seed: int = 0) -> Tuple[np.ndarray, Optional[np.ndarray]]:
+    """Taps [dim, K] and bias [dim] (or None) of a depthwise causal conv1d,
+    fp32, drawn uniform in +-1/sqrt(K): the default initialisation range of a
+    Conv1d whose fan-in is K (one input channel per group)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    bound = 1.0 / np.sqrt(K)
+    w = rng.uniform(-bound, bound, (dim, K)).astype(np.float32)
+    b = rng.uniform(-bound, bound, dim).astype(np.float32) if bias else None
+    return w, b
+
+
+def algorithmic_bytes_conv(batch: int, L: int, dim: int, K: int, io: str,
+                           bias: bool = True) -> int:
+    """Bytes the standalone conv1d + SiLU must move at least once: x read and u
+    written per element, the taps (and bias) once."""
+    es = 2 if io == "bf16" else 4
+    return 2 * batch * L * dim * es + dim * K * 4 + (dim * 4 if bias else 0)
 
 
 def algorithmic_bytes_scan(spec: ScanSpec) -> int:

@@ -7,8 +7,9 @@ has not been built (``python -m selective_state_space_119_b300.build``); there
 is no CPU fallback.
 
 The functions carry the C names (``ssm_selective_scan_fwd``,
-``ssm_state_update``, ``ssm_scan_workspace_bytes``, ``ssm_scan_plan``,
-``ssm_get_device_status``, ``ssm_strerror``) and take torch tensors. The raw
+``ssm_state_update``, ``ssm_causal_conv1d_silu``, ``ssm_scan_workspace_bytes``,
+``ssm_scan_plan``, ``ssm_get_device_status``, ``ssm_strerror``) and take torch
+tensors. The raw
 ctypes handle is ``lib`` for callers that hold plain device pointers.
 """
 from __future__ import annotations
@@ -41,7 +42,8 @@ SSM_ERR_ALIAS = -8
 # Every symbol include/ssm.h declares.
 EXPORTED = ("ssm_selective_scan_fwd", "ssm_state_update", "ssm_scan_workspace_bytes",
             "ssm_scan_plan", "ssm_get_device_status", "ssm_strerror", "ssm_last_cuda_error",
-            "ssm_version", "ssm_selective_scan_fwd_static", "ssm_selective_scan_fwd_from_state")
+            "ssm_version", "ssm_selective_scan_fwd_static", "ssm_selective_scan_fwd_from_state",
+            "ssm_selective_scan_fwd_conv", "ssm_causal_conv1d_silu")
 
 # Size of the library-owned scratch of ssm_selective_scan_fwd_static (include/ssm.h).
 SSM_STATIC_SCRATCH_BYTES = 16 << 20
@@ -69,6 +71,11 @@ lib.ssm_selective_scan_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, c
 lib.ssm_selective_scan_fwd_from_state.restype = ctypes.c_int
 lib.ssm_selective_scan_fwd_from_state.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                                   ctypes.c_int, _vp, _vp, _vp, _dims_p, _vp]
+lib.ssm_selective_scan_fwd_conv.restype = ctypes.c_int
+lib.ssm_selective_scan_fwd_conv.argtypes = [_vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
+                                            _vp, _vp, ctypes.c_int, _vp, _vp, _dims_p, _vp]
+lib.ssm_causal_conv1d_silu.restype = ctypes.c_int
+lib.ssm_causal_conv1d_silu.argtypes = [_vp, _vp, _vp, ctypes.c_int, _vp, _dims_p, _vp]
 lib.ssm_selective_scan_fwd_static.restype = ctypes.c_int
 lib.ssm_selective_scan_fwd_static.argtypes = list(lib.ssm_selective_scan_fwd.argtypes)
 lib.ssm_state_update.restype = ctypes.c_int
@@ -179,7 +186,8 @@ def alloc_workspace(batch, seqlen, dim, dstate, io, device, chunk_len_hint=0, ti
 def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
                            delta_softplus=False, out=None, final_state=None,
                            return_final_state=True, workspace=None, chunk_len_hint=0,
-                           tile_config_hint=0, stream=None, h0=None) -> Tuple[object, Optional[object]]:
+                           tile_config_hint=0, stream=None, h0=None, conv_w=None,
+                           conv_b=None) -> Tuple[object, Optional[object]]:
     """Selective scan over x [batch, L, dim] (see include/ssm.h).
 
     Returns (out, final_state); final_state is None when not requested.
@@ -188,6 +196,9 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
     (allocated per call when omitted). ``h0`` ([batch, dim, N] fp32), when
     given, is the state before the first token
     (ssm_selective_scan_fwd_from_state); otherwise the scan starts from zero.
+    ``conv_w`` ([dim, K] fp32, K <= 4) and ``conv_b`` ([dim] fp32 or None)
+    put the causal conv1d + SiLU input stage in front of the scan
+    (ssm_selective_scan_fwd_conv): x is then the conv's input.
     """
     torch = _torch()
     batch, L, dim = x.shape
@@ -218,15 +229,52 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
         _ptr(out, "out", io, (batch, L, dim), dev),
         _ptr(final_state, "final_state", torch.float32, (batch, dim, N), dev),
     )
+    if conv_w is not None and h0 is not None:
+        raise ValueError("the fused conv input stage starts from h = 0; h0 is not supported")
+    if conv_w is None and conv_b is not None:
+        raise ValueError("conv_b needs conv_w")
     with torch.cuda.device(dev):
-        if h0 is None:
+        if conv_w is not None:
+            if conv_w.dim() != 2 or conv_w.shape[0] != dim:
+                raise ValueError("conv_w must have shape (dim, K), got %s" % (tuple(conv_w.shape),))
+            K = int(conv_w.shape[1])
+            wp = _ptr(conv_w, "conv_w", torch.float32, (dim, K), dev)
+            bp = _ptr(conv_b, "conv_b", torch.float32, (dim,), dev)
+            rc = lib.ssm_selective_scan_fwd_conv(args[0], wp, bp, K, *args[1:],
+                                                 ctypes.byref(dims), _stream(dev, stream))
+        elif h0 is None:
             rc = lib.ssm_selective_scan_fwd(*args, ctypes.byref(dims), _stream(dev, stream))
         else:
             h0p = _ptr(h0, "h0", torch.float32, (batch, dim, N), dev)
             rc = lib.ssm_selective_scan_fwd_from_state(*args[:9], h0p, *args[9:],
                                                        ctypes.byref(dims), _stream(dev, stream))
-    _check(rc, "ssm_selective_scan_fwd" if h0 is None else "ssm_selective_scan_fwd_from_state")
+    _check(rc, "ssm_selective_scan_fwd_conv" if conv_w is not None else
+           "ssm_selective_scan_fwd" if h0 is None else "ssm_selective_scan_fwd_from_state")
     return out, final_state
+
+
+def ssm_causal_conv1d_silu(x, conv_w, conv_b=None, out=None, stream=None):
+    """u = silu(causal depthwise conv1d(x)) over x [batch, L, dim] with taps
+    conv_w [dim, K] fp32 (K <= 4) and bias conv_b [dim] fp32 or None. Returns u
+    (same shape and dtype as x; ``out`` may be passed preallocated)."""
+    torch = _torch()
+    batch, L, dim = x.shape
+    dev = x.device
+    if conv_w.dim() != 2 or conv_w.shape[0] != dim:
+        raise ValueError("conv_w must have shape (dim, K), got %s" % (tuple(conv_w.shape),))
+    K = int(conv_w.shape[1])
+    if out is None:
+        out = torch.empty_like(x)
+    dims = make_dims(batch, L, dim, 16, _io_code(x))
+    with torch.cuda.device(dev):
+        rc = lib.ssm_causal_conv1d_silu(
+            _ptr(x, "x", x.dtype, (batch, L, dim), dev),
+            _ptr(conv_w, "conv_w", torch.float32, (dim, K), dev),
+            _ptr(conv_b, "conv_b", torch.float32, (dim,), dev), K,
+            _ptr(out, "out", x.dtype, (batch, L, dim), dev),
+            ctypes.byref(dims), _stream(dev, stream))
+    _check(rc, "ssm_causal_conv1d_silu")
+    return out
 
 
 def ssm_selective_scan_fwd_static(x, delta, A, B, C, D=None, z=None, delta_bias=None,
@@ -311,3 +359,4 @@ def ssm_get_device_status(batch, seqlen, dim, dstate, io, workspace, chunk_len_h
 # Short aliases.
 selective_scan_fwd = ssm_selective_scan_fwd
 state_update = ssm_state_update
+causal_conv1d_silu = ssm_causal_conv1d_silu

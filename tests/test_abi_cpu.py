@@ -152,3 +152,40 @@ def test_from_state_rejects_bad_arguments_before_launch():
     assert call(h0=None) == L.SSM_ERR_NULL                     # the state is required
     assert call(h0=FAKE + (1 << 31) + 4) == L.SSM_ERR_ALIGN
     assert call(fs=FAKE + (1 << 31)) == L.SSM_ERR_ALIAS         # final state over h0
+
+
+def test_conv_entry_points_reject_bad_arguments_before_launch():
+    d = L.make_dims(1, 4, 8, 16, "bf16", workspace=FAKE + (1 << 34), workspace_bytes=1 << 20)
+    W = FAKE + (1 << 32)
+
+    def scan(w=W, k=4, b=None, out=FAKE + (1 << 30), dims=d):
+        return L.lib.ssm_selective_scan_fwd_conv(
+            FAKE, w, b, k, FAKE + 4096, FAKE + 8192, FAKE + 12288, FAKE + 16384, None, None,
+            None, 0, out, None, ctypes.byref(dims), None)
+
+    def conv(w=W, k=4, b=None, u=FAKE + (1 << 30), x=FAKE, dims=d):
+        return L.lib.ssm_causal_conv1d_silu(x, w, b, k, u, ctypes.byref(dims), None)
+
+    for f in (scan, conv):
+        assert f(w=None) == L.SSM_ERR_NULL                      # the taps are required
+        assert f(k=0) == L.SSM_ERR_DIMS and f(k=5) == L.SSM_ERR_DIMS
+        assert f(w=W + 4) == L.SSM_ERR_ALIGN
+        assert f(b=W + 8) == L.SSM_ERR_ALIGN
+    assert scan(out=W) == L.SSM_ERR_ALIAS                       # out over the taps
+    assert conv(u=W + 16) == L.SSM_ERR_ALIAS
+    assert conv(u=FAKE) == L.SSM_ERR_ALIAS                      # not in-place
+    assert conv(u=FAKE + 16) == L.SSM_ERR_ALIAS                 # nor shifted over x
+    # the fused stage runs tile configuration 0 only
+    for hint, ok in ((0, True), (1, True), (2, False), (4, False)):
+        dh = L.make_dims(1, 4, 8, 16, "bf16", workspace=FAKE + (1 << 34), workspace_bytes=1 << 20,
+                         tile_config_hint=hint)
+        rc = scan(dims=dh, out=W)      # an alias is reported after the hint check
+        assert rc == (L.SSM_ERR_ALIAS if ok else L.SSM_ERR_DIMS), (hint, rc)
+    # the standalone conv ignores dstate and the hints
+    dz = L.make_dims(1, 4, 8, 3, "bf16", tile_config_hint=4, chunk_len_hint=7)
+    assert conv(w=None, dims=dz) == L.SSM_ERR_NULL
+    # empty problems enqueue nothing and need no pointers
+    de = L.make_dims(0, 4, 8, 16, "bf16")
+    assert conv(w=None, u=None, x=None, dims=de) == L.SSM_OK
+    # bf16 dim must be a multiple of 8
+    assert conv(dims=L.make_dims(1, 4, 12, 16, "bf16")) == L.SSM_ERR_ALIGN
