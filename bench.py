@@ -13,8 +13,10 @@ bias), gate), i.e. every step of the scan path. Rank 0 prints one JSON line.
 * e2e: the same metric through the same C-ABI call with host buffers:
   pinned host -> device copies of the step's inputs and a device -> host copy
   of its output inside the timed region.
-* roofline: algorithmic bytes per call / average call time, against the
-  measured HBM copy bandwidth of this GPU model.
+* roofline: the binding unit of the scan, the SFU: the SFU operations the
+  method needs per call / average call time, against the measured ex2 rate;
+  hbm_roofline: algorithmic bytes per call / call time against the measured
+  HBM copy bandwidth; floors_us: the per-call floor of each unit.
 * decode: the recurrent step ssm_state_update on the decode workload (batch
   256, dim 5120, N 16), rotating over several cached states.
 * input_stage: the causal conv1d + SiLU (width 4) alone, fused in front of
@@ -289,12 +291,11 @@ def bench_scan(args, rank, world, local):
     res = {
         "value": value, "ms_per_step": slowest / args.steps * 1e3,
         "gbps": achieved,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "ssm_selective_scan_fwd call (%d kernel%s)"
-                               % (plan["kernels"], "s" if plan["kernels"] > 1 else ""),
-                     "algorithmic_bytes_per_call": alg_bytes},
-        "alu_roofline": alu_roofline(spec, per_call),
+        "roofline": alu_roofline(spec, per_call, plan),
+        "hbm_roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_call": alg_bytes},
+        "floors_us": time_floors(spec, alg_bytes, peak),
         "gpu_launches": args.steps * plan["kernels"],
         "clocks": clocks.summary(t_wall0, t_wall1),
         "plan": plan,
@@ -346,21 +347,43 @@ def bench_scan(args, rank, world, local):
 # SFU (MUFU) exponential rate of one B300 SM per clock, measured with a probe of
 # back-to-back independent ex2.approx.ftz.f32 at full occupancy: 29.1 per SM per
 # clock (the nominal 2 x 16 of Blackwell Ultra's doubled SFU), 148 SMs, at the
-# 2032 MHz maximum SM clock.
+# 2032 MHz maximum SM clock. FP32 lanes per SM per clock: 128 (nominal).
 EX2_PER_SM_CLK = 29.1
+FP32_PER_SM_CLK = 128.0
 SMS = 148
 SM_MAX_MHZ = 2032.0
 
 
-def alu_roofline(spec, per_call_s):
-    """The exponentials the method needs (N per element for exp(dt A), one more
-    per element for softplus and one for the silu gate) per second, against the
-    SFU peak."""
-    per_elem = spec.N + (1 if spec.delta_softplus else 0) + (1 if spec.gate else 0)
+def exps_per_element(spec):
+    """SFU operations the method needs per element: N exponentials for
+    exp(dt A), two for softplus (e^v and the log) and two for the silu gate
+    (e^-z and the reciprocal)."""
+    return spec.N + (2 if spec.delta_softplus else 0) + (2 if spec.gate else 0)
+
+
+def fp32_ops_per_element(spec):
+    """FP32 operations the method needs per element: per state dt*A, (dt x)*B,
+    the h update and the C.h readout (4N), plus dt*x, the D skip and the gate."""
+    return 4 * spec.N + 3
+
+
+def time_floors(spec, alg_bytes, hbm_gbs):
+    """Lower bounds on one call (us) from each unit: HBM bytes, SFU exps, FP32 ops."""
+    sfu = spec.elements * exps_per_element(spec) / (EX2_PER_SM_CLK * SMS * SM_MAX_MHZ * 1e6)
+    fp32 = spec.elements * fp32_ops_per_element(spec) / (FP32_PER_SM_CLK * SMS * SM_MAX_MHZ * 1e6)
+    return {"hbm": alg_bytes / (hbm_gbs * 1e9) * 1e6, "sfu": sfu * 1e6, "fp32": fp32 * 1e6}
+
+
+def alu_roofline(spec, per_call_s, plan):
+    """The binding roofline of the scan: the SFU operations the method needs
+    per second against the SFU peak (the largest of the three floors)."""
+    per_elem = exps_per_element(spec)
     achieved = spec.elements * per_elem / per_call_s / 1e12
     peak = EX2_PER_SM_CLK * SMS * SM_MAX_MHZ * 1e6 / 1e12
-    return {"bound": "alu", "unit": "T exp/s", "achieved": achieved, "peak": peak,
-            "frac": achieved / peak, "exp_per_element": per_elem,
+    return {"bound": "alu", "unit": "T SFU op/s", "achieved": achieved, "peak": peak,
+            "frac": achieved / peak, "traffic": None, "sfu_ops_per_element": per_elem,
+            "kernel": "scan_kernel, one ssm_selective_scan_fwd call (%d launch%s)"
+                      % (plan["kernels"], "es" if plan["kernels"] > 1 else ""),
             "peak_basis": "measured ex2 rate 29.1 per SM per clock x 148 SMs x 2032 MHz"}
 
 
@@ -656,7 +679,8 @@ def main(argv=None):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f32", "io_dtype": spec.io, "data": "synthetic",
                 "config": workload_config(spec), "gbps": res["gbps"],
-                "roofline": res["roofline"], "alu_roofline": res["alu_roofline"], "e2e": res["e2e"],
+                "roofline": res["roofline"], "hbm_roofline": res["hbm_roofline"],
+                "floors_us": res["floors_us"], "e2e": res["e2e"],
                 "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
                 "plan": res["plan"], "check": res["check"]}
         if "decode" in res:
