@@ -17,7 +17,8 @@ What it computes (page title, section):
     Algorithm" and "Mamba's Innovation: Selection": A of shape [D, N],
     delta = softplus(delta), gate y * silu(z).
   * "State-space models (Mamba, S4)", "Training vs Inference Modes": the
-    O(1)-per-token recurrent step on a cached state.
+    O(1)-per-token recurrent step on a cached state, and training through the
+    scan (its gradients: ``selective_scan_bwd``).
 """
 from __future__ import annotations
 
@@ -72,6 +73,9 @@ def _bind(lib):
         [_i64] * 3 + [_dp] * 9 + [ctypes.c_int] + [_dp])
     lib.oracle_causal_conv1d_silu.restype = None
     lib.oracle_causal_conv1d_silu.argtypes = [_i64] * 4 + [_dp] * 4
+    lib.oracle_selective_scan_bwd.restype = ctypes.c_int
+    lib.oracle_selective_scan_bwd.argtypes = (
+        [_i64] * 4 + [_dp] * 8 + [ctypes.c_int] + [_dp] * 12 + [ctypes.c_int])
     return lib
 
 
@@ -186,6 +190,43 @@ def _conv_method(self, x, w, bias=None):
 Oracle.causal_conv1d_silu = _conv_method
 
 
+def _bwd_method(self, x, delta, A, B, C, dout, D=None, z=None, delta_bias=None,
+                delta_softplus=False, h0=None, dh_final=None, nthreads=None):
+    """Gradients of the selective scan for the loss sum(dout * out) (+ sum(dh_final
+    * final_state)). Returns a dict of float64 arrays: dx, ddelta, dz (None
+    without z) [batch, L, dim]; dA [dim, N]; dB, dC [batch, L, N]; dD, ddelta_bias
+    [dim] (None without D / delta_bias); dh0 [batch, dim, N]."""
+    x = _f64(x)
+    batch, L, dim = x.shape
+    A = _f64(A)
+    N = A.shape[1]
+    delta = _f64(delta, (batch, L, dim))
+    A = _f64(A, (dim, N))
+    B, C = _f64(B, (batch, L, N)), _f64(C, (batch, L, N))
+    D, z = _f64(D, (dim,)), _f64(z, (batch, L, dim))
+    delta_bias = _f64(delta_bias, (dim,))
+    h0, dh_final = _f64(h0, (batch, dim, N)), _f64(dh_final, (batch, dim, N))
+    dout = _f64(dout, (batch, L, dim))
+    g = {"dx": np.zeros((batch, L, dim)), "ddelta": np.zeros((batch, L, dim)),
+         "dA": np.zeros((dim, N)), "dB": np.zeros((batch, L, N)), "dC": np.zeros((batch, L, N)),
+         "dD": np.zeros(dim) if D is not None else None,
+         "dz": np.zeros((batch, L, dim)) if z is not None else None,
+         "ddelta_bias": np.zeros(dim) if delta_bias is not None else None,
+         "dh0": np.zeros((batch, dim, N))}
+    rc = self._lib.oracle_selective_scan_bwd(
+        batch, L, dim, N, _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+        _ptr(delta_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(dout), _ptr(dh_final),
+        _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+        _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]),
+        int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("oracle_selective_scan_bwd failed (%d)" % rc)
+    return g
+
+
+Oracle.selective_scan_bwd = _bwd_method
+
+
 def default() -> Oracle:
     """The oracle built from ssm_oracle.c (compiled on first use)."""
     global _default
@@ -217,3 +258,7 @@ def state_update(*a, **k):
 
 def causal_conv1d_silu(*a, **k):
     return default().causal_conv1d_silu(*a, **k)
+
+
+def selective_scan_bwd(*a, **k):
+    return default().selective_scan_bwd(*a, **k)

@@ -228,3 +228,187 @@ void oracle_causal_conv1d_silu(int64_t batch, int64_t L, int64_t dim, int64_t K,
                 u[(b * L + t) * dim + d] = oracle_silu(pre);
             }
 }
+
+/*
+ * Gradients of the selective scan (the reverse-mode derivative of
+ * oracle_selective_scan, from the chain rule on its loop; the pages ask that
+ * gradients flow through the discretization: "State Space Models -- Mamba, S4,
+ * and Beyond", section "Verification Checklist", and "State-space models
+ * (Mamba, S4)", section "Training vs Inference Modes": training runs the scan
+ * in parallel and backpropagates through it).
+ *
+ * Given dout = dLoss/dout [batch, L, dim] and, optionally, dh_final =
+ * dLoss/dfinal_state [batch, dim, N], with per token (one channel)
+ *   v = delta + bias,  dt = softplus(v) or v,  a[n] = exp(dt A[n]),
+ *   h[n] = a[n] hp[n] + dt x B[n]   (hp: the state before the token),
+ *   y = sum_n C[n] h[n] + D x,      out = y * silu(z)  (or y),
+ * the reverse sweep carries G[n] = dLoss/dh[n] from the last token back:
+ *   dy     = dout * silu(z)                      dz = dout * y * silu'(z)
+ *   G[n]   = a_next[n] G_next[n] + dy C[n]       (a_next G_next = dh_final at the end)
+ *   dC[n] += dy h[n]          dB[n] += G[n] dt x        dx = dy D + dt sum_n G[n] B[n]
+ *   ddt    = sum_n G[n] (x B[n] + A[n] a[n] hp[n])     dA[n] += G[n] dt a[n] hp[n]
+ *   ddelta = ddt * sigmoid(v) (softplus) or ddt;  dbias += ddelta;  dD += dy x
+ *   dh0[n] = a_0[n] G_0[n]
+ * dB and dC sum over channels d (B, C are shared by all channels); dA, dD and
+ * dbias sum over batch rows and tokens. Optional outputs may be NULL; dD, dz,
+ * dbias are only defined when D, z, delta_bias were given.
+ *
+ * Channels are split across threads; each thread sums its own dA, dD, dbias,
+ * dB and dC and the partial sums are added in thread order (deterministic for a
+ * given thread count). Returns 0, or -1 on bad arguments / allocation failure.
+ */
+typedef struct {
+    int64_t batch, L, dim, N;
+    const double *x, *delta, *A, *B, *C, *D, *z, *delta_bias, *h0, *dout, *dh_final;
+    int delta_softplus;
+    double *dx, *ddelta, *dz, *dh0;               /* per channel: written directly */
+    double *dA, *dB, *dC, *dD, *dbias;            /* this thread's partial sums */
+    int64_t chan_begin, chan_end;
+    int failed;
+} bwd_job;
+
+static double oracle_sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
+
+static void bwd_channel(bwd_job* j, int64_t b, int64_t d, double* hp, double* dtv, double* yv,
+                        double* G)
+{
+    const int64_t L = j->L, dim = j->dim, N = j->N;
+    const double* Ad = j->A + d * N;                              /* A[d, :] */
+    const double* h0c = j->h0 ? j->h0 + (b * dim + d) * N : NULL; /* h0[b, d, :] */
+    const double bias = j->delta_bias ? j->delta_bias[d] : 0.0;
+    /* forward sweep: keep the state before every token, dt and y (pre-gate) */
+    double* h = hp + L * N;   /* running state (the slot after the last token) */
+    for (int64_t n = 0; n < N; ++n) h[n] = h0c ? h0c[n] : 0.0;
+    for (int64_t t = 0; t < L; ++t) {
+        const int64_t e = (b * L + t) * dim + d;
+        const double* Bt = j->B + (b * L + t) * N;
+        const double* Ct = j->C + (b * L + t) * N;
+        const double v = j->delta[e] + bias;
+        const double dt = j->delta_softplus ? oracle_softplus(v) : v;
+        dtv[t] = dt;
+        double acc = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            hp[t * N + n] = h[n];
+            h[n] = exp(dt * Ad[n]) * h[n] + dt * Bt[n] * j->x[e];
+            acc += Ct[n] * h[n];
+        }
+        yv[t] = acc + (j->D ? j->D[d] * j->x[e] : 0.0);
+    }
+    /* reverse sweep */
+    for (int64_t n = 0; n < N; ++n) G[n] = j->dh_final ? j->dh_final[(b * dim + d) * N + n] : 0.0;
+    for (int64_t t = L - 1; t >= 0; --t) {
+        const int64_t e = (b * L + t) * dim + d;
+        const double* Bt = j->B + (b * L + t) * N;
+        const double* Ct = j->C + (b * L + t) * N;
+        const double xv = j->x[e], dt = dtv[t];
+        double dy = j->dout[e];
+        if (j->z) {
+            const double s = oracle_sigmoid(j->z[e]);
+            if (j->dz) j->dz[e] = j->dout[e] * yv[t] * s * (1.0 + j->z[e] * (1.0 - s));
+            dy *= j->z[e] * s;
+        }
+        double dx = j->D ? dy * j->D[d] : 0.0;
+        if (j->D) j->dD[d] += dy * xv;
+        double ddt = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            const double a = exp(dt * Ad[n]);
+            const double hprev = hp[t * N + n];
+            const double ht = a * hprev + dt * Bt[n] * xv;
+            const double g = G[n] + dy * Ct[n];           /* dLoss/dh_t */
+            j->dC[(b * L + t) * N + n] += dy * ht;
+            j->dB[(b * L + t) * N + n] += g * dt * xv;
+            dx += g * dt * Bt[n];
+            ddt += g * (xv * Bt[n] + Ad[n] * a * hprev);
+            j->dA[d * N + n] += g * dt * a * hprev;
+            G[n] = a * g;                                  /* carried to the token before */
+        }
+        const double dd = j->delta_softplus ? ddt * oracle_sigmoid(j->delta[e] + bias) : ddt;
+        if (j->ddelta) j->ddelta[e] = dd;
+        if (j->delta_bias) j->dbias[d] += dd;
+        if (j->dx) j->dx[e] = dx;
+    }
+    if (j->dh0)
+        for (int64_t n = 0; n < N; ++n) j->dh0[(b * dim + d) * N + n] = G[n];
+}
+
+static void* bwd_worker(void* arg)
+{
+    bwd_job* j = (bwd_job*)arg;
+    const int64_t L = j->L, N = j->N;
+    double* hp = (double*)malloc((size_t)((L + 1) * N + 2 * L + N) * sizeof(double));
+    if (!hp) { j->failed = 1; return NULL; }
+    double* dtv = hp + (L + 1) * N;
+    double* yv = dtv + L;
+    double* G = yv + L;
+    for (int64_t c = j->chan_begin; c < j->chan_end; ++c)
+        bwd_channel(j, c / j->dim, c % j->dim, hp, dtv, yv, G);
+    free(hp);
+    return NULL;
+}
+
+int oracle_selective_scan_bwd(int64_t batch, int64_t L, int64_t dim, int64_t N,
+                              const double* x, const double* delta, const double* A,
+                              const double* B, const double* C, const double* D,
+                              const double* z, const double* delta_bias, int delta_softplus,
+                              const double* h0, const double* dout, const double* dh_final,
+                              double* dx, double* ddelta, double* dA, double* dB, double* dC,
+                              double* dD, double* dz, double* ddelta_bias, double* dh0,
+                              int nthreads)
+{
+    if (batch < 0 || L < 0 || dim < 0 || N <= 0) return -1;
+    if (!x || !delta || !A || !B || !C || !dout) return -1;
+    const int64_t nchan = batch * dim;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 64) nthreads = 64;
+    if ((int64_t)nthreads > nchan) nthreads = nchan > 0 ? (int)nchan : 1;
+    const size_t nA = (size_t)(dim * N), nBC = (size_t)(batch * L * N), nd = (size_t)dim;
+    const size_t per = nA + 2 * nBC + 2 * nd;   /* dA, dB, dC, dD, dbias */
+    double* part = (double*)calloc((size_t)nthreads * per, sizeof(double));
+    if (!part) return -1;
+
+    bwd_job jobs[64];
+    pthread_t tid[64];
+    for (int i = 0; i < nthreads; ++i) {
+        bwd_job* j = &jobs[i];
+        j->batch = batch; j->L = L; j->dim = dim; j->N = N;
+        j->x = x; j->delta = delta; j->A = A; j->B = B; j->C = C; j->D = D; j->z = z;
+        j->delta_bias = delta_bias; j->h0 = h0; j->dout = dout; j->dh_final = dh_final;
+        j->delta_softplus = delta_softplus;
+        j->dx = dx; j->ddelta = ddelta; j->dz = dz; j->dh0 = dh0;
+        double* p = part + (size_t)i * per;
+        j->dA = p; j->dB = p + nA; j->dC = p + nA + nBC; j->dD = p + nA + 2 * nBC;
+        j->dbias = p + nA + 2 * nBC + nd;
+        j->chan_begin = nchan * i / nthreads;
+        j->chan_end = nchan * (i + 1) / nthreads;
+        j->failed = 0;
+    }
+    int rc = 0;
+    if (nthreads == 1) {
+        bwd_worker(&jobs[0]);
+    } else {
+        int started = 0;
+        for (int i = 0; i < nthreads; ++i) {
+            if (pthread_create(&tid[i], NULL, bwd_worker, &jobs[i]) != 0) { rc = -1; break; }
+            ++started;
+        }
+        for (int i = 0; i < started; ++i) pthread_join(tid[i], NULL);
+    }
+    for (int i = 0; i < nthreads; ++i)
+        if (jobs[i].failed) rc = -1;
+    /* partial sums, added in thread order */
+    if (dA) for (size_t k = 0; k < nA; ++k) dA[k] = 0.0;
+    if (dB) for (size_t k = 0; k < nBC; ++k) dB[k] = 0.0;
+    if (dC) for (size_t k = 0; k < nBC; ++k) dC[k] = 0.0;
+    if (dD) for (size_t k = 0; k < nd; ++k) dD[k] = 0.0;
+    if (ddelta_bias) for (size_t k = 0; k < nd; ++k) ddelta_bias[k] = 0.0;
+    for (int i = 0; i < nthreads; ++i) {
+        const bwd_job* j = &jobs[i];
+        if (dA) for (size_t k = 0; k < nA; ++k) dA[k] += j->dA[k];
+        if (dB) for (size_t k = 0; k < nBC; ++k) dB[k] += j->dB[k];
+        if (dC) for (size_t k = 0; k < nBC; ++k) dC[k] += j->dC[k];
+        if (dD && D) for (size_t k = 0; k < nd; ++k) dD[k] += j->dD[k];
+        if (ddelta_bias && delta_bias) for (size_t k = 0; k < nd; ++k) ddelta_bias[k] += j->dbias[k];
+    }
+    free(part);
+    return rc;
+}

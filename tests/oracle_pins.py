@@ -17,6 +17,9 @@ Sources (page title, section):
     "Verification Checklist" (recurrent inference must reproduce the scan).
   * "Mamba: State Space Models Challenge Transformers", "Mamba's Innovation:
     Selection" (softplus on delta, output gate y * silu(z)).
+  * The gradients of the scan (training through it: "State-space models
+    (Mamba, S4)", "Training vs Inference Modes") are pinned to finite
+    differences of the forward and to PyTorch autograd through a plain loop.
 """
 from __future__ import annotations
 
@@ -390,7 +393,149 @@ def pin_conv_causal(orc, seed=23):
     assert np.all(moved[0, 12:16] != base[0, 12:16]), "conv misses a tap"
 
 
+# --------------------------------------------------------------------------
+# gradients (the backward of the scan)
+# --------------------------------------------------------------------------
+def _bwd_case(r, batch, L, dim, N, softplus, full):
+    """A small random problem; full=True gives every optional input."""
+    c = {"x": r.standard_normal((batch, L, dim)),
+         "delta": (r.standard_normal((batch, L, dim)) * 0.5 if softplus
+                   else r.uniform(0.05, 0.5, (batch, L, dim))),
+         "A": -np.exp(r.standard_normal((dim, N)) * 0.5),
+         "B": r.standard_normal((batch, L, N)), "C": r.standard_normal((batch, L, N)),
+         "D": r.uniform(0.5, 1.5, dim) if full else None,
+         "z": r.standard_normal((batch, L, dim)) if full else None,
+         "delta_bias": r.standard_normal(dim) * 0.3 if full else None,
+         "h0": r.standard_normal((batch, dim, N)) if full else None}
+    dout = r.standard_normal((batch, L, dim))
+    dhf = r.standard_normal((batch, dim, N)) if full else None
+    return c, dout, dhf
+
+
+_GRAD_OF = {"x": "dx", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+            "z": "dz", "delta_bias": "ddelta_bias", "h0": "dh0"}
+
+
+def pin_bwd_finite_differences(orc, seed=31):
+    """Every gradient equals the central difference of the oracle's own loss
+    sum(dout * out) + sum(dh_final * final_state) (step 1e-6, truncation error
+    ~1e-12): the backward is the derivative of the forward."""
+    r = _rng(seed)
+    for softplus, full, shape in ((True, True, (2, 5, 3, 4)), (False, False, (1, 6, 2, 1)),
+                                  (True, False, (2, 4, 2, 2))):
+        c, dout, dhf = _bwd_case(r, *shape, softplus, full)
+        g = orc.selective_scan_bwd(c["x"], c["delta"], c["A"], c["B"], c["C"], dout, D=c["D"],
+                                   z=c["z"], delta_bias=c["delta_bias"],
+                                   delta_softplus=softplus, h0=c["h0"], dh_final=dhf)
+
+        def loss(**kw):
+            a = dict(c)
+            a.update(kw)
+            out, fs = orc.selective_scan(a["x"], a["delta"], a["A"], a["B"], a["C"], D=a["D"],
+                                         z=a["z"], delta_bias=a["delta_bias"],
+                                         delta_softplus=softplus, h0=a["h0"])
+            return float((out * dout).sum() + (0.0 if dhf is None else (fs * dhf).sum()))
+
+        eps = 1e-6
+        for name, arr in c.items():
+            if arr is None:
+                continue
+            fd = np.zeros_like(arr)
+            for i in np.ndindex(arr.shape):
+                p, m = arr.copy(), arr.copy()
+                p[i] += eps
+                m[i] -= eps
+                fd[i] = (loss(**{name: p}) - loss(**{name: m})) / (2 * eps)
+            _close(g[_GRAD_OF[name]], fd, 1e-6, 1e-7, "d%s vs finite differences" % name)
+        for name in ("D", "z", "delta_bias"):
+            if c[name] is None:
+                assert g[_GRAD_OF[name]] is None
+
+
+def _torch_scan(x, delta, A, B, C, D, z, bias, softplus, h0):
+    """The scan as a plain PyTorch float64 loop (autograd records it)."""
+    import torch
+    batch, L, dim = x.shape
+    N = A.shape[1]
+    h = h0 if h0 is not None else torch.zeros(batch, dim, N, dtype=torch.float64)
+    ys = []
+    for t in range(L):
+        v = delta[:, t] + (bias if bias is not None else 0.0)
+        dt = torch.nn.functional.softplus(v) if softplus else v
+        h = torch.exp(dt[..., None] * A) * h + (dt * x[:, t])[..., None] * B[:, t, None, :]
+        y = (h * C[:, t, None, :]).sum(-1)
+        if D is not None:
+            y = y + D * x[:, t]
+        if z is not None:
+            y = y * torch.nn.functional.silu(z[:, t])
+        ys.append(y)
+    return torch.stack(ys, 1), h
+
+
+def pin_bwd_autograd(orc, seed=32):
+    """The oracle's gradients equal PyTorch autograd through a plain float64
+    loop of the same recurrence (an independent derivation)."""
+    import torch
+    r = _rng(seed)
+    for softplus, full, shape in ((True, True, (2, 9, 5, 4)), (False, True, (1, 7, 3, 8)),
+                                  (True, False, (3, 6, 2, 2))):
+        c, dout, dhf = _bwd_case(r, *shape, softplus, full)
+        tens = {k: (None if v is None else torch.tensor(v, requires_grad=True))
+                for k, v in c.items()}
+        out, fs = _torch_scan(tens["x"], tens["delta"], tens["A"], tens["B"], tens["C"],
+                              tens["D"], tens["z"], tens["delta_bias"], softplus, tens["h0"])
+        loss = (out * torch.tensor(dout)).sum()
+        if dhf is not None:
+            loss = loss + (fs * torch.tensor(dhf)).sum()
+        loss.backward()
+        g = orc.selective_scan_bwd(c["x"], c["delta"], c["A"], c["B"], c["C"], dout, D=c["D"],
+                                   z=c["z"], delta_bias=c["delta_bias"],
+                                   delta_softplus=softplus, h0=c["h0"], dh_final=dhf)
+        for name, t in tens.items():
+            if t is not None:
+                _close(g[_GRAD_OF[name]], t.grad.numpy(), 1e-10, 1e-12,
+                       "d%s vs autograd" % name)
+
+
+def pin_bwd_channel_sums(orc, seed=33):
+    """dB and dC sum the channels' contributions and dA, dD, dbias sum the
+    batch rows': the gradient of a multi-channel problem equals the sum over
+    one-channel (and one-row) problems; per-channel gradients are unchanged."""
+    r = _rng(seed)
+    c, dout, dhf = _bwd_case(r, 2, 8, 3, 4, True, True)
+    kw = dict(delta_softplus=True, nthreads=1)
+    g = orc.selective_scan_bwd(c["x"], c["delta"], c["A"], c["B"], c["C"], dout, D=c["D"],
+                               z=c["z"], delta_bias=c["delta_bias"], h0=c["h0"], dh_final=dhf,
+                               **kw)
+    dB, dC = np.zeros_like(c["B"]), np.zeros_like(c["C"])
+    for b in range(2):
+        for d in range(3):
+            sl = lambda a: None if a is None else a[b:b + 1, :, d:d + 1]
+            gd = orc.selective_scan_bwd(sl(c["x"]), sl(c["delta"]), c["A"][d:d + 1],
+                                        c["B"][b:b + 1], c["C"][b:b + 1], sl(dout),
+                                        D=c["D"][d:d + 1], z=sl(c["z"]),
+                                        delta_bias=c["delta_bias"][d:d + 1],
+                                        h0=c["h0"][b:b + 1, d:d + 1],
+                                        dh_final=dhf[b:b + 1, d:d + 1], **kw)
+            dB[b] += gd["dB"][0]
+            dC[b] += gd["dC"][0]
+            _close(gd["dx"][0, :, 0], g["dx"][b, :, d], 1e-12, 1e-14, "dx per channel")
+            _close(gd["ddelta"][0, :, 0], g["ddelta"][b, :, d], 1e-12, 1e-14, "ddelta per channel")
+            _close(gd["dh0"][0, 0], g["dh0"][b, d], 1e-12, 1e-14, "dh0 per channel")
+    _close(dB, g["dB"], 1e-12, 1e-14, "dB = sum over channels")
+    _close(dC, g["dC"], 1e-12, 1e-14, "dC = sum over channels")
+    g4 = orc.selective_scan_bwd(c["x"], c["delta"], c["A"], c["B"], c["C"], dout, D=c["D"],
+                                z=c["z"], delta_bias=c["delta_bias"], h0=c["h0"],
+                                dh_final=dhf, delta_softplus=True, nthreads=4)
+    for k in g:
+        if g[k] is not None:
+            _close(g4[k], g[k], 1e-12, 1e-14, "%s, 4 threads vs 1" % k)
+
+
 ALL_PINS = [
+    pin_bwd_finite_differences,
+    pin_bwd_autograd,
+    pin_bwd_channel_sums,
     pin_conv_library,
     pin_conv_taps,
     pin_conv_causal,

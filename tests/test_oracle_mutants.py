@@ -52,6 +52,22 @@ MUTANTS = [
     ("conv_drops_bias", "double pre = bias ? bias[d] : 0.0;", "double pre = 0.0;"),
     ("conv_without_silu", "u[(b * L + t) * dim + d] = oracle_silu(pre);",
      "u[(b * L + t) * dim + d] = pre;"),
+    ("bwd_dC_reads_state_before_update", "j->dC[(b * L + t) * N + n] += dy * ht;",
+     "j->dC[(b * L + t) * N + n] += dy * hprev;"),
+    ("bwd_carry_drops_decay", "G[n] = a * g;", "G[n] = g;"),
+    ("bwd_ddt_drops_input_term", "ddt += g * (xv * Bt[n] + Ad[n] * a * hprev);",
+     "ddt += g * (Ad[n] * a * hprev);"),
+    ("bwd_softplus_derivative_missing",
+     "const double dd = j->delta_softplus ? ddt * oracle_sigmoid(j->delta[e] + bias) : ddt;",
+     "const double dd = ddt;"),
+    ("bwd_silu_derivative_wrong", "s * (1.0 + j->z[e] * (1.0 - s))", "s"),
+    ("bwd_dA_missing_dt", "j->dA[d * N + n] += g * dt * a * hprev;",
+     "j->dA[d * N + n] += g * a * hprev;"),
+    ("bwd_dx_drops_D", "double dx = j->D ? dy * j->D[d] : 0.0;", "double dx = 0.0;"),
+    ("bwd_dB_drops_x", "j->dB[(b * L + t) * N + n] += g * dt * xv;",
+     "j->dB[(b * L + t) * N + n] += g * dt;"),
+    ("bwd_dh0_one_step_late", "j->dh0[(b * dim + d) * N + n] = G[n];",
+     "j->dh0[(b * dim + d) * N + n] = G[n] / exp(dtv[0] * Ad[n]);"),
 ]
 
 
