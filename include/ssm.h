@@ -186,6 +186,58 @@ int ssm_selective_scan_fwd_conv(const void* x, const float* conv_w, const float*
                                 float* final_state, const ssm_dims* dims, ssm_stream_t stream);
 
 /*
+ * Training through the scan ("State-space models (Mamba, S4)", "Training vs
+ * Inference Modes": training runs the scan over whole sequences and
+ * backpropagates through it; "State Space Models -- Mamba, S4, and Beyond",
+ * "Verification Checklist": gradients flow through the discretization).
+ * dstate must be 16 and tile_config_hint 0 or 1 (SSM_ERR_DIMS otherwise).
+ *
+ * ssm_selective_scan_fwd_ckpt -- ssm_selective_scan_fwd_from_state (h0 may be
+ * NULL for zero) that also saves the fp32 state before every 8th token:
+ *   ckpt : [batch, ceil(seqlen / 8), dim, 16] fp32, ckpt[b, m, d, :] = the
+ *          state before token 8m; ssm_scan_checkpoint_bytes(dims) bytes;
+ *          an output (must not overlap anything else)
+ * The backward recomputes the states in between from these.
+ */
+size_t ssm_scan_checkpoint_bytes(const ssm_dims* dims);
+int ssm_selective_scan_fwd_ckpt(const void* x, const void* delta, const float* A, const void* B,
+                                const void* C, const float* D, const void* z,
+                                const float* delta_bias, int delta_softplus, const float* h0,
+                                void* out, float* final_state, float* ckpt, const ssm_dims* dims,
+                                ssm_stream_t stream);
+
+/*
+ * ssm_selective_scan_bwd -- gradients of the scan for a loss L(out,
+ * final_state), given dout = dL/dout and optionally dfinal_state =
+ * dL/dfinal_state. The forward's inputs are passed again, with the ckpt its
+ * checkpointing call wrote (same sizes, dtypes, flags and h0):
+ *   dout                : [batch, seqlen, dim] io dtype (read only)
+ *   dfinal_state        : [batch, dim, 16] fp32 or NULL (zero)
+ *   dx, ddelta          : [batch, seqlen, dim] io dtype; ddelta is the gradient
+ *                         of the delta input (through softplus and the bias)
+ *   dz                  : [batch, seqlen, dim] io dtype, given exactly when z is
+ *                         (SSM_ERR_NULL otherwise)
+ *   dB, dC              : [batch, seqlen, 16] io dtype (summed over channels)
+ *   dA                  : [dim, 16] fp32 (summed over batch rows and tokens)
+ *   dD, ddelta_bias     : [dim] fp32 or NULL (not computed); defined whether or
+ *                         not D / delta_bias were given (their gradient at zero)
+ *   dh0                 : [batch, dim, 16] fp32 or NULL: dL/dh0
+ * Every gradient is written, not accumulated. Outputs must not overlap inputs,
+ * each other or the workspace (SSM_ERR_ALIAS). dims->workspace must hold
+ * ssm_scan_bwd_workspace_bytes(dims) bytes (no initial contents needed). The
+ * sums over channels, rows and chunks are added in a fixed order: results do
+ * not depend on scheduling. seqlen == 0 zeroes dA, dD, ddelta_bias and copies
+ * dfinal_state (or zero) to dh0.
+ */
+size_t ssm_scan_bwd_workspace_bytes(const ssm_dims* dims);
+int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z, const float* delta_bias,
+                           int delta_softplus, const float* ckpt, const void* dout,
+                           const float* dfinal_state, void* dx, void* ddelta, float* dA, void* dB,
+                           void* dC, float* dD, void* dz, float* ddelta_bias, float* dh0,
+                           const ssm_dims* dims, ssm_stream_t stream);
+
+/*
  * ssm_state_update -- one token of recurrent generation on a cached state
  * ("State-space models (Mamba, S4)", "Training vs Inference Modes"). Exactly
  * one step of the scan above, with the state updated in place:

@@ -161,6 +161,42 @@ int check_aligned(const void* const (&ptrs)[K]) {
     return SSM_OK;
 }
 
+// Saved states of the checkpointing forward: the state before every
+// kCkptTokens-th token, [batch][ceil(L / kCkptTokens)][dim][N] fp32.
+size_t ckpt_bytes(const ssm_dims* d) {
+    return size_t(d->batch) * size_t((d->seqlen + ssm::kCkptTokens - 1) / ssm::kCkptTokens) *
+           size_t(d->dim) * size_t(d->dstate) * 4;
+}
+
+// Workspace of the backward: status header, the reverse chunk carries, and the
+// per-CTA shares of the summed gradients.
+struct BwdLayout {
+    size_t off_Q = 0, off_S = 0, off_BC = 0, off_A = 0, off_D = 0, off_bias = 0, bytes = 0;
+};
+
+BwdLayout bwd_layout(const ssm_dims* d, const ssm::ScanPlan& p) {
+    BwdLayout o;
+    const size_t b = size_t(d->batch), L = size_t(d->seqlen), dim = size_t(d->dim);
+    const size_t N = size_t(d->dstate), K = size_t(p.nchunks), tiles = size_t(p.tiles);
+    size_t off = ssm::kWsHeaderBytes;
+    if (K > 1) {
+        o.off_Q = off;
+        off += align256(b * (K - 1) * dim * N * 4);
+        o.off_S = off;
+        off += align256(b * (K - 1) * dim * 4);
+    }
+    o.off_BC = off;
+    off += align256(b * tiles * L * 2 * N * 4);
+    o.off_A = off;
+    off += align256(b * K * dim * N * 4);
+    o.off_D = off;
+    off += align256(b * K * dim * 4);
+    o.off_bias = off;
+    off += align256(b * K * dim * 4);
+    o.bytes = off;
+    return o;
+}
+
 }  // namespace
 
 extern "C" {
@@ -224,9 +260,12 @@ struct ConvIn {
 int scan_impl(const void* x, const void* delta, const float* A, const void* B, const void* C,
               const float* D, const void* z, const float* delta_bias, int delta_softplus,
               const float* h0, void* out, float* final_state, const ssm_dims* dims,
-              ssm_stream_t stream, const ConvIn& cv = ConvIn{}) {
+              ssm_stream_t stream, const ConvIn& cv = ConvIn{}, float* ckpt = nullptr) {
     int rc = check_dims(dims, true);
     if (rc != SSM_OK) return rc;
+    // the checkpointing forward feeds the backward, built for dstate 16 and
+    // tile configuration 0
+    if (ckpt && (dims->dstate != 16 || dims->tile_config_hint > 1)) return SSM_ERR_DIMS;
     // the fused input stage runs tile configuration 0 only
     if (cv.w && dims->dstate == 16 && dims->tile_config_hint > 1) return SSM_ERR_DIMS;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -245,7 +284,7 @@ int scan_impl(const void* x, const void* delta, const float* A, const void* B, c
     if (!x || !delta || !A || !B || !C || !out) return SSM_ERR_NULL;
     {
         const void* const ptrs[] = {x, delta, A, B, C, D, z, delta_bias, h0, out, final_state,
-                                    dims->workspace, cv.w, cv.b};
+                                    dims->workspace, cv.w, cv.b, ckpt};
         rc = check_aligned(ptrs);
         if (rc != SSM_OK) return rc;
     }
@@ -268,7 +307,10 @@ int scan_impl(const void* x, const void* delta, const float* A, const void* B, c
                             {cv.w, size_t(dim) * size_t(cv.k) * 4},
                             {cv.b, size_t(dim) * 4}};
         const Range outs[] = {{out, elems * es},
-                              {final_state, size_t(batch) * dim * N * 4}};
+                              {final_state, size_t(batch) * dim * N * 4},
+                              {ckpt, size_t(batch) * size_t((L + ssm::kCkptTokens - 1) /
+                                                            ssm::kCkptTokens) *
+                                         size_t(dim) * size_t(N) * 4}};
         rc = check_alias(in, outs);
         if (rc != SSM_OK) return rc;
     }
@@ -278,6 +320,7 @@ int scan_impl(const void* x, const void* delta, const float* A, const void* B, c
     a.delta_bias = delta_bias; a.softplus = delta_softplus ? 1 : 0;
     a.h0 = h0;
     a.conv_w = cv.w; a.conv_b = cv.b; a.conv_k = cv.k;
+    a.ckpt = ckpt; a.nckpt = (L + ssm::kCkptTokens - 1) / ssm::kCkptTokens;
     a.out = out; a.final_state = final_state;
     a.batch = batch; a.L = L; a.dim = dim;
     a.chunk_len = p.chunk_len; a.nchunks = p.nchunks; a.tiles = p.tiles;
@@ -325,6 +368,117 @@ int ssm_selective_scan_fwd_conv(const void* x, const float* conv_w, const float*
     cv.w = conv_w; cv.b = conv_b; cv.k = conv_k;
     return scan_impl(x, delta, A, B, C, D, z, delta_bias, delta_softplus, nullptr, out,
                      final_state, dims, stream, cv);
+}
+
+size_t ssm_scan_checkpoint_bytes(const ssm_dims* dims) {
+    if (check_dims(dims, true) != SSM_OK) return 0;
+    if (dims->batch == 0 || dims->dim == 0 || dims->seqlen == 0) return 0;
+    return ckpt_bytes(dims);
+}
+
+int ssm_selective_scan_fwd_ckpt(const void* x, const void* delta, const float* A, const void* B,
+                                const void* C, const float* D, const void* z,
+                                const float* delta_bias, int delta_softplus, const float* h0,
+                                void* out, float* final_state, float* ckpt, const ssm_dims* dims,
+                                ssm_stream_t stream) {
+    if (!dims) return SSM_ERR_NULL;
+    if (dims->dstate != 16 || dims->tile_config_hint > 1) return SSM_ERR_DIMS;
+    if (!ckpt && dims->batch > 0 && dims->dim > 0 && dims->seqlen > 0) return SSM_ERR_NULL;
+    return scan_impl(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, out, final_state,
+                     dims, stream, ConvIn{}, ckpt);
+}
+
+size_t ssm_scan_bwd_workspace_bytes(const ssm_dims* dims) {
+    if (check_dims(dims, true) != SSM_OK) return 0;
+    if (dims->dstate != 16 || dims->tile_config_hint > 1) return 0;
+    ssm::ScanPlan p;
+    if (make_plan(dims, &p) != SSM_OK || p.nchunks == 0) return 0;
+    return bwd_layout(dims, p).bytes;
+}
+
+int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z, const float* delta_bias,
+                           int delta_softplus, const float* ckpt, const void* dout,
+                           const float* dfinal_state, void* dx, void* ddelta, float* dA, void* dB,
+                           void* dC, float* dD, void* dz, float* ddelta_bias, float* dh0,
+                           const ssm_dims* dims, ssm_stream_t stream) {
+    int rc = check_dims(dims, true);
+    if (rc != SSM_OK) return rc;
+    if (dims->dstate != 16 || dims->tile_config_hint > 1) return SSM_ERR_DIMS;
+    if (dims->batch == 0 || dims->dim == 0) return SSM_OK;
+    if ((z == nullptr) != (dz == nullptr) && dims->seqlen > 0) return SSM_ERR_NULL;
+    if (!dA) return SSM_ERR_NULL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t batch = dims->batch, L = dims->seqlen, dim = dims->dim, N = dims->dstate;
+    const size_t state_bytes = size_t(batch) * size_t(dim) * size_t(N) * 4;
+    if (L == 0) {
+        // no token: the parameters get no gradient and dLoss/dh0 = dLoss/dfinal_state
+        const void* const ptrs[] = {dA, dD, ddelta_bias, dh0, dfinal_state};
+        rc = check_aligned(ptrs);
+        if (rc != SSM_OK) return rc;
+        if (dh0 && dfinal_state && overlap({dh0, state_bytes}, {dfinal_state, state_bytes}))
+            return SSM_ERR_ALIAS;
+        rc = set_cuda(cudaMemsetAsync(dA, 0, size_t(dim) * size_t(N) * 4, s));
+        if (rc == SSM_OK && dD) rc = set_cuda(cudaMemsetAsync(dD, 0, size_t(dim) * 4, s));
+        if (rc == SSM_OK && ddelta_bias)
+            rc = set_cuda(cudaMemsetAsync(ddelta_bias, 0, size_t(dim) * 4, s));
+        if (rc == SSM_OK && dh0)
+            rc = set_cuda(dfinal_state ? cudaMemcpyAsync(dh0, dfinal_state, state_bytes,
+                                                         cudaMemcpyDeviceToDevice, s)
+                                       : cudaMemsetAsync(dh0, 0, state_bytes, s));
+        return rc;
+    }
+    if (!x || !delta || !A || !B || !C || !ckpt || !dout || !dx || !ddelta || !dB || !dC)
+        return SSM_ERR_NULL;
+    {
+        const void* const ptrs[] = {x,  delta,  A,  B,  C,  D,  z,  delta_bias, ckpt, dout,
+                                    dfinal_state, dx, ddelta, dA, dB, dC, dD, dz, ddelta_bias,
+                                    dh0, dims->workspace};
+        rc = check_aligned(ptrs);
+        if (rc != SSM_OK) return rc;
+    }
+    ssm::ScanPlan p;
+    rc = make_plan(dims, &p);
+    if (rc != SSM_OK) return rc;
+    const BwdLayout lay = bwd_layout(dims, p);
+    if (!dims->workspace || dims->workspace_bytes < lay.bytes) return SSM_ERR_WORKSPACE;
+    {
+        const size_t es = io_size(dims->io_dtype);
+        const size_t elems = size_t(batch) * size_t(L) * size_t(dim);
+        const size_t rows = size_t(batch) * size_t(L) * size_t(N);
+        const Range in[] = {{x, elems * es},       {delta, elems * es},
+                            {z, elems * es},       {dout, elems * es},
+                            {B, rows * es},        {C, rows * es},
+                            {A, size_t(dim) * N * 4}, {D, size_t(dim) * 4},
+                            {delta_bias, size_t(dim) * 4}, {ckpt, ckpt_bytes(dims)},
+                            {dfinal_state, state_bytes}};
+        const Range outs[] = {{dx, elems * es},     {ddelta, elems * es},
+                              {dz, elems * es},     {dB, rows * es},
+                              {dC, rows * es},      {dA, size_t(dim) * N * 4},
+                              {dD, size_t(dim) * 4}, {ddelta_bias, size_t(dim) * 4},
+                              {dh0, state_bytes},   {dims->workspace, lay.bytes}};
+        rc = check_alias(in, outs);
+        if (rc != SSM_OK) return rc;
+    }
+    char* ws = static_cast<char*>(dims->workspace);
+    ssm::BwdArgs a{};
+    a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
+    a.delta_bias = delta_bias; a.softplus = delta_softplus ? 1 : 0;
+    a.ckpt = ckpt; a.nckpt = (L + ssm::kCkptTokens - 1) / ssm::kCkptTokens;
+    a.dout = dout; a.dfinal = dfinal_state;
+    a.dx = dx; a.ddelta = ddelta; a.dz = dz; a.dh0 = dh0;
+    a.dB = dB; a.dC = dC; a.dA = dA; a.dD = dD; a.dbias = ddelta_bias;
+    a.batch = batch; a.L = L; a.dim = dim;
+    a.chunk_len = p.chunk_len; a.nchunks = p.nchunks; a.tiles = p.tiles;
+    if (p.nchunks > 1) {
+        a.wsQ = reinterpret_cast<float*>(ws + lay.off_Q);
+        a.wsS = reinterpret_cast<float*>(ws + lay.off_S);
+    }
+    a.pBC = reinterpret_cast<float*>(ws + lay.off_BC);
+    a.pA = reinterpret_cast<float*>(ws + lay.off_A);
+    a.pD = reinterpret_cast<float*>(ws + lay.off_D);
+    a.pbias = reinterpret_cast<float*>(ws + lay.off_bias);
+    return set_cuda(ssm::launch_scan_bwd(a, dims->io_dtype, s));
 }
 
 int ssm_causal_conv1d_silu(const void* x, const float* conv_w, const float* conv_b, int conv_k,

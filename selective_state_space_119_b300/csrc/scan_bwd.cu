@@ -1,0 +1,501 @@
+// scan_bwd.cu -- gradients of the selective scan (the backward of training
+// through it).
+//
+// "State-space models (Mamba, S4)", "Training vs Inference Modes": training
+// runs the scan over whole sequences and backpropagates through it; "State
+// Space Models -- Mamba, S4, and Beyond", "Verification Checklist": gradients
+// flow through the discretization. For one channel, with per token
+//   dt = softplus(delta + bias) (or delta + bias), a[n] = exp(dt A[n]),
+//   h[n] = a[n] hp[n] + dt x B[n],  y = C . h + D x,  out = y silu(z),
+// the reverse sweep carries Q[n] = a_{t+1}[n] dLoss/dh_{t+1}[n] from the end:
+//   dy = dout silu(z),  g[n] = Q[n] + dy C[n]  (= dLoss/dh_t[n]),  Q[n] <- a[n] g[n]
+//   dC[n] += dy h[n],   dB[n] += g[n] dt x,    dA[n] += g[n] dt (a[n] hp[n])
+//   dx = dt sum_n g[n] B[n] + dy D,  ddt = x sum_n g[n] B[n] + sum_n g[n] A[n] (a[n] hp[n])
+//   ddelta = ddt sigmoid(delta + bias) (softplus) or ddt,  dz = dout y silu'(z)
+// where a[n] hp[n] = h[n] - dt x B[n] needs no second state.
+//
+// The states come from a checkpointing forward (the state before every 8th
+// token, fp32). Per 8-token block, in reverse order, a CTA reloads the block's
+// first state, recomputes the block's 8 states forward into shared memory,
+// then runs the reverse sweep over them. The sequence is split into the same
+// L-chunks as the forward: a first pass computes, for every chunk but the
+// first, its reverse carry from zero (Q at its first token) and its sum of dt;
+// each chunk of the gradient pass composes the carries of the chunks to its
+// right, Q <- exp(A S_i) Q + Q_i, starting from dLoss/dfinal_state.
+//
+// Layout of the lanes is the forward's: lanes 2p, 2p+1 own channels 2p, 2p+1
+// of a 128-channel tile; lane j of the pair holds states [8j, 8j+8) of both
+// (slot 0 = own channel, slot 1 = partner). dB and dC sum over channels: per
+// token each lane holds 16 partial sums (its 8 states of dB and of dC, both
+// channels added), a 4-step reduce-scatter over the 16 lanes of equal j leaves
+// one warp sum per lane, the 4 warps are added in shared memory, and every
+// 128-channel tile writes its sums to a workspace that a last kernel adds up
+// (no atomics: the result does not depend on scheduling). dA, dD and dbias are
+// summed per CTA in registers and added the same way.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+
+namespace ssm {
+namespace {
+
+constexpr int kBwdWarps = 4;
+constexpr int kBwdThreads = 32 * kBwdWarps;
+constexpr int kBwdChannels = kBwdThreads;      // one channel per lane
+constexpr int TB = kCkptTokens;                // tokens per block (8)
+constexpr float kLn2f = 0.6931471805599453f;
+
+// Shared memory of one CTA (N = 16).
+template <typename T, int N>
+struct BwdSmem {
+    static constexpr int VEC = 16 / sizeof(T);            // elements per 16-byte chunk
+    static constexpr int ROWC = kBwdChannels / VEC;       // chunks per token row of a tile
+    static constexpr int TILE = TB * kBwdChannels;        // elements of one [TB][128] tile
+    // staged inputs of one block: x, delta, z, dout tiles, then B and C rows
+    static constexpr int kX = 0, kDelta = TILE, kZ = 2 * TILE, kDout = 3 * TILE;
+    static constexpr int kB = 4 * TILE, kC = 4 * TILE + TB * N;
+    static constexpr int IN_ELEMS = 4 * TILE + 2 * TB * N;
+    // byte offsets
+    static constexpr int oIn = 0;
+    static constexpr int oBC = (IN_ELEMS * int(sizeof(T)) + 127) & ~127;  // fp32 [TB][2N]
+    static constexpr int oHist = oBC + TB * 2 * N * 4;                    // float4 [TB][N/4][128]
+    static constexpr int oRed = oHist + TB * (N / 4) * kBwdThreads * 16;   // fp32 [4][TB][32]
+    static constexpr int oDt = oRed + kBwdWarps * TB * 32 * 4;             // float2 [TB][128]
+    static constexpr int oY = oDt + TB * kBwdThreads * 8;                  // fp32 [TB][128]
+    static constexpr int kBytes = oY + TB * kBwdThreads * 4;
+    static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
+    static_assert(N == 16, "the backward is built for dstate 16");
+};
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// The two channels (2p, 2p+1) of one token row in shared memory.
+__device__ __forceinline__ float2 lds_pair(const float* p) {
+    return *reinterpret_cast<const float2*>(p);
+}
+__device__ __forceinline__ float2 lds_pair(const __nv_bfloat16* p) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ void st_io(float* p, float v) { *p = v; }
+__device__ __forceinline__ void st_io(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// One block's inputs into shared memory: the [TB x 128] tiles of x, delta,
+// (z,) dout and the TB rows of B and C, as 16-byte loads spread over the CTA
+// (rows past the end of the sequence and channels past dim read as zero).
+template <typename T, int N, bool GATE, int MODE>
+__device__ __forceinline__ void stage_block(const BwdArgs& a, T* in, int64_t b, int64_t dbase,
+                                            int64_t u0, int cnt) {
+    using Sm = BwdSmem<T, N>;
+    constexpr int VEC = Sm::VEC, ROWC = Sm::ROWC;
+    constexpr int NTILES = 4;
+    constexpr int TILE_CHUNKS = TB * ROWC;
+    constexpr int BC_CHUNKS = TB * N / VEC;                  // per B or C
+    constexpr int TOTAL = NTILES * TILE_CHUNKS + 2 * BC_CHUNKS;
+    for (int i = threadIdx.x; i < TOTAL; i += kBwdThreads) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        T* dst;
+        if (i < NTILES * TILE_CHUNKS) {
+            const int which = i / TILE_CHUNKS, r = i % TILE_CHUNKS;
+            const int tt = r / ROWC, c = (r % ROWC) * VEC;
+            dst = in + which * Sm::TILE + tt * kBwdChannels + c;
+            // the state-carry pass reads no x; z only with the gate
+            const bool used = (MODE == 1 || which != 0) && (GATE || which != 2);
+            if (used && tt < cnt && dbase + c < a.dim) {
+                const void* base = which == 0 ? a.x : which == 1 ? a.delta : which == 2 ? a.z : a.dout;
+                v = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(base) +
+                                                        ((b * a.L + u0 + tt) * a.dim + dbase + c)));
+            }
+        } else {
+            const int r = i - NTILES * TILE_CHUNKS;
+            const int which = r / BC_CHUNKS, e = (r % BC_CHUNKS) * VEC;
+            const int tt = e / N, n = e % N;
+            dst = in + (which ? Sm::kC : Sm::kB) + e;
+            const T* src = static_cast<const T*>(which ? a.C : a.B);
+            if (tt < cnt && (MODE == 1 || which == 1))   // the carry pass needs no B
+                v = __ldg(reinterpret_cast<const uint4*>(src + (b * a.L + u0 + tt) * N + n));
+        }
+        *reinterpret_cast<uint4*>(dst) = v;
+    }
+}
+
+// MODE 0: reverse carry of chunks 1 .. nchunks-1 from zero (Q at the chunk's
+// first token, and its sum of dt). MODE 1: the gradients of one chunk.
+template <typename T, int N, bool SOFTPLUS, bool GATE, int MODE>
+__global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs a) {
+    using Sm = BwdSmem<T, N>;
+    constexpr int NS = 2, SPL = N / NS;
+    extern __shared__ __align__(128) unsigned char smem[];
+    T* in = reinterpret_cast<T*>(smem + Sm::oIn);
+    float* bcs = reinterpret_cast<float*>(smem + Sm::oBC);
+    float4* hist = reinterpret_cast<float4*>(smem + Sm::oHist);
+    float* red = reinterpret_cast<float*>(smem + Sm::oRed);
+    float2* dts = reinterpret_cast<float2*>(smem + Sm::oDt);   // dt of both slots per token
+    float* ys = reinterpret_cast<float*>(smem + Sm::oY);       // y (before the gate), own channel
+
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int64_t lin = blockIdx.x;   // chunk-major: ((k * batch) + b) * tiles + tile
+    const int64_t tile = lin % a.tiles;
+    const int64_t b = (lin / a.tiles) % a.batch;
+    const int64_t k = lin / (a.tiles * a.batch) + (MODE == 0 ? 1 : 0);
+    const int64_t t_begin = k * a.chunk_len;
+    const int64_t t_end = min(a.L, t_begin + a.chunk_len);
+    const int nblk = static_cast<int>((t_end - t_begin + TB - 1) / TB);
+    const int64_t dbase = tile * kBwdChannels;
+
+    // this lane: own channel d; slot r holds channel (d - j) + (j ^ r)
+    const int j = lane & 1;
+    const int pc = tid & ~1;                      // the pair's first channel in the tile
+    const int64_t d = dbase + tid;
+    const bool ch_ok = d < a.dim;                 // dim is even: pairs are whole
+    const int64_t dsafe = ch_ok ? d : 0;
+    float A2[NS][SPL], Q[NS][SPL], dA[NS][SPL], bias[NS];
+#pragma unroll
+    for (int r = 0; r < NS; ++r) {
+        const int64_t dr = dsafe - j + (j ^ r);
+        bias[r] = (a.delta_bias && ch_ok) ? __ldg(a.delta_bias + dr) : 0.f;
+#pragma unroll
+        for (int q = 0; q < SPL; ++q) {
+            A2[r][q] = ch_ok ? __ldg(a.A + dr * N + j * SPL + q) * kLog2e : 0.f;
+            Q[r][q] = 0.f;
+            dA[r][q] = 0.f;
+        }
+        if (MODE == 1 && ch_ok) {
+            // the carry entering the chunk from the right: dLoss/dfinal_state,
+            // then the chunks nchunks-1 .. k+1 in turn, Q <- exp(A S_i) Q + Q_i
+            if (a.dfinal) {
+#pragma unroll
+                for (int q = 0; q < SPL; ++q) Q[r][q] = a.dfinal[(b * a.dim + dr) * N + j * SPL + q];
+            }
+            for (int64_t i = a.nchunks - 1; i > k; --i) {
+                const int64_t idx = (b * (a.nchunks - 1) + (i - 1)) * a.dim + dr;
+                const float S = a.wsS[idx];
+                const float* Qi = a.wsQ + idx * N + j * SPL;
+#pragma unroll
+                for (int q = 0; q < SPL; ++q) Q[r][q] = fmaf(ex2(A2[r][q] * S), Q[r][q], Qi[q]);
+            }
+        }
+    }
+    const float Dd = (MODE == 1 && a.D && ch_ok) ? __ldg(a.D + dsafe) : 0.f;
+    float dD_acc = 0.f, dbias_acc = 0.f, S_acc = 0.f;
+
+    for (int blk = nblk - 1; blk >= 0; --blk) {
+        const int64_t u0 = t_begin + static_cast<int64_t>(blk) * TB;
+        const int cnt = static_cast<int>(t_end - u0 < TB ? t_end - u0 : TB);
+        __syncthreads();   // the previous block is done with in, bcs and red
+        stage_block<T, N, GATE, MODE>(a, in, b, dbase, u0, cnt);
+        __syncthreads();
+        for (int i = tid; i < TB * 2 * N; i += kBwdThreads) {
+            const int tt = i / (2 * N), c = i % (2 * N);
+            bcs[i] = to_f(in[(c < N ? Sm::kB : Sm::kC - N) + tt * N + c]);
+        }
+        __syncthreads();
+
+        // dt and x of both slots for one token (dt = 0 past the end)
+        auto token = [&](int tt, float (&dt)[NS], float (&xv)[NS]) {
+            const float2 xp = lds_pair(in + Sm::kX + tt * kBwdChannels + pc);
+            const float2 dp = lds_pair(in + Sm::kDelta + tt * kBwdChannels + pc);
+#pragma unroll
+            for (int r = 0; r < NS; ++r) {
+                const bool hi = (j ^ r) != 0;
+                xv[r] = hi ? xp.y : xp.x;
+                float v = (hi ? dp.y : dp.x) + bias[r];
+                if constexpr (SOFTPLUS) v = softplus(v);
+                dt[r] = (tt < cnt && ch_ok) ? v : 0.f;
+            }
+        };
+
+        if constexpr (MODE == 1) {
+            // ---- forward recompute of the block's states from its checkpoint ----
+            float h[NS][SPL];
+#pragma unroll
+            for (int r = 0; r < NS; ++r) {
+                const int64_t dr = dsafe - j + (j ^ r);
+                const float* cp = a.ckpt + ((b * a.nckpt + u0 / TB) * a.dim + dr) * N + j * SPL;
+#pragma unroll
+                for (int q = 0; q < SPL; q += 4) {
+                    const float4 v = ch_ok ? *reinterpret_cast<const float4*>(cp + q)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    h[r][q] = v.x; h[r][q + 1] = v.y; h[r][q + 2] = v.z; h[r][q + 3] = v.w;
+                }
+            }
+#pragma unroll 1
+            for (int tt = 0; tt < TB; ++tt) {
+                float dt[NS], xv[NS], yp[NS];
+                token(tt, dt, xv);
+                dts[tt * kBwdThreads + tid] = make_float2(dt[0], dt[1]);
+                const float* Bt = bcs + tt * 2 * N + j * SPL;
+                const float* Ct = Bt + N;
+#pragma unroll
+                for (int r = 0; r < NS; ++r) {
+                    const float dtx = dt[r] * xv[r];
+                    yp[r] = 0.f;
+#pragma unroll
+                    for (int q = 0; q < SPL; ++q) {
+                        h[r][q] = fmaf(ex2(dt[r] * A2[r][q]), h[r][q], dtx * Bt[q]);
+                        yp[r] = fmaf(Ct[q], h[r][q], yp[r]);
+                    }
+                }
+#pragma unroll
+                for (int c4 = 0; c4 < N / 4; ++c4) {
+                    const int r = c4 / (SPL / 4), q = (c4 % (SPL / 4)) * 4;
+                    hist[(tt * (N / 4) + c4) * kBwdThreads + tid] =
+                        make_float4(h[r][q], h[r][q + 1], h[r][q + 2], h[r][q + 3]);
+                }
+                // the partner's slot 1 is this lane's channel
+                ys[tt * kBwdThreads + tid] =
+                    yp[0] + __shfl_xor_sync(0xffffffffu, yp[1], 1) + Dd * xv[0];
+            }
+        } else {
+#pragma unroll 1
+            for (int tt = 0; tt < TB; ++tt) {
+                float dt[NS], xv[NS];
+                token(tt, dt, xv);
+                dts[tt * kBwdThreads + tid] = make_float2(dt[0], dt[1]);
+            }
+        }
+
+        // ---- reverse sweep over the block ----
+#pragma unroll 1
+        for (int tt = TB - 1; tt >= 0; --tt) {
+            const float* Bt = bcs + tt * 2 * N + j * SPL;
+            const float* Ct = Bt + N;
+            const float2 gp = lds_pair(in + Sm::kDout + tt * kBwdChannels + pc);
+            float zv[NS], dy[NS], dt[NS];
+            float gate_ds = 1.f;   // silu'(z) of the own channel
+            {
+                const float2 dtp = dts[tt * kBwdThreads + tid];
+                dt[0] = dtp.x;
+                dt[1] = dtp.y;
+            }
+#pragma unroll
+            for (int r = 0; r < NS; ++r) dy[r] = ((j ^ r) != 0) ? gp.y : gp.x;
+            if constexpr (GATE) {
+                const float2 zp = lds_pair(in + Sm::kZ + tt * kBwdChannels + pc);
+#pragma unroll
+                for (int r = 0; r < NS; ++r) {
+                    zv[r] = ((j ^ r) != 0) ? zp.y : zp.x;
+                    const float sg = 1.f / (1.f + __expf(-zv[r]));
+                    if (r == 0) gate_ds = sg * fmaf(zv[r], 1.f - sg, 1.f);
+                    dy[r] *= zv[r] * sg;
+                }
+            }
+            if constexpr (MODE == 0) {
+#pragma unroll
+                for (int r = 0; r < NS; ++r)
+#pragma unroll
+                    for (int q = 0; q < SPL; ++q) {
+                        const float g = fmaf(dy[r], Ct[q], Q[r][q]);
+                        Q[r][q] = ex2(dt[r] * A2[r][q]) * g;
+                    }
+                S_acc += dt[0];
+            } else {
+                float xv[NS];
+                {
+                    const float2 xp = lds_pair(in + Sm::kX + tt * kBwdChannels + pc);
+#pragma unroll
+                    for (int r = 0; r < NS; ++r) xv[r] = ((j ^ r) != 0) ? xp.y : xp.x;
+                }
+                float hreg[NS][SPL];
+#pragma unroll
+                for (int c4 = 0; c4 < N / 4; ++c4) {
+                    const int r = c4 / (SPL / 4), q = (c4 % (SPL / 4)) * 4;
+                    const float4 v = hist[(tt * (N / 4) + c4) * kBwdThreads + tid];
+                    hreg[r][q] = v.x; hreg[r][q + 1] = v.y; hreg[r][q + 2] = v.z; hreg[r][q + 3] = v.w;
+                }
+                float dxs[NS], saw[NS], vals[2 * SPL];
+#pragma unroll
+                for (int q = 0; q < 2 * SPL; ++q) vals[q] = 0.f;
+#pragma unroll
+                for (int r = 0; r < NS; ++r) {
+                    const float dtx = dt[r] * xv[r];
+                    dxs[r] = 0.f;
+                    saw[r] = 0.f;
+#pragma unroll
+                    for (int q = 0; q < SPL; ++q) {
+                        const float av = ex2(dt[r] * A2[r][q]);
+                        const float wv = fmaf(-dtx, Bt[q], hreg[r][q]);     // a * h_{t-1}
+                        const float g = fmaf(dy[r], Ct[q], Q[r][q]);        // dLoss/dh_t
+                        dxs[r] = fmaf(g, Bt[q], dxs[r]);
+                        const float gw = g * wv;
+                        saw[r] = fmaf(gw, A2[r][q], saw[r]);
+                        dA[r][q] = fmaf(gw, dt[r], dA[r][q]);
+                        vals[q] = fmaf(g, dtx, vals[q]);                    // dB
+                        vals[SPL + q] = fmaf(dy[r], hreg[r][q], vals[SPL + q]);  // dC
+                        Q[r][q] = av * g;
+                    }
+                }
+                const float dxs_own = dxs[0] + __shfl_xor_sync(0xffffffffu, dxs[1], 1);
+                const float saw_own = saw[0] + __shfl_xor_sync(0xffffffffu, saw[1], 1);
+                if (tt < cnt && ch_ok) {
+                    const int64_t e = (b * a.L + u0 + tt) * a.dim + d;
+                    const float dout_own = (j ? gp.y : gp.x);
+                    st_io(static_cast<T*>(a.dx) + e, fmaf(dt[0], dxs_own, dy[0] * Dd));
+                    const float ddt = fmaf(xv[0], dxs_own, kLn2f * saw_own);
+                    float dd = ddt;
+                    if constexpr (SOFTPLUS) {
+                        const float2 dp = lds_pair(in + Sm::kDelta + tt * kBwdChannels + pc);
+                        const float v = (j ? dp.y : dp.x) + bias[0];
+                        dd = ddt / (1.f + __expf(-v));
+                    }
+                    st_io(static_cast<T*>(a.ddelta) + e, dd);
+                    if constexpr (GATE)
+                        st_io(static_cast<T*>(a.dz) + e, dout_own * ys[tt * kBwdThreads + tid] * gate_ds);
+                    dD_acc = fmaf(dy[0], xv[0], dD_acc);
+                    dbias_acc += dd;
+                }
+                // dB | dC of this token summed over the warp's channels: a
+                // reduce-scatter over the 16 lanes of equal j (xor 16, 8, 4, 2)
+                // leaves lane l with entry ((l >> 1) & 15) of its j
+#pragma unroll
+                for (int m = 16, half = SPL; m >= 2; m >>= 1, half >>= 1) {
+                    const bool up = (lane & m) != 0;
+#pragma unroll
+                    for (int i = 0; i < half; ++i) {
+                        const float send = up ? vals[i] : vals[i + half];
+                        const float keep = up ? vals[i + half] : vals[i];
+                        vals[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                    }
+                }
+                red[(w * TB + tt) * 32 + lane] = vals[0];
+            }
+        }
+        if constexpr (MODE == 1) {
+            __syncthreads();
+            // the 4 warps' sums, written as this tile's share of dB | dC
+            for (int i = tid; i < TB * 32; i += kBwdThreads) {
+                const int tt = i / 32, l = i % 32;
+                if (tt >= cnt) continue;
+                float s = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < kBwdWarps; ++ww) s += red[(ww * TB + tt) * 32 + l];
+                const int idx = (l >> 1) & 15, n = (l & 1) * SPL + (idx % SPL);
+                const int c = idx < SPL ? n : N + n;
+                a.pBC[((b * a.tiles + tile) * a.L + u0 + tt) * (2 * N) + c] = s;
+            }
+        }
+    }
+
+    // ---- per-chunk results ----
+    if (!ch_ok) return;
+#pragma unroll
+    for (int r = 0; r < NS; ++r) {
+        const int64_t dr = dsafe - j + (j ^ r);
+        if constexpr (MODE == 0) {
+            float* dst = a.wsQ + ((b * (a.nchunks - 1) + (k - 1)) * a.dim + dr) * N + j * SPL;
+#pragma unroll
+            for (int q = 0; q < SPL; ++q) dst[q] = Q[r][q];
+        } else {
+            float* dst = a.pA + ((b * a.nchunks + k) * a.dim + dr) * N + j * SPL;
+#pragma unroll
+            for (int q = 0; q < SPL; ++q) dst[q] = dA[r][q];
+            if (k == 0 && a.dh0) {
+                float* h0g = a.dh0 + (b * a.dim + dr) * N + j * SPL;
+#pragma unroll
+                for (int q = 0; q < SPL; ++q) h0g[q] = Q[r][q];
+            }
+        }
+    }
+    if constexpr (MODE == 0) {
+        a.wsS[(b * (a.nchunks - 1) + (k - 1)) * a.dim + d] = S_acc;
+    } else {
+        a.pD[(b * a.nchunks + k) * a.dim + d] = dD_acc;
+        a.pbias[(b * a.nchunks + k) * a.dim + d] = dbias_acc;
+    }
+}
+
+// The sums over channel tiles (dB, dC) and over batch rows and chunks (dA, dD,
+// dbias) of the per-CTA shares, added in a fixed order.
+template <typename T, int N>
+__global__ void __launch_bounds__(256) scan_bwd_reduce_kernel(const BwdArgs a) {
+    const int64_t nBC = a.batch * a.L * 2 * N, nA = a.dim * N, nd = a.dim;
+    const int64_t total = nBC + nA + 2 * nd;
+    const int64_t rows = a.batch * a.nchunks;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        if (i < nBC) {
+            const int64_t bt = i / (2 * N), c = i % (2 * N);
+            const int64_t b = bt / a.L, t = bt % a.L;
+            float s = 0.f;
+            for (int64_t tile = 0; tile < a.tiles; ++tile)
+                s += a.pBC[((b * a.tiles + tile) * a.L + t) * (2 * N) + c];
+            st_io(static_cast<T*>(c < N ? a.dB : a.dC) + bt * N + (c % N), s);
+        } else if (i < nBC + nA) {
+            const int64_t e = i - nBC;
+            float s = 0.f;
+            for (int64_t r = 0; r < rows; ++r) s += a.pA[r * nA + e];
+            a.dA[e] = s;
+        } else {
+            const int64_t e = i - nBC - nA;
+            const bool is_bias = e >= nd;
+            const int64_t dd = is_bias ? e - nd : e;
+            float* out = is_bias ? a.dbias : a.dD;
+            if (!out) continue;
+            const float* part = is_bias ? a.pbias : a.pD;
+            float s = 0.f;
+            for (int64_t r = 0; r < rows; ++r) s += part[r * nd + dd];
+            out[dd] = s;
+        }
+    }
+}
+
+template <typename T, int N, bool SOFTPLUS, bool GATE, int MODE>
+cudaError_t launch_mode(const BwdArgs& a, int64_t ctas, cudaStream_t s) {
+    using Sm = BwdSmem<T, N>;
+    static std::mutex mu;
+    static bool done[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            e = cudaFuncSetAttribute(scan_bwd_kernel<T, N, SOFTPLUS, GATE, MODE>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::kBytes);
+            if (e != cudaSuccess) return e;
+            done[dev] = true;
+        }
+    }
+    scan_bwd_kernel<T, N, SOFTPLUS, GATE, MODE>
+        <<<static_cast<unsigned>(ctas), kBwdThreads, Sm::kBytes, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int N, bool SOFTPLUS, bool GATE>
+cudaError_t launch_flags(const BwdArgs& a, cudaStream_t s) {
+    const int64_t per_chunk = a.tiles * a.batch;
+    cudaError_t e;
+    if (a.nchunks > 1 &&
+        (e = launch_mode<T, N, SOFTPLUS, GATE, 0>(a, per_chunk * (a.nchunks - 1), s)) != cudaSuccess)
+        return e;
+    if ((e = launch_mode<T, N, SOFTPLUS, GATE, 1>(a, per_chunk * a.nchunks, s)) != cudaSuccess)
+        return e;
+    const int64_t total = a.batch * a.L * 2 * N + a.dim * N + 2 * a.dim;
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, 148 * 16);
+    scan_bwd_reduce_kernel<T, N><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_typed(const BwdArgs& a, cudaStream_t s) {
+    constexpr int N = 16;
+    const bool gate = a.z != nullptr;
+    if (a.softplus)
+        return gate ? launch_flags<T, N, true, true>(a, s) : launch_flags<T, N, true, false>(a, s);
+    return gate ? launch_flags<T, N, false, true>(a, s) : launch_flags<T, N, false, false>(a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_scan_bwd(const BwdArgs& a, int io, cudaStream_t s) {
+    return io == 1 ? launch_typed<__nv_bfloat16>(a, s) : launch_typed<float>(a, s);
+}
+
+}  // namespace ssm

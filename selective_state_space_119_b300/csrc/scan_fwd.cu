@@ -199,7 +199,8 @@ __device__ __forceinline__ float lds_elem(const __nv_bfloat16* p) {
 // causal depthwise conv1d + SiLU) instead of x. They are template flags so
 // that the per-token body has no branches and the compiler can overlap
 // successive tokens.
-template <typename T, int N, typename TC, int MODE, bool SOFTPLUS, bool GATE, bool CONV>
+template <typename T, int N, typename TC, int MODE, bool SOFTPLUS, bool GATE, bool CONV,
+          bool CKPT = false>
 __global__ void __launch_bounds__(Cfg<T, N, TC>::THREADS, 1)
 scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dt,
             const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
@@ -393,6 +394,28 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         Tok cur = prep(0);
 #pragma unroll 8
         for (int tl = 0; tl < TS; ++tl) {
+            if constexpr (MODE == 1 && CKPT) {
+                // the state before token t0 + tl, every kCkptTokens tokens
+                // (stages start on a multiple of kCkptTokens): saved for the
+                // backward, which recomputes the states in between
+                if ((tl % kCkptTokens) == 0 && tl < lim && ch_ok) {
+                    const int64_t m = (t0 + tl) / kCkptTokens;
+#pragma unroll
+                    for (int r = 0; r < NS; ++r) {
+                        const int64_t dr = dsafe - j + (j ^ r);
+                        float* dst = a.ckpt + ((b * a.nckpt + m) * a.dim + dr) * N + j * SPL;
+                        if constexpr (SPL % 4 == 0) {
+#pragma unroll
+                            for (int q = 0; q < SPL; q += 4)
+                                *reinterpret_cast<float4*>(dst + q) =
+                                    make_float4(h[r][q], h[r][q + 1], h[r][q + 2], h[r][q + 3]);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < SPL; ++q) dst[q] = h[r][q];
+                        }
+                    }
+                }
+            }
             const Tok nxt = prep((tl + 1) & (TS - 1));
             // this lane's states of B_t (then C_t)
             float bv[2 * SPL];
@@ -514,7 +537,7 @@ cudaError_t make_tmap(CUtensorMap* tm, const void* base, int64_t batch, int64_t 
 
 // Raise the dynamic shared-memory limit of one kernel instantiation, once per
 // device (the statics are per instantiation).
-template <typename T, int N, typename TC, int MODE, bool SP, bool GATE, bool CONV>
+template <typename T, int N, typename TC, int MODE, bool SP, bool GATE, bool CONV, bool CKPT>
 cudaError_t allow_smem() {
     static std::mutex mu;
     static bool done[128] = {};
@@ -524,14 +547,14 @@ cudaError_t allow_smem() {
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(scan_kernel<T, N, TC, MODE, SP, GATE, CONV>,
+    e = cudaFuncSetAttribute(scan_kernel<T, N, TC, MODE, SP, GATE, CONV, CKPT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem<T, N, TC, MODE, CONV>::kBytes);
     if (e == cudaSuccess) done[dev] = true;
     return e;
 }
 
-template <typename T, int N, typename TC, bool SOFTPLUS, bool GATE, bool CONV>
+template <typename T, int N, typename TC, bool SOFTPLUS, bool GATE, bool CONV, bool CKPT>
 cudaError_t launch_flags(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     using Cf = Cfg<T, N, TC>;
     if (p.channels_per_cta != Cf::DT) return cudaErrorInvalidValue;
@@ -554,26 +577,26 @@ cudaError_t launch_flags(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     }
     const int64_t per_chunk = p.tiles * a.batch;
     if (p.nchunks > 1) {
-        if ((e = allow_smem<T, N, TC, 0, SOFTPLUS, false, CONV>()) != cudaSuccess) return e;
+        if ((e = allow_smem<T, N, TC, 0, SOFTPLUS, false, CONV, false>()) != cudaSuccess) return e;
         scan_kernel<T, N, TC, 0, SOFTPLUS, false, CONV>
             <<<static_cast<unsigned>(per_chunk * (p.nchunks - 1)), Cf::THREADS,
                Smem<T, N, TC, 0, CONV>::kBytes, s>>>(tx, tdt, tz, tB, tC, tout, a);
     }
-    if ((e = allow_smem<T, N, TC, 1, SOFTPLUS, GATE, CONV>()) != cudaSuccess) return e;
-    scan_kernel<T, N, TC, 1, SOFTPLUS, GATE, CONV>
+    if ((e = allow_smem<T, N, TC, 1, SOFTPLUS, GATE, CONV, CKPT>()) != cudaSuccess) return e;
+    scan_kernel<T, N, TC, 1, SOFTPLUS, GATE, CONV, CKPT>
         <<<static_cast<unsigned>(per_chunk * p.nchunks), Cf::THREADS,
            Smem<T, N, TC, 1, CONV>::kBytes, s>>>(tx, tdt, tz, tB, tC, tout, a);
     return cudaGetLastError();
 }
 
-template <typename T, int N, typename TC, bool CONV>
+template <typename T, int N, typename TC, bool CONV, bool CKPT = false>
 cudaError_t launch_cfg(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     const bool sp = a.softplus != 0, gate = a.z != nullptr;
     if (sp)
-        return gate ? launch_flags<T, N, TC, true, true, CONV>(a, p, s)
-                    : launch_flags<T, N, TC, true, false, CONV>(a, p, s);
-    return gate ? launch_flags<T, N, TC, false, true, CONV>(a, p, s)
-                : launch_flags<T, N, TC, false, false, CONV>(a, p, s);
+        return gate ? launch_flags<T, N, TC, true, true, CONV, CKPT>(a, p, s)
+                    : launch_flags<T, N, TC, true, false, CONV, CKPT>(a, p, s);
+    return gate ? launch_flags<T, N, TC, false, true, CONV, CKPT>(a, p, s)
+                : launch_flags<T, N, TC, false, false, CONV, CKPT>(a, p, s);
 }
 
 // The tile configurations by id (the same table as scan_lanes... in ssm_internal.h).
@@ -585,9 +608,12 @@ using Tile3 = TileCfg<3>;
 template <typename T, int N>
 cudaError_t launch_typed(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     // the fused conv input stage is built for tile configuration 0 only (the
-    // planner never picks another one for it)
-    if (a.conv_w) return p.tile_cfg == 0 ? launch_cfg<T, N, Tile0, true>(a, p, s)
-                                         : cudaErrorInvalidValue;
+    // library never plans another one for it)
+    if (a.conv_w) return p.tile_cfg == 0 && !a.ckpt ? launch_cfg<T, N, Tile0, true>(a, p, s)
+                                                    : cudaErrorInvalidValue;
+    // so is the checkpointing forward (training)
+    if (a.ckpt) return p.tile_cfg == 0 ? launch_cfg<T, N, Tile0, false, true>(a, p, s)
+                                       : cudaErrorInvalidValue;
     if constexpr (N == 16) {
         switch (p.tile_cfg) {
             case 0: return launch_cfg<T, N, Tile0, false>(a, p, s);

@@ -62,6 +62,8 @@ struct ScanArgs {
     const float* conv_w;  // [dim][conv_k] causal conv taps of the fused input stage, or NULL
     const float* conv_b;  // [dim] conv bias, or NULL
     int conv_k;           // conv width (1 .. 4) when conv_w is given
+    float* ckpt;          // [batch][nckpt][dim][N]: state before every kCkptTokens-th token, or NULL
+    int64_t nckpt;        // ceil(L / kCkptTokens)
     float* ws_H;   // [batch][nchunks-1][dim][N]: chunk-local end states (from h = 0)
     float* ws_S;   // [batch][nchunks-1][dim]: sum of dt over each chunk
     unsigned int* status;  // workspace status word (sticky; 0 = ok; no current kernel sets it)
@@ -82,6 +84,11 @@ struct StepArgs {
     int64_t batch, dim;
 };
 
+// Tokens between two saved states of a checkpointing forward (the backward
+// recomputes the states in between). Chunks and stages are multiples of it.
+constexpr int kCkptTokens = 8;
+static_assert(kScanStageTokens % kCkptTokens == 0, "stages start on a checkpoint");
+
 // Widest causal conv of the Mamba block's input stage (d_conv = 4 on the pages).
 constexpr int kMaxConvK = 4;
 
@@ -94,10 +101,48 @@ struct ConvArgs {
     int k;
 };
 
+// The gradient pass of the scan (dstate 16). Chunking follows the forward's
+// plan with 128-channel tiles.
+struct BwdArgs {
+    const void* x;
+    const void* delta;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* delta_bias;
+    int softplus;
+    const float* ckpt;    // [batch][nckpt][dim][N] from the checkpointing forward
+    int64_t nckpt;
+    const void* dout;     // [batch][L][dim]
+    const float* dfinal;  // [batch][dim][N] or NULL
+    void* dx;             // [batch][L][dim] io
+    void* ddelta;
+    void* dz;             // NULL without the gate
+    float* dh0;           // [batch][dim][N] or NULL
+    void* dB;             // [batch][L][N] io
+    void* dC;
+    float* dA;            // [dim][N]
+    float* dD;            // [dim] or NULL
+    float* dbias;         // [dim] or NULL
+    int64_t batch, L, dim;
+    int64_t chunk_len, nchunks, tiles;
+    // workspace
+    float* wsQ;    // [batch][nchunks-1][dim][N]: reverse carry of chunks 1.. from zero
+    float* wsS;    // [batch][nchunks-1][dim]: sum of dt over those chunks
+    float* pBC;    // [batch][tiles][L][2N]: each tile's share of dB | dC
+    float* pA;     // [batch][nchunks][dim][N]
+    float* pD;     // [batch][nchunks][dim]
+    float* pbias;  // [batch][nchunks][dim]
+};
+
 // Enqueue one full scan (all phases). io: 0 = fp32, 1 = bf16.
 cudaError_t launch_scan(const ScanArgs& a, const ScanPlan& p, int io, int N, cudaStream_t s);
 // Enqueue one decode step.
 cudaError_t launch_state_update(const StepArgs& a, int io, int N, cudaStream_t s);
+// Enqueue the gradient passes (reverse carries, gradients, reduction).
+cudaError_t launch_scan_bwd(const BwdArgs& a, int io, cudaStream_t s);
 // Enqueue the standalone causal depthwise conv1d + SiLU.
 cudaError_t launch_conv1d_silu(const ConvArgs& a, int io, cudaStream_t s);
 

@@ -43,7 +43,9 @@ SSM_ERR_ALIAS = -8
 EXPORTED = ("ssm_selective_scan_fwd", "ssm_state_update", "ssm_scan_workspace_bytes",
             "ssm_scan_plan", "ssm_get_device_status", "ssm_strerror", "ssm_last_cuda_error",
             "ssm_version", "ssm_selective_scan_fwd_static", "ssm_selective_scan_fwd_from_state",
-            "ssm_selective_scan_fwd_conv", "ssm_causal_conv1d_silu")
+            "ssm_selective_scan_fwd_conv", "ssm_causal_conv1d_silu", "ssm_scan_checkpoint_bytes",
+            "ssm_selective_scan_fwd_ckpt", "ssm_scan_bwd_workspace_bytes",
+            "ssm_selective_scan_bwd")
 
 # Size of the library-owned scratch of ssm_selective_scan_fwd_static (include/ssm.h).
 SSM_STATIC_SCRATCH_BYTES = 16 << 20
@@ -76,6 +78,16 @@ lib.ssm_selective_scan_fwd_conv.argtypes = [_vp, _vp, _vp, ctypes.c_int, _vp, _v
                                             _vp, _vp, ctypes.c_int, _vp, _vp, _dims_p, _vp]
 lib.ssm_causal_conv1d_silu.restype = ctypes.c_int
 lib.ssm_causal_conv1d_silu.argtypes = [_vp, _vp, _vp, ctypes.c_int, _vp, _dims_p, _vp]
+lib.ssm_scan_checkpoint_bytes.restype = ctypes.c_size_t
+lib.ssm_scan_checkpoint_bytes.argtypes = [_dims_p]
+lib.ssm_selective_scan_fwd_ckpt.restype = ctypes.c_int
+lib.ssm_selective_scan_fwd_ckpt.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
+                                            _vp, _vp, _vp, _vp, _dims_p, _vp]
+lib.ssm_scan_bwd_workspace_bytes.restype = ctypes.c_size_t
+lib.ssm_scan_bwd_workspace_bytes.argtypes = [_dims_p]
+lib.ssm_selective_scan_bwd.restype = ctypes.c_int
+lib.ssm_selective_scan_bwd.argtypes = ([_vp] * 8 + [ctypes.c_int] + [_vp] * 12 +
+                                       [_dims_p, _vp])
 lib.ssm_selective_scan_fwd_static.restype = ctypes.c_int
 lib.ssm_selective_scan_fwd_static.argtypes = list(lib.ssm_selective_scan_fwd.argtypes)
 lib.ssm_state_update.restype = ctypes.c_int
@@ -354,6 +366,102 @@ def ssm_get_device_status(batch, seqlen, dim, dstate, io, workspace, chunk_len_h
     dev = workspace.device if workspace is not None else torch.device("cuda")
     with torch.cuda.device(dev):
         return int(lib.ssm_get_device_status(ctypes.byref(dims), _stream(dev, stream)))
+
+
+def ssm_scan_checkpoint_bytes(batch, seqlen, dim, dstate, io) -> int:
+    d = make_dims(batch, seqlen, dim, dstate, io)
+    return int(lib.ssm_scan_checkpoint_bytes(ctypes.byref(d)))
+
+
+def ssm_scan_bwd_workspace_bytes(batch, seqlen, dim, dstate, io, chunk_len_hint=0,
+                                 tile_config_hint=0) -> int:
+    d = make_dims(batch, seqlen, dim, dstate, io, chunk_len_hint=chunk_len_hint,
+                  tile_config_hint=tile_config_hint)
+    return int(lib.ssm_scan_bwd_workspace_bytes(ctypes.byref(d)))
+
+
+def ssm_selective_scan_fwd_ckpt(x, delta, A, B, C, D=None, z=None, delta_bias=None,
+                                delta_softplus=False, h0=None, out=None, final_state=None,
+                                ckpt=None, workspace=None, chunk_len_hint=0, stream=None):
+    """The scan that also saves the state before every 8th token for the
+    backward. Returns (out, final_state, ckpt); ckpt is [batch, ceil(L/8), dim,
+    16] fp32."""
+    torch = _torch()
+    batch, L, dim = x.shape
+    N = A.shape[1]
+    io = x.dtype
+    dev = x.device
+    if out is None:
+        out = torch.empty_like(x)
+    if final_state is None:
+        final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+    if ckpt is None:
+        ckpt = torch.empty((batch, (L + 7) // 8, dim, N), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(batch, L, dim, N, _io_code(x), dev, chunk_len_hint)
+    ws_ptr = _ptr(workspace, "workspace", torch.uint8, device=dev)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    dims = make_dims(batch, L, dim, N, _io_code(x), ws_ptr, ws_bytes, chunk_len_hint)
+    with torch.cuda.device(dev):
+        rc = lib.ssm_selective_scan_fwd_ckpt(
+            _ptr(x, "x", io, (batch, L, dim), dev), _ptr(delta, "delta", io, (batch, L, dim), dev),
+            _ptr(A, "A", torch.float32, (dim, N), dev), _ptr(B, "B", io, (batch, L, N), dev),
+            _ptr(C, "C", io, (batch, L, N), dev), _ptr(D, "D", torch.float32, (dim,), dev),
+            _ptr(z, "z", io, (batch, L, dim), dev),
+            _ptr(delta_bias, "delta_bias", torch.float32, (dim,), dev),
+            1 if delta_softplus else 0, _ptr(h0, "h0", torch.float32, (batch, dim, N), dev),
+            _ptr(out, "out", io, (batch, L, dim), dev),
+            _ptr(final_state, "final_state", torch.float32, (batch, dim, N), dev),
+            _ptr(ckpt, "ckpt", torch.float32, (batch, (L + 7) // 8, dim, N), dev),
+            ctypes.byref(dims), _stream(dev, stream))
+    _check(rc, "ssm_selective_scan_fwd_ckpt")
+    return out, final_state, ckpt
+
+
+def ssm_selective_scan_bwd(x, delta, A, B, C, ckpt, dout, D=None, z=None, delta_bias=None,
+                           delta_softplus=False, dfinal_state=None, want_dD=True,
+                           want_ddelta_bias=True, want_dh0=False, workspace=None,
+                           chunk_len_hint=0, stream=None) -> dict:
+    """Gradients of the scan (include/ssm.h). Returns a dict with dx, ddelta,
+    dA, dB, dC and, when asked for / defined, dD, dz, ddelta_bias, dh0."""
+    torch = _torch()
+    batch, L, dim = x.shape
+    N = A.shape[1]
+    io = x.dtype
+    dev = x.device
+    g = {"dx": torch.empty_like(x), "ddelta": torch.empty_like(x),
+         "dA": torch.empty((dim, N), dtype=torch.float32, device=dev),
+         "dB": torch.empty((batch, L, N), dtype=io, device=dev),
+         "dC": torch.empty((batch, L, N), dtype=io, device=dev),
+         "dD": torch.empty(dim, dtype=torch.float32, device=dev) if want_dD else None,
+         "dz": torch.empty_like(x) if z is not None else None,
+         "ddelta_bias": (torch.empty(dim, dtype=torch.float32, device=dev)
+                         if want_ddelta_bias else None),
+         "dh0": (torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+                 if want_dh0 else None)}
+    if workspace is None:
+        n = ssm_scan_bwd_workspace_bytes(batch, L, dim, N, _io_code(x), chunk_len_hint)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+    dims = make_dims(batch, L, dim, N, _io_code(x), _ptr(workspace, "workspace", torch.uint8,
+                                                         device=dev),
+                     workspace.numel(), chunk_len_hint)
+    with torch.cuda.device(dev):
+        rc = lib.ssm_selective_scan_bwd(
+            _ptr(x, "x", io, (batch, L, dim), dev), _ptr(delta, "delta", io, (batch, L, dim), dev),
+            _ptr(A, "A", torch.float32, (dim, N), dev), _ptr(B, "B", io, (batch, L, N), dev),
+            _ptr(C, "C", io, (batch, L, N), dev), _ptr(D, "D", torch.float32, (dim,), dev),
+            _ptr(z, "z", io, (batch, L, dim), dev),
+            _ptr(delta_bias, "delta_bias", torch.float32, (dim,), dev),
+            1 if delta_softplus else 0,
+            _ptr(ckpt, "ckpt", torch.float32, (batch, (L + 7) // 8, dim, N), dev),
+            _ptr(dout, "dout", io, (batch, L, dim), dev),
+            _ptr(dfinal_state, "dfinal_state", torch.float32, (batch, dim, N), dev),
+            _ptr(g["dx"], "dx"), _ptr(g["ddelta"], "ddelta"), _ptr(g["dA"], "dA"),
+            _ptr(g["dB"], "dB"), _ptr(g["dC"], "dC"), _ptr(g["dD"], "dD"), _ptr(g["dz"], "dz"),
+            _ptr(g["ddelta_bias"], "ddelta_bias"), _ptr(g["dh0"], "dh0"),
+            ctypes.byref(dims), _stream(dev, stream))
+    _check(rc, "ssm_selective_scan_bwd")
+    return g
 
 
 # Short aliases.

@@ -189,3 +189,48 @@ def test_conv_entry_points_reject_bad_arguments_before_launch():
     assert conv(w=None, u=None, x=None, dims=de) == L.SSM_OK
     # bf16 dim must be a multiple of 8
     assert conv(dims=L.make_dims(1, 4, 12, 16, "bf16")) == L.SSM_ERR_ALIGN
+
+
+def test_training_entry_points_reject_bad_arguments_before_launch():
+    d = L.make_dims(1, 20, 16, 16, "bf16", workspace=FAKE + (1 << 34), workspace_bytes=1 << 24)
+    CK = FAKE + (1 << 32)
+
+    def fwd(ck=CK, dims=d, out=FAKE + (1 << 30)):
+        return L.lib.ssm_selective_scan_fwd_ckpt(FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288,
+                                                 FAKE + 16384, None, None, None, 0, None, out,
+                                                 None, ck, ctypes.byref(dims), None)
+
+    assert fwd(ck=None) == L.SSM_ERR_NULL
+    assert fwd(ck=CK + 4) == L.SSM_ERR_ALIGN
+    assert fwd(out=CK) == L.SSM_ERR_ALIAS                              # out over the checkpoints
+    assert fwd(dims=L.make_dims(1, 20, 16, 8, "bf16")) == L.SSM_ERR_DIMS   # dstate 16 only
+    assert fwd(dims=L.make_dims(1, 20, 16, 16, "bf16", tile_config_hint=3)) == L.SSM_ERR_DIMS
+    # sizes: a state before every 8th token
+    assert L.ssm_scan_checkpoint_bytes(2, 20, 16, 16, "bf16") == 2 * 3 * 16 * 16 * 4
+    assert L.ssm_scan_checkpoint_bytes(2, 0, 16, 16, "bf16") == 0
+
+    G = FAKE + (1 << 36)   # gradients live here, far from the inputs
+
+    def bwd(dims=d, z=None, dz=None, dx=G, dA=G + 65536, ckpt=CK, dh0=None):
+        return L.lib.ssm_selective_scan_bwd(
+            FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288, FAKE + 16384, None, z, None, 0, ckpt,
+            FAKE + 20480, None, dx, G + 4096, dA, G + 8192, G + 12288, None, dz, None, dh0,
+            ctypes.byref(dims), None)
+
+    assert bwd(ckpt=None) == L.SSM_ERR_NULL
+    assert bwd(dA=None) == L.SSM_ERR_NULL
+    assert bwd(z=FAKE + 24576) == L.SSM_ERR_NULL                       # z without dz
+    assert bwd(dz=G + 16384) == L.SSM_ERR_NULL                         # dz without z
+    assert bwd(dx=G + 2) == L.SSM_ERR_ALIGN
+    assert bwd(dx=FAKE) == L.SSM_ERR_ALIAS                              # dx over x
+    assert bwd(dx=G + 4096) == L.SSM_ERR_ALIAS                          # dx over ddelta
+    assert bwd(dh0=CK) == L.SSM_ERR_ALIAS                               # dh0 over the checkpoints
+    assert bwd(dims=L.make_dims(1, 20, 16, 4, "bf16")) == L.SSM_ERR_DIMS
+    small = L.make_dims(1, 20, 16, 16, "bf16", workspace=FAKE + (1 << 34), workspace_bytes=256)
+    assert bwd(dims=small) == L.SSM_ERR_WORKSPACE
+    # workspace: the per-tile shares of dB | dC, dA, dD, dbias (+ carries when chunked)
+    ws1 = L.ssm_scan_bwd_workspace_bytes(2, 1000, 512, 16, "bf16", chunk_len_hint=1024)
+    ws8 = L.ssm_scan_bwd_workspace_bytes(2, 1000, 512, 16, "bf16", chunk_len_hint=128)
+    assert ws1 >= 256 + 2 * 4 * 1000 * 32 * 4 + 2 * 512 * 16 * 4
+    assert ws8 > ws1
+    assert L.ssm_scan_bwd_workspace_bytes(2, 1000, 512, 8, "bf16") == 0

@@ -1,0 +1,191 @@
+"""GPU parity of training through the scan: the checkpointing forward
+(ssm_selective_scan_fwd_ckpt) and the gradients (ssm_selective_scan_bwd)
+against the float64 oracle ("State-space models (Mamba, S4)", "Training vs
+Inference Modes"; "State Space Models -- Mamba, S4, and Beyond", "Verification
+Checklist": gradients flow through the discretization).
+
+Covered: the saved states equal the oracle's state after each 8-token prefix
+(with and without L-chunks, from h0); every gradient (dx, ddelta, dz, dB, dC,
+dA, dD, ddelta_bias, dh0) against the oracle's backward over fp32 and bf16
+I/O, softplus on/off, gate on/off, D and bias on/off, dLoss/dfinal_state
+on/off, several L-chunk plans, ragged sequence ends and channel tiles; an empty
+sequence; the benchmark-size workload.
+
+Tolerances (gradients are sums over up to L tokens and, for dB/dC, over every
+channel; they are compared against the largest entry of each array, at least 1,
+and the L2 norm, at least sqrt(size)):
+  fp32 I/O: max |err| <= 2e-4 * max(1, max|ref|), rel L2 <= 5e-5
+  bf16 I/O: max |err| <= 2e-2 * max(1, max|ref|), rel L2 <= 1e-2 (outputs rounded to bf16)
+"""
+import numpy as np
+import pytest
+
+import gpu_util as G
+import oracle
+from selective_state_space_119_b300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": (2e-4, 5e-5), "bf16": (2e-2, 1e-2), "state": (2e-4, 5e-5)}
+
+
+@pytest.fixture(scope="module")
+def torch():
+    t = pytest.importorskip("torch")
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from selective_state_space_119_b300 import build
+    build.build(quiet=True)
+    return t
+
+
+def grad_parity(got, ref, kind, what):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), "%s: non-finite" % what
+    mx, l2 = TOL[kind]
+    # scales floored at 1 (and sqrt(size)): a gradient that is exactly zero
+    # (dA with h0 = 0 and one token) is compared in absolute terms
+    scale = max(float(np.abs(ref).max()), 1.0) if ref.size else 1.0
+    err = np.abs(got - ref)
+    worst = float(err.max()) / scale if err.size else 0.0
+    nref = max(float(np.linalg.norm(ref)), float(np.sqrt(ref.size)))
+    rel = float(np.linalg.norm(got - ref)) / nref if ref.size else 0.0
+    assert worst <= mx, "%s: max|err|/max|ref| = %.3e > %.0e" % (what, worst, mx)
+    assert rel <= l2, "%s: rel L2 %.3e > %.0e" % (what, rel, l2)
+
+
+def _store(arr, io):
+    return I.store(np.asarray(arr, np.float64), io)
+
+
+def _case(spec, seed, with_h0=False, with_dfinal=False):
+    inp = I.make_scan_inputs(spec)
+    r = np.random.default_rng(seed)
+    dout = _store(r.standard_normal((spec.batch, spec.L, spec.dim)), spec.io)
+    h0 = (r.standard_normal((spec.batch, spec.dim, spec.N)).astype(np.float32)
+          if with_h0 else None)
+    dfin = (r.standard_normal((spec.batch, spec.dim, spec.N)).astype(np.float32)
+            if with_dfinal else None)
+    return inp, dout, h0, dfin
+
+
+def _gpu_train(inp, softplus, dout, h0=None, dfinal=None, hint=0, want_dh0=False):
+    from selective_state_space_119_b300 import libssm
+    t = {k: G.dev(v) for k, v in inp.items()}
+    out, fs, ck = libssm.ssm_selective_scan_fwd_ckpt(
+        t["x"], t["delta"], t["A"], t["B"], t["C"], D=t.get("D"), z=t.get("z"),
+        delta_bias=t.get("delta_bias"), delta_softplus=softplus, h0=G.dev(h0),
+        chunk_len_hint=hint)
+    g = libssm.ssm_selective_scan_bwd(
+        t["x"], t["delta"], t["A"], t["B"], t["C"], ck, G.dev(dout), D=t.get("D"), z=t.get("z"),
+        delta_bias=t.get("delta_bias"), delta_softplus=softplus, dfinal_state=G.dev(dfinal),
+        want_dh0=want_dh0, chunk_len_hint=hint)
+    return out, fs, ck, g
+
+
+def _oracle_bwd(inp, softplus, dout, h0=None, dfinal=None):
+    return oracle.selective_scan_bwd(
+        I.widen(inp["x"]), I.widen(inp["delta"]), np.asarray(inp["A"], np.float64),
+        I.widen(inp["B"]), I.widen(inp["C"]), I.widen(dout),
+        D=None if inp.get("D") is None else np.asarray(inp["D"], np.float64),
+        z=I.widen(inp.get("z")),
+        delta_bias=None if inp.get("delta_bias") is None else np.asarray(inp["delta_bias"], np.float64),
+        delta_softplus=softplus, h0=None if h0 is None else h0.astype(np.float64),
+        dh_final=None if dfinal is None else dfinal.astype(np.float64))
+
+
+def _check_grads(g, ref, io, what, z_given=True, dh0=False):
+    for k in ("dx", "ddelta", "dB", "dC"):
+        grad_parity(G.host64(g[k]), ref[k], io, "%s %s" % (k, what))
+    if z_given:
+        grad_parity(G.host64(g["dz"]), ref["dz"], io, "dz " + what)
+    grad_parity(G.host64(g["dA"]), ref["dA"], "state", "dA " + what)
+    if ref["dD"] is not None:
+        grad_parity(G.host64(g["dD"]), ref["dD"], "state", "dD " + what)
+    if ref["ddelta_bias"] is not None:
+        grad_parity(G.host64(g["ddelta_bias"]), ref["ddelta_bias"], "state", "dbias " + what)
+    if dh0:
+        grad_parity(G.host64(g["dh0"]), ref["dh0"], "state", "dh0 " + what)
+
+
+@pytest.mark.parametrize("hint", [0, 64, 96])
+def test_checkpoints_are_prefix_states(torch, hint):
+    spec = I.ScanSpec(2, 301, 264, io="f32", delta_kind="softplus_bias", A_kind="lognormal",
+                      D_kind="uniform", seed=61)
+    inp, dout, h0, _ = _case(spec, 62, with_h0=True)
+    out, fs, ck, _ = _gpu_train(inp, True, dout, h0=h0, hint=hint)
+    ck = G.host64(ck)
+    assert ck.shape == (2, 38, 264, 16)
+    for m in (0, 1, 8, 12, 37):
+        L = 8 * m
+        sub = {k: (np.ascontiguousarray(v[:, :L]) if k in ("x", "delta", "z", "B", "C")
+                   and v is not None else v) for k, v in inp.items()}
+        _, ref = G.oracle_scan(sub, True, h0=h0.astype(np.float64)) if L > 0 else (None, h0)
+        G.parity(ck[:, m], ref, "state", "checkpoint %d (hint %d)" % (m, hint))
+    ry, rh = G.oracle_scan(inp, True, h0=h0.astype(np.float64))
+    G.parity(G.host64(out), ry, "f32", "checkpointing forward y")
+    G.parity(G.host64(fs), rh, "state", "checkpointing forward final state")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("hint", [0, 64, 96])
+def test_gradients_softplus_gate(torch, io, hint):
+    spec = I.ScanSpec(2, 300, 264, io=io, delta_kind="softplus_bias", A_kind="lognormal",
+                      D_kind="uniform", seed=63)
+    inp, dout, h0, dfin = _case(spec, 64, with_h0=True, with_dfinal=True)
+    _, _, _, g = _gpu_train(inp, True, dout, h0=h0, dfinal=dfin, hint=hint, want_dh0=True)
+    ref = _oracle_bwd(inp, True, dout, h0=h0, dfinal=dfin)
+    _check_grads(g, ref, io, "(%s, hint %d)" % (io, hint), dh0=True)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("gate,D_kind", [(False, "none"), (True, "one"), (False, "uniform")])
+def test_gradients_plain_delta(torch, io, gate, D_kind):
+    spec = I.ScanSpec(1, 203, 136, io=io, gate=gate, D_kind=D_kind, seed=65)
+    inp, dout, _, _ = _case(spec, 66)
+    _, _, _, g = _gpu_train(inp, False, dout, hint=64)
+    ref = _oracle_bwd(inp, False, dout)
+    _check_grads(g, ref, io, "(%s, gate %s, D %s)" % (io, gate, D_kind), z_given=gate)
+    # dD and ddelta_bias are the gradients at zero when D / bias are absent
+    if D_kind == "none":
+        x, gy = I.widen(inp["x"]), I.widen(dout)
+        if gate:
+            zz = I.widen(inp["z"])
+            gy = gy * zz / (1 + np.exp(-zz))
+        grad_parity(G.host64(g["dD"]), (gy * x).sum(axis=(0, 1)), "state", "dD at D = 0")
+    grad_parity(G.host64(g["ddelta_bias"]), ref["ddelta"].sum(axis=(0, 1)), "state",
+                "ddelta_bias = sum of ddelta")
+
+
+@pytest.mark.parametrize("L", [1, 7, 8, 9, 33])
+def test_gradients_short_sequences(torch, L):
+    spec = I.ScanSpec(2, L, 128, io="f32", delta_kind="softplus_bias", seed=67)
+    inp, dout, _, dfin = _case(spec, 68, with_dfinal=True)
+    _, _, _, g = _gpu_train(inp, True, dout, dfinal=dfin, want_dh0=True)
+    ref = _oracle_bwd(inp, True, dout, dfinal=dfin)
+    _check_grads(g, ref, "f32", "(L %d)" % L, dh0=True)
+
+
+def test_empty_sequence(torch):
+    from selective_state_space_119_b300 import libssm
+    t = torch
+    x = t.zeros((2, 0, 16), dtype=t.float32, device="cuda")
+    BC = t.zeros((2, 0, 16), dtype=t.float32, device="cuda")
+    A = -t.ones((16, 16), device="cuda")
+    ck = t.zeros((2, 0, 16, 16), device="cuda")
+    dfin = t.randn(2, 16, 16, device="cuda")
+    g = libssm.ssm_selective_scan_bwd(x, x, A, BC, BC, ck, x, dfinal_state=dfin, want_dh0=True)
+    assert float(g["dA"].abs().max()) == 0.0 and float(g["dD"].abs().max()) == 0.0
+    assert t.equal(g["dh0"], dfin)
+
+
+def test_benchmark_workload_gradients(torch):
+    """Batch 4, L 2048, dim 1536, bf16, softplus(delta + bias), gate: every
+    gradient against the oracle's full backward."""
+    spec = I.WORKLOADS["scan_bf16_b4_L2048_d1536_softplus"]
+    inp, dout, _, _ = _case(spec, 69)
+    _, _, _, g = _gpu_train(inp, True, dout)
+    ref = _oracle_bwd(inp, True, dout)
+    _check_grads(g, ref, "bf16", "(benchmark workload)")
