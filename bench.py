@@ -21,6 +21,8 @@ bias), gate), i.e. every step of the scan path. Rank 0 prints one JSON line.
   256, dim 5120, N 16), rotating over several cached states.
 * input_stage: the causal conv1d + SiLU (width 4) alone, fused in front of
   the scan, and as two calls (conv, then the scan on its output).
+* train: training through the scan on the same workload, the checkpointing
+  forward and the backward (every gradient), per call.
 * cpu_baseline: the float64 CPU oracle timed on this host (rank 0, N = 1).
 
 N > 1 (torchrun): every rank runs its own replica of the workload on its own
@@ -341,6 +343,8 @@ def bench_scan(args, rank, world, local):
         res["decode"] = bench_decode(args, dev, stream)
     if not args.no_input_stage:
         res["input_stage"] = bench_input_stage(args, spec, dev, stream)
+    if not args.no_train and spec.N == 16:
+        res["train"] = bench_train(args, spec, dev, stream)
     return res, spec
 
 
@@ -547,6 +551,96 @@ def bench_input_stage(args, spec, dev, stream):
                                "unit": "elems/s", "kernels_per_call": plan["kernels"] + 1}}
 
 
+def bench_train(args, spec, dev, stream):
+    """Training through the scan on the scan workload: the checkpointing
+    forward and the backward (every gradient), each over rotating input sets
+    larger than twice the L2 cache; dout ~ N(0, 1) in the I/O dtype."""
+    import torch
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+
+    inp = I.make_scan_inputs(spec)
+    io = libssm.SSM_BF16 if spec.io == "bf16" else libssm.SSM_F32
+    scan_bytes = I.algorithmic_bytes_scan(spec)
+    nsets = max(2, min(8, math.ceil(2 * L2_BYTES / scan_bytes) + 1))
+    base = {k: _upload(v, dev) for k, v in inp.items()}
+    gen = torch.Generator(device=dev).manual_seed(spec.seed + 11)
+    sets = []
+    for _ in range(nsets):
+        st = {k: (None if base[k] is None else (base[k] if k in ("A", "D", "delta_bias")
+                                                 else base[k].clone())) for k in base}
+        st["dout"] = torch.randn(base["x"].shape, generator=gen, device=dev).to(base["x"].dtype)
+        st["ckpt"] = torch.empty((spec.batch, (spec.L + 7) // 8, spec.dim, spec.N),
+                                 dtype=torch.float32, device=dev)
+        sets.append(st)
+    B_, L_, D_, N_ = spec.batch, spec.L, spec.dim, spec.N
+    ws = libssm.alloc_workspace(B_, L_, D_, N_, io, dev)
+    fdims = libssm.make_dims(B_, L_, D_, N_, io, None if ws is None else ws.data_ptr(),
+                             0 if ws is None else ws.numel())
+    nb = libssm.ssm_scan_bwd_workspace_bytes(B_, L_, D_, N_, io)
+    bws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    bdims = libssm.make_dims(B_, L_, D_, N_, io, bws.data_ptr(), nb)
+    out = torch.empty_like(base["x"])
+    fs = torch.empty((B_, D_, N_), dtype=torch.float32, device=dev)
+    g = {"dx": torch.empty_like(base["x"]), "ddelta": torch.empty_like(base["x"]),
+         "dz": torch.empty_like(base["x"]) if base["z"] is not None else None,
+         "dA": torch.empty((D_, N_), dtype=torch.float32, device=dev),
+         "dB": torch.empty((B_, L_, N_), dtype=base["x"].dtype, device=dev),
+         "dC": torch.empty((B_, L_, N_), dtype=base["x"].dtype, device=dev),
+         "dD": torch.empty(D_, dtype=torch.float32, device=dev),
+         "dbias": torch.empty(D_, dtype=torch.float32, device=dev)}
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    sp = 1 if spec.delta_softplus else 0
+
+    def fwd(i):
+        st = sets[i % nsets]
+        rc = libssm.lib.ssm_selective_scan_fwd_ckpt(
+            _vp(st["x"]), _vp(st["delta"]), _vp(st["A"]), _vp(st["B"]), _vp(st["C"]),
+            _vp(st["D"]), _vp(st["z"]), _vp(st["delta_bias"]), sp, None, _vp(out), _vp(fs),
+            _vp(st["ckpt"]), ctypes.byref(fdims), sptr)
+        if rc != 0:
+            raise libssm.SSMError(rc, "ssm_selective_scan_fwd_ckpt")
+
+    def bwd(i):
+        st = sets[i % nsets]
+        rc = libssm.lib.ssm_selective_scan_bwd(
+            _vp(st["x"]), _vp(st["delta"]), _vp(st["A"]), _vp(st["B"]), _vp(st["C"]),
+            _vp(st["D"]), _vp(st["z"]), _vp(st["delta_bias"]), sp, _vp(st["ckpt"]),
+            _vp(st["dout"]), None, _vp(g["dx"]), _vp(g["ddelta"]), _vp(g["dA"]), _vp(g["dB"]),
+            _vp(g["dC"]), _vp(g["dD"]), _vp(g["dz"]), _vp(g["dbias"]), None,
+            ctypes.byref(bdims), sptr)
+        if rc != 0:
+            raise libssm.SSMError(rc, "ssm_selective_scan_bwd")
+
+    def timed(fn, n):
+        for i in range(max(args.warmup, 3)):
+            fn(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    for i in range(nsets):          # every set's checkpoints exist before the first backward
+        fwd(i)
+    n = max(16, min(args.steps, 400))
+    t_f = timed(fwd, n)
+    t_b = timed(bwd, n)
+    plan = libssm.ssm_scan_plan(B_, L_, D_, N_, io)
+    elems = spec.elements
+    return {"timed_calls": n, "input_sets": nsets, "dout": "N(0,1)",
+            "fwd_ckpt": {"us_per_call": t_f * 1e6, "value": elems / t_f, "unit": "elems/s",
+                         "kernels_per_call": plan["kernels"]},
+            "bwd": {"us_per_call": t_b * 1e6, "value": elems / t_b, "unit": "elems/s",
+                    "kernels_per_call": (2 if plan["nchunks"] > 1 else 1) + 1,
+                    "workspace_bytes": nb},
+            "step": {"us_per_call": (t_f + t_b) * 1e6, "value": elems / (t_f + t_b),
+                     "unit": "elems/s"}}
+
+
 # ---------------------------------------------------------------------------
 # the CPU oracle arm
 # ---------------------------------------------------------------------------
@@ -650,6 +744,8 @@ def main(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-input-stage", action="store_true",
                     help="skip the conv1d + SiLU input-stage timings")
+    ap.add_argument("--no-train", action="store_true",
+                    help="skip the training (checkpointing forward + backward) timings")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,
                     help="minimum wall time of the CPU oracle baseline")
     args = ap.parse_args(argv)
@@ -687,6 +783,8 @@ def main(argv=None):
             line["decode"] = res["decode"]
         if "input_stage" in res:
             line["input_stage"] = res["input_stage"]
+        if "train" in res:
+            line["train"] = res["train"]
         if world == 1:
             from selective_state_space_119_b300 import inputs as I
             inp = I.make_scan_inputs(spec)

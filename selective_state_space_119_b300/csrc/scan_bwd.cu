@@ -46,11 +46,13 @@ namespace {
 constexpr int kBwdWarps = 4;
 constexpr int kBwdThreads = 32 * kBwdWarps;
 constexpr int kBwdChannels = kBwdThreads;      // one channel per lane
-constexpr int TB = kCkptTokens;                // tokens per block (8)
+constexpr int kGradTokens = kCkptTokens;       // tokens per block of the gradient pass (8)
+constexpr int kCarryTokens = 32;               // tokens per block of the reverse-carry pass
 constexpr float kLn2f = 0.6931471805599453f;
 
-// Shared memory of one CTA (N = 16).
-template <typename T, int N>
+// Shared memory of one CTA (N = 16): TB-token blocks; the gradient pass
+// (GRAD) also keeps the block's states, dt and y, and the dB | dC warp sums.
+template <typename T, int N, int TB, bool GRAD>
 struct BwdSmem {
     static constexpr int VEC = 16 / sizeof(T);            // elements per 16-byte chunk
     static constexpr int ROWC = kBwdChannels / VEC;       // chunks per token row of a tile
@@ -59,14 +61,15 @@ struct BwdSmem {
     static constexpr int kX = 0, kDelta = TILE, kZ = 2 * TILE, kDout = 3 * TILE;
     static constexpr int kB = 4 * TILE, kC = 4 * TILE + TB * N;
     static constexpr int IN_ELEMS = 4 * TILE + 2 * TB * N;
-    // byte offsets
+    // byte offsets: two staging buffers (the next block loads while this one computes)
+    static constexpr int IN_BYTES = (IN_ELEMS * int(sizeof(T)) + 127) & ~127;
     static constexpr int oIn = 0;
-    static constexpr int oBC = (IN_ELEMS * int(sizeof(T)) + 127) & ~127;  // fp32 [TB][2N]
+    static constexpr int oBC = 2 * IN_BYTES;                               // fp32 [TB][2N]
     static constexpr int oHist = oBC + TB * 2 * N * 4;                    // float4 [TB][N/4][128]
-    static constexpr int oRed = oHist + TB * (N / 4) * kBwdThreads * 16;   // fp32 [4][TB][32]
-    static constexpr int oDt = oRed + kBwdWarps * TB * 32 * 4;             // float2 [TB][128]
-    static constexpr int oY = oDt + TB * kBwdThreads * 8;                  // fp32 [TB][128]
-    static constexpr int kBytes = oY + TB * kBwdThreads * 4;
+    static constexpr int oRed = oHist + (GRAD ? TB * (N / 4) * kBwdThreads * 16 : 0);  // fp32 [4][TB][32]
+    static constexpr int oDt = oRed + (GRAD ? kBwdWarps * TB * 32 * 4 : 0);  // float2 [TB][128]
+    static constexpr int oY = oDt + (GRAD ? TB * kBwdThreads * 8 : 0);        // fp32 [TB][128]
+    static constexpr int kBytes = oY + (GRAD ? TB * kBwdThreads * 4 : 0);
     static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
     static_assert(N == 16, "the backward is built for dstate 16");
 };
@@ -86,53 +89,66 @@ __device__ __forceinline__ float2 lds_pair(const __nv_bfloat16* p) {
 __device__ __forceinline__ void st_io(float* p, float v) { *p = v; }
 __device__ __forceinline__ void st_io(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
-// One block's inputs into shared memory: the [TB x 128] tiles of x, delta,
-// (z,) dout and the TB rows of B and C, as 16-byte loads spread over the CTA
-// (rows past the end of the sequence and channels past dim read as zero).
-template <typename T, int N, bool GATE, int MODE>
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    const int n = valid ? 16 : 0;   // 0: write zeros, read nothing
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(n)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int K>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(K) : "memory");
+}
+
+// Starts the copies of one block's inputs into shared memory: the [TB x 128]
+// tiles of x, delta, (z,) dout and the TB rows of B and C, as 16-byte
+// asynchronous copies spread over the CTA (rows past the end of the sequence
+// and channels past dim are written as zeros). Tiles the pass does not read
+// are not copied.
+template <typename T, int N, int TB, bool GATE, int MODE>
 __device__ __forceinline__ void stage_block(const BwdArgs& a, T* in, int64_t b, int64_t dbase,
                                             int64_t u0, int cnt) {
-    using Sm = BwdSmem<T, N>;
+    using Sm = BwdSmem<T, N, TB, MODE == 1>;
     constexpr int VEC = Sm::VEC, ROWC = Sm::ROWC;
     constexpr int NTILES = 4;
     constexpr int TILE_CHUNKS = TB * ROWC;
     constexpr int BC_CHUNKS = TB * N / VEC;                  // per B or C
     constexpr int TOTAL = NTILES * TILE_CHUNKS + 2 * BC_CHUNKS;
     for (int i = threadIdx.x; i < TOTAL; i += kBwdThreads) {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        T* dst;
         if (i < NTILES * TILE_CHUNKS) {
             const int which = i / TILE_CHUNKS, r = i % TILE_CHUNKS;
-            const int tt = r / ROWC, c = (r % ROWC) * VEC;
-            dst = in + which * Sm::TILE + tt * kBwdChannels + c;
             // the state-carry pass reads no x; z only with the gate
-            const bool used = (MODE == 1 || which != 0) && (GATE || which != 2);
-            if (used && tt < cnt && dbase + c < a.dim) {
-                const void* base = which == 0 ? a.x : which == 1 ? a.delta : which == 2 ? a.z : a.dout;
-                v = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(base) +
-                                                        ((b * a.L + u0 + tt) * a.dim + dbase + c)));
-            }
+            if ((MODE == 0 && which == 0) || (!GATE && which == 2)) continue;
+            const int tt = r / ROWC, c = (r % ROWC) * VEC;
+            const void* base = which == 0 ? a.x : which == 1 ? a.delta : which == 2 ? a.z : a.dout;
+            const bool valid = tt < cnt && dbase + c < a.dim;
+            const T* src = static_cast<const T*>(base) +
+                           (valid ? (b * a.L + u0 + tt) * a.dim + dbase + c : 0);
+            cp_async16(in + which * Sm::TILE + tt * kBwdChannels + c, src, valid);
         } else {
             const int r = i - NTILES * TILE_CHUNKS;
             const int which = r / BC_CHUNKS, e = (r % BC_CHUNKS) * VEC;
+            if (MODE == 0 && which == 0) continue;           // the carry pass needs no B
             const int tt = e / N, n = e % N;
-            dst = in + (which ? Sm::kC : Sm::kB) + e;
-            const T* src = static_cast<const T*>(which ? a.C : a.B);
-            if (tt < cnt && (MODE == 1 || which == 1))   // the carry pass needs no B
-                v = __ldg(reinterpret_cast<const uint4*>(src + (b * a.L + u0 + tt) * N + n));
+            const bool valid = tt < cnt;
+            const T* src = static_cast<const T*>(which ? a.C : a.B) +
+                           (valid ? (b * a.L + u0 + tt) * N + n : 0);
+            cp_async16(in + (which ? Sm::kC : Sm::kB) + e, src, valid);
         }
-        *reinterpret_cast<uint4*>(dst) = v;
     }
+    cp_async_commit();
 }
 
 // MODE 0: reverse carry of chunks 1 .. nchunks-1 from zero (Q at the chunk's
 // first token, and its sum of dt). MODE 1: the gradients of one chunk.
 template <typename T, int N, bool SOFTPLUS, bool GATE, int MODE>
 __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs a) {
-    using Sm = BwdSmem<T, N>;
+    constexpr int TB = MODE == 1 ? kGradTokens : kCarryTokens;
+    using Sm = BwdSmem<T, N, TB, MODE == 1>;
     constexpr int NS = 2, SPL = N / NS;
     extern __shared__ __align__(128) unsigned char smem[];
-    T* in = reinterpret_cast<T*>(smem + Sm::oIn);
+    T* const in0 = reinterpret_cast<T*>(smem + Sm::oIn);        // two staging buffers
     float* bcs = reinterpret_cast<float*>(smem + Sm::oBC);
     float4* hist = reinterpret_cast<float4*>(smem + Sm::oHist);
     float* red = reinterpret_cast<float*>(smem + Sm::oRed);
@@ -185,11 +201,26 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
     const float Dd = (MODE == 1 && a.D && ch_ok) ? __ldg(a.D + dsafe) : 0.f;
     float dD_acc = 0.f, dbias_acc = 0.f, S_acc = 0.f;
 
+    auto block_start = [&](int blk) { return t_begin + static_cast<int64_t>(blk) * TB; };
+    auto block_count = [&](int blk) {
+        const int64_t u = block_start(blk);
+        return static_cast<int>(t_end - u < TB ? t_end - u : TB);
+    };
+    auto buffer = [&](int blk) { return in0 + (blk & 1) * (Sm::IN_BYTES / int(sizeof(T))); };
+    stage_block<T, N, TB, GATE, MODE>(a, buffer(nblk - 1), b, dbase, block_start(nblk - 1),
+                                      block_count(nblk - 1));
     for (int blk = nblk - 1; blk >= 0; --blk) {
-        const int64_t u0 = t_begin + static_cast<int64_t>(blk) * TB;
-        const int cnt = static_cast<int>(t_end - u0 < TB ? t_end - u0 : TB);
-        __syncthreads();   // the previous block is done with in, bcs and red
-        stage_block<T, N, GATE, MODE>(a, in, b, dbase, u0, cnt);
+        const int64_t u0 = block_start(blk);
+        const int cnt = block_count(blk);
+        T* const in = buffer(blk);
+        __syncthreads();   // the previous block is done with its buffer, bcs and red
+        if (blk > 0) {
+            stage_block<T, N, TB, GATE, MODE>(a, buffer(blk - 1), b, dbase, block_start(blk - 1),
+                                              block_count(blk - 1));
+            cp_async_wait<1>();   // this thread's copies of the current block have landed
+        } else {
+            cp_async_wait<0>();
+        }
         __syncthreads();
         for (int i = tid; i < TB * 2 * N; i += kBwdThreads) {
             const int tt = i / (2 * N), c = i % (2 * N);
@@ -197,18 +228,17 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
         }
         __syncthreads();
 
-        // dt and x of both slots for one token (dt = 0 past the end)
+        // dt and x of both slots for one token (dt = 0 past the end); each lane
+        // forms its own channel's dt and takes the partner's by a shuffle
         auto token = [&](int tt, float (&dt)[NS], float (&xv)[NS]) {
             const float2 xp = lds_pair(in + Sm::kX + tt * kBwdChannels + pc);
             const float2 dp = lds_pair(in + Sm::kDelta + tt * kBwdChannels + pc);
-#pragma unroll
-            for (int r = 0; r < NS; ++r) {
-                const bool hi = (j ^ r) != 0;
-                xv[r] = hi ? xp.y : xp.x;
-                float v = (hi ? dp.y : dp.x) + bias[r];
-                if constexpr (SOFTPLUS) v = softplus(v);
-                dt[r] = (tt < cnt && ch_ok) ? v : 0.f;
-            }
+            xv[0] = j ? xp.y : xp.x;
+            xv[1] = j ? xp.x : xp.y;
+            float v = (j ? dp.y : dp.x) + bias[0];
+            if constexpr (SOFTPLUS) v = softplus(v);
+            dt[0] = (tt < cnt && ch_ok) ? v : 0.f;
+            dt[1] = __shfl_xor_sync(0xffffffffu, dt[0], 1);
         };
 
         if constexpr (MODE == 1) {
@@ -225,7 +255,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
                     h[r][q] = v.x; h[r][q + 1] = v.y; h[r][q + 2] = v.z; h[r][q + 3] = v.w;
                 }
             }
-#pragma unroll 1
+#pragma unroll 2
             for (int tt = 0; tt < TB; ++tt) {
                 float dt[NS], xv[NS], yp[NS];
                 token(tt, dt, xv);
@@ -234,13 +264,21 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
                 const float* Ct = Bt + N;
 #pragma unroll
                 for (int r = 0; r < NS; ++r) {
-                    const float dtx = dt[r] * xv[r];
-                    yp[r] = 0.f;
+                    // packed f32x2 arithmetic over state pairs, as in the forward
+                    const float2 dt2 = make_float2(dt[r], dt[r]);
+                    const float2 dtx2 = make_float2(dt[r] * xv[r], dt[r] * xv[r]);
+                    float2 y2 = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int q = 0; q < SPL; ++q) {
-                        h[r][q] = fmaf(ex2(dt[r] * A2[r][q]), h[r][q], dtx * Bt[q]);
-                        yp[r] = fmaf(Ct[q], h[r][q], yp[r]);
+                    for (int q = 0; q < SPL; q += 2) {
+                        const float2 arg = __fmul2_rn(dt2, make_float2(A2[r][q], A2[r][q + 1]));
+                        const float2 bx = __fmul2_rn(dtx2, make_float2(Bt[q], Bt[q + 1]));
+                        const float2 hn = __ffma2_rn(make_float2(ex2(arg.x), ex2(arg.y)),
+                                                     make_float2(h[r][q], h[r][q + 1]), bx);
+                        h[r][q] = hn.x;
+                        h[r][q + 1] = hn.y;
+                        y2 = __ffma2_rn(make_float2(Ct[q], Ct[q + 1]), hn, y2);
                     }
+                    yp[r] = y2.x + y2.y;
                 }
 #pragma unroll
                 for (int c4 = 0; c4 < N / 4; ++c4) {
@@ -252,48 +290,47 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
                 ys[tt * kBwdThreads + tid] =
                     yp[0] + __shfl_xor_sync(0xffffffffu, yp[1], 1) + Dd * xv[0];
             }
-        } else {
-#pragma unroll 1
-            for (int tt = 0; tt < TB; ++tt) {
-                float dt[NS], xv[NS];
-                token(tt, dt, xv);
-                dts[tt * kBwdThreads + tid] = make_float2(dt[0], dt[1]);
-            }
         }
 
         // ---- reverse sweep over the block ----
-#pragma unroll 1
+#pragma unroll (MODE == 1 ? 2 : 4)
         for (int tt = TB - 1; tt >= 0; --tt) {
             const float* Bt = bcs + tt * 2 * N + j * SPL;
             const float* Ct = Bt + N;
             const float2 gp = lds_pair(in + Sm::kDout + tt * kBwdChannels + pc);
             float zv[NS], dy[NS], dt[NS];
             float gate_ds = 1.f;   // silu'(z) of the own channel
-            {
+            if constexpr (MODE == 1) {
                 const float2 dtp = dts[tt * kBwdThreads + tid];
                 dt[0] = dtp.x;
                 dt[1] = dtp.y;
+            } else {
+                float xv[NS];
+                token(tt, dt, xv);
             }
-#pragma unroll
-            for (int r = 0; r < NS; ++r) dy[r] = ((j ^ r) != 0) ? gp.y : gp.x;
+            dy[0] = j ? gp.y : gp.x;
             if constexpr (GATE) {
                 const float2 zp = lds_pair(in + Sm::kZ + tt * kBwdChannels + pc);
-#pragma unroll
-                for (int r = 0; r < NS; ++r) {
-                    zv[r] = ((j ^ r) != 0) ? zp.y : zp.x;
-                    const float sg = 1.f / (1.f + __expf(-zv[r]));
-                    if (r == 0) gate_ds = sg * fmaf(zv[r], 1.f - sg, 1.f);
-                    dy[r] *= zv[r] * sg;
-                }
+                zv[0] = j ? zp.y : zp.x;
+                const float sg = 1.f / (1.f + __expf(-zv[0]));
+                gate_ds = sg * fmaf(zv[0], 1.f - sg, 1.f);
+                dy[0] *= zv[0] * sg;
             }
+            dy[1] = __shfl_xor_sync(0xffffffffu, dy[0], 1);   // the partner's channel
             if constexpr (MODE == 0) {
 #pragma unroll
-                for (int r = 0; r < NS; ++r)
+                for (int r = 0; r < NS; ++r) {
+                    const float2 dt2 = make_float2(dt[r], dt[r]), dy2 = make_float2(dy[r], dy[r]);
 #pragma unroll
-                    for (int q = 0; q < SPL; ++q) {
-                        const float g = fmaf(dy[r], Ct[q], Q[r][q]);
-                        Q[r][q] = ex2(dt[r] * A2[r][q]) * g;
+                    for (int q = 0; q < SPL; q += 2) {
+                        const float2 g = __ffma2_rn(dy2, make_float2(Ct[q], Ct[q + 1]),
+                                                    make_float2(Q[r][q], Q[r][q + 1]));
+                        const float2 arg = __fmul2_rn(dt2, make_float2(A2[r][q], A2[r][q + 1]));
+                        const float2 qn = __fmul2_rn(make_float2(ex2(arg.x), ex2(arg.y)), g);
+                        Q[r][q] = qn.x;
+                        Q[r][q + 1] = qn.y;
                     }
+                }
                 S_acc += dt[0];
             } else {
                 float xv[NS];
@@ -314,22 +351,38 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
                 for (int q = 0; q < 2 * SPL; ++q) vals[q] = 0.f;
 #pragma unroll
                 for (int r = 0; r < NS; ++r) {
+                    // packed f32x2 arithmetic over state pairs
                     const float dtx = dt[r] * xv[r];
-                    dxs[r] = 0.f;
-                    saw[r] = 0.f;
+                    const float2 dt2 = make_float2(dt[r], dt[r]), dy2 = make_float2(dy[r], dy[r]);
+                    const float2 dtx2 = make_float2(dtx, dtx), ndtx2 = make_float2(-dtx, -dtx);
+                    float2 dxs2 = make_float2(0.f, 0.f), saw2 = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int q = 0; q < SPL; ++q) {
-                        const float av = ex2(dt[r] * A2[r][q]);
-                        const float wv = fmaf(-dtx, Bt[q], hreg[r][q]);     // a * h_{t-1}
-                        const float g = fmaf(dy[r], Ct[q], Q[r][q]);        // dLoss/dh_t
-                        dxs[r] = fmaf(g, Bt[q], dxs[r]);
-                        const float gw = g * wv;
-                        saw[r] = fmaf(gw, A2[r][q], saw[r]);
-                        dA[r][q] = fmaf(gw, dt[r], dA[r][q]);
-                        vals[q] = fmaf(g, dtx, vals[q]);                    // dB
-                        vals[SPL + q] = fmaf(dy[r], hreg[r][q], vals[SPL + q]);  // dC
-                        Q[r][q] = av * g;
+                    for (int q = 0; q < SPL; q += 2) {
+                        const float2 B2 = make_float2(Bt[q], Bt[q + 1]);
+                        const float2 h2 = make_float2(hreg[r][q], hreg[r][q + 1]);
+                        const float2 A22 = make_float2(A2[r][q], A2[r][q + 1]);
+                        const float2 arg = __fmul2_rn(dt2, A22);
+                        const float2 wv = __ffma2_rn(ndtx2, B2, h2);              // a * h_{t-1}
+                        const float2 g = __ffma2_rn(dy2, make_float2(Ct[q], Ct[q + 1]),
+                                                    make_float2(Q[r][q], Q[r][q + 1]));  // dLoss/dh_t
+                        dxs2 = __ffma2_rn(g, B2, dxs2);
+                        const float2 gw = __fmul2_rn(g, wv);
+                        saw2 = __ffma2_rn(gw, A22, saw2);
+                        const float2 da = __ffma2_rn(gw, dt2, make_float2(dA[r][q], dA[r][q + 1]));
+                        dA[r][q] = da.x;
+                        dA[r][q + 1] = da.y;
+                        const float2 vb = __ffma2_rn(g, dtx2, make_float2(vals[q], vals[q + 1]));
+                        vals[q] = vb.x;                                           // dB
+                        vals[q + 1] = vb.y;
+                        const float2 vc = __ffma2_rn(dy2, h2, make_float2(vals[SPL + q], vals[SPL + q + 1]));
+                        vals[SPL + q] = vc.x;                                     // dC
+                        vals[SPL + q + 1] = vc.y;
+                        const float2 qn = __fmul2_rn(make_float2(ex2(arg.x), ex2(arg.y)), g);
+                        Q[r][q] = qn.x;
+                        Q[r][q + 1] = qn.y;
                     }
+                    dxs[r] = dxs2.x + dxs2.y;
+                    saw[r] = saw2.x + saw2.y;
                 }
                 const float dxs_own = dxs[0] + __shfl_xor_sync(0xffffffffu, dxs[1], 1);
                 const float saw_own = saw[0] + __shfl_xor_sync(0xffffffffu, saw[1], 1);
@@ -447,7 +500,7 @@ __global__ void __launch_bounds__(256) scan_bwd_reduce_kernel(const BwdArgs a) {
 
 template <typename T, int N, bool SOFTPLUS, bool GATE, int MODE>
 cudaError_t launch_mode(const BwdArgs& a, int64_t ctas, cudaStream_t s) {
-    using Sm = BwdSmem<T, N>;
+    using Sm = BwdSmem<T, N, MODE == 1 ? kGradTokens : kCarryTokens, MODE == 1>;
     static std::mutex mu;
     static bool done[128] = {};
     int dev = 0;
