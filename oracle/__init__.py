@@ -65,12 +65,15 @@ def _bind(lib):
     lib.oracle_silu.argtypes = [ctypes.c_double]
     lib.oracle_recurrence.restype = None
     lib.oracle_recurrence.argtypes = [_i64, _i64, _dp, _dp, _dp, _dp, _dp, _dp]
-    lib.oracle_selective_scan.restype = ctypes.c_int
-    lib.oracle_selective_scan.argtypes = (
-        [_i64] * 4 + [_dp] * 8 + [ctypes.c_int] + [_dp] * 3 + [ctypes.c_int])
-    lib.oracle_state_update.restype = ctypes.c_int
-    lib.oracle_state_update.argtypes = (
-        [_i64] * 3 + [_dp] * 9 + [ctypes.c_int] + [_dp])
+    for name in ("oracle_selective_scan", "oracle_selective_scan_zoh"):
+        getattr(lib, name).restype = ctypes.c_int
+        getattr(lib, name).argtypes = (
+            [_i64] * 4 + [_dp] * 8 + [ctypes.c_int] + [_dp] * 3 + [ctypes.c_int])
+    for name in ("oracle_state_update", "oracle_state_update_zoh"):
+        getattr(lib, name).restype = ctypes.c_int
+        getattr(lib, name).argtypes = [_i64] * 3 + [_dp] * 9 + [ctypes.c_int] + [_dp]
+    lib.oracle_phi.restype = ctypes.c_double
+    lib.oracle_phi.argtypes = [ctypes.c_double]
     lib.oracle_causal_conv1d_silu.restype = None
     lib.oracle_causal_conv1d_silu.argtypes = [_i64] * 4 + [_dp] * 4
     lib.oracle_selective_scan_bwd.restype = ctypes.c_int
@@ -123,9 +126,13 @@ class Oracle:
         self._lib.oracle_recurrence(L, N, _ptr(Abar), _ptr(Bbar), _ptr(C), _ptr(x), _ptr(h), _ptr(y))
         return y, h
 
+    def phi(self, z: float) -> float:
+        return self._lib.oracle_phi(float(z))
+
     def selective_scan(self, x, delta, A, B, C, D=None, z=None, delta_bias=None,
-                       delta_softplus=False, h0=None, nthreads=None):
-        """Selective scan over [batch, L, dim] with a [dim, N] diagonal A.
+                       delta_softplus=False, h0=None, nthreads=None, zoh=False):
+        """Selective scan over [batch, L, dim] with a [dim, N] diagonal A;
+        zoh=True takes the exact zero-order-hold Bbar = dt * phi(dt A) * B.
 
         Returns (out [batch, L, dim], final_state [batch, dim, N]), both float64.
         """
@@ -142,7 +149,8 @@ class Oracle:
         h0 = _f64(h0, (batch, dim, N))
         out = np.zeros((batch, L, dim), dtype=np.float64)
         fs = np.zeros((batch, dim, N), dtype=np.float64)
-        rc = self._lib.oracle_selective_scan(
+        fn = self._lib.oracle_selective_scan_zoh if zoh else self._lib.oracle_selective_scan
+        rc = fn(
             batch, L, dim, N, _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
             _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(out),
             _ptr(fs), int(nthreads or default_threads()))
@@ -151,7 +159,7 @@ class Oracle:
         return out, fs
 
     def state_update(self, state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
-                     delta_softplus=False):
+                     delta_softplus=False, zoh=False):
         """One recurrent step. state: [batch, dim, N] (not modified; a new array is
         returned). x, delta, z: [batch, dim]; B, C: [batch, N].
 
@@ -165,7 +173,8 @@ class Oracle:
         D, z = _f64(D, (dim,)), _f64(z, (batch, dim))
         delta_bias = _f64(delta_bias, (dim,))
         out = np.zeros((batch, dim), dtype=np.float64)
-        rc = self._lib.oracle_state_update(
+        fn = self._lib.oracle_state_update_zoh if zoh else self._lib.oracle_state_update
+        rc = fn(
             batch, dim, N, _ptr(st), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
             _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(out))
         if rc != 0:
@@ -242,6 +251,10 @@ def softplus(v):
 
 def silu(z):
     return default().silu(z)
+
+
+def phi(z):
+    return default().phi(z)
 
 
 def recurrence(*a, **k):

@@ -51,6 +51,16 @@ double oracle_softplus(double v) { return fmax(v, 0.0) + log1p(exp(-fabs(v))); }
 double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
 
 /*
+ * phi(z) = (e^z - 1) / z, with phi(0) = 1: the exact zero-order-hold input
+ * matrix of a diagonal state is Bbar = A^-1 (e^{A dt} - 1) B = dt * phi(dt A) * B
+ * ("State-space models (Mamba, S4)", section "From Continuous to Discrete: The
+ * Key Step": the exact solution for an input held constant over the step; and
+ * its flashcard Bbar = (A^-1 (e^{A Delta} - I)) B). expm1 keeps it accurate as
+ * z -> 0, where it tends to 1 and the first-order form dt * B is recovered.
+ */
+double oracle_phi(double z) { return z == 0.0 ? 1.0 : expm1(z) / z; }
+
+/*
  * The recurrence with the discretized parameters given directly, one channel:
  *   h[n] <- Abar[t,n] * h[n] + Bbar[t,n] * x[t]
  *   y[t]  = sum_n C[t,n] * h[n]           (h after the update)
@@ -74,6 +84,7 @@ typedef struct {
     int64_t batch, L, dim, N;
     const double *x, *delta, *A, *B, *C, *D, *z, *delta_bias, *h0;
     int delta_softplus;
+    int zoh;                      /* exact zero-order-hold Bbar instead of dt * B */
     double *out, *final_state;
     int64_t chan_begin, chan_end; /* channel = b * dim + d */
 } scan_job;
@@ -96,7 +107,8 @@ static void scan_channel(const scan_job* j, int64_t b, int64_t d, double* h)
         double acc = 0.0;
         for (int64_t n = 0; n < N; ++n) {
             const double dA = exp(dt * j->A[d * N + n]);          /* Abar */
-            const double dBx = dt * j->B[(b * L + t) * N + n] * xv; /* Bbar x */
+            const double dBx = dt * j->B[(b * L + t) * N + n] * xv  /* Bbar x */
+                               * (j->zoh ? oracle_phi(dt * j->A[d * N + n]) : 1.0);
             h[n] = dA * h[n] + dBx;
             acc += j->C[(b * L + t) * N + n] * h[n];
         }
@@ -127,11 +139,38 @@ static void* scan_worker(void* arg)
  * are split across nthreads POSIX threads; each channel is one sequential loop.
  * Returns 0, or -1 on bad arguments / thread failure.
  */
+static int scan_run(int64_t batch, int64_t L, int64_t dim, int64_t N, const double* x,
+                    const double* delta, const double* A, const double* B, const double* C,
+                    const double* D, const double* z, const double* delta_bias,
+                    int delta_softplus, int zoh, const double* h0, double* out,
+                    double* final_state, int nthreads);
+
 int oracle_selective_scan(int64_t batch, int64_t L, int64_t dim, int64_t N,
                           const double* x, const double* delta, const double* A,
                           const double* B, const double* C, const double* D,
                           const double* z, const double* delta_bias, int delta_softplus,
                           const double* h0, double* out, double* final_state, int nthreads)
+{
+    return scan_run(batch, L, dim, N, x, delta, A, B, C, D, z, delta_bias, delta_softplus, 0,
+                    h0, out, final_state, nthreads);
+}
+
+/* The same scan with the exact zero-order-hold Bbar = dt * phi(dt A) * B. */
+int oracle_selective_scan_zoh(int64_t batch, int64_t L, int64_t dim, int64_t N,
+                              const double* x, const double* delta, const double* A,
+                              const double* B, const double* C, const double* D,
+                              const double* z, const double* delta_bias, int delta_softplus,
+                              const double* h0, double* out, double* final_state, int nthreads)
+{
+    return scan_run(batch, L, dim, N, x, delta, A, B, C, D, z, delta_bias, delta_softplus, 1,
+                    h0, out, final_state, nthreads);
+}
+
+static int scan_run(int64_t batch, int64_t L, int64_t dim, int64_t N, const double* x,
+                    const double* delta, const double* A, const double* B, const double* C,
+                    const double* D, const double* z, const double* delta_bias,
+                    int delta_softplus, int zoh, const double* h0, double* out,
+                    double* final_state, int nthreads)
 {
     if (batch < 0 || L < 0 || dim < 0 || N <= 0) return -1;
     if (!x || !delta || !A || !B || !C || !out) return -1;
@@ -147,6 +186,7 @@ int oracle_selective_scan(int64_t batch, int64_t L, int64_t dim, int64_t N,
         j->batch = batch; j->L = L; j->dim = dim; j->N = N;
         j->x = x; j->delta = delta; j->A = A; j->B = B; j->C = C; j->D = D; j->z = z;
         j->delta_bias = delta_bias; j->h0 = h0; j->delta_softplus = delta_softplus;
+        j->zoh = zoh;
         j->out = out; j->final_state = final_state;
         j->chan_begin = nchan * i / nthreads;
         j->chan_end = nchan * (i + 1) / nthreads;
@@ -172,11 +212,36 @@ int oracle_selective_scan(int64_t batch, int64_t L, int64_t dim, int64_t N,
  * above on a persisted state, updated in place.
  *   state : [batch, dim, N]   x, delta, z, out : [batch, dim]   B, C : [batch, N]
  */
+static int state_update_run(int64_t batch, int64_t dim, int64_t N, double* state,
+                            const double* x, const double* delta, const double* A,
+                            const double* B, const double* C, const double* D, const double* z,
+                            const double* delta_bias, int delta_softplus, int zoh, double* out);
+
 int oracle_state_update(int64_t batch, int64_t dim, int64_t N, double* state,
                         const double* x, const double* delta, const double* A,
                         const double* B, const double* C, const double* D,
                         const double* z, const double* delta_bias, int delta_softplus,
                         double* out)
+{
+    return state_update_run(batch, dim, N, state, x, delta, A, B, C, D, z, delta_bias,
+                            delta_softplus, 0, out);
+}
+
+/* The same step with the exact zero-order-hold Bbar. */
+int oracle_state_update_zoh(int64_t batch, int64_t dim, int64_t N, double* state,
+                            const double* x, const double* delta, const double* A,
+                            const double* B, const double* C, const double* D,
+                            const double* z, const double* delta_bias, int delta_softplus,
+                            double* out)
+{
+    return state_update_run(batch, dim, N, state, x, delta, A, B, C, D, z, delta_bias,
+                            delta_softplus, 1, out);
+}
+
+static int state_update_run(int64_t batch, int64_t dim, int64_t N, double* state,
+                            const double* x, const double* delta, const double* A,
+                            const double* B, const double* C, const double* D, const double* z,
+                            const double* delta_bias, int delta_softplus, int zoh, double* out)
 {
     if (batch < 0 || dim < 0 || N <= 0) return -1;
     if (!state || !x || !delta || !A || !B || !C || !out) return -1;
@@ -190,7 +255,8 @@ int oracle_state_update(int64_t batch, int64_t dim, int64_t N, double* state,
             double acc = 0.0;
             for (int64_t n = 0; n < N; ++n) {
                 double* h = &state[e * N + n];
-                *h = exp(dt * A[d * N + n]) * (*h) + dt * B[b * N + n] * xv;
+                *h = exp(dt * A[d * N + n]) * (*h) + dt * B[b * N + n] * xv
+                     * (zoh ? oracle_phi(dt * A[d * N + n]) : 1.0);
                 acc += C[b * N + n] * (*h);
             }
             double y = acc;

@@ -532,7 +532,96 @@ def pin_bwd_channel_sums(orc, seed=33):
             _close(g4[k], g[k], 1e-12, 1e-14, "%s, 4 threads vs 1" % k)
 
 
+# --------------------------------------------------------------------------
+# exact zero-order hold ("State-space models (Mamba, S4)", "From Continuous to
+# Discrete: The Key Step": exact for an input held constant over each step)
+# --------------------------------------------------------------------------
+def pin_phi(orc):
+    """phi(z) = (e^z - 1)/z: 1 at 0, its Taylor series near 0, numpy elsewhere."""
+    assert orc.phi(0.0) == 1.0
+    for zz in (1e-9, -1e-7, 3e-5):
+        series = 1 + zz / 2 + zz * zz / 6
+        _close(orc.phi(zz), series, 1e-15, 0.0, "phi series at %g" % zz)
+    for zz in (-20.0, -1.5, -0.3, 0.7, 2.0):
+        _close(orc.phi(zz), np.expm1(zz) / zz, 1e-15, 0.0, "phi at %g" % zz)
+
+
+def pin_zoh_closed_form(orc, seed=41):
+    """Constant dt, x, B: L ZOH steps land exactly on the continuous solution
+    h(T) = e^{AT} h0 + (e^{AT} - 1)/A B x at T = L dt, for any L; y reads it."""
+    r = _rng(seed)
+    N, L = 4, 37
+    A = -np.exp(r.standard_normal((1, N)))
+    B = r.standard_normal(N)
+    C = r.standard_normal(N)
+    h0 = r.standard_normal((1, 1, N))
+    dt, xv, Dv = 0.07, 0.8, 1.3
+    x = np.full((1, L, 1), xv)
+    out, fs = orc.selective_scan(x, np.full((1, L, 1), dt), A, np.tile(B, (1, L, 1)),
+                                 np.tile(C, (1, L, 1)), D=np.array([Dv]), h0=h0, zoh=True)
+    for k in (1, 5, L):
+        T = k * dt
+        hk = np.exp(A[0] * T) * h0[0, 0] + np.expm1(A[0] * T) / A[0] * B * xv
+        if k == L:
+            _close(fs[0, 0], hk, 1e-12, 1e-14, "ZOH final state vs continuous solution")
+        _close(out[0, k - 1, 0], C @ hk + Dv * xv, 1e-12, 1e-14, "ZOH y_%d" % k)
+
+
+def pin_zoh_ode(orc, seed=42):
+    """Per-token inputs: each ZOH step equals integrating h' = A h + B_t x_t over
+    [0, dt_t] numerically (scipy solve_ivp, rtol 1e-12); first-order dt B does not."""
+    from scipy.integrate import solve_ivp
+    r = _rng(seed)
+    N, L = 3, 12
+    A = -np.exp(r.standard_normal((1, N)) * 0.7)
+    B = r.standard_normal((1, L, N))
+    C = r.standard_normal((1, L, N))
+    x = r.standard_normal((1, L, 1))
+    dt = r.uniform(0.05, 0.6, (1, L, 1))
+    h = r.standard_normal(N)
+    out, fs = orc.selective_scan(x, dt, A, B, C, h0=h[None, None, :], zoh=True)
+    for t in range(L):
+        sol = solve_ivp(lambda _, y: A[0] * y + B[0, t] * x[0, t, 0], (0.0, dt[0, t, 0]), h,
+                        rtol=1e-12, atol=1e-14, method="DOP853")
+        h = sol.y[:, -1]
+        _close(out[0, t, 0], C[0, t] @ h, 1e-9, 1e-11, "ZOH y_%d vs ODE" % t)
+    _close(fs[0, 0], h, 1e-9, 1e-11, "ZOH final state vs ODE")
+    out1, _ = orc.selective_scan(x, dt, A, B, C, h0=None)
+    outz, _ = orc.selective_scan(x, dt, A, B, C, h0=None, zoh=True)
+    assert np.abs(out1 - outz).max() > 1e-3, "first-order and ZOH must differ at these steps"
+
+
+def pin_zoh_small_step(orc, seed=43):
+    """As dt -> 0, ZOH tends to the first-order form: the difference per step is
+    dt B x (phi(dt A) - 1) ~ dt^2 A B x / 2."""
+    r = _rng(seed)
+    c = _random_case(r, batch=1, L=16, dim=3, N=4)
+    small = np.full_like(c["delta"], 1e-6)
+    o1, f1 = orc.selective_scan(c["x"], small, c["A"], c["B"], c["C"], D=c["D"])
+    oz, fz = orc.selective_scan(c["x"], small, c["A"], c["B"], c["C"], D=c["D"], zoh=True)
+    _close(oz, o1, 1e-5, 1e-12, "ZOH -> first order as dt -> 0")
+    assert np.abs(fz - f1).max() > 0.0
+
+
+def pin_zoh_decode(orc, seed=44):
+    """The ZOH decode step is one token of the ZOH scan from the same state."""
+    r = _rng(seed)
+    c = _random_case(r, batch=2, L=1, dim=3, N=4)
+    st = r.standard_normal((2, 3, 4))
+    oz, fz = orc.selective_scan(c["x"], c["delta"], c["A"], c["B"], c["C"], D=c["D"], z=c["z"],
+                                h0=st, zoh=True)
+    od, sd = orc.state_update(st, c["x"][:, 0], c["delta"][:, 0], c["A"], c["B"][:, 0],
+                              c["C"][:, 0], D=c["D"], z=c["z"][:, 0], zoh=True)
+    _close(od, oz[:, 0], 1e-14, 1e-15, "ZOH decode y")
+    _close(sd, fz, 1e-14, 1e-15, "ZOH decode state")
+
+
 ALL_PINS = [
+    pin_phi,
+    pin_zoh_closed_form,
+    pin_zoh_ode,
+    pin_zoh_small_step,
+    pin_zoh_decode,
     pin_bwd_finite_differences,
     pin_bwd_autograd,
     pin_bwd_channel_sums,

@@ -52,6 +52,11 @@ MUTANTS = [
     ("conv_drops_bias", "double pre = bias ? bias[d] : 0.0;", "double pre = 0.0;"),
     ("conv_without_silu", "u[(b * L + t) * dim + d] = oracle_silu(pre);",
      "u[(b * L + t) * dim + d] = pre;"),
+    ("zoh_phi_drops_division", "return z == 0.0 ? 1.0 : expm1(z) / z;",
+     "return z == 0.0 ? 1.0 : expm1(z);"),
+    ("zoh_ignored_in_scan", "* (j->zoh ? oracle_phi(dt * j->A[d * N + n]) : 1.0);", "* 1.0;"),
+    ("zoh_phi_wrong_sign", "oracle_phi(dt * j->A[d * N + n])", "oracle_phi(-dt * j->A[d * N + n])"),
+    ("zoh_ignored_in_decode", "* (zoh ? oracle_phi(dt * A[d * N + n]) : 1.0);", "* 1.0;"),
     ("bwd_dC_reads_state_before_update", "j->dC[(b * L + t) * N + n] += dy * ht;",
      "j->dC[(b * L + t) * N + n] += dy * hprev;"),
     ("bwd_carry_drops_decay", "G[n] = a * g;", "G[n] = g;"),
