@@ -96,8 +96,21 @@ typedef struct {
                                  0..3 of the scan: 4, 2, 1 or 3 warps per CTA
                                  (32 channels per warp); dstate 16 only,
                                  other dstate always use configuration 0      */
-    int32_t reserved;         /* must be 0 */
+    int32_t flags;            /* SSM_FLAG_* bits; 0 for the defaults          */
 } ssm_dims;
+
+/*
+ * SSM_FLAG_ZOH -- the exact zero-order-hold input matrix instead of the first-
+ * order dt * B: Bbar = A^-1 (e^{A dt} - 1) B = dt * phi(dt A) * B with phi(z) =
+ * (e^z - 1) / z ("State-space models (Mamba, S4)", "From Continuous to
+ * Discrete: The Key Step": the exact solution for an input held constant over
+ * the step, and its flashcard Bbar = (A^-1 (e^{A Delta} - I)) B). Abar is the
+ * same exp(dt A) either way. Taken by ssm_selective_scan_fwd,
+ * ssm_selective_scan_fwd_from_state, ssm_selective_scan_fwd_static (dstate 16,
+ * tile_config_hint 0 or 1) and ssm_state_update (any dstate); the other entry
+ * points return SSM_ERR_DIMS when it is set. Any other bit is SSM_ERR_DIMS.
+ */
+#define SSM_FLAG_ZOH 1
 
 /*
  * ssm_selective_scan_fwd -- the selective scan over a whole sequence.

@@ -69,6 +69,7 @@ int check_dims(const ssm_dims* d, bool scan) {
     if (scan && d->chunk_len_hint < 0) return SSM_ERR_DIMS;
     if (scan && (d->tile_config_hint < 0 || d->tile_config_hint > ssm::kScanTileConfigs))
         return SSM_ERR_DIMS;
+    if (d->flags & ~SSM_FLAG_ZOH) return SSM_ERR_DIMS;
     const int64_t L = scan ? d->seqlen : 1;
     if (d->batch > 0 && d->dim > 0 && L > 0 &&
         (d->batch > kMaxElems / d->dim || d->batch * d->dim > kMaxElems / L))
@@ -268,6 +269,11 @@ int scan_impl(const void* x, const void* delta, const float* A, const void* B, c
     if (ckpt && (dims->dstate != 16 || dims->tile_config_hint > 1)) return SSM_ERR_DIMS;
     // the fused input stage runs tile configuration 0 only
     if (cv.w && dims->dstate == 16 && dims->tile_config_hint > 1) return SSM_ERR_DIMS;
+    // the exact zero-order hold is built for dstate 16, tile configuration 0,
+    // without the fused input stage or checkpoints
+    if ((dims->flags & SSM_FLAG_ZOH) &&
+        (dims->dstate != 16 || dims->tile_config_hint > 1 || cv.w || ckpt))
+        return SSM_ERR_DIMS;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // Empty problems: nothing to read (empty tensors may carry NULL pointers).
     if (dims->batch == 0 || dims->dim == 0) return SSM_OK;
@@ -321,6 +327,7 @@ int scan_impl(const void* x, const void* delta, const float* A, const void* B, c
     a.h0 = h0;
     a.conv_w = cv.w; a.conv_b = cv.b; a.conv_k = cv.k;
     a.ckpt = ckpt; a.nckpt = (L + ssm::kCkptTokens - 1) / ssm::kCkptTokens;
+    a.zoh = (dims->flags & SSM_FLAG_ZOH) ? 1 : 0;
     a.out = out; a.final_state = final_state;
     a.batch = batch; a.L = L; a.dim = dim;
     a.chunk_len = p.chunk_len; a.nchunks = p.nchunks; a.tiles = p.tiles;
@@ -404,7 +411,7 @@ int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A, con
                            const ssm_dims* dims, ssm_stream_t stream) {
     int rc = check_dims(dims, true);
     if (rc != SSM_OK) return rc;
-    if (dims->dstate != 16 || dims->tile_config_hint > 1) return SSM_ERR_DIMS;
+    if (dims->dstate != 16 || dims->tile_config_hint > 1 || dims->flags) return SSM_ERR_DIMS;
     if (dims->batch == 0 || dims->dim == 0) return SSM_OK;
     if ((z == nullptr) != (dz == nullptr) && dims->seqlen > 0) return SSM_ERR_NULL;
     if (!dA) return SSM_ERR_NULL;
@@ -487,7 +494,7 @@ int ssm_causal_conv1d_silu(const void* x, const float* conv_w, const float* conv
     if (conv_k < 1 || conv_k > ssm::kMaxConvK) return SSM_ERR_DIMS;
     // only the [batch, seqlen, dim] sizes and io_dtype matter here
     ssm_dims d = *dims;
-    d.dstate = 16; d.chunk_len_hint = 0; d.tile_config_hint = 0;
+    d.dstate = 16; d.chunk_len_hint = 0; d.tile_config_hint = 0; d.flags = 0;
     int rc = check_dims(&d, true);
     if (rc != SSM_OK) return rc;
     if (d.batch == 0 || d.seqlen == 0 || d.dim == 0) return SSM_OK;
@@ -542,6 +549,7 @@ int ssm_state_update(float* state, const void* x, const void* delta, const float
     a.state = state; a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
     a.delta_bias = delta_bias; a.softplus = delta_softplus ? 1 : 0; a.out = out;
     a.batch = batch; a.dim = dim;
+    a.zoh = (dims->flags & SSM_FLAG_ZOH) ? 1 : 0;
     return set_cuda(ssm::launch_state_update(a, dims->io_dtype, static_cast<int>(N),
                                              reinterpret_cast<cudaStream_t>(stream)));
 }

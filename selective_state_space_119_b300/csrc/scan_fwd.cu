@@ -187,6 +187,43 @@ __device__ __forceinline__ float state_step(float dt, float dtx, const float* __
     }
 }
 
+// The same step with the exact zero-order-hold input term: Bbar x = x B m with
+// m = dt phi(dt A) = (e^{dt A} - 1) / A. Near z = dt A = 0 the difference
+// e^z - 1 of the SFU's 2^s loses ~2e-7 / |z| of relative accuracy, so for
+// |z| < 0.1 m = dt (1 + z/2 + z^2/6 + z^3/24 + z^4/120) (truncation < 1.4e-8);
+// elsewhere m = (2^s - 1) * (1 / A) with 1 / A kept per state (no division).
+template <int SPL, bool READOUT>
+__device__ __forceinline__ float state_step_zoh(float dt, float xv, const float* __restrict__ bc,
+                                                const float (&A2)[SPL], const float (&invA)[SPL],
+                                                float (&h)[SPL]) {
+    static_assert(SPL % 2 == 0, "pairs of states");
+    float2 acc = make_float2(0.f, 0.f);
+    const float2 dt2 = make_float2(dt, dt), x2 = make_float2(xv, xv);
+    const float2 ln2 = make_float2(0.6931471805599453f, 0.6931471805599453f);
+    const float2 one = make_float2(1.f, 1.f), mone = make_float2(-1.f, -1.f);
+#pragma unroll
+    for (int q = 0; q < SPL; q += 2) {
+        const float2 arg = __fmul2_rn(dt2, make_float2(A2[q], A2[q + 1]));
+        const float2 dA = make_float2(ex2(arg.x), ex2(arg.y));
+        const float2 zz = __fmul2_rn(arg, ln2);
+        float2 p = __ffma2_rn(zz, make_float2(1.f / 120.f, 1.f / 120.f),
+                              make_float2(1.f / 24.f, 1.f / 24.f));
+        p = __ffma2_rn(zz, p, make_float2(1.f / 6.f, 1.f / 6.f));
+        p = __ffma2_rn(zz, p, make_float2(0.5f, 0.5f));
+        p = __ffma2_rn(zz, p, one);
+        const float2 ms = __fmul2_rn(dt2, p);
+        const float2 mf = __fmul2_rn(__ffma2_rn(dA, one, mone), make_float2(invA[q], invA[q + 1]));
+        const float2 m = make_float2(fabsf(zz.x) < 0.1f ? ms.x : mf.x,
+                                     fabsf(zz.y) < 0.1f ? ms.y : mf.y);
+        const float2 bx = __fmul2_rn(__fmul2_rn(x2, make_float2(bc[q], bc[q + 1])), m);
+        const float2 hn = __ffma2_rn(dA, make_float2(h[q], h[q + 1]), bx);
+        h[q] = hn.x;
+        h[q + 1] = hn.y;
+        if constexpr (READOUT) acc = __ffma2_rn(make_float2(bc[SPL + q], bc[SPL + q + 1]), hn, acc);
+    }
+    return acc.x + acc.y;
+}
+
 __device__ __forceinline__ void sts_elem(float* p, float v) { *p = v; }
 __device__ __forceinline__ void sts_elem(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 __device__ __forceinline__ float lds_elem(const float* p) { return *p; }
@@ -200,7 +237,7 @@ __device__ __forceinline__ float lds_elem(const __nv_bfloat16* p) {
 // that the per-token body has no branches and the compiler can overlap
 // successive tokens.
 template <typename T, int N, typename TC, int MODE, bool SOFTPLUS, bool GATE, bool CONV,
-          bool CKPT = false>
+          bool CKPT = false, bool ZOH = false>
 __global__ void __launch_bounds__(Cfg<T, N, TC>::THREADS, 1)
 scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dt,
             const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
@@ -299,6 +336,14 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     }
     const float bias = (a.delta_bias && ch_ok) ? __ldg(a.delta_bias + dsafe) : 0.f;
     const float Dd = (MODE == 1 && a.D && ch_ok) ? __ldg(a.D + dsafe) : 0.f;
+    float invA[NS][SPL];   // 1 / A per state (exact zero-order hold only)
+    if constexpr (ZOH) {
+#pragma unroll
+        for (int r = 0; r < NS; ++r)
+#pragma unroll
+            for (int q = 0; q < SPL; ++q)
+                invA[r][q] = A2[r][q] != 0.f ? kLog2e / A2[r][q] : 0.f;
+    }
     // conv taps of the own channel, right-aligned in a width-4 window (the
     // last tap multiplies the current token)
     float cw[kConvMaxK], cb = 0.f;
@@ -366,7 +411,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         // (The prefetch after the last token wraps to token 0 of the stage and
         // is discarded.)
         struct Tok {
-            float dt[NS], dtx[NS], x;
+            float dt[NS], dtx[NS], x, xp;   // xp: the partner's x (exact zero-order hold)
         };
         const int lim = static_cast<int>(t_end - t0 < TS ? t_end - t0 : TS);  // valid tokens
         auto prep = [&](int tl) {
@@ -388,6 +433,7 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             if constexpr (NS == 2) {
                 k.dt[1] = __shfl_xor_sync(0xffffffffu, k.dt[0], 1);
                 k.dtx[1] = __shfl_xor_sync(0xffffffffu, k.dtx[0], 1);
+                if constexpr (ZOH) k.xp = __shfl_xor_sync(0xffffffffu, k.x, 1);
             }
             return k;
         };
@@ -425,7 +471,11 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 float part[NS];
 #pragma unroll
                 for (int r = 0; r < NS; ++r)
-                    part[r] = state_step<SPL, true>(cur.dt[r], cur.dtx[r], bv, A2[r], h[r]);
+                    if constexpr (ZOH)
+                        part[r] = state_step_zoh<SPL, true>(cur.dt[r], r ? cur.xp : cur.x, bv,
+                                                            A2[r], invA[r], h[r]);
+                    else
+                        part[r] = state_step<SPL, true>(cur.dt[r], cur.dtx[r], bv, A2[r], h[r]);
                 float y = part[0];
                 if constexpr (NS == 2) y += __shfl_xor_sync(0xffffffffu, part[1], 1);
                 y = fmaf(Dd, cur.x, y);
@@ -437,7 +487,11 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 dt_sum += cur.dt[0];
 #pragma unroll
                 for (int r = 0; r < NS; ++r)
-                    state_step<SPL, false>(cur.dt[r], cur.dtx[r], bv, A2[r], h[r]);
+                    if constexpr (ZOH)
+                        state_step_zoh<SPL, false>(cur.dt[r], r ? cur.xp : cur.x, bv, A2[r],
+                                                   invA[r], h[r]);
+                    else
+                        state_step<SPL, false>(cur.dt[r], cur.dtx[r], bv, A2[r], h[r]);
             }
             cur = nxt;
         }
@@ -537,7 +591,8 @@ cudaError_t make_tmap(CUtensorMap* tm, const void* base, int64_t batch, int64_t 
 
 // Raise the dynamic shared-memory limit of one kernel instantiation, once per
 // device (the statics are per instantiation).
-template <typename T, int N, typename TC, int MODE, bool SP, bool GATE, bool CONV, bool CKPT>
+template <typename T, int N, typename TC, int MODE, bool SP, bool GATE, bool CONV, bool CKPT,
+          bool ZOH>
 cudaError_t allow_smem() {
     static std::mutex mu;
     static bool done[128] = {};
@@ -547,14 +602,15 @@ cudaError_t allow_smem() {
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(scan_kernel<T, N, TC, MODE, SP, GATE, CONV, CKPT>,
+    e = cudaFuncSetAttribute(scan_kernel<T, N, TC, MODE, SP, GATE, CONV, CKPT, ZOH>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem<T, N, TC, MODE, CONV>::kBytes);
     if (e == cudaSuccess) done[dev] = true;
     return e;
 }
 
-template <typename T, int N, typename TC, bool SOFTPLUS, bool GATE, bool CONV, bool CKPT>
+template <typename T, int N, typename TC, bool SOFTPLUS, bool GATE, bool CONV, bool CKPT,
+          bool ZOH>
 cudaError_t launch_flags(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     using Cf = Cfg<T, N, TC>;
     if (p.channels_per_cta != Cf::DT) return cudaErrorInvalidValue;
@@ -577,26 +633,27 @@ cudaError_t launch_flags(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     }
     const int64_t per_chunk = p.tiles * a.batch;
     if (p.nchunks > 1) {
-        if ((e = allow_smem<T, N, TC, 0, SOFTPLUS, false, CONV, false>()) != cudaSuccess) return e;
-        scan_kernel<T, N, TC, 0, SOFTPLUS, false, CONV>
+        if ((e = allow_smem<T, N, TC, 0, SOFTPLUS, false, CONV, false, ZOH>()) != cudaSuccess)
+            return e;
+        scan_kernel<T, N, TC, 0, SOFTPLUS, false, CONV, false, ZOH>
             <<<static_cast<unsigned>(per_chunk * (p.nchunks - 1)), Cf::THREADS,
                Smem<T, N, TC, 0, CONV>::kBytes, s>>>(tx, tdt, tz, tB, tC, tout, a);
     }
-    if ((e = allow_smem<T, N, TC, 1, SOFTPLUS, GATE, CONV, CKPT>()) != cudaSuccess) return e;
-    scan_kernel<T, N, TC, 1, SOFTPLUS, GATE, CONV, CKPT>
+    if ((e = allow_smem<T, N, TC, 1, SOFTPLUS, GATE, CONV, CKPT, ZOH>()) != cudaSuccess) return e;
+    scan_kernel<T, N, TC, 1, SOFTPLUS, GATE, CONV, CKPT, ZOH>
         <<<static_cast<unsigned>(per_chunk * p.nchunks), Cf::THREADS,
            Smem<T, N, TC, 1, CONV>::kBytes, s>>>(tx, tdt, tz, tB, tC, tout, a);
     return cudaGetLastError();
 }
 
-template <typename T, int N, typename TC, bool CONV, bool CKPT = false>
+template <typename T, int N, typename TC, bool CONV, bool CKPT = false, bool ZOH = false>
 cudaError_t launch_cfg(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     const bool sp = a.softplus != 0, gate = a.z != nullptr;
     if (sp)
-        return gate ? launch_flags<T, N, TC, true, true, CONV, CKPT>(a, p, s)
-                    : launch_flags<T, N, TC, true, false, CONV, CKPT>(a, p, s);
-    return gate ? launch_flags<T, N, TC, false, true, CONV, CKPT>(a, p, s)
-                : launch_flags<T, N, TC, false, false, CONV, CKPT>(a, p, s);
+        return gate ? launch_flags<T, N, TC, true, true, CONV, CKPT, ZOH>(a, p, s)
+                    : launch_flags<T, N, TC, true, false, CONV, CKPT, ZOH>(a, p, s);
+    return gate ? launch_flags<T, N, TC, false, true, CONV, CKPT, ZOH>(a, p, s)
+                : launch_flags<T, N, TC, false, false, CONV, CKPT, ZOH>(a, p, s);
 }
 
 // The tile configurations by id (the same table as scan_lanes... in ssm_internal.h).
@@ -609,11 +666,20 @@ template <typename T, int N>
 cudaError_t launch_typed(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     // the fused conv input stage is built for tile configuration 0 only (the
     // library never plans another one for it)
-    if (a.conv_w) return p.tile_cfg == 0 && !a.ckpt ? launch_cfg<T, N, Tile0, true>(a, p, s)
-                                                    : cudaErrorInvalidValue;
+    if (a.conv_w) return p.tile_cfg == 0 && !a.ckpt && !a.zoh
+                             ? launch_cfg<T, N, Tile0, true>(a, p, s)
+                             : cudaErrorInvalidValue;
     // so is the checkpointing forward (training)
-    if (a.ckpt) return p.tile_cfg == 0 ? launch_cfg<T, N, Tile0, false, true>(a, p, s)
-                                       : cudaErrorInvalidValue;
+    if (a.ckpt) return p.tile_cfg == 0 && !a.zoh ? launch_cfg<T, N, Tile0, false, true>(a, p, s)
+                                                 : cudaErrorInvalidValue;
+    // and the exact zero-order hold (dstate 16)
+    if (a.zoh) {
+        if constexpr (N == 16)
+            return p.tile_cfg == 0 ? launch_cfg<T, N, Tile0, false, false, true>(a, p, s)
+                                   : cudaErrorInvalidValue;
+        else
+            return cudaErrorInvalidValue;
+    }
     if constexpr (N == 16) {
         switch (p.tile_cfg) {
             case 0: return launch_cfg<T, N, Tile0, false>(a, p, s);

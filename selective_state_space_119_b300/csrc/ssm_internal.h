@@ -64,6 +64,7 @@ struct ScanArgs {
     int conv_k;           // conv width (1 .. 4) when conv_w is given
     float* ckpt;          // [batch][nckpt][dim][N]: state before every kCkptTokens-th token, or NULL
     int64_t nckpt;        // ceil(L / kCkptTokens)
+    int zoh;              // exact zero-order-hold Bbar instead of dt * B
     float* ws_H;   // [batch][nchunks-1][dim][N]: chunk-local end states (from h = 0)
     float* ws_S;   // [batch][nchunks-1][dim]: sum of dt over each chunk
     unsigned int* status;  // workspace status word (sticky; 0 = ok; no current kernel sets it)
@@ -82,6 +83,7 @@ struct StepArgs {
     int softplus;
     void* out;
     int64_t batch, dim;
+    int zoh;              // exact zero-order-hold Bbar instead of dt * B
 };
 
 // Tokens between two saved states of a checkpointing forward (the backward

@@ -6,6 +6,8 @@
 // Beyond", "Mamba (S6 -- Selective State Space)", this is one t-iteration of
 // the scan: dt = softplus?(delta + bias), h <- exp(dt A[d,:]) h + dt B x,
 // y = C . h + D x, out = y * silu(z); the fp32 state is updated in place.
+// With the exact zero-order hold ("State-space models (Mamba, S4)", "From
+// Continuous to Discrete: The Key Step") the input term is (e^{dt A} - 1)/A B x.
 //
 // The step is bound by HBM traffic on the state (N fp32 read + written per
 // channel). LANES = N / NPL lanes share a channel, each holding NPL = 4 states
@@ -47,7 +49,18 @@ __device__ __forceinline__ void ld_vec(const T* p, float (&v)[NPL]) {
     }
 }
 
-template <typename T, int N>
+// m = dt phi(dt A) = (e^{dt A} - 1) / A of the exact zero-order hold (Taylor
+// series for |dt A| < 0.1, where the difference e^z - 1 would cancel).
+__device__ __forceinline__ float zoh_m(float dt, float A, float dA) {
+    const float zz = dt * A;
+    float p = fmaf(zz, 1.f / 120.f, 1.f / 24.f);
+    p = fmaf(zz, p, 1.f / 6.f);
+    p = fmaf(zz, p, 0.5f);
+    p = fmaf(zz, p, 1.f);
+    return fabsf(zz) < 0.1f ? dt * p : (dA - 1.f) / A;
+}
+
+template <typename T, int N, bool ZOH>
 __global__ void __launch_bounds__(kStepThreads) state_update_kernel(const StepArgs a) {
     constexpr int NPL = N >= 4 ? 4 : N;        // states per lane
     constexpr int LANES = N / NPL;             // lanes per channel (1, 2 or 4)
@@ -109,7 +122,10 @@ __global__ void __launch_bounds__(kStepThreads) state_update_kernel(const StepAr
         float y = 0.f;
 #pragma unroll
         for (int j = 0; j < NPL; ++j) {
-            h[it][j] = fmaf(ex2(dtv * (A2[it][j] * kLog2e)), h[it][j], dtx * Bv[it][j]);
+            const float dA = ex2(dtv * (A2[it][j] * kLog2e));
+            // first order: Bbar x = dt x B; exact zero-order hold: x B m
+            const float bx = ZOH ? xv[it] * Bv[it][j] * zoh_m(dtv, A2[it][j], dA) : dtx * Bv[it][j];
+            h[it][j] = fmaf(dA, h[it][j], bx);
             y = fmaf(Cv[it][j], h[it][j], y);
         }
         if (active[it]) {
@@ -132,8 +148,8 @@ __global__ void __launch_bounds__(kStepThreads) state_update_kernel(const StepAr
     }
 }
 
-template <typename T, int N>
-cudaError_t launch_typed(const StepArgs& a, cudaStream_t s) {
+template <typename T, int N, bool ZOH>
+cudaError_t launch_zoh(const StepArgs& a, cudaStream_t s) {
     constexpr int NPL = N >= 4 ? 4 : N;
     constexpr int CH_PER_CTA = kStepThreads / (N / NPL);
     constexpr int64_t kMaxGridY = 65535;
@@ -152,9 +168,14 @@ cudaError_t launch_typed(const StepArgs& a, cudaStream_t s) {
         p.C = static_cast<const T*>(a.C) + b0 * N;
         const dim3 grid(static_cast<unsigned>((a.dim + per_cta - 1) / per_cta),
                         static_cast<unsigned>(p.batch));
-        state_update_kernel<T, N><<<grid, kStepThreads, 0, s>>>(p);
+        state_update_kernel<T, N, ZOH><<<grid, kStepThreads, 0, s>>>(p);
     }
     return cudaGetLastError();
+}
+
+template <typename T, int N>
+cudaError_t launch_typed(const StepArgs& a, cudaStream_t s) {
+    return a.zoh ? launch_zoh<T, N, true>(a, s) : launch_zoh<T, N, false>(a, s);
 }
 
 template <typename T>

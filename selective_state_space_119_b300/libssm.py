@@ -38,6 +38,7 @@ SSM_ERR_WORKSPACE = -5
 SSM_ERR_CUDA = -6
 SSM_ERR_TIMEOUT = -7
 SSM_ERR_ALIAS = -8
+SSM_FLAG_ZOH = 1      # exact zero-order-hold Bbar (include/ssm.h)
 
 # Every symbol include/ssm.h declares.
 EXPORTED = ("ssm_selective_scan_fwd", "ssm_state_update", "ssm_scan_workspace_bytes",
@@ -56,7 +57,7 @@ class ssm_dims(ctypes.Structure):
                 ("dstate", ctypes.c_int64), ("io_dtype", ctypes.c_int32),
                 ("chunk_len_hint", ctypes.c_int32), ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_size_t), ("tile_config_hint", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("flags", ctypes.c_int32)]
 
 
 class ssm_plan(ctypes.Structure):
@@ -126,10 +127,10 @@ def _check(rc: int, where: str) -> None:
 
 
 def make_dims(batch, seqlen, dim, dstate, io, workspace=None, workspace_bytes=0,
-              chunk_len_hint=0, tile_config_hint=0) -> ssm_dims:
+              chunk_len_hint=0, tile_config_hint=0, flags=0) -> ssm_dims:
     io_code = io if isinstance(io, int) else (SSM_BF16 if str(io) in ("bf16", "torch.bfloat16") else SSM_F32)
     return ssm_dims(int(batch), int(seqlen), int(dim), int(dstate), io_code, int(chunk_len_hint),
-                    workspace, int(workspace_bytes), int(tile_config_hint), 0)
+                    workspace, int(workspace_bytes), int(tile_config_hint), int(flags))
 
 
 def ssm_scan_workspace_bytes(batch, seqlen, dim, dstate, io, chunk_len_hint=0,
@@ -199,7 +200,7 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
                            delta_softplus=False, out=None, final_state=None,
                            return_final_state=True, workspace=None, chunk_len_hint=0,
                            tile_config_hint=0, stream=None, h0=None, conv_w=None,
-                           conv_b=None) -> Tuple[object, Optional[object]]:
+                           conv_b=None, zoh=False) -> Tuple[object, Optional[object]]:
     """Selective scan over x [batch, L, dim] (see include/ssm.h).
 
     Returns (out, final_state); final_state is None when not requested.
@@ -210,7 +211,8 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
     (ssm_selective_scan_fwd_from_state); otherwise the scan starts from zero.
     ``conv_w`` ([dim, K] fp32, K <= 4) and ``conv_b`` ([dim] fp32 or None)
     put the causal conv1d + SiLU input stage in front of the scan
-    (ssm_selective_scan_fwd_conv): x is then the conv's input.
+    (ssm_selective_scan_fwd_conv): x is then the conv's input. ``zoh=True``
+    takes the exact zero-order-hold Bbar (SSM_FLAG_ZOH).
     """
     torch = _torch()
     batch, L, dim = x.shape
@@ -227,7 +229,7 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
     ws_ptr = _ptr(workspace, "workspace", torch.uint8, device=dev)
     ws_bytes = workspace.numel() if workspace is not None else 0
     dims = make_dims(batch, L, dim, N, _io_code(x), ws_ptr, ws_bytes, chunk_len_hint,
-                     tile_config_hint)
+                     tile_config_hint, SSM_FLAG_ZOH if zoh else 0)
     args = (
         _ptr(x, "x", io, (batch, L, dim), dev),
         _ptr(delta, "delta", io, (batch, L, dim), dev),
@@ -326,16 +328,17 @@ def ssm_selective_scan_fwd_static(x, delta, A, B, C, D=None, z=None, delta_bias=
 
 
 def ssm_state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
-                     delta_softplus=False, out=None, stream=None):
+                     delta_softplus=False, out=None, stream=None, zoh=False):
     """One recurrent step; ``state`` [batch, dim, N] fp32 is updated in place.
-    x, delta, z: [batch, dim]; B, C: [batch, N]. Returns out [batch, dim]."""
+    x, delta, z: [batch, dim]; B, C: [batch, N]. Returns out [batch, dim].
+    ``zoh=True`` takes the exact zero-order-hold Bbar."""
     torch = _torch()
     batch, dim, N = state.shape
     io = x.dtype
     dev = x.device
     if out is None:
         out = torch.empty_like(x)
-    dims = make_dims(batch, 1, dim, N, _io_code(x))
+    dims = make_dims(batch, 1, dim, N, _io_code(x), flags=SSM_FLAG_ZOH if zoh else 0)
     args = (
         _ptr(state, "state", torch.float32, (batch, dim, N), dev),
         _ptr(x, "x", io, (batch, dim), dev),

@@ -234,3 +234,35 @@ def test_training_entry_points_reject_bad_arguments_before_launch():
     assert ws1 >= 256 + 2 * 4 * 1000 * 32 * 4 + 2 * 512 * 16 * 4
     assert ws8 > ws1
     assert L.ssm_scan_bwd_workspace_bytes(2, 1000, 512, 8, "bf16") == 0
+
+
+def test_flags_are_validated():
+    assert ctypes.sizeof(L.ssm_dims) == 4 * 8 + 2 * 4 + 8 + 8 + 2 * 4   # flags took the spare slot
+    d = L.make_dims(1, 20, 16, 16, "bf16", workspace=FAKE + (1 << 34), workspace_bytes=1 << 24,
+                    flags=2)                                            # unknown bit
+    scan = L.lib.ssm_selective_scan_fwd
+    args = (FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288, FAKE + 16384, None, None, None, 0,
+            FAKE + (1 << 30), None)
+    assert scan(*args, ctypes.byref(d), None) == L.SSM_ERR_DIMS
+    # the exact zero-order hold: dstate 16, tile configuration 0, no checkpoints / conv / backward
+    z8 = L.make_dims(1, 20, 16, 8, "bf16", workspace=FAKE + (1 << 34), workspace_bytes=1 << 24,
+                     flags=L.SSM_FLAG_ZOH)
+    assert scan(*args, ctypes.byref(z8), None) == L.SSM_ERR_DIMS
+    zt = L.make_dims(1, 20, 16, 16, "bf16", workspace=FAKE + (1 << 34), workspace_bytes=1 << 24,
+                     flags=L.SSM_FLAG_ZOH, tile_config_hint=3)
+    assert scan(*args, ctypes.byref(zt), None) == L.SSM_ERR_DIMS
+    z16 = L.make_dims(1, 20, 16, 16, "bf16", workspace=FAKE + (1 << 34), workspace_bytes=1 << 24,
+                      flags=L.SSM_FLAG_ZOH)
+    # accepted up to the alias check (out over x), so no launch happens here
+    bad = args[:9] + (FAKE, None)
+    assert scan(*bad, ctypes.byref(z16), None) == L.SSM_ERR_ALIAS
+    assert L.lib.ssm_selective_scan_fwd_ckpt(*args[:9], None, FAKE + (1 << 30), None,
+                                             FAKE + (1 << 32), ctypes.byref(z16),
+                                             None) == L.SSM_ERR_DIMS
+    assert L.lib.ssm_selective_scan_fwd_conv(FAKE, FAKE + (1 << 32), None, 4, *args[1:],
+                                             ctypes.byref(z16), None) == L.SSM_ERR_DIMS
+    G = FAKE + (1 << 36)
+    assert L.lib.ssm_selective_scan_bwd(
+        FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288, FAKE + 16384, None, None, None, 0,
+        FAKE + (1 << 32), FAKE + 20480, None, G, G + 4096, G + 65536, G + 8192, G + 12288,
+        None, None, None, None, ctypes.byref(z16), None) == L.SSM_ERR_DIMS
