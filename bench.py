@@ -23,6 +23,8 @@ bias), gate), i.e. every step of the scan path. Rank 0 prints one JSON line.
   the scan, and as two calls (conv, then the scan on its output).
 * train: training through the scan on the same workload, the checkpointing
   forward and the backward (every gradient), per call.
+* bc_per_channel: the scan with per-channel B, C on the same shapes (bound by
+  HBM: its roofline is the copy bandwidth).
 * cpu_baseline: the float64 CPU oracle timed on this host (rank 0, N = 1).
 
 N > 1 (torchrun): every rank runs its own replica of the workload on its own
@@ -345,6 +347,8 @@ def bench_scan(args, rank, world, local):
         res["input_stage"] = bench_input_stage(args, spec, dev, stream)
     if not args.no_train and spec.N == 16:
         res["train"] = bench_train(args, spec, dev, stream)
+    if not args.no_bcd and spec.N == 16:
+        res["bc_per_channel"] = bench_bcd(args, spec, dev, stream)
     return res, spec
 
 
@@ -641,6 +645,64 @@ def bench_train(args, spec, dev, stream):
                      "unit": "elems/s"}}
 
 
+def bench_bcd(args, spec, dev, stream):
+    """The scan with per-channel B, C ([batch, L, dim, N], SSM_FLAG_BC_PER_CHANNEL)
+    on the scan workload's shapes: bound by HBM (each channel reads its own
+    2 N values per token), so its roofline is the measured copy bandwidth."""
+    import torch
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+
+    inp = I.make_scan_inputs(spec)
+    B4, C4 = I.make_bc_per_channel(spec)
+    io = libssm.SSM_BF16 if spec.io == "bf16" else libssm.SSM_F32
+    alg = I.algorithmic_bytes_scan_bcd(spec)
+    nsets = 2 if alg > 2 * L2_BYTES else max(2, min(8, math.ceil(2 * L2_BYTES / alg) + 1))
+    base = {k: _upload(v, dev) for k, v in inp.items()}
+    base["B"], base["C"] = _upload(B4, dev), _upload(C4, dev)
+    sets = []
+    for i in range(nsets):
+        st = {k: (None if base[k] is None else (base[k] if (k in ("A", "D", "delta_bias") or i == 0)
+                                                 else base[k].clone())) for k in base}
+        st["out"] = torch.empty_like(base["x"])
+        sets.append(st)
+    B_, L_, D_, N_ = spec.batch, spec.L, spec.dim, spec.N
+    ws = libssm.alloc_workspace(B_, L_, D_, N_, io, dev)
+    dims = libssm.make_dims(B_, L_, D_, N_, io, None if ws is None else ws.data_ptr(),
+                            0 if ws is None else ws.numel(), flags=libssm.SSM_FLAG_BC_PER_CHANNEL)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    sp = 1 if spec.delta_softplus else 0
+
+    def call(i):
+        st = sets[i % nsets]
+        rc = libssm.lib.ssm_selective_scan_fwd(
+            _vp(st["x"]), _vp(st["delta"]), _vp(st["A"]), _vp(st["B"]), _vp(st["C"]),
+            _vp(st["D"]), _vp(st["z"]), _vp(st["delta_bias"]), sp, _vp(st["out"]), None,
+            ctypes.byref(dims), sptr)
+        if rc != 0:
+            raise libssm.SSMError(rc, "ssm_selective_scan_fwd (per-channel B, C)")
+
+    for i in range(max(args.warmup, 3)):
+        call(i)
+    torch.cuda.synchronize()
+    n = max(16, min(args.steps, 400))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        call(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3 / n
+    peak, kind = measured_peaks()
+    gbs = alg / sec / 1e9
+    plan = libssm.ssm_scan_plan(B_, L_, D_, N_, io)
+    return {"us_per_call": sec * 1e6, "value": spec.elements / sec, "unit": "elems/s",
+            "timed_calls": n, "input_sets": nsets, "kernels_per_call": plan["kernels"],
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "traffic": None, "peak_kind": kind,
+                         "algorithmic_bytes_per_call": alg}}
+
+
 # ---------------------------------------------------------------------------
 # the CPU oracle arm
 # ---------------------------------------------------------------------------
@@ -746,6 +808,8 @@ def main(argv=None):
                     help="skip the conv1d + SiLU input-stage timings")
     ap.add_argument("--no-train", action="store_true",
                     help="skip the training (checkpointing forward + backward) timings")
+    ap.add_argument("--no-bcd", action="store_true",
+                    help="skip the per-channel B, C scan timing")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,
                     help="minimum wall time of the CPU oracle baseline")
     args = ap.parse_args(argv)
@@ -785,6 +849,8 @@ def main(argv=None):
             line["input_stage"] = res["input_stage"]
         if "train" in res:
             line["train"] = res["train"]
+        if "bc_per_channel" in res:
+            line["bc_per_channel"] = res["bc_per_channel"]
         if world == 1:
             from selective_state_space_119_b300 import inputs as I
             inp = I.make_scan_inputs(spec)

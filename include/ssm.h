@@ -108,9 +108,21 @@ typedef struct {
  * same exp(dt A) either way. Taken by ssm_selective_scan_fwd,
  * ssm_selective_scan_fwd_from_state, ssm_selective_scan_fwd_static (dstate 16,
  * tile_config_hint 0 or 1) and ssm_state_update (any dstate); the other entry
- * points return SSM_ERR_DIMS when it is set. Any other bit is SSM_ERR_DIMS.
+ * points return SSM_ERR_DIMS when it is set. An unknown bit is SSM_ERR_DIMS.
  */
 #define SSM_FLAG_ZOH 1
+
+/*
+ * SSM_FLAG_BC_PER_CHANNEL -- B and C hold one row per channel: [batch, seqlen,
+ * dim, dstate] instead of [batch, seqlen, dstate] shared by all channels (the
+ * shape "Mamba: State Space Models Challenge Transformers", "Selective Scan
+ * Algorithm" gives them in its docstring). Each channel then reads its own 2 *
+ * dstate values per token and the scan is bound by HBM. Taken by
+ * ssm_selective_scan_fwd, ssm_selective_scan_fwd_from_state and
+ * ssm_selective_scan_fwd_static with dstate 16, tile_config_hint 0 or 1, and
+ * not together with SSM_FLAG_ZOH; other entry points return SSM_ERR_DIMS.
+ */
+#define SSM_FLAG_BC_PER_CHANNEL 2
 
 /*
  * ssm_selective_scan_fwd -- the selective scan over a whole sequence.

@@ -236,6 +236,34 @@ def _bwd_method(self, x, delta, A, B, C, dout, D=None, z=None, delta_bias=None,
 Oracle.selective_scan_bwd = _bwd_method
 
 
+def _bcd_method(self, x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
+                h0=None, nthreads=None):
+    """The scan with per-channel B, C [batch, L, dim, N]: every channel d is the
+    one-channel scan of the oracle with its own rows B[:, :, d], C[:, :, d]
+    (channels are independent). Returns (out, final_state) like selective_scan."""
+    x = _f64(x)
+    batch, L, dim = x.shape
+    B, C = _f64(B), _f64(C)
+    N = B.shape[3]
+    out = np.zeros((batch, L, dim))
+    fs = np.zeros((batch, dim, N))
+    A = _f64(A, (dim, N))
+    for d in range(dim):
+        sl = (slice(None), slice(None), slice(d, d + 1))
+        o, f = self.selective_scan(
+            x[sl], _f64(delta)[sl], A[d:d + 1], B[:, :, d], C[:, :, d],
+            D=None if D is None else _f64(D)[d:d + 1], z=None if z is None else _f64(z)[sl],
+            delta_bias=None if delta_bias is None else _f64(delta_bias)[d:d + 1],
+            delta_softplus=delta_softplus, h0=None if h0 is None else _f64(h0)[:, d:d + 1],
+            nthreads=1)
+        out[:, :, d] = o[:, :, 0]
+        fs[:, d] = f[:, 0]
+    return out, fs
+
+
+Oracle.selective_scan_bcd = _bcd_method
+
+
 def default() -> Oracle:
     """The oracle built from ssm_oracle.c (compiled on first use)."""
     global _default
@@ -275,3 +303,7 @@ def causal_conv1d_silu(*a, **k):
 
 def selective_scan_bwd(*a, **k):
     return default().selective_scan_bwd(*a, **k)
+
+
+def selective_scan_bcd(*a, **k):
+    return default().selective_scan_bcd(*a, **k)

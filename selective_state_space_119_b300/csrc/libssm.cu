@@ -69,7 +69,7 @@ int check_dims(const ssm_dims* d, bool scan) {
     if (scan && d->chunk_len_hint < 0) return SSM_ERR_DIMS;
     if (scan && (d->tile_config_hint < 0 || d->tile_config_hint > ssm::kScanTileConfigs))
         return SSM_ERR_DIMS;
-    if (d->flags & ~SSM_FLAG_ZOH) return SSM_ERR_DIMS;
+    if (d->flags & ~(SSM_FLAG_ZOH | SSM_FLAG_BC_PER_CHANNEL)) return SSM_ERR_DIMS;
     const int64_t L = scan ? d->seqlen : 1;
     if (d->batch > 0 && d->dim > 0 && L > 0 &&
         (d->batch > kMaxElems / d->dim || d->batch * d->dim > kMaxElems / L))
@@ -97,6 +97,13 @@ int make_plan(const ssm_dims* d, ssm::ScanPlan* p) {
     int64_t chunk;
     if (d->chunk_len_hint > 0) {
         chunk = d->chunk_len_hint;
+    } else if (d->flags & SSM_FLAG_BC_PER_CHANNEL) {
+        // per-channel B, C are bound by HBM: split the sequence until about 4
+        // output CTAs per SM keep enough loads in flight (measured best for
+        // b4 L2048 d1536: 13 chunks), chunks of at least 128 tokens
+        const int64_t k = std::max<int64_t>(
+            1, std::min<int64_t>((4 * kSms + per_chunk - 1) / per_chunk, L / 128));
+        chunk = ((L + k - 1) / k + TS - 1) / TS * TS;
     } else {
         // modelled time of every chunk count (see the planning note above)
         chunk = (L + TS - 1) / TS * TS;
@@ -274,6 +281,11 @@ int scan_impl(const void* x, const void* delta, const float* A, const void* B, c
     if ((dims->flags & SSM_FLAG_ZOH) &&
         (dims->dstate != 16 || dims->tile_config_hint > 1 || cv.w || ckpt))
         return SSM_ERR_DIMS;
+    // so are per-channel B and C (and not with the exact zero-order hold)
+    const bool bc_per_channel = (dims->flags & SSM_FLAG_BC_PER_CHANNEL) != 0;
+    if (bc_per_channel && (dims->dstate != 16 || dims->tile_config_hint > 1 || cv.w || ckpt ||
+                           (dims->flags & SSM_FLAG_ZOH)))
+        return SSM_ERR_DIMS;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // Empty problems: nothing to read (empty tensors may carry NULL pointers).
     if (dims->batch == 0 || dims->dim == 0) return SSM_OK;
@@ -303,7 +315,7 @@ int scan_impl(const void* x, const void* delta, const float* A, const void* B, c
     const int64_t batch = dims->batch, L = dims->seqlen, dim = dims->dim, N = dims->dstate;
     const size_t es = io_size(dims->io_dtype);
     const size_t elems = size_t(batch) * size_t(L) * size_t(dim);
-    const size_t rows = size_t(batch) * size_t(L) * size_t(N);
+    const size_t rows = size_t(batch) * size_t(L) * size_t(N) * (bc_per_channel ? size_t(dim) : 1);
     {
         const Range in[] = {{x, elems * es},      {delta, elems * es},
                             {z, elems * es},      {B, rows * es},
@@ -337,6 +349,7 @@ int scan_impl(const void* x, const void* delta, const float* A, const void* B, c
         a.ws_H = reinterpret_cast<float*>(ws + p.ws_off_H);
         a.ws_S = reinterpret_cast<float*>(ws + p.ws_off_S);
     }
+    if (bc_per_channel) return set_cuda(ssm::launch_scan_bcd(a, p, dims->io_dtype, s));
     return set_cuda(ssm::launch_scan(a, p, dims->io_dtype, static_cast<int>(N), s));
 }
 
@@ -526,6 +539,7 @@ int ssm_state_update(float* state, const void* x, const void* delta, const float
                      const ssm_dims* dims, ssm_stream_t stream) {
     int rc = check_dims(dims, false);
     if (rc != SSM_OK) return rc;
+    if (dims->flags & SSM_FLAG_BC_PER_CHANNEL) return SSM_ERR_DIMS;
     if (dims->batch == 0 || dims->dim == 0) return SSM_OK;   // nothing to update
     if (!state || !x || !delta || !A || !B || !C || !out) return SSM_ERR_NULL;
     {

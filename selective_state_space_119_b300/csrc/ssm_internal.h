@@ -143,6 +143,8 @@ struct BwdArgs {
 cudaError_t launch_scan(const ScanArgs& a, const ScanPlan& p, int io, int N, cudaStream_t s);
 // Enqueue one decode step.
 cudaError_t launch_state_update(const StepArgs& a, int io, int N, cudaStream_t s);
+// Enqueue the scan with per-channel B and C ([batch][L][dim][N], dstate 16).
+cudaError_t launch_scan_bcd(const ScanArgs& a, const ScanPlan& p, int io, cudaStream_t s);
 // Enqueue the gradient passes (reverse carries, gradients, reduction).
 cudaError_t launch_scan_bwd(const BwdArgs& a, int io, cudaStream_t s);
 // Enqueue the standalone causal depthwise conv1d + SiLU.

@@ -275,6 +275,25 @@ def algorithmic_bytes_conv(batch: int, L: int, dim: int, K: int, io: str,
     return 2 * batch * L * dim * es + dim * K * 4 + (dim * 4 if bias else 0)
 
 
+def make_bc_per_channel(spec: ScanSpec, seed: Optional[int] = None):
+    """Per-channel B, C [batch, L, dim, N] ~ N(0, 1) in the stored I/O dtype
+    (the rows a scan with per-channel B, C reads instead of the shared ones)."""
+    rng = np.random.Generator(np.random.PCG64((spec.seed if seed is None else seed) + 500))
+    shape = (spec.batch, spec.L, spec.dim, spec.N)
+    return _normal_chunked(rng, shape, 1.0, spec.io), _normal_chunked(rng, shape, 1.0, spec.io)
+
+
+def algorithmic_bytes_scan_bcd(spec: ScanSpec) -> int:
+    """Bytes of the scan with per-channel B, C: x, delta, z, y per element and
+    B, C rows per element (2 N values), A, D, bias once, the final state."""
+    es = 2 if spec.io == "bf16" else 4
+    per_elem = (4 if spec.gate else 3) * es + 2 * spec.N * es
+    extra = spec.dim * spec.N * 4 + 2 * spec.dim * 4
+    if spec.final_state:
+        extra += spec.batch * spec.dim * spec.N * 4
+    return spec.elements * per_elem + extra
+
+
 def algorithmic_bytes_scan(spec: ScanSpec) -> int:
     """Bytes the scan must move at least once: x, delta, z read and y written
     per element; B and C per (b, t); A, D, delta_bias once; final_state written."""

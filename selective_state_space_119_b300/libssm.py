@@ -39,6 +39,7 @@ SSM_ERR_CUDA = -6
 SSM_ERR_TIMEOUT = -7
 SSM_ERR_ALIAS = -8
 SSM_FLAG_ZOH = 1      # exact zero-order-hold Bbar (include/ssm.h)
+SSM_FLAG_BC_PER_CHANNEL = 2   # B, C of shape [batch, L, dim, N] (include/ssm.h)
 
 # Every symbol include/ssm.h declares.
 EXPORTED = ("ssm_selective_scan_fwd", "ssm_state_update", "ssm_scan_workspace_bytes",
@@ -212,7 +213,8 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
     ``conv_w`` ([dim, K] fp32, K <= 4) and ``conv_b`` ([dim] fp32 or None)
     put the causal conv1d + SiLU input stage in front of the scan
     (ssm_selective_scan_fwd_conv): x is then the conv's input. ``zoh=True``
-    takes the exact zero-order-hold Bbar (SSM_FLAG_ZOH).
+    takes the exact zero-order-hold Bbar (SSM_FLAG_ZOH). B and C of shape
+    [batch, L, dim, N] select per-channel rows (SSM_FLAG_BC_PER_CHANNEL).
     """
     torch = _torch()
     batch, L, dim = x.shape
@@ -228,14 +230,17 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
                                     tile_config_hint)
     ws_ptr = _ptr(workspace, "workspace", torch.uint8, device=dev)
     ws_bytes = workspace.numel() if workspace is not None else 0
+    bcd = B.dim() == 4          # per-channel B, C: [batch, L, dim, N]
+    bc_shape = (batch, L, dim, N) if bcd else (batch, L, N)
     dims = make_dims(batch, L, dim, N, _io_code(x), ws_ptr, ws_bytes, chunk_len_hint,
-                     tile_config_hint, SSM_FLAG_ZOH if zoh else 0)
+                     tile_config_hint, (SSM_FLAG_ZOH if zoh else 0) |
+                     (SSM_FLAG_BC_PER_CHANNEL if bcd else 0))
     args = (
         _ptr(x, "x", io, (batch, L, dim), dev),
         _ptr(delta, "delta", io, (batch, L, dim), dev),
         _ptr(A, "A", torch.float32, (dim, N), dev),
-        _ptr(B, "B", io, (batch, L, N), dev),
-        _ptr(C, "C", io, (batch, L, N), dev),
+        _ptr(B, "B", io, bc_shape, dev),
+        _ptr(C, "C", io, bc_shape, dev),
         _ptr(D, "D", torch.float32, (dim,), dev),
         _ptr(z, "z", io, (batch, L, dim), dev),
         _ptr(delta_bias, "delta_bias", torch.float32, (dim,), dev),

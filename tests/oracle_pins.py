@@ -616,7 +616,38 @@ def pin_zoh_decode(orc, seed=44):
     _close(sd, fz, 1e-14, 1e-15, "ZOH decode state")
 
 
+# --------------------------------------------------------------------------
+# per-channel B, C ("Mamba: State Space Models Challenge Transformers",
+# "Selective Scan Algorithm": B, C of shape [B, L, D, N] in its docstring)
+# --------------------------------------------------------------------------
+def pin_bc_per_channel(orc, seed=45):
+    """Per-channel B, C: each channel equals the explicit unrolled sum with its
+    own rows; rows equal across channels give the shared-B, C scan exactly."""
+    r = _rng(seed)
+    c = _random_case(r, batch=2, L=10, dim=3, N=4)
+    B4 = r.standard_normal((2, 10, 3, 4))
+    C4 = r.standard_normal((2, 10, 3, 4))
+    bias = r.standard_normal(3) * 0.2
+    h0 = r.standard_normal((2, 3, 4))
+    out, fs = orc.selective_scan_bcd(c["x"], c["delta"], c["A"], B4, C4, D=c["D"], z=c["z"],
+                                     delta_bias=bias, delta_softplus=True, h0=h0)
+    for d in range(3):
+        sl = slice(d, d + 1)
+        y, hL = _unrolled(c["x"][:, :, sl], c["delta"][:, :, sl], c["A"][sl], B4[:, :, d],
+                          C4[:, :, d], c["D"][sl], c["z"][:, :, sl], bias[sl], True, h0[:, sl])
+        _close(out[:, :, sl], y, 1e-12, 1e-13, "per-channel y, channel %d" % d)
+        _close(fs[:, sl], hL, 1e-12, 1e-13, "per-channel final state, channel %d" % d)
+    Bs = np.repeat(c["B"][:, :, None, :], 3, 2)   # the shared rows, once per channel
+    Cs = np.repeat(c["C"][:, :, None, :], 3, 2)
+    o1, f1 = orc.selective_scan(c["x"][:, :10], c["delta"][:, :10], c["A"], c["B"][:, :10],
+                                c["C"][:, :10], D=c["D"], h0=h0)
+    o2, f2 = orc.selective_scan_bcd(c["x"][:, :10], c["delta"][:, :10], c["A"],
+                                    Bs[:, :10], Cs[:, :10], D=c["D"], h0=h0)
+    assert np.array_equal(o1, o2) and np.array_equal(f1, f2), "shared rows = shared B, C"
+
+
 ALL_PINS = [
+    pin_bc_per_channel,
     pin_phi,
     pin_zoh_closed_form,
     pin_zoh_ode,

@@ -239,7 +239,7 @@ def test_training_entry_points_reject_bad_arguments_before_launch():
 def test_flags_are_validated():
     assert ctypes.sizeof(L.ssm_dims) == 4 * 8 + 2 * 4 + 8 + 8 + 2 * 4   # flags took the spare slot
     d = L.make_dims(1, 20, 16, 16, "bf16", workspace=FAKE + (1 << 34), workspace_bytes=1 << 24,
-                    flags=2)                                            # unknown bit
+                    flags=4)                                            # unknown bit
     scan = L.lib.ssm_selective_scan_fwd
     args = (FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288, FAKE + 16384, None, None, None, 0,
             FAKE + (1 << 30), None)
@@ -266,3 +266,35 @@ def test_flags_are_validated():
         FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288, FAKE + 16384, None, None, None, 0,
         FAKE + (1 << 32), FAKE + 20480, None, G, G + 4096, G + 65536, G + 8192, G + 12288,
         None, None, None, None, ctypes.byref(z16), None) == L.SSM_ERR_DIMS
+
+
+def test_bc_per_channel_flag_is_validated():
+    F = L.SSM_FLAG_BC_PER_CHANNEL
+    scan = L.lib.ssm_selective_scan_fwd
+
+    def dims(**kw):
+        base = dict(workspace=FAKE + (1 << 34), workspace_bytes=1 << 24, flags=F)
+        base.update(kw)
+        return L.make_dims(1, 20, 16, 16, "bf16", **base)
+
+    # out over B, where B now spans batch * L * dim * N elements (20 * 16 * 16 * 2 bytes)
+    args = (FAKE, FAKE + (1 << 20), FAKE + (2 << 20), FAKE + (3 << 20), FAKE + (4 << 20), None,
+            None, None, 0)
+    assert scan(*args, FAKE + (3 << 20) + 8192, None, ctypes.byref(dims()), None) == L.SSM_ERR_ALIAS
+    assert scan(*args, FAKE + (3 << 20) + 10240 - 64, None, ctypes.byref(dims()),
+                None) == L.SSM_ERR_ALIAS
+    # with shared B (no flag) the same out lies past B's 640 bytes: accepted up to the next check
+    d0 = dims(flags=0)
+    assert scan(*args, FAKE + (3 << 20) + 8192, FAKE, ctypes.byref(d0), None) == L.SSM_ERR_ALIAS
+    # dstate 16 only, tile configuration 0, not with the exact zero-order hold
+    assert scan(*args, FAKE + (5 << 20), None,
+                ctypes.byref(L.make_dims(1, 20, 16, 8, "bf16", flags=F)), None) == L.SSM_ERR_DIMS
+    assert scan(*args, FAKE + (5 << 20), None, ctypes.byref(dims(tile_config_hint=2)),
+                None) == L.SSM_ERR_DIMS
+    assert scan(*args, FAKE + (5 << 20), None, ctypes.byref(dims(flags=F | L.SSM_FLAG_ZOH)),
+                None) == L.SSM_ERR_DIMS
+    # the decode step has no per-channel rows
+    st = L.make_dims(2, 1, 16, 16, "bf16", flags=F)
+    assert L.lib.ssm_state_update(FAKE + (6 << 20), FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288,
+                                  FAKE + 16384, None, None, None, 0, FAKE + 20480,
+                                  ctypes.byref(st), None) == L.SSM_ERR_DIMS
