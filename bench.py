@@ -667,9 +667,10 @@ def bench_bcd(args, spec, dev, stream):
         st["out"] = torch.empty_like(base["x"])
         sets.append(st)
     B_, L_, D_, N_ = spec.batch, spec.L, spec.dim, spec.N
-    ws = libssm.alloc_workspace(B_, L_, D_, N_, io, dev)
+    F = libssm.SSM_FLAG_BC_PER_CHANNEL
+    ws = libssm.alloc_workspace(B_, L_, D_, N_, io, dev, flags=F)
     dims = libssm.make_dims(B_, L_, D_, N_, io, None if ws is None else ws.data_ptr(),
-                            0 if ws is None else ws.numel(), flags=libssm.SSM_FLAG_BC_PER_CHANNEL)
+                            0 if ws is None else ws.numel(), flags=F)
     sptr = ctypes.c_void_p(stream.cuda_stream)
     sp = 1 if spec.delta_softplus else 0
 
@@ -695,7 +696,7 @@ def bench_bcd(args, spec, dev, stream):
     sec = e0.elapsed_time(e1) / 1e3 / n
     peak, kind = measured_peaks()
     gbs = alg / sec / 1e9
-    plan = libssm.ssm_scan_plan(B_, L_, D_, N_, io)
+    plan = libssm.ssm_scan_plan(B_, L_, D_, N_, io, flags=F)
     return {"us_per_call": sec * 1e6, "value": spec.elements / sec, "unit": "elems/s",
             "timed_calls": n, "input_sets": nsets, "kernels_per_call": plan["kernels"],
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",

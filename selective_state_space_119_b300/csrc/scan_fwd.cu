@@ -61,6 +61,7 @@
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 #include "ssm_tma.cuh"
+#include "ssm_tmap.h"
 
 namespace ssm {
 namespace {
@@ -550,45 +551,6 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled encode_fn() {
-    static EncodeTiled fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return static_cast<EncodeTiled>(nullptr);
-        return reinterpret_cast<EncodeTiled>(p);
-    }();
-    return fn;
-}
-
-// [batch][L][dim] tensor, box of `box_channels` channels x `box_rows` tokens x
-// 1 batch row (elements before the sequence start, past its end or past the
-// last channel read as zero).
-template <typename T>
-cudaError_t make_tmap(CUtensorMap* tm, const void* base, int64_t batch, int64_t L, int64_t dim,
-                      int box_channels, int box_rows = kScanStageTokens) {
-    EncodeTiled fn = encode_fn();
-    if (!fn) return cudaErrorNotSupported;
-    const cuuint64_t es = sizeof(T);
-    const cuuint64_t gdim[3] = {cuuint64_t(dim), cuuint64_t(L), cuuint64_t(batch)};
-    const cuuint64_t gstride[2] = {cuuint64_t(dim) * es, cuuint64_t(L) * cuuint64_t(dim) * es};
-    const cuuint32_t box[3] = {cuuint32_t(box_channels), cuuint32_t(box_rows), 1};
-    const cuuint32_t estride[3] = {1, 1, 1};
-    const CUresult r = fn(tm, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                          3, const_cast<void*>(base), gdim, gstride, box, estride,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 // Raise the dynamic shared-memory limit of one kernel instantiation, once per
 // device (the statics are per instantiation).
 template <typename T, int N, typename TC, int MODE, bool SP, bool GATE, bool CONV, bool CKPT,
@@ -616,20 +578,20 @@ cudaError_t launch_flags(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     if (p.channels_per_cta != Cf::DT) return cudaErrorInvalidValue;
     CUtensorMap tx, tdt, tz, tB, tC, tout;
     cudaError_t e;
-    if ((e = make_tmap<T>(&tx, a.x, a.batch, a.L, a.dim, Cf::DT,
+    if ((e = make_tmap_cached<T>(&tx, a.x, a.batch, a.L, a.dim, Cf::DT,
                           Smem<T, N, TC, 1, CONV>::XR)) != cudaSuccess)
         return e;
-    if ((e = make_tmap<T>(&tdt, a.delta, a.batch, a.L, a.dim, Cf::DT)) != cudaSuccess) return e;
-    if ((e = make_tmap<T>(&tout, a.out, a.batch, a.L, a.dim, Cf::DT)) != cudaSuccess) return e;
+    if ((e = make_tmap_cached<T>(&tdt, a.delta, a.batch, a.L, a.dim, Cf::DT)) != cudaSuccess) return e;
+    if ((e = make_tmap_cached<T>(&tout, a.out, a.batch, a.L, a.dim, Cf::DT)) != cudaSuccess) return e;
     tz = tx;
-    if (GATE && (e = make_tmap<T>(&tz, a.z, a.batch, a.L, a.dim, Cf::DT)) != cudaSuccess) return e;
+    if (GATE && (e = make_tmap_cached<T>(&tz, a.z, a.batch, a.L, a.dim, Cf::DT)) != cudaSuccess) return e;
     // B, C [batch][L][N]: box of N states x TS tokens (only when a row is a
     // whole number of 16-byte units; otherwise the kernel reads them directly)
     tB = tx;
     tC = tx;
     if constexpr (Smem<T, N, TC, 1>::BC_TMA) {
-        if ((e = make_tmap<T>(&tB, a.B, a.batch, a.L, N, N)) != cudaSuccess) return e;
-        if ((e = make_tmap<T>(&tC, a.C, a.batch, a.L, N, N)) != cudaSuccess) return e;
+        if ((e = make_tmap_cached<T>(&tB, a.B, a.batch, a.L, N, N)) != cudaSuccess) return e;
+        if ((e = make_tmap_cached<T>(&tC, a.C, a.batch, a.L, N, N)) != cudaSuccess) return e;
     }
     const int64_t per_chunk = p.tiles * a.batch;
     if (p.nchunks > 1) {

@@ -135,15 +135,16 @@ def make_dims(batch, seqlen, dim, dstate, io, workspace=None, workspace_bytes=0,
 
 
 def ssm_scan_workspace_bytes(batch, seqlen, dim, dstate, io, chunk_len_hint=0,
-                             tile_config_hint=0) -> int:
+                             tile_config_hint=0, flags=0) -> int:
     d = make_dims(batch, seqlen, dim, dstate, io, chunk_len_hint=chunk_len_hint,
-                  tile_config_hint=tile_config_hint)
+                  tile_config_hint=tile_config_hint, flags=flags)
     return int(lib.ssm_scan_workspace_bytes(ctypes.byref(d)))
 
 
-def ssm_scan_plan(batch, seqlen, dim, dstate, io, chunk_len_hint=0, tile_config_hint=0) -> dict:
+def ssm_scan_plan(batch, seqlen, dim, dstate, io, chunk_len_hint=0, tile_config_hint=0,
+                  flags=0) -> dict:
     d = make_dims(batch, seqlen, dim, dstate, io, chunk_len_hint=chunk_len_hint,
-                  tile_config_hint=tile_config_hint)
+                  tile_config_hint=tile_config_hint, flags=flags)
     p = ssm_plan()
     _check(lib.ssm_scan_plan(ctypes.byref(d), ctypes.byref(p)), "ssm_scan_plan")
     return {k: getattr(p, k) for k, _ in ssm_plan._fields_}
@@ -188,10 +189,12 @@ def _stream(device, stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def alloc_workspace(batch, seqlen, dim, dstate, io, device, chunk_len_hint=0, tile_config_hint=0):
+def alloc_workspace(batch, seqlen, dim, dstate, io, device, chunk_len_hint=0, tile_config_hint=0,
+                    flags=0):
     """Zero-filled workspace tensor (uint8) of the size the scan needs, or None."""
     torch = _torch()
-    n = ssm_scan_workspace_bytes(batch, seqlen, dim, dstate, io, chunk_len_hint, tile_config_hint)
+    n = ssm_scan_workspace_bytes(batch, seqlen, dim, dstate, io, chunk_len_hint, tile_config_hint,
+                                 flags)
     if n == 0:
         return None
     return torch.zeros(n, dtype=torch.uint8, device=device)
@@ -225,16 +228,16 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
         out = torch.empty_like(x)
     if final_state is None and return_final_state:
         final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
-    if workspace is None:
-        workspace = alloc_workspace(batch, L, dim, N, _io_code(x), dev, chunk_len_hint,
-                                    tile_config_hint)
-    ws_ptr = _ptr(workspace, "workspace", torch.uint8, device=dev)
-    ws_bytes = workspace.numel() if workspace is not None else 0
     bcd = B.dim() == 4          # per-channel B, C: [batch, L, dim, N]
     bc_shape = (batch, L, dim, N) if bcd else (batch, L, N)
+    flags = (SSM_FLAG_ZOH if zoh else 0) | (SSM_FLAG_BC_PER_CHANNEL if bcd else 0)
+    if workspace is None:
+        workspace = alloc_workspace(batch, L, dim, N, _io_code(x), dev, chunk_len_hint,
+                                    tile_config_hint, flags)
+    ws_ptr = _ptr(workspace, "workspace", torch.uint8, device=dev)
+    ws_bytes = workspace.numel() if workspace is not None else 0
     dims = make_dims(batch, L, dim, N, _io_code(x), ws_ptr, ws_bytes, chunk_len_hint,
-                     tile_config_hint, (SSM_FLAG_ZOH if zoh else 0) |
-                     (SSM_FLAG_BC_PER_CHANNEL if bcd else 0))
+                     tile_config_hint, flags)
     args = (
         _ptr(x, "x", io, (batch, L, dim), dev),
         _ptr(delta, "delta", io, (batch, L, dim), dev),
