@@ -98,11 +98,11 @@ int make_plan(const ssm_dims* d, ssm::ScanPlan* p) {
     if (d->chunk_len_hint > 0) {
         chunk = d->chunk_len_hint;
     } else if (d->flags & SSM_FLAG_BC_PER_CHANNEL) {
-        // per-channel B, C are bound by HBM: split the sequence until about 4
+        // per-channel B, C are bound by HBM: split the sequence until about 2.5
         // output CTAs per SM keep enough loads in flight (measured best for
-        // b4 L2048 d1536: 13 chunks), chunks of at least 128 tokens
+        // b4 L2048 d1536: 8 chunks), chunks of at least 128 tokens
         const int64_t k = std::max<int64_t>(
-            1, std::min<int64_t>((4 * kSms + per_chunk - 1) / per_chunk, L / 128));
+            1, std::min<int64_t>((5 * kSms / 2 + per_chunk - 1) / per_chunk, L / 128));
         chunk = ((L + k - 1) / k + TS - 1) / TS * TS;
     } else {
         // modelled time of every chunk count (see the planning note above)

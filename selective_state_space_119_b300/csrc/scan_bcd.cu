@@ -13,8 +13,9 @@
 // One lane owns one channel and all N of its states. A warp's 32 consecutive
 // channels read one contiguous 1 KB row of B (and of C) per token, so the loads
 // are fully coalesced and go straight from global memory into a ring of 4
-// (bf16) or 2 (fp32) tokens held in registers (the loads of a later token are
-// issued while a token computes); CTAs of 4 warps keep the loads in flight.
+// (bf16) or 2 (fp32) tokens held in registers (twice that in the chunk-state
+// pass, which reads no C); the loads of a later token are issued while a token
+// computes.
 // The L-chunk plan, the chunk-state pass and the carry composition are those of
 // the shared-B scan (same workspace layout).
 #include <cuda_bf16.h>
@@ -26,10 +27,12 @@ namespace ssm {
 namespace {
 
 constexpr int kBcdThreads = 128;    // = the 128-channel tile of configuration 0
-// tokens of loads in flight per lane (fp32 rows are twice as wide)
-template <typename T>
+// tokens of loads in flight per lane: the chunk-state pass reads no C (half
+// the bytes per token), so it keeps twice as many tokens in flight; fp32 rows
+// are twice as wide as bf16 ones
+template <typename T, int MODE>
 struct RingTokens {
-    static constexpr int value = sizeof(T) == 2 ? 4 : 2;
+    static constexpr int value = (sizeof(T) == 2 ? 4 : 2) * (MODE == 0 ? 2 : 1);
 };
 
 template <typename T, int N>
@@ -93,7 +96,7 @@ template <typename T, int N, int MODE, bool SOFTPLUS, bool GATE>
 __global__ void __launch_bounds__(kBcdThreads) scan_bcd_kernel(const ScanArgs a) {
     constexpr bool WITH_C = MODE == 1, WITH_Z = MODE == 1 && GATE;
     using S = Slot<T, N, WITH_C, WITH_Z>;
-    constexpr int kRing = RingTokens<T>::value;
+    constexpr int kRing = RingTokens<T, MODE>::value;
     const int64_t lin = blockIdx.x;   // chunk-major: ((k * batch) + b) * tiles + tile
     const int64_t tile = lin % a.tiles;
     const int64_t b = (lin / a.tiles) % a.batch;
