@@ -25,6 +25,20 @@
  *  - "State Space Models and Mamba", "Mamba: Selective State Spaces"
  *    (Delta_t = softplus(Linear(x_t))).
  *
+ * Entry points:
+ *  - the scan: ssm_selective_scan_fwd (from h = 0), _from_state (from a given
+ *    state), _static (library-owned scratch), _conv (the Mamba block's causal
+ *    conv1d + SiLU fused in front), and the input stage alone,
+ *    ssm_causal_conv1d_silu;
+ *  - training: ssm_selective_scan_fwd_ckpt (saves states for the backward)
+ *    and ssm_selective_scan_bwd (every gradient);
+ *  - generation: ssm_state_update (one token on a cached state);
+ *  - variants through dims->flags: SSM_FLAG_ZOH (exact zero-order-hold Bbar)
+ *    and SSM_FLAG_BC_PER_CHANNEL (B, C [batch, seqlen, dim, dstate]);
+ *  - sizes, plans and errors: ssm_scan_workspace_bytes, ssm_scan_plan,
+ *    ssm_scan_checkpoint_bytes, ssm_scan_bwd_workspace_bytes,
+ *    ssm_get_device_status, ssm_strerror, ssm_last_cuda_error, ssm_version.
+ *
  * Conventions for every entry point:
  *  - All tensors are contiguous, row-major, in DEVICE memory, caller-owned.
  *    The library never allocates, frees or keeps pointers past a call.

@@ -52,6 +52,12 @@
 // the chunk end get dt = dt x = 0, which leaves h unchanged exactly
 // (exp(0) = 1), and are not stored. No thread ever waits for another CTA; a
 // TMA wait that gives up sets the workspace status word and the CTA stops.
+//
+// Template flags of the kernel: SOFTPLUS and GATE (the delta transform and
+// the output gate); CONV, the Mamba block's causal conv1d + SiLU fused in front
+// (the x tile carries the 3 rows before the stage and u replaces x); CKPT, the
+// output pass also saves the state before every 8th token for the backward;
+// ZOH, the exact zero-order-hold input term (e^{dt A} - 1) / A B x.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
