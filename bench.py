@@ -295,10 +295,11 @@ def bench_scan(args, rank, world, local):
     res = {
         "value": value, "ms_per_step": slowest / args.steps * 1e3,
         "gbps": achieved,
-        "roofline": alu_roofline(spec, per_call, plan),
+        "roofline": dict(alu_roofline(spec, per_call, plan),
+                         traffic=scan_traffic(args.workload)),
         "hbm_roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
-                         "algorithmic_bytes_per_call": alg_bytes},
+                         "frac": achieved / peak, "traffic": scan_traffic(args.workload),
+                         "peak_kind": peak_kind, "algorithmic_bytes_per_call": alg_bytes},
         "floors_us": time_floors(spec, alg_bytes, peak),
         "gpu_launches": args.steps * plan["kernels"],
         "clocks": clocks.summary(t_wall0, t_wall1),
@@ -380,6 +381,34 @@ def time_floors(spec, alg_bytes, hbm_gbs):
     sfu = spec.elements * exps_per_element(spec) / (EX2_PER_SM_CLK * SMS * SM_MAX_MHZ * 1e6)
     fp32 = spec.elements * fp32_ops_per_element(spec) / (FP32_PER_SM_CLK * SMS * SM_MAX_MHZ * 1e6)
     return {"hbm": alg_bytes / (hbm_gbs * 1e9) * 1e6, "sfu": sfu * 1e6, "fp32": fp32 * 1e6}
+
+
+# DRAM traffic of one scan call of the benchmark workload (both launches:
+# chunk-state pass + output pass), dram__bytes_read.sum + dram__bytes_write.sum
+# from the ncu capture summarised in profiles/scan_launches_b4_L2048_d1536.md.
+# It holds only for the kernel source it was taken on: the sha256 below covers
+# the scan kernel and the headers it includes; any change there reports null.
+SCAN_TRAFFIC = {"workload": "scan_bf16_b4_L2048_d1536_softplus",
+                "bytes_per_call": 43608064 + 1024 + 78255104 + 703232,
+                "sha256": "d83dbb920848ca3edef4035565abd6efa1bb257ac11d95d685b8e93379ae147b"}
+SCAN_SOURCES = ("scan_fwd.cu", "ssm_device.cuh", "ssm_tma.cuh", "ssm_tmap.h", "ssm_internal.h")
+
+
+def scan_source_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "selective_state_space_119_b300", "csrc")
+    for name in SCAN_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def scan_traffic(spec_name):
+    if (SCAN_TRAFFIC["bytes_per_call"] is None or spec_name != SCAN_TRAFFIC["workload"]
+            or scan_source_sha256() != SCAN_TRAFFIC["sha256"]):
+        return None
+    return SCAN_TRAFFIC["bytes_per_call"]
 
 
 def alu_roofline(spec, per_call_s, plan):
