@@ -13,12 +13,12 @@
 // channel). LANES = N / NPL lanes share a channel, each holding NPL = 4 states
 // (one 128-bit load and store), so a warp reads and writes 512 contiguous
 // bytes of state per instruction; the state is streamed (read once, written
-// once) with evict-first cache hints. A CTA covers one batch row (the grid's
-// y index) and kItems * CH_PER_CTA channels; each thread handles kItems
-// channel groups that lie CH_PER_CTA channels apart, with all their loads
-// issued before any arithmetic, to keep enough bytes in flight per SM. The
-// partial C . h sums meet through butterfly shuffles; lane 0 of each group
-// writes y.
+// once) with evict-first cache hints. A CTA covers CH_PER_CTA channels of
+// kItems consecutive batch rows (the grid's y index); each lane group handles
+// its channel in all kItems rows, so A, the bias and D are loaded once for
+// them (every row reads the same [dim, N] A), with all loads issued before any
+// arithmetic, to keep enough bytes in flight per SM. The partial C . h sums
+// meet through butterfly shuffles; lane 0 of each group writes y.
 #include <cuda_bf16.h>
 
 #include "ssm_device.cuh"
@@ -68,63 +68,70 @@ __global__ void __launch_bounds__(kStepThreads) state_update_kernel(const StepAr
 
     const int lane_in_ch = threadIdx.x % LANES;
     const int n0 = lane_in_ch * NPL;
-    const int64_t b = blockIdx.y;              // batch row (2-D grid: no index division)
+    // One channel per lane group; the kItems items are kItems batch rows of that
+    // channel (2-D grid: the y index picks the rows), so A, the bias and D are
+    // loaded once and serve every row.
+    const int64_t dd = static_cast<int64_t>(blockIdx.x) * CH_PER_CTA + threadIdx.x / LANES;
+    const bool d_ok = dd < a.dim;
+    const int64_t d = d_ok ? dd : 0;
     const T* __restrict__ x = static_cast<const T*>(a.x);
     const T* __restrict__ delta = static_cast<const T*>(a.delta);
     const T* __restrict__ Bg = static_cast<const T*>(a.B);
     const T* __restrict__ Cg = static_cast<const T*>(a.C);
     const T* __restrict__ z = static_cast<const T*>(a.z);
 
+    float A2[NPL];
+    if constexpr (NPL == 4) {
+        const float4 av = __ldg(reinterpret_cast<const float4*>(a.A + d * N + n0));
+        A2[0] = av.x; A2[1] = av.y; A2[2] = av.z; A2[3] = av.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < NPL; ++j) A2[j] = __ldg(a.A + d * N + n0 + j);
+    }
+    const float bias = a.delta_bias ? __ldg(a.delta_bias + d) : 0.f;
+    const float Dd = a.D ? __ldg(a.D + d) : 0.f;
+
     // ---- loads of every item first ----
     int64_t ch[kItems];
     bool active[kItems];
-    float xv[kItems], dt[kItems], zv[kItems], h[kItems][NPL], A2[kItems][NPL], Bv[kItems][NPL],
-        Cv[kItems][NPL];
+    float xv[kItems], dt[kItems], zv[kItems], h[kItems][NPL], Bv[kItems][NPL], Cv[kItems][NPL];
 #pragma unroll
     for (int it = 0; it < kItems; ++it) {
-        // Whole groups of LANES lanes share the same channel, so the shuffles
-        // below always run with every participant present.
-        const int64_t dd = (static_cast<int64_t>(blockIdx.x) * kItems + it) * CH_PER_CTA +
-                           threadIdx.x / LANES;
-        active[it] = dd < a.dim;
-        const int64_t d = active[it] ? dd : 0;
+        // Whole groups of LANES lanes share the same channel and row, so the
+        // shuffles below always run with every participant present.
+        const int64_t bb = static_cast<int64_t>(blockIdx.y) * kItems + it;
+        active[it] = d_ok && bb < a.batch;
+        const int64_t b = bb < a.batch ? bb : 0;
         ch[it] = b * a.dim + d;
         const int64_t c = ch[it];
         xv[it] = IO<T>::ld(x + c);
-        dt[it] = IO<T>::ld(delta + c);
+        dt[it] = IO<T>::ld(delta + c) + bias;
         zv[it] = z ? IO<T>::ld(z + c) : 0.f;
         const float* st = a.state + c * N + n0;
         if constexpr (NPL == 4) {
             const float4 hv = __ldcs(reinterpret_cast<const float4*>(st));
             h[it][0] = hv.x; h[it][1] = hv.y; h[it][2] = hv.z; h[it][3] = hv.w;
-            const float4 av = __ldg(reinterpret_cast<const float4*>(a.A + d * N + n0));
-            A2[it][0] = av.x; A2[it][1] = av.y; A2[it][2] = av.z; A2[it][3] = av.w;
         } else {
 #pragma unroll
-            for (int j = 0; j < NPL; ++j) {
-                h[it][j] = __ldcs(st + j);
-                A2[it][j] = __ldg(a.A + d * N + n0 + j);
-            }
+            for (int j = 0; j < NPL; ++j) h[it][j] = __ldcs(st + j);
         }
         ld_vec<T, NPL>(Bg + b * N + n0, Bv[it]);
         ld_vec<T, NPL>(Cg + b * N + n0, Cv[it]);
-        if (a.delta_bias) dt[it] += __ldg(a.delta_bias + d);
     }
 
     // ---- arithmetic and stores ----
 #pragma unroll
     for (int it = 0; it < kItems; ++it) {
         const int64_t c = ch[it];
-        const int64_t d = c - b * a.dim;
         float dtv = dt[it];
         if (a.softplus) dtv = softplus(dtv);
         const float dtx = dtv * xv[it];
         float y = 0.f;
 #pragma unroll
         for (int j = 0; j < NPL; ++j) {
-            const float dA = ex2(dtv * (A2[it][j] * kLog2e));
+            const float dA = ex2(dtv * (A2[j] * kLog2e));
             // first order: Bbar x = dt x B; exact zero-order hold: x B m
-            const float bx = ZOH ? xv[it] * Bv[it][j] * zoh_m(dtv, A2[it][j], dA) : dtx * Bv[it][j];
+            const float bx = ZOH ? xv[it] * Bv[it][j] * zoh_m(dtv, A2[j], dA) : dtx * Bv[it][j];
             h[it][j] = fmaf(dA, h[it][j], bx);
             y = fmaf(Cv[it][j], h[it][j], y);
         }
@@ -141,7 +148,7 @@ __global__ void __launch_bounds__(kStepThreads) state_update_kernel(const StepAr
 #pragma unroll
         for (int off = 1; off < LANES; off <<= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
         if (active[it] && lane_in_ch == 0) {
-            if (a.D) y = fmaf(__ldg(a.D + d), xv[it], y);
+            y = fmaf(Dd, xv[it], y);
             if (z) y *= silu(zv[it]);
             IO<T>::st(static_cast<T*>(a.out) + c, y);
         }
@@ -152,12 +159,11 @@ template <typename T, int N, bool ZOH>
 cudaError_t launch_zoh(const StepArgs& a, cudaStream_t s) {
     constexpr int NPL = N >= 4 ? 4 : N;
     constexpr int CH_PER_CTA = kStepThreads / (N / NPL);
-    constexpr int64_t kMaxGridY = 65535;
-    const int64_t per_cta = int64_t(CH_PER_CTA) * kItems;
-    // batch rows go on the grid's y axis, in slices of at most 65535 rows
-    for (int64_t b0 = 0; b0 < a.batch; b0 += kMaxGridY) {
+    constexpr int64_t kMaxRows = 65535 * kItems;   // rows of one launch (grid y limit)
+    // kItems batch rows per CTA row of the grid, in slices of at most kMaxRows rows
+    for (int64_t b0 = 0; b0 < a.batch; b0 += kMaxRows) {
         StepArgs p = a;
-        p.batch = a.batch - b0 < kMaxGridY ? a.batch - b0 : kMaxGridY;
+        p.batch = a.batch - b0 < kMaxRows ? a.batch - b0 : kMaxRows;
         const int64_t e = b0 * a.dim;      // elements before the slice
         p.state = a.state + e * N;
         p.x = static_cast<const T*>(a.x) + e;
@@ -166,8 +172,8 @@ cudaError_t launch_zoh(const StepArgs& a, cudaStream_t s) {
         p.out = static_cast<T*>(a.out) + e;
         p.B = static_cast<const T*>(a.B) + b0 * N;
         p.C = static_cast<const T*>(a.C) + b0 * N;
-        const dim3 grid(static_cast<unsigned>((a.dim + per_cta - 1) / per_cta),
-                        static_cast<unsigned>(p.batch));
+        const dim3 grid(static_cast<unsigned>((a.dim + CH_PER_CTA - 1) / CH_PER_CTA),
+                        static_cast<unsigned>((p.batch + kItems - 1) / kItems));
         state_update_kernel<T, N, ZOH><<<grid, kStepThreads, 0, s>>>(p);
     }
     return cudaGetLastError();
