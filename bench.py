@@ -12,7 +12,8 @@ bias), gate), i.e. every step of the scan path. Rank 0 prints one JSON line.
   larger than twice the L2 cache, so every step reads its inputs from HBM.
 * e2e: the same metric through the same C-ABI call with host buffers:
   pinned host -> device copies of the step's inputs and a device -> host copy
-  of its output inside the timed region.
+  of its output inside the timed region, every step; the copies of one step
+  overlap the compute of its neighbours (three streams, two buffer sets).
 * roofline: the binding unit of the scan, the SFU: the SFU operations the
   method needs per call / average call time, against the measured ex2 rate;
   hbm_roofline: algorithmic bytes per call / call time against the measured
@@ -307,36 +308,69 @@ def bench_scan(args, rank, world, local):
         "input_sets": nsets,
     }
 
-    # end to end: pinned host buffers, copies inside the timed region
+    # end to end: pinned host buffers; every step copies its inputs in and its
+    # output out inside the timed region. The copies of one step overlap the
+    # compute of its neighbours: three streams (in, compute, out), two device
+    # buffer sets, ordered by events (a set's inputs are overwritten only after
+    # the compute two steps back has read them, its output only after the copy
+    # out two steps back has read it).
     host = {k: (None if base[k] is None else base[k].cpu().pin_memory())
             for k in ("x", "delta", "z", "B", "C")}
-    s0 = sets[0]
-    h_out = torch.empty(s0["out"].shape, dtype=s0["out"].dtype).pin_memory()
+    e2e_sets = sets[:2]
+    h_outs = [torch.empty(e2e_sets[0]["out"].shape, dtype=e2e_sets[0]["out"].dtype).pin_memory()
+              for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_outs[0].numel() * h_outs[0].element_size()
     k_e2e = max(3, min(args.steps, 50))
+    s_in, s_cmp, s_out = (torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+    cmp_ptr = ctypes.c_void_p(s_cmp.cuda_stream)
+    cmp_args = [(_vp(st["x"]), _vp(st["delta"]), _vp(st["A"]), _vp(st["B"]), _vp(st["C"]),
+                 _vp(st["D"]), _vp(st["z"]), _vp(st["delta_bias"]),
+                 1 if spec.delta_softplus else 0, _vp(st["out"]), _vp(st["fs"]),
+                 ctypes.byref(dims), cmp_ptr) for st in e2e_sets]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for k, t in host.items():
-            if t is not None:
-                s0[k].copy_(t, non_blocking=True)
-        step(0)
-        h_out.copy_(s0["out"], non_blocking=True)
+    def e2e_step(i):
+        k = i % 2
+        st = e2e_sets[k]
+        if i >= 2:
+            s_in.wait_event(ev_cmp[k])
+        with torch.cuda.stream(s_in):
+            for name, t in host.items():
+                if t is not None:
+                    st[name].copy_(t, non_blocking=True)
+            ev_in[k].record(s_in)
+        s_cmp.wait_event(ev_in[k])
+        if i >= 2:
+            s_cmp.wait_event(ev_out[k])
+        rc = fn(*cmp_args[k])
+        if rc != 0:
+            raise libssm.SSMError(rc, "ssm_selective_scan_fwd")
+        ev_cmp[k].record(s_cmp)
+        s_out.wait_event(ev_cmp[k])
+        with torch.cuda.stream(s_out):
+            h_outs[k].copy_(st["out"], non_blocking=True)
+            ev_out[k].record(s_out)
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(4):
+        e2e_step(i)
     torch.cuda.synchronize()
     if dist.is_initialized():
         dist.barrier()
-    e0.record(stream)
-    for _ in range(k_e2e):
-        e2e_step()
-    e1.record(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(k_e2e):
+        e2e_step(i)
+    e1.record(s_out)           # after the last copy out, which follows every other step
     torch.cuda.synchronize()
     e2e_sec = e0.elapsed_time(e1) / 1e3
     e2e_value, _ = aggregate(elems * k_e2e, e2e_sec)
     res["e2e"] = {"value": e2e_value, "unit": "elems/s", "h2d_bytes_per_step": h2d,
-                  "d2h_bytes_per_step": d2h, "steps": k_e2e}
+                  "d2h_bytes_per_step": d2h, "steps": k_e2e,
+                  "pipelined": "copies in, compute and copies out of neighbouring steps "
+                               "overlap (3 streams, 2 device buffer sets)"}
 
     # quick self-check of the timed output against the oracle on a few channels
     res["check"] = parity_probe(spec, inp, sets[0]["out"]) if rank == 0 else None
