@@ -37,7 +37,8 @@
  *    and SSM_FLAG_BC_PER_CHANNEL (B, C [batch, seqlen, dim, dstate]);
  *  - sizes, plans and errors: ssm_scan_workspace_bytes, ssm_scan_plan,
  *    ssm_scan_checkpoint_bytes, ssm_scan_bwd_workspace_bytes,
- *    ssm_get_device_status, ssm_strerror, ssm_last_cuda_error, ssm_version.
+ *    ssm_get_device_status, ssm_strerror, ssm_last_cuda_error, ssm_version;
+ *  - a test of the failure path: ssm_debug_timeout_probe.
  *
  * Conventions for every entry point:
  *  - All tensors are contiguous, row-major, in DEVICE memory, caller-owned.
@@ -343,6 +344,19 @@ typedef struct {
     int32_t tile_config;    /* tile configuration id (0..3)             */
 } ssm_plan;
 int ssm_scan_plan(const ssm_dims* dims, ssm_plan* plan);
+
+/*
+ * ssm_debug_timeout_probe -- for tests of the failure path. Enqueues a one-CTA
+ * kernel that waits, with the scan kernels' bounded mbarrier wait, on a barrier
+ * nothing arrives on, gives up after max_polls probes (1 .. 2^24; each probe may
+ * suspend the thread for a short, hardware-chosen time) and sets the status
+ * word of `workspace` (at least 256 bytes, 16-byte aligned) as a scan kernel
+ * whose copy never landed would. The next ssm_get_device_status on that
+ * workspace returns SSM_ERR_TIMEOUT. Nothing faults or hangs; the context
+ * stays usable.
+ */
+int ssm_debug_timeout_probe(void* workspace, size_t workspace_bytes, uint32_t max_polls,
+                            ssm_stream_t stream);
 
 /* Synchronizes `stream`, then reads the device-side status word of the
  * workspace: SSM_OK, or SSM_ERR_TIMEOUT when a bounded wait inside a scan

@@ -568,6 +568,16 @@ int ssm_state_update(float* state, const void* x, const void* delta, const float
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int ssm_debug_timeout_probe(void* workspace, size_t workspace_bytes, uint32_t max_polls,
+                            ssm_stream_t stream) {
+    if (!workspace) return SSM_ERR_NULL;
+    if (workspace_bytes < ssm::kWsHeaderBytes) return SSM_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return SSM_ERR_ALIGN;
+    if (max_polls < 1 || max_polls > (1u << 24)) return SSM_ERR_DIMS;
+    return set_cuda(ssm::launch_timeout_probe(static_cast<unsigned int*>(workspace), max_polls,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int ssm_get_device_status(const ssm_dims* dims, ssm_stream_t stream) {
     int rc = check_dims(dims, true);
     if (rc != SSM_OK) return rc;

@@ -147,6 +147,8 @@ cudaError_t launch_state_update(const StepArgs& a, int io, int N, cudaStream_t s
 cudaError_t launch_scan_bcd(const ScanArgs& a, const ScanPlan& p, int io, cudaStream_t s);
 // Enqueue the gradient passes (reverse carries, gradients, reduction).
 cudaError_t launch_scan_bwd(const BwdArgs& a, int io, cudaStream_t s);
+// Enqueue the failure-path probe: a bounded wait that runs out and sets *status.
+cudaError_t launch_timeout_probe(unsigned int* status, uint32_t max_polls, cudaStream_t s);
 // Enqueue the standalone causal depthwise conv1d + SiLU.
 cudaError_t launch_conv1d_silu(const ConvArgs& a, int io, cudaStream_t s);
 

@@ -47,7 +47,7 @@ EXPORTED = ("ssm_selective_scan_fwd", "ssm_state_update", "ssm_scan_workspace_by
             "ssm_version", "ssm_selective_scan_fwd_static", "ssm_selective_scan_fwd_from_state",
             "ssm_selective_scan_fwd_conv", "ssm_causal_conv1d_silu", "ssm_scan_checkpoint_bytes",
             "ssm_selective_scan_fwd_ckpt", "ssm_scan_bwd_workspace_bytes",
-            "ssm_selective_scan_bwd")
+            "ssm_selective_scan_bwd", "ssm_debug_timeout_probe")
 
 # Size of the library-owned scratch of ssm_selective_scan_fwd_static (include/ssm.h).
 SSM_STATIC_SCRATCH_BYTES = 16 << 20
@@ -99,6 +99,8 @@ lib.ssm_scan_workspace_bytes.restype = ctypes.c_size_t
 lib.ssm_scan_workspace_bytes.argtypes = [_dims_p]
 lib.ssm_scan_plan.restype = ctypes.c_int
 lib.ssm_scan_plan.argtypes = [_dims_p, ctypes.POINTER(ssm_plan)]
+lib.ssm_debug_timeout_probe.restype = ctypes.c_int
+lib.ssm_debug_timeout_probe.argtypes = [_vp, ctypes.c_size_t, ctypes.c_uint32, _vp]
 lib.ssm_get_device_status.restype = ctypes.c_int
 lib.ssm_get_device_status.argtypes = [_dims_p, _vp]
 lib.ssm_strerror.restype = ctypes.c_char_p

@@ -298,3 +298,12 @@ def test_bc_per_channel_flag_is_validated():
     assert L.lib.ssm_state_update(FAKE + (6 << 20), FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288,
                                   FAKE + 16384, None, None, None, 0, FAKE + 20480,
                                   ctypes.byref(st), None) == L.SSM_ERR_DIMS
+
+
+def test_timeout_probe_rejects_bad_arguments_before_launch():
+    f = L.lib.ssm_debug_timeout_probe
+    assert f(None, 256, 1000, None) == L.SSM_ERR_NULL
+    assert f(FAKE, 255, 1000, None) == L.SSM_ERR_WORKSPACE
+    assert f(FAKE + 4, 256, 1000, None) == L.SSM_ERR_ALIGN
+    assert f(FAKE, 256, 0, None) == L.SSM_ERR_DIMS
+    assert f(FAKE, 256, (1 << 24) + 1, None) == L.SSM_ERR_DIMS

@@ -257,3 +257,25 @@ def test_device_status_ok_after_calls(torch):
     ws = libssm.alloc_workspace(1, 256, 16, 16, "bf16", "cuda", chunk_len_hint=16)
     G.gpu_scan(inp, False, chunk_len_hint=16, workspace=ws)
     assert libssm.ssm_get_device_status(1, 256, 16, 16, "bf16", ws, chunk_len_hint=16) == 0
+
+
+def test_bounded_wait_that_runs_out_reports_timeout(torch):
+    """Failure detection without a fault: a kernel's bounded wait on a barrier
+    that nothing arrives on gives up, sets the workspace status word, and the
+    host reads SSM_ERR_TIMEOUT; the word is cleared once read and the context
+    keeps working (a scan right after matches the oracle)."""
+    import ctypes
+    from selective_state_space_119_b300 import libssm
+    t = torch
+    ws = t.zeros(256, dtype=t.uint8, device="cuda")
+    rc = libssm.lib.ssm_debug_timeout_probe(ctypes.c_void_p(ws.data_ptr()), 256, 20000,
+                                            ctypes.c_void_p(t.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    assert libssm.ssm_get_device_status(1, 256, 16, 16, "bf16", ws, chunk_len_hint=256) == \
+        libssm.SSM_ERR_TIMEOUT
+    assert libssm.ssm_get_device_status(1, 256, 16, 16, "bf16", ws, chunk_len_hint=256) == 0
+    spec = I.ScanSpec(1, 256, 16, io="f32", seed=91)
+    inp = I.make_scan_inputs(spec)
+    out, _ = G.gpu_scan(inp, False)
+    ry, _ = G.oracle_scan(inp, False)
+    G.parity(G.host64(out), ry, "f32", "scan after a timed-out wait")
