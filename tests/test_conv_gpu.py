@@ -166,3 +166,31 @@ def test_full_size_workload_sampled(torch):
     ry, rh = _fused_ref(inp, True, w, b, dsel)
     G.parity(G.host64(out)[:, :, dsel], ry, "bf16", "fused y full size")
     G.parity(G.host64(fs)[:, dsel], rh, "state", "fused final state full size")
+
+
+def test_guard_bands_untouched(torch):
+    """u of the standalone conv and y of the fused scan, written into the middle
+    of pattern-filled buffers (ragged sequence end, channel count not a multiple
+    of a tile): the bands stay untouched; a second call is bit-identical."""
+    from selective_state_space_119_b300 import libssm
+    t = torch
+    spec = I.ScanSpec(2, 203, 136, io="bf16", gate=True, seed=57)
+    inp = I.make_scan_inputs(spec)
+    w, b = I.make_conv_weights(136, 4, True, seed=58)
+    n, pad = 2 * 203 * 136, 4096
+    big = t.full((pad + n + pad,), 7.0, dtype=t.bfloat16, device="cuda")
+    u = big[pad:pad + n].view(2, 203, 136)
+    libssm.ssm_causal_conv1d_silu(G.dev(inp["x"]), G.dev(w), G.dev(b), out=u)
+    t.cuda.synchronize()
+    assert t.all(big[:pad] == 7.0) and t.all(big[pad + n:] == 7.0)
+    G.parity(G.host64(u), _conv_ref(inp["x"], w, b), "bf16", "conv in guarded buffer")
+    u2 = libssm.ssm_causal_conv1d_silu(G.dev(inp["x"]), G.dev(w), G.dev(b))
+    assert t.equal(u, u2)
+    big2 = t.full((pad + n + pad,), 7.0, dtype=t.bfloat16, device="cuda")
+    out = big2[pad:pad + n].view(2, 203, 136)
+    libssm.ssm_selective_scan_fwd(
+        G.dev(inp["x"]), G.dev(inp["delta"]), G.dev(inp["A"]), G.dev(inp["B"]), G.dev(inp["C"]),
+        D=G.dev(inp["D"]), z=G.dev(inp["z"]), out=out, chunk_len_hint=64, conv_w=G.dev(w),
+        conv_b=G.dev(b))
+    t.cuda.synchronize()
+    assert t.all(big2[:pad] == 7.0) and t.all(big2[pad + n:] == 7.0)

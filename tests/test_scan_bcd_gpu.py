@@ -94,3 +94,27 @@ def test_bcd_benchmark_size_sampled(torch):
     ry, rh = _ref(inp, B4, C4, True, dsel=dsel)
     G.parity(G.host64(out)[:, :, dsel], ry, "bf16", "per-channel y, benchmark size")
     G.parity(G.host64(fs)[:, dsel], rh, "state", "per-channel final state, benchmark size")
+
+
+def test_bcd_guard_bands_and_bitwise_repeat(torch):
+    from selective_state_space_119_b300 import libssm
+    t = torch
+    spec = I.ScanSpec(2, 203, 136, io="bf16", seed=85)
+    inp = I.make_scan_inputs(spec)
+    B4, C4 = I.make_bc_per_channel(spec)
+    n, nf, pad = 2 * 203 * 136, 2 * 136 * 16, 4096
+    big = t.full((pad + n + pad,), 9.0, dtype=t.bfloat16, device="cuda")
+    fbig = t.full((pad + nf + pad,), -9.0, dtype=t.float32, device="cuda")
+    out = big[pad:pad + n].view(2, 203, 136)
+    fs = fbig[pad:pad + nf].view(2, 136, 16)
+    args = (G.dev(inp["x"]), G.dev(inp["delta"]), G.dev(inp["A"]), G.dev(B4), G.dev(C4))
+    libssm.ssm_selective_scan_fwd(*args, D=G.dev(inp["D"]), z=G.dev(inp["z"]), out=out,
+                                  final_state=fs, chunk_len_hint=64)
+    t.cuda.synchronize()
+    assert t.all(big[:pad] == 9.0) and t.all(big[pad + n:] == 9.0)
+    assert t.all(fbig[:pad] == -9.0) and t.all(fbig[pad + nf:] == -9.0)
+    o2, f2 = libssm.ssm_selective_scan_fwd(*args, D=G.dev(inp["D"]), z=G.dev(inp["z"]),
+                                           chunk_len_hint=64)
+    assert t.equal(out, o2) and t.equal(fs, f2)
+    ry, rh = _ref(inp, B4, C4, False)
+    G.parity(G.host64(out), ry, "bf16", "per-channel y in guarded buffer")

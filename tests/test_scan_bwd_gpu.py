@@ -189,3 +189,67 @@ def test_benchmark_workload_gradients(torch):
     _, _, _, g = _gpu_train(inp, True, dout)
     ref = _oracle_bwd(inp, True, dout)
     _check_grads(g, ref, "bf16", "(benchmark workload)")
+
+
+def _guarded(torch, shape, dtype, fill, pad=4096):
+    n = 1
+    for s in shape:
+        n *= s
+    big = torch.full((pad + n + pad,), fill, dtype=dtype, device="cuda")
+    return big, big[pad:pad + n].view(*shape), pad, n
+
+
+def test_gradients_guard_bands_and_bitwise_repeat(torch):
+    """Every gradient written into the middle of a pattern-filled buffer: the
+    bands before and after stay untouched (no write out of bounds, ragged
+    sequence end and channel tile), and a second call gives bit-identical
+    gradients (the sums are added in a fixed order)."""
+    import ctypes
+    from selective_state_space_119_b300 import libssm
+    t = torch
+    spec = I.ScanSpec(2, 203, 136, io="bf16", delta_kind="softplus_bias", A_kind="lognormal",
+                      D_kind="uniform", seed=75)
+    inp, dout, h0, dfin = _case(spec, 76, with_h0=True, with_dfinal=True)
+    d = {k: G.dev(v) for k, v in inp.items()}
+    _, _, ck = libssm.ssm_selective_scan_fwd_ckpt(
+        d["x"], d["delta"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+        delta_bias=d["delta_bias"], delta_softplus=True, h0=G.dev(h0), chunk_len_hint=64)
+    b, L, D, N = 2, 203, 136, 16
+    io = t.bfloat16
+    # keep every uploaded input referenced until the kernels have run (a freed
+    # temporary would be handed to the next upload by the caching allocator)
+    dout_t, dfin_t = G.dev(dout), G.dev(dfin)
+
+    def run():
+        outs = {"dx": _guarded(t, (b, L, D), io, 3.0), "ddelta": _guarded(t, (b, L, D), io, 3.0),
+                "dz": _guarded(t, (b, L, D), io, 3.0), "dB": _guarded(t, (b, L, N), io, 3.0),
+                "dC": _guarded(t, (b, L, N), io, 3.0),
+                "dA": _guarded(t, (D, N), t.float32, -5.0), "dD": _guarded(t, (D,), t.float32, -5.0),
+                "dbias": _guarded(t, (D,), t.float32, -5.0),
+                "dh0": _guarded(t, (b, D, N), t.float32, -5.0)}
+        nb = libssm.ssm_scan_bwd_workspace_bytes(b, L, D, N, "bf16", chunk_len_hint=64)
+        ws = t.full((nb,), 0x5A, dtype=t.uint8, device="cuda")     # no initial contents needed
+        dims = libssm.make_dims(b, L, D, N, "bf16", ws.data_ptr(), nb, chunk_len_hint=64)
+        p = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())
+        rc = libssm.lib.ssm_selective_scan_bwd(
+            p(d["x"]), p(d["delta"]), p(d["A"]), p(d["B"]), p(d["C"]), p(d["D"]), p(d["z"]),
+            p(d["delta_bias"]), 1, p(ck), p(dout_t), p(dfin_t),
+            p(outs["dx"][1]), p(outs["ddelta"][1]), p(outs["dA"][1]), p(outs["dB"][1]),
+            p(outs["dC"][1]), p(outs["dD"][1]), p(outs["dz"][1]), p(outs["dbias"][1]),
+            p(outs["dh0"][1]), ctypes.byref(dims),
+            ctypes.c_void_p(t.cuda.current_stream().cuda_stream))
+        assert rc == 0
+        t.cuda.synchronize()
+        for k, (big, view, pad, n) in outs.items():
+            fill = 3.0 if big.dtype == io else -5.0
+            assert t.all(big[:pad] == fill) and t.all(big[pad + n:] == fill), "guard band of " + k
+        return {k: v[1].clone() for k, v in outs.items()}
+
+    g1 = run()
+    g2 = run()
+    for k in g1:
+        assert t.equal(g1[k], g2[k]), "not bit-identical: " + k
+    ref = _oracle_bwd(inp, True, dout, h0=h0, dfinal=dfin)
+    g = {"dx": g1["dx"], "ddelta": g1["ddelta"], "dz": g1["dz"], "dB": g1["dB"], "dC": g1["dC"],
+         "dA": g1["dA"], "dD": g1["dD"], "ddelta_bias": g1["dbias"], "dh0": g1["dh0"]}
+    _check_grads(g, ref, "bf16", "(guarded buffers)", dh0=True)
