@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
             const float* Bt = bcs + tt * 2 * N + j * SPL;
             const float* Ct = Bt + N;
             const float2 gp = lds_pair(in + Sm::kDout + tt * kBwdChannels + pc);
-            float zv[NS], dy[NS], dt[NS];
+            float dy[NS], dt[NS];
             float gate_ds = 1.f;   // silu'(z) of the own channel
             if constexpr (MODE == 1) {
                 const float2 dtp = dts[tt * kBwdThreads + tid];
@@ -311,10 +311,10 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
             dy[0] = j ? gp.y : gp.x;
             if constexpr (GATE) {
                 const float2 zp = lds_pair(in + Sm::kZ + tt * kBwdChannels + pc);
-                zv[0] = j ? zp.y : zp.x;
-                const float sg = 1.f / (1.f + __expf(-zv[0]));
-                gate_ds = sg * fmaf(zv[0], 1.f - sg, 1.f);
-                dy[0] *= zv[0] * sg;
+                const float zo = j ? zp.y : zp.x;   // z of the own channel
+                const float sg = 1.f / (1.f + __expf(-zo));
+                gate_ds = sg * fmaf(zo, 1.f - sg, 1.f);
+                dy[0] *= zo * sg;
             }
             dy[1] = __shfl_xor_sync(0xffffffffu, dy[0], 1);   // the partner's channel
             if constexpr (MODE == 0) {
