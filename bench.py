@@ -55,6 +55,12 @@ DEFAULT_WORKLOAD = "scan_bf16_b4_L2048_d1536_softplus"
 DECODE_WORKLOAD = "decode_bf16_b256_d5120_x64"
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6400.0
+NOMINAL_HBM_GBS = 7700.0      # B300 HBM3e datasheet bandwidth, for context beside the measured peak
+
+
+def nominal(achieved_gbs):
+    """The same achieved bandwidth as a fraction of the nominal HBM3e figure."""
+    return {"nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved_gbs / NOMINAL_HBM_GBS}
 
 
 # ---------------------------------------------------------------------------
@@ -298,9 +304,10 @@ def bench_scan(args, rank, world, local):
         "gbps": achieved,
         "roofline": dict(alu_roofline(spec, per_call, plan),
                          traffic=scan_traffic(args.workload)),
-        "hbm_roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": scan_traffic(args.workload),
-                         "peak_kind": peak_kind, "algorithmic_bytes_per_call": alg_bytes},
+        "hbm_roofline": dict({"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                              "frac": achieved / peak, "traffic": scan_traffic(args.workload),
+                              "peak_kind": peak_kind, "algorithmic_bytes_per_call": alg_bytes},
+                             **nominal(achieved)),
         "floors_us": time_floors(spec, alg_bytes, peak),
         "gpu_launches": args.steps * plan["kernels"],
         "clocks": clocks.summary(t_wall0, t_wall1),
@@ -523,9 +530,9 @@ def bench_decode(args, dev, stream):
     return {"workload": DECODE_WORKLOAD, "metric": "decode elems/s (B*D per step)",
             "value": spec.batch * spec.dim / sec, "unit": "elems/s", "us_per_step": sec * 1e6,
             "us_per_64_steps": sec * 64 * 1e6, "states_rotated": nstates, "timed_steps": n,
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                         "frac": gbs / peak, "traffic": None, "peak_kind": kind,
-                         "algorithmic_bytes_per_call": alg}}
+            "roofline": dict({"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                              "frac": gbs / peak, "traffic": None, "peak_kind": kind,
+                              "algorithmic_bytes_per_call": alg}, **nominal(gbs))}
 
 
 def bench_input_stage(args, spec, dev, stream):
@@ -609,9 +616,11 @@ def bench_input_stage(args, spec, dev, stream):
     elems = spec.elements
     return {"conv_width": K, "timed_calls": n, "input_sets": nsets,
             "conv": {"us_per_call": t_conv * 1e6, "value": elems / t_conv, "unit": "elems/s",
-                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                                  "frac": gbs / peak, "traffic": None, "peak_kind": kind,
-                                  "algorithmic_bytes_per_call": conv_bytes}},
+                     "roofline": dict({"bound": "hbm", "achieved": gbs, "peak": peak,
+                                       "unit": "GB/s", "frac": gbs / peak, "traffic": None,
+                                       "peak_kind": kind,
+                                       "algorithmic_bytes_per_call": conv_bytes},
+                                      **nominal(gbs))},
             "fused_scan": {"us_per_call": t_fused * 1e6, "value": elems / t_fused,
                            "unit": "elems/s", "kernels_per_call": plan["kernels"]},
             "conv_then_scan": {"us_per_call": t_two * 1e6, "value": elems / t_two,
@@ -762,9 +771,9 @@ def bench_bcd(args, spec, dev, stream):
     plan = libssm.ssm_scan_plan(B_, L_, D_, N_, io, flags=F)
     return {"us_per_call": sec * 1e6, "value": spec.elements / sec, "unit": "elems/s",
             "timed_calls": n, "input_sets": nsets, "kernels_per_call": plan["kernels"],
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                         "frac": gbs / peak, "traffic": None, "peak_kind": kind,
-                         "algorithmic_bytes_per_call": alg}}
+            "roofline": dict({"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                              "frac": gbs / peak, "traffic": None, "peak_kind": kind,
+                              "algorithmic_bytes_per_call": alg}, **nominal(gbs))}
 
 
 # ---------------------------------------------------------------------------
