@@ -330,8 +330,9 @@ int ssm_selective_scan_fwd_static(const void* x, const void* delta, const float*
 
 /* Bytes of workspace ssm_selective_scan_fwd needs for these sizes (256 when
  * the scan runs in one pass, 0 for empty problems). Depends only on batch,
- * seqlen, dim, dstate, io_dtype, chunk_len_hint and tile_config_hint; returns
- * 0 for invalid sizes. */
+ * seqlen, dim, dstate, io_dtype, chunk_len_hint, tile_config_hint and flags
+ * (per-channel B, C are planned with more L-chunks); returns 0 for invalid
+ * sizes. */
 size_t ssm_scan_workspace_bytes(const ssm_dims* dims);
 
 /* Launch plan the scan will use for these sizes (for benchmarks and tests). */
