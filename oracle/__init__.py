@@ -72,13 +72,15 @@ def _bind(lib):
     for name in ("oracle_state_update", "oracle_state_update_zoh"):
         getattr(lib, name).restype = ctypes.c_int
         getattr(lib, name).argtypes = [_i64] * 3 + [_dp] * 9 + [ctypes.c_int] + [_dp]
-    lib.oracle_phi.restype = ctypes.c_double
-    lib.oracle_phi.argtypes = [ctypes.c_double]
+    for name in ("oracle_phi", "oracle_phi_prime"):
+        getattr(lib, name).restype = ctypes.c_double
+        getattr(lib, name).argtypes = [ctypes.c_double]
     lib.oracle_causal_conv1d_silu.restype = None
     lib.oracle_causal_conv1d_silu.argtypes = [_i64] * 4 + [_dp] * 4
-    lib.oracle_selective_scan_bwd.restype = ctypes.c_int
-    lib.oracle_selective_scan_bwd.argtypes = (
-        [_i64] * 4 + [_dp] * 8 + [ctypes.c_int] + [_dp] * 12 + [ctypes.c_int])
+    for name in ("oracle_selective_scan_bwd", "oracle_selective_scan_bwd_zoh"):
+        getattr(lib, name).restype = ctypes.c_int
+        getattr(lib, name).argtypes = (
+            [_i64] * 4 + [_dp] * 8 + [ctypes.c_int] + [_dp] * 12 + [ctypes.c_int])
     return lib
 
 
@@ -128,6 +130,9 @@ class Oracle:
 
     def phi(self, z: float) -> float:
         return self._lib.oracle_phi(float(z))
+
+    def phi_prime(self, z: float) -> float:
+        return self._lib.oracle_phi_prime(float(z))
 
     def selective_scan(self, x, delta, A, B, C, D=None, z=None, delta_bias=None,
                        delta_softplus=False, h0=None, nthreads=None, zoh=False):
@@ -200,11 +205,12 @@ Oracle.causal_conv1d_silu = _conv_method
 
 
 def _bwd_method(self, x, delta, A, B, C, dout, D=None, z=None, delta_bias=None,
-                delta_softplus=False, h0=None, dh_final=None, nthreads=None):
+                delta_softplus=False, h0=None, dh_final=None, nthreads=None, zoh=False):
     """Gradients of the selective scan for the loss sum(dout * out) (+ sum(dh_final
-    * final_state)). Returns a dict of float64 arrays: dx, ddelta, dz (None
-    without z) [batch, L, dim]; dA [dim, N]; dB, dC [batch, L, N]; dD, ddelta_bias
-    [dim] (None without D / delta_bias); dh0 [batch, dim, N]."""
+    * final_state)); zoh=True differentiates the exact zero-order-hold scan.
+    Returns a dict of float64 arrays: dx, ddelta, dz (None without z)
+    [batch, L, dim]; dA [dim, N]; dB, dC [batch, L, N]; dD, ddelta_bias [dim]
+    (None without D / delta_bias); dh0 [batch, dim, N]."""
     x = _f64(x)
     batch, L, dim = x.shape
     A = _f64(A)
@@ -222,7 +228,8 @@ def _bwd_method(self, x, delta, A, B, C, dout, D=None, z=None, delta_bias=None,
          "dz": np.zeros((batch, L, dim)) if z is not None else None,
          "ddelta_bias": np.zeros(dim) if delta_bias is not None else None,
          "dh0": np.zeros((batch, dim, N))}
-    rc = self._lib.oracle_selective_scan_bwd(
+    fn = self._lib.oracle_selective_scan_bwd_zoh if zoh else self._lib.oracle_selective_scan_bwd
+    rc = fn(
         batch, L, dim, N, _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
         _ptr(delta_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(dout), _ptr(dh_final),
         _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
@@ -237,7 +244,7 @@ Oracle.selective_scan_bwd = _bwd_method
 
 
 def _bcd_method(self, x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
-                h0=None, nthreads=None):
+                h0=None, nthreads=None, zoh=False):
     """The scan with per-channel B, C [batch, L, dim, N]: every channel d is the
     one-channel scan of the oracle with its own rows B[:, :, d], C[:, :, d]
     (channels are independent). Returns (out, final_state) like selective_scan."""
@@ -255,13 +262,56 @@ def _bcd_method(self, x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_
             D=None if D is None else _f64(D)[d:d + 1], z=None if z is None else _f64(z)[sl],
             delta_bias=None if delta_bias is None else _f64(delta_bias)[d:d + 1],
             delta_softplus=delta_softplus, h0=None if h0 is None else _f64(h0)[:, d:d + 1],
-            nthreads=1)
+            nthreads=1, zoh=zoh)
         out[:, :, d] = o[:, :, 0]
         fs[:, d] = f[:, 0]
     return out, fs
 
 
 Oracle.selective_scan_bcd = _bcd_method
+
+
+def _bcd_bwd_method(self, x, delta, A, B, C, dout, D=None, z=None, delta_bias=None,
+                    delta_softplus=False, h0=None, dh_final=None, nthreads=None, zoh=False):
+    """Gradients of the per-channel B, C scan: channel d is the one-channel scan
+    with rows B[:, :, d], C[:, :, d], so its gradients are those of that scan
+    (dB, dC of a one-channel problem sum over that channel alone). Returns the
+    dict of selective_scan_bwd with dB, dC of shape [batch, L, dim, N]."""
+    x = _f64(x)
+    batch, L, dim = x.shape
+    B, C = _f64(B), _f64(C)
+    N = B.shape[3]
+    A = _f64(A, (dim, N))
+    sl3 = lambda a, d: None if a is None else _f64(a)[:, :, d:d + 1]
+    sl1 = lambda a, d: None if a is None else _f64(a)[d:d + 1]
+    sl2 = lambda a, d: None if a is None else _f64(a)[:, d:d + 1]
+    g = {"dx": np.zeros((batch, L, dim)), "ddelta": np.zeros((batch, L, dim)),
+         "dA": np.zeros((dim, N)), "dB": np.zeros((batch, L, dim, N)),
+         "dC": np.zeros((batch, L, dim, N)),
+         "dD": np.zeros(dim) if D is not None else None,
+         "dz": np.zeros((batch, L, dim)) if z is not None else None,
+         "ddelta_bias": np.zeros(dim) if delta_bias is not None else None,
+         "dh0": np.zeros((batch, dim, N))}
+    for d in range(dim):
+        gd = self.selective_scan_bwd(
+            sl3(x, d), sl3(delta, d), A[d:d + 1], B[:, :, d], C[:, :, d], sl3(dout, d),
+            D=sl1(D, d), z=sl3(z, d), delta_bias=sl1(delta_bias, d),
+            delta_softplus=delta_softplus, h0=sl2(h0, d), dh_final=sl2(dh_final, d),
+            nthreads=1, zoh=zoh)
+        for k in ("dx", "ddelta", "dz"):
+            if g[k] is not None:
+                g[k][:, :, d] = gd[k][:, :, 0]
+        g["dA"][d] = gd["dA"][0]
+        g["dB"][:, :, d] = gd["dB"]
+        g["dC"][:, :, d] = gd["dC"]
+        for k in ("dD", "ddelta_bias"):
+            if g[k] is not None:
+                g[k][d] = gd[k][0]
+        g["dh0"][:, d] = gd["dh0"][:, 0]
+    return g
+
+
+Oracle.selective_scan_bcd_bwd = _bcd_bwd_method
 
 
 def default() -> Oracle:
@@ -283,6 +333,10 @@ def silu(z):
 
 def phi(z):
     return default().phi(z)
+
+
+def phi_prime(z):
+    return default().phi_prime(z)
 
 
 def recurrence(*a, **k):
@@ -307,3 +361,7 @@ def selective_scan_bwd(*a, **k):
 
 def selective_scan_bcd(*a, **k):
     return default().selective_scan_bcd(*a, **k)
+
+
+def selective_scan_bcd_bwd(*a, **k):
+    return default().selective_scan_bcd_bwd(*a, **k)

@@ -61,6 +61,28 @@ double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
 double oracle_phi(double z) { return z == 0.0 ? 1.0 : expm1(z) / z; }
 
 /*
+ * phi'(z), the derivative of phi, needed by the gradient of the zero-order-hold
+ * Bbar with respect to A. Since phi(z) = integral_0^1 e^{zs} ds,
+ *   phi'(z) = integral_0^1 s e^{zs} ds = sum_{k>=0} z^k / (k! (k + 2))
+ *           = (e^z (z - 1) + 1) / z^2                     (z != 0),
+ * with phi'(0) = 1/2. The closed form cancels badly for small |z|, so the
+ * series (terms below 1e-19 after k = 20 when |z| <= 1) is summed there and the
+ * closed form used elsewhere.
+ */
+double oracle_phi_prime(double z)
+{
+    if (fabs(z) <= 1.0) {
+        double term = 1.0, sum = 0.0;   /* term = z^k / k! */
+        for (int k = 0; k <= 24; ++k) {
+            sum += term / (k + 2);
+            term *= z / (k + 1);
+        }
+        return sum;
+    }
+    return (exp(z) * (z - 1.0) + 1.0) / (z * z);
+}
+
+/*
  * The recurrence with the discretized parameters given directly, one channel:
  *   h[n] <- Abar[t,n] * h[n] + Bbar[t,n] * x[t]
  *   y[t]  = sum_n C[t,n] * h[n]           (h after the update)
@@ -319,6 +341,14 @@ void oracle_causal_conv1d_silu(int64_t batch, int64_t L, int64_t dim, int64_t K,
  * dbias sum over batch rows and tokens. Optional outputs may be NULL; dD, dz,
  * dbias are only defined when D, z, delta_bias were given.
  *
+ * With the exact zero-order hold (oracle_selective_scan_bwd_zoh) the input term
+ * is dt phi(dt A[n]) B[n] x = (e^{dt A[n]} - 1)/A[n] B[n] x; its derivative in
+ * dt is a[n] B[n] x (phi(z) + z phi'(z) = e^z) and in A[n] is
+ * dt^2 phi'(dt A[n]) B[n] x, so with p[n] = phi(dt A[n]):
+ *   dB[n] += G[n] dt p[n] x    dx = dy D + dt sum_n G[n] p[n] B[n]
+ *   ddt    = sum_n G[n] (a[n] x B[n] + A[n] a[n] hp[n])
+ *   dA[n] += G[n] (dt a[n] hp[n] + dt^2 phi'(dt A[n]) B[n] x)
+ *
  * Channels are split across threads; each thread sums its own dA, dD, dbias,
  * dB and dC and the partial sums are added in thread order (deterministic for a
  * given thread count). Returns 0, or -1 on bad arguments / allocation failure.
@@ -327,6 +357,7 @@ typedef struct {
     int64_t batch, L, dim, N;
     const double *x, *delta, *A, *B, *C, *D, *z, *delta_bias, *h0, *dout, *dh_final;
     int delta_softplus;
+    int zoh;                                      /* exact zero-order-hold Bbar */
     double *dx, *ddelta, *dz, *dh0;               /* per channel: written directly */
     double *dA, *dB, *dC, *dD, *dbias;            /* this thread's partial sums */
     int64_t chan_begin, chan_end;
@@ -355,7 +386,8 @@ static void bwd_channel(bwd_job* j, int64_t b, int64_t d, double* hp, double* dt
         double acc = 0.0;
         for (int64_t n = 0; n < N; ++n) {
             hp[t * N + n] = h[n];
-            h[n] = exp(dt * Ad[n]) * h[n] + dt * Bt[n] * j->x[e];
+            const double p = j->zoh ? oracle_phi(dt * Ad[n]) : 1.0;
+            h[n] = exp(dt * Ad[n]) * h[n] + dt * p * Bt[n] * j->x[e];
             acc += Ct[n] * h[n];
         }
         yv[t] = acc + (j->D ? j->D[d] * j->x[e] : 0.0);
@@ -378,14 +410,17 @@ static void bwd_channel(bwd_job* j, int64_t b, int64_t d, double* hp, double* dt
         double ddt = 0.0;
         for (int64_t n = 0; n < N; ++n) {
             const double a = exp(dt * Ad[n]);
+            const double p = j->zoh ? oracle_phi(dt * Ad[n]) : 1.0;   /* Bbar = dt p B */
             const double hprev = hp[t * N + n];
-            const double ht = a * hprev + dt * Bt[n] * xv;
+            const double ht = a * hprev + dt * p * Bt[n] * xv;
             const double g = G[n] + dy * Ct[n];           /* dLoss/dh_t */
             j->dC[(b * L + t) * N + n] += dy * ht;
-            j->dB[(b * L + t) * N + n] += g * dt * xv;
-            dx += g * dt * Bt[n];
-            ddt += g * (xv * Bt[n] + Ad[n] * a * hprev);
-            j->dA[d * N + n] += g * dt * a * hprev;
+            j->dB[(b * L + t) * N + n] += g * dt * p * xv;
+            dx += g * dt * p * Bt[n];
+            ddt += g * ((j->zoh ? a : 1.0) * xv * Bt[n] + Ad[n] * a * hprev);
+            j->dA[d * N + n] += g * (dt * a * hprev
+                                     + (j->zoh ? dt * dt * oracle_phi_prime(dt * Ad[n]) * Bt[n] * xv
+                                               : 0.0));
             G[n] = a * g;                                  /* carried to the token before */
         }
         const double dd = j->delta_softplus ? ddt * oracle_sigmoid(j->delta[e] + bias) : ddt;
@@ -412,6 +447,14 @@ static void* bwd_worker(void* arg)
     return NULL;
 }
 
+static int bwd_run(int64_t batch, int64_t L, int64_t dim, int64_t N, const double* x,
+                   const double* delta, const double* A, const double* B, const double* C,
+                   const double* D, const double* z, const double* delta_bias,
+                   int delta_softplus, int zoh, const double* h0, const double* dout,
+                   const double* dh_final, double* dx, double* ddelta, double* dA, double* dB,
+                   double* dC, double* dD, double* dz, double* ddelta_bias, double* dh0,
+                   int nthreads);
+
 int oracle_selective_scan_bwd(int64_t batch, int64_t L, int64_t dim, int64_t N,
                               const double* x, const double* delta, const double* A,
                               const double* B, const double* C, const double* D,
@@ -420,6 +463,32 @@ int oracle_selective_scan_bwd(int64_t batch, int64_t L, int64_t dim, int64_t N,
                               double* dx, double* ddelta, double* dA, double* dB, double* dC,
                               double* dD, double* dz, double* ddelta_bias, double* dh0,
                               int nthreads)
+{
+    return bwd_run(batch, L, dim, N, x, delta, A, B, C, D, z, delta_bias, delta_softplus, 0, h0,
+                   dout, dh_final, dx, ddelta, dA, dB, dC, dD, dz, ddelta_bias, dh0, nthreads);
+}
+
+/* The gradients of the scan with the exact zero-order-hold Bbar. */
+int oracle_selective_scan_bwd_zoh(int64_t batch, int64_t L, int64_t dim, int64_t N,
+                                  const double* x, const double* delta, const double* A,
+                                  const double* B, const double* C, const double* D,
+                                  const double* z, const double* delta_bias, int delta_softplus,
+                                  const double* h0, const double* dout, const double* dh_final,
+                                  double* dx, double* ddelta, double* dA, double* dB, double* dC,
+                                  double* dD, double* dz, double* ddelta_bias, double* dh0,
+                                  int nthreads)
+{
+    return bwd_run(batch, L, dim, N, x, delta, A, B, C, D, z, delta_bias, delta_softplus, 1, h0,
+                   dout, dh_final, dx, ddelta, dA, dB, dC, dD, dz, ddelta_bias, dh0, nthreads);
+}
+
+static int bwd_run(int64_t batch, int64_t L, int64_t dim, int64_t N, const double* x,
+                   const double* delta, const double* A, const double* B, const double* C,
+                   const double* D, const double* z, const double* delta_bias,
+                   int delta_softplus, int zoh, const double* h0, const double* dout,
+                   const double* dh_final, double* dx, double* ddelta, double* dA, double* dB,
+                   double* dC, double* dD, double* dz, double* ddelta_bias, double* dh0,
+                   int nthreads)
 {
     if (batch < 0 || L < 0 || dim < 0 || N <= 0) return -1;
     if (!x || !delta || !A || !B || !C || !dout) return -1;
@@ -440,6 +509,7 @@ int oracle_selective_scan_bwd(int64_t batch, int64_t L, int64_t dim, int64_t N,
         j->x = x; j->delta = delta; j->A = A; j->B = B; j->C = C; j->D = D; j->z = z;
         j->delta_bias = delta_bias; j->h0 = h0; j->dout = dout; j->dh_final = dh_final;
         j->delta_softplus = delta_softplus;
+        j->zoh = zoh;
         j->dx = dx; j->ddelta = ddelta; j->dz = dz; j->dh0 = dh0;
         double* p = part + (size_t)i * per;
         j->dA = p; j->dB = p + nA; j->dC = p + nA + nBC; j->dD = p + nA + 2 * nBC;

@@ -452,8 +452,10 @@ def pin_bwd_finite_differences(orc, seed=31):
                 assert g[_GRAD_OF[name]] is None
 
 
-def _torch_scan(x, delta, A, B, C, D, z, bias, softplus, h0):
-    """The scan as a plain PyTorch float64 loop (autograd records it)."""
+def _torch_scan(x, delta, A, B, C, D, z, bias, softplus, h0, zoh=False):
+    """The scan as a plain PyTorch float64 loop (autograd records it). B, C of
+    shape [batch, L, dim, N] are per channel; zoh=True takes the input term
+    (e^{dt A} - 1)/A B x of the exact zero-order hold (A must be nonzero)."""
     import torch
     batch, L, dim = x.shape
     N = A.shape[1]
@@ -462,8 +464,11 @@ def _torch_scan(x, delta, A, B, C, D, z, bias, softplus, h0):
     for t in range(L):
         v = delta[:, t] + (bias if bias is not None else 0.0)
         dt = torch.nn.functional.softplus(v) if softplus else v
-        h = torch.exp(dt[..., None] * A) * h + (dt * x[:, t])[..., None] * B[:, t, None, :]
-        y = (h * C[:, t, None, :]).sum(-1)
+        Bt = B[:, t] if B.dim() == 4 else B[:, t, None, :]
+        Ct = C[:, t] if C.dim() == 4 else C[:, t, None, :]
+        step = torch.expm1(dt[..., None] * A) / A if zoh else dt[..., None]
+        h = torch.exp(dt[..., None] * A) * h + step * x[:, t, :, None] * Bt
+        y = (h * Ct).sum(-1)
         if D is not None:
             y = y + D * x[:, t]
         if z is not None:
@@ -646,7 +651,129 @@ def pin_bc_per_channel(orc, seed=45):
     assert np.array_equal(o1, o2) and np.array_equal(f1, f2), "shared rows = shared B, C"
 
 
+
+# --------------------------------------------------------------------------
+# gradients of the variants (exact zero-order hold, per-channel B, C)
+# --------------------------------------------------------------------------
+def pin_phi_prime(orc):
+    """phi'(z) = integral_0^1 s e^{zs} ds, since phi(z) is the mean of e^{zs}
+    over s in [0, 1]: 1/2 at 0; adaptive quadrature on both sides of |z| = 1
+    (where the oracle switches from its series to the closed form); and the
+    central difference of numpy's expm1(z)/z."""
+    from scipy.integrate import quad
+    assert orc.phi_prime(0.0) == 0.5
+    for zz in (-30.0, -4.0, -1.2, -1.0, -0.999, -0.3, -1e-4, 1e-6, 0.5, 1.0, 1.001, 3.0):
+        val, _ = quad(lambda sv: sv * np.exp(zz * sv), 0.0, 1.0, epsabs=0.0, epsrel=1e-13)
+        _close(orc.phi_prime(zz), val, 1e-12, 0.0, "phi' at %g vs quadrature" % zz)
+    for zz in (-2.5, -0.7, 0.4):
+        hh = 1e-5
+        fd = (np.expm1(zz + hh) / (zz + hh) - np.expm1(zz - hh) / (zz - hh)) / (2 * hh)
+        _close(orc.phi_prime(zz), fd, 1e-8, 0.0, "phi' at %g vs central difference" % zz)
+
+
+def _variant_case(r, shape, softplus, full, per_channel):
+    c, dout, dhf = _bwd_case(r, *shape, softplus, full)
+    if per_channel:
+        batch, L, dim, N = shape
+        c["B"] = r.standard_normal((batch, L, dim, N))
+        c["C"] = r.standard_normal((batch, L, dim, N))
+    return c, dout, dhf
+
+
+def _variant_grads(orc, c, dout, dhf, softplus, zoh, per_channel):
+    fn = orc.selective_scan_bcd_bwd if per_channel else orc.selective_scan_bwd
+    return fn(c["x"], c["delta"], c["A"], c["B"], c["C"], dout, D=c["D"], z=c["z"],
+              delta_bias=c["delta_bias"], delta_softplus=softplus, h0=c["h0"], dh_final=dhf,
+              zoh=zoh)
+
+
+def pin_bwd_variants_finite_differences(orc, seed=51):
+    """The gradients of the zero-order-hold scan and of the per-channel B, C scan
+    equal the central differences of the oracle's own forward of that variant
+    (itself pinned to the ODE and to the unrolled sum)."""
+    r = _rng(seed)
+    for zoh, per_channel, softplus, full, shape in ((True, False, True, True, (2, 4, 2, 3)),
+                                                    (True, False, False, False, (1, 5, 2, 2)),
+                                                    (False, True, True, True, (1, 4, 3, 2)),
+                                                    (True, True, True, True, (1, 3, 2, 3))):
+        c, dout, dhf = _variant_case(r, shape, softplus, full, per_channel)
+        g = _variant_grads(orc, c, dout, dhf, softplus, zoh, per_channel)
+        fwd = orc.selective_scan_bcd if per_channel else orc.selective_scan
+
+        def loss(**kw):
+            a = dict(c)
+            a.update(kw)
+            out, fs = fwd(a["x"], a["delta"], a["A"], a["B"], a["C"], D=a["D"], z=a["z"],
+                          delta_bias=a["delta_bias"], delta_softplus=softplus, h0=a["h0"],
+                          zoh=zoh)
+            return float((out * dout).sum() + (0.0 if dhf is None else (fs * dhf).sum()))
+
+        eps = 1e-6
+        for name, arr in c.items():
+            if arr is None:
+                continue
+            fd = np.zeros_like(arr)
+            for i in np.ndindex(arr.shape):
+                p, m = arr.copy(), arr.copy()
+                p[i] += eps
+                m[i] -= eps
+                fd[i] = (loss(**{name: p}) - loss(**{name: m})) / (2 * eps)
+            _close(g[_GRAD_OF[name]], fd, 1e-6, 1e-7,
+                   "d%s vs finite differences (zoh=%s, per-channel=%s)" % (name, zoh, per_channel))
+
+
+def pin_bwd_variants_autograd(orc, seed=52):
+    """The gradients of both variants equal PyTorch autograd through a plain
+    float64 loop (the zero-order hold written with torch.expm1)."""
+    import torch
+    r = _rng(seed)
+    for zoh, per_channel, softplus, full, shape in ((True, False, True, True, (2, 7, 3, 4)),
+                                                    (True, False, False, True, (1, 6, 2, 5)),
+                                                    (False, True, True, True, (2, 6, 3, 4)),
+                                                    (True, True, False, False, (1, 5, 2, 3))):
+        c, dout, dhf = _variant_case(r, shape, softplus, full, per_channel)
+        tens = {k: (None if v is None else torch.tensor(v, requires_grad=True))
+                for k, v in c.items()}
+        out, fs = _torch_scan(tens["x"], tens["delta"], tens["A"], tens["B"], tens["C"],
+                              tens["D"], tens["z"], tens["delta_bias"], softplus, tens["h0"],
+                              zoh=zoh)
+        loss = (out * torch.tensor(dout)).sum()
+        if dhf is not None:
+            loss = loss + (fs * torch.tensor(dhf)).sum()
+        loss.backward()
+        g = _variant_grads(orc, c, dout, dhf, softplus, zoh, per_channel)
+        for name, t in tens.items():
+            if t is not None:
+                _close(g[_GRAD_OF[name]], t.grad.numpy(), 1e-10, 1e-12,
+                       "d%s vs autograd (zoh=%s, per-channel=%s)" % (name, zoh, per_channel))
+
+
+def pin_bwd_per_channel_shared_rows(orc, seed=53):
+    """Per-channel rows that repeat the shared B, C rows give the shared scan's
+    gradients: dB, dC summed over channels equal the shared dB, dC, and every
+    other gradient is unchanged (with and without the zero-order hold)."""
+    r = _rng(seed)
+    for zoh in (False, True):
+        c, dout, dhf = _bwd_case(r, 2, 6, 3, 4, True, True)
+        g = orc.selective_scan_bwd(c["x"], c["delta"], c["A"], c["B"], c["C"], dout, D=c["D"],
+                                   z=c["z"], delta_bias=c["delta_bias"], delta_softplus=True,
+                                   h0=c["h0"], dh_final=dhf, zoh=zoh)
+        B4 = np.repeat(c["B"][:, :, None, :], 3, 2)
+        C4 = np.repeat(c["C"][:, :, None, :], 3, 2)
+        g4 = orc.selective_scan_bcd_bwd(c["x"], c["delta"], c["A"], B4, C4, dout, D=c["D"],
+                                        z=c["z"], delta_bias=c["delta_bias"],
+                                        delta_softplus=True, h0=c["h0"], dh_final=dhf, zoh=zoh)
+        _close(g4["dB"].sum(2), g["dB"], 1e-12, 1e-13, "per-channel dB summed (zoh=%s)" % zoh)
+        _close(g4["dC"].sum(2), g["dC"], 1e-12, 1e-13, "per-channel dC summed (zoh=%s)" % zoh)
+        for k in ("dx", "ddelta", "dz", "dA", "dD", "ddelta_bias", "dh0"):
+            _close(g4[k], g[k], 1e-12, 1e-13, "%s per-channel vs shared (zoh=%s)" % (k, zoh))
+
+
 ALL_PINS = [
+    pin_phi_prime,
+    pin_bwd_variants_finite_differences,
+    pin_bwd_variants_autograd,
+    pin_bwd_per_channel_shared_rows,
     pin_bc_per_channel,
     pin_phi,
     pin_zoh_closed_form,

@@ -60,19 +60,32 @@ MUTANTS = [
     ("bwd_dC_reads_state_before_update", "j->dC[(b * L + t) * N + n] += dy * ht;",
      "j->dC[(b * L + t) * N + n] += dy * hprev;"),
     ("bwd_carry_drops_decay", "G[n] = a * g;", "G[n] = g;"),
-    ("bwd_ddt_drops_input_term", "ddt += g * (xv * Bt[n] + Ad[n] * a * hprev);",
+    ("bwd_ddt_drops_input_term", "ddt += g * ((j->zoh ? a : 1.0) * xv * Bt[n] + Ad[n] * a * hprev);",
      "ddt += g * (Ad[n] * a * hprev);"),
     ("bwd_softplus_derivative_missing",
      "const double dd = j->delta_softplus ? ddt * oracle_sigmoid(j->delta[e] + bias) : ddt;",
      "const double dd = ddt;"),
     ("bwd_silu_derivative_wrong", "s * (1.0 + j->z[e] * (1.0 - s))", "s"),
-    ("bwd_dA_missing_dt", "j->dA[d * N + n] += g * dt * a * hprev;",
-     "j->dA[d * N + n] += g * a * hprev;"),
+    ("bwd_dA_missing_dt", "j->dA[d * N + n] += g * (dt * a * hprev",
+     "j->dA[d * N + n] += g * (a * hprev"),
     ("bwd_dx_drops_D", "double dx = j->D ? dy * j->D[d] : 0.0;", "double dx = 0.0;"),
-    ("bwd_dB_drops_x", "j->dB[(b * L + t) * N + n] += g * dt * xv;",
-     "j->dB[(b * L + t) * N + n] += g * dt;"),
+    ("bwd_dB_drops_x", "j->dB[(b * L + t) * N + n] += g * dt * p * xv;",
+     "j->dB[(b * L + t) * N + n] += g * dt * p;"),
     ("bwd_dh0_one_step_late", "j->dh0[(b * dim + d) * N + n] = G[n];",
      "j->dh0[(b * dim + d) * N + n] = G[n] / exp(dtv[0] * Ad[n]);"),
+    ("phi_prime_series_wrong_denominator", "sum += term / (k + 2);", "sum += term / (k + 1);"),
+    ("phi_prime_closed_form_wrong_sign", "(exp(z) * (z - 1.0) + 1.0)", "(exp(z) * (z + 1.0) - 1.0)"),
+    ("bwd_zoh_recompute_first_order",
+     "const double p = j->zoh ? oracle_phi(dt * Ad[n]) : 1.0;\n            h[n] =",
+     "const double p = 1.0;\n            h[n] ="),
+    ("bwd_zoh_dB_drops_phi", "j->dB[(b * L + t) * N + n] += g * dt * p * xv;",
+     "j->dB[(b * L + t) * N + n] += g * dt * xv;"),
+    ("bwd_zoh_dx_drops_phi", "dx += g * dt * p * Bt[n];", "dx += g * dt * Bt[n];"),
+    ("bwd_zoh_ddt_first_order_input_term", "(j->zoh ? a : 1.0) * xv * Bt[n]", "xv * Bt[n]"),
+    ("bwd_zoh_dA_drops_hold_term", "(j->zoh ? dt * dt * oracle_phi_prime(dt * Ad[n])",
+     "(0 ? dt * dt * oracle_phi_prime(dt * Ad[n])"),
+    ("bwd_zoh_dA_hold_term_one_dt", "dt * dt * oracle_phi_prime(dt * Ad[n])",
+     "dt * oracle_phi_prime(dt * Ad[n])"),
 ]
 
 
