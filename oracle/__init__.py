@@ -77,6 +77,8 @@ def _bind(lib):
         getattr(lib, name).argtypes = [ctypes.c_double]
     lib.oracle_causal_conv1d_silu.restype = None
     lib.oracle_causal_conv1d_silu.argtypes = [_i64] * 4 + [_dp] * 4
+    lib.oracle_causal_conv1d_silu_bwd.restype = None
+    lib.oracle_causal_conv1d_silu_bwd.argtypes = [_i64] * 4 + [_dp] * 7
     for name in ("oracle_selective_scan_bwd", "oracle_selective_scan_bwd_zoh"):
         getattr(lib, name).restype = ctypes.c_int
         getattr(lib, name).argtypes = (
@@ -202,6 +204,47 @@ def _conv_method(self, x, w, bias=None):
 
 
 Oracle.causal_conv1d_silu = _conv_method
+
+
+def _conv_bwd_method(self, x, w, du, bias=None):
+    """Gradients of the input stage for dLoss/du = du [batch, L, dim]. Returns a
+    dict of float64 arrays: dx [batch, L, dim], dw [dim, K], dbias [dim] (the
+    gradient at zero when bias is None)."""
+    x = _f64(x)
+    batch, L, dim = x.shape
+    w = _f64(w)
+    K = w.shape[1]
+    w = _f64(w, (dim, K))
+    bias = _f64(bias, (dim,))
+    du = _f64(du, (batch, L, dim))
+    g = {"dx": np.zeros((batch, L, dim)), "dw": np.zeros((dim, K)), "dbias": np.zeros(dim)}
+    self._lib.oracle_causal_conv1d_silu_bwd(batch, L, dim, K, _ptr(x), _ptr(w), _ptr(bias),
+                                            _ptr(du), _ptr(g["dx"]), _ptr(g["dw"]),
+                                            _ptr(g["dbias"]))
+    return g
+
+
+Oracle.causal_conv1d_silu_bwd = _conv_bwd_method
+
+
+def _conv_scan_bwd_method(self, x, delta, A, B, C, conv_w, dout, conv_bias=None, D=None, z=None,
+                          delta_bias=None, delta_softplus=False, h0=None, dh_final=None,
+                          nthreads=None):
+    """Gradients of the input stage followed by the scan (the scan reads
+    u = silu(conv(x)) where it would read x, the D skip included): the scan's
+    gradients at x = u, then dx, dconv_w, dconv_bias from the input stage's
+    backward fed du = the scan's dx. Returns the dict of selective_scan_bwd
+    (dx now the gradient of the stage's input) plus dconv_w, dconv_bias."""
+    u = self.causal_conv1d_silu(x, conv_w, conv_bias)
+    g = self.selective_scan_bwd(u, delta, A, B, C, dout, D=D, z=z, delta_bias=delta_bias,
+                                delta_softplus=delta_softplus, h0=h0, dh_final=dh_final,
+                                nthreads=nthreads)
+    gc = self.causal_conv1d_silu_bwd(x, conv_w, g["dx"], bias=conv_bias)
+    g["dx"], g["dconv_w"], g["dconv_bias"] = gc["dx"], gc["dw"], gc["dbias"]
+    return g
+
+
+Oracle.selective_scan_conv_bwd = _conv_scan_bwd_method
 
 
 def _bwd_method(self, x, delta, A, B, C, dout, D=None, z=None, delta_bias=None,
@@ -353,6 +396,14 @@ def state_update(*a, **k):
 
 def causal_conv1d_silu(*a, **k):
     return default().causal_conv1d_silu(*a, **k)
+
+
+def causal_conv1d_silu_bwd(*a, **k):
+    return default().causal_conv1d_silu_bwd(*a, **k)
+
+
+def selective_scan_conv_bwd(*a, **k):
+    return default().selective_scan_conv_bwd(*a, **k)
 
 
 def selective_scan_bwd(*a, **k):

@@ -318,6 +318,43 @@ void oracle_causal_conv1d_silu(int64_t batch, int64_t L, int64_t dim, int64_t K,
 }
 
 /*
+ * Gradients of the input stage above for a loss with dLoss/du = du (the chain
+ * rule on its loop, in the same order). With s(p) = 1 / (1 + e^-p) and
+ * silu'(p) = s(p) (1 + p (1 - s(p))):
+ *   dpre[t]      = du[t] silu'(pre[t])
+ *   dx[t-(K-1)+k] += dpre[t] w[d,k]        (the taps that read that token)
+ *   dw[d,k]      += dpre[t] x[t-(K-1)+k]   (over batch rows and tokens)
+ *   dbias[d]     += dpre[t]
+ * Outputs are overwritten; dw and dbias may be NULL. Layouts as the forward.
+ */
+void oracle_causal_conv1d_silu_bwd(int64_t batch, int64_t L, int64_t dim, int64_t K,
+                                   const double* x, const double* w, const double* bias,
+                                   const double* du, double* dx, double* dw, double* dbias)
+{
+    for (int64_t i = 0; i < batch * L * dim; ++i) dx[i] = 0.0;
+    if (dw) for (int64_t i = 0; i < dim * K; ++i) dw[i] = 0.0;
+    if (dbias) for (int64_t i = 0; i < dim; ++i) dbias[i] = 0.0;
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t t = 0; t < L; ++t)
+            for (int64_t d = 0; d < dim; ++d) {
+                double pre = bias ? bias[d] : 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    const int64_t s = t - (K - 1) + k;
+                    if (s >= 0) pre += w[d * K + k] * x[(b * L + s) * dim + d];
+                }
+                const double sg = 1.0 / (1.0 + exp(-pre));
+                const double dpre = du[(b * L + t) * dim + d] * sg * (1.0 + pre * (1.0 - sg));
+                for (int64_t k = 0; k < K; ++k) {
+                    const int64_t s = t - (K - 1) + k;
+                    if (s < 0) continue;
+                    dx[(b * L + s) * dim + d] += dpre * w[d * K + k];
+                    if (dw) dw[d * K + k] += dpre * x[(b * L + s) * dim + d];
+                }
+                if (dbias) dbias[d] += dpre;
+            }
+}
+
+/*
  * Gradients of the selective scan (the reverse-mode derivative of
  * oracle_selective_scan, from the chain rule on its loop; the pages ask that
  * gradients flow through the discretization: "State Space Models -- Mamba, S4,

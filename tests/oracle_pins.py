@@ -393,6 +393,72 @@ def pin_conv_causal(orc, seed=23):
     assert np.all(moved[0, 12:16] != base[0, 12:16]), "conv misses a tap"
 
 
+def _torch_conv_silu(x, w, bias):
+    """The input stage with PyTorch's own depthwise conv1d: [batch, L, dim] in,
+    left padding K - 1 on both sides cut back to the first L outputs."""
+    import torch
+    K = w.shape[1]
+    pre = torch.nn.functional.conv1d(x.transpose(1, 2), w[:, None, :], bias=bias, padding=K - 1,
+                                     groups=w.shape[0])[:, :, :x.shape[1]]
+    return torch.nn.functional.silu(pre).transpose(1, 2)
+
+
+def pin_conv_bwd(orc, seed=24):
+    """The input stage's gradients (dx, dw, dbias) equal central differences of
+    the oracle's own forward and PyTorch autograd through
+    torch.nn.functional.conv1d, for K = 1..4, with and without a bias."""
+    import torch
+    r = _rng(seed)
+    for K in (1, 2, 3, 4):
+        x, w, bias = _conv_case(r, K, batch=2, L=9, dim=3)
+        du = r.standard_normal(x.shape)
+        for b_ in (bias, None):
+            g = orc.causal_conv1d_silu_bwd(x, w, du, bias=b_)
+            tx, tw = torch.tensor(x, requires_grad=True), torch.tensor(w, requires_grad=True)
+            tb = torch.tensor(b_ if b_ is not None else np.zeros(3), requires_grad=True)
+            (_torch_conv_silu(tx, tw, tb) * torch.tensor(du)).sum().backward()
+            for name, t in (("dx", tx), ("dw", tw), ("dbias", tb)):
+                _close(g[name], t.grad.numpy(), 1e-12, 1e-13, "conv %s vs autograd, K=%d" % (name, K))
+        eps = 1e-6
+        for name, arr in (("x", x), ("w", w), ("bias", bias)):
+            fd = np.zeros_like(arr)
+            for i in np.ndindex(arr.shape):
+                p, m = arr.copy(), arr.copy()
+                p[i] += eps
+                m[i] -= eps
+                a = {"x": x, "w": w, "bias": bias}
+                lp = (orc.causal_conv1d_silu(**dict(a, **{name: p})) * du).sum()
+                lm = (orc.causal_conv1d_silu(**dict(a, **{name: m})) * du).sum()
+                fd[i] = (lp - lm) / (2 * eps)
+            g = orc.causal_conv1d_silu_bwd(x, w, du, bias=bias)
+            _close(g["d" + name], fd, 1e-6, 1e-7, "conv d%s vs finite differences, K=%d" % (name, K))
+
+
+def pin_conv_scan_bwd(orc, seed=25):
+    """The input stage followed by the scan: every gradient, the conv's weights
+    and bias included, equals PyTorch autograd through conv1d + SiLU and the
+    plain float64 loop of the scan."""
+    import torch
+    r = _rng(seed)
+    c, dout, dhf = _bwd_case(r, 2, 8, 3, 4, True, True)
+    w = r.standard_normal((3, 4)) * 0.5
+    cb = r.standard_normal(3) * 0.2
+    g = orc.selective_scan_conv_bwd(c["x"], c["delta"], c["A"], c["B"], c["C"], w, dout,
+                                    conv_bias=cb, D=c["D"], z=c["z"],
+                                    delta_bias=c["delta_bias"], delta_softplus=True, h0=c["h0"],
+                                    dh_final=dhf)
+    tens = {k: torch.tensor(v, requires_grad=True) for k, v in c.items()}
+    tw, tcb = torch.tensor(w, requires_grad=True), torch.tensor(cb, requires_grad=True)
+    u = _torch_conv_silu(tens["x"], tw, tcb)
+    out, fs = _torch_scan(u, tens["delta"], tens["A"], tens["B"], tens["C"], tens["D"],
+                          tens["z"], tens["delta_bias"], True, tens["h0"])
+    ((out * torch.tensor(dout)).sum() + (fs * torch.tensor(dhf)).sum()).backward()
+    for name, t in tens.items():
+        _close(g[_GRAD_OF[name]], t.grad.numpy(), 1e-10, 1e-12, "conv+scan d%s vs autograd" % name)
+    _close(g["dconv_w"], tw.grad.numpy(), 1e-10, 1e-12, "conv+scan dconv_w vs autograd")
+    _close(g["dconv_bias"], tcb.grad.numpy(), 1e-10, 1e-12, "conv+scan dconv_bias vs autograd")
+
+
 # --------------------------------------------------------------------------
 # gradients (the backward of the scan)
 # --------------------------------------------------------------------------
@@ -770,6 +836,8 @@ def pin_bwd_per_channel_shared_rows(orc, seed=53):
 
 
 ALL_PINS = [
+    pin_conv_bwd,
+    pin_conv_scan_bwd,
     pin_phi_prime,
     pin_bwd_variants_finite_differences,
     pin_bwd_variants_autograd,

@@ -16,6 +16,14 @@ import oracle_pins
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                    "oracle", "ssm_oracle.c")
 
+# the input stage's forward loop body
+CONV_FWD = ("double pre = bias ? bias[d] : 0.0;\n"
+            "                for (int64_t k = 0; k < K; ++k) {\n"
+            "                    const int64_t s = t - (K - 1) + k;\n"
+            "                    if (s >= 0) pre += w[d * K + k] * x[(b * L + s) * dim + d];\n"
+            "                }\n"
+            "                u[(b * L + t) * dim + d] = oracle_silu(pre);")
+
 # (name, text in the oracle source, replacement)
 MUTANTS = [
     ("drop_D_skip", "if (j->D) y += j->D[d] * xv;", ""),
@@ -46,10 +54,10 @@ MUTANTS = [
     ("core_recurrence_drops_state", "h[n] = Abar[t * N + n] * h[n] + Bbar[t * N + n] * x[t];",
      "h[n] = Abar[t * N + n] + Bbar[t * N + n] * x[t];"),
     ("core_readout_drops_C", "acc += C[t * N + n] * h[n];", "acc += h[n];"),
-    ("conv_kernel_flipped", "pre += w[d * K + k] * x[(b * L + s) * dim + d];",
-     "pre += w[d * K + (K - 1 - k)] * x[(b * L + s) * dim + d];"),
-    ("conv_shift_off_by_one", "const int64_t s = t - (K - 1) + k;", "const int64_t s = t - K + k;"),
-    ("conv_drops_bias", "double pre = bias ? bias[d] : 0.0;", "double pre = 0.0;"),
+    # the forward's window (the backward recomputes the same pre-activation)
+    ("conv_kernel_flipped", CONV_FWD, CONV_FWD.replace("w[d * K + k]", "w[d * K + (K - 1 - k)]")),
+    ("conv_shift_off_by_one", CONV_FWD, CONV_FWD.replace("t - (K - 1) + k", "t - K + k")),
+    ("conv_drops_bias", CONV_FWD, CONV_FWD.replace("bias ? bias[d] : 0.0", "0.0")),
     ("conv_without_silu", "u[(b * L + t) * dim + d] = oracle_silu(pre);",
      "u[(b * L + t) * dim + d] = pre;"),
     ("zoh_phi_drops_division", "return z == 0.0 ? 1.0 : expm1(z) / z;",
@@ -86,6 +94,16 @@ MUTANTS = [
      "(0 ? dt * dt * oracle_phi_prime(dt * Ad[n])"),
     ("bwd_zoh_dA_hold_term_one_dt", "dt * dt * oracle_phi_prime(dt * Ad[n])",
      "dt * oracle_phi_prime(dt * Ad[n])"),
+    ("conv_bwd_sigmoid_not_silu_derivative", "du[(b * L + t) * dim + d] * sg * (1.0 + pre * (1.0 - sg))",
+     "du[(b * L + t) * dim + d] * sg"),
+    ("conv_bwd_dx_flipped_taps", "dx[(b * L + s) * dim + d] += dpre * w[d * K + k];",
+     "dx[(b * L + s) * dim + d] += dpre * w[d * K + (K - 1 - k)];"),
+    ("conv_bwd_dw_reads_current_token", "if (dw) dw[d * K + k] += dpre * x[(b * L + s) * dim + d];",
+     "if (dw) dw[d * K + k] += dpre * x[(b * L + t) * dim + d];"),
+    ("conv_bwd_drops_bias_in_pre", "double pre = bias ? bias[d] : 0.0;\n                for (int64_t k = 0; k < K; ++k) {\n                    const int64_t s = t - (K - 1) + k;\n                    if (s >= 0) pre += w[d * K + k] * x[(b * L + s) * dim + d];\n                }\n                const double sg",
+     "double pre = 0.0;\n                for (int64_t k = 0; k < K; ++k) {\n                    const int64_t s = t - (K - 1) + k;\n                    if (s >= 0) pre += w[d * K + k] * x[(b * L + s) * dim + d];\n                }\n                const double sg"),
+    ("conv_bwd_dbias_drops_derivative", "if (dbias) dbias[d] += dpre;",
+     "if (dbias) dbias[d] += du[(b * L + t) * dim + d];"),
 ]
 
 
