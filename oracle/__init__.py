@@ -77,6 +77,8 @@ def _bind(lib):
         getattr(lib, name).argtypes = [ctypes.c_double]
     lib.oracle_causal_conv1d_silu.restype = None
     lib.oracle_causal_conv1d_silu.argtypes = [_i64] * 4 + [_dp] * 4
+    lib.oracle_ssd.restype = ctypes.c_int
+    lib.oracle_ssd.argtypes = [_i64] * 6 + [_dp] * 7 + [ctypes.c_int] + [_dp] * 3 + [ctypes.c_int]
     lib.oracle_causal_conv1d_silu_bwd.restype = None
     lib.oracle_causal_conv1d_silu_bwd.argtypes = [_i64] * 4 + [_dp] * 7
     for name in ("oracle_selective_scan_bwd", "oracle_selective_scan_bwd_zoh"):
@@ -225,6 +227,32 @@ def _conv_bwd_method(self, x, w, du, bias=None):
 
 
 Oracle.causal_conv1d_silu_bwd = _conv_bwd_method
+
+
+def _ssd_method(self, x, dt, A, B, C, D=None, dt_bias=None, dt_softplus=False, h0=None,
+                nthreads=None):
+    """Mamba-2's SSD layer: x [batch, L, H, P]; dt [batch, L, H]; A, D, dt_bias
+    [H]; B, C [batch, L, G, N] (head hd reads group hd // (H // G)); h0
+    [batch, H, P, N]. Returns (y [batch, L, H, P], final_state [batch, H, P, N])."""
+    x = _f64(x)
+    batch, L, H, P = x.shape
+    B = _f64(B)
+    G, N = B.shape[2], B.shape[3]
+    B, C = _f64(B, (batch, L, G, N)), _f64(C, (batch, L, G, N))
+    dt, A = _f64(dt, (batch, L, H)), _f64(A, (H,))
+    D, dt_bias = _f64(D, (H,)), _f64(dt_bias, (H,))
+    h0 = _f64(h0, (batch, H, P, N))
+    y = np.zeros((batch, L, H, P))
+    fs = np.zeros((batch, H, P, N))
+    rc = self._lib.oracle_ssd(batch, L, H, P, G, N, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                              _ptr(D), _ptr(dt_bias), int(bool(dt_softplus)), _ptr(h0), _ptr(y),
+                              _ptr(fs), int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("oracle_ssd failed (%d)" % rc)
+    return y, fs
+
+
+Oracle.ssd = _ssd_method
 
 
 def _conv_scan_bwd_method(self, x, delta, A, B, C, conv_w, dout, conv_bias=None, D=None, z=None,
@@ -400,6 +428,10 @@ def causal_conv1d_silu(*a, **k):
 
 def causal_conv1d_silu_bwd(*a, **k):
     return default().causal_conv1d_silu_bwd(*a, **k)
+
+
+def ssd(*a, **k):
+    return default().ssd(*a, **k)
 
 
 def selective_scan_conv_bwd(*a, **k):

@@ -585,3 +585,102 @@ static int bwd_run(int64_t batch, int64_t L, int64_t dim, int64_t N, const doubl
     free(part);
     return rc;
 }
+
+/*
+ * The SSD layer of Mamba-2 ("Mamba: State Space Models Challenge Transformers",
+ * section "Mamba-2: Improved Architecture": a multi-head structure with
+ * n_heads heads of d_head channels and a d_state-wide state per channel; "State
+ * Space Models and Mamba", section "Mamba 2 and Hybrid Architectures": the SSM
+ * recast as a structured matrix multiplication, dual to attention). The pages
+ * give the block as a stub; the readings
+ * taken here are the plainest ones the selective scan supports:
+ *  - each head hd has one scalar decay A[hd] (a multiple of the identity, the
+ *    structure that makes the layer a masked matrix product) and one step
+ *    dt[b,t,hd] shared by its P channels;
+ *  - B, C rows of width N are shared by the heads of a group: head hd reads
+ *    group g = hd / (H / G) (consecutive heads share a group; G divides H);
+ *  - dt = dt_raw + dt_bias (if given), then softplus if asked, as in the scan;
+ *  - D is per head; there is no gate inside the layer.
+ * Per batch row b, head hd, token t, channel p < P and state n < N:
+ *   a = exp(dt A[hd]);   h[p][n] <- a h[p][n] + dt x[b,t,hd,p] B[b,t,g,n]
+ *   y[b,t,hd,p] = sum_n C[b,t,g,n] h[p][n] + D[hd] x[b,t,hd,p]
+ * Layouts (row-major): x, y [batch, L, H, P]; dt [batch, L, H]; A, D, dt_bias [H];
+ * B, C [batch, L, G, N]; h0, final_state [batch, H, P, N]. h0, D, dt_bias and
+ * final_state may be NULL. Threads split the (b, hd) pairs. Returns 0, or -1 on
+ * bad arguments or a failed allocation / thread.
+ */
+typedef struct {
+    int64_t batch, L, H, P, G, N;
+    const double *x, *dt, *A, *B, *C, *D, *dt_bias, *h0;
+    int dt_softplus;
+    double *y, *final_state;
+    int64_t begin, end;   /* pairs b * H + hd */
+} ssd_job;
+
+static void* ssd_worker(void* arg)
+{
+    const ssd_job* j = (const ssd_job*)arg;
+    const int64_t L = j->L, H = j->H, P = j->P, G = j->G, N = j->N;
+    double* h = (double*)malloc((size_t)(P * N) * sizeof(double));
+    if (!h) return (void*)1;
+    for (int64_t pair = j->begin; pair < j->end; ++pair) {
+        const int64_t b = pair / H, hd = pair % H, g = hd / (H / G);
+        for (int64_t i = 0; i < P * N; ++i) h[i] = j->h0 ? j->h0[pair * P * N + i] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            double dt = j->dt[(b * L + t) * H + hd];
+            if (j->dt_bias) dt += j->dt_bias[hd];
+            if (j->dt_softplus) dt = oracle_softplus(dt);
+            const double a = exp(dt * j->A[hd]);
+            const double* Bt = j->B + ((b * L + t) * G + g) * N;
+            const double* Ct = j->C + ((b * L + t) * G + g) * N;
+            for (int64_t p = 0; p < P; ++p) {
+                const int64_t e = ((b * L + t) * H + hd) * P + p;   /* x[b, t, hd, p] */
+                double acc = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    h[p * N + n] = a * h[p * N + n] + dt * j->x[e] * Bt[n];
+                    acc += Ct[n] * h[p * N + n];
+                }
+                j->y[e] = acc + (j->D ? j->D[hd] * j->x[e] : 0.0);
+            }
+        }
+        if (j->final_state)
+            for (int64_t i = 0; i < P * N; ++i) j->final_state[pair * P * N + i] = h[i];
+    }
+    free(h);
+    return NULL;
+}
+
+int oracle_ssd(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t G, int64_t N,
+               const double* x, const double* dt, const double* A, const double* B,
+               const double* C, const double* D, const double* dt_bias, int dt_softplus,
+               const double* h0, double* y, double* final_state, int nthreads)
+{
+    if (batch < 0 || L < 0 || H <= 0 || P <= 0 || G <= 0 || N <= 0 || H % G != 0) return -1;
+    if (!x || !dt || !A || !B || !C || !y) return -1;
+    const int64_t npairs = batch * H;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if ((int64_t)nthreads > npairs) nthreads = npairs > 0 ? (int)npairs : 1;
+    ssd_job jobs[256];
+    pthread_t tid[256];
+    for (int i = 0; i < nthreads; ++i) {
+        ssd_job* j = &jobs[i];
+        j->batch = batch; j->L = L; j->H = H; j->P = P; j->G = G; j->N = N;
+        j->x = x; j->dt = dt; j->A = A; j->B = B; j->C = C; j->D = D; j->dt_bias = dt_bias;
+        j->h0 = h0; j->dt_softplus = dt_softplus; j->y = y; j->final_state = final_state;
+        j->begin = npairs * i / nthreads;
+        j->end = npairs * (i + 1) / nthreads;
+    }
+    if (nthreads == 1) return ssd_worker(&jobs[0]) ? -1 : 0;
+    int started = 0, rc = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        if (pthread_create(&tid[i], NULL, ssd_worker, &jobs[i]) != 0) { rc = -1; break; }
+        ++started;
+    }
+    for (int i = 0; i < started; ++i) {
+        void* r = NULL;
+        pthread_join(tid[i], &r);
+        if (r) rc = -1;
+    }
+    return rc;
+}

@@ -835,7 +835,88 @@ def pin_bwd_per_channel_shared_rows(orc, seed=53):
             _close(g4[k], g[k], 1e-12, 1e-13, "%s per-channel vs shared (zoh=%s)" % (k, zoh))
 
 
+
+# --------------------------------------------------------------------------
+# Mamba-2's SSD layer ("Mamba: State Space Models Challenge Transformers",
+# "Mamba-2: Improved Architecture"; "State Space Models and Mamba", "Mamba 2 and
+# Hybrid Architectures": the SSM as a structured matrix multiplication)
+# --------------------------------------------------------------------------
+def _ssd_case(r, batch, L, H, P, G, N, full):
+    return {"x": r.standard_normal((batch, L, H, P)),
+            "dt": (r.standard_normal((batch, L, H)) * 0.5 if full
+                   else r.uniform(0.02, 0.3, (batch, L, H))),
+            "A": -np.exp(r.standard_normal(H) * 0.5),
+            "B": r.standard_normal((batch, L, G, N)), "C": r.standard_normal((batch, L, G, N)),
+            "D": r.uniform(0.5, 1.5, H) if full else None,
+            "dt_bias": r.standard_normal(H) * 0.3 if full else None,
+            "h0": r.standard_normal((batch, H, P, N)) if full else None}
+
+
+def pin_ssd_as_selective_scan(orc, seed=61):
+    """SSD is the selective scan with one decay per head: channel d = hd * P + p
+    of a per-channel-B, C scan with A[d, :] = A[hd], delta = dt of its head and
+    the rows of its head's group gives the same y and final state; with one
+    group the shared-B, C scan does."""
+    r = _rng(seed)
+    for (batch, L, H, P, G, N), full in (((2, 9, 4, 3, 2, 5), True), ((1, 7, 2, 4, 1, 3), False)):
+        c = _ssd_case(r, batch, L, H, P, G, N, full)
+        y, fs = orc.ssd(c["x"], c["dt"], c["A"], c["B"], c["C"], D=c["D"], dt_bias=c["dt_bias"],
+                        dt_softplus=full, h0=c["h0"])
+        head = np.repeat(np.arange(H), P)             # head of channel d
+        grp = head // (H // G)
+        x = c["x"].reshape(batch, L, H * P)
+        delta = c["dt"][:, :, head]
+        A = np.repeat(c["A"][head][:, None], N, 1)
+        rep = lambda a: None if a is None else a[head]
+        h0 = None if c["h0"] is None else c["h0"].reshape(batch, H * P, N)
+        out, f = orc.selective_scan_bcd(x, delta, A, c["B"][:, :, grp], c["C"][:, :, grp],
+                                        D=rep(c["D"]), delta_bias=rep(c["dt_bias"]),
+                                        delta_softplus=full, h0=h0)
+        _close(y.reshape(batch, L, H * P), out, 1e-12, 1e-13, "SSD y vs per-channel scan")
+        _close(fs.reshape(batch, H * P, N), f, 1e-12, 1e-13, "SSD state vs per-channel scan")
+        if G == 1:
+            o1, f1 = orc.selective_scan(x, delta, A, c["B"][:, :, 0], c["C"][:, :, 0],
+                                        D=rep(c["D"]), delta_bias=rep(c["dt_bias"]),
+                                        delta_softplus=full, h0=h0)
+            _close(y.reshape(batch, L, H * P), o1, 1e-12, 1e-13, "SSD y vs shared-B scan")
+
+
+def pin_ssd_matrix_form(orc, seed=62):
+    """The dual form: per batch row and head, y = M X + D X (+ the decayed h0
+    read by C) with the masked matrix M[t, s] = (C_t . B_s) e^{A (S_t - S_s)}
+    dt_s for s <= t and 0 above the diagonal, S the running sum of dt; the final
+    state is e^{A S_L} h0 + sum_s e^{A (S_L - S_s)} dt_s x_s B_s^T."""
+    r = _rng(seed)
+    for (batch, L, H, P, G, N), full in (((2, 12, 4, 3, 2, 6), True), ((1, 10, 3, 2, 3, 4), False),
+                                         ((1, 8, 2, 5, 1, 3), True)):
+        c = _ssd_case(r, batch, L, H, P, G, N, full)
+        y, fs = orc.ssd(c["x"], c["dt"], c["A"], c["B"], c["C"], D=c["D"], dt_bias=c["dt_bias"],
+                        dt_softplus=full, h0=c["h0"])
+        for b in range(batch):
+            for hd in range(H):
+                g = hd // (H // G)
+                v = c["dt"][b, :, hd] + (c["dt_bias"][hd] if c["dt_bias"] is not None else 0.0)
+                dt = np.logaddexp(0.0, v) if full else v
+                S = np.cumsum(dt)
+                Bm, Cm, X = c["B"][b, :, g], c["C"][b, :, g], c["x"][b, :, hd]
+                M = np.tril((Cm @ Bm.T) * np.exp(c["A"][hd] * (S[:, None] - S[None, :]))
+                            * dt[None, :])
+                want = M @ X
+                hL = (np.exp(c["A"][hd] * (S[-1] - S)) * dt)[:, None, None] \
+                    * (X[:, :, None] * Bm[:, None, :])
+                hL = hL.sum(0)
+                if c["h0"] is not None:
+                    want += np.exp(c["A"][hd] * S)[:, None] * (Cm @ c["h0"][b, hd].T)
+                    hL += np.exp(c["A"][hd] * S[-1]) * c["h0"][b, hd]
+                if c["D"] is not None:
+                    want += c["D"][hd] * X
+                _close(y[b, :, hd], want, 1e-10, 1e-12, "SSD y vs matrix form, b=%d head=%d" % (b, hd))
+                _close(fs[b, hd], hL, 1e-10, 1e-12, "SSD state vs matrix form, b=%d head=%d" % (b, hd))
+
+
 ALL_PINS = [
+    pin_ssd_as_selective_scan,
+    pin_ssd_matrix_form,
     pin_conv_bwd,
     pin_conv_scan_bwd,
     pin_phi_prime,

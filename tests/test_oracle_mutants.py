@@ -104,6 +104,16 @@ MUTANTS = [
      "double pre = 0.0;\n                for (int64_t k = 0; k < K; ++k) {\n                    const int64_t s = t - (K - 1) + k;\n                    if (s >= 0) pre += w[d * K + k] * x[(b * L + s) * dim + d];\n                }\n                const double sg"),
     ("conv_bwd_dbias_drops_derivative", "if (dbias) dbias[d] += dpre;",
      "if (dbias) dbias[d] += du[(b * L + t) * dim + d];"),
+    ("ssd_group_interleaved", "g = hd / (H / G);", "g = hd % G;"),
+    ("ssd_drops_dt_bias", "if (j->dt_bias) dt += j->dt_bias[hd];", ""),
+    ("ssd_decay_without_dt", "const double a = exp(dt * j->A[hd]);", "const double a = exp(j->A[hd]);"),
+    ("ssd_drops_decay", "h[p * N + n] = a * h[p * N + n] + dt * j->x[e] * Bt[n];",
+     "h[p * N + n] = h[p * N + n] + dt * j->x[e] * Bt[n];"),
+    ("ssd_reads_B_for_C", "acc += Ct[n] * h[p * N + n];", "acc += Bt[n] * h[p * N + n];"),
+    ("ssd_drops_D", "j->y[e] = acc + (j->D ? j->D[hd] * j->x[e] : 0.0);", "j->y[e] = acc;"),
+    ("ssd_dt_per_channel_slot", "double dt = j->dt[(b * L + t) * H + hd];",
+     "double dt = j->dt[(b * L + t) * H + (hd + 1) % H];"),
+    ("ssd_h0_ignored", "h[i] = j->h0 ? j->h0[pair * P * N + i] : 0.0;", "h[i] = 0.0;"),
 ]
 
 
