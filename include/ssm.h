@@ -82,8 +82,8 @@ enum {
                                of 8 (bf16) / 4 (fp32)                             */
     SSM_ERR_WORKSPACE = -5, /* workspace NULL or smaller than ssm_scan_workspace_bytes */
     SSM_ERR_CUDA = -6,      /* a CUDA launch or query failed (see ssm_last_cuda_error) */
-    SSM_ERR_TIMEOUT = -7,   /* device side: a bounded wait gave up (reserved: no
-                               current kernel waits on another CTA)           */
+    SSM_ERR_TIMEOUT = -7,   /* device side: a scan kernel's bounded wait for its
+                               own TMA copy gave up (ssm_get_device_status)   */
     SSM_ERR_ALIAS = -8      /* an output overlaps an input                         */
 };
 

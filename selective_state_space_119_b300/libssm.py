@@ -14,6 +14,7 @@ ctypes handle is ``lib`` for callers that hold plain device pointers.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional, Tuple
@@ -185,10 +186,25 @@ def _ptr(t, name, dtype=None, shape=None, device=None) -> Optional[int]:
     return t.data_ptr()
 
 
-def _stream(device, stream):
+def _device_of(t, name):
+    """The CUDA device of t; host tensors are refused (there is no CPU path)."""
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    return t.device
+
+
+@contextlib.contextmanager
+def _launch_on(device, stream):
+    """Device and stream of one call, yielding the stream handle for the C call.
+    The wrapper allocates its outputs and per-call workspace (and zero-fills the
+    workspace) inside this context, on the stream the kernels are enqueued on,
+    so the kernels run after the fill and the caching allocator does not hand
+    that memory to other work before they finish."""
     torch = _torch()
-    s = stream if stream is not None else torch.cuda.current_stream(device)
-    return ctypes.c_void_p(s.cuda_stream)
+    with torch.cuda.device(device):
+        s = stream if stream is not None else torch.cuda.current_stream(device)
+        with torch.cuda.stream(s):
+            yield ctypes.c_void_p(s.cuda_stream)
 
 
 def alloc_workspace(batch, seqlen, dim, dstate, io, device, chunk_len_hint=0, tile_config_hint=0,
@@ -225,17 +241,37 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
     batch, L, dim = x.shape
     N = A.shape[1]
     io = x.dtype
-    dev = x.device
-    if out is None:
-        out = torch.empty_like(x)
-    if final_state is None and return_final_state:
-        final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+    dev = _device_of(x, "x")
+    if conv_w is not None and h0 is not None:
+        raise ValueError("the fused conv input stage starts from h = 0; h0 is not supported")
+    if conv_w is None and conv_b is not None:
+        raise ValueError("conv_b needs conv_w")
     bcd = B.dim() == 4          # per-channel B, C: [batch, L, dim, N]
     bc_shape = (batch, L, dim, N) if bcd else (batch, L, N)
     flags = (SSM_FLAG_ZOH if zoh else 0) | (SSM_FLAG_BC_PER_CHANNEL if bcd else 0)
-    if workspace is None:
-        workspace = alloc_workspace(batch, L, dim, N, _io_code(x), dev, chunk_len_hint,
-                                    tile_config_hint, flags)
+    with _launch_on(dev, stream) as sp:
+        if out is None:
+            out = torch.empty_like(x)
+        if final_state is None and return_final_state:
+            final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+        if workspace is None:
+            workspace = alloc_workspace(batch, L, dim, N, _io_code(x), dev, chunk_len_hint,
+                                        tile_config_hint, flags)
+        rc, where = _scan_fwd_call(x, delta, A, B, C, D, z, delta_bias, delta_softplus, out,
+                                   final_state, workspace, chunk_len_hint, tile_config_hint,
+                                   h0, conv_w, conv_b, flags, bc_shape, sp)
+    _check(rc, where)
+    return out, final_state
+
+
+def _scan_fwd_call(x, delta, A, B, C, D, z, delta_bias, delta_softplus, out, final_state,
+                   workspace, chunk_len_hint, tile_config_hint, h0, conv_w, conv_b, flags,
+                   bc_shape, sp):
+    torch = _torch()
+    batch, L, dim = x.shape
+    N = A.shape[1]
+    io = x.dtype
+    dev = _device_of(x, "x")
     ws_ptr = _ptr(workspace, "workspace", torch.uint8, device=dev)
     ws_bytes = workspace.numel() if workspace is not None else 0
     dims = make_dims(batch, L, dim, N, _io_code(x), ws_ptr, ws_bytes, chunk_len_hint,
@@ -253,28 +289,21 @@ def ssm_selective_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None,
         _ptr(out, "out", io, (batch, L, dim), dev),
         _ptr(final_state, "final_state", torch.float32, (batch, dim, N), dev),
     )
-    if conv_w is not None and h0 is not None:
-        raise ValueError("the fused conv input stage starts from h = 0; h0 is not supported")
-    if conv_w is None and conv_b is not None:
-        raise ValueError("conv_b needs conv_w")
-    with torch.cuda.device(dev):
-        if conv_w is not None:
-            if conv_w.dim() != 2 or conv_w.shape[0] != dim:
-                raise ValueError("conv_w must have shape (dim, K), got %s" % (tuple(conv_w.shape),))
-            K = int(conv_w.shape[1])
-            wp = _ptr(conv_w, "conv_w", torch.float32, (dim, K), dev)
-            bp = _ptr(conv_b, "conv_b", torch.float32, (dim,), dev)
-            rc = lib.ssm_selective_scan_fwd_conv(args[0], wp, bp, K, *args[1:],
-                                                 ctypes.byref(dims), _stream(dev, stream))
-        elif h0 is None:
-            rc = lib.ssm_selective_scan_fwd(*args, ctypes.byref(dims), _stream(dev, stream))
-        else:
-            h0p = _ptr(h0, "h0", torch.float32, (batch, dim, N), dev)
-            rc = lib.ssm_selective_scan_fwd_from_state(*args[:9], h0p, *args[9:],
-                                                       ctypes.byref(dims), _stream(dev, stream))
-    _check(rc, "ssm_selective_scan_fwd_conv" if conv_w is not None else
-           "ssm_selective_scan_fwd" if h0 is None else "ssm_selective_scan_fwd_from_state")
-    return out, final_state
+    if conv_w is not None:
+        if conv_w.dim() != 2 or conv_w.shape[0] != dim:
+            raise ValueError("conv_w must have shape (dim, K), got %s" % (tuple(conv_w.shape),))
+        K = int(conv_w.shape[1])
+        wp = _ptr(conv_w, "conv_w", torch.float32, (dim, K), dev)
+        bp = _ptr(conv_b, "conv_b", torch.float32, (dim,), dev)
+        return (lib.ssm_selective_scan_fwd_conv(args[0], wp, bp, K, *args[1:],
+                                                ctypes.byref(dims), sp),
+                "ssm_selective_scan_fwd_conv")
+    if h0 is None:
+        return lib.ssm_selective_scan_fwd(*args, ctypes.byref(dims), sp), "ssm_selective_scan_fwd"
+    h0p = _ptr(h0, "h0", torch.float32, (batch, dim, N), dev)
+    return (lib.ssm_selective_scan_fwd_from_state(*args[:9], h0p, *args[9:], ctypes.byref(dims),
+                                                  sp),
+            "ssm_selective_scan_fwd_from_state")
 
 
 def ssm_causal_conv1d_silu(x, conv_w, conv_b=None, out=None, stream=None):
@@ -283,20 +312,20 @@ def ssm_causal_conv1d_silu(x, conv_w, conv_b=None, out=None, stream=None):
     (same shape and dtype as x; ``out`` may be passed preallocated)."""
     torch = _torch()
     batch, L, dim = x.shape
-    dev = x.device
+    dev = _device_of(x, "x")
     if conv_w.dim() != 2 or conv_w.shape[0] != dim:
         raise ValueError("conv_w must have shape (dim, K), got %s" % (tuple(conv_w.shape),))
     K = int(conv_w.shape[1])
-    if out is None:
-        out = torch.empty_like(x)
     dims = make_dims(batch, L, dim, 16, _io_code(x))
-    with torch.cuda.device(dev):
+    with _launch_on(dev, stream) as sp:
+        if out is None:
+            out = torch.empty_like(x)
         rc = lib.ssm_causal_conv1d_silu(
             _ptr(x, "x", x.dtype, (batch, L, dim), dev),
             _ptr(conv_w, "conv_w", torch.float32, (dim, K), dev),
             _ptr(conv_b, "conv_b", torch.float32, (dim,), dev), K,
             _ptr(out, "out", x.dtype, (batch, L, dim), dev),
-            ctypes.byref(dims), _stream(dev, stream))
+            ctypes.byref(dims), sp)
     _check(rc, "ssm_causal_conv1d_silu")
     return out
 
@@ -312,11 +341,25 @@ def ssm_selective_scan_fwd_static(x, delta, A, B, C, D=None, z=None, delta_bias=
     batch, L, dim = x.shape
     N = A.shape[1]
     io = x.dtype
-    dev = x.device
-    if out is None:
-        out = torch.empty_like(x)
-    if final_state is None and return_final_state:
-        final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+    dev = _device_of(x, "x")
+    with _launch_on(dev, stream) as sp:
+        if out is None:
+            out = torch.empty_like(x)
+        if final_state is None and return_final_state:
+            final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+        rc = _static_call(x, delta, A, B, C, D, z, delta_bias, delta_softplus, out, final_state,
+                          chunk_len_hint, tile_config_hint, sp)
+    _check(rc, "ssm_selective_scan_fwd_static")
+    return out, final_state
+
+
+def _static_call(x, delta, A, B, C, D, z, delta_bias, delta_softplus, out, final_state,
+                 chunk_len_hint, tile_config_hint, sp):
+    torch = _torch()
+    batch, L, dim = x.shape
+    N = A.shape[1]
+    io = x.dtype
+    dev = _device_of(x, "x")
     dims = make_dims(batch, L, dim, N, _io_code(x), None, 0, chunk_len_hint, tile_config_hint)
     args = (
         _ptr(x, "x", io, (batch, L, dim), dev),
@@ -331,10 +374,7 @@ def ssm_selective_scan_fwd_static(x, delta, A, B, C, D=None, z=None, delta_bias=
         _ptr(out, "out", io, (batch, L, dim), dev),
         _ptr(final_state, "final_state", torch.float32, (batch, dim, N), dev),
     )
-    with torch.cuda.device(dev):
-        rc = lib.ssm_selective_scan_fwd_static(*args, ctypes.byref(dims), _stream(dev, stream))
-    _check(rc, "ssm_selective_scan_fwd_static")
-    return out, final_state
+    return lib.ssm_selective_scan_fwd_static(*args, ctypes.byref(dims), sp)
 
 
 def ssm_state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
@@ -345,9 +385,10 @@ def ssm_state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
     torch = _torch()
     batch, dim, N = state.shape
     io = x.dtype
-    dev = x.device
+    dev = _device_of(state, "state")
     if out is None:
-        out = torch.empty_like(x)
+        with _launch_on(dev, stream):
+            out = torch.empty_like(x)
     dims = make_dims(batch, 1, dim, N, _io_code(x), flags=SSM_FLAG_ZOH if zoh else 0)
     args = (
         _ptr(state, "state", torch.float32, (batch, dim, N), dev),
@@ -362,8 +403,8 @@ def ssm_state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
         1 if delta_softplus else 0,
         _ptr(out, "out", io, (batch, dim), dev),
     )
-    with torch.cuda.device(dev):
-        rc = lib.ssm_state_update(*args, ctypes.byref(dims), _stream(dev, stream))
+    with _launch_on(dev, stream) as sp:
+        rc = lib.ssm_state_update(*args, ctypes.byref(dims), sp)
     _check(rc, "ssm_state_update")
     return out
 
@@ -376,9 +417,9 @@ def ssm_get_device_status(batch, seqlen, dim, dstate, io, workspace, chunk_len_h
     ws_bytes = workspace.numel() if workspace is not None else 0
     dims = make_dims(batch, seqlen, dim, dstate, io, ws_ptr, ws_bytes, chunk_len_hint,
                      tile_config_hint)
-    dev = workspace.device if workspace is not None else torch.device("cuda")
-    with torch.cuda.device(dev):
-        return int(lib.ssm_get_device_status(ctypes.byref(dims), _stream(dev, stream)))
+    dev = _device_of(workspace, "workspace") if workspace is not None else torch.device("cuda")
+    with _launch_on(dev, stream) as sp:
+        return int(lib.ssm_get_device_status(ctypes.byref(dims), sp))
 
 
 def ssm_scan_checkpoint_bytes(batch, seqlen, dim, dstate, io) -> int:
@@ -403,19 +444,19 @@ def ssm_selective_scan_fwd_ckpt(x, delta, A, B, C, D=None, z=None, delta_bias=No
     batch, L, dim = x.shape
     N = A.shape[1]
     io = x.dtype
-    dev = x.device
-    if out is None:
-        out = torch.empty_like(x)
-    if final_state is None:
-        final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
-    if ckpt is None:
-        ckpt = torch.empty((batch, (L + 7) // 8, dim, N), dtype=torch.float32, device=dev)
-    if workspace is None:
-        workspace = alloc_workspace(batch, L, dim, N, _io_code(x), dev, chunk_len_hint)
-    ws_ptr = _ptr(workspace, "workspace", torch.uint8, device=dev)
-    ws_bytes = workspace.numel() if workspace is not None else 0
-    dims = make_dims(batch, L, dim, N, _io_code(x), ws_ptr, ws_bytes, chunk_len_hint)
-    with torch.cuda.device(dev):
+    dev = _device_of(x, "x")
+    with _launch_on(dev, stream) as sp:
+        if out is None:
+            out = torch.empty_like(x)
+        if final_state is None:
+            final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+        if ckpt is None:
+            ckpt = torch.empty((batch, (L + 7) // 8, dim, N), dtype=torch.float32, device=dev)
+        if workspace is None:
+            workspace = alloc_workspace(batch, L, dim, N, _io_code(x), dev, chunk_len_hint)
+        ws_ptr = _ptr(workspace, "workspace", torch.uint8, device=dev)
+        ws_bytes = workspace.numel() if workspace is not None else 0
+        dims = make_dims(batch, L, dim, N, _io_code(x), ws_ptr, ws_bytes, chunk_len_hint)
         rc = lib.ssm_selective_scan_fwd_ckpt(
             _ptr(x, "x", io, (batch, L, dim), dev), _ptr(delta, "delta", io, (batch, L, dim), dev),
             _ptr(A, "A", torch.float32, (dim, N), dev), _ptr(B, "B", io, (batch, L, N), dev),
@@ -426,7 +467,7 @@ def ssm_selective_scan_fwd_ckpt(x, delta, A, B, C, D=None, z=None, delta_bias=No
             _ptr(out, "out", io, (batch, L, dim), dev),
             _ptr(final_state, "final_state", torch.float32, (batch, dim, N), dev),
             _ptr(ckpt, "ckpt", torch.float32, (batch, (L + 7) // 8, dim, N), dev),
-            ctypes.byref(dims), _stream(dev, stream))
+            ctypes.byref(dims), sp)
     _check(rc, "ssm_selective_scan_fwd_ckpt")
     return out, final_state, ckpt
 
@@ -441,7 +482,22 @@ def ssm_selective_scan_bwd(x, delta, A, B, C, ckpt, dout, D=None, z=None, delta_
     batch, L, dim = x.shape
     N = A.shape[1]
     io = x.dtype
-    dev = x.device
+    dev = _device_of(x, "x")
+    with _launch_on(dev, stream) as sp:
+        rc, g = _bwd_call(x, delta, A, B, C, ckpt, dout, D, z, delta_bias, delta_softplus,
+                          dfinal_state, want_dD, want_ddelta_bias, want_dh0, workspace,
+                          chunk_len_hint, sp)
+    _check(rc, "ssm_selective_scan_bwd")
+    return g
+
+
+def _bwd_call(x, delta, A, B, C, ckpt, dout, D, z, delta_bias, delta_softplus, dfinal_state,
+              want_dD, want_ddelta_bias, want_dh0, workspace, chunk_len_hint, sp):
+    torch = _torch()
+    batch, L, dim = x.shape
+    N = A.shape[1]
+    io = x.dtype
+    dev = _device_of(x, "x")
     g = {"dx": torch.empty_like(x), "ddelta": torch.empty_like(x),
          "dA": torch.empty((dim, N), dtype=torch.float32, device=dev),
          "dB": torch.empty((batch, L, N), dtype=io, device=dev),
@@ -458,23 +514,21 @@ def ssm_selective_scan_bwd(x, delta, A, B, C, ckpt, dout, D=None, z=None, delta_
     dims = make_dims(batch, L, dim, N, _io_code(x), _ptr(workspace, "workspace", torch.uint8,
                                                          device=dev),
                      workspace.numel(), chunk_len_hint)
-    with torch.cuda.device(dev):
-        rc = lib.ssm_selective_scan_bwd(
-            _ptr(x, "x", io, (batch, L, dim), dev), _ptr(delta, "delta", io, (batch, L, dim), dev),
-            _ptr(A, "A", torch.float32, (dim, N), dev), _ptr(B, "B", io, (batch, L, N), dev),
-            _ptr(C, "C", io, (batch, L, N), dev), _ptr(D, "D", torch.float32, (dim,), dev),
-            _ptr(z, "z", io, (batch, L, dim), dev),
-            _ptr(delta_bias, "delta_bias", torch.float32, (dim,), dev),
-            1 if delta_softplus else 0,
-            _ptr(ckpt, "ckpt", torch.float32, (batch, (L + 7) // 8, dim, N), dev),
-            _ptr(dout, "dout", io, (batch, L, dim), dev),
-            _ptr(dfinal_state, "dfinal_state", torch.float32, (batch, dim, N), dev),
-            _ptr(g["dx"], "dx"), _ptr(g["ddelta"], "ddelta"), _ptr(g["dA"], "dA"),
-            _ptr(g["dB"], "dB"), _ptr(g["dC"], "dC"), _ptr(g["dD"], "dD"), _ptr(g["dz"], "dz"),
-            _ptr(g["ddelta_bias"], "ddelta_bias"), _ptr(g["dh0"], "dh0"),
-            ctypes.byref(dims), _stream(dev, stream))
-    _check(rc, "ssm_selective_scan_bwd")
-    return g
+    rc = lib.ssm_selective_scan_bwd(
+        _ptr(x, "x", io, (batch, L, dim), dev), _ptr(delta, "delta", io, (batch, L, dim), dev),
+        _ptr(A, "A", torch.float32, (dim, N), dev), _ptr(B, "B", io, (batch, L, N), dev),
+        _ptr(C, "C", io, (batch, L, N), dev), _ptr(D, "D", torch.float32, (dim,), dev),
+        _ptr(z, "z", io, (batch, L, dim), dev),
+        _ptr(delta_bias, "delta_bias", torch.float32, (dim,), dev),
+        1 if delta_softplus else 0,
+        _ptr(ckpt, "ckpt", torch.float32, (batch, (L + 7) // 8, dim, N), dev),
+        _ptr(dout, "dout", io, (batch, L, dim), dev),
+        _ptr(dfinal_state, "dfinal_state", torch.float32, (batch, dim, N), dev),
+        _ptr(g["dx"], "dx"), _ptr(g["ddelta"], "ddelta"), _ptr(g["dA"], "dA"),
+        _ptr(g["dB"], "dB"), _ptr(g["dC"], "dC"), _ptr(g["dD"], "dD"), _ptr(g["dz"], "dz"),
+        _ptr(g["ddelta_bias"], "ddelta_bias"), _ptr(g["dh0"], "dh0"),
+        ctypes.byref(dims), sp)
+    return rc, g
 
 
 # Short aliases.

@@ -7,7 +7,7 @@ and L-chunks with ragged tails; every optional argument on and off; dstate
 delta; long-memory carries across many chunks (no D, no gate, so nothing masks
 a broken carry); an impulse that must travel through every chunk boundary;
 the three full-size bf16 workloads on sampled channels (all tokens); bitwise
-determinism; guard bands around the outputs; and argument errors.
+determinism, also on a caller's side stream; guard bands around the outputs; and argument errors.
 """
 import numpy as np
 import pytest
@@ -210,6 +210,23 @@ def test_deterministic(torch):
     spec, inp = _small(delta_kind="softplus_bias", A_kind="lognormal")
     a, fa = G.gpu_scan(inp, True, chunk_len_hint=48)
     b, fb = G.gpu_scan(inp, True, chunk_len_hint=48)
+    assert torch.equal(a, b) and torch.equal(fa, fb)
+
+
+def test_side_stream(torch):
+    """A call on a caller's side stream: the binding allocates the outputs and
+    zero-fills the per-call workspace on that stream, so the result equals the
+    current stream's bit for bit."""
+    from selective_state_space_119_b300 import libssm
+    spec, inp = _small(delta_kind="softplus_bias", A_kind="lognormal")
+    a, fa = G.gpu_scan(inp, True, chunk_len_hint=48)
+    args = [G.dev(inp[k]) for k in ("x", "delta", "A", "B", "C")]
+    kw = {k: G.dev(inp.get(k)) for k in ("D", "z", "delta_bias")}
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    b, fb = libssm.ssm_selective_scan_fwd(*args, delta_softplus=True, chunk_len_hint=48,
+                                          stream=side, **kw)
+    side.synchronize()
     assert torch.equal(a, b) and torch.equal(fa, fb)
 
 
