@@ -26,7 +26,12 @@ bias), gate), i.e. every step of the scan path. Rank 0 prints one JSON line.
   forward and the backward (every gradient), per call.
 * bc_per_channel: the scan with per-channel B, C on the same shapes (bound by
   HBM: its roofline is the copy bandwidth).
-* cpu_baseline: the float64 CPU oracle timed on this host (rank 0, N = 1).
+* zoh: the scan with the exact zero-order-hold Bbar on the same workload,
+  against the same SFU roofline.
+  A side leg that fails reports {"error": ...} in its place; the headline
+  line is still printed.
+* cpu_baseline: the float64 CPU oracle timed on this host (rank 0, N = 1);
+  check: its last pass compared with the last timed GPU output, every element.
 
 N > 1 (torchrun): every rank runs its own replica of the workload on its own
 GPU (the scan has no cross-channel exchange: weak scaling, no collective on
@@ -379,18 +384,28 @@ def bench_scan(args, rank, world, local):
                   "pipelined": "copies in, compute and copies out of neighbouring steps "
                                "overlap (3 streams, 2 device buffer sets)"}
 
-    # quick self-check of the timed output against the oracle on a few channels
-    res["check"] = parity_probe(spec, inp, sets[0]["out"]) if rank == 0 else None
+    # the last timed output (every set holds the same input values), for the
+    # CPU-baseline leg to compare with the oracle's output on the host
+    res["out_host"] = (sets[0]["out"].float().cpu().numpy().astype("float64")
+                       if rank == 0 and world == 1 else None)
     del sets
     torch.cuda.empty_cache()
-    if not args.no_decode:
-        res["decode"] = bench_decode(args, dev, stream)
-    if not args.no_input_stage:
-        res["input_stage"] = bench_input_stage(args, spec, dev, stream)
-    if not args.no_train and spec.N == 16:
-        res["train"] = bench_train(args, spec, dev, stream)
-    if not args.no_bcd and spec.N == 16:
-        res["bc_per_channel"] = bench_bcd(args, spec, dev, stream)
+    legs = (("decode", not args.no_decode, lambda: bench_decode(args, dev, stream)),
+            ("input_stage", not args.no_input_stage,
+             lambda: bench_input_stage(args, spec, dev, stream)),
+            ("train", not args.no_train and spec.N == 16,
+             lambda: bench_train(args, spec, dev, stream)),
+            ("bc_per_channel", not args.no_bcd and spec.N == 16,
+             lambda: bench_bcd(args, spec, dev, stream)),
+            ("zoh", not args.no_zoh and spec.N == 16,
+             lambda: bench_zoh(args, spec, dev, stream)))
+    for name, wanted, run in legs:
+        if not wanted:
+            continue
+        try:
+            res[name] = run()
+        except Exception as e:   # a failed side leg is reported, not fatal to the headline
+            res[name] = {"error": "%s: %s" % (type(e).__name__, e)}
     return res, spec
 
 
@@ -465,24 +480,13 @@ def alu_roofline(spec, per_call_s, plan):
             "peak_basis": "measured ex2 rate 29.1 per SM per clock x 148 SMs x 2032 MHz"}
 
 
-def parity_probe(spec, inp, out):
-    """Compare 8 channels of the last timed output with the oracle."""
+def output_check(got, ref):
+    """Error statistics of the timed output against a reference output (both
+    float64 host arrays): relative L2 and max |err| / (1 + |ref|)."""
     import numpy as np
-    import torch
-    import oracle
-    from selective_state_space_119_b300 import inputs as I
-    dsel = np.linspace(0, spec.dim - 1, 8).astype(np.int64)
-    ry, _ = oracle.selective_scan(
-        I.widen(inp["x"][:, :, dsel]), I.widen(inp["delta"][:, :, dsel]), inp["A"][dsel],
-        I.widen(inp["B"]), I.widen(inp["C"]),
-        D=None if inp["D"] is None else inp["D"][dsel],
-        z=None if inp["z"] is None else I.widen(inp["z"][:, :, dsel]),
-        delta_bias=None if inp["delta_bias"] is None else inp["delta_bias"][dsel],
-        delta_softplus=spec.delta_softplus)
-    y = out[:, :, torch.as_tensor(dsel, device=out.device)].float().cpu().numpy().astype(np.float64)
-    rel = float(np.linalg.norm(y - ry) / np.linalg.norm(ry))
-    mx = float(np.max(np.abs(y - ry) / (1 + np.abs(ry))))
-    return {"channels": len(dsel), "rel_l2": rel, "max_scaled_err": mx}
+    rel = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    mx = float(np.max(np.abs(got - ref) / (1 + np.abs(ref))))
+    return {"elements": int(got.size), "rel_l2": rel, "max_scaled_err": mx}
 
 
 def bench_decode(args, dev, stream):
@@ -776,12 +780,69 @@ def bench_bcd(args, spec, dev, stream):
                               "algorithmic_bytes_per_call": alg}, **nominal(gbs))}
 
 
+def bench_zoh(args, spec, dev, stream):
+    """The scan with the exact zero-order-hold Bbar (SSM_FLAG_ZOH) on the scan
+    workload: the same inputs, bytes and SFU operations per element as the
+    first-order scan (the hold term (e^{dt A} - 1)/A reuses the exponential),
+    plus its FP32 work; reported against the same SFU roofline."""
+    import torch
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+
+    inp = I.make_scan_inputs(spec)
+    io = libssm.SSM_BF16 if spec.io == "bf16" else libssm.SSM_F32
+    alg = I.algorithmic_bytes_scan(spec)
+    nsets = max(2, min(16, math.ceil(2 * L2_BYTES / alg) + 1))
+    base = {k: _upload(v, dev) for k, v in inp.items()}
+    sets = []
+    for i in range(nsets):
+        st = {k: (None if base[k] is None else (base[k] if (k in ("A", "D", "delta_bias") or i == 0)
+                                                 else base[k].clone())) for k in base}
+        st["out"] = torch.empty_like(base["x"])
+        sets.append(st)
+    B_, L_, D_, N_ = spec.batch, spec.L, spec.dim, spec.N
+    F = libssm.SSM_FLAG_ZOH
+    ws = libssm.alloc_workspace(B_, L_, D_, N_, io, dev, flags=F)
+    dims = libssm.make_dims(B_, L_, D_, N_, io, None if ws is None else ws.data_ptr(),
+                            0 if ws is None else ws.numel(), flags=F)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    sp = 1 if spec.delta_softplus else 0
+
+    def call(i):
+        st = sets[i % nsets]
+        rc = libssm.lib.ssm_selective_scan_fwd(
+            _vp(st["x"]), _vp(st["delta"]), _vp(st["A"]), _vp(st["B"]), _vp(st["C"]),
+            _vp(st["D"]), _vp(st["z"]), _vp(st["delta_bias"]), sp, _vp(st["out"]), None,
+            ctypes.byref(dims), sptr)
+        if rc != 0:
+            raise libssm.SSMError(rc, "ssm_selective_scan_fwd (exact zero-order hold)")
+
+    for i in range(max(args.warmup, 3)):
+        call(i)
+    torch.cuda.synchronize()
+    n = max(16, min(args.steps, 400))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        call(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3 / n
+    plan = libssm.ssm_scan_plan(B_, L_, D_, N_, io, flags=F)
+    roof = alu_roofline(spec, sec, plan)
+    roof["kernel"] = roof["kernel"].replace("scan_kernel", "scan_kernel with the ZOH flag")
+    return {"us_per_call": sec * 1e6, "value": spec.elements / sec, "unit": "elems/s",
+            "timed_calls": n, "input_sets": nsets, "kernels_per_call": plan["kernels"],
+            "roofline": roof, "algorithmic_bytes_per_call": alg}
+
+
 # ---------------------------------------------------------------------------
 # the CPU oracle arm
 # ---------------------------------------------------------------------------
 def cpu_oracle_rate(spec, inp, min_seconds: float, max_passes: int = 100):
     """Time the float64 oracle over whole passes of the workload on every host
-    thread until min_seconds have passed (at least one pass)."""
+    thread until min_seconds have passed (at least one pass). Returns the rate,
+    the threads, the passes, the seconds and the output of the last pass."""
     import oracle
     from selective_state_space_119_b300 import inputs as I
     threads = oracle.default_threads()
@@ -791,12 +852,12 @@ def cpu_oracle_rate(spec, inp, min_seconds: float, max_passes: int = 100):
               delta_softplus=spec.delta_softplus, nthreads=threads)
     passes, t0 = 0, time.perf_counter()
     while True:
-        oracle.selective_scan(*args, **kw)
+        out, _ = oracle.selective_scan(*args, **kw)
         passes += 1
         el = time.perf_counter() - t0
         if el >= min_seconds or passes >= max_passes:
             break
-    return spec.elements * passes / el, threads, passes, el
+    return spec.elements * passes / el, threads, passes, el, out
 
 
 def run_reference(args, rank, world, budget_s: float = 120.0):
@@ -883,6 +944,8 @@ def main(argv=None):
                     help="skip the training (checkpointing forward + backward) timings")
     ap.add_argument("--no-bcd", action="store_true",
                     help="skip the per-channel B, C scan timing")
+    ap.add_argument("--no-zoh", action="store_true",
+                    help="skip the exact zero-order-hold scan timing")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,
                     help="minimum wall time of the CPU oracle baseline")
     args = ap.parse_args(argv)
@@ -915,23 +978,21 @@ def main(argv=None):
                 "roofline": res["roofline"], "hbm_roofline": res["hbm_roofline"],
                 "floors_us": res["floors_us"], "e2e": res["e2e"],
                 "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
-                "plan": res["plan"], "check": res["check"]}
-        if "decode" in res:
-            line["decode"] = res["decode"]
-        if "input_stage" in res:
-            line["input_stage"] = res["input_stage"]
-        if "train" in res:
-            line["train"] = res["train"]
-        if "bc_per_channel" in res:
-            line["bc_per_channel"] = res["bc_per_channel"]
+                "plan": res["plan"], "check": None}
+        for leg in ("decode", "input_stage", "train", "bc_per_channel", "zoh"):
+            if leg in res:
+                line[leg] = res[leg]
         if world == 1:
             from selective_state_space_119_b300 import inputs as I
             inp = I.make_scan_inputs(spec)
-            rate, threads, passes, el = cpu_oracle_rate(spec, inp, args.cpu_seconds)
+            rate, threads, passes, el, ref = cpu_oracle_rate(spec, inp, args.cpu_seconds)
             line["cpu_baseline"] = {
                 "value": rate, "unit": "elems/s", "cores": threads, "kind": "oracle",
                 "sample": "whole workload (%d x %d x %d), %d pass(es), %.1f s, all host threads"
                           % (spec.batch, spec.L, spec.dim, passes, el)}
+            # the oracle's last pass against the last timed GPU output, every element
+            line["check"] = dict(output_check(res["out_host"], ref),
+                                 against="the cpu_baseline leg's oracle output")
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

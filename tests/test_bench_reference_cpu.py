@@ -25,3 +25,17 @@ def test_reference_arm_prints_the_contract_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["h2d_bytes_per_step"] == 0
     assert e2e["d2h_bytes_per_step"] == 0
+
+
+def test_output_check_statistics():
+    """The bench's output check: relative L2 and max |err| / (1 + |ref|)."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    ref = np.array([1.0, -2.0, 0.0, 4.0])
+    got = ref + np.array([0.0, 0.5, 0.1, 0.0])
+    c = bench.output_check(got, ref)
+    assert c["elements"] == 4
+    assert abs(c["rel_l2"] - np.sqrt(0.26) / np.sqrt(21.0)) < 1e-15
+    assert abs(c["max_scaled_err"] - 0.5 / 3.0) < 1e-15
+    assert bench.output_check(ref, ref)["rel_l2"] == 0.0
