@@ -662,6 +662,26 @@ def pin_zoh_ode(orc, seed=42):
     assert np.abs(out1 - outz).max() > 1e-3, "first-order and ZOH must differ at these steps"
 
 
+def pin_zoh_library(orc, seed=46):
+    """One ZOH step equals SciPy's zero-order-hold discretization of the
+    continuous system (scipy.signal.cont2discrete, method "zoh", which takes the
+    matrix exponential of the augmented [[A, B], [0, 0]] dt): h1 = Ad h0 + Bd x."""
+    from scipy.signal import cont2discrete
+    r = _rng(seed)
+    N = 5
+    for dt in (1e-3, 0.07, 0.9):
+        A = -np.exp(r.standard_normal(N))
+        B = r.standard_normal(N)
+        h0 = r.standard_normal(N)
+        xv = r.standard_normal()
+        Ad, Bd, _, _, _ = cont2discrete((np.diag(A), B[:, None], np.ones((1, N)), np.zeros((1, 1))),
+                                        dt, method="zoh")
+        _, fs = orc.selective_scan(np.full((1, 1, 1), xv), np.full((1, 1, 1), dt), A[None, :],
+                                   B[None, None, :], np.zeros((1, 1, N)), h0=h0[None, None, :],
+                                   zoh=True)
+        _close(fs[0, 0], Ad @ h0 + Bd[:, 0] * xv, 1e-11, 1e-13, "ZOH step vs cont2discrete, dt=%g" % dt)
+
+
 def pin_zoh_small_step(orc, seed=43):
     """As dt -> 0, ZOH tends to the first-order form: the difference per step is
     dt B x (phi(dt A) - 1) ~ dt^2 A B x / 2."""
@@ -928,6 +948,7 @@ ALL_PINS = [
     pin_zoh_closed_form,
     pin_zoh_ode,
     pin_zoh_small_step,
+    pin_zoh_library,
     pin_zoh_decode,
     pin_bwd_finite_differences,
     pin_bwd_autograd,
