@@ -307,3 +307,17 @@ def test_timeout_probe_rejects_bad_arguments_before_launch():
     assert f(FAKE + 4, 256, 1000, None) == L.SSM_ERR_ALIGN
     assert f(FAKE, 256, 0, None) == L.SSM_ERR_DIMS
     assert f(FAKE, 256, (1 << 24) + 1, None) == L.SSM_ERR_DIMS
+
+
+def test_plans_of_the_measured_workloads():
+    """The planner's choices for the benchmark workloads are the ones measured
+    fastest on the B300 (chunk counts swept from 1 to 64): a change to the plan
+    model that moves them must be re-measured, not slip in."""
+    p = L.ssm_scan_plan(4, 2048, 1536, 16, "bf16")
+    assert (p["chunk_len"], p["nchunks"], p["ctas"], p["kernels"]) == (352, 6, 288, 2)
+    p = L.ssm_scan_plan(8, 4096, 2048, 16, "bf16")
+    assert (p["nchunks"], p["ctas"], p["kernels"]) == (1, 128, 1)
+    p = L.ssm_scan_plan(1, 131072, 5120, 16, "bf16")
+    assert p["nchunks"] == 37
+    p = L.ssm_scan_plan(4, 2048, 1536, 16, "bf16", flags=L.SSM_FLAG_BC_PER_CHANNEL)
+    assert (p["chunk_len"], p["nchunks"]) == (256, 8)
