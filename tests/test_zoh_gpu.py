@@ -69,6 +69,26 @@ def test_zoh_scan_softplus(torch, io):
     G.parity(G.host64(fs), rh, "state", "ZOH final state softplus")
 
 
+def test_zoh_benchmark_size_sampled(torch):
+    """Batch 4, L 2048, dim 1536, bf16, softplus(delta + bias), gate, with the
+    exact zero-order hold and the library's plan (6 chunks): sampled channels,
+    every token, against the oracle."""
+    spec = I.WORKLOADS["scan_bf16_b4_L2048_d1536_softplus"]
+    inp = I.make_scan_inputs(spec)
+    out, fs = _gpu(inp, True)
+    dsel = np.array([0, 1, 127, 128, 999, 1535])
+    sub = dict(inp)
+    for k in ("x", "delta", "z"):
+        if inp.get(k) is not None:
+            sub[k] = inp[k][:, :, dsel]
+    for k in ("A", "D", "delta_bias"):
+        if inp.get(k) is not None:
+            sub[k] = np.asarray(inp[k])[dsel]
+    ry, rh = _ref(sub, True)
+    G.parity(G.host64(out)[:, :, dsel], ry, "bf16", "ZOH y, benchmark size")
+    G.parity(G.host64(fs)[:, dsel], rh, "state", "ZOH final state, benchmark size")
+
+
 def test_zoh_changes_the_result(torch):
     spec = I.ScanSpec(1, 128, 128, io="f32", delta_lo=0.05, delta_hi=0.5, seed=73)
     inp = I.make_scan_inputs(spec)
