@@ -342,6 +342,33 @@ def _bcd_method(self, x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_
 Oracle.selective_scan_bcd = _bcd_method
 
 
+def _bcd_step_method(self, state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
+                     delta_softplus=False, zoh=False):
+    """One recurrent step with per-channel B, C [batch, dim, N]: channel d is the
+    one-channel step of the oracle with its own rows B[:, d], C[:, d]. state
+    [batch, dim, N] is not modified. Returns (out [batch, dim], new_state)."""
+    st = _f64(state)
+    batch, dim, N = st.shape
+    B, C = _f64(B, (batch, dim, N)), _f64(C, (batch, dim, N))
+    x, delta = _f64(x, (batch, dim)), _f64(delta, (batch, dim))
+    A = _f64(A, (dim, N))
+    out = np.zeros((batch, dim))
+    new = np.zeros((batch, dim, N))
+    col = lambda a, d: None if a is None else _f64(a)[:, d:d + 1]
+    vec = lambda a, d: None if a is None else _f64(a)[d:d + 1]
+    for d in range(dim):
+        o, h = self.state_update(st[:, d:d + 1], x[:, d:d + 1], delta[:, d:d + 1], A[d:d + 1],
+                                 B[:, d], C[:, d], D=vec(D, d), z=col(z, d),
+                                 delta_bias=vec(delta_bias, d), delta_softplus=delta_softplus,
+                                 zoh=zoh)
+        out[:, d] = o[:, 0]
+        new[:, d] = h[:, 0]
+    return out, new
+
+
+Oracle.state_update_bcd = _bcd_step_method
+
+
 def _bcd_bwd_method(self, x, delta, A, B, C, dout, D=None, z=None, delta_bias=None,
                     delta_softplus=False, h0=None, dh_final=None, nthreads=None, zoh=False):
     """Gradients of the per-channel B, C scan: channel d is the one-channel scan
@@ -440,6 +467,10 @@ def selective_scan_conv_bwd(*a, **k):
 
 def selective_scan_bwd(*a, **k):
     return default().selective_scan_bwd(*a, **k)
+
+
+def state_update_bcd(*a, **k):
+    return default().state_update_bcd(*a, **k)
 
 
 def selective_scan_bcd(*a, **k):

@@ -934,6 +934,33 @@ def pin_ssd_matrix_form(orc, seed=62):
                 _close(fs[b, hd], hL, 1e-10, 1e-12, "SSD state vs matrix form, b=%d head=%d" % (b, hd))
 
 
+
+def pin_bc_per_channel_decode(orc, seed=47):
+    """The per-channel decode step is one token of the per-channel scan from the
+    same state (with and without the zero-order hold), and with rows equal
+    across channels it is the shared-B, C step exactly."""
+    r = _rng(seed)
+    c = _random_case(r, batch=2, L=1, dim=3, N=4)
+    st = r.standard_normal((2, 3, 4))
+    B4 = r.standard_normal((2, 1, 3, 4))
+    C4 = r.standard_normal((2, 1, 3, 4))
+    bias = r.standard_normal(3) * 0.2
+    for zoh in (False, True):
+        oz, fz = orc.selective_scan_bcd(c["x"], c["delta"], c["A"], B4, C4, D=c["D"], z=c["z"],
+                                        delta_bias=bias, delta_softplus=True, h0=st, zoh=zoh)
+        od, sd = orc.state_update_bcd(st, c["x"][:, 0], c["delta"][:, 0], c["A"], B4[:, 0],
+                                      C4[:, 0], D=c["D"], z=c["z"][:, 0], delta_bias=bias,
+                                      delta_softplus=True, zoh=zoh)
+        _close(od, oz[:, 0], 1e-14, 1e-15, "per-channel decode y (zoh=%s)" % zoh)
+        _close(sd, fz, 1e-14, 1e-15, "per-channel decode state (zoh=%s)" % zoh)
+    Bs = np.repeat(c["B"][:, 0, None, :], 3, 1)
+    Cs = np.repeat(c["C"][:, 0, None, :], 3, 1)
+    o1, s1 = orc.state_update(st, c["x"][:, 0], c["delta"][:, 0], c["A"], c["B"][:, 0],
+                              c["C"][:, 0], D=c["D"])
+    o2, s2 = orc.state_update_bcd(st, c["x"][:, 0], c["delta"][:, 0], c["A"], Bs, Cs, D=c["D"])
+    assert np.array_equal(o1, o2) and np.array_equal(s1, s2), "shared rows = shared B, C step"
+
+
 ALL_PINS = [
     pin_ssd_as_selective_scan,
     pin_ssd_matrix_form,
@@ -944,6 +971,7 @@ ALL_PINS = [
     pin_bwd_variants_autograd,
     pin_bwd_per_channel_shared_rows,
     pin_bc_per_channel,
+    pin_bc_per_channel_decode,
     pin_phi,
     pin_zoh_closed_form,
     pin_zoh_ode,
