@@ -961,9 +961,44 @@ def pin_bc_per_channel_decode(orc, seed=47):
     assert np.array_equal(o1, o2) and np.array_equal(s1, s2), "shared rows = shared B, C step"
 
 
+
+def pin_ssd_chunked_form(orc, seed=63):
+    """The chunked form of the matrix product: per chunk of Q tokens (the last one
+    ragged), y = tril((C Bᵀ) ∘ e^{A (s_t - s_u)} dt_u) X (the chunk's own tokens,
+    s the running sum of dt inside the chunk) + e^{A s_t} C_t h_inᵀ (the state
+    carried in) + D x, and the state passed on is e^{A s_Q} h_in + Σ_u
+    e^{A (s_Q - s_u)} dt_u x_u B_uᵀ. Every chunk size gives the oracle's y and
+    final state."""
+    r = _rng(seed)
+    batch, L, H, P, G, N = 2, 23, 4, 3, 2, 5
+    c = _ssd_case(r, batch, L, H, P, G, N, True)
+    y, fs = orc.ssd(c["x"], c["dt"], c["A"], c["B"], c["C"], D=c["D"], dt_bias=c["dt_bias"],
+                    dt_softplus=True, h0=c["h0"])
+    for Q in (1, 4, 7, 23, 32):
+        for b in range(batch):
+            for hd in range(H):
+                g = hd // (H // G)
+                a = c["A"][hd]
+                dt_all = np.logaddexp(0.0, c["dt"][b, :, hd] + c["dt_bias"][hd])
+                h = c["h0"][b, hd].copy()                    # [P, N]
+                yc = np.zeros((L, P))
+                for t0 in range(0, L, Q):
+                    t1 = min(L, t0 + Q)
+                    dt = dt_all[t0:t1]
+                    sl = np.cumsum(dt)
+                    Bm, Cm, X = c["B"][b, t0:t1, g], c["C"][b, t0:t1, g], c["x"][b, t0:t1, hd]
+                    M = np.tril((Cm @ Bm.T) * np.exp(a * (sl[:, None] - sl[None, :])) * dt[None, :])
+                    yc[t0:t1] = M @ X + np.exp(a * sl)[:, None] * (Cm @ h.T) + c["D"][hd] * X
+                    w = np.exp(a * (sl[-1] - sl)) * dt
+                    h = np.exp(a * sl[-1]) * h + (X * w[:, None]).T @ Bm
+                _close(yc, y[b, :, hd], 1e-10, 1e-12, "SSD chunked y, Q=%d b=%d head=%d" % (Q, b, hd))
+                _close(h, fs[b, hd], 1e-10, 1e-12, "SSD chunked state, Q=%d b=%d head=%d" % (Q, b, hd))
+
+
 ALL_PINS = [
     pin_ssd_as_selective_scan,
     pin_ssd_matrix_form,
+    pin_ssd_chunked_form,
     pin_conv_bwd,
     pin_conv_scan_bwd,
     pin_phi_prime,
