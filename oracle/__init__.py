@@ -19,6 +19,18 @@ What it computes (page title, section):
   * "State-space models (Mamba, S4)", "Training vs Inference Modes": the
     O(1)-per-token recurrent step on a cached state, and training through the
     scan (its gradients: ``selective_scan_bwd``).
+  * The variants: the exact zero-order hold (``zoh=True``; "State-space models
+    (Mamba, S4)", "From Continuous to Discrete: The Key Step"), per-channel B, C
+    (``selective_scan_bcd``, ``state_update_bcd``; the docstring shapes of
+    "Mamba: State Space Models Challenge Transformers", "Selective Scan
+    Algorithm") and their gradients (``selective_scan_bwd(zoh=True)``,
+    ``selective_scan_bcd_bwd``).
+  * The block's input stage, causal conv1d + SiLU, and its gradient
+    (``causal_conv1d_silu``, ``causal_conv1d_silu_bwd``, chained onto the scan by
+    ``selective_scan_conv_bwd``).
+  * Mamba-2's SSD layer (``ssd``; "Mamba: State Space Models Challenge
+    Transformers", "Mamba-2: Improved Architecture", and "State Space Models and
+    Mamba", "Mamba 2 and Hybrid Architectures").
 """
 from __future__ import annotations
 
