@@ -19,7 +19,15 @@ Sources (page title, section):
     Selection" (softplus on delta, output gate y * silu(z)).
   * The gradients of the scan (training through it: "State-space models
     (Mamba, S4)", "Training vs Inference Modes") are pinned to finite
-    differences of the forward and to PyTorch autograd through a plain loop.
+    differences of the forward and to PyTorch autograd through a plain loop;
+    so are those of the variants and of the input stage (autograd through
+    torch.nn.functional.conv1d).
+  * The exact zero-order hold ("State-space models (Mamba, S4)", "From
+    Continuous to Discrete: The Key Step") is pinned to its closed form, to ODE
+    integration (scipy solve_ivp) and to scipy.signal.cont2discrete.
+  * Mamba-2's SSD layer ("State Space Models and Mamba", "Mamba 2 and Hybrid
+    Architectures": a structured matrix multiplication) is pinned to the scan
+    with tied parameters, to the masked matrix form and to its chunked form.
 """
 from __future__ import annotations
 
