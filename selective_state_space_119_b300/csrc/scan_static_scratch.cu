@@ -12,35 +12,25 @@
 // The array is a file-scope __device__ variable: every GPU that loads libssm
 // holds SSM_STATIC_SCRATCH_BYTES of it until the process exits. Host code may
 // not pass the array's name to a kernel (on the host it names a host-side
-// stand-in, not device memory), so its device address is looked up once per
-// device with cudaGetSymbolAddress, with that device current, and cached.
+// stand-in, not device memory), so every call looks up its device address on
+// the current device with cudaGetSymbolAddress. The lookup is host work of a
+// few microseconds; it is not cached, so an address from a context that was
+// torn down (cudaDeviceReset) is never reused.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "ssm.h"
+#include "ssm_internal.h"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_scan_scratch[SSM_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 128;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_scan_scratch on the current device (looked up on the
-// first call for that device, then cached).
+// Device address of g_scan_scratch in the current context.
 int scratch_address(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSM_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_scan_scratch);
-        if (e != cudaSuccess || p == nullptr) return SSM_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_scan_scratch);
+    if (e != cudaSuccess || p == nullptr) return SSM_ERR_CUDA;
+    *out = p;
     return SSM_OK;
 }
 
@@ -66,7 +56,37 @@ extern "C" int ssm_selective_scan_fwd_static(const void* x, const void* delta, c
     }
     // Same validation, plan and kernels as the workspace entry point; only the
     // scratch differs. Nothing in the scratch has to start at zero: every carry
-    // is written before it is read within a call.
+    // is written before it is read within a call, and the status word at its
+    // start is only ever set (by a wait that gave up) and cleared by
+    // ssm_get_static_status.
     return ssm_selective_scan_fwd(x, delta, A, B, C, D, z, delta_bias, delta_softplus, out,
                                   final_state, &d, stream);
+}
+
+// The status word at the start of the library's scratch: the same word a
+// caller workspace holds, read and cleared the same way as ssm_get_device_status.
+extern "C" int ssm_get_static_status(ssm_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SSM_ERR_CUDA;
+    void* p = nullptr;
+    int rc = scratch_address(&p);
+    if (rc != SSM_OK) return rc;
+    uint32_t status = 0;
+    if (cudaMemcpy(&status, p, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (status == 0) return SSM_OK;
+    if (cudaMemset(p, 0, sizeof(status)) != cudaSuccess) return SSM_ERR_CUDA;
+    return -static_cast<int>(status);
+}
+
+// For tests of the failure path on this scratch: the bounded-wait probe of
+// ssm_debug_timeout_probe aimed at the library's status word.
+extern "C" int ssm_debug_timeout_probe_static(uint32_t max_polls, ssm_stream_t stream) {
+    if (max_polls == 0 || max_polls > (1u << 24)) return SSM_ERR_DIMS;
+    void* p = nullptr;
+    const int rc = scratch_address(&p);
+    if (rc != SSM_OK) return rc;
+    const cudaError_t e = ssm::launch_timeout_probe(static_cast<unsigned int*>(p), max_polls,
+                                                    reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }

@@ -114,6 +114,7 @@ int main(void)
     expect(ssm_causal_conv1d_silu(dummy, dummy, NULL, 5, dummy, &d, NULL), SSM_ERR_DIMS,
            "conv width 5");
     expect(ssm_debug_timeout_probe(NULL, 256, 16, NULL), SSM_ERR_NULL, "probe without workspace");
+    expect(ssm_debug_timeout_probe_static(0, NULL), SSM_ERR_DIMS, "static probe without polls");
 
     /* empty problems are no-ops that succeed without any pointer */
     {

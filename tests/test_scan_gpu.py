@@ -172,6 +172,45 @@ def test_impulse_crosses_every_chunk(torch):
     assert np.abs(ry[:, -16:]).max() > 1e-4
 
 
+def _unstructure(A, rows):
+    """A copy of A whose given rows lose the structure A[d, n] = A[d, 0] (n + 1)
+    that selects the power-ladder decay factors: their last entry moves one
+    ulp toward zero (the oracle is given the same A)."""
+    A = np.array(A, dtype=np.float32, copy=True)
+    A[rows, -1] = np.nextafter(A[rows, -1], np.float32(0))
+    return A
+
+
+def _structured(dim, seed):
+    """A[d, n] = a_d (n + 1) in fp32 with a_d = -exp(N(0, 0.5^2)): the
+    structure with a different decay rate per channel."""
+    a = (-np.exp(np.random.default_rng(seed).standard_normal(dim) * 0.5)).astype(np.float32)
+    return a[:, None] * (np.arange(16, dtype=np.float32) + np.float32(1))
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+@pytest.mark.parametrize("hint", [0, 64, 512])
+def test_structured_and_general_decay_paths(torch, hint, io):
+    """The same long-memory inputs through the power-ladder path (A = -(n+1),
+    and a_d (n+1) with a rate per channel), through the general path (one ulp
+    off the structure in every row), and mixed within a CTA (every other warp
+    and the ragged last warp general), each against the oracle; the power
+    ladder and the per-state exponentials agree with each other too."""
+    spec, inp = _small(batch=2, L=1100, dim=264, io=io, delta_lo=1e-4, delta_hi=1e-2,
+                       D_kind="none", gate=False)
+    out_s, _ = G.gpu_scan(inp, False, final_state=False, chunk_len_hint=hint)
+    _check(spec, inp, hint)
+    A_gen = _unstructure(inp["A"], np.arange(spec.dim))
+    out_g, _ = G.gpu_scan(inp, False, final_state=False, chunk_len_hint=hint, A=A_gen)
+    _check(spec, inp, hint, A=A_gen)
+    G.parity(G.host64(out_s), G.host64(out_g), io, "power ladder vs per-state exponentials")
+    mixed = np.r_[32:64, 96:128, 160:192, 224:256, 256:264]
+    _check(spec, inp, hint, A=_unstructure(inp["A"], mixed))
+    A_rate = _structured(spec.dim, 11)
+    _check(spec, inp, hint, A=A_rate)
+    _check(spec, inp, hint, A=_unstructure(A_rate, mixed))
+
+
 @pytest.mark.parametrize("name", ["scan_bf16_b4_L2048_d1536_softplus",
                                   "scan_bf16_b8_L4096_d2048",
                                   "scan_bf16_b1_L131072_d5120"])

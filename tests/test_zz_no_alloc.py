@@ -68,11 +68,37 @@ def test_static_scratch_matches_workspace_entry_point(torch):
 
 def test_static_scratch_refuses_oversized_problems(torch):
     from selective_state_space_119_b300 import libssm
-    # 64 x 255 chunk carries of 4096 channels need far more than 16 MiB
+    # 64 x 255 chunk carries of 4096 channels need far more than 16 MiB; the
+    # buffers are NULL, so no ordering of the checks can reach a launch
     dims = libssm.make_dims(64, 4096, 4096, 16, libssm.SSM_BF16, chunk_len_hint=16)
     assert libssm.lib.ssm_scan_workspace_bytes(ctypes.byref(dims)) > libssm.SSM_STATIC_SCRATCH_BYTES
-    fake = 0x7f0000000000          # never dereferenced: the call is refused first
     rc = libssm.lib.ssm_selective_scan_fwd_static(
-        fake, fake + (1 << 33), fake + (2 << 33), fake + (3 << 33), fake + (4 << 33), None,
-        None, None, 0, fake + (5 << 33), None, ctypes.byref(dims), None)
+        None, None, None, None, None, None, None, None, 0, None, None, ctypes.byref(dims), None)
     assert rc == libssm.SSM_ERR_WORKSPACE
+
+
+def test_static_scratch_reports_a_wait_that_gave_up(torch):
+    """A bounded wait that runs out on the static scratch's status word is
+    reported by ssm_get_static_status (once: reading clears it), and the next
+    static call still matches the workspace entry point."""
+    from selective_state_space_119_b300 import libssm
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert libssm.lib.ssm_get_static_status(stream) == libssm.SSM_OK
+    assert libssm.lib.ssm_debug_timeout_probe_static(1 << 12, stream) == libssm.SSM_OK
+    assert libssm.lib.ssm_get_static_status(stream) == libssm.SSM_ERR_TIMEOUT
+    assert libssm.lib.ssm_get_static_status(stream) == libssm.SSM_OK
+    spec = I.ScanSpec(1, 300, 128, io="bf16", delta_kind="softplus_bias",
+                      A_kind="lognormal", D_kind="uniform", seed=903)
+    inp = I.make_scan_inputs(spec)
+    t = {k: G.dev(v) for k, v in inp.items()}
+    ref_out, _ = libssm.ssm_selective_scan_fwd(
+        t["x"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+        delta_bias=t["delta_bias"], delta_softplus=True, chunk_len_hint=64)
+    out = torch.full_like(t["x"], float("nan"))
+    dims = libssm.make_dims(1, 300, 128, 16, libssm.SSM_BF16, chunk_len_hint=64)
+    rc = libssm.lib.ssm_selective_scan_fwd_static(
+        _vp(t["x"]), _vp(t["delta"]), _vp(t["A"]), _vp(t["B"]), _vp(t["C"]), _vp(t["D"]),
+        _vp(t["z"]), _vp(t["delta_bias"]), 1, _vp(out), None, ctypes.byref(dims), stream)
+    assert rc == 0, libssm.ssm_strerror(rc)
+    assert libssm.lib.ssm_get_static_status(stream) == libssm.SSM_OK
+    G.parity(G.host64(out), G.host64(ref_out), "bf16", "static scratch after a timeout")
