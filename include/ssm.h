@@ -38,7 +38,9 @@
  *  - sizes, plans and errors: ssm_scan_workspace_bytes, ssm_scan_plan,
  *    ssm_scan_checkpoint_bytes, ssm_scan_bwd_workspace_bytes,
  *    ssm_get_device_status, ssm_strerror, ssm_last_cuda_error, ssm_version;
- *  - a test of the failure path: ssm_debug_timeout_probe.
+ *  - Mamba-2's SSD layer: ssm_ssd_fwd (tensor cores), ssm_ssd_workspace_bytes,
+ *    ssm_ssd_get_device_status;
+ *  - tests of the failure path: ssm_debug_timeout_probe, _static.
  *
  * Conventions for every entry point:
  *  - All tensors are contiguous, row-major, in DEVICE memory, caller-owned.
@@ -293,6 +295,50 @@ int ssm_state_update(float* state, const void* x, const void* delta, const float
                      const float* delta_bias, int delta_softplus, void* out,
                      const ssm_dims* dims, ssm_stream_t stream);
 
+/*
+ * ssm_ssd_fwd -- Mamba-2's SSD layer ("Mamba: State Space Models Challenge
+ * Transformers", "Mamba-2: Improved Architecture": a multi-head structure, the
+ * pages' sizes n_heads 8, d_head 64, d_state 128; "State Space Models and
+ * Mamba", "Mamba 2 and Hybrid Architectures": the SSM as a structured matrix
+ * multiplication). Per batch row b and head hd, with one scalar decay per head
+ * and one step per token shared by the head's d_head channels:
+ *
+ *     dt_t = dt[b,t,hd] (+ dt_bias[hd])  (then softplus, if asked)
+ *     h_t  = exp(dt_t A[hd]) h_{t-1} + dt_t x[b,t,hd,:] B[b,t,g,:]^T   (h: [P, N])
+ *     y[b,t,hd,:] = h_t C[b,t,g,:] + D[hd] x[b,t,hd,:]
+ *
+ * where head hd reads group g = hd / (nheads / ngroups). Layouts (row-major):
+ *   x, y            : [batch, seqlen, nheads, headdim] bf16
+ *   dt              : [batch, seqlen, nheads] bf16
+ *   A, D, dt_bias   : [nheads] fp32 (D, dt_bias may be NULL)
+ *   B, C            : [batch, seqlen, ngroups, dstate] bf16
+ *   h0, final_state : [batch, nheads, headdim, dstate] fp32 (h0 NULL = zero;
+ *                     final_state may be NULL)
+ * Supported: io_dtype SSM_BF16, headdim 64, dstate 128, ngroups dividing
+ * nheads (SSM_ERR_DIMS / SSM_ERR_DTYPE otherwise). The products run on the
+ * tensor cores with fp32 accumulation; operands the kernel forms itself are
+ * carried as a bf16 pair (high part + remainder). dims->workspace must hold
+ * ssm_ssd_workspace_bytes(dims) (256) bytes, zero-filled once: its first word
+ * is the status word that ssm_ssd_get_device_status reads (SSM_ERR_TIMEOUT
+ * when a bounded wait gave up). Pointers 16-byte aligned; y and final_state
+ * must not overlap an input. Enqueues one kernel on `stream`.
+ */
+typedef struct {
+    int64_t batch, seqlen, nheads, headdim, ngroups, dstate;
+    int32_t io_dtype;
+    int32_t flags;          /* 0 */
+    void* workspace;
+    size_t workspace_bytes;
+} ssm_ssd_dims;
+
+size_t ssm_ssd_workspace_bytes(const ssm_ssd_dims* dims);
+int ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                const float* D, const float* dt_bias, int dt_softplus, const float* h0,
+                void* y, float* final_state, const ssm_ssd_dims* dims, ssm_stream_t stream);
+/* Synchronizes `stream`, then reads and clears the status word of the SSD
+ * workspace (as ssm_get_device_status does for the scan). */
+int ssm_ssd_get_device_status(const ssm_ssd_dims* dims, ssm_stream_t stream);
+
 /* Size of the library-owned scratch used by ssm_selective_scan_fwd_static. */
 #define SSM_STATIC_SCRATCH_BYTES (16u << 20)
 
@@ -315,18 +361,32 @@ int ssm_state_update(float* state, const void* x, const void* delta, const float
  * ssm_selective_scan_fwd with a workspace, or a larger chunk_len_hint, which
  * needs fewer carries). The call allocates nothing.
  *
- * The first call on each device looks up the array's device address (with
- * that device current) and caches it; make that first call before any stream
- * capture. Every call on a device shares the one array, which keeps the last
- * call's contents (nothing in it has to start at zero): calls that can overlap
- * on the GPU -- on different streams, or from different host threads -- race
- * on it and must be serialized by the caller.
+ * Every call looks up the array's device address in the current context
+ * (cudaGetSymbolAddress; nothing is cached, so a context torn down and
+ * recreated is handled). The first call on a device may load the library's
+ * device code into that context: make it before any stream capture. Every call
+ * on a device shares the one array, which keeps the last call's contents
+ * (nothing in it has to start at zero): calls that can overlap on the GPU --
+ * on different streams, or from different host threads -- race on it and must
+ * be serialized by the caller.
+ *
+ * Device-side failures: the array starts with the same status word a caller
+ * workspace holds. A bounded wait inside a scan kernel that gives up sets it
+ * (the call's outputs are then undefined); ssm_get_static_status reads and
+ * clears it. ssm_get_device_status does not apply to this entry point.
  */
 int ssm_selective_scan_fwd_static(const void* x, const void* delta, const float* A,
                                   const void* B, const void* C, const float* D,
                                   const void* z, const float* delta_bias, int delta_softplus,
                                   void* out, float* final_state, const ssm_dims* dims,
                                   ssm_stream_t stream);
+
+/* Synchronizes `stream`, then reads the status word of the scratch of
+ * ssm_selective_scan_fwd_static on the current device: SSM_OK, or
+ * SSM_ERR_TIMEOUT when a bounded wait inside a scan kernel running on that
+ * scratch gave up since the word was last read. Reading a nonzero word clears
+ * it. Allocates nothing. */
+int ssm_get_static_status(ssm_stream_t stream);
 
 /* Bytes of workspace ssm_selective_scan_fwd needs for these sizes (256 when
  * the scan runs in one pass, 0 for empty problems). Depends only on batch,
@@ -358,6 +418,11 @@ int ssm_scan_plan(const ssm_dims* dims, ssm_plan* plan);
  */
 int ssm_debug_timeout_probe(void* workspace, size_t workspace_bytes, uint32_t max_polls,
                             ssm_stream_t stream);
+
+/* The same probe aimed at the status word of the scratch of
+ * ssm_selective_scan_fwd_static on the current device; the next
+ * ssm_get_static_status returns SSM_ERR_TIMEOUT. */
+int ssm_debug_timeout_probe_static(uint32_t max_polls, ssm_stream_t stream);
 
 /* Synchronizes `stream`, then reads the device-side status word of the
  * workspace: SSM_OK, or SSM_ERR_TIMEOUT when a bounded wait inside a scan

@@ -350,7 +350,29 @@ int scan_impl(const void* x, const void* delta, const float* A, const void* B, c
         a.ws_S = reinterpret_cast<float*>(ws + p.ws_off_S);
     }
     if (bc_per_channel) return set_cuda(ssm::launch_scan_bcd(a, p, dims->io_dtype, s));
+    // dstate 16 on the planner's own tile: the one-lane-per-channel kernel
+    if (N == 16 && dims->tile_config_hint == 0 && !cv.w && !ckpt && !a.zoh)
+        return set_cuda(ssm::launch_scan16(a, p, dims->io_dtype, s));
     return set_cuda(ssm::launch_scan(a, p, dims->io_dtype, static_cast<int>(N), s));
+}
+
+}  // namespace
+
+namespace {
+
+int check_ssd(const ssm_ssd_dims* d) {
+    if (!d) return SSM_ERR_NULL;
+    if (d->io_dtype != SSM_BF16) return d->io_dtype == SSM_F32 ? SSM_ERR_DIMS : SSM_ERR_DTYPE;
+    if (d->batch < 0 || d->seqlen < 0 || d->nheads <= 0 || d->ngroups <= 0) return SSM_ERR_DIMS;
+    if (d->headdim != 64 || d->dstate != 128 || d->nheads % d->ngroups != 0) return SSM_ERR_DIMS;
+    if (d->flags != 0) return SSM_ERR_DIMS;
+    if (d->batch >= kMaxDim || d->seqlen >= kMaxDim || d->nheads >= (int64_t(1) << 20))
+        return SSM_ERR_DIMS;
+    if (d->batch * d->nheads >= (int64_t(1) << 31)) return SSM_ERR_DIMS;
+    if (d->batch > 0 && d->seqlen > 0 &&
+        d->batch * d->seqlen > kMaxElems / (d->nheads * d->headdim))
+        return SSM_ERR_DIMS;
+    return SSM_OK;
 }
 
 }  // namespace
@@ -576,6 +598,76 @@ int ssm_debug_timeout_probe(void* workspace, size_t workspace_bytes, uint32_t ma
     if (max_polls < 1 || max_polls > (1u << 24)) return SSM_ERR_DIMS;
     return set_cuda(ssm::launch_timeout_probe(static_cast<unsigned int*>(workspace), max_polls,
                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t ssm_ssd_workspace_bytes(const ssm_ssd_dims* dims) {
+    return check_ssd(dims) == SSM_OK ? ssm::kWsHeaderBytes : 0;
+}
+
+int ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                const float* D, const float* dt_bias, int dt_softplus, const float* h0,
+                void* y, float* final_state, const ssm_ssd_dims* dims, ssm_stream_t stream) {
+    int rc = check_ssd(dims);
+    if (rc != SSM_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t b = dims->batch, L = dims->seqlen, H = dims->nheads, G = dims->ngroups;
+    const int64_t P = dims->headdim, N = dims->dstate;
+    if (b == 0) return SSM_OK;
+    const size_t state_bytes = size_t(b) * size_t(H) * size_t(P) * size_t(N) * 4;
+    if (L == 0) {
+        if (!final_state) return SSM_OK;
+        if (!aligned16(final_state) || (h0 && !aligned16(h0))) return SSM_ERR_ALIGN;
+        if (h0 && overlap({h0, state_bytes}, {final_state, state_bytes})) return SSM_ERR_ALIAS;
+        return set_cuda(h0 ? cudaMemcpyAsync(final_state, h0, state_bytes,
+                                             cudaMemcpyDeviceToDevice, s)
+                           : cudaMemsetAsync(final_state, 0, state_bytes, s));
+    }
+    if (!x || !dt || !A || !B || !C || !y) return SSM_ERR_NULL;
+    {
+        const void* const ptrs[] = {x, dt, A, B, C, D, dt_bias, h0, y, final_state,
+                                    dims->workspace};
+        rc = check_aligned(ptrs);
+        if (rc != SSM_OK) return rc;
+    }
+    if (!dims->workspace || dims->workspace_bytes < ssm::kWsHeaderBytes) return SSM_ERR_WORKSPACE;
+    const size_t xe = size_t(b) * size_t(L) * size_t(H) * size_t(P) * 2;
+    const size_t re = size_t(b) * size_t(L) * size_t(G) * size_t(N) * 2;
+    {
+        const Range in[] = {{x, xe},
+                            {dt, size_t(b) * size_t(L) * size_t(H) * 2},
+                            {A, size_t(H) * 4},
+                            {B, re},
+                            {C, re},
+                            {D, size_t(H) * 4},
+                            {dt_bias, size_t(H) * 4},
+                            {h0, state_bytes},
+                            {dims->workspace, ssm::kWsHeaderBytes}};
+        const Range outs[] = {{y, xe}, {final_state, state_bytes}};
+        rc = check_alias(in, outs);
+        if (rc != SSM_OK) return rc;
+    }
+    ssm::SsdLaunch l{};
+    l.x = x; l.dt = dt; l.A = A; l.B = B; l.C = C; l.D = D; l.dt_bias = dt_bias;
+    l.softplus = dt_softplus ? 1 : 0; l.h0 = h0; l.y = y; l.final_state = final_state;
+    l.batch = b; l.L = L; l.H = H; l.G = G;
+    l.status = static_cast<unsigned int*>(dims->workspace);
+    return set_cuda(ssm::launch_ssd(l, s));
+}
+
+int ssm_ssd_get_device_status(const ssm_ssd_dims* dims, ssm_stream_t stream) {
+    const int rc0 = check_ssd(dims);
+    if (rc0 != SSM_OK) return rc0;
+    int rc = set_cuda(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+    if (rc != SSM_OK) return rc;
+    if (!dims->workspace || dims->workspace_bytes < sizeof(uint32_t)) return SSM_ERR_WORKSPACE;
+    uint32_t status = 0;
+    rc = set_cuda(cudaMemcpy(&status, dims->workspace, sizeof(status), cudaMemcpyDeviceToHost));
+    if (rc != SSM_OK) return rc;
+    if (status != 0) {
+        rc = set_cuda(cudaMemset(dims->workspace, 0, sizeof(status)));
+        if (rc != SSM_OK) return rc;
+    }
+    return status == 0 ? SSM_OK : -static_cast<int>(status);
 }
 
 int ssm_get_device_status(const ssm_dims* dims, ssm_stream_t stream) {

@@ -1,0 +1,460 @@
+// ssd.cu -- Mamba-2's SSD layer on the tensor cores (tcgen05), sm_103a.
+//
+// The layer ("Mamba: State Space Models Challenge Transformers", "Mamba-2:
+// Improved Architecture": heads of d_head channels with a d_state-wide state
+// each; "State Space Models and Mamba", "Mamba 2 and Hybrid Architectures":
+// the SSM recast as a structured matrix multiplication). Per batch row b and
+// head hd, with one scalar decay A[hd], one step dt[b,t,hd] per token shared
+// by the head's P channels and B, C rows of the head's group g:
+//   h_t = exp(dt_t A) h_{t-1} + dt_t x_t B_t^T     (h: [P, N])
+//   y_t = h_t C_t + D x_t
+// Because the decay is a scalar per head, a chunk of Q tokens is a few dense
+// products. With s_t = A * (dt_0 + ... + dt_t) inside the chunk and h_in the
+// state entering it:
+//   G  = C B^T                                  [Q x Q]   (K = N)
+//   M  = G o (exp(s_t - s_u) dt_u)_{u <= t}     masked decay, CUDA cores
+//   Y  = M X + diag(exp(s_t)) C h_in^T + D X    [Q x P]   (K = Q, then K = N)
+//   S  = (w o X)^T B,  w_u = exp(s_Q - s_u) dt_u          (K = Q)
+//   h_out = exp(s_Q) h_in + S
+// This kernel runs one CTA per (batch row, head) over the chunks in order,
+// the state in fp32 registers. Per chunk TMA (cp.async.bulk.tensor, 128-byte
+// swizzle) brings the C, B and X tiles; one thread issues the tcgen05.mma
+// products into tensor memory; the CTA's 128 threads (thread t owns row t of
+// every [Q x .] accumulator, thread n row n of S^T) form M, w o X and the
+// epilogue on the CUDA cores. Operands that the CUDA cores produce (M, w o X
+// and h) are split into a bf16 high part and a bf16 remainder, two products
+// each, so that every product carries about 16 significant bits more than one
+// bf16 rounding would.
+//
+// Sizes: Q = 128 tokens per chunk, P = 64 (d_head), N = 128 (d_state), bf16
+// x, dt, B, C, y; fp32 A, D, dt_bias, h0, final state.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+#include "ssm_tc.cuh"
+#include "ssm_tma.cuh"
+#include "ssm_tmap.h"
+
+namespace ssm {
+namespace {
+
+constexpr int kQ = 128;     // tokens per chunk
+constexpr int kP = 64;      // channels per head
+constexpr int kNs = 128;    // state width
+constexpr int kThreads = 128;
+constexpr uint32_t kPolls = 1u << 24;
+constexpr uint32_t kStatusTimeout = 7;
+
+// shared memory (byte offsets from a 1024-aligned base)
+constexpr int kBlk = kQ * 128;                 // one [128 rows x 64] bf16 block: 16 KB
+constexpr int oC = 0;                          // C tile: rows t, K = n (2 blocks)
+constexpr int oB = oC + 2 * kBlk;              // B tile: rows u, n (2 blocks)
+constexpr int oX = oB + 2 * kBlk;              // X tile: rows u, p (1 block); y in place
+constexpr int oMh = oX + kBlk;                 // M high: rows t, K = u (2 blocks)
+constexpr int oMl = oMh + 2 * kBlk;            // M remainder
+constexpr int oWh = oMl + 2 * kBlk;            // w o X high: rows u, p
+constexpr int oWl = oWh + kBlk;
+constexpr int oHh = oWl + kBlk;                // h high: rows n, p
+constexpr int oHl = oHh + kBlk;
+constexpr int oDt = oHl + kBlk;                // dt [Q] f32
+constexpr int oS2 = oDt + kQ * 4;              // s log2 e [Q] f32
+constexpr int oWs = oS2 + kQ * 4;              // warp partial sums [4] f32
+constexpr int oBar = oWs + 64;                 // mbarriers: load, mma
+constexpr int oTm = oBar + 16;                 // TMEM base address
+constexpr int kSmemUsed = oTm + 16;
+constexpr int kSmemBytes = kSmemUsed + 1024;   // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+
+// TMEM columns: G [0, 128), Y [128, 192), Y2 [192, 256), S^T [256, 320)
+constexpr uint32_t kColG = 0, kColY = 128, kColY2 = 192, kColS = 256, kTmemCols = 512;
+
+constexpr uint32_t kIdG = tc::idesc_bf16(128, kQ, false, false);   // C (K-major) B^T (K-major)
+constexpr uint32_t kIdS = tc::idesc_bf16(128, kP, true, true);     // B^T (MN-major) wX (MN-major)
+constexpr uint32_t kIdY = tc::idesc_bf16(128, kP, false, true);    // M (K-major) X (MN-major)
+
+struct SsdArgs {
+    const void* dt;           // [batch, L, H] bf16
+    const float* A;           // [H]
+    const float* D;           // [H] or NULL
+    const float* dt_bias;     // [H] or NULL
+    int softplus;
+    const float* h0;          // [batch, H, P, N] or NULL
+    float* final_state;       // [batch, H, P, N] or NULL
+    int64_t batch, L, H, G;
+    unsigned int* status;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ float bf16_round(float v) {
+    return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// Row r of a [128 x 64] swizzled block holds 64 values; write 8 of them (one
+// 16-byte chunk, columns 8c .. 8c+7) as bf16 high parts and remainders.
+__device__ __forceinline__ void put8_split(unsigned char* hi, unsigned char* lo, uint32_t r,
+                                           uint32_t c, const float (&v)[8]) {
+    float h[8], l[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        h[i] = bf16_round(v[i]);
+        l[i] = v[i] - h[i];
+    }
+    const uint32_t off = tc::sw128(r, 8 * c);
+    *reinterpret_cast<uint4*>(hi + off) =
+        make_uint4(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]), pack_bf16(h[4], h[5]),
+                   pack_bf16(h[6], h[7]));
+    *reinterpret_cast<uint4*>(lo + off) =
+        make_uint4(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]), pack_bf16(l[4], l[5]),
+                   pack_bf16(l[6], l[7]));
+}
+
+__device__ __forceinline__ void get8(const unsigned char* blk, uint32_t r, uint32_t c, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(blk + tc::sw128(r, 8 * c));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* tm, int c0, int c1, int c2,
+                                            int c3, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* tm, int c0, int c1, int c2, int c3,
+                                             const void* src) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+            reinterpret_cast<uint64_t>(tm)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(src))
+        : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
+           const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_y,
+           const SsdArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    // the swizzled tiles need 1024-byte aligned shared-memory addresses
+    const uint32_t s_raw = smem_u32(smem_raw);
+    unsigned char* sm = smem_raw + (((s_raw + 1023u) & ~1023u) - s_raw);
+    float* sdt = reinterpret_cast<float*>(sm + oDt);
+    float* ss2 = reinterpret_cast<float*>(sm + oS2);
+    float* swarp = reinterpret_cast<float*>(sm + oWs);
+    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + oBar);
+    uint64_t* bar_mma = bar_ld + 1;
+    uint32_t* tm_slot = reinterpret_cast<uint32_t*>(sm + oTm);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t b = blockIdx.x / a.H, hd = blockIdx.x % a.H;
+    const int64_t g = hd / (a.H / a.G);
+    const int nchunks = static_cast<int>((a.L + kQ - 1) / kQ);
+    const float A2 = __ldg(a.A + hd) * kLog2e;
+    const float Dh = a.D ? __ldg(a.D + hd) : 0.f;
+    const float bias = a.dt_bias ? __ldg(a.dt_bias + hd) : 0.f;
+    const uint32_t sbase = smem_u32(sm);
+
+    if (tid == 0) {
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tm_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tm_slot;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;   // this warp's TMEM lanes
+
+    // the state: thread n holds h[p][n] for p = 0 .. 63 (fp32), and writes it
+    // as the MN-major operand [n rows x p] of C h^T
+    float h[kP];
+    {
+        const int n = tid;
+#pragma unroll
+        for (int p = 0; p < kP; ++p)
+            h[p] = a.h0 ? a.h0[(((b * a.H + hd) * kP) + p) * kNs + n] : 0.f;
+#pragma unroll
+        for (int c = 0; c < kP / 8; ++c) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = h[8 * c + i];
+            put8_split(sm + oHh, sm + oHl, n, c, v);
+        }
+    }
+
+    uint32_t ld_phase = 0, mma_phase = 0;
+    bool ok = true, load_pending = false;
+    for (int c = 0; c < nchunks && ok; ++c) {
+        const int t0 = c * kQ;
+        if (tid == 0) {
+            mbar_arrive_expect_tx(bar_ld, 2 * 2 * kBlk + kBlk);
+            const int gg = static_cast<int>(g), bb = static_cast<int>(b);
+            tma_load_4d(sm + oC, &tm_C, 0, gg, t0, bb, bar_ld);
+            tma_load_4d(sm + oC + kBlk, &tm_C, 64, gg, t0, bb, bar_ld);
+            tma_load_4d(sm + oB, &tm_B, 0, gg, t0, bb, bar_ld);
+            tma_load_4d(sm + oB + kBlk, &tm_B, 64, gg, t0, bb, bar_ld);
+            tma_load_4d(sm + oX, &tm_x, 0, static_cast<int>(hd), t0, bb, bar_ld);
+            load_pending = true;
+        }
+        // dt of the chunk (0 past the sequence end), then s = A * cumsum(dt)
+        {
+            const int64_t t = t0 + tid;
+            float v = 0.f;
+            if (t < a.L) {
+                v = IO<__nv_bfloat16>::ld(static_cast<const __nv_bfloat16*>(a.dt) +
+                                          (b * a.L + t) * a.H + hd) + bias;
+                if (a.softplus) v = softplus(v);
+            }
+            sdt[tid] = v;
+            float cs = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_up_sync(0xffffffffu, cs, o);
+                if (lane >= o) cs += u;
+            }
+            if (lane == 31) swarp[warp] = cs;
+            __syncthreads();
+            for (int w = 0; w < warp; ++w) cs += swarp[w];
+            ss2[tid] = cs * A2;   // s_t log2 e
+        }
+        // (the next read of swarp is a chunk later, after several barriers)
+        ok = mbar_wait_bounded(bar_ld, ld_phase, kPolls);
+        if (ok) load_pending = false;
+        ld_phase ^= 1;
+        __syncthreads();   // ss2 complete
+        const float s_end = ss2[kQ - 1];
+        // w o X (high and remainder), row u = this thread, w_u = exp(s_end - s_u) dt_u
+        {
+            const int u = tid;
+            const float w = ex2(s_end - ss2[u]) * sdt[u];
+#pragma unroll
+            for (int cc = 0; cc < kP / 8; ++cc) {
+                float v[8];
+                get8(sm + oX, u, cc, v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] *= w;
+                put8_split(sm + oWh, sm + oWl, u, cc, v);
+            }
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        ok = !__syncthreads_or(!ok);
+        tc::fence_after_sync();
+        if (ok && tid == 0) {
+            // G = C B^T: 8 steps of K = 16 over the two 64-wide n blocks
+#pragma unroll
+            for (int k = 0; k < kNs / 16; ++k) {
+                const uint32_t off = (k >> 2) * kBlk + (k & 3) * 32;
+                tc::mma_bf16(tmem + kColG, tc::desc_sw128(sbase + oC + off, 16, 1024),
+                             tc::desc_sw128(sbase + oB + off, 16, 1024), kIdG, k > 0);
+            }
+            // S^T = B^T (w o X): A = the B tile read MN-major (M = n over two
+            // 64-wide blocks 16 KB apart), B = w o X MN-major; K = u in steps of 16 rows
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                const uint32_t wx = sbase + (part ? oWl : oWh);
+#pragma unroll
+                for (int k = 0; k < kQ / 16; ++k) {
+                    const uint32_t off = k * 2048;
+                    tc::mma_bf16(tmem + kColS, tc::desc_sw128(sbase + oB + off, kBlk, 1024),
+                                 tc::desc_sw128(wx + off, 1024, 1024), kIdS, part > 0 || k > 0);
+                }
+            }
+            tc::mma_commit(bar_mma);
+        }
+        ok = ok && mbar_wait_bounded(bar_mma, mma_phase, kPolls);
+        mma_phase ^= 1;
+        tc::fence_after_sync();
+        // M = G o decay o dt (row t = this thread), high and remainder
+        {
+            const int t = tid;
+            const float st = ss2[t];
+#pragma unroll
+            for (int q = 0; q < kQ / 32; ++q) {
+                float gv[32];
+                tc::tmem_ld32(tmem + lane_base + kColG + 32 * q, gv);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    float v[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int u = 32 * q + 8 * cc + i;
+                        v[i] = u <= t ? gv[8 * cc + i] * sdt[u] * ex2(st - ss2[u]) : 0.f;
+                    }
+                    const int ublk = (32 * q) / 64;              // which 64-wide u block
+                    const int cch = ((32 * q) % 64) / 8 + cc;     // 16-byte chunk in the row
+                    put8_split(sm + oMh + ublk * kBlk, sm + oMl + ublk * kBlk, t, cch, v);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        ok = !__syncthreads_or(!ok);
+        tc::fence_after_sync();
+        if (ok && tid == 0) {
+            // Y = M X: A = M (K-major, K = u over two blocks), B = X MN-major
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                const uint32_t m = sbase + (part ? oMl : oMh);
+#pragma unroll
+                for (int k = 0; k < kQ / 16; ++k) {
+                    const uint32_t offa = (k >> 2) * kBlk + (k & 3) * 32;
+                    tc::mma_bf16(tmem + kColY, tc::desc_sw128(m + offa, 16, 1024),
+                                 tc::desc_sw128(sbase + oX + k * 2048, 1024, 1024), kIdY,
+                                 part > 0 || k > 0);
+                }
+            }
+            // Y2 = C h^T: A = C (K-major, K = n), B = h MN-major (rows n)
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                const uint32_t hb = sbase + (part ? oHl : oHh);
+#pragma unroll
+                for (int k = 0; k < kNs / 16; ++k) {
+                    const uint32_t offa = (k >> 2) * kBlk + (k & 3) * 32;
+                    tc::mma_bf16(tmem + kColY2, tc::desc_sw128(sbase + oC + offa, 16, 1024),
+                                 tc::desc_sw128(hb + k * 2048, 1024, 1024), kIdY,
+                                 part > 0 || k > 0);
+                }
+            }
+            tc::mma_commit(bar_mma);
+        }
+        ok = ok && mbar_wait_bounded(bar_mma, mma_phase, kPolls);
+        mma_phase ^= 1;
+        tc::fence_after_sync();
+        // epilogue: y = Y + exp(s_t) Y2 + D x (row t), in place over x;
+        // state: h <- exp(s_end) h + S (row n = this thread)
+        {
+            const int t = tid;
+            const float et = ex2(ss2[t]);
+#pragma unroll
+            for (int q = 0; q < kP / 32; ++q) {
+                float yv[32], y2[32];
+                tc::tmem_ld32(tmem + lane_base + kColY + 32 * q, yv);
+                tc::tmem_ld32(tmem + lane_base + kColY2 + 32 * q, y2);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    float xv[8];
+                    const int ch = 4 * q + cc;
+                    get8(sm + oX, t, ch, xv);
+                    float o[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        o[i] = fmaf(Dh, xv[i], fmaf(et, y2[8 * cc + i], yv[8 * cc + i]));
+                    *reinterpret_cast<uint4*>(sm + oX + tc::sw128(t, 8 * ch)) =
+                        make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
+                                   pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
+                }
+            }
+            const float eend = ex2(s_end);
+#pragma unroll
+            for (int q = 0; q < kP / 32; ++q) {
+                float sv[32];
+                tc::tmem_ld32(tmem + lane_base + kColS + 32 * q, sv);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) h[32 * q + i] = fmaf(eend, h[32 * q + i], sv[i]);
+            }
+#pragma unroll
+            for (int cc = 0; cc < kP / 8; ++cc) {
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = h[8 * cc + i];
+                put8_split(sm + oHh, sm + oHl, tid, cc, v);
+            }
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        ok = !__syncthreads_or(!ok);
+        tc::fence_after_sync();
+        if (ok && tid == 0) {
+            tma_store_4d(&tm_y, 0, static_cast<int>(hd), t0, static_cast<int>(b), sm + oX);
+            bulk_commit();
+            bulk_wait_read<0>();   // the X tile is reloaded by the next chunk
+        }
+        __syncthreads();
+    }
+    if (tid == 0) bulk_wait_all();
+    if (!ok) {
+        if (tid == 0) {
+            // let a load in flight land before the CTA releases its memory
+            if (load_pending) mbar_wait_bounded(bar_ld, ld_phase ^ 1, kPolls);
+            if (a.status) atomicExch(a.status, kStatusTimeout);
+        }
+    } else if (a.final_state) {
+        const int n = tid;
+#pragma unroll
+        for (int p = 0; p < kP; ++p)
+            a.final_state[(((b * a.H + hd) * kP) + p) * kNs + n] = h[p];
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// 4-D [batch][L][rows][64k] bf16 tensor map with a 128-byte swizzle and a box
+// of 64 x 1 x 128 x 1 (rows = heads or groups; inner = channels or states).
+cudaError_t make_tmap4(CUtensorMap* tm, const void* base, int64_t batch, int64_t L, int64_t rows,
+                       int64_t inner) {
+    EncodeTiled fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t gdim[4] = {cuuint64_t(inner), cuuint64_t(rows), cuuint64_t(L), cuuint64_t(batch)};
+    const cuuint64_t gstride[3] = {cuuint64_t(inner) * 2, cuuint64_t(rows * inner) * 2,
+                                   cuuint64_t(L * rows * inner) * 2};
+    const cuuint32_t box[4] = {64, 1, cuuint32_t(kQ), 1};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gdim,
+                          gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_ssd(const SsdLaunch& l, cudaStream_t s) {
+    static std::mutex mu;
+    static bool done[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            e = cudaFuncSetAttribute(ssd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemBytes);
+            if (e != cudaSuccess) return e;
+            done[dev] = true;
+        }
+    }
+    CUtensorMap tx, tB, tC, ty;
+    if ((e = make_tmap4(&tx, l.x, l.batch, l.L, l.H, kP)) != cudaSuccess) return e;
+    if ((e = make_tmap4(&ty, l.y, l.batch, l.L, l.H, kP)) != cudaSuccess) return e;
+    if ((e = make_tmap4(&tB, l.B, l.batch, l.L, l.G, kNs)) != cudaSuccess) return e;
+    if ((e = make_tmap4(&tC, l.C, l.batch, l.L, l.G, kNs)) != cudaSuccess) return e;
+    SsdArgs a{};
+    a.dt = l.dt; a.A = l.A; a.D = l.D; a.dt_bias = l.dt_bias; a.softplus = l.softplus;
+    a.h0 = l.h0; a.final_state = l.final_state;
+    a.batch = l.batch; a.L = l.L; a.H = l.H; a.G = l.G; a.status = l.status;
+    ssd_kernel<<<static_cast<unsigned>(l.batch * l.H), kThreads, kSmemBytes, s>>>(tx, tB, tC, ty, a);
+    return cudaGetLastError();
+}
+
+}  // namespace ssm

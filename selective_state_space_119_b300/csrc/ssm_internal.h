@@ -141,12 +141,33 @@ struct BwdArgs {
 
 // Enqueue one full scan (all phases). io: 0 = fp32, 1 = bf16.
 cudaError_t launch_scan(const ScanArgs& a, const ScanPlan& p, int io, int N, cudaStream_t s);
+// The same for dstate 16 with 128-channel tiles and no fused input stage,
+// checkpoints or variant (one lane per channel, structured-A fast path).
+cudaError_t launch_scan16(const ScanArgs& a, const ScanPlan& p, int io, cudaStream_t s);
 // Enqueue one decode step.
 cudaError_t launch_state_update(const StepArgs& a, int io, int N, cudaStream_t s);
 // Enqueue the scan with per-channel B and C ([batch][L][dim][N], dstate 16).
 cudaError_t launch_scan_bcd(const ScanArgs& a, const ScanPlan& p, int io, cudaStream_t s);
 // Enqueue the gradient passes (reverse carries, gradients, reduction).
 cudaError_t launch_scan_bwd(const BwdArgs& a, int io, cudaStream_t s);
+// Mamba-2's SSD layer (bf16 I/O, d_head 64, d_state 128): one launch.
+struct SsdLaunch {
+    const void* x;            // [batch, L, H, 64] bf16
+    const void* dt;           // [batch, L, H] bf16
+    const float* A;           // [H]
+    const void* B;            // [batch, L, G, 128] bf16
+    const void* C;
+    const float* D;           // [H] or NULL
+    const float* dt_bias;     // [H] or NULL
+    int softplus;
+    const float* h0;          // [batch, H, 64, 128] or NULL
+    void* y;                  // [batch, L, H, 64] bf16
+    float* final_state;       // [batch, H, 64, 128] or NULL
+    int64_t batch, L, H, G;
+    unsigned int* status;     // workspace status word
+};
+cudaError_t launch_ssd(const SsdLaunch& l, cudaStream_t s);
+
 // Enqueue the failure-path probe: a bounded wait that runs out and sets *status.
 cudaError_t launch_timeout_probe(unsigned int* status, uint32_t max_polls, cudaStream_t s);
 // Enqueue the standalone causal depthwise conv1d + SiLU.

@@ -161,6 +161,33 @@ WORKLOADS: Dict[str, object] = {
 }
 
 
+@dataclasses.dataclass(frozen=True)
+class SsdSpec:
+    """One Mamba-2 SSD workload: x [batch, L, H, P], dt [batch, L, H], B, C
+    [batch, L, G, N]. dt = softplus(u + bias) with u ~ N(0, 0.5^2) and
+    softplus(bias[hd]) log-uniform in [dt_lo, dt_hi]; A[hd] = -U(1, 16); x, B,
+    C ~ N(0, 1); D ~ U(0.5, 1.5); h0 (when drawn) ~ N(0, 1)."""
+    batch: int
+    L: int
+    H: int = 8
+    P: int = 64
+    G: int = 1
+    N: int = 128
+    dt_lo: float = 1e-3
+    dt_hi: float = 1e-1
+    seed: int = 0
+
+    @property
+    def elements(self) -> int:
+        return self.batch * self.L * self.H * self.P
+
+
+# The SSD layer at the pages' Mamba-2 sizes (8 heads of 64 channels, d_state 128).
+SSD_WORKLOADS: Dict[str, SsdSpec] = {
+    "ssd_bf16_b16_L8192_h8_p64_n128": SsdSpec(16, 8192, seed=1101),
+}
+
+
 def _loguniform(rng, lo, hi, size):
     return np.exp(np.log(lo) + (np.log(hi) - np.log(lo)) * rng.random(size))
 
@@ -322,4 +349,34 @@ def algorithmic_bytes_decode_step(spec: DecodeSpec) -> int:
     total += spec.dim * spec.N * 4
     if spec.D_kind != "none":
         total += spec.dim * 4
+    return total
+
+
+def make_ssd_inputs(spec: SsdSpec, with_h0: bool = False,
+                    seed: Optional[int] = None) -> Dict[str, np.ndarray]:
+    """Draw one set of SSD inputs (x, dt, B, C as bf16 bits; A, D, dt_bias fp32;
+    h0 fp32 or None). Draw order: x, dt (u), bias, A, B, C, D, h0."""
+    rng = np.random.Generator(np.random.PCG64(spec.seed if seed is None else seed))
+    b, L, H, P, G, N = spec.batch, spec.L, spec.H, spec.P, spec.G, spec.N
+    out: Dict[str, Optional[np.ndarray]] = {}
+    out["x"] = _normal_chunked(rng, (b, L, H, P), 1.0, "bf16")
+    out["dt"] = _normal_chunked(rng, (b, L, H), 0.5, "bf16")
+    s = _loguniform(rng, spec.dt_lo, spec.dt_hi, H)
+    out["dt_bias"] = np.log(np.expm1(s)).astype(np.float32)
+    out["A"] = (-rng.uniform(1.0, 16.0, H)).astype(np.float32)
+    out["B"] = _normal_chunked(rng, (b, L, G, N), 1.0, "bf16")
+    out["C"] = _normal_chunked(rng, (b, L, G, N), 1.0, "bf16")
+    out["D"] = rng.uniform(0.5, 1.5, H).astype(np.float32)
+    out["h0"] = rng.standard_normal((b, H, P, N)).astype(np.float32) if with_h0 else None
+    return out
+
+
+def algorithmic_bytes_ssd(spec: SsdSpec, final_state: bool = True) -> int:
+    """Bytes the SSD layer must move at least once: x read and y written per
+    element, dt per (b, t, head), B and C per (b, t, group), A, D, bias once,
+    the final state written."""
+    b, L, H, P, G, N = spec.batch, spec.L, spec.H, spec.P, spec.G, spec.N
+    total = 2 * b * L * H * P * 2 + b * L * H * 2 + 2 * b * L * G * N * 2 + 3 * H * 4
+    if final_state:
+        total += b * H * P * N * 4
     return total

@@ -48,7 +48,9 @@ EXPORTED = ("ssm_selective_scan_fwd", "ssm_state_update", "ssm_scan_workspace_by
             "ssm_version", "ssm_selective_scan_fwd_static", "ssm_selective_scan_fwd_from_state",
             "ssm_selective_scan_fwd_conv", "ssm_causal_conv1d_silu", "ssm_scan_checkpoint_bytes",
             "ssm_selective_scan_fwd_ckpt", "ssm_scan_bwd_workspace_bytes",
-            "ssm_selective_scan_bwd", "ssm_debug_timeout_probe")
+            "ssm_selective_scan_bwd", "ssm_debug_timeout_probe", "ssm_get_static_status",
+            "ssm_debug_timeout_probe_static", "ssm_ssd_fwd", "ssm_ssd_workspace_bytes",
+            "ssm_ssd_get_device_status")
 
 # Size of the library-owned scratch of ssm_selective_scan_fwd_static (include/ssm.h).
 SSM_STATIC_SCRATCH_BYTES = 16 << 20
@@ -68,8 +70,22 @@ class ssm_plan(ctypes.Structure):
                 ("kernels", ctypes.c_int32), ("tile_config", ctypes.c_int32)]
 
 
+class ssm_ssd_dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
+                ("headdim", ctypes.c_int64), ("ngroups", ctypes.c_int64), ("dstate", ctypes.c_int64),
+                ("io_dtype", ctypes.c_int32), ("flags", ctypes.c_int32),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
 _vp = ctypes.c_void_p
 _dims_p = ctypes.POINTER(ssm_dims)
+_ssd_p = ctypes.POINTER(ssm_ssd_dims)
+lib.ssm_ssd_fwd.restype = ctypes.c_int
+lib.ssm_ssd_fwd.argtypes = [_vp] * 7 + [ctypes.c_int] + [_vp] * 3 + [_ssd_p, _vp]
+lib.ssm_ssd_workspace_bytes.restype = ctypes.c_size_t
+lib.ssm_ssd_workspace_bytes.argtypes = [_ssd_p]
+lib.ssm_ssd_get_device_status.restype = ctypes.c_int
+lib.ssm_ssd_get_device_status.argtypes = [_ssd_p, _vp]
 lib.ssm_selective_scan_fwd.restype = ctypes.c_int
 lib.ssm_selective_scan_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
                                        _vp, _vp, _dims_p, _vp]
@@ -102,6 +118,10 @@ lib.ssm_scan_plan.restype = ctypes.c_int
 lib.ssm_scan_plan.argtypes = [_dims_p, ctypes.POINTER(ssm_plan)]
 lib.ssm_debug_timeout_probe.restype = ctypes.c_int
 lib.ssm_debug_timeout_probe.argtypes = [_vp, ctypes.c_size_t, ctypes.c_uint32, _vp]
+lib.ssm_debug_timeout_probe_static.restype = ctypes.c_int
+lib.ssm_debug_timeout_probe_static.argtypes = [ctypes.c_uint32, _vp]
+lib.ssm_get_static_status.restype = ctypes.c_int
+lib.ssm_get_static_status.argtypes = [_vp]
 lib.ssm_get_device_status.restype = ctypes.c_int
 lib.ssm_get_device_status.argtypes = [_dims_p, _vp]
 lib.ssm_strerror.restype = ctypes.c_char_p
@@ -535,3 +555,50 @@ def _bwd_call(x, delta, A, B, C, ckpt, dout, D, z, delta_bias, delta_softplus, d
 selective_scan_fwd = ssm_selective_scan_fwd
 state_update = ssm_state_update
 causal_conv1d_silu = ssm_causal_conv1d_silu
+
+
+# ---------------------------------------------------------------------------
+# Mamba-2 SSD
+# ---------------------------------------------------------------------------
+def make_ssd_dims(batch, seqlen, nheads, headdim, ngroups, dstate, workspace=None,
+                  workspace_bytes=0) -> ssm_ssd_dims:
+    return ssm_ssd_dims(int(batch), int(seqlen), int(nheads), int(headdim), int(ngroups),
+                        int(dstate), SSM_BF16, 0, workspace, int(workspace_bytes))
+
+
+def ssm_ssd_fwd(x, dt, A, B, C, D=None, dt_bias=None, dt_softplus=False, h0=None, y=None,
+                final_state=None, return_final_state=True, workspace=None, stream=None):
+    """Mamba-2's SSD layer (see include/ssm.h): x [batch, L, H, 64] bf16, dt
+    [batch, L, H] bf16, A, D, dt_bias [H] fp32, B, C [batch, L, G, 128] bf16,
+    h0 [batch, H, 64, 128] fp32 or None. Returns (y, final_state or None)."""
+    torch = _torch()
+    device = _device_of(x, "x")
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    with _launch_on(device, stream) as sp:
+        if y is None:
+            y = torch.empty_like(x)
+        if final_state is None and return_final_state:
+            final_state = torch.empty((batch, H, P, N), dtype=torch.float32, device=device)
+        if workspace is None:
+            workspace = torch.zeros(256, dtype=torch.uint8, device=device)
+        dims = make_ssd_dims(batch, L, H, P, G, N, workspace.data_ptr(), workspace.numel())
+        bf, f32 = torch.bfloat16, torch.float32
+        rc = lib.ssm_ssd_fwd(
+            _ptr(x, "x", bf, device=device), _ptr(dt, "dt", bf, (batch, L, H), device),
+            _ptr(A, "A", f32, (H,), device), _ptr(B, "B", bf, (batch, L, G, N), device),
+            _ptr(C, "C", bf, (batch, L, G, N), device), _ptr(D, "D", f32, (H,), device),
+            _ptr(dt_bias, "dt_bias", f32, (H,), device), 1 if dt_softplus else 0,
+            _ptr(h0, "h0", f32, (batch, H, P, N), device), _ptr(y, "y", bf, x.shape, device),
+            _ptr(final_state, "final_state", f32, (batch, H, P, N), device),
+            ctypes.byref(dims), sp)
+    _check(rc, "ssm_ssd_fwd")
+    return y, final_state
+
+
+def ssm_ssd_get_device_status(batch, seqlen, nheads, ngroups, workspace, stream=None) -> int:
+    torch = _torch()
+    dims = make_ssd_dims(batch, seqlen, nheads, 64, ngroups, 128, workspace.data_ptr(),
+                         workspace.numel())
+    s = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+    return int(lib.ssm_ssd_get_device_status(ctypes.byref(dims), ctypes.c_void_p(s.cuda_stream)))
