@@ -4,34 +4,39 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 One step is one ssm_selective_scan_fwd call over one batch of the workload
-(default: bf16, batch 4, L 2048, d_inner 1536, d_state 16, softplus(delta +
-bias), gate), i.e. every step of the scan path. Rank 0 prints one JSON line.
+(default: the long-sequence workload, bf16, batch 1, L 131072, d_inner 5120,
+d_state 16, delta log-uniform in [1e-4, 1e-2], A = -(n + 1), D = 1, gate,
+final state), i.e. every step of the scan path. Rank 0 prints one JSON line.
 
 * value: elements (batch * L * dim) per second over the K timed steps, inputs
-  resident in HBM; the K steps rotate over several input sets whose total is
-  larger than twice the L2 cache, so every step reads its inputs from HBM.
+  resident in HBM; the K steps rotate over input sets whose total is larger
+  than twice the L2 cache, so every step reads its inputs from HBM.
 * e2e: the same metric through the same C-ABI call with host buffers:
   pinned host -> device copies of the step's inputs and a device -> host copy
   of its output inside the timed region, every step; the copies of one step
   overlap the compute of its neighbours (three streams, two buffer sets).
-* roofline: the binding unit of the scan, the SFU: the SFU operations the
-  method needs per call / average call time, against the measured ex2 rate;
-  hbm_roofline: algorithmic bytes per call / call time against the measured
-  HBM copy bandwidth; floors_us: the per-call floor of each unit.
+* roofline: the unit with the highest floor for the workload (HBM bytes, SFU
+  exponentials or FP32 operations the method needs), its achieved rate
+  against its measured peak; hbm_roofline: algorithmic bytes per call / call
+  time against the measured HBM copy bandwidth; floors_us: each unit's floor.
+* check / cpu_baseline: the float64 CPU oracle over blocks of channels (every
+  batch row and token) in a seeded order, within a time budget, compared
+  element by element with the last timed output and final state; its rate on
+  this host's cores (rank 0, N = 1).
+* side: the other two bf16 scan workloads (batch 8, L 4096, d_inner 2048; and
+  batch 4, L 2048, d_inner 1536 with softplus(delta + bias) and a general A),
+  each with its own value, roofline and check.
 * decode: the recurrent step ssm_state_update on the decode workload (batch
   256, dim 5120, N 16), rotating over several cached states.
-* input_stage: the causal conv1d + SiLU (width 4) alone, fused in front of
-  the scan, and as two calls (conv, then the scan on its output).
-* train: training through the scan on the same workload, the checkpointing
-  forward and the backward (every gradient), per call.
-* bc_per_channel: the scan with per-channel B, C on the same shapes (bound by
-  HBM: its roofline is the copy bandwidth).
-* zoh: the scan with the exact zero-order-hold Bbar on the same workload,
-  against the same SFU roofline.
+* ssd: Mamba-2's SSD layer on the tensor cores (batch 16, L 8192, 8 heads of
+  64 channels, d_state 128): its tensor-pipe and HBM rooflines and parity on
+  sampled heads against the oracle.
+* input_stage, train, bc_per_channel, zoh (on the batch 4, L 2048 workload):
+  the causal conv1d + SiLU (width 4) alone, fused and as two calls; training
+  through the scan (checkpointing forward and backward); the scan with
+  per-channel B, C (HBM-bound); the scan with the exact zero-order hold.
   A side leg that fails reports {"error": ...} in its place; the headline
   line is still printed.
-* cpu_baseline: the float64 CPU oracle timed on this host (rank 0, N = 1);
-  check: its last pass compared with the last timed GPU output, every element.
 
 N > 1 (torchrun): every rank runs its own replica of the workload on its own
 GPU (the scan has no cross-channel exchange: weak scaling, no collective on
@@ -56,7 +61,11 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "selective-scan elems/s (B·L·D) and achieved HBM GB/s vs B300 peak, 1 GPU"
-DEFAULT_WORKLOAD = "scan_bf16_b4_L2048_d1536_softplus"
+DEFAULT_WORKLOAD = "scan_bf16_b1_L131072_d5120"
+# the other scan workloads, timed as side legs with their own roofline and check
+SIDE_WORKLOADS = ("scan_bf16_b8_L4096_d2048", "scan_bf16_b4_L2048_d1536_softplus")
+# the workload of the input-stage, training, per-channel B, C and exact-ZOH legs
+LEG_WORKLOAD = "scan_bf16_b4_L2048_d1536_softplus"
 DECODE_WORKLOAD = "decode_bf16_b256_d5120_x64"
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6400.0
@@ -232,32 +241,41 @@ def _vp(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def bench_scan(args, rank, world, local):
+def _scan_sets(spec, inp, dev, nsets):
+    """nsets device copies of the per-element inputs (A, D and the bias are
+    shared), each with its own output and final-state buffers."""
     import torch
-    from selective_state_space_119_b300 import inputs as I
-    from selective_state_space_119_b300 import libssm
-
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    spec = I.WORKLOADS[args.workload]
-    inp = I.make_scan_inputs(spec)
-    io = libssm.SSM_BF16 if spec.io == "bf16" else libssm.SSM_F32
-    elems = spec.elements
-    alg_bytes = I.algorithmic_bytes_scan(spec)
-
-    # input sets, rotated so that no step finds its inputs in L2
-    per_set = alg_bytes
-    nsets = max(2, min(16, math.ceil(2 * L2_BYTES / per_set) + 1))
     base = {k: _upload(v, dev) for k, v in inp.items()}
     sets = []
     for i in range(nsets):
-        s = {k: (None if base[k] is None else (base[k] if k in ("A", "D", "delta_bias")
+        s = {k: (None if base[k] is None else (base[k] if (k in ("A", "D", "delta_bias") or i == 0)
                                                 else base[k].clone()))
              for k in base}
         s["out"] = torch.empty_like(base["x"])
         s["fs"] = (torch.empty((spec.batch, spec.dim, spec.N), dtype=torch.float32, device=dev)
                    if spec.final_state else None)
         sets.append(s)
+    return base, sets
+
+
+def time_scan(name, args, rank, world, dev, steps, warmup, e2e=False):
+    """Time ssm_selective_scan_fwd on one workload: `steps` calls over rotating
+    input sets whose total exceeds twice the L2 (a single set already does for
+    the long-sequence workload), CUDA events on the launching stream, barrier
+    and maximum over ranks. Returns the result dict, the host inputs and the
+    set whose output the oracle check reads."""
+    import torch
+    import torch.distributed as dist
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+
+    spec = I.WORKLOADS[name]
+    inp = I.make_scan_inputs(spec)
+    io = libssm.SSM_BF16 if spec.io == "bf16" else libssm.SSM_F32
+    elems = spec.elements
+    alg_bytes = I.algorithmic_bytes_scan(spec)
+    nsets = max(2, min(16, math.ceil(2 * L2_BYTES / alg_bytes) + 1))
+    base, sets = _scan_sets(spec, inp, dev, nsets)
     plan = libssm.ssm_scan_plan(spec.batch, spec.L, spec.dim, spec.N, io)
     ws = libssm.alloc_workspace(spec.batch, spec.L, spec.dim, spec.N, io, dev)
     dims = libssm.make_dims(spec.batch, spec.L, spec.dim, spec.N, io,
@@ -275,19 +293,17 @@ def bench_scan(args, rank, world, local):
         if rc != 0:
             raise libssm.SSMError(rc, "ssm_selective_scan_fwd")
 
-    clocks = ClockSampler(local).start()
-    for i in range(args.warmup):
+    clocks = ClockSampler(dev.index if dev.index is not None else 0).start()
+    for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
-
-    import torch.distributed as dist
     if dist.is_initialized():
         dist.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
     e0.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         step(i)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -296,36 +312,49 @@ def bench_scan(args, rank, world, local):
         dist.barrier()
     clocks.stop()
     sec = e0.elapsed_time(e1) / 1e3
-    value, slowest = aggregate(elems * args.steps, sec)
+    value, slowest = aggregate(elems * steps, sec)
     status = libssm.ssm_get_device_status(spec.batch, spec.L, spec.dim, spec.N, io, ws)
     if status != 0:
         raise libssm.SSMError(status, "device status")
+    # the set the last timed step wrote (every set holds the same input values)
+    last = sets[(steps - 1) % nsets]
 
-    per_call = sec / args.steps
+    per_call = sec / steps
     peak, peak_kind = measured_peaks()
     achieved = alg_bytes / per_call / 1e9
+    hbm = dict({"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": scan_traffic(name),
+                "peak_kind": peak_kind, "algorithmic_bytes_per_call": alg_bytes},
+               **nominal(achieved))
     res = {
-        "value": value, "ms_per_step": slowest / args.steps * 1e3,
+        "workload": name, "value": value, "unit": "elems/s",
+        "ms_per_step": slowest / steps * 1e3, "steps": steps, "warmup": warmup,
         "gbps": achieved,
-        "roofline": dict(alu_roofline(spec, per_call, plan),
-                         traffic=scan_traffic(args.workload)),
-        "hbm_roofline": dict({"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                              "frac": achieved / peak, "traffic": scan_traffic(args.workload),
-                              "peak_kind": peak_kind, "algorithmic_bytes_per_call": alg_bytes},
-                             **nominal(achieved)),
+        "roofline": binding_roofline(spec, per_call, plan, hbm, peak),
+        "hbm_roofline": hbm,
         "floors_us": time_floors(spec, alg_bytes, peak),
-        "gpu_launches": args.steps * plan["kernels"],
+        "gpu_launches": steps * plan["kernels"],
         "clocks": clocks.summary(t_wall0, t_wall1),
-        "plan": plan,
-        "input_sets": nsets,
+        "plan": plan, "input_sets": nsets, "config": workload_config(spec),
     }
+    if e2e:
+        res["e2e"] = time_scan_e2e(spec, sets, base, dims, fn, steps, dev)
+    keep = {"out": last["out"], "fs": last["fs"]}
+    del sets, base, call_args
+    return res, spec, inp, keep
 
-    # end to end: pinned host buffers; every step copies its inputs in and its
-    # output out inside the timed region. The copies of one step overlap the
-    # compute of its neighbours: three streams (in, compute, out), two device
-    # buffer sets, ordered by events (a set's inputs are overwritten only after
-    # the compute two steps back has read them, its output only after the copy
-    # out two steps back has read it).
+
+def time_scan_e2e(spec, sets, base, dims, fn, steps, dev):
+    """The same metric through the same C-ABI call with host buffers: pinned
+    host -> device copies of the step's inputs and a device -> host copy of its
+    output inside the timed region, every step. The copies of one step overlap
+    the compute of its neighbours: three streams (in, compute, out), two device
+    buffer sets, ordered by events (a set's inputs are overwritten only after
+    the compute two steps back has read them, its output only after the copy
+    out two steps back has read it)."""
+    import torch
+    import torch.distributed as dist
+    from selective_state_space_119_b300 import libssm
     host = {k: (None if base[k] is None else base[k].cpu().pin_memory())
             for k in ("x", "delta", "z", "B", "C")}
     e2e_sets = sets[:2]
@@ -333,7 +362,7 @@ def bench_scan(args, rank, world, local):
               for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     d2h = h_outs[0].numel() * h_outs[0].element_size()
-    k_e2e = max(3, min(args.steps, 50))
+    k_e2e = max(3, min(steps, 50))
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev))
     cmp_ptr = ctypes.c_void_p(s_cmp.cuda_stream)
     cmp_args = [(_vp(st["x"]), _vp(st["delta"]), _vp(st["A"]), _vp(st["B"]), _vp(st["C"]),
@@ -378,27 +407,115 @@ def bench_scan(args, rank, world, local):
     e1.record(s_out)           # after the last copy out, which follows every other step
     torch.cuda.synchronize()
     e2e_sec = e0.elapsed_time(e1) / 1e3
-    e2e_value, _ = aggregate(elems * k_e2e, e2e_sec)
-    res["e2e"] = {"value": e2e_value, "unit": "elems/s", "h2d_bytes_per_step": h2d,
-                  "d2h_bytes_per_step": d2h, "steps": k_e2e,
-                  "pipelined": "copies in, compute and copies out of neighbouring steps "
-                               "overlap (3 streams, 2 device buffer sets)"}
+    e2e_value, _ = aggregate(spec.elements * k_e2e, e2e_sec)
+    out = {"value": e2e_value, "unit": "elems/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": k_e2e,
+           "pipelined": "copies in, compute and copies out of neighbouring steps "
+                        "overlap (3 streams, 2 device buffer sets)"}
+    del host, h_outs
+    return out
 
-    # the last timed output (every set holds the same input values), for the
-    # CPU-baseline leg to compare with the oracle's output on the host
-    res["out_host"] = (sets[0]["out"].float().cpu().numpy().astype("float64")
-                       if rank == 0 and world == 1 else None)
-    del sets
+
+def oracle_check(spec, inp, keep, budget_s, block=256, seed=0):
+    """The float64 oracle over blocks of channels (every batch row and token),
+    taken in a seeded random order until budget_s seconds of oracle time have
+    passed (at least one block), compared element by element with the GPU's
+    timed output and final state. Returns (check, cpu_baseline): the errors,
+    and the oracle's rate over the channels it ran (its own call time only)."""
+    import numpy as np
+    import oracle
+    from selective_state_space_119_b300 import inputs as I
+    threads = oracle.default_threads()
+    nblk = (spec.dim + block - 1) // block
+    order = np.random.Generator(np.random.PCG64(seed)).permutation(nblk)
+    B, C = I.widen(inp["B"]), I.widen(inp["C"])
+    se = sr = 0.0
+    mx = fs_mx = 0.0
+    done = 0
+    osec = 0.0
+    for bi in order:
+        d0, d1 = int(bi) * block, min(spec.dim, (int(bi) + 1) * block)
+        xs = I.widen(inp["x"][:, :, d0:d1])
+        ds = I.widen(inp["delta"][:, :, d0:d1])
+        zs = None if inp["z"] is None else I.widen(inp["z"][:, :, d0:d1])
+        t0 = time.perf_counter()
+        ref, rfs = oracle.selective_scan(
+            xs, ds, inp["A"][d0:d1], B, C,
+            D=None if inp["D"] is None else inp["D"][d0:d1], z=zs,
+            delta_bias=None if inp["delta_bias"] is None else inp["delta_bias"][d0:d1],
+            delta_softplus=spec.delta_softplus, nthreads=threads)
+        osec += time.perf_counter() - t0
+        got = keep["out"][:, :, d0:d1].float().cpu().numpy().astype(np.float64)
+        err = got - ref
+        se += float(np.sum(err * err))
+        sr += float(np.sum(ref * ref))
+        mx = max(mx, float(np.max(np.abs(err) / (1 + np.abs(ref)))))
+        if keep["fs"] is not None:
+            gfs = keep["fs"][:, d0:d1, :].cpu().numpy().astype(np.float64)
+            fs_mx = max(fs_mx, float(np.max(np.abs(gfs - rfs) / (1 + np.abs(rfs)))))
+        done += d1 - d0
+        if osec >= budget_s:
+            break
+    elems = spec.batch * spec.L * done
+    check = {"elements": elems, "channels": done, "of_channels": spec.dim,
+             "rel_l2": math.sqrt(se / sr) if sr > 0 else 0.0, "max_scaled_err": mx,
+             "against": "the float64 oracle (cpu_baseline leg) on the same inputs",
+             "tolerance": ({"rel_l2": 3e-3, "max_scaled_err": 2e-2} if spec.io == "bf16"
+                           else {"max_scaled_err": 1e-4})}
+    if keep["fs"] is not None:
+        check["final_state_max_scaled_err"] = fs_mx
+        check["final_state_tolerance"] = 1e-4
+    cpu = {"value": elems / osec, "unit": "elems/s", "cores": threads, "kind": "oracle",
+           "sample": "%d of %d channels (blocks of %d in a seeded order, every batch row and "
+                     "token), %.1f s of float64 oracle on %d host threads"
+                     % (done, spec.dim, block, osec, threads)}
+    return check, cpu
+
+
+def bench_scan(args, rank, world, local):
+    import torch
+    from selective_state_space_119_b300 import inputs as I
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    check_here = rank == 0 and world == 1
+    res, spec, inp, keep = time_scan(args.workload, args, rank, world, dev, args.steps,
+                                     args.warmup, e2e=True)
+    if check_here:
+        res["check"], res["cpu_baseline"] = oracle_check(spec, inp, keep, args.cpu_seconds)
+    del keep, inp
     torch.cuda.empty_cache()
+
+    # the other scan workloads, each with its own roofline and oracle check
+    side = {}
+    if not args.no_side:
+        for name in SIDE_WORKLOADS:
+            if name == args.workload:
+                continue
+            try:
+                r, sspec, sinp, skeep = time_scan(name, args, rank, world, dev,
+                                                  max(args.steps, 10), args.warmup)
+                if check_here:
+                    r["check"], r["cpu_baseline"] = oracle_check(sspec, sinp, skeep,
+                                                                 args.cpu_seconds / 4)
+                for k in ("clocks", "steps", "warmup"):
+                    r.pop(k, None)
+                side[name] = r
+                del skeep, sinp
+            except Exception as e:   # a failed side leg is reported, not fatal
+                side[name] = {"error": "%s: %s" % (type(e).__name__, e)}
+            torch.cuda.empty_cache()
+    res["side"] = side
+
+    lspec = I.WORKLOADS[LEG_WORKLOAD]
     legs = (("decode", not args.no_decode, lambda: bench_decode(args, dev, stream)),
             ("input_stage", not args.no_input_stage,
-             lambda: bench_input_stage(args, spec, dev, stream)),
-            ("train", not args.no_train and spec.N == 16,
-             lambda: bench_train(args, spec, dev, stream)),
-            ("bc_per_channel", not args.no_bcd and spec.N == 16,
-             lambda: bench_bcd(args, spec, dev, stream)),
-            ("zoh", not args.no_zoh and spec.N == 16,
-             lambda: bench_zoh(args, spec, dev, stream)))
+             lambda: bench_input_stage(args, lspec, dev, stream)),
+            ("train", not args.no_train, lambda: bench_train(args, lspec, dev, stream)),
+            ("bc_per_channel", not args.no_bcd, lambda: bench_bcd(args, lspec, dev, stream)),
+            ("zoh", not args.no_zoh, lambda: bench_zoh(args, lspec, dev, stream)),
+            ("ssd", not args.no_ssd, lambda: bench_ssd(args, dev, stream)))
     for name, wanted, run in legs:
         if not wanted:
             continue
@@ -406,29 +523,45 @@ def bench_scan(args, rank, world, local):
             res[name] = run()
         except Exception as e:   # a failed side leg is reported, not fatal to the headline
             res[name] = {"error": "%s: %s" % (type(e).__name__, e)}
+        torch.cuda.empty_cache()
     return res, spec
 
 
-# SFU (MUFU) exponential rate of one B300 SM per clock, measured with a probe of
-# back-to-back independent ex2.approx.ftz.f32 at full occupancy: 29.1 per SM per
-# clock (the nominal 2 x 16 of Blackwell Ultra's doubled SFU), 148 SMs, at the
-# 2032 MHz maximum SM clock. FP32 lanes per SM per clock: 128 (nominal).
-EX2_PER_SM_CLK = 29.1
+# SFU (MUFU) exponential rate of one B300 SM per clock and FP32 lane
+# operations per SM per clock, measured with a probe at full occupancy: 148 x 8
+# CTAs of 256 threads, each thread running 16 independent chains of
+# ex2.approx.ftz.f32, fma.rn.f32 or fma.rn.f32x2 for 2048 x 4 steps, cycles
+# taken from each SM's own clock counter (first start to last end of its
+# CTAs), the instruction counts confirmed with ncu (sm__inst_executed_pipe_fma,
+# _fmaheavy, _fmalite, _xu). Results: ex2 32.0, FFMA 125.2 and FFMA2 127.6 FP32
+# operations per SM per clock (an FFMA2 occupies both FMA half-pipes for one
+# issue: packing halves the issue slots, not the pipe time), 8 FFMA2 + 2 ex2
+# mixed 116. 148 SMs; the 2032 MHz maximum SM clock.
+EX2_PER_SM_CLK = 32.0
 FP32_PER_SM_CLK = 128.0
 SMS = 148
 SM_MAX_MHZ = 2032.0
 
 
+def structured_A(spec):
+    """A[d, n] = a_d (n + 1): exp(dt A[d, :]) is the powers 1..N of one
+    exponential per channel and token."""
+    return spec.A_kind == "s4d"
+
+
 def exps_per_element(spec):
-    """SFU operations the method needs per element: N exponentials for
-    exp(dt A), two for softplus (e^v and the log) and two for the silu gate
+    """SFU operations the method needs per element: the exponentials of
+    exp(dt A) (N of them, or one when A[d, n] = a_d (n + 1), whose powers give
+    the rest), two for softplus (e^v and the log) and two for the silu gate
     (e^-z and the reciprocal)."""
-    return spec.N + (2 if spec.delta_softplus else 0) + (2 if spec.gate else 0)
+    return ((1 if structured_A(spec) else spec.N) + (2 if spec.delta_softplus else 0)
+            + (2 if spec.gate else 0))
 
 
 def fp32_ops_per_element(spec):
-    """FP32 operations the method needs per element: per state dt*A, (dt x)*B,
-    the h update and the C.h readout (4N), plus dt*x, the D skip and the gate."""
+    """FP32 operations the method needs per element: per state dt*A (or the
+    power that replaces it), (dt x)*B, the h update and the C.h readout (4N),
+    plus dt*x, the D skip and the gate."""
     return 4 * spec.N + 3
 
 
@@ -439,15 +572,14 @@ def time_floors(spec, alg_bytes, hbm_gbs):
     return {"hbm": alg_bytes / (hbm_gbs * 1e9) * 1e6, "sfu": sfu * 1e6, "fp32": fp32 * 1e6}
 
 
-# DRAM traffic of one scan call of the benchmark workload (both launches:
-# chunk-state pass + output pass), dram__bytes_read.sum + dram__bytes_write.sum
-# from the ncu capture summarised in profiles/scan_launches_b4_L2048_d1536.md.
-# It holds only for the kernel source it was taken on: the sha256 below covers
-# the scan kernel and the headers it includes; any change there reports null.
-SCAN_TRAFFIC = {"workload": "scan_bf16_b4_L2048_d1536_softplus",
-                "bytes_per_call": 43607808 + 5632 + 78255360 + 759552,
-                "sha256": "a19f03079bff8d8bde37b0b179a0213db41b0d2c25bbae62266af8777d03099b"}
-SCAN_SOURCES = ("scan_fwd.cu", "ssm_device.cuh", "ssm_tma.cuh", "ssm_tmap.h", "ssm_internal.h")
+# DRAM traffic of one scan call (every launch of the call),
+# dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture per
+# workload (a capture of a shorter sequence scaled by the tokens, where the
+# full workload is too large to capture). A figure holds only for the kernel
+# source it was taken on: the sha256 covers the scan kernel and the headers it
+# includes; any change there reports null.
+SCAN_TRAFFIC = {}
+SCAN_SOURCES = ("scan16.cu", "scan_fwd.cu", "ssm_device.cuh", "ssm_tma.cuh", "ssm_tmap.h", "ssm_internal.h")
 
 
 def scan_source_sha256():
@@ -461,23 +593,38 @@ def scan_source_sha256():
 
 
 def scan_traffic(spec_name):
-    if (SCAN_TRAFFIC["bytes_per_call"] is None or spec_name != SCAN_TRAFFIC["workload"]
-            or scan_source_sha256() != SCAN_TRAFFIC["sha256"]):
+    t = SCAN_TRAFFIC.get(spec_name)
+    if t is None or scan_source_sha256() != t["sha256"]:
         return None
-    return SCAN_TRAFFIC["bytes_per_call"]
+    return t["bytes_per_call"]
 
 
-def alu_roofline(spec, per_call_s, plan):
-    """The binding roofline of the scan: the SFU operations the method needs
-    per second against the SFU peak (the largest of the three floors)."""
-    per_elem = exps_per_element(spec)
+def binding_roofline(spec, per_call_s, plan, hbm, hbm_peak):
+    """The roofline of the unit whose floor is highest for this workload: HBM
+    (algorithmic bytes), the SFU (exponentials the method needs) or the FP32
+    pipe (its FP32 operations), each achieved rate against that unit's peak."""
+    floors = time_floors(spec, hbm["algorithmic_bytes_per_call"], hbm_peak)
+    unit = max(floors, key=floors.get)
+    kernel = ("scan_kernel, one ssm_selective_scan_fwd call (%d launch%s)"
+              % (plan["kernels"], "es" if plan["kernels"] > 1 else ""))
+    if unit == "hbm":
+        return dict(hbm, kernel=kernel)
+    if unit == "sfu":
+        per_elem = exps_per_element(spec)
+        peak = EX2_PER_SM_CLK * SMS * SM_MAX_MHZ * 1e6 / 1e12
+        basis = "measured ex2 rate %.1f per SM per clock x %d SMs x %.0f MHz" % (
+            EX2_PER_SM_CLK, SMS, SM_MAX_MHZ)
+        name = "T SFU op/s"
+    else:
+        per_elem = fp32_ops_per_element(spec)
+        peak = FP32_PER_SM_CLK * SMS * SM_MAX_MHZ * 1e6 / 1e12
+        basis = "measured FP32 rate %.0f lane-ops per SM per clock x %d SMs x %.0f MHz" % (
+            FP32_PER_SM_CLK, SMS, SM_MAX_MHZ)
+        name = "T FP32 op/s"
     achieved = spec.elements * per_elem / per_call_s / 1e12
-    peak = EX2_PER_SM_CLK * SMS * SM_MAX_MHZ * 1e6 / 1e12
-    return {"bound": "alu", "unit": "T SFU op/s", "achieved": achieved, "peak": peak,
-            "frac": achieved / peak, "traffic": None, "sfu_ops_per_element": per_elem,
-            "kernel": "scan_kernel, one ssm_selective_scan_fwd call (%d launch%s)"
-                      % (plan["kernels"], "es" if plan["kernels"] > 1 else ""),
-            "peak_basis": "measured ex2 rate 29.1 per SM per clock x 148 SMs x 2032 MHz"}
+    return {"bound": "alu", "unit": name, "achieved": achieved, "peak": peak,
+            "frac": achieved / peak, "traffic": hbm["traffic"], "ops_per_element": per_elem,
+            "pipe": unit, "kernel": kernel, "peak_basis": basis}
 
 
 def output_check(got, ref):
@@ -829,37 +976,123 @@ def bench_zoh(args, spec, dev, stream):
     torch.cuda.synchronize()
     sec = e0.elapsed_time(e1) / 1e3 / n
     plan = libssm.ssm_scan_plan(B_, L_, D_, N_, io, flags=F)
-    roof = alu_roofline(spec, sec, plan)
-    roof["kernel"] = roof["kernel"].replace("scan_kernel", "scan_kernel with the ZOH flag")
+    # the exact hold needs the N exponentials of exp(dt A) (its input term
+    # reuses them), softplus's two and the gate's two: the SFU binds
+    per_elem = spec.N + (2 if spec.delta_softplus else 0) + (2 if spec.gate else 0)
+    peak = EX2_PER_SM_CLK * SMS * SM_MAX_MHZ * 1e6 / 1e12
+    achieved = spec.elements * per_elem / sec / 1e12
+    roof = {"bound": "alu", "unit": "T SFU op/s", "achieved": achieved, "peak": peak,
+            "frac": achieved / peak, "traffic": None, "ops_per_element": per_elem, "pipe": "sfu",
+            "kernel": "scan_kernel with the ZOH flag, one ssm_selective_scan_fwd call (%d "
+                      "launches)" % plan["kernels"],
+            "peak_basis": "measured ex2 rate %.1f per SM per clock x %d SMs x %.0f MHz"
+                          % (EX2_PER_SM_CLK, SMS, SM_MAX_MHZ)}
     return {"us_per_call": sec * 1e6, "value": spec.elements / sec, "unit": "elems/s",
             "timed_calls": n, "input_sets": nsets, "kernels_per_call": plan["kernels"],
             "roofline": roof, "algorithmic_bytes_per_call": alg}
 
 
+SSD_WORKLOAD = "ssd_bf16_b16_L8192_h8_p64_n128"
+
+
+def ssd_flops_per_chunk_head(Q=128, P=64, N=128):
+    """Tensor-core FLOPs the chunked SSD form needs per (chunk, head): C B^T
+    (2 Q Q N), the masked product with X (2 Q Q P), the carried state read by
+    C (2 Q N P) and the chunk state (2 Q N P), one bf16 product each."""
+    return 2 * Q * Q * N + 2 * Q * Q * P + 2 * 2 * Q * N * P
+
+
+def bench_ssd(args, dev, stream):
+    """Mamba-2's SSD layer (tensor cores) on its workload: time per call, the
+    tensor-pipe roofline (the FLOPs of the chunked form against the measured
+    bf16 peak), the HBM roofline beside it, and parity on sampled (batch row,
+    head) pairs against the oracle."""
+    import numpy as np
+    import torch
+    import oracle
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+
+    spec = I.SSD_WORKLOADS[SSD_WORKLOAD]
+    inp = I.make_ssd_inputs(spec)
+    t = {k: _upload(v, dev) for k, v in inp.items()}
+    alg = I.algorithmic_bytes_ssd(spec)
+    nsets = max(2, min(8, math.ceil(2 * L2_BYTES / alg) + 1))
+    xs = [t["x"]] + [t["x"].clone() for _ in range(nsets - 1)]
+    ys = [torch.empty_like(t["x"]) for _ in range(nsets)]
+    fs = torch.empty((spec.batch, spec.H, spec.P, spec.N), dtype=torch.float32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    dims = libssm.make_ssd_dims(spec.batch, spec.L, spec.H, spec.P, spec.G, spec.N,
+                                ws.data_ptr(), 256)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    def call(i):
+        rc = libssm.lib.ssm_ssd_fwd(
+            _vp(xs[i % nsets]), _vp(t["dt"]), _vp(t["A"]), _vp(t["B"]), _vp(t["C"]), _vp(t["D"]),
+            _vp(t["dt_bias"]), 1, None, _vp(ys[i % nsets]), _vp(fs), ctypes.byref(dims), sptr)
+        if rc != 0:
+            raise libssm.SSMError(rc, "ssm_ssd_fwd")
+
+    for i in range(max(args.warmup, 3)):
+        call(i)
+    torch.cuda.synchronize()
+    n = max(10, min(args.steps, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        call(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3 / n
+    st = libssm.ssm_ssd_get_device_status(spec.batch, spec.L, spec.H, spec.G, ws)
+    if st != 0:
+        raise libssm.SSMError(st, "ssd device status")
+    chunks = (spec.L + 127) // 128
+    flops = ssd_flops_per_chunk_head() * chunks * spec.H * spec.batch
+    tf = flops / sec / 1e12
+    peak_tf = measured_bf16_tflops()
+    peak, kind = measured_peaks()
+    gbs = alg / sec / 1e9
+    # parity on a few (batch row, head) pairs of the last timed call
+    y_last = ys[(n - 1) % nsets]
+    bsel, hsel = np.array([0, spec.batch - 1]), np.array([0, spec.H - 1])
+    sub = {k: (v if v is None or k in ("A", "D", "dt_bias") else v[bsel]) for k, v in inp.items()}
+    ry, rfs = oracle.ssd(I.widen(sub["x"][:, :, hsel]), I.widen(sub["dt"][:, :, hsel]),
+                         sub["A"][hsel], I.widen(sub["B"]), I.widen(sub["C"]), D=sub["D"][hsel],
+                         dt_bias=sub["dt_bias"][hsel], dt_softplus=True)
+    bt, ht = torch.as_tensor(bsel, device=dev), torch.as_tensor(hsel, device=dev)
+    got = y_last[bt][:, :, ht].float().cpu().numpy().astype(np.float64)
+    gfs = fs[bt][:, ht].cpu().numpy().astype(np.float64)
+    return {"workload": SSD_WORKLOAD, "us_per_call": sec * 1e6,
+            "value": spec.elements / sec, "unit": "elems/s (batch * L * heads * head_dim)",
+            "timed_calls": n, "input_sets": nsets, "kernels_per_call": 1,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": tf / peak_tf, "traffic": None,
+                         "flops_per_call": flops,
+                         "peak_kind": "measured bf16 dense (burst)",
+                         "kernel": "ssd_kernel (tcgen05.mma, one launch)"},
+            "hbm_roofline": dict({"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                                  "frac": gbs / peak, "traffic": None, "peak_kind": kind,
+                                  "algorithmic_bytes_per_call": alg}, **nominal(gbs)),
+            "check": dict(output_check(got, ry),
+                          final_state_max_scaled_err=float(
+                              np.max(np.abs(gfs - rfs) / (1 + np.abs(rfs)))),
+                          against="the float64 oracle on batch rows %s, heads %s"
+                                  % (bsel.tolist(), hsel.tolist()))}
+
+
+def measured_bf16_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1800.0
+
+
 # ---------------------------------------------------------------------------
 # the CPU oracle arm
 # ---------------------------------------------------------------------------
-def cpu_oracle_rate(spec, inp, min_seconds: float, max_passes: int = 100):
-    """Time the float64 oracle over whole passes of the workload on every host
-    thread until min_seconds have passed (at least one pass). Returns the rate,
-    the threads, the passes, the seconds and the output of the last pass."""
-    import oracle
-    from selective_state_space_119_b300 import inputs as I
-    threads = oracle.default_threads()
-    args = (I.widen(inp["x"]), I.widen(inp["delta"]), inp["A"], I.widen(inp["B"]),
-            I.widen(inp["C"]))
-    kw = dict(D=inp["D"], z=I.widen(inp["z"]), delta_bias=inp["delta_bias"],
-              delta_softplus=spec.delta_softplus, nthreads=threads)
-    passes, t0 = 0, time.perf_counter()
-    while True:
-        out, _ = oracle.selective_scan(*args, **kw)
-        passes += 1
-        el = time.perf_counter() - t0
-        if el >= min_seconds or passes >= max_passes:
-            break
-    return spec.elements * passes / el, threads, passes, el, out
-
-
 def run_reference(args, rank, world, budget_s: float = 120.0):
     """The float64 CPU oracle as the reference arm. One step = the oracle over
     every token and batch row of a rotating subset of channels, the subset
@@ -946,8 +1179,13 @@ def main(argv=None):
                     help="skip the per-channel B, C scan timing")
     ap.add_argument("--no-zoh", action="store_true",
                     help="skip the exact zero-order-hold scan timing")
-    ap.add_argument("--cpu-seconds", type=float, default=8.0,
-                    help="minimum wall time of the CPU oracle baseline")
+    ap.add_argument("--no-ssd", action="store_true",
+                    help="skip the Mamba-2 SSD layer timing")
+    ap.add_argument("--no-side", action="store_true",
+                    help="skip the other scan workloads (side legs)")
+    ap.add_argument("--cpu-seconds", type=float, default=30.0,
+                    help="oracle time budget of the headline's check and cpu_baseline "
+                         "(the side legs get a quarter each)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -974,25 +1212,15 @@ def main(argv=None):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f32", "io_dtype": spec.io, "data": "synthetic",
-                "config": workload_config(spec), "gbps": res["gbps"],
+                "config": res["config"], "gbps": res["gbps"],
                 "roofline": res["roofline"], "hbm_roofline": res["hbm_roofline"],
                 "floors_us": res["floors_us"], "e2e": res["e2e"],
                 "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
-                "plan": res["plan"], "check": None}
-        for leg in ("decode", "input_stage", "train", "bc_per_channel", "zoh"):
+                "plan": res["plan"], "check": res.get("check"),
+                "cpu_baseline": res.get("cpu_baseline")}
+        for leg in ("side", "decode", "input_stage", "train", "bc_per_channel", "zoh", "ssd"):
             if leg in res:
                 line[leg] = res[leg]
-        if world == 1:
-            from selective_state_space_119_b300 import inputs as I
-            inp = I.make_scan_inputs(spec)
-            rate, threads, passes, el, ref = cpu_oracle_rate(spec, inp, args.cpu_seconds)
-            line["cpu_baseline"] = {
-                "value": rate, "unit": "elems/s", "cores": threads, "kind": "oracle",
-                "sample": "whole workload (%d x %d x %d), %d pass(es), %.1f s, all host threads"
-                          % (spec.batch, spec.L, spec.dim, passes, el)}
-            # the oracle's last pass against the last timed GPU output, every element
-            line["check"] = dict(output_check(res["out_host"], ref),
-                                 against="the cpu_baseline leg's oracle output")
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
