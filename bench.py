@@ -858,12 +858,31 @@ def bench_train(args, spec, dev, stream):
     t_b = timed(bwd, n)
     plan = libssm.ssm_scan_plan(B_, L_, D_, N_, io)
     elems = spec.elements
+    # The backward's binding unit: its FP32 operations per element are the
+    # forward's 4N + 3 (the states recomputed from the checkpoints) plus 8 per
+    # state for the adjoint sweep (dh carried back through a and fed by C dy;
+    # the dC, dB, dt and dA terms) plus 7 per element (dx, dz, the softplus and
+    # gate derivatives); its SFU operations the forward's N + 4 plus one (the
+    # softplus derivative's sigmoid).
+    fp32 = (4 * spec.N + 3) + 8 * spec.N + 7
+    sfu = spec.N + (2 if spec.delta_softplus else 0) + (2 if spec.gate else 0) + 1
+    f_peak = FP32_PER_SM_CLK * SMS * SM_MAX_MHZ * 1e6 / 1e12
+    s_peak = EX2_PER_SM_CLK * SMS * SM_MAX_MHZ * 1e6 / 1e12
+    fp32_t, sfu_t = elems * fp32 / f_peak / 1e12, elems * sfu / s_peak / 1e12
+    pipe, per, peak = (("fp32", fp32, f_peak) if fp32_t >= sfu_t else ("sfu", sfu, s_peak))
+    ach = elems * per / t_b / 1e12
+    bwd_roof = {"bound": "alu", "unit": "T %s op/s" % pipe.upper(), "achieved": ach,
+                "peak": peak, "frac": ach / peak, "traffic": None, "pipe": pipe,
+                "ops_per_element": per,
+                "floors_us": {"fp32": fp32_t * 1e6, "sfu": sfu_t * 1e6},
+                "kernel": "scan_bwd_kernel (+ reverse-carry pass and reduction), one "
+                          "ssm_selective_scan_bwd call"}
     return {"timed_calls": n, "input_sets": nsets, "dout": "N(0,1)",
             "fwd_ckpt": {"us_per_call": t_f * 1e6, "value": elems / t_f, "unit": "elems/s",
                          "kernels_per_call": plan["kernels"]},
             "bwd": {"us_per_call": t_b * 1e6, "value": elems / t_b, "unit": "elems/s",
                     "kernels_per_call": (2 if plan["nchunks"] > 1 else 1) + 1,
-                    "workspace_bytes": nb},
+                    "workspace_bytes": nb, "roofline": bwd_roof},
             "step": {"us_per_call": (t_f + t_b) * 1e6, "value": elems / (t_f + t_b),
                      "unit": "elems/s"}}
 

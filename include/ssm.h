@@ -137,7 +137,9 @@ typedef struct {
  * dstate values per token and the scan is bound by HBM. Taken by
  * ssm_selective_scan_fwd, ssm_selective_scan_fwd_from_state and
  * ssm_selective_scan_fwd_static with dstate 16, tile_config_hint 0 or 1, and
- * not together with SSM_FLAG_ZOH; other entry points return SSM_ERR_DIMS.
+ * not together with SSM_FLAG_ZOH; by ssm_state_update (any dstate, also with
+ * SSM_FLAG_ZOH), whose B and C are then [batch, dim, dstate]; other entry
+ * points return SSM_ERR_DIMS.
  */
 #define SSM_FLAG_BC_PER_CHANNEL 2
 
@@ -286,7 +288,8 @@ int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A, con
  *
  *   state            : [batch, dim, dstate] fp32, read and overwritten
  *   x, delta, z, out : [batch, dim] io dtype (z may be NULL)
- *   B, C             : [batch, dstate] io dtype
+ *   B, C             : [batch, dstate] io dtype ([batch, dim, dstate] with
+ *                      SSM_FLAG_BC_PER_CHANNEL in dims->flags)
  *   A, D, delta_bias, delta_softplus : as for the scan
  * dims->seqlen and the workspace fields are ignored.
  */
@@ -391,8 +394,9 @@ int ssm_get_static_status(ssm_stream_t stream);
 /* Bytes of workspace ssm_selective_scan_fwd needs for these sizes (256 when
  * the scan runs in one pass, 0 for empty problems). Depends only on batch,
  * seqlen, dim, dstate, io_dtype, chunk_len_hint, tile_config_hint and flags
- * (per-channel B, C are planned with more L-chunks); returns 0 for invalid
- * sizes. */
+ * (per-channel B, C are planned with more L-chunks) and, when chunk_len_hint
+ * is 0, on the current device's multiprocessor count (148 when no device is
+ * present); returns 0 for invalid sizes. */
 size_t ssm_scan_workspace_bytes(const ssm_dims* dims);
 
 /* Launch plan the scan will use for these sizes (for benchmarks and tests). */

@@ -10,6 +10,7 @@
 
 #include "ssm.h"
 #include "ssm_internal.h"
+#include "ssm_tmap.h"
 
 namespace {
 
@@ -18,31 +19,30 @@ thread_local int g_last_cuda_error = 0;
 constexpr int64_t kMaxDim = int64_t(1) << 31;     // per-axis limit
 constexpr int64_t kMaxElems = int64_t(1) << 40;   // batch * seqlen * dim limit
 // Planning. A CTA of the scan covers channels_per_cta channels of one batch
-// row over one L-chunk, and a B300 SM keeps kResidentCtas of them (shared
-// memory bounds it). Splitting the sequence into K chunks multiplies the CTAs
-// by K, which fills more of the 148 SMs, at the price of scanning every chunk
-// but the last twice (the chunk-state pass costs about kStatePassCost of the
-// output pass per token). The plan takes the K of least modelled time:
+// row over one L-chunk, and an SM keeps several of them. Splitting the
+// sequence into K chunks multiplies the CTAs by K, which fills more of the
+// SMs, at the price of a chunk-state pass over every chunk but the last (about
+// kStatePassCost of the output pass per token). The plan takes the K of least
+// modelled time:
 //   time ~ chunk_len * (wave_cost(output CTAs) + kStatePassCost * wave_cost(state CTAs))
-// where wave_cost(n) sums, over the waves of n CTAs on 148 SMs, the cost of
-// the busiest SM of the wave: 1 for one CTA, kTwoCtaCost for two (two CTAs
-// share an SM's pipes at better than half speed each), plus kSplitCost for
-// the extra launch a split needs (one token of a lone CTA takes about 0.1 us;
-// a launch about 3 us). The constants come from timing the bf16
-// N = 16 workloads (chunk counts 1..64) on a B300.
-constexpr int64_t kSms = 148;
+// where wave_cost(n) sums, over the waves of n CTAs on the device's SMs, the
+// cost of the busiest SM of the wave: 1 for one CTA, kTwoCtaCost for two. The
+// constants are a fit to the measured chunk-count sweeps of the three bf16
+// dstate-16 workloads on a B300 (the fastest measured counts: 37 chunks for b1
+// L131072 d5120, 6 for b4 L2048 d1536, 8-16 for b8 L4096 d2048); the SM count
+// is the current device's (148 when there is none, for host-side planning).
 constexpr int64_t kResidentCtas = 2;
-constexpr double kTwoCtaCost = 1.44;
-constexpr double kStatePassCost = 0.7;
-constexpr double kSplitCost = 30.0;
+constexpr double kTwoCtaCost = 1.2;
+constexpr double kStatePassCost = 0.4;
+constexpr double kSplitCost = 0.0;
 constexpr int64_t kMinChunk = 256;
-constexpr int64_t kMaxChunks = 256;
+constexpr int64_t kMaxChunks = 64;    // the range the sweeps measured
 
-double wave_cost(int64_t ctas) {
-    const int64_t per_wave = kSms * kResidentCtas;
+double wave_cost(int64_t ctas, int64_t sms) {
+    const int64_t per_wave = sms * kResidentCtas;
     const int64_t full = ctas / per_wave, rem = ctas % per_wave;
     double c = double(full) * (kResidentCtas > 1 ? kTwoCtaCost : 1.0);
-    if (rem > 0) c += rem > kSms ? kTwoCtaCost : 1.0;
+    if (rem > 0) c += rem > sms ? kTwoCtaCost : 1.0;
     return c;
 }
 
@@ -94,6 +94,7 @@ int make_plan(const ssm_dims* d, ssm::ScanPlan* p) {
     p->channels_per_cta = ssm::scan_tile_channels(p->tile_cfg);
     p->tiles = (dim + p->channels_per_cta - 1) / p->channels_per_cta;
     const int64_t per_chunk = p->tiles * batch;
+    const int64_t sms = ssm::device_sms();
     int64_t chunk;
     if (d->chunk_len_hint > 0) {
         chunk = d->chunk_len_hint;
@@ -102,18 +103,18 @@ int make_plan(const ssm_dims* d, ssm::ScanPlan* p) {
         // output CTAs per SM keep enough loads in flight (measured best for
         // b4 L2048 d1536: 8 chunks), chunks of at least 128 tokens
         const int64_t k = std::max<int64_t>(
-            1, std::min<int64_t>((5 * kSms / 2 + per_chunk - 1) / per_chunk, L / 128));
+            1, std::min<int64_t>((5 * sms / 2 + per_chunk - 1) / per_chunk, L / 128));
         chunk = ((L + k - 1) / k + TS - 1) / TS * TS;
     } else {
         // modelled time of every chunk count (see the planning note above)
         chunk = (L + TS - 1) / TS * TS;
-        double best = double(chunk) * wave_cost(per_chunk);
+        double best = double(chunk) * wave_cost(per_chunk, sms);
         const int64_t kmax = std::min<int64_t>(kMaxChunks, std::max<int64_t>(1, L / kMinChunk));
         for (int64_t k = 2; k <= kmax; ++k) {
             const int64_t c = ((L + k - 1) / k + TS - 1) / TS * TS;
             const int64_t nk = (L + c - 1) / c;
-            const double t = double(c) * (wave_cost(per_chunk * nk) +
-                                          kStatePassCost * wave_cost(per_chunk * (nk - 1))) +
+            const double t = double(c) * (wave_cost(per_chunk * nk, sms) +
+                                          kStatePassCost * wave_cost(per_chunk * (nk - 1), sms)) +
                              kSplitCost;
             if (t < best) {
                 best = t;
@@ -561,7 +562,7 @@ int ssm_state_update(float* state, const void* x, const void* delta, const float
                      const ssm_dims* dims, ssm_stream_t stream) {
     int rc = check_dims(dims, false);
     if (rc != SSM_OK) return rc;
-    if (dims->flags & SSM_FLAG_BC_PER_CHANNEL) return SSM_ERR_DIMS;
+    const bool bcd = (dims->flags & SSM_FLAG_BC_PER_CHANNEL) != 0;
     if (dims->batch == 0 || dims->dim == 0) return SSM_OK;   // nothing to update
     if (!state || !x || !delta || !A || !B || !C || !out) return SSM_ERR_NULL;
     {
@@ -572,10 +573,11 @@ int ssm_state_update(float* state, const void* x, const void* delta, const float
     const int64_t batch = dims->batch, dim = dims->dim, N = dims->dstate;
     const size_t es = io_size(dims->io_dtype);
     const size_t bd = size_t(batch) * size_t(dim);
+    const size_t rows = (bcd ? bd : size_t(batch)) * size_t(N);   // B, C elements
     {
         const Range in[] = {{x, bd * es},          {delta, bd * es},
-                            {z, bd * es},          {B, size_t(batch) * N * es},
-                            {C, size_t(batch) * N * es}, {A, size_t(dim) * N * 4},
+                            {z, bd * es},          {B, rows * es},
+                            {C, rows * es},        {A, size_t(dim) * N * 4},
                             {D, size_t(dim) * 4},  {delta_bias, size_t(dim) * 4}};
         const Range outs[] = {{out, bd * es}, {state, bd * N * 4}};
         rc = check_alias(in, outs);
@@ -586,6 +588,7 @@ int ssm_state_update(float* state, const void* x, const void* delta, const float
     a.delta_bias = delta_bias; a.softplus = delta_softplus ? 1 : 0; a.out = out;
     a.batch = batch; a.dim = dim;
     a.zoh = (dims->flags & SSM_FLAG_ZOH) ? 1 : 0;
+    a.bc_per_channel = bcd ? 1 : 0;
     return set_cuda(ssm::launch_state_update(a, dims->io_dtype, static_cast<int>(N),
                                              reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -56,41 +56,49 @@ namespace ssm {
 namespace {
 
 constexpr int kN = 16;
-constexpr int kTS = kScanStageTokens;
 constexpr uint32_t kPolls = 1u << 24;      // bound on one mbarrier wait (about a second)
 constexpr uint32_t kStatusTimeout = 7;     // -SSM_ERR_TIMEOUT
 
 // Shared-memory layout of one CTA. A stage holds the x, delta (and z) tiles
-// [kTS][DT] and the B (and C) rows [kTS][16] of 32 tokens; bcf holds the fp32
+// [TS][DT] and the B (and C) rows [TS][16] of TS tokens; bcf holds the fp32
 // B | C rows of the stage being computed and of the next one.
-template <typename T, int W, int NST, int MODE>
+template <typename T, int W, int CPL, int NST, int MODE, int TS>
 struct Lay {
-    static constexpr int DT = 32 * W;                        // channels per CTA
-    static constexpr int TILE = kTS * DT;                    // elements of a tile
+    static constexpr int DT = 32 * W * CPL;                  // channels per CTA
+    static constexpr int TILE = TS * DT;                     // elements of a tile
     static constexpr int TILE_B = TILE * int(sizeof(T));
     static constexpr int NT = MODE == 1 ? 3 : 2;             // x, delta (, z)
     static constexpr int NBC = MODE == 1 ? 2 : 1;            // B (, C)
     static constexpr int ROW = NBC * kN;                     // floats per token in bcf
-    static constexpr int ROWS_B = kTS * kN * int(sizeof(T)); // bytes of one stage's B rows
+    static constexpr int ROWS_B = TS * kN * int(sizeof(T));  // bytes of one stage's B rows
     static constexpr int STAGE = NT * TILE_B + NBC * ROWS_B;
     static constexpr int kDelta = TILE_B;                    // byte offsets in a stage
     static constexpr int kZ = 2 * TILE_B;
     static constexpr int kB = NT * TILE_B;
-    static constexpr int kBC = NST * STAGE;                  // [2][kTS][ROW] f32
-    static constexpr int kBar = kBC + 2 * kTS * ROW * 4;
+    static constexpr int kBC = NST * STAGE;                  // [2][TS][ROW] f32
+    static constexpr int kBar = kBC + 2 * TS * ROW * 4;
     static constexpr int kBytes = kBar + NST * 8;
     static_assert(TILE_B % 128 == 0 && ROWS_B % 128 == 0 && STAGE % 128 == 0,
                   "TMA destinations stay 128-byte aligned");
     static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
+    static_assert(kScanStageTokens % TS == 0, "chunks are whole stages");
 };
 
-__device__ __forceinline__ float ld_io(const float* p) { return *p; }
-__device__ __forceinline__ float ld_io(const __nv_bfloat16* p) {
-    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16);
-}
-__device__ __forceinline__ void st_io(float* p, float v) { *p = v; }
-__device__ __forceinline__ void st_io(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
-
+// CPL consecutive channels of one token row in shared memory (the kernel is
+// written for CPL channels per lane; one is built).
+template <typename T, int CPL> struct Row;
+template <> struct Row<float, 1> {
+    __device__ __forceinline__ static void ld(const float* p, float (&v)[1]) { v[0] = *p; }
+    __device__ __forceinline__ static void st(float* p, const float (&v)[1]) { *p = v[0]; }
+};
+template <> struct Row<__nv_bfloat16, 1> {
+    __device__ __forceinline__ static void ld(const __nv_bfloat16* p, float (&v)[1]) {
+        v[0] = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16);
+    }
+    __device__ __forceinline__ static void st(__nv_bfloat16* p, const float (&v)[1]) {
+        *p = __float2bfloat16_rn(v[0]);
+    }
+};
 __device__ __forceinline__ void ld4(const float* p, float& a, float& b, float& c, float& d) {
     const float4 u = *reinterpret_cast<const float4*>(p);
     a = u.x; b = u.y; c = u.z; d = u.w;
@@ -136,14 +144,19 @@ __device__ __forceinline__ void scaled_powers16(float c, float s, float (&w)[kN]
     }
 }
 
+// The decay factors of a general row: f[n] = 2^(dt A[n] log2 e).
+__device__ __forceinline__ void exps16(float dt, const float (&A2)[kN], float (&f)[kN]) {
+#pragma unroll
+    for (int q = 0; q < kN; q += 2) {
+        const float2 arg = __fmul2_rn(make_float2(dt, dt), make_float2(A2[q], A2[q + 1]));
+        f[q] = ex2(arg.x);
+        f[q + 1] = ex2(arg.y);
+    }
+}
+
 // One token of the recurrence and its readout: h <- f h + dtx B; returns C . h.
-__device__ __forceinline__ float step16(const float (&f)[kN], float dtx, const float* __restrict__ bc,
-                                        float (&h)[kN]) {
-    float Bv[kN], Cv[kN];
-#pragma unroll
-    for (int q = 0; q < kN; q += 4) ld4(bc + q, Bv[q], Bv[q + 1], Bv[q + 2], Bv[q + 3]);
-#pragma unroll
-    for (int q = 0; q < kN; q += 4) ld4(bc + kN + q, Cv[q], Cv[q + 1], Cv[q + 2], Cv[q + 3]);
+__device__ __forceinline__ float step16(const float (&f)[kN], float dtx, const float (&Bv)[kN],
+                                        const float (&Cv)[kN], float (&h)[kN]) {
     const float2 dtx2 = make_float2(dtx, dtx);
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -161,11 +174,7 @@ __device__ __forceinline__ float step16(const float (&f)[kN], float dtx, const f
 }
 
 // One token of the chunk-state sum: H += w B.
-__device__ __forceinline__ void accum16(const float (&w)[kN], const float* __restrict__ bc,
-                                        float (&H)[kN]) {
-    float Bv[kN];
-#pragma unroll
-    for (int q = 0; q < kN; q += 4) ld4(bc + q, Bv[q], Bv[q + 1], Bv[q + 2], Bv[q + 3]);
+__device__ __forceinline__ void accum16(const float (&w)[kN], const float (&Bv)[kN], float (&H)[kN]) {
 #pragma unroll
     for (int q = 0; q < kN; q += 2) {
         const float2 u = __ffma2_rn(make_float2(w[q], w[q + 1]), make_float2(Bv[q], Bv[q + 1]),
@@ -175,14 +184,23 @@ __device__ __forceinline__ void accum16(const float (&w)[kN], const float* __res
     }
 }
 
+template <int K>
+__device__ __forceinline__ void lds_row(const float* p, float (&v)[K]) {
+#pragma unroll
+    for (int q = 0; q < K; q += 4) ld4(p + q, v[q], v[q + 1], v[q + 2], v[q + 3]);
+}
+
 // MODE 1: the output pass. MODE 0: the chunk-state pass (tokens last to first).
-template <typename T, int W, int NST, int MODE, bool SOFTPLUS, bool GATE>
-__global__ void __launch_bounds__(32 * W, 1)
+// Lane l owns the CPL consecutive channels dbase + CPL l + c, c < CPL, and all
+// 16 states of each; one load of B_t (and C_t) serves all of them.
+template <typename T, int W, int CPL, int NST, int TS, int MODE, bool SOFTPLUS, bool GATE>
+__global__ void __launch_bounds__(32 * W, 4)
 scan16_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dt,
               const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
               const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_out,
               const ScanArgs a) {
-    using Ly = Lay<T, W, NST, MODE>;
+    using Ly = Lay<T, W, CPL, NST, MODE, TS>;
+    using RW = Row<T, CPL>;
     constexpr int DT = Ly::DT, ROW = Ly::ROW, THREADS = 32 * W;
     constexpr bool has_z = MODE == 1 && GATE;
 
@@ -197,7 +215,7 @@ scan16_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
     const int64_t k = lin / (a.tiles * a.batch);
     const int64_t t_begin = k * a.chunk_len;
     const int64_t t_end = min(a.L, t_begin + a.chunk_len);
-    const int nstages = static_cast<int>((t_end - t_begin + kTS - 1) / kTS);
+    const int nstages = static_cast<int>((t_end - t_begin + TS - 1) / TS);
     const int64_t dbase = tile * DT;
     const uint32_t stage_tx = static_cast<uint32_t>(
         (has_z ? 3 : 2) * Ly::TILE_B + Ly::NBC * Ly::ROWS_B);
@@ -212,7 +230,7 @@ scan16_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
     auto issue = [&](int i) {   // the i-th stage in visiting order
         const int buf = i % NST;
         unsigned char* dst = smem + static_cast<size_t>(buf) * Ly::STAGE;
-        const int t = static_cast<int>(t_begin + static_cast<int64_t>(stage_of(i)) * kTS);
+        const int t = static_cast<int>(t_begin + static_cast<int64_t>(stage_of(i)) * TS);
         const int bb = static_cast<int>(b);
         mbar_arrive_expect_tx(&full[buf], stage_tx);
         tma_load_3d(dst, &tm_x, static_cast<int>(dbase), t, bb, &full[buf]);
@@ -224,70 +242,80 @@ scan16_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
     if (tid == 0)
         for (int i = 0; i < NST && i < nstages; ++i) issue(i);
 
-    // ---- this lane's channel ----
-    const int col = tid;
-    const int64_t d = dbase + col;
-    const bool ch_ok = d < a.dim;
-    const int64_t dsafe = ch_ok ? d : 0;
-    float Arow[kN];
-    {
-        const float4* ap = reinterpret_cast<const float4*>(a.A + dsafe * kN);
+    // ---- this lane's channels ----
+    const int col = tid * CPL;   // first own channel within the tile
+    bool ch_ok[CPL];
+    int64_t dch[CPL];
+    float A2[CPL][kN], a2[CPL], bias[CPL], Dd[CPL];
+    bool mine = true;   // A[d, n] = A[d, 0] (n + 1) exactly, for every own row
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+        dch[c] = dbase + col + c;
+        ch_ok[c] = dch[c] < a.dim;
+        const int64_t ds = ch_ok[c] ? dch[c] : 0;
+        const float4* ap = reinterpret_cast<const float4*>(a.A + ds * kN);
+        float Arow[kN];
 #pragma unroll
         for (int q = 0; q < kN / 4; ++q) {
             const float4 u = __ldg(ap + q);
             Arow[4 * q] = u.x; Arow[4 * q + 1] = u.y; Arow[4 * q + 2] = u.z; Arow[4 * q + 3] = u.w;
         }
+        bool st = true;
+#pragma unroll
+        for (int n = 1; n < kN; ++n) st = st && (Arow[n] == Arow[0] * float(n + 1));
+        mine = mine && (st || !ch_ok[c]);
+#pragma unroll
+        for (int n = 0; n < kN; ++n) A2[c][n] = ch_ok[c] ? Arow[n] * kLog2e : 0.f;
+        a2[c] = A2[c][0];   // a log2 e (structured rows)
+        bias[c] = (a.delta_bias && ch_ok[c]) ? __ldg(a.delta_bias + ds) : 0.f;
+        Dd[c] = (MODE == 1 && a.D && ch_ok[c]) ? __ldg(a.D + ds) : 0.f;
     }
-    bool mine = true;   // A[d, n] = A[d, 0] (n + 1) exactly
-#pragma unroll
-    for (int n = 1; n < kN; ++n) mine = mine && (Arow[n] == Arow[0] * float(n + 1));
-    const bool structured = __all_sync(0xffffffffu, mine || !ch_ok);
-    float A2[kN];
-#pragma unroll
-    for (int n = 0; n < kN; ++n) A2[n] = ch_ok ? Arow[n] * kLog2e : 0.f;
-    const float a2 = A2[0];   // a log2 e (structured rows)
-    const float bias = (a.delta_bias && ch_ok) ? __ldg(a.delta_bias + dsafe) : 0.f;
-    const float Dd = (MODE == 1 && a.D && ch_ok) ? __ldg(a.D + dsafe) : 0.f;
+    const bool structured = __all_sync(0xffffffffu, mine);
 
-    float h[kN];
+    float h[CPL][kN];
 #pragma unroll
-    for (int n = 0; n < kN; ++n) h[n] = 0.f;
-    if (MODE == 1 && ch_ok) {
-        if (a.h0) {
-            const float4* hp = reinterpret_cast<const float4*>(a.h0 + (b * a.dim + d) * kN);
+    for (int c = 0; c < CPL; ++c) {
 #pragma unroll
-            for (int q = 0; q < kN / 4; ++q) {
-                const float4 u = hp[q];
-                h[4 * q] = u.x; h[4 * q + 1] = u.y; h[4 * q + 2] = u.z; h[4 * q + 3] = u.w;
+        for (int n = 0; n < kN; ++n) h[c][n] = 0.f;
+        if (MODE == 1 && ch_ok[c]) {
+            if (a.h0) {
+                const float4* hp =
+                    reinterpret_cast<const float4*>(a.h0 + (b * a.dim + dch[c]) * kN);
+#pragma unroll
+                for (int q = 0; q < kN / 4; ++q) {
+                    const float4 u = hp[q];
+                    h[c][4 * q] = u.x; h[c][4 * q + 1] = u.y; h[c][4 * q + 2] = u.z;
+                    h[c][4 * q + 3] = u.w;
+                }
             }
-        }
-        // the state entering chunk k: h <- exp(A S_i) h + H_i over chunks 0 .. k-1
-        for (int64_t i = 0; i < k; ++i) {
-            const int64_t idx = (b * (a.nchunks - 1) + i) * a.dim + d;
-            const float S = a.ws_S[idx];
-            const float4* Hp = reinterpret_cast<const float4*>(a.ws_H + idx * kN);
+            // the state entering chunk k: h <- exp(A S_i) h + H_i over chunks 0 .. k-1
+            for (int64_t i = 0; i < k; ++i) {
+                const int64_t idx = (b * (a.nchunks - 1) + i) * a.dim + dch[c];
+                const float S = a.ws_S[idx];
+                const float4* Hp = reinterpret_cast<const float4*>(a.ws_H + idx * kN);
 #pragma unroll
-            for (int q = 0; q < kN / 4; ++q) {
-                const float4 u = Hp[q];
-                h[4 * q] = fmaf(ex2(A2[4 * q] * S), h[4 * q], u.x);
-                h[4 * q + 1] = fmaf(ex2(A2[4 * q + 1] * S), h[4 * q + 1], u.y);
-                h[4 * q + 2] = fmaf(ex2(A2[4 * q + 2] * S), h[4 * q + 2], u.z);
-                h[4 * q + 3] = fmaf(ex2(A2[4 * q + 3] * S), h[4 * q + 3], u.w);
+                for (int q = 0; q < kN / 4; ++q) {
+                    const float4 u = Hp[q];
+                    h[c][4 * q] = fmaf(ex2(A2[c][4 * q] * S), h[c][4 * q], u.x);
+                    h[c][4 * q + 1] = fmaf(ex2(A2[c][4 * q + 1] * S), h[c][4 * q + 1], u.y);
+                    h[c][4 * q + 2] = fmaf(ex2(A2[c][4 * q + 2] * S), h[c][4 * q + 2], u.z);
+                    h[c][4 * q + 3] = fmaf(ex2(A2[c][4 * q + 3] * S), h[c][4 * q + 3], u.w);
+                }
             }
         }
     }
 
     // ---- B (and C) rows of a stage -> fp32 bcf[slot][t][B | C] ----
     constexpr int VE = 16 / int(sizeof(T));               // elements per 16-byte vector
-    constexpr int NVEC = Ly::NBC * kTS * kN / VE;
+    constexpr int NVEC = Ly::NBC * TS * kN / VE;
     auto convert_bc = [&](int i) {
         const unsigned char* staged = smem + static_cast<size_t>(i % NST) * Ly::STAGE + Ly::kB;
-        float* dst = bcf + (i & 1) * kTS * ROW;
+        float* dst = bcf + (i & 1) * TS * ROW;
         for (int idx = tid; idx < NVEC; idx += THREADS) {
-            const int which = idx / (kTS * kN / VE);
-            const int r = idx % (kTS * kN / VE);
+            const int which = idx / (TS * kN / VE);
+            const int r = idx % (TS * kN / VE);
             const int t = r / (kN / VE), n0 = (r % (kN / VE)) * VE;
-            const unsigned char* src = staged + (which * kTS * kN + t * kN + n0) * int(sizeof(T));
+            const unsigned char* src = staged + (which * TS * kN + t * kN + n0) * int(sizeof(T));
             float* o = dst + t * ROW + which * kN + n0;
             if constexpr (sizeof(T) == 2) {
                 const uint4 u = *reinterpret_cast<const uint4*>(src);
@@ -309,103 +337,120 @@ scan16_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
 
     // chunk-state pass: dt summed over the later stages (Rb) and, within a
     // stage, over the tokens after the current one (Rl): R = Rb + Rl
-    float Rb = 0.f;
+    float Rb[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) Rb[c] = 0.f;
 
     int i = 0;
     for (; i < nstages && !aborted; ++i) {
         const int buf = i % NST;
         unsigned char* stg = smem + static_cast<size_t>(buf) * Ly::STAGE;
-        T* xt = reinterpret_cast<T*>(stg);
-        const T* dlt = reinterpret_cast<const T*>(stg + Ly::kDelta);
-        const T* zt = reinterpret_cast<const T*>(stg + Ly::kZ);
-        const float* bc = bcf + (i & 1) * kTS * ROW;
-        const int64_t t0 = t_begin + static_cast<int64_t>(stage_of(i)) * kTS;
+        T* xt = reinterpret_cast<T*>(stg) + col;
+        const T* dlt = reinterpret_cast<const T*>(stg + Ly::kDelta) + col;
+        const T* zt = reinterpret_cast<const T*>(stg + Ly::kZ) + col;
+        const float* bc = bcf + (i & 1) * TS * ROW;
+        const int64_t t0 = t_begin + static_cast<int64_t>(stage_of(i)) * TS;
         ok = i == 0 || mbar_wait_bounded(&full[buf], static_cast<uint32_t>((i / NST) & 1), kPolls);
-        const int lim = static_cast<int>(t_end - t0 < kTS ? t_end - t0 : kTS);   // valid tokens
+        const int lim = static_cast<int>(t_end - t0 < TS ? t_end - t0 : TS);   // valid tokens
 
         // the token's x, dt (0 past the sequence end: h unchanged) and dt x
-        auto prep = [&](int tl, float& xv, float& dt, float& dtx) {
-            xv = ld_io(xt + tl * DT + col);
-            float v = ld_io(dlt + tl * DT + col) + bias;
-            if constexpr (SOFTPLUS) v = softplus(v);
-            dt = tl < lim ? v : 0.f;
-            dtx = dt * xv;
+        auto prep = [&](int tl, float (&xv)[CPL], float (&dt)[CPL], float (&dtx)[CPL]) {
+            float dv[CPL];
+            RW::ld(xt + tl * DT, xv);
+            RW::ld(dlt + tl * DT, dv);
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                float v = dv[c] + bias[c];
+                if constexpr (SOFTPLUS) v = softplus(v);
+                dt[c] = tl < lim ? v : 0.f;
+                dtx[c] = dt[c] * xv[c];
+            }
         };
 
         if constexpr (MODE == 1) {
             // software-pipelined by one token: the next token's x, dt, dt x
             // are formed before this token's update
-            float xc, dc, dxc;
+            float xc[CPL], dc[CPL], dxc[CPL];
             prep(0, xc, dc, dxc);
+            auto token = [&](int tl, bool st_path) {
+                float xn[CPL], dn[CPL], dxn[CPL];
+                prep((tl + 1) & (TS - 1), xn, dn, dxn);
+                float Bv[kN], Cv[kN];
+                lds_row<kN>(bc + tl * ROW, Bv);
+                lds_row<kN>(bc + tl * ROW + kN, Cv);
+                float y[CPL], zv[CPL];
+                if constexpr (has_z) RW::ld(zt + tl * DT, zv);
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) {
+                    float f[kN];
+                    if (st_path)
+                        powers16(dc[c] * a2[c], f);
+                    else
+                        exps16(dc[c], A2[c], f);
+                    y[c] = fmaf(Dd[c], xc[c], step16(f, dxc[c], Bv, Cv, h[c]));
+                    if constexpr (has_z) y[c] *= silu(zv[c]);
+                }
+                RW::st(xt + tl * DT, y);   // in place over x (already read)
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) {
+                    xc[c] = xn[c]; dc[c] = dn[c]; dxc[c] = dxn[c];
+                }
+            };
             if (structured) {
 #pragma unroll 4
-                for (int tl = 0; tl < kTS; ++tl) {
-                    float xn, dn, dxn;
-                    prep((tl + 1) & (kTS - 1), xn, dn, dxn);
-                    float f[kN];
-                    powers16(dc * a2, f);
-                    float y = step16(f, dxc, bc + tl * ROW, h);
-                    y = fmaf(Dd, xc, y);
-                    if constexpr (has_z) y *= silu(ld_io(zt + tl * DT + col));
-                    st_io(xt + tl * DT + col, y);   // in place over x (already read)
-                    xc = xn; dc = dn; dxc = dxn;
-                }
+                for (int tl = 0; tl < TS; ++tl) token(tl, true);
             } else {
 #pragma unroll 4
-                for (int tl = 0; tl < kTS; ++tl) {
-                    float xn, dn, dxn;
-                    prep((tl + 1) & (kTS - 1), xn, dn, dxn);
-                    float f[kN];
-#pragma unroll
-                    for (int q = 0; q < kN; q += 2) {
-                        const float2 arg = __fmul2_rn(make_float2(dc, dc), make_float2(A2[q], A2[q + 1]));
-                        f[q] = ex2(arg.x);
-                        f[q + 1] = ex2(arg.y);
-                    }
-                    float y = step16(f, dxc, bc + tl * ROW, h);
-                    y = fmaf(Dd, xc, y);
-                    if constexpr (has_z) y *= silu(ld_io(zt + tl * DT + col));
-                    st_io(xt + tl * DT + col, y);
-                    xc = xn; dc = dn; dxc = dxn;
-                }
+                for (int tl = 0; tl < TS; ++tl) token(tl, false);
             }
         } else {
             // chunk state: tokens last to first; h accumulates sum_t w_t B_t
-            float Rl = 0.f;
-            if (structured) {
-                const float sb = a2 * Rb;
-#pragma unroll 4
-                for (int tl = kTS - 1; tl >= 0; --tl) {
-                    float xv, dt, dtx;
-                    prep(tl, xv, dt, dtx);
-                    float w[kN];
-                    scaled_powers16(dtx, fmaf(a2, Rl, sb), w);
-                    accum16(w, bc + tl * ROW, h);
-                    Rl += dt;
-                }
-            } else {
-                float base[kN];
+            float Rl[CPL], sb[CPL], base[CPL][kN];
 #pragma unroll
-                for (int n = 0; n < kN; ++n) base[n] = A2[n] * Rb;
-#pragma unroll 4
-                for (int tl = kTS - 1; tl >= 0; --tl) {
-                    float xv, dt, dtx;
-                    prep(tl, xv, dt, dtx);
-                    float w[kN];
-#pragma unroll
-                    for (int q = 0; q < kN; q += 2) {
-                        const float2 arg = __ffma2_rn(make_float2(A2[q], A2[q + 1]), make_float2(Rl, Rl),
-                                                      make_float2(base[q], base[q + 1]));
-                        const float2 g = make_float2(ex2(arg.x), ex2(arg.y));
-                        const float2 u = __fmul2_rn(make_float2(dtx, dtx), g);
-                        w[q] = u.x;
-                        w[q + 1] = u.y;
-                    }
-                    accum16(w, bc + tl * ROW, h);
-                    Rl += dt;
-                }
+            for (int c = 0; c < CPL; ++c) {
+                Rl[c] = 0.f;
+                sb[c] = a2[c] * Rb[c];
             }
-            Rb += Rl;
+            auto token = [&](int tl, bool st_path) {
+                float xv[CPL], dt[CPL], dtx[CPL];
+                prep(tl, xv, dt, dtx);
+                float Bv[kN];
+                lds_row<kN>(bc + tl * ROW, Bv);
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) {
+                    float w[kN];
+                    if (st_path) {
+                        scaled_powers16(dtx[c], fmaf(a2[c], Rl[c], sb[c]), w);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < kN; q += 2) {
+                            const float2 arg =
+                                __ffma2_rn(make_float2(A2[c][q], A2[c][q + 1]),
+                                           make_float2(Rl[c], Rl[c]),
+                                           make_float2(base[c][q], base[c][q + 1]));
+                            const float2 u = __fmul2_rn(make_float2(dtx[c], dtx[c]),
+                                                        make_float2(ex2(arg.x), ex2(arg.y)));
+                            w[q] = u.x;
+                            w[q + 1] = u.y;
+                        }
+                    }
+                    accum16(w, Bv, h[c]);
+                    Rl[c] += dt[c];
+                }
+            };
+            if (structured) {
+#pragma unroll 4
+                for (int tl = TS - 1; tl >= 0; --tl) token(tl, true);
+            } else {
+#pragma unroll
+                for (int c = 0; c < CPL; ++c)
+#pragma unroll
+                    for (int n = 0; n < kN; ++n) base[c][n] = A2[c][n] * Rb[c];
+#pragma unroll 4
+                for (int tl = TS - 1; tl >= 0; --tl) token(tl, false);
+            }
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) Rb[c] += Rl[c];
         }
 
         // B / C of the next stage (its bcf half was last read during stage i - 1)
@@ -419,7 +464,7 @@ scan16_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         if (tid == 0 && !aborted) {
             if constexpr (MODE == 1) {
                 tma_store_3d(&tm_out, static_cast<int>(dbase), static_cast<int>(t0),
-                             static_cast<int>(b), xt);
+                             static_cast<int>(b), stg);
                 bulk_commit();
                 // the buffer is refilled once the store has read it
                 bulk_wait_read<0>();
@@ -440,26 +485,29 @@ scan16_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         }
         return;
     }
-    if (!ch_ok) return;
-    if (MODE == 0) {
-        const int64_t idx = (b * (a.nchunks - 1) + k) * a.dim + d;
-        float4* Hp = reinterpret_cast<float4*>(a.ws_H + idx * kN);
 #pragma unroll
-        for (int q = 0; q < kN / 4; ++q)
-            Hp[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-        a.ws_S[idx] = Rb;
-    } else if (a.final_state && k == a.nchunks - 1) {
-        float4* fs = reinterpret_cast<float4*>(a.final_state + (b * a.dim + d) * kN);
+    for (int c = 0; c < CPL; ++c) {
+        if (!ch_ok[c]) continue;
+        if (MODE == 0) {
+            const int64_t idx = (b * (a.nchunks - 1) + k) * a.dim + dch[c];
+            float4* Hp = reinterpret_cast<float4*>(a.ws_H + idx * kN);
 #pragma unroll
-        for (int q = 0; q < kN / 4; ++q)
-            fs[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+            for (int q = 0; q < kN / 4; ++q)
+                Hp[q] = make_float4(h[c][4 * q], h[c][4 * q + 1], h[c][4 * q + 2], h[c][4 * q + 3]);
+            a.ws_S[idx] = Rb[c];
+        } else if (a.final_state && k == a.nchunks - 1) {
+            float4* fs = reinterpret_cast<float4*>(a.final_state + (b * a.dim + dch[c]) * kN);
+#pragma unroll
+            for (int q = 0; q < kN / 4; ++q)
+                fs[q] = make_float4(h[c][4 * q], h[c][4 * q + 1], h[c][4 * q + 2], h[c][4 * q + 3]);
+        }
     }
 }
 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-template <typename T, int W, int NST, int MODE, bool SP, bool GATE>
+template <typename T, int W, int CPL, int NST, int TS, int MODE, bool SP, bool GATE>
 cudaError_t allow_smem16() {
     static std::mutex mu;
     static bool done[128] = {};
@@ -469,49 +517,50 @@ cudaError_t allow_smem16() {
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(scan16_kernel<T, W, NST, MODE, SP, GATE>,
+    e = cudaFuncSetAttribute(scan16_kernel<T, W, CPL, NST, TS, MODE, SP, GATE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Lay<T, W, NST, MODE>::kBytes);
+                             Lay<T, W, CPL, NST, MODE, TS>::kBytes);
     if (e == cudaSuccess) done[dev] = true;
     return e;
 }
 
-template <typename T, int W, int NST, bool SP, bool GATE>
+template <typename T, int W, int CPL, int NST, int TS, bool SP, bool GATE>
 cudaError_t launch16_flags(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
-    constexpr int DT = 32 * W;
+    constexpr int DT = 32 * W * CPL;
     if (p.channels_per_cta != DT) return cudaErrorInvalidValue;
     CUtensorMap tx, tdt, tz, tB, tC;
     cudaError_t e;
-    if ((e = make_tmap_cached<T>(&tx, a.x, a.batch, a.L, a.dim, DT)) != cudaSuccess) return e;
-    if ((e = make_tmap_cached<T>(&tdt, a.delta, a.batch, a.L, a.dim, DT)) != cudaSuccess) return e;
+    if ((e = make_tmap_cached<T>(&tx, a.x, a.batch, a.L, a.dim, DT, TS)) != cudaSuccess) return e;
+    if ((e = make_tmap_cached<T>(&tdt, a.delta, a.batch, a.L, a.dim, DT, TS)) != cudaSuccess) return e;
     CUtensorMap tout;
-    if ((e = make_tmap_cached<T>(&tout, a.out, a.batch, a.L, a.dim, DT)) != cudaSuccess) return e;
+    if ((e = make_tmap_cached<T>(&tout, a.out, a.batch, a.L, a.dim, DT, TS)) != cudaSuccess) return e;
     tz = tx;
-    if (GATE && (e = make_tmap_cached<T>(&tz, a.z, a.batch, a.L, a.dim, DT)) != cudaSuccess) return e;
-    if ((e = make_tmap_cached<T>(&tB, a.B, a.batch, a.L, kN, kN)) != cudaSuccess) return e;
-    if ((e = make_tmap_cached<T>(&tC, a.C, a.batch, a.L, kN, kN)) != cudaSuccess) return e;
+    if (GATE && (e = make_tmap_cached<T>(&tz, a.z, a.batch, a.L, a.dim, DT, TS)) != cudaSuccess)
+        return e;
+    if ((e = make_tmap_cached<T>(&tB, a.B, a.batch, a.L, kN, kN, TS)) != cudaSuccess) return e;
+    if ((e = make_tmap_cached<T>(&tC, a.C, a.batch, a.L, kN, kN, TS)) != cudaSuccess) return e;
     const int64_t per_chunk = p.tiles * a.batch;
     if (p.nchunks > 1) {
-        if ((e = allow_smem16<T, W, NST, 0, SP, false>()) != cudaSuccess) return e;
-        scan16_kernel<T, W, NST, 0, SP, false>
+        if ((e = allow_smem16<T, W, CPL, NST, TS, 0, SP, false>()) != cudaSuccess) return e;
+        scan16_kernel<T, W, CPL, NST, TS, 0, SP, false>
             <<<static_cast<unsigned>(per_chunk * (p.nchunks - 1)), 32 * W,
-               Lay<T, W, NST, 0>::kBytes, s>>>(tx, tdt, tz, tB, tC, tout, a);
+               Lay<T, W, CPL, NST, 0, TS>::kBytes, s>>>(tx, tdt, tz, tB, tC, tout, a);
     }
-    if ((e = allow_smem16<T, W, NST, 1, SP, GATE>()) != cudaSuccess) return e;
-    scan16_kernel<T, W, NST, 1, SP, GATE>
-        <<<static_cast<unsigned>(per_chunk * p.nchunks), 32 * W, Lay<T, W, NST, 1>::kBytes, s>>>(
-            tx, tdt, tz, tB, tC, tout, a);
+    if ((e = allow_smem16<T, W, CPL, NST, TS, 1, SP, GATE>()) != cudaSuccess) return e;
+    scan16_kernel<T, W, CPL, NST, TS, 1, SP, GATE>
+        <<<static_cast<unsigned>(per_chunk * p.nchunks), 32 * W,
+           Lay<T, W, CPL, NST, 1, TS>::kBytes, s>>>(tx, tdt, tz, tB, tC, tout, a);
     return cudaGetLastError();
 }
 
-template <typename T, int W, int NST>
+template <typename T, int W, int CPL, int NST, int TS>
 cudaError_t launch16_cfg(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     const bool sp = a.softplus != 0, gate = a.z != nullptr;
     if (sp)
-        return gate ? launch16_flags<T, W, NST, true, true>(a, p, s)
-                    : launch16_flags<T, W, NST, true, false>(a, p, s);
-    return gate ? launch16_flags<T, W, NST, false, true>(a, p, s)
-                : launch16_flags<T, W, NST, false, false>(a, p, s);
+        return gate ? launch16_flags<T, W, CPL, NST, TS, true, true>(a, p, s)
+                    : launch16_flags<T, W, CPL, NST, TS, true, false>(a, p, s);
+    return gate ? launch16_flags<T, W, CPL, NST, TS, false, true>(a, p, s)
+                : launch16_flags<T, W, CPL, NST, TS, false, false>(a, p, s);
 }
 
 }  // namespace
@@ -519,7 +568,12 @@ cudaError_t launch16_cfg(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
 cudaError_t launch_scan16(const ScanArgs& a, const ScanPlan& p, int io, cudaStream_t s) {
     // bf16: 4 warps (128 channels), a 2-stage ring; fp32 I/O: the same tile,
     // whose larger stages still fit twice
-    return io == 1 ? launch16_cfg<__nv_bfloat16, 4, 2>(a, p, s) : launch16_cfg<float, 4, 2>(a, p, s);
+    // 4 warps (128 channels) of one channel per lane, 32-token stages, a
+    // 2-stage ring: the fastest of the measured layouts (two channels per
+    // lane, and 16-token stages with 4 CTAs per SM, measured slower or equal)
+    constexpr int CPL = 1, W = 4, TS = 32, NST = 2;
+    return io == 1 ? launch16_cfg<__nv_bfloat16, W / CPL, CPL, NST, TS>(a, p, s)
+                   : launch16_cfg<float, W / CPL, CPL, NST, TS>(a, p, s);
 }
 
 }  // namespace ssm

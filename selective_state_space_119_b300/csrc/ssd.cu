@@ -64,8 +64,8 @@ constexpr int oHl = oHh + kBlk;
 constexpr int oDt = oHl + kBlk;                // dt [Q] f32
 constexpr int oS2 = oDt + kQ * 4;              // s log2 e [Q] f32
 constexpr int oWs = oS2 + kQ * 4;              // warp partial sums [4] f32
-constexpr int oBar = oWs + 64;                 // mbarriers: load, mma
-constexpr int oTm = oBar + 16;                 // TMEM base address
+constexpr int oBar = oWs + 64;                 // mbarriers: B, C, X loads, mma
+constexpr int oTm = oBar + 32;                 // TMEM base address
 constexpr int kSmemUsed = oTm + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -155,8 +155,12 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     float* sdt = reinterpret_cast<float*>(sm + oDt);
     float* ss2 = reinterpret_cast<float*>(sm + oS2);
     float* swarp = reinterpret_cast<float*>(sm + oWs);
-    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + oBar);
-    uint64_t* bar_mma = bar_ld + 1;
+    // one load barrier per tile, so that each tile's next load can start as
+    // soon as the products that read it have completed
+    uint64_t* bar_B = reinterpret_cast<uint64_t*>(sm + oBar);
+    uint64_t* bar_C = bar_B + 1;
+    uint64_t* bar_X = bar_B + 2;
+    uint64_t* bar_mma = bar_B + 3;
     uint32_t* tm_slot = reinterpret_cast<uint32_t*>(sm + oTm);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -169,7 +173,9 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     const uint32_t sbase = smem_u32(sm);
 
     if (tid == 0) {
-        mbar_init(bar_ld, 1);
+        mbar_init(bar_B, 1);
+        mbar_init(bar_C, 1);
+        mbar_init(bar_X, 1);
         mbar_init(bar_mma, 1);
         fence_mbar_init();
     }
@@ -200,20 +206,38 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         }
     }
 
-    uint32_t ld_phase = 0, mma_phase = 0;
-    bool ok = true, load_pending = false;
+    const int gg = static_cast<int>(g), bb = static_cast<int>(b), hh = static_cast<int>(hd);
+    // the barrier phase of each tile's load in flight, -1 for none (thread 0
+    // only; the abort path waits for them)
+    int pend_B = -1, pend_C = -1, pend_X = -1;
+    auto load_B = [&](int c) {
+        mbar_arrive_expect_tx(bar_B, 2 * kBlk);
+        tma_load_4d(sm + oB, &tm_B, 0, gg, c * kQ, bb, bar_B);
+        tma_load_4d(sm + oB + kBlk, &tm_B, 64, gg, c * kQ, bb, bar_B);
+        pend_B = c & 1;
+    };
+    auto load_C = [&](int c) {
+        mbar_arrive_expect_tx(bar_C, 2 * kBlk);
+        tma_load_4d(sm + oC, &tm_C, 0, gg, c * kQ, bb, bar_C);
+        tma_load_4d(sm + oC + kBlk, &tm_C, 64, gg, c * kQ, bb, bar_C);
+        pend_C = c & 1;
+    };
+    auto load_X = [&](int c) {
+        mbar_arrive_expect_tx(bar_X, kBlk);
+        tma_load_4d(sm + oX, &tm_x, 0, hh, c * kQ, bb, bar_X);
+        pend_X = c & 1;
+    };
+    if (tid == 0) {
+        load_B(0);
+        load_C(0);
+        load_X(0);
+    }
+
+    uint32_t mma_phase = 0;
+    bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
         const int t0 = c * kQ;
-        if (tid == 0) {
-            mbar_arrive_expect_tx(bar_ld, 2 * 2 * kBlk + kBlk);
-            const int gg = static_cast<int>(g), bb = static_cast<int>(b);
-            tma_load_4d(sm + oC, &tm_C, 0, gg, t0, bb, bar_ld);
-            tma_load_4d(sm + oC + kBlk, &tm_C, 64, gg, t0, bb, bar_ld);
-            tma_load_4d(sm + oB, &tm_B, 0, gg, t0, bb, bar_ld);
-            tma_load_4d(sm + oB + kBlk, &tm_B, 64, gg, t0, bb, bar_ld);
-            tma_load_4d(sm + oX, &tm_x, 0, static_cast<int>(hd), t0, bb, bar_ld);
-            load_pending = true;
-        }
+        const uint32_t ld_phase = static_cast<uint32_t>(c & 1);   // each tile loads once per chunk
         // dt of the chunk (0 past the sequence end), then s = A * cumsum(dt)
         {
             const int64_t t = t0 + tid;
@@ -236,9 +260,9 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             ss2[tid] = cs * A2;   // s_t log2 e
         }
         // (the next read of swarp is a chunk later, after several barriers)
-        ok = mbar_wait_bounded(bar_ld, ld_phase, kPolls);
-        if (ok) load_pending = false;
-        ld_phase ^= 1;
+        ok = mbar_wait_bounded(bar_B, ld_phase, kPolls) && mbar_wait_bounded(bar_C, ld_phase, kPolls) &&
+             mbar_wait_bounded(bar_X, ld_phase, kPolls);
+        if (ok) pend_B = pend_C = pend_X = -1;
         __syncthreads();   // ss2 complete
         const float s_end = ss2[kQ - 1];
         // w o X (high and remainder), row u = this thread, w_u = exp(s_end - s_u) dt_u
@@ -283,6 +307,8 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         ok = ok && mbar_wait_bounded(bar_mma, mma_phase, kPolls);
         mma_phase ^= 1;
         tc::fence_after_sync();
+        // G and S^T are done with the B tile: the next chunk's B can land
+        if (ok && tid == 0 && c + 1 < nchunks) load_B(c + 1);
         // M = G o decay o dt (row t = this thread), high and remainder
         {
             const int t = tid;
@@ -339,6 +365,8 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         ok = ok && mbar_wait_bounded(bar_mma, mma_phase, kPolls);
         mma_phase ^= 1;
         tc::fence_after_sync();
+        // Y2 is done with the C tile: the next chunk's C can land
+        if (ok && tid == 0 && c + 1 < nchunks) load_C(c + 1);
         // epilogue: y = Y + exp(s_t) Y2 + D x (row t), in place over x;
         // state: h <- exp(s_end) h + S (row n = this thread)
         {
@@ -387,6 +415,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             tma_store_4d(&tm_y, 0, static_cast<int>(hd), t0, static_cast<int>(b), sm + oX);
             bulk_commit();
             bulk_wait_read<0>();   // the X tile is reloaded by the next chunk
+            if (c + 1 < nchunks) load_X(c + 1);
         }
         __syncthreads();
     }
@@ -394,7 +423,10 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     if (!ok) {
         if (tid == 0) {
             // let a load in flight land before the CTA releases its memory
-            if (load_pending) mbar_wait_bounded(bar_ld, ld_phase ^ 1, kPolls);
+            // (each tile load still in flight is waited for once more, bounded)
+            if (pend_B >= 0) mbar_wait_bounded(bar_B, static_cast<uint32_t>(pend_B), kPolls);
+            if (pend_C >= 0) mbar_wait_bounded(bar_C, static_cast<uint32_t>(pend_C), kPolls);
+            if (pend_X >= 0) mbar_wait_bounded(bar_X, static_cast<uint32_t>(pend_X), kPolls);
             if (a.status) atomicExch(a.status, kStatusTimeout);
         }
     } else if (a.final_state) {

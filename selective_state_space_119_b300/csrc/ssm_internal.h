@@ -84,6 +84,7 @@ struct StepArgs {
     void* out;
     int64_t batch, dim;
     int zoh;              // exact zero-order-hold Bbar instead of dt * B
+    int bc_per_channel;   // B, C of shape [batch, dim, N] instead of [batch, N]
 };
 
 // Tokens between two saved states of a checkpointing forward (the backward

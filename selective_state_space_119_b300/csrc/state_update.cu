@@ -8,6 +8,9 @@
 // y = C . h + D x, out = y * silu(z); the fp32 state is updated in place.
 // With the exact zero-order hold ("State-space models (Mamba, S4)", "From
 // Continuous to Discrete: The Key Step") the input term is (e^{dt A} - 1)/A B x.
+// With per-channel B, C ("Mamba: State Space Models Challenge Transformers",
+// "Selective Scan Algorithm": B, C of shape [B, L, D, N]) the token's rows are
+// [batch, dim, N], one per channel, read like the state.
 //
 // The step is bound by HBM traffic on the state (N fp32 read + written per
 // channel). LANES = N / NPL lanes share a channel, each holding NPL = 4 states
@@ -60,7 +63,7 @@ __device__ __forceinline__ float zoh_m(float dt, float A, float dA) {
     return fabsf(zz) < 0.1f ? dt * p : (dA - 1.f) / A;
 }
 
-template <typename T, int N, bool ZOH>
+template <typename T, int N, bool ZOH, bool BCD>
 __global__ void __launch_bounds__(kStepThreads) state_update_kernel(const StepArgs a) {
     constexpr int NPL = N >= 4 ? 4 : N;        // states per lane
     constexpr int LANES = N / NPL;             // lanes per channel (1, 2 or 4)
@@ -115,8 +118,10 @@ __global__ void __launch_bounds__(kStepThreads) state_update_kernel(const StepAr
 #pragma unroll
             for (int j = 0; j < NPL; ++j) h[it][j] = __ldcs(st + j);
         }
-        ld_vec<T, NPL>(Bg + b * N + n0, Bv[it]);
-        ld_vec<T, NPL>(Cg + b * N + n0, Cv[it]);
+        // shared rows [batch, N], or the channel's own rows [batch, dim, N]
+        const int64_t row = BCD ? c : b;
+        ld_vec<T, NPL>(Bg + row * N + n0, Bv[it]);
+        ld_vec<T, NPL>(Cg + row * N + n0, Cv[it]);
     }
 
     // ---- arithmetic and stores ----
@@ -155,7 +160,7 @@ __global__ void __launch_bounds__(kStepThreads) state_update_kernel(const StepAr
     }
 }
 
-template <typename T, int N, bool ZOH>
+template <typename T, int N, bool ZOH, bool BCD>
 cudaError_t launch_zoh(const StepArgs& a, cudaStream_t s) {
     constexpr int NPL = N >= 4 ? 4 : N;
     constexpr int CH_PER_CTA = kStepThreads / (N / NPL);
@@ -170,18 +175,20 @@ cudaError_t launch_zoh(const StepArgs& a, cudaStream_t s) {
         p.delta = static_cast<const T*>(a.delta) + e;
         p.z = a.z ? static_cast<const T*>(a.z) + e : nullptr;
         p.out = static_cast<T*>(a.out) + e;
-        p.B = static_cast<const T*>(a.B) + b0 * N;
-        p.C = static_cast<const T*>(a.C) + b0 * N;
+        p.B = static_cast<const T*>(a.B) + (BCD ? e : b0) * N;
+        p.C = static_cast<const T*>(a.C) + (BCD ? e : b0) * N;
         const dim3 grid(static_cast<unsigned>((a.dim + CH_PER_CTA - 1) / CH_PER_CTA),
                         static_cast<unsigned>((p.batch + kItems - 1) / kItems));
-        state_update_kernel<T, N, ZOH><<<grid, kStepThreads, 0, s>>>(p);
+        state_update_kernel<T, N, ZOH, BCD><<<grid, kStepThreads, 0, s>>>(p);
     }
     return cudaGetLastError();
 }
 
 template <typename T, int N>
 cudaError_t launch_typed(const StepArgs& a, cudaStream_t s) {
-    return a.zoh ? launch_zoh<T, N, true>(a, s) : launch_zoh<T, N, false>(a, s);
+    if (a.bc_per_channel)
+        return a.zoh ? launch_zoh<T, N, true, true>(a, s) : launch_zoh<T, N, false, true>(a, s);
+    return a.zoh ? launch_zoh<T, N, true, false>(a, s) : launch_zoh<T, N, false, false>(a, s);
 }
 
 template <typename T>

@@ -400,7 +400,8 @@ def _static_call(x, delta, A, B, C, D, z, delta_bias, delta_softplus, out, final
 def ssm_state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
                      delta_softplus=False, out=None, stream=None, zoh=False):
     """One recurrent step; ``state`` [batch, dim, N] fp32 is updated in place.
-    x, delta, z: [batch, dim]; B, C: [batch, N]. Returns out [batch, dim].
+    x, delta, z: [batch, dim]; B, C: [batch, N], or [batch, dim, N] (one row
+    per channel: SSM_FLAG_BC_PER_CHANNEL). Returns out [batch, dim].
     ``zoh=True`` takes the exact zero-order-hold Bbar."""
     torch = _torch()
     batch, dim, N = state.shape
@@ -409,14 +410,17 @@ def ssm_state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
     if out is None:
         with _launch_on(dev, stream):
             out = torch.empty_like(x)
-    dims = make_dims(batch, 1, dim, N, _io_code(x), flags=SSM_FLAG_ZOH if zoh else 0)
+    bcd = B.dim() == 3
+    flags = (SSM_FLAG_ZOH if zoh else 0) | (SSM_FLAG_BC_PER_CHANNEL if bcd else 0)
+    rows = (batch, dim, N) if bcd else (batch, N)
+    dims = make_dims(batch, 1, dim, N, _io_code(x), flags=flags)
     args = (
         _ptr(state, "state", torch.float32, (batch, dim, N), dev),
         _ptr(x, "x", io, (batch, dim), dev),
         _ptr(delta, "delta", io, (batch, dim), dev),
         _ptr(A, "A", torch.float32, (dim, N), dev),
-        _ptr(B, "B", io, (batch, N), dev),
-        _ptr(C, "C", io, (batch, N), dev),
+        _ptr(B, "B", io, rows, dev),
+        _ptr(C, "C", io, rows, dev),
         _ptr(D, "D", torch.float32, (dim,), dev),
         _ptr(z, "z", io, (batch, dim), dev),
         _ptr(delta_bias, "delta_bias", torch.float32, (dim,), dev),

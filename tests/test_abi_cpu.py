@@ -293,11 +293,12 @@ def test_bc_per_channel_flag_is_validated():
                 None) == L.SSM_ERR_DIMS
     assert scan(*args, FAKE + (5 << 20), None, ctypes.byref(dims(flags=F | L.SSM_FLAG_ZOH)),
                 None) == L.SSM_ERR_DIMS
-    # the decode step has no per-channel rows
+    # the decode step takes per-channel rows too; B then spans [batch, dim, N]
+    # (2 x 16 x 16 bf16 = 1024 bytes), so an output 640 bytes into it overlaps
     st = L.make_dims(2, 1, 16, 16, "bf16", flags=F)
     assert L.lib.ssm_state_update(FAKE + (6 << 20), FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288,
-                                  FAKE + 16384, None, None, None, 0, FAKE + 20480,
-                                  ctypes.byref(st), None) == L.SSM_ERR_DIMS
+                                  FAKE + 16384, None, None, None, 0, FAKE + 12288 + 640,
+                                  ctypes.byref(st), None) == L.SSM_ERR_ALIAS
 
 
 def test_timeout_probe_rejects_bad_arguments_before_launch():
@@ -311,12 +312,14 @@ def test_timeout_probe_rejects_bad_arguments_before_launch():
 
 def test_plans_of_the_measured_workloads():
     """The planner's choices for the benchmark workloads are the ones measured
-    fastest on the B300 (chunk counts swept from 1 to 64): a change to the plan
-    model that moves them must be re-measured, not slip in."""
+    fastest on the B300 (chunk counts swept; 16 chunks for b8 L4096 d2048 is
+    within 1 % of the fastest measured, 8), planned here for 148 SMs (no
+    device): a change to the plan model that moves them must be re-measured,
+    not slip in."""
     p = L.ssm_scan_plan(4, 2048, 1536, 16, "bf16")
     assert (p["chunk_len"], p["nchunks"], p["ctas"], p["kernels"]) == (352, 6, 288, 2)
     p = L.ssm_scan_plan(8, 4096, 2048, 16, "bf16")
-    assert (p["nchunks"], p["ctas"], p["kernels"]) == (1, 128, 1)
+    assert p["nchunks"] == 16 and p["ctas"] == 2048 and p["kernels"] == 2
     p = L.ssm_scan_plan(1, 131072, 5120, 16, "bf16")
     assert p["nchunks"] == 37
     p = L.ssm_scan_plan(4, 2048, 1536, 16, "bf16", flags=L.SSM_FLAG_BC_PER_CHANNEL)

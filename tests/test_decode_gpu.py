@@ -119,3 +119,54 @@ def test_state_guard_bands_and_errors(torch):
                                 G.dev(s["C"]),
                                 out=state.view(torch.bfloat16).view(-1)[:256].view(4, 64))
     assert e.value.code == libssm.SSM_ERR_ALIAS
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+@pytest.mark.parametrize("N", [4, 16])
+@pytest.mark.parametrize("zoh", [False, True])
+def test_per_channel_rows_decode_step(torch, io, N, zoh):
+    """B, C with one row per channel ([batch, dim, N]): each step against the
+    oracle's per-channel step (Oracle.state_update_bcd) over three tokens, with
+    softplus(delta + bias), D and the gate; rows past the last full warp and
+    batch rows past a CTA row are covered by dim 264 and batch 5."""
+    from selective_state_space_119_b300 import libssm
+    spec = I.DecodeSpec(5, 264, N=N, steps=3, io=io, seed=31 + N)
+    inp = I.make_decode_inputs(spec)
+    r = np.random.default_rng(77 + N)
+    B4 = I.store(r.standard_normal((3, 5, 264, N)), io)
+    C4 = I.store(r.standard_normal((3, 5, 264, N)), io)
+    bias = r.uniform(-3.0, -1.0, 264).astype(np.float32)
+    state = G.dev(inp["state0"])
+    ref_state = inp["state0"].astype(np.float64)
+    for t in range(3):
+        y = libssm.ssm_state_update(state, G.dev(inp["x"][t]), G.dev(inp["delta"][t]),
+                                    G.dev(inp["A"]), G.dev(B4[t]), G.dev(C4[t]),
+                                    D=G.dev(inp["D"]), z=G.dev(inp["z"][t]),
+                                    delta_bias=G.dev(bias), delta_softplus=True, zoh=zoh)
+        ry, ref_state = oracle.default().state_update_bcd(
+            ref_state, I.widen(inp["x"][t]), I.widen(inp["delta"][t]),
+            np.asarray(inp["A"], np.float64), I.widen(B4[t]), I.widen(C4[t]),
+            D=np.asarray(inp["D"], np.float64), z=I.widen(inp["z"][t]), delta_bias=bias,
+            delta_softplus=True, zoh=zoh)
+        G.parity(G.host64(y), ry, io, "per-channel step %d y" % t)
+        G.parity(G.host64(state), ref_state, "state", "per-channel step %d state" % t)
+
+
+def test_per_channel_rows_decode_equals_per_channel_scan(torch):
+    """k per-channel steps from zero equal the GPU's per-channel scan over the
+    same k tokens (y per token and the final state)."""
+    from selective_state_space_119_b300 import libssm
+    spec = I.ScanSpec(2, 40, 128, io="bf16", seed=45)
+    inp = I.make_scan_inputs(spec)
+    B4, C4 = I.make_bc_per_channel(spec)
+    t = {k: G.dev(v) for k, v in inp.items()}
+    out, fs = libssm.ssm_selective_scan_fwd(t["x"], t["delta"], t["A"], G.dev(B4), G.dev(C4),
+                                            D=t["D"], z=t["z"], delta_softplus=False)
+    state = torch.zeros((2, 128, 16), dtype=torch.float32, device="cuda")
+    ys = []
+    for k in range(40):
+        ys.append(libssm.ssm_state_update(
+            state, t["x"][:, k].contiguous(), t["delta"][:, k].contiguous(), t["A"],
+            G.dev(B4[:, k]), G.dev(C4[:, k]), D=t["D"], z=t["z"][:, k].contiguous()))
+    G.parity(G.host64(torch.stack(ys, dim=1)), G.host64(out), "bf16", "steps vs per-channel scan")
+    G.parity(G.host64(state), G.host64(fs), "state", "steps vs per-channel scan state")
