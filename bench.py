@@ -578,8 +578,13 @@ def time_floors(spec, alg_bytes, hbm_gbs):
 # full workload is too large to capture). A figure holds only for the kernel
 # source it was taken on: the sha256 covers the scan kernel and the headers it
 # includes; any change there reports null.
-SCAN_TRAFFIC = {}
-SCAN_SOURCES = ("scan16.cu", "scan_fwd.cu", "ssm_device.cuh", "ssm_tma.cuh", "ssm_tmap.h", "ssm_internal.h")
+SCAN_TRAFFIC = {
+    # both passes at L 16384 (the same 37-chunk plan, 1/8 of the tokens):
+    # 339,388,672 + 686,803,200 bytes, scaled by 8 to L 131072
+    "scan_bf16_b1_L131072_d5120": {"bytes_per_call": 8 * (339388672 + 686803200),
+                                   "sha256": "314a8fdff130936bcf5a0e6edbe36697223d4209644377eb20e37eae59544864"},
+}
+SCAN_SOURCES = ("scan16.cu", "ssm_device.cuh", "ssm_tma.cuh", "ssm_tmap.h")
 
 
 def scan_source_sha256():
@@ -755,16 +760,37 @@ def bench_input_stage(args, spec, dev, stream):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / 1e3 / n
 
+    # the stage's backward: dx, dconv_w, dconv_b for dLoss/du = the u of a set
+    cdims = libssm.make_dims(spec.batch, spec.L, spec.dim, 16, io)
+    nbw = int(libssm.lib.ssm_causal_conv1d_silu_bwd_workspace_bytes(ctypes.byref(cdims), K))
+    bws = torch.empty(nbw, dtype=torch.uint8, device=dev)
+    bdims = libssm.make_dims(spec.batch, spec.L, spec.dim, 16, io, bws.data_ptr(), nbw)
+    dxs = torch.empty_like(sets[0]["x"])
+    dwt = torch.empty((spec.dim, K), dtype=torch.float32, device=dev)
+    dbt = torch.empty((spec.dim,), dtype=torch.float32, device=dev)
+
+    def conv_bwd(i):
+        st = sets[i % nsets]
+        rc = libssm.lib.ssm_causal_conv1d_silu_bwd(
+            _vp(st["x"]), _vp(wt), _vp(bt), K, _vp(st["u"]), _vp(dxs), _vp(dwt), _vp(dbt),
+            ctypes.byref(bdims), sptr)
+        if rc != 0:
+            raise libssm.SSMError(rc, "ssm_causal_conv1d_silu_bwd")
+
     n = max(64, min(args.steps, 2000))
     t_conv = timed(conv, n)
     t_fused = timed(fused, n)
     t_two = timed(two_calls, n)
+    t_cbwd = timed(conv_bwd, n)
     status = libssm.ssm_get_device_status(spec.batch, spec.L, spec.dim, spec.N, io, ws)
     if status != 0:
         raise libssm.SSMError(status, "device status")
     peak, kind = measured_peaks()
     gbs = conv_bytes / t_conv / 1e9
     elems = spec.elements
+    # the backward reads x and du and writes dx per element (the taps and the
+    # per-block shares of dw, dbias are small)
+    bwd_bytes = 3 * elems * (2 if spec.io == "bf16" else 4) + 2 * spec.dim * (K + 1) * 4
     return {"conv_width": K, "timed_calls": n, "input_sets": nsets,
             "conv": {"us_per_call": t_conv * 1e6, "value": elems / t_conv, "unit": "elems/s",
                      "roofline": dict({"bound": "hbm", "achieved": gbs, "peak": peak,
@@ -775,7 +801,15 @@ def bench_input_stage(args, spec, dev, stream):
             "fused_scan": {"us_per_call": t_fused * 1e6, "value": elems / t_fused,
                            "unit": "elems/s", "kernels_per_call": plan["kernels"]},
             "conv_then_scan": {"us_per_call": t_two * 1e6, "value": elems / t_two,
-                               "unit": "elems/s", "kernels_per_call": plan["kernels"] + 1}}
+                               "unit": "elems/s", "kernels_per_call": plan["kernels"] + 1},
+            "conv_bwd": {"us_per_call": t_cbwd * 1e6, "value": elems / t_cbwd, "unit": "elems/s",
+                         "kernels_per_call": 2,
+                         "roofline": dict({"bound": "hbm", "achieved": bwd_bytes / t_cbwd / 1e9,
+                                           "peak": peak, "unit": "GB/s",
+                                           "frac": bwd_bytes / t_cbwd / 1e9 / peak,
+                                           "traffic": None, "peak_kind": kind,
+                                           "algorithmic_bytes_per_call": bwd_bytes},
+                                          **nominal(bwd_bytes / t_cbwd / 1e9))}}
 
 
 def bench_train(args, spec, dev, stream):

@@ -29,7 +29,7 @@
  *  - the scan: ssm_selective_scan_fwd (from h = 0), _from_state (from a given
  *    state), _static (library-owned scratch), _conv (the Mamba block's causal
  *    conv1d + SiLU fused in front), and the input stage alone,
- *    ssm_causal_conv1d_silu;
+ *    ssm_causal_conv1d_silu, with its gradients ssm_causal_conv1d_silu_bwd;
  *  - training: ssm_selective_scan_fwd_ckpt (saves states for the backward)
  *    and ssm_selective_scan_bwd (every gradient);
  *  - generation: ssm_state_update (one token on a cached state);
@@ -123,9 +123,12 @@ typedef struct {
  * Discrete: The Key Step": the exact solution for an input held constant over
  * the step, and its flashcard Bbar = (A^-1 (e^{A Delta} - I)) B). Abar is the
  * same exp(dt A) either way. Taken by ssm_selective_scan_fwd,
- * ssm_selective_scan_fwd_from_state, ssm_selective_scan_fwd_static (dstate 16,
- * tile_config_hint 0 or 1) and ssm_state_update (any dstate); the other entry
- * points return SSM_ERR_DIMS when it is set. An unknown bit is SSM_ERR_DIMS.
+ * ssm_selective_scan_fwd_from_state, ssm_selective_scan_fwd_static, the
+ * training pair ssm_selective_scan_fwd_ckpt / ssm_selective_scan_bwd (dstate
+ * 16, tile_config_hint 0 or 1; the backward then differentiates the exact hold:
+ * e^{dt A} in dt and dt^2 phi'(dt A) in A) and ssm_state_update (any dstate);
+ * the other entry points return SSM_ERR_DIMS when it is set. An unknown bit is
+ * SSM_ERR_DIMS.
  */
 #define SSM_FLAG_ZOH 1
 
@@ -280,6 +283,28 @@ int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A, con
                            const float* dfinal_state, void* dx, void* ddelta, float* dA, void* dB,
                            void* dC, float* dD, void* dz, float* ddelta_bias, float* dh0,
                            const ssm_dims* dims, ssm_stream_t stream);
+
+/*
+ * ssm_causal_conv1d_silu_bwd -- the gradients of the input stage
+ * (ssm_causal_conv1d_silu) for a loss whose gradient with respect to its output
+ * u is du; the chain rule on the stage's definition ("State Space Models --
+ * Mamba, S4, and Beyond", "Mamba (S6 -- Selective State Space)", MambaBlock:
+ * Conv1d of width d_conv, left padding d_conv - 1, then SiLU):
+ *   dpre_t = du_t silu'(pre_t),  dx_s = sum_k w[k] dpre_{s+K-1-k},
+ *   dconv_w[d,k] = sum_{b,t} dpre_t x_{t-K+1+k},  dconv_b[d] = sum_{b,t} dpre_t.
+ *   x, du, dx : [batch, seqlen, dim] io dtype
+ *   conv_w    : [dim, conv_k] fp32 (1 <= conv_k <= 4); conv_b [dim] fp32 or NULL
+ *   dconv_w   : [dim, conv_k] fp32; dconv_b [dim] fp32 or NULL (not computed)
+ * dims->workspace must hold ssm_causal_conv1d_silu_bwd_workspace_bytes(dims,
+ * conv_k) bytes (no initial contents needed). The sums over rows and tokens
+ * are added in a fixed order. Chained after ssm_selective_scan_bwd (du = the
+ * scan's dx), it gives the gradients of the input stage followed by the scan.
+ * Two launches on `stream`.
+ */
+size_t ssm_causal_conv1d_silu_bwd_workspace_bytes(const ssm_dims* dims, int conv_k);
+int ssm_causal_conv1d_silu_bwd(const void* x, const float* conv_w, const float* conv_b,
+                               int conv_k, const void* du, void* dx, float* dconv_w,
+                               float* dconv_b, const ssm_dims* dims, ssm_stream_t stream);
 
 /*
  * ssm_state_update -- one token of recurrent generation on a cached state

@@ -279,8 +279,7 @@ int scan_impl(const void* x, const void* delta, const float* A, const void* B, c
     if (cv.w && dims->dstate == 16 && dims->tile_config_hint > 1) return SSM_ERR_DIMS;
     // the exact zero-order hold is built for dstate 16, tile configuration 0,
     // without the fused input stage or checkpoints
-    if ((dims->flags & SSM_FLAG_ZOH) &&
-        (dims->dstate != 16 || dims->tile_config_hint > 1 || cv.w || ckpt))
+    if ((dims->flags & SSM_FLAG_ZOH) && (dims->dstate != 16 || dims->tile_config_hint > 1 || cv.w))
         return SSM_ERR_DIMS;
     // so are per-channel B and C (and not with the exact zero-order hold)
     const bool bc_per_channel = (dims->flags & SSM_FLAG_BC_PER_CHANNEL) != 0;
@@ -447,7 +446,9 @@ int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A, con
                            const ssm_dims* dims, ssm_stream_t stream) {
     int rc = check_dims(dims, true);
     if (rc != SSM_OK) return rc;
-    if (dims->dstate != 16 || dims->tile_config_hint > 1 || dims->flags) return SSM_ERR_DIMS;
+    // dstate 16, the planner's tile; of the variants, the exact zero-order hold
+    if (dims->dstate != 16 || dims->tile_config_hint > 1 || (dims->flags & ~SSM_FLAG_ZOH))
+        return SSM_ERR_DIMS;
     if (dims->batch == 0 || dims->dim == 0) return SSM_OK;
     if ((z == nullptr) != (dz == nullptr) && dims->seqlen > 0) return SSM_ERR_NULL;
     if (!dA) return SSM_ERR_NULL;
@@ -507,6 +508,7 @@ int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A, con
     ssm::BwdArgs a{};
     a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
     a.delta_bias = delta_bias; a.softplus = delta_softplus ? 1 : 0;
+    a.zoh = (dims->flags & SSM_FLAG_ZOH) ? 1 : 0;
     a.ckpt = ckpt; a.nckpt = (L + ssm::kCkptTokens - 1) / ssm::kCkptTokens;
     a.dout = dout; a.dfinal = dfinal_state;
     a.dx = dx; a.ddelta = ddelta; a.dz = dz; a.dh0 = dh0;
@@ -554,6 +556,64 @@ int ssm_causal_conv1d_silu(const void* x, const float* conv_w, const float* conv
     a.batch = d.batch; a.L = d.seqlen; a.dim = d.dim; a.k = conv_k;
     return set_cuda(ssm::launch_conv1d_silu(a, d.io_dtype,
                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t ssm_causal_conv1d_silu_bwd_workspace_bytes(const ssm_dims* dims, int conv_k) {
+    if (!dims || conv_k < 1 || conv_k > ssm::kMaxConvK) return 0;
+    ssm_dims d = *dims;
+    d.dstate = 16; d.chunk_len_hint = 0; d.tile_config_hint = 0; d.flags = 0;
+    if (check_dims(&d, true) != SSM_OK) return 0;
+    if (d.batch == 0 || d.seqlen == 0 || d.dim == 0) return 0;
+    return ssm::kWsHeaderBytes +
+           align256(ssm::conv1d_bwd_partial_floats(d.batch, d.seqlen, d.dim, conv_k) * 4);
+}
+
+int ssm_causal_conv1d_silu_bwd(const void* x, const float* conv_w, const float* conv_b,
+                               int conv_k, const void* du, void* dx, float* dconv_w,
+                               float* dconv_b, const ssm_dims* dims, ssm_stream_t stream) {
+    if (!dims) return SSM_ERR_NULL;
+    if (conv_k < 1 || conv_k > ssm::kMaxConvK) return SSM_ERR_DIMS;
+    ssm_dims d = *dims;
+    d.dstate = 16; d.chunk_len_hint = 0; d.tile_config_hint = 0; d.flags = 0;
+    int rc = check_dims(&d, true);
+    if (rc != SSM_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (d.dim == 0) return SSM_OK;
+    if (d.batch == 0 || d.seqlen == 0) {
+        // no token: the weight and bias gradients are zero
+        if (!dconv_w) return SSM_ERR_NULL;
+        if (!aligned16(dconv_w) || (dconv_b && !aligned16(dconv_b))) return SSM_ERR_ALIGN;
+        rc = set_cuda(cudaMemsetAsync(dconv_w, 0, size_t(d.dim) * conv_k * 4, s));
+        if (rc == SSM_OK && dconv_b) rc = set_cuda(cudaMemsetAsync(dconv_b, 0, size_t(d.dim) * 4, s));
+        return rc;
+    }
+    if (!x || !conv_w || !du || !dx || !dconv_w) return SSM_ERR_NULL;
+    {
+        const void* const ptrs[] = {x, conv_w, conv_b, du, dx, dconv_w, dconv_b, dims->workspace};
+        rc = check_aligned(ptrs);
+        if (rc != SSM_OK) return rc;
+    }
+    const size_t need = ssm_causal_conv1d_silu_bwd_workspace_bytes(&d, conv_k);
+    if (!dims->workspace || dims->workspace_bytes < need) return SSM_ERR_WORKSPACE;
+    const size_t elems = size_t(d.batch) * size_t(d.seqlen) * size_t(d.dim);
+    const size_t es = io_size(d.io_dtype);
+    {
+        const Range in[] = {{x, elems * es},
+                            {conv_w, size_t(d.dim) * size_t(conv_k) * 4},
+                            {conv_b, size_t(d.dim) * 4},
+                            {du, elems * es},
+                            {dims->workspace, need}};
+        const Range outs[] = {{dx, elems * es},
+                              {dconv_w, size_t(d.dim) * size_t(conv_k) * 4},
+                              {dconv_b, size_t(d.dim) * 4}};
+        rc = check_alias(in, outs);
+        if (rc != SSM_OK) return rc;
+    }
+    ssm::ConvBwdArgs a{};
+    a.x = x; a.w = conv_w; a.b = conv_b; a.du = du; a.dx = dx; a.dw = dconv_w; a.db = dconv_b;
+    a.part = reinterpret_cast<float*>(static_cast<char*>(dims->workspace) + ssm::kWsHeaderBytes);
+    a.batch = d.batch; a.L = d.seqlen; a.dim = d.dim; a.k = conv_k;
+    return set_cuda(ssm::launch_conv1d_silu_bwd(a, d.io_dtype, s));
 }
 
 int ssm_state_update(float* state, const void* x, const void* delta, const float* A,

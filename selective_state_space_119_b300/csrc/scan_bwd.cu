@@ -12,7 +12,15 @@
 //   dC[n] += dy h[n],   dB[n] += g[n] dt x,    dA[n] += g[n] dt (a[n] hp[n])
 //   dx = dt sum_n g[n] B[n] + dy D,  ddt = x sum_n g[n] B[n] + sum_n g[n] A[n] (a[n] hp[n])
 //   ddelta = ddt sigmoid(delta + bias) (softplus) or ddt,  dz = dout y silu'(z)
-// where a[n] hp[n] = h[n] - dt x B[n] needs no second state.
+// where a[n] hp[n] = h[n] - dt x B[n] needs no second state. With the exact
+// zero-order hold ("State-space models (Mamba, S4)", "From Continuous to
+// Discrete: The Key Step") the input term is x B[n] m[n], m = (e^{dt A} - 1)/A
+// = dt phi(dt A), whose derivatives are e^{dt A} in dt and dt^2 phi'(dt A) in
+// A (phi'(z) = integral_0^1 s e^{zs} ds), so that
+//   dx = sum_n g[n] B[n] m[n] + dy D,  dB[n] += g[n] x m[n],
+//   ddt = x sum_n g[n] B[n] e^{dt A[n]} + sum_n g[n] A[n] (a[n] hp[n]),
+//   dA[n] += g[n] (dt (a[n] hp[n]) + x B[n] dt^2 phi'(dt A[n])),
+// and a[n] hp[n] = h[n] - x B[n] m[n].
 //
 // The states come from a checkpointing forward (the state before every 8th
 // token, fp32). Per 8-token block, in reverse order, a CTA reloads the block's
@@ -73,6 +81,26 @@ struct BwdSmem {
     static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
     static_assert(N == 16, "the backward is built for dstate 16");
 };
+
+// m = (e^z - 1) / A for z = dt A, e = e^z, with the Taylor series of dt phi(z)
+// below |z| = 0.1 where the difference e^z - 1 of the SFU's 2^s would cancel.
+__device__ __forceinline__ float zoh_m(float dt, float z, float e, float invA) {
+    const float p = fmaf(z, fmaf(z, fmaf(z, fmaf(z, 1.f / 120.f, 1.f / 24.f), 1.f / 6.f), 0.5f), 1.f);
+    return fabsf(z) < 0.1f ? dt * p : (e - 1.f) * invA;
+}
+
+// phi'(z) = integral_0^1 s e^{zs} ds = sum_k z^k / (k! (k + 2)): the series for
+// |z| <= 1 (13 terms, truncation below 2^-30), (e^z (z - 1) + 1) / z^2 above.
+__device__ __forceinline__ float phi_prime(float z, float e) {
+    float p = 1.f / (479001600.f * 14.f);   // k = 12
+    constexpr float c[12] = {1.f / 2.f,            1.f / 3.f,          1.f / 8.f,
+                             1.f / 30.f,           1.f / 144.f,        1.f / 840.f,
+                             1.f / 5760.f,         1.f / 45360.f,      1.f / 403200.f,
+                             1.f / 3991680.f,      1.f / 43545600.f,   1.f / 518918400.f};
+#pragma unroll
+    for (int k = 11; k >= 0; --k) p = fmaf(p, z, c[k]);
+    return fabsf(z) <= 1.f ? p : __fdividef(fmaf(e, z - 1.f, 1.f), z * z);
+}
 
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
@@ -142,7 +170,7 @@ __device__ __forceinline__ void stage_block(const BwdArgs& a, T* in, int64_t b, 
 
 // MODE 0: reverse carry of chunks 1 .. nchunks-1 from zero (Q at the chunk's
 // first token, and its sum of dt). MODE 1: the gradients of one chunk.
-template <typename T, int N, bool SOFTPLUS, bool GATE, int MODE>
+template <typename T, int N, bool SOFTPLUS, bool GATE, int MODE, bool ZOH = false>
 __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs a) {
     constexpr int TB = MODE == 1 ? kGradTokens : kCarryTokens;
     using Sm = BwdSmem<T, N, TB, MODE == 1>;
@@ -200,6 +228,13 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
     }
     const float Dd = (MODE == 1 && a.D && ch_ok) ? __ldg(a.D + dsafe) : 0.f;
     float dD_acc = 0.f, dbias_acc = 0.f, S_acc = 0.f;
+    float invA[NS][SPL];   // 1 / A per state (exact zero-order hold only)
+    if constexpr (ZOH) {
+#pragma unroll
+        for (int r = 0; r < NS; ++r)
+#pragma unroll
+            for (int q = 0; q < SPL; ++q) invA[r][q] = A2[r][q] != 0.f ? kLog2e / A2[r][q] : 0.f;
+    }
 
     auto block_start = [&](int blk) { return t_begin + static_cast<int64_t>(blk) * TB; };
     auto block_count = [&](int blk) {
@@ -264,6 +299,18 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
                 const float* Ct = Bt + N;
 #pragma unroll
                 for (int r = 0; r < NS; ++r) {
+                    if constexpr (ZOH) {
+                        float y1 = 0.f;
+#pragma unroll
+                        for (int q = 0; q < SPL; ++q) {
+                            const float e = ex2(dt[r] * A2[r][q]);
+                            const float m = zoh_m(dt[r], dt[r] * A2[r][q] * kLn2f, e, invA[r][q]);
+                            h[r][q] = fmaf(e, h[r][q], xv[r] * Bt[q] * m);
+                            y1 = fmaf(Ct[q], h[r][q], y1);
+                        }
+                        yp[r] = y1;
+                        continue;
+                    }
                     // packed f32x2 arithmetic over state pairs, as in the forward
                     const float2 dt2 = make_float2(dt[r], dt[r]);
                     const float2 dtx2 = make_float2(dt[r] * xv[r], dt[r] * xv[r]);
@@ -346,11 +393,36 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
                     const float4 v = hist[(tt * (N / 4) + c4) * kBwdThreads + tid];
                     hreg[r][q] = v.x; hreg[r][q + 1] = v.y; hreg[r][q + 2] = v.z; hreg[r][q + 3] = v.w;
                 }
-                float dxs[NS], saw[NS], vals[2 * SPL];
+                float dxs[NS], saw[NS], sbe[NS], vals[2 * SPL];
 #pragma unroll
                 for (int q = 0; q < 2 * SPL; ++q) vals[q] = 0.f;
 #pragma unroll
                 for (int r = 0; r < NS; ++r) {
+                    if constexpr (ZOH) {
+                        float dx1 = 0.f, sa1 = 0.f, sb1 = 0.f;
+#pragma unroll
+                        for (int q = 0; q < SPL; ++q) {
+                            const float z = dt[r] * A2[r][q] * kLn2f;   // dt A
+                            const float e = ex2(dt[r] * A2[r][q]);
+                            const float m = zoh_m(dt[r], z, e, invA[r][q]);
+                            const float xB = xv[r] * Bt[q];
+                            const float wv = fmaf(-xB, m, hreg[r][q]);          // a h_{t-1}
+                            const float g = fmaf(dy[r], Ct[q], Q[r][q]);        // dLoss/dh_t
+                            dx1 = fmaf(g * Bt[q], m, dx1);
+                            sa1 = fmaf(g * wv, A2[r][q], sa1);
+                            sb1 = fmaf(g * Bt[q], e, sb1);
+                            dA[r][q] = fmaf(g, fmaf(wv, dt[r], xB * dt[r] * dt[r] * phi_prime(z, e)),
+                                            dA[r][q]);
+                            vals[q] = fmaf(g, xv[r] * m, vals[q]);                // dB
+                            vals[SPL + q] = fmaf(dy[r], hreg[r][q], vals[SPL + q]);  // dC
+                            Q[r][q] = e * g;
+                        }
+                        dxs[r] = dx1;
+                        saw[r] = sa1;
+                        sbe[r] = sb1;
+                        continue;
+                    }
+                    sbe[r] = 0.f;
                     // packed f32x2 arithmetic over state pairs
                     const float dtx = dt[r] * xv[r];
                     const float2 dt2 = make_float2(dt[r], dt[r]), dy2 = make_float2(dy[r], dy[r]);
@@ -386,11 +458,15 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
                 }
                 const float dxs_own = dxs[0] + __shfl_xor_sync(0xffffffffu, dxs[1], 1);
                 const float saw_own = saw[0] + __shfl_xor_sync(0xffffffffu, saw[1], 1);
+                const float sbe_own = ZOH ? sbe[0] + __shfl_xor_sync(0xffffffffu, sbe[1], 1) : 0.f;
                 if (tt < cnt && ch_ok) {
                     const int64_t e = (b * a.L + u0 + tt) * a.dim + d;
                     const float dout_own = (j ? gp.y : gp.x);
-                    st_io(static_cast<T*>(a.dx) + e, fmaf(dt[0], dxs_own, dy[0] * Dd));
-                    const float ddt = fmaf(xv[0], dxs_own, kLn2f * saw_own);
+                    // first order: dx = dt sum g B, ddt = x sum g B + sum g A (a hp);
+                    // zero-order hold: dx = sum g B m, ddt = x sum g B e^{dt A} + sum g A (a hp)
+                    st_io(static_cast<T*>(a.dx) + e,
+                          ZOH ? fmaf(dy[0], Dd, dxs_own) : fmaf(dt[0], dxs_own, dy[0] * Dd));
+                    const float ddt = fmaf(xv[0], ZOH ? sbe_own : dxs_own, kLn2f * saw_own);
                     float dd = ddt;
                     if constexpr (SOFTPLUS) {
                         const float2 dp = lds_pair(in + Sm::kDelta + tt * kBwdChannels + pc);
@@ -498,7 +574,7 @@ __global__ void __launch_bounds__(256) scan_bwd_reduce_kernel(const BwdArgs a) {
     }
 }
 
-template <typename T, int N, bool SOFTPLUS, bool GATE, int MODE>
+template <typename T, int N, bool SOFTPLUS, bool GATE, int MODE, bool ZOH>
 cudaError_t launch_mode(const BwdArgs& a, int64_t ctas, cudaStream_t s) {
     using Sm = BwdSmem<T, N, MODE == 1 ? kGradTokens : kCarryTokens, MODE == 1>;
     static std::mutex mu;
@@ -510,13 +586,13 @@ cudaError_t launch_mode(const BwdArgs& a, int64_t ctas, cudaStream_t s) {
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!done[dev]) {
-            e = cudaFuncSetAttribute(scan_bwd_kernel<T, N, SOFTPLUS, GATE, MODE>,
+            e = cudaFuncSetAttribute(scan_bwd_kernel<T, N, SOFTPLUS, GATE, MODE, ZOH>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::kBytes);
             if (e != cudaSuccess) return e;
             done[dev] = true;
         }
     }
-    scan_bwd_kernel<T, N, SOFTPLUS, GATE, MODE>
+    scan_bwd_kernel<T, N, SOFTPLUS, GATE, MODE, ZOH>
         <<<static_cast<unsigned>(ctas), kBwdThreads, Sm::kBytes, s>>>(a);
     return cudaGetLastError();
 }
@@ -525,11 +601,15 @@ template <typename T, int N, bool SOFTPLUS, bool GATE>
 cudaError_t launch_flags(const BwdArgs& a, cudaStream_t s) {
     const int64_t per_chunk = a.tiles * a.batch;
     cudaError_t e;
+    // the reverse carries involve only the decay e^{dt A}: one carry pass
+    // serves both input terms
     if (a.nchunks > 1 &&
-        (e = launch_mode<T, N, SOFTPLUS, GATE, 0>(a, per_chunk * (a.nchunks - 1), s)) != cudaSuccess)
+        (e = launch_mode<T, N, SOFTPLUS, GATE, 0, false>(a, per_chunk * (a.nchunks - 1), s)) !=
+            cudaSuccess)
         return e;
-    if ((e = launch_mode<T, N, SOFTPLUS, GATE, 1>(a, per_chunk * a.nchunks, s)) != cudaSuccess)
-        return e;
+    e = a.zoh ? launch_mode<T, N, SOFTPLUS, GATE, 1, true>(a, per_chunk * a.nchunks, s)
+              : launch_mode<T, N, SOFTPLUS, GATE, 1, false>(a, per_chunk * a.nchunks, s);
+    if (e != cudaSuccess) return e;
     const int64_t total = a.batch * a.L * 2 * N + a.dim * N + 2 * a.dim;
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, 148 * 16);
     scan_bwd_reduce_kernel<T, N><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);

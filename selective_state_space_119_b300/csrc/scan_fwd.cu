@@ -637,9 +637,13 @@ cudaError_t launch_typed(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     if (a.conv_w) return p.tile_cfg == 0 && !a.ckpt && !a.zoh
                              ? launch_cfg<T, N, Tile0, true>(a, p, s)
                              : cudaErrorInvalidValue;
-    // so is the checkpointing forward (training)
-    if (a.ckpt) return p.tile_cfg == 0 && !a.zoh ? launch_cfg<T, N, Tile0, false, true>(a, p, s)
-                                                 : cudaErrorInvalidValue;
+    // so is the checkpointing forward (training), first order or exact hold
+    if (a.ckpt) {
+        if (p.tile_cfg != 0) return cudaErrorInvalidValue;
+        if constexpr (N == 16)
+            if (a.zoh) return launch_cfg<T, N, Tile0, false, true, true>(a, p, s);
+        return a.zoh ? cudaErrorInvalidValue : launch_cfg<T, N, Tile0, false, true>(a, p, s);
+    }
     // and the exact zero-order hold (dstate 16)
     if (a.zoh) {
         if constexpr (N == 16)

@@ -233,20 +233,29 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         load_X(0);
     }
 
+    // this thread's token of chunk c: raw dt (bf16), 0 past the sequence end
+    auto load_dt = [&](int c) {
+        const int64_t t = int64_t(c) * kQ + tid;
+        return t < a.L ? IO<__nv_bfloat16>::ld(static_cast<const __nv_bfloat16*>(a.dt) +
+                                                (b * a.L + t) * a.H + hd)
+                       : 0.f;
+    };
+    float dt_next = load_dt(0);
+
     uint32_t mma_phase = 0;
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
         const int t0 = c * kQ;
         const uint32_t ld_phase = static_cast<uint32_t>(c & 1);   // each tile loads once per chunk
-        // dt of the chunk (0 past the sequence end), then s = A * cumsum(dt)
+        // dt of the chunk (0 past the sequence end; loaded a chunk ahead, so
+        // the load is off the chunk's critical path), then s = A * cumsum(dt)
         {
-            const int64_t t = t0 + tid;
             float v = 0.f;
-            if (t < a.L) {
-                v = IO<__nv_bfloat16>::ld(static_cast<const __nv_bfloat16*>(a.dt) +
-                                          (b * a.L + t) * a.H + hd) + bias;
+            if (t0 + tid < a.L) {
+                v = dt_next + bias;
                 if (a.softplus) v = softplus(v);
             }
+            dt_next = load_dt(c + 1);
             sdt[tid] = v;
             float cs = v;
 #pragma unroll

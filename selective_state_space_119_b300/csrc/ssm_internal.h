@@ -104,6 +104,23 @@ struct ConvArgs {
     int k;
 };
 
+// Gradients of the input stage for dLoss/du = du.
+struct ConvBwdArgs {
+    const void* x;          // [batch][L][dim]
+    const float* w;         // [dim][k]
+    const float* b;         // [dim] or NULL
+    const void* du;         // [batch][L][dim]
+    void* dx;               // [batch][L][dim]
+    float* dw;              // [dim][k]
+    float* db;              // [dim] or NULL
+    float* part;            // workspace: the per-block shares of dw | dbias
+    int64_t batch, L, dim;
+    int k;
+};
+// fp32 values of the per-block shares (the workspace after its header).
+size_t conv1d_bwd_partial_floats(int64_t batch, int64_t L, int64_t dim, int k);
+cudaError_t launch_conv1d_silu_bwd(const ConvBwdArgs& a, int io, cudaStream_t s);
+
 // The gradient pass of the scan (dstate 16). Chunking follows the forward's
 // plan with 128-channel tiles.
 struct BwdArgs {
@@ -131,6 +148,7 @@ struct BwdArgs {
     float* dbias;         // [dim] or NULL
     int64_t batch, L, dim;
     int64_t chunk_len, nchunks, tiles;
+    int zoh;              // exact zero-order-hold input term
     // workspace
     float* wsQ;    // [batch][nchunks-1][dim][N]: reverse carry of chunks 1.. from zero
     float* wsS;    // [batch][nchunks-1][dim]: sum of dt over those chunks

@@ -50,7 +50,8 @@ EXPORTED = ("ssm_selective_scan_fwd", "ssm_state_update", "ssm_scan_workspace_by
             "ssm_selective_scan_fwd_ckpt", "ssm_scan_bwd_workspace_bytes",
             "ssm_selective_scan_bwd", "ssm_debug_timeout_probe", "ssm_get_static_status",
             "ssm_debug_timeout_probe_static", "ssm_ssd_fwd", "ssm_ssd_workspace_bytes",
-            "ssm_ssd_get_device_status")
+            "ssm_ssd_get_device_status", "ssm_causal_conv1d_silu_bwd",
+            "ssm_causal_conv1d_silu_bwd_workspace_bytes")
 
 # Size of the library-owned scratch of ssm_selective_scan_fwd_static (include/ssm.h).
 SSM_STATIC_SCRATCH_BYTES = 16 << 20
@@ -97,6 +98,11 @@ lib.ssm_selective_scan_fwd_conv.argtypes = [_vp, _vp, _vp, ctypes.c_int, _vp, _v
                                             _vp, _vp, ctypes.c_int, _vp, _vp, _dims_p, _vp]
 lib.ssm_causal_conv1d_silu.restype = ctypes.c_int
 lib.ssm_causal_conv1d_silu.argtypes = [_vp, _vp, _vp, ctypes.c_int, _vp, _dims_p, _vp]
+lib.ssm_causal_conv1d_silu_bwd.restype = ctypes.c_int
+lib.ssm_causal_conv1d_silu_bwd.argtypes = [_vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                           _dims_p, _vp]
+lib.ssm_causal_conv1d_silu_bwd_workspace_bytes.restype = ctypes.c_size_t
+lib.ssm_causal_conv1d_silu_bwd_workspace_bytes.argtypes = [_dims_p, ctypes.c_int]
 lib.ssm_scan_checkpoint_bytes.restype = ctypes.c_size_t
 lib.ssm_scan_checkpoint_bytes.argtypes = [_dims_p]
 lib.ssm_selective_scan_fwd_ckpt.restype = ctypes.c_int
@@ -350,6 +356,35 @@ def ssm_causal_conv1d_silu(x, conv_w, conv_b=None, out=None, stream=None):
     return out
 
 
+def ssm_causal_conv1d_silu_bwd(x, conv_w, du, conv_b=None, want_dbias=True, stream=None):
+    """Gradients of the input stage for dLoss/du = du (include/ssm.h): returns
+    (dx [batch, L, dim] like x, dconv_w [dim, K] fp32, dconv_b [dim] fp32 or
+    None)."""
+    torch = _torch()
+    batch, L, dim = x.shape
+    dev = _device_of(x, "x")
+    if conv_w.dim() != 2 or conv_w.shape[0] != dim:
+        raise ValueError("conv_w must have shape (dim, K), got %s" % (tuple(conv_w.shape),))
+    K = int(conv_w.shape[1])
+    dims = make_dims(batch, L, dim, 16, _io_code(x))
+    n = int(lib.ssm_causal_conv1d_silu_bwd_workspace_bytes(ctypes.byref(dims), K))
+    with _launch_on(dev, stream) as sp:
+        dx = torch.empty_like(x)
+        dw = torch.empty((dim, K), dtype=torch.float32, device=dev)
+        db = torch.empty((dim,), dtype=torch.float32, device=dev) if want_dbias else None
+        ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+        dims = make_dims(batch, L, dim, 16, _io_code(x), ws.data_ptr(), n)
+        rc = lib.ssm_causal_conv1d_silu_bwd(
+            _ptr(x, "x", x.dtype, (batch, L, dim), dev),
+            _ptr(conv_w, "conv_w", torch.float32, (dim, K), dev),
+            _ptr(conv_b, "conv_b", torch.float32, (dim,), dev), K,
+            _ptr(du, "du", x.dtype, (batch, L, dim), dev), _ptr(dx, "dx", x.dtype, None, dev),
+            _ptr(dw, "dconv_w", torch.float32, None, dev),
+            _ptr(db, "dconv_b", torch.float32, None, dev), ctypes.byref(dims), sp)
+    _check(rc, "ssm_causal_conv1d_silu_bwd")
+    return dx, dw, db
+
+
 def ssm_selective_scan_fwd_static(x, delta, A, B, C, D=None, z=None, delta_bias=None,
                                   delta_softplus=False, out=None, final_state=None,
                                   return_final_state=True, chunk_len_hint=0,
@@ -460,10 +495,11 @@ def ssm_scan_bwd_workspace_bytes(batch, seqlen, dim, dstate, io, chunk_len_hint=
 
 def ssm_selective_scan_fwd_ckpt(x, delta, A, B, C, D=None, z=None, delta_bias=None,
                                 delta_softplus=False, h0=None, out=None, final_state=None,
-                                ckpt=None, workspace=None, chunk_len_hint=0, stream=None):
+                                ckpt=None, workspace=None, chunk_len_hint=0, stream=None,
+                                zoh=False):
     """The scan that also saves the state before every 8th token for the
     backward. Returns (out, final_state, ckpt); ckpt is [batch, ceil(L/8), dim,
-    16] fp32."""
+    16] fp32. ``zoh=True`` scans with the exact zero-order-hold Bbar."""
     torch = _torch()
     batch, L, dim = x.shape
     N = A.shape[1]
@@ -480,7 +516,8 @@ def ssm_selective_scan_fwd_ckpt(x, delta, A, B, C, D=None, z=None, delta_bias=No
             workspace = alloc_workspace(batch, L, dim, N, _io_code(x), dev, chunk_len_hint)
         ws_ptr = _ptr(workspace, "workspace", torch.uint8, device=dev)
         ws_bytes = workspace.numel() if workspace is not None else 0
-        dims = make_dims(batch, L, dim, N, _io_code(x), ws_ptr, ws_bytes, chunk_len_hint)
+        dims = make_dims(batch, L, dim, N, _io_code(x), ws_ptr, ws_bytes, chunk_len_hint,
+                         flags=SSM_FLAG_ZOH if zoh else 0)
         rc = lib.ssm_selective_scan_fwd_ckpt(
             _ptr(x, "x", io, (batch, L, dim), dev), _ptr(delta, "delta", io, (batch, L, dim), dev),
             _ptr(A, "A", torch.float32, (dim, N), dev), _ptr(B, "B", io, (batch, L, N), dev),
@@ -499,9 +536,11 @@ def ssm_selective_scan_fwd_ckpt(x, delta, A, B, C, D=None, z=None, delta_bias=No
 def ssm_selective_scan_bwd(x, delta, A, B, C, ckpt, dout, D=None, z=None, delta_bias=None,
                            delta_softplus=False, dfinal_state=None, want_dD=True,
                            want_ddelta_bias=True, want_dh0=False, workspace=None,
-                           chunk_len_hint=0, stream=None) -> dict:
+                           chunk_len_hint=0, stream=None, zoh=False) -> dict:
     """Gradients of the scan (include/ssm.h). Returns a dict with dx, ddelta,
-    dA, dB, dC and, when asked for / defined, dD, dz, ddelta_bias, dh0."""
+    dA, dB, dC and, when asked for / defined, dD, dz, ddelta_bias, dh0.
+    ``zoh=True`` differentiates the exact zero-order-hold scan (the checkpoints
+    must come from a ``zoh=True`` checkpointing forward)."""
     torch = _torch()
     batch, L, dim = x.shape
     N = A.shape[1]
@@ -510,13 +549,13 @@ def ssm_selective_scan_bwd(x, delta, A, B, C, ckpt, dout, D=None, z=None, delta_
     with _launch_on(dev, stream) as sp:
         rc, g = _bwd_call(x, delta, A, B, C, ckpt, dout, D, z, delta_bias, delta_softplus,
                           dfinal_state, want_dD, want_ddelta_bias, want_dh0, workspace,
-                          chunk_len_hint, sp)
+                          chunk_len_hint, sp, zoh)
     _check(rc, "ssm_selective_scan_bwd")
     return g
 
 
 def _bwd_call(x, delta, A, B, C, ckpt, dout, D, z, delta_bias, delta_softplus, dfinal_state,
-              want_dD, want_ddelta_bias, want_dh0, workspace, chunk_len_hint, sp):
+              want_dD, want_ddelta_bias, want_dh0, workspace, chunk_len_hint, sp, zoh=False):
     torch = _torch()
     batch, L, dim = x.shape
     N = A.shape[1]
@@ -537,7 +576,7 @@ def _bwd_call(x, delta, A, B, C, ckpt, dout, D, z, delta_bias, delta_softplus, d
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
     dims = make_dims(batch, L, dim, N, _io_code(x), _ptr(workspace, "workspace", torch.uint8,
                                                          device=dev),
-                     workspace.numel(), chunk_len_hint)
+                     workspace.numel(), chunk_len_hint, flags=SSM_FLAG_ZOH if zoh else 0)
     rc = lib.ssm_selective_scan_bwd(
         _ptr(x, "x", io, (batch, L, dim), dev), _ptr(delta, "delta", io, (batch, L, dim), dev),
         _ptr(A, "A", torch.float32, (dim, N), dev), _ptr(B, "B", io, (batch, L, N), dev),

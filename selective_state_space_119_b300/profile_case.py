@@ -1,0 +1,90 @@
+"""Run one kernel case a few times, for profilers (ncu) and quick timings.
+
+    python -m selective_state_space_119_b300.profile_case scan --batch 1 --seqlen 16384 \\
+        --dim 5120 [--A s4d|lognormal] [--softplus] [--chunk-len 0] [--calls 3]
+    python -m selective_state_space_119_b300.profile_case ssd --batch 16 --seqlen 1024 \\
+        [--heads 8] [--groups 1] [--calls 3]
+
+The inputs are the seeded workload distributions of ``inputs`` (the scan's
+long-sequence recipe by default: delta log-uniform in [1e-4, 1e-2], gate, D = 1,
+final state). Every call goes through the C ABI; the script prints the plan and
+the CUDA-event time of the last call and exits non-zero on any library error.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import sys
+
+import numpy as np
+
+
+def _dev(torch, a):
+    if a is None:
+        return None
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run_scan(args, torch):
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+    if args.softplus:
+        spec = I.ScanSpec(args.batch, args.seqlen, args.dim, io="bf16",
+                          delta_kind="softplus_bias", A_kind=args.A, D_kind="uniform", seed=3)
+    else:
+        spec = I.ScanSpec(args.batch, args.seqlen, args.dim, io="bf16", delta_lo=1e-4,
+                          delta_hi=1e-2, A_kind=args.A, seed=3)
+    t = {k: _dev(torch, v) for k, v in I.make_scan_inputs(spec).items()}
+    plan = libssm.ssm_scan_plan(spec.batch, spec.L, spec.dim, 16, "bf16",
+                                chunk_len_hint=args.chunk_len)
+    print("plan", plan, flush=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.calls):
+        e0.record()
+        libssm.ssm_selective_scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], D=t["D"],
+                                      z=t["z"], delta_bias=t["delta_bias"],
+                                      delta_softplus=spec.delta_softplus,
+                                      chunk_len_hint=args.chunk_len)
+        e1.record()
+    torch.cuda.synchronize()
+    print("last call %.3f ms" % e0.elapsed_time(e1), flush=True)
+
+
+def run_ssd(args, torch):
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+    spec = I.SsdSpec(args.batch, args.seqlen, H=args.heads, G=args.groups, seed=5)
+    t = {k: _dev(torch, v) for k, v in I.make_ssd_inputs(spec).items()}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.calls):
+        e0.record()
+        libssm.ssm_ssd_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], D=t["D"],
+                           dt_bias=t["dt_bias"], dt_softplus=True)
+        e1.record()
+    torch.cuda.synchronize()
+    print("last call %.3f ms" % e0.elapsed_time(e1), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("kernel", choices=["scan", "ssd"])
+    ap.add_argument("--batch", type=int, required=True)
+    ap.add_argument("--seqlen", type=int, required=True)
+    ap.add_argument("--dim", type=int, default=5120)
+    ap.add_argument("--A", default="s4d", choices=["s4d", "lognormal"])
+    ap.add_argument("--softplus", action="store_true")
+    ap.add_argument("--chunk-len", type=int, default=0)
+    ap.add_argument("--heads", type=int, default=8)
+    ap.add_argument("--groups", type=int, default=1)
+    ap.add_argument("--calls", type=int, default=3)
+    args = ap.parse_args(argv)
+    import torch
+    if not torch.cuda.is_available():
+        sys.exit("no CUDA device")
+    (run_scan if args.kernel == "scan" else run_ssd)(args, torch)
+
+
+if __name__ == "__main__":
+    main()

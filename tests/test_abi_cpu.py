@@ -244,7 +244,7 @@ def test_flags_are_validated():
     args = (FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288, FAKE + 16384, None, None, None, 0,
             FAKE + (1 << 30), None)
     assert scan(*args, ctypes.byref(d), None) == L.SSM_ERR_DIMS
-    # the exact zero-order hold: dstate 16, tile configuration 0, no checkpoints / conv / backward
+    # the exact zero-order hold: dstate 16, tile configuration 0, no fused conv
     z8 = L.make_dims(1, 20, 16, 8, "bf16", workspace=FAKE + (1 << 34), workspace_bytes=1 << 24,
                      flags=L.SSM_FLAG_ZOH)
     assert scan(*args, ctypes.byref(z8), None) == L.SSM_ERR_DIMS
@@ -256,16 +256,20 @@ def test_flags_are_validated():
     # accepted up to the alias check (out over x), so no launch happens here
     bad = args[:9] + (FAKE, None)
     assert scan(*bad, ctypes.byref(z16), None) == L.SSM_ERR_ALIAS
+    # the checkpointing forward takes the hold too: accepted up to the alias
+    # check (its checkpoints over x), so no launch happens here
     assert L.lib.ssm_selective_scan_fwd_ckpt(*args[:9], None, FAKE + (1 << 30), None,
-                                             FAKE + (1 << 32), ctypes.byref(z16),
-                                             None) == L.SSM_ERR_DIMS
+                                             FAKE, ctypes.byref(z16),
+                                             None) == L.SSM_ERR_ALIAS
     assert L.lib.ssm_selective_scan_fwd_conv(FAKE, FAKE + (1 << 32), None, 4, *args[1:],
                                              ctypes.byref(z16), None) == L.SSM_ERR_DIMS
+    # the backward takes the hold too: accepted up to the alias check (dx over
+    # x), so no launch happens here
     G = FAKE + (1 << 36)
     assert L.lib.ssm_selective_scan_bwd(
         FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288, FAKE + 16384, None, None, None, 0,
-        FAKE + (1 << 32), FAKE + 20480, None, G, G + 4096, G + 65536, G + 8192, G + 12288,
-        None, None, None, None, ctypes.byref(z16), None) == L.SSM_ERR_DIMS
+        FAKE + (1 << 32), FAKE + 20480, None, FAKE, G + 4096, G + 65536, G + 8192, G + 12288,
+        None, None, None, None, ctypes.byref(z16), None) == L.SSM_ERR_ALIAS
 
 
 def test_bc_per_channel_flag_is_validated():

@@ -93,21 +93,21 @@ def _case(spec, seed, with_h0=False, with_dfinal=False):
     return inp, dout, h0, dfin
 
 
-def _gpu_train(inp, softplus, dout, h0=None, dfinal=None, hint=0, want_dh0=False):
+def _gpu_train(inp, softplus, dout, h0=None, dfinal=None, hint=0, want_dh0=False, zoh=False):
     from selective_state_space_119_b300 import libssm
     t = {k: G.dev(v) for k, v in inp.items()}
     out, fs, ck = libssm.ssm_selective_scan_fwd_ckpt(
         t["x"], t["delta"], t["A"], t["B"], t["C"], D=t.get("D"), z=t.get("z"),
         delta_bias=t.get("delta_bias"), delta_softplus=softplus, h0=G.dev(h0),
-        chunk_len_hint=hint)
+        chunk_len_hint=hint, zoh=zoh)
     g = libssm.ssm_selective_scan_bwd(
         t["x"], t["delta"], t["A"], t["B"], t["C"], ck, G.dev(dout), D=t.get("D"), z=t.get("z"),
         delta_bias=t.get("delta_bias"), delta_softplus=softplus, dfinal_state=G.dev(dfinal),
-        want_dh0=want_dh0, chunk_len_hint=hint)
+        want_dh0=want_dh0, chunk_len_hint=hint, zoh=zoh)
     return out, fs, ck, g
 
 
-def _oracle_bwd(inp, softplus, dout, h0=None, dfinal=None):
+def _oracle_bwd(inp, softplus, dout, h0=None, dfinal=None, zoh=False):
     return oracle.selective_scan_bwd(
         I.widen(inp["x"]), I.widen(inp["delta"]), np.asarray(inp["A"], np.float64),
         I.widen(inp["B"]), I.widen(inp["C"]), I.widen(dout),
@@ -115,7 +115,7 @@ def _oracle_bwd(inp, softplus, dout, h0=None, dfinal=None):
         z=I.widen(inp.get("z")),
         delta_bias=None if inp.get("delta_bias") is None else np.asarray(inp["delta_bias"], np.float64),
         delta_softplus=softplus, h0=None if h0 is None else h0.astype(np.float64),
-        dh_final=None if dfinal is None else dfinal.astype(np.float64))
+        dh_final=None if dfinal is None else dfinal.astype(np.float64), zoh=zoh)
 
 
 def _check_grads(g, ref, io, what, z_given=True, dh0=False):
@@ -277,3 +277,29 @@ def test_gradients_guard_bands_and_bitwise_repeat(torch):
     g = {"dx": g1["dx"], "ddelta": g1["ddelta"], "dz": g1["dz"], "dB": g1["dB"], "dC": g1["dC"],
          "dA": g1["dA"], "dD": g1["dD"], "ddelta_bias": g1["dbias"], "dh0": g1["dh0"]}
     _check_grads(g, ref, "bf16", "(guarded buffers)", dh0=True)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("hint", [0, 64])
+@pytest.mark.parametrize("softplus", [True, False])
+def test_zero_order_hold_gradients(torch, io, hint, softplus):
+    """Training through the scan with the exact zero-order hold: the
+    checkpointing forward equals the oracle's ZOH scan, and every gradient the
+    oracle's ZOH backward (the hold term's e^{dt A} in dt and dt^2 phi'(dt A) in
+    A), from h0 and with dLoss/dfinal_state, on both sides of the series /
+    closed-form switches of m and phi' (delta up to 0.3 with |A| up to ~5)."""
+    spec = I.ScanSpec(2, 300, 136, io=io, delta_kind="softplus_bias" if softplus else "loguniform",
+                      delta_lo=1e-3, delta_hi=0.3, A_kind="lognormal", D_kind="uniform", seed=67)
+    inp, dout, h0, dfin = _case(spec, 68, with_h0=True, with_dfinal=True)
+    out, fs, _, g = _gpu_train(inp, softplus, dout, h0=h0, dfinal=dfin, hint=hint,
+                               want_dh0=True, zoh=True)
+    ry, rh = oracle.selective_scan(
+        I.widen(inp["x"]), I.widen(inp["delta"]), np.asarray(inp["A"], np.float64),
+        I.widen(inp["B"]), I.widen(inp["C"]), D=np.asarray(inp["D"], np.float64),
+        z=I.widen(inp["z"]),
+        delta_bias=None if inp["delta_bias"] is None else np.asarray(inp["delta_bias"], np.float64),
+        delta_softplus=softplus, h0=h0.astype(np.float64), zoh=True)
+    G.parity(G.host64(out), ry, io, "ZOH checkpointing forward y")
+    G.parity(G.host64(fs), rh, "state", "ZOH checkpointing forward final state")
+    ref = _oracle_bwd(inp, softplus, dout, h0=h0, dfinal=dfin, zoh=True)
+    _check_grads(g, ref, io, "(ZOH, %s, hint %d, softplus %s)" % (io, hint, softplus), dh0=True)
