@@ -973,11 +973,98 @@ def bench_bcd(args, spec, dev, stream):
     peak, kind = measured_peaks()
     gbs = alg / sec / 1e9
     plan = libssm.ssm_scan_plan(B_, L_, D_, N_, io, flags=F)
-    return {"us_per_call": sec * 1e6, "value": spec.elements / sec, "unit": "elems/s",
-            "timed_calls": n, "input_sets": nsets, "kernels_per_call": plan["kernels"],
-            "roofline": dict({"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                              "frac": gbs / peak, "traffic": None, "peak_kind": kind,
-                              "algorithmic_bytes_per_call": alg}, **nominal(gbs))}
+    res = {"us_per_call": sec * 1e6, "value": spec.elements / sec, "unit": "elems/s",
+           "timed_calls": n, "input_sets": nsets, "kernels_per_call": plan["kernels"],
+           "roofline": dict({"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                             "frac": gbs / peak, "traffic": None, "peak_kind": kind,
+                             "algorithmic_bytes_per_call": alg}, **nominal(gbs))}
+    res["train"] = _bench_bcd_train(args, spec, sets, nsets, dev, stream, n)
+    return res
+
+
+def _bench_bcd_train(args, spec, sets, nsets, dev, stream, n):
+    """Training with per-channel B, C: the checkpointing forward and the
+    backward (dout ~ N(0, 1)), each timed alone over the rotating input sets;
+    the backward against HBM (it moves the B, C rows in and the dB, dC rows out)."""
+    import numpy as np
+    import torch
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+    B_, L_, D_, N_ = spec.batch, spec.L, spec.dim, spec.N
+    io = libssm.SSM_BF16 if spec.io == "bf16" else libssm.SSM_F32
+    F = libssm.SSM_FLAG_BC_PER_CHANNEL
+    rng = np.random.default_rng(spec.seed + 900)
+    for st in sets:
+        st["dout"] = _upload(I.store(rng.standard_normal((B_, L_, D_)), spec.io), dev)
+        st["ck"] = torch.empty((B_, (L_ + 7) // 8, D_, N_), dtype=torch.float32, device=dev)
+    ws = libssm.alloc_workspace(B_, L_, D_, N_, io, dev, flags=F)
+    dims = libssm.make_dims(B_, L_, D_, N_, io, None if ws is None else ws.data_ptr(),
+                            0 if ws is None else ws.numel(), flags=F)
+    nb = libssm.ssm_scan_bwd_workspace_bytes(B_, L_, D_, N_, io, flags=F)
+    wsb = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+    dims_b = libssm.make_dims(B_, L_, D_, N_, io, wsb.data_ptr(), nb, flags=F)
+    x0 = sets[0]["x"]
+    g = {"dx": torch.empty_like(x0), "ddelta": torch.empty_like(x0),
+         "dz": torch.empty_like(x0) if spec.gate else None,
+         "dB": torch.empty_like(sets[0]["B"]), "dC": torch.empty_like(sets[0]["C"]),
+         "dA": torch.empty((D_, N_), dtype=torch.float32, device=dev),
+         "dD": torch.empty(D_, dtype=torch.float32, device=dev),
+         "dbias": torch.empty(D_, dtype=torch.float32, device=dev)}
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    sp = 1 if spec.delta_softplus else 0
+
+    def fwd(i):
+        st = sets[i % nsets]
+        rc = libssm.lib.ssm_selective_scan_fwd_ckpt(
+            _vp(st["x"]), _vp(st["delta"]), _vp(st["A"]), _vp(st["B"]), _vp(st["C"]),
+            _vp(st["D"]), _vp(st["z"]), _vp(st["delta_bias"]), sp, None, _vp(st["out"]), None,
+            _vp(st["ck"]), ctypes.byref(dims), sptr)
+        if rc != 0:
+            raise libssm.SSMError(rc, "ssm_selective_scan_fwd_ckpt (per-channel B, C)")
+
+    def bwd(i):
+        st = sets[i % nsets]
+        rc = libssm.lib.ssm_selective_scan_bwd(
+            _vp(st["x"]), _vp(st["delta"]), _vp(st["A"]), _vp(st["B"]), _vp(st["C"]),
+            _vp(st["D"]), _vp(st["z"]), _vp(st["delta_bias"]), sp, _vp(st["ck"]),
+            _vp(st["dout"]), None, _vp(g["dx"]), _vp(g["ddelta"]), _vp(g["dA"]), _vp(g["dB"]),
+            _vp(g["dC"]), _vp(g["dD"]), _vp(g["dz"]), _vp(g["dbias"]), None,
+            ctypes.byref(dims_b), sptr)
+        if rc != 0:
+            raise libssm.SSMError(rc, "ssm_selective_scan_bwd (per-channel B, C)")
+
+    def timed(fn):
+        for i in range(max(args.warmup, 3)):
+            fn(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    for i in range(nsets):     # every set's checkpoints, before the backward reads them
+        fwd(i)
+    t_fwd = timed(fwd)
+    t_bwd = timed(bwd)
+    peak, kind = measured_peaks()
+    alg = I.algorithmic_bytes_scan_bcd_bwd(spec)
+    gbs = alg / t_bwd / 1e9
+    plan = libssm.ssm_scan_plan(B_, L_, D_, N_, io, flags=F)
+    return {"timed_calls": n, "dout": "N(0,1)",
+            "fwd_ckpt": {"us_per_call": t_fwd * 1e6, "value": spec.elements / t_fwd,
+                         "unit": "elems/s", "kernels_per_call": plan["kernels"]},
+            "bwd": {"us_per_call": t_bwd * 1e6, "value": spec.elements / t_bwd, "unit": "elems/s",
+                    "kernels_per_call": 3 if plan["nchunks"] > 1 else 2,
+                    "workspace_bytes": nb,
+                    "roofline": dict({"bound": "hbm", "achieved": gbs, "peak": peak,
+                                      "unit": "GB/s", "frac": gbs / peak, "traffic": None,
+                                      "peak_kind": kind, "algorithmic_bytes_per_call": alg,
+                                      "kernel": "bcd_grad_kernel (+ reverse-carry pass and "
+                                                "reduction), one ssm_selective_scan_bwd call"},
+                                     **nominal(gbs))}}
 
 
 def bench_zoh(args, spec, dev, stream):

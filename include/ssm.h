@@ -138,11 +138,13 @@ typedef struct {
  * shape "Mamba: State Space Models Challenge Transformers", "Selective Scan
  * Algorithm" gives them in its docstring). Each channel then reads its own 2 *
  * dstate values per token and the scan is bound by HBM. Taken by
- * ssm_selective_scan_fwd, ssm_selective_scan_fwd_from_state and
- * ssm_selective_scan_fwd_static with dstate 16, tile_config_hint 0 or 1, and
- * not together with SSM_FLAG_ZOH; by ssm_state_update (any dstate, also with
- * SSM_FLAG_ZOH), whose B and C are then [batch, dim, dstate]; other entry
- * points return SSM_ERR_DIMS.
+ * ssm_selective_scan_fwd, ssm_selective_scan_fwd_from_state,
+ * ssm_selective_scan_fwd_static and the training pair
+ * ssm_selective_scan_fwd_ckpt / ssm_selective_scan_bwd (whose dB and dC then
+ * have B's shape) with dstate 16, tile_config_hint 0 or 1, and not together
+ * with SSM_FLAG_ZOH; by ssm_state_update (any dstate, also with SSM_FLAG_ZOH),
+ * whose B and C are then [batch, dim, dstate]; other entry points return
+ * SSM_ERR_DIMS.
  */
 #define SSM_FLAG_BC_PER_CHANNEL 2
 
@@ -238,6 +240,8 @@ int ssm_selective_scan_fwd_conv(const void* x, const float* conv_w, const float*
  * backpropagates through it; "State Space Models -- Mamba, S4, and Beyond",
  * "Verification Checklist": gradients flow through the discretization).
  * dstate must be 16 and tile_config_hint 0 or 1 (SSM_ERR_DIMS otherwise).
+ * dims->flags may hold SSM_FLAG_ZOH or SSM_FLAG_BC_PER_CHANNEL (not both); the
+ * checkpointing forward and the backward of one step take the same flags.
  *
  * ssm_selective_scan_fwd_ckpt -- ssm_selective_scan_fwd_from_state (h0 may be
  * NULL for zero) that also saves the fp32 state before every 8th token:
@@ -264,7 +268,9 @@ int ssm_selective_scan_fwd_ckpt(const void* x, const void* delta, const float* A
  *                         of the delta input (through softplus and the bias)
  *   dz                  : [batch, seqlen, dim] io dtype, given exactly when z is
  *                         (SSM_ERR_NULL otherwise)
- *   dB, dC              : [batch, seqlen, 16] io dtype (summed over channels)
+ *   dB, dC              : [batch, seqlen, 16] io dtype (summed over channels);
+ *                         [batch, seqlen, dim, 16] with SSM_FLAG_BC_PER_CHANNEL
+ *                         (B and C of that shape too; nothing summed)
  *   dA                  : [dim, 16] fp32 (summed over batch rows and tokens)
  *   dD, ddelta_bias     : [dim] fp32 or NULL (not computed); defined whether or
  *                         not D / delta_bias were given (their gradient at zero)

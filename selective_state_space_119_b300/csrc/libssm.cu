@@ -178,7 +178,8 @@ size_t ckpt_bytes(const ssm_dims* d) {
 }
 
 // Workspace of the backward: status header, the reverse chunk carries, and the
-// per-CTA shares of the summed gradients.
+// per-CTA shares of the summed gradients (no dB | dC shares with per-channel
+// rows: nothing sums over channels there).
 struct BwdLayout {
     size_t off_Q = 0, off_S = 0, off_BC = 0, off_A = 0, off_D = 0, off_bias = 0, bytes = 0;
 };
@@ -195,7 +196,7 @@ BwdLayout bwd_layout(const ssm_dims* d, const ssm::ScanPlan& p) {
         off += align256(b * (K - 1) * dim * 4);
     }
     o.off_BC = off;
-    off += align256(b * tiles * L * 2 * N * 4);
+    if (!(d->flags & SSM_FLAG_BC_PER_CHANNEL)) off += align256(b * tiles * L * 2 * N * 4);
     o.off_A = off;
     off += align256(b * K * dim * N * 4);
     o.off_D = off;
@@ -283,7 +284,7 @@ int scan_impl(const void* x, const void* delta, const float* A, const void* B, c
         return SSM_ERR_DIMS;
     // so are per-channel B and C (and not with the exact zero-order hold)
     const bool bc_per_channel = (dims->flags & SSM_FLAG_BC_PER_CHANNEL) != 0;
-    if (bc_per_channel && (dims->dstate != 16 || dims->tile_config_hint > 1 || cv.w || ckpt ||
+    if (bc_per_channel && (dims->dstate != 16 || dims->tile_config_hint > 1 || cv.w ||
                            (dims->flags & SSM_FLAG_ZOH)))
         return SSM_ERR_DIMS;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -446,9 +447,12 @@ int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A, con
                            const ssm_dims* dims, ssm_stream_t stream) {
     int rc = check_dims(dims, true);
     if (rc != SSM_OK) return rc;
-    // dstate 16, the planner's tile; of the variants, the exact zero-order hold
-    if (dims->dstate != 16 || dims->tile_config_hint > 1 || (dims->flags & ~SSM_FLAG_ZOH))
+    // dstate 16, the planner's tile; either variant (the exact zero-order hold or
+    // per-channel B and C), not both, as in the forward
+    if (dims->dstate != 16 || dims->tile_config_hint > 1 ||
+        ((dims->flags & SSM_FLAG_ZOH) && (dims->flags & SSM_FLAG_BC_PER_CHANNEL)))
         return SSM_ERR_DIMS;
+    const bool bc_per_channel = (dims->flags & SSM_FLAG_BC_PER_CHANNEL) != 0;
     if (dims->batch == 0 || dims->dim == 0) return SSM_OK;
     if ((z == nullptr) != (dz == nullptr) && dims->seqlen > 0) return SSM_ERR_NULL;
     if (!dA) return SSM_ERR_NULL;
@@ -489,7 +493,8 @@ int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A, con
     {
         const size_t es = io_size(dims->io_dtype);
         const size_t elems = size_t(batch) * size_t(L) * size_t(dim);
-        const size_t rows = size_t(batch) * size_t(L) * size_t(N);
+        const size_t rows =
+            size_t(batch) * size_t(L) * size_t(N) * (bc_per_channel ? size_t(dim) : 1);
         const Range in[] = {{x, elems * es},       {delta, elems * es},
                             {z, elems * es},       {dout, elems * es},
                             {B, rows * es},        {C, rows * es},
@@ -519,10 +524,11 @@ int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A, con
         a.wsQ = reinterpret_cast<float*>(ws + lay.off_Q);
         a.wsS = reinterpret_cast<float*>(ws + lay.off_S);
     }
-    a.pBC = reinterpret_cast<float*>(ws + lay.off_BC);
+    a.pBC = bc_per_channel ? nullptr : reinterpret_cast<float*>(ws + lay.off_BC);
     a.pA = reinterpret_cast<float*>(ws + lay.off_A);
     a.pD = reinterpret_cast<float*>(ws + lay.off_D);
     a.pbias = reinterpret_cast<float*>(ws + lay.off_bias);
+    if (bc_per_channel) return set_cuda(ssm::launch_scan_bcd_bwd(a, dims->io_dtype, s));
     return set_cuda(ssm::launch_scan_bwd(a, dims->io_dtype, s));
 }
 

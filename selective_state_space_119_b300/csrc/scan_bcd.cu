@@ -90,9 +90,10 @@ struct Slot {
 };
 
 // MODE 1: the output pass (composes the chunk carries, writes y and the final
-// state); MODE 0: the chunk-state pass (end state from 0 and sum of dt of every
-// chunk but the last). One lane = one channel.
-template <typename T, int N, int MODE, bool SOFTPLUS, bool GATE>
+// state; with CKPT also the state before every kCkptTokens-th token, for the
+// backward); MODE 0: the chunk-state pass (end state from 0 and sum of dt of
+// every chunk but the last). One lane = one channel.
+template <typename T, int N, int MODE, bool SOFTPLUS, bool GATE, bool CKPT = false>
 __global__ void __launch_bounds__(kBcdThreads) scan_bcd_kernel(const ScanArgs a) {
     constexpr bool WITH_C = MODE == 1, WITH_Z = MODE == 1 && GATE;
     using S = Slot<T, N, WITH_C, WITH_Z>;
@@ -159,6 +160,15 @@ __global__ void __launch_bounds__(kBcdThreads) scan_bcd_kernel(const ScanArgs a)
             const S cur = ring[u];
             load(ring[u], t + kRing);   // the loads of a later token, in flight meanwhile
             const bool valid = ch_ok && t < t_end;
+            if constexpr (CKPT) {
+                if (valid && t % kCkptTokens == 0) {
+                    float4* ck = reinterpret_cast<float4*>(
+                        a.ckpt + ((b * a.nckpt + t / kCkptTokens) * a.dim + d) * N);
+#pragma unroll
+                    for (int q = 0; q < N / 4; ++q)
+                        ck[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+                }
+            }
             const float xv = __uint_as_float(cur.x);
             float dt = __uint_as_float(cur.dl) + bias;
             if constexpr (SOFTPLUS) dt = softplus(dt);
@@ -206,8 +216,12 @@ cudaError_t launch_flags(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     if (p.nchunks > 1)
         scan_bcd_kernel<T, N, 0, SOFTPLUS, false>
             <<<static_cast<unsigned>(per_chunk * (p.nchunks - 1)), kBcdThreads, 0, s>>>(a);
-    scan_bcd_kernel<T, N, 1, SOFTPLUS, GATE>
-        <<<static_cast<unsigned>(per_chunk * p.nchunks), kBcdThreads, 0, s>>>(a);
+    if (a.ckpt)
+        scan_bcd_kernel<T, N, 1, SOFTPLUS, GATE, true>
+            <<<static_cast<unsigned>(per_chunk * p.nchunks), kBcdThreads, 0, s>>>(a);
+    else
+        scan_bcd_kernel<T, N, 1, SOFTPLUS, GATE>
+            <<<static_cast<unsigned>(per_chunk * p.nchunks), kBcdThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -141,7 +141,7 @@ struct BwdArgs {
     void* ddelta;
     void* dz;             // NULL without the gate
     float* dh0;           // [batch][dim][N] or NULL
-    void* dB;             // [batch][L][N] io
+    void* dB;             // [batch][L][N] io ([batch][L][dim][N] with per-channel rows)
     void* dC;
     float* dA;            // [dim][N]
     float* dD;            // [dim] or NULL
@@ -169,6 +169,8 @@ cudaError_t launch_state_update(const StepArgs& a, int io, int N, cudaStream_t s
 cudaError_t launch_scan_bcd(const ScanArgs& a, const ScanPlan& p, int io, cudaStream_t s);
 // Enqueue the gradient passes (reverse carries, gradients, reduction).
 cudaError_t launch_scan_bwd(const BwdArgs& a, int io, cudaStream_t s);
+// The same for per-channel B and C (dB, dC [batch][L][dim][N]; pBC unused).
+cudaError_t launch_scan_bcd_bwd(const BwdArgs& a, int io, cudaStream_t s);
 // Mamba-2's SSD layer (bf16 I/O, d_head 64, d_state 128): one launch.
 struct SsdLaunch {
     const void* x;            // [batch, L, H, 64] bf16

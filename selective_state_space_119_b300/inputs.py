@@ -321,6 +321,18 @@ def algorithmic_bytes_scan_bcd(spec: ScanSpec) -> int:
     return spec.elements * per_elem + extra
 
 
+def algorithmic_bytes_scan_bcd_bwd(spec: ScanSpec) -> int:
+    """Bytes of the backward with per-channel B, C: x, delta, (z,) dout and the
+    B, C rows read, dx, ddelta, (dz,) and the dB, dC rows written per element;
+    the saved state before every 8th token read (16 fp32 per channel and 8
+    tokens); A, D, bias read and dA, dD, dbias written once."""
+    es = 2 if spec.io == "bf16" else 4
+    scalars = (7 if spec.gate else 5) * es
+    per_elem = scalars + 4 * spec.N * es + spec.N * 4 / 8
+    extra = 2 * (spec.dim * spec.N * 4 + 2 * spec.dim * 4)
+    return int(spec.elements * per_elem) + extra
+
+
 def algorithmic_bytes_scan(spec: ScanSpec) -> int:
     """Bytes the scan must move at least once: x, delta, z read and y written
     per element; B and C per (b, t); A, D, delta_bias once; final_state written."""

@@ -487,9 +487,9 @@ def ssm_scan_checkpoint_bytes(batch, seqlen, dim, dstate, io) -> int:
 
 
 def ssm_scan_bwd_workspace_bytes(batch, seqlen, dim, dstate, io, chunk_len_hint=0,
-                                 tile_config_hint=0) -> int:
+                                 tile_config_hint=0, flags=0) -> int:
     d = make_dims(batch, seqlen, dim, dstate, io, chunk_len_hint=chunk_len_hint,
-                  tile_config_hint=tile_config_hint)
+                  tile_config_hint=tile_config_hint, flags=flags)
     return int(lib.ssm_scan_bwd_workspace_bytes(ctypes.byref(d)))
 
 
@@ -499,12 +499,16 @@ def ssm_selective_scan_fwd_ckpt(x, delta, A, B, C, D=None, z=None, delta_bias=No
                                 zoh=False):
     """The scan that also saves the state before every 8th token for the
     backward. Returns (out, final_state, ckpt); ckpt is [batch, ceil(L/8), dim,
-    16] fp32. ``zoh=True`` scans with the exact zero-order-hold Bbar."""
+    16] fp32. ``zoh=True`` scans with the exact zero-order-hold Bbar; B and C of
+    shape [batch, L, dim, 16] select per-channel rows."""
     torch = _torch()
     batch, L, dim = x.shape
     N = A.shape[1]
     io = x.dtype
     dev = _device_of(x, "x")
+    bcd = B.dim() == 4
+    bc_shape = (batch, L, dim, N) if bcd else (batch, L, N)
+    flags = (SSM_FLAG_ZOH if zoh else 0) | (SSM_FLAG_BC_PER_CHANNEL if bcd else 0)
     with _launch_on(dev, stream) as sp:
         if out is None:
             out = torch.empty_like(x)
@@ -513,15 +517,16 @@ def ssm_selective_scan_fwd_ckpt(x, delta, A, B, C, D=None, z=None, delta_bias=No
         if ckpt is None:
             ckpt = torch.empty((batch, (L + 7) // 8, dim, N), dtype=torch.float32, device=dev)
         if workspace is None:
-            workspace = alloc_workspace(batch, L, dim, N, _io_code(x), dev, chunk_len_hint)
+            workspace = alloc_workspace(batch, L, dim, N, _io_code(x), dev, chunk_len_hint,
+                                        flags=flags)
         ws_ptr = _ptr(workspace, "workspace", torch.uint8, device=dev)
         ws_bytes = workspace.numel() if workspace is not None else 0
         dims = make_dims(batch, L, dim, N, _io_code(x), ws_ptr, ws_bytes, chunk_len_hint,
-                         flags=SSM_FLAG_ZOH if zoh else 0)
+                         flags=flags)
         rc = lib.ssm_selective_scan_fwd_ckpt(
             _ptr(x, "x", io, (batch, L, dim), dev), _ptr(delta, "delta", io, (batch, L, dim), dev),
-            _ptr(A, "A", torch.float32, (dim, N), dev), _ptr(B, "B", io, (batch, L, N), dev),
-            _ptr(C, "C", io, (batch, L, N), dev), _ptr(D, "D", torch.float32, (dim,), dev),
+            _ptr(A, "A", torch.float32, (dim, N), dev), _ptr(B, "B", io, bc_shape, dev),
+            _ptr(C, "C", io, bc_shape, dev), _ptr(D, "D", torch.float32, (dim,), dev),
             _ptr(z, "z", io, (batch, L, dim), dev),
             _ptr(delta_bias, "delta_bias", torch.float32, (dim,), dev),
             1 if delta_softplus else 0, _ptr(h0, "h0", torch.float32, (batch, dim, N), dev),
@@ -540,7 +545,9 @@ def ssm_selective_scan_bwd(x, delta, A, B, C, ckpt, dout, D=None, z=None, delta_
     """Gradients of the scan (include/ssm.h). Returns a dict with dx, ddelta,
     dA, dB, dC and, when asked for / defined, dD, dz, ddelta_bias, dh0.
     ``zoh=True`` differentiates the exact zero-order-hold scan (the checkpoints
-    must come from a ``zoh=True`` checkpointing forward)."""
+    must come from a ``zoh=True`` checkpointing forward). B and C of shape
+    [batch, L, dim, 16] differentiate the per-channel scan (dB, dC then have
+    that shape too)."""
     torch = _torch()
     batch, L, dim = x.shape
     N = A.shape[1]
@@ -561,10 +568,13 @@ def _bwd_call(x, delta, A, B, C, ckpt, dout, D, z, delta_bias, delta_softplus, d
     N = A.shape[1]
     io = x.dtype
     dev = _device_of(x, "x")
+    bcd = B.dim() == 4
+    bc_shape = (batch, L, dim, N) if bcd else (batch, L, N)
+    flags = (SSM_FLAG_ZOH if zoh else 0) | (SSM_FLAG_BC_PER_CHANNEL if bcd else 0)
     g = {"dx": torch.empty_like(x), "ddelta": torch.empty_like(x),
          "dA": torch.empty((dim, N), dtype=torch.float32, device=dev),
-         "dB": torch.empty((batch, L, N), dtype=io, device=dev),
-         "dC": torch.empty((batch, L, N), dtype=io, device=dev),
+         "dB": torch.empty(bc_shape, dtype=io, device=dev),
+         "dC": torch.empty(bc_shape, dtype=io, device=dev),
          "dD": torch.empty(dim, dtype=torch.float32, device=dev) if want_dD else None,
          "dz": torch.empty_like(x) if z is not None else None,
          "ddelta_bias": (torch.empty(dim, dtype=torch.float32, device=dev)
@@ -572,15 +582,16 @@ def _bwd_call(x, delta, A, B, C, ckpt, dout, D, z, delta_bias, delta_softplus, d
          "dh0": (torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
                  if want_dh0 else None)}
     if workspace is None:
-        n = ssm_scan_bwd_workspace_bytes(batch, L, dim, N, _io_code(x), chunk_len_hint)
+        n = ssm_scan_bwd_workspace_bytes(batch, L, dim, N, _io_code(x), chunk_len_hint,
+                                         flags=flags)
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
     dims = make_dims(batch, L, dim, N, _io_code(x), _ptr(workspace, "workspace", torch.uint8,
                                                          device=dev),
-                     workspace.numel(), chunk_len_hint, flags=SSM_FLAG_ZOH if zoh else 0)
+                     workspace.numel(), chunk_len_hint, flags=flags)
     rc = lib.ssm_selective_scan_bwd(
         _ptr(x, "x", io, (batch, L, dim), dev), _ptr(delta, "delta", io, (batch, L, dim), dev),
-        _ptr(A, "A", torch.float32, (dim, N), dev), _ptr(B, "B", io, (batch, L, N), dev),
-        _ptr(C, "C", io, (batch, L, N), dev), _ptr(D, "D", torch.float32, (dim,), dev),
+        _ptr(A, "A", torch.float32, (dim, N), dev), _ptr(B, "B", io, bc_shape, dev),
+        _ptr(C, "C", io, bc_shape, dev), _ptr(D, "D", torch.float32, (dim,), dev),
         _ptr(z, "z", io, (batch, L, dim), dev),
         _ptr(delta_bias, "delta_bias", torch.float32, (dim,), dev),
         1 if delta_softplus else 0,

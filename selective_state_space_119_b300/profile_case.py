@@ -4,6 +4,8 @@
         --dim 5120 [--A s4d|lognormal] [--softplus] [--chunk-len 0] [--calls 3]
     python -m selective_state_space_119_b300.profile_case ssd --batch 16 --seqlen 1024 \\
         [--heads 8] [--groups 1] [--calls 3]
+    python -m selective_state_space_119_b300.profile_case bcd_train --batch 4 --seqlen 2048 \\
+        --dim 1536 [--calls 3]
 
 The inputs are the seeded workload distributions of ``inputs`` (the scan's
 long-sequence recipe by default: delta log-uniform in [1e-4, 1e-2], gate, D = 1,
@@ -67,9 +69,39 @@ def run_ssd(args, torch):
     print("last call %.3f ms" % e0.elapsed_time(e1), flush=True)
 
 
+def run_bcd_train(args, torch):
+    """Training with per-channel B, C on the softplus recipe: each call is one
+    plain forward, one checkpointing forward and one backward (dout ~ N(0, 1))."""
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+    spec = I.ScanSpec(args.batch, args.seqlen, args.dim, io="bf16", delta_kind="softplus_bias",
+                      A_kind=args.A, D_kind="uniform", seed=3)
+    t = {k: _dev(torch, v) for k, v in I.make_scan_inputs(spec).items()}
+    B4, C4 = (_dev(torch, v) for v in I.make_bc_per_channel(spec))
+    rng = np.random.default_rng(4)
+    dout = _dev(torch, I.store(rng.standard_normal((spec.batch, spec.L, spec.dim)), "bf16"))
+    plan = libssm.ssm_scan_plan(spec.batch, spec.L, spec.dim, 16, "bf16",
+                                flags=libssm.SSM_FLAG_BC_PER_CHANNEL)
+    print("plan", plan, flush=True)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    kw = dict(D=t["D"], z=t["z"], delta_bias=t["delta_bias"], delta_softplus=True)
+    for i in range(args.calls):
+        ev[0].record()
+        libssm.ssm_selective_scan_fwd(t["x"], t["delta"], t["A"], B4, C4, **kw)
+        ev[1].record()
+        _, _, ck = libssm.ssm_selective_scan_fwd_ckpt(t["x"], t["delta"], t["A"], B4, C4, **kw)
+        ev[2].record()
+        libssm.ssm_selective_scan_bwd(t["x"], t["delta"], t["A"], B4, C4, ck, dout, **kw)
+        ev[3].record()
+    torch.cuda.synchronize()
+    print("last call: fwd %.3f ms, fwd_ckpt %.3f ms, bwd %.3f ms (allocations included)"
+          % (ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]), ev[2].elapsed_time(ev[3])),
+          flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("kernel", choices=["scan", "ssd"])
+    ap.add_argument("kernel", choices=["scan", "ssd", "bcd_train"])
     ap.add_argument("--batch", type=int, required=True)
     ap.add_argument("--seqlen", type=int, required=True)
     ap.add_argument("--dim", type=int, default=5120)
@@ -83,7 +115,7 @@ def main(argv=None):
     import torch
     if not torch.cuda.is_available():
         sys.exit("no CUDA device")
-    (run_scan if args.kernel == "scan" else run_ssd)(args, torch)
+    {"scan": run_scan, "ssd": run_ssd, "bcd_train": run_bcd_train}[args.kernel](args, torch)
 
 
 if __name__ == "__main__":

@@ -102,11 +102,11 @@ int main(void)
         bad.seqlen = -1;
         expect(ssm_scan_plan(&bad, &p), SSM_ERR_DIMS, "negative seqlen");
         bad = d;
-        bad.flags = SSM_FLAG_BC_PER_CHANNEL;   /* the backward takes the hold, not per-channel rows */
+        bad.flags = SSM_FLAG_ZOH | SSM_FLAG_BC_PER_CHANNEL;   /* one variant at a time */
         expect(ssm_selective_scan_bwd(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, NULL,
                                       NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
                                       NULL, &bad, NULL),
-               SSM_ERR_DIMS, "backward with per-channel rows");
+               SSM_ERR_DIMS, "backward with both variants");
     }
     expect(ssm_state_update(NULL, dummy, dummy, dummy, dummy, dummy, NULL, NULL, NULL, 0, dummy,
                             &d, NULL),

@@ -297,6 +297,20 @@ def test_bc_per_channel_flag_is_validated():
                 None) == L.SSM_ERR_DIMS
     assert scan(*args, FAKE + (5 << 20), None, ctypes.byref(dims(flags=F | L.SSM_FLAG_ZOH)),
                 None) == L.SSM_ERR_DIMS
+    # the training pair takes per-channel rows: the checkpointing forward is
+    # accepted up to the alias check (its checkpoints over x), the backward too,
+    # with dB 1024 bytes into B (inside B's per-channel 10240 bytes, past the
+    # 640 of a shared row set); both variants at once are refused
+    assert L.lib.ssm_selective_scan_fwd_ckpt(*args, None, FAKE + (5 << 20), None, FAKE,
+                                             ctypes.byref(dims()), None) == L.SSM_ERR_ALIAS
+    G = FAKE + (1 << 36)
+    bwd = L.lib.ssm_selective_scan_bwd
+    grads = lambda dB: (G, G + (1 << 20), G + (2 << 20), dB, G + (3 << 20), None, None, None,
+                        None)
+    assert bwd(*args, FAKE + (6 << 20), FAKE + (7 << 20), None, *grads(FAKE + (3 << 20) + 1024),
+               ctypes.byref(dims()), None) == L.SSM_ERR_ALIAS
+    assert bwd(*args, FAKE + (6 << 20), FAKE + (7 << 20), None, *grads(G + (4 << 20)),
+               ctypes.byref(dims(flags=F | L.SSM_FLAG_ZOH)), None) == L.SSM_ERR_DIMS
     # the decode step takes per-channel rows too; B then spans [batch, dim, N]
     # (2 x 16 x 16 bf16 = 1024 bytes), so an output 640 bytes into it overlaps
     st = L.make_dims(2, 1, 16, 16, "bf16", flags=F)
