@@ -13,18 +13,24 @@
 // state entering it:
 //   G  = C B^T                                  [Q x Q]   (K = N)
 //   M  = G o (exp(s_t - s_u) dt_u)_{u <= t}     masked decay, CUDA cores
-//   Y  = M X + diag(exp(s_t)) C h_in^T + D X    [Q x P]   (K = Q, then K = N)
+//   Y  = (M + D I) X + diag(exp(s_t)) C h_in^T [Q x P]   (K = Q, then K = N)
 //   S  = (w o X)^T B,  w_u = exp(s_Q - s_u) dt_u          (K = Q)
 //   h_out = exp(s_Q) h_in + S
 // This kernel runs one CTA per (batch row, head) over the chunks in order,
 // the state in fp32 registers. Per chunk TMA (cp.async.bulk.tensor, 128-byte
 // swizzle) brings the C, B and X tiles; one thread issues the tcgen05.mma
-// products into tensor memory; the CTA's 128 threads (thread t owns row t of
-// every [Q x .] accumulator, thread n row n of S^T) form M, w o X and the
-// epilogue on the CUDA cores. Operands that the CUDA cores produce (M, w o X
-// and h) are split into a bf16 high part and a bf16 remainder, two products
-// each, so that every product carries about 16 significant bits more than one
-// bf16 rounding would.
+// products into tensor memory; the CTA's 256 threads form M, w o X and the
+// epilogue on the CUDA cores (a thread owns one row of every [Q x .]
+// accumulator, the row of its warp's TMEM lane quarter, and half of its
+// columns: warps w and w + 4 split them). The products are issued as soon as
+// their operands are ready, so that the tensor cores work while the CUDA cores
+// do: G = C B^T and Y2 = C h^T as soon as the B and C tiles have landed (during
+// the cumulative sum of dt and w o X), S^T while M is formed; D x rides in M's
+// diagonal, so that X is free (and reloaded) once Y = M X has completed, and y
+// is staged in the w o X tile for its store. Operands that the CUDA cores
+// produce (M, w o X and h) are split into a bf16 high part and a bf16
+// remainder, two products each, so that every product carries about 16
+// significant bits more than one bf16 rounding would.
 //
 // Sizes: Q = 128 tokens per chunk, P = 64 (d_head), N = 128 (d_state), bf16
 // x, dt, B, C, y; fp32 A, D, dt_bias, h0, final state.
@@ -46,7 +52,8 @@ namespace {
 constexpr int kQ = 128;     // tokens per chunk
 constexpr int kP = 64;      // channels per head
 constexpr int kNs = 128;    // state width
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;   // warps w and w + 4 share TMEM lane quarter w mod 4
+constexpr int kIssuer = 128;    // the thread that issues TMA loads and MMAs (warp 4, lane 0)
 constexpr uint32_t kPolls = 1u << 24;
 constexpr uint32_t kStatusTimeout = 7;
 
@@ -64,8 +71,8 @@ constexpr int oHl = oHh + kBlk;
 constexpr int oDt = oHl + kBlk;                // dt [Q] f32
 constexpr int oS2 = oDt + kQ * 4;              // s log2 e [Q] f32
 constexpr int oWs = oS2 + kQ * 4;              // warp partial sums [4] f32
-constexpr int oBar = oWs + 64;                 // mbarriers: B, C, X loads, mma
-constexpr int oTm = oBar + 32;                 // TMEM base address
+constexpr int oBar = oWs + 64;                 // mbarriers: B, C, X loads; 3 product groups
+constexpr int oTm = oBar + 64;                 // TMEM base address
 constexpr int kSmemUsed = oTm + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -155,15 +162,21 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     float* sdt = reinterpret_cast<float*>(sm + oDt);
     float* ss2 = reinterpret_cast<float*>(sm + oS2);
     float* swarp = reinterpret_cast<float*>(sm + oWs);
-    // one load barrier per tile, so that each tile's next load can start as
-    // soon as the products that read it have completed
+    // one barrier per tile load, so that each tile's next load can start as
+    // soon as the products that read it have completed, and one per group of
+    // products
     uint64_t* bar_B = reinterpret_cast<uint64_t*>(sm + oBar);
     uint64_t* bar_C = bar_B + 1;
     uint64_t* bar_X = bar_B + 2;
-    uint64_t* bar_mma = bar_B + 3;
+    uint64_t* bar_G = bar_B + 3;   // G = C B^T and Y2 = C h^T
+    uint64_t* bar_S = bar_B + 4;   // S^T = B^T (w o X)
+    uint64_t* bar_Y = bar_B + 5;   // Y = M X
     uint32_t* tm_slot = reinterpret_cast<uint32_t*>(sm + oTm);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, grp = warp >> 2;
+    const int row = 32 * quarter + lane;   // this thread's TMEM lane and tile row
+    const bool issuer = tid == kIssuer;
     const int64_t b = blockIdx.x / a.H, hd = blockIdx.x % a.H;
     const int64_t g = hd / (a.H / a.G);
     const int nchunks = static_cast<int>((a.L + kQ - 1) / kQ);
@@ -172,11 +185,8 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     const float bias = a.dt_bias ? __ldg(a.dt_bias + hd) : 0.f;
     const uint32_t sbase = smem_u32(sm);
 
-    if (tid == 0) {
-        mbar_init(bar_B, 1);
-        mbar_init(bar_C, 1);
-        mbar_init(bar_X, 1);
-        mbar_init(bar_mma, 1);
+    if (issuer) {
+        for (int i = 0; i < 6; ++i) mbar_init(bar_B + i, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -187,29 +197,32 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tm_slot;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;   // this warp's TMEM lanes
+    const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;   // this warp's TMEM lanes
 
-    // the state: thread n holds h[p][n] for p = 0 .. 63 (fp32), and writes it
-    // as the MN-major operand [n rows x p] of C h^T
-    float h[kP];
+    // the state: thread (row n, group g) holds h[p][n] for p = 32 g .. 32 g + 31
+    // (fp32) and writes it as rows n of the MN-major operand [n x p] of C h^T
+    float h[32];
     {
-        const int n = tid;
+        const int n = row;
 #pragma unroll
-        for (int p = 0; p < kP; ++p)
-            h[p] = a.h0 ? a.h0[(((b * a.H + hd) * kP) + p) * kNs + n] : 0.f;
+        for (int i = 0; i < 32; ++i)
+            h[i] = a.h0 ? a.h0[(((b * a.H + hd) * kP) + 32 * grp + i) * kNs + n] : 0.f;
 #pragma unroll
-        for (int c = 0; c < kP / 8; ++c) {
+        for (int k = 0; k < 4; ++k) {
             float v[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = h[8 * c + i];
-            put8_split(sm + oHh, sm + oHl, n, c, v);
+            for (int i = 0; i < 8; ++i) v[i] = h[8 * k + i];
+            put8_split(sm + oHh, sm + oHl, n, 4 * grp + k, v);
         }
     }
+    // the first chunk's C h^T reads these rows through the async proxy
+    fence_proxy_async_smem();
+    __syncthreads();
 
     const int gg = static_cast<int>(g), bb = static_cast<int>(b), hh = static_cast<int>(hd);
-    // the barrier phase of each tile's load in flight, -1 for none (thread 0
-    // only; the abort path waits for them)
-    int pend_B = -1, pend_C = -1, pend_X = -1;
+    // the barrier phase of each load and product group in flight, -1 for none
+    // (issuer only; the abort path waits for them)
+    int pend_B = -1, pend_C = -1, pend_X = -1, pend_G = -1, pend_S = -1, pend_Y = -1;
     auto load_B = [&](int c) {
         mbar_arrive_expect_tx(bar_B, 2 * kBlk);
         tma_load_4d(sm + oB, &tm_B, 0, gg, c * kQ, bb, bar_B);
@@ -227,29 +240,58 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         tma_load_4d(sm + oX, &tm_x, 0, hh, c * kQ, bb, bar_X);
         pend_X = c & 1;
     };
-    if (tid == 0) {
+    if (issuer) {
         load_B(0);
         load_C(0);
         load_X(0);
     }
 
-    // this thread's token of chunk c: raw dt (bf16), 0 past the sequence end
+    // this thread's token of chunk c (threads 0 .. 127): raw dt (bf16), 0 past
+    // the sequence end
     auto load_dt = [&](int c) {
         const int64_t t = int64_t(c) * kQ + tid;
         return t < a.L ? IO<__nv_bfloat16>::ld(static_cast<const __nv_bfloat16*>(a.dt) +
                                                 (b * a.L + t) * a.H + hd)
                        : 0.f;
     };
-    float dt_next = load_dt(0);
+    float dt_next = tid < kQ ? load_dt(0) : 0.f;
 
-    uint32_t mma_phase = 0;
     bool ok = true;
-    for (int c = 0; c < nchunks && ok; ++c) {
+    for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kQ;
-        const uint32_t ld_phase = static_cast<uint32_t>(c & 1);   // each tile loads once per chunk
-        // dt of the chunk (0 past the sequence end; loaded a chunk ahead, so
-        // the load is off the chunk's critical path), then s = A * cumsum(dt)
-        {
+        const uint32_t ph = static_cast<uint32_t>(c & 1);   // every barrier completes once per chunk
+        // G = C B^T and Y2 = C h^T as soon as the B and C tiles have landed (h
+        // is the state after the previous chunks, written by their epilogue)
+        if (issuer) {
+            ok = mbar_wait_bounded(bar_B, ph, kPolls) && mbar_wait_bounded(bar_C, ph, kPolls);
+            if (ok) {
+                pend_B = pend_C = -1;
+                tc::fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < kNs / 16; ++k) {   // K = n in steps of 16 over two blocks
+                    const uint32_t off = (k >> 2) * kBlk + (k & 3) * 32;
+                    tc::mma_bf16(tmem + kColG, tc::desc_sw128(sbase + oC + off, 16, 1024),
+                                 tc::desc_sw128(sbase + oB + off, 16, 1024), kIdG, k > 0);
+                }
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {   // B = h MN-major (rows n), high then remainder
+                    const uint32_t hb = sbase + (part ? oHl : oHh);
+#pragma unroll
+                    for (int k = 0; k < kNs / 16; ++k) {
+                        const uint32_t offa = (k >> 2) * kBlk + (k & 3) * 32;
+                        tc::mma_bf16(tmem + kColY2, tc::desc_sw128(sbase + oC + offa, 16, 1024),
+                                     tc::desc_sw128(hb + k * 2048, 1024, 1024), kIdY,
+                                     part > 0 || k > 0);
+                    }
+                }
+                tc::mma_commit(bar_G);
+                pend_G = static_cast<int>(ph);
+            }
+        }
+        // dt of the chunk (0 past the sequence end; loaded a chunk ahead), then
+        // s = A * cumsum(dt), one token per thread of warps 0-3
+        float cs = 0.f;
+        if (tid < kQ) {
             float v = 0.f;
             if (t0 + tid < a.L) {
                 v = dt_next + bias;
@@ -257,29 +299,34 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             }
             dt_next = load_dt(c + 1);
             sdt[tid] = v;
-            float cs = v;
+            cs = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float u = __shfl_up_sync(0xffffffffu, cs, o);
                 if (lane >= o) cs += u;
             }
             if (lane == 31) swarp[warp] = cs;
-            __syncthreads();
+        }
+        // the previous chunk's y store has read its staging tile (w o X below)
+        if (issuer && c > 0) bulk_wait_read<0>();
+        if (__syncthreads_or(!ok)) break;
+        if (tid < kQ) {
             for (int w = 0; w < warp; ++w) cs += swarp[w];
             ss2[tid] = cs * A2;   // s_t log2 e
         }
-        // (the next read of swarp is a chunk later, after several barriers)
-        ok = mbar_wait_bounded(bar_B, ld_phase, kPolls) && mbar_wait_bounded(bar_C, ld_phase, kPolls) &&
-             mbar_wait_bounded(bar_X, ld_phase, kPolls);
-        if (ok) pend_B = pend_C = pend_X = -1;
-        __syncthreads();   // ss2 complete
+        // (the next write of swarp is a chunk later, after several barriers)
+        ok = mbar_wait_bounded(bar_X, ph, kPolls);
+        if (ok && issuer) pend_X = -1;
+        if (__syncthreads_or(!ok)) break;   // ss2 complete
         const float s_end = ss2[kQ - 1];
-        // w o X (high and remainder), row u = this thread, w_u = exp(s_end - s_u) dt_u
+        // w o X (high and remainder): row u = this thread's row, columns of its
+        // group, w_u = exp(s_end - s_u) dt_u
         {
-            const int u = tid;
+            const int u = row;
             const float w = ex2(s_end - ss2[u]) * sdt[u];
 #pragma unroll
-            for (int cc = 0; cc < kP / 8; ++cc) {
+            for (int k = 0; k < 4; ++k) {
+                const int cc = 4 * grp + k;
                 float v[8];
                 get8(sm + oX, u, cc, v);
 #pragma unroll
@@ -289,16 +336,9 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         }
         fence_proxy_async_smem();
         tc::fence_before_sync();
-        ok = !__syncthreads_or(!ok);
+        __syncthreads();
         tc::fence_after_sync();
-        if (ok && tid == 0) {
-            // G = C B^T: 8 steps of K = 16 over the two 64-wide n blocks
-#pragma unroll
-            for (int k = 0; k < kNs / 16; ++k) {
-                const uint32_t off = (k >> 2) * kBlk + (k & 3) * 32;
-                tc::mma_bf16(tmem + kColG, tc::desc_sw128(sbase + oC + off, 16, 1024),
-                             tc::desc_sw128(sbase + oB + off, 16, 1024), kIdG, k > 0);
-            }
+        if (issuer) {
             // S^T = B^T (w o X): A = the B tile read MN-major (M = n over two
             // 64-wide blocks 16 KB apart), B = w o X MN-major; K = u in steps of 16 rows
 #pragma unroll
@@ -311,40 +351,63 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                                  tc::desc_sw128(wx + off, 1024, 1024), kIdS, part > 0 || k > 0);
                 }
             }
-            tc::mma_commit(bar_mma);
+            tc::mma_commit(bar_S);
+            pend_S = static_cast<int>(ph);
         }
-        ok = ok && mbar_wait_bounded(bar_mma, mma_phase, kPolls);
-        mma_phase ^= 1;
+        // M = G o decay o dt + D on the diagonal (so that M X carries D x), row
+        // t = this thread's row, high and remainder, while S computes. Warps w
+        // and w + 4 split the 32-column blocks q of rows 32 (w mod 4) ..: the
+        // blocks q > w mod 4 lie above the diagonal (zero), q < w mod 4 below it
+        // (no mask).
+        ok = mbar_wait_bounded(bar_G, ph, kPolls);
         tc::fence_after_sync();
-        // G and S^T are done with the B tile: the next chunk's B can land
-        if (ok && tid == 0 && c + 1 < nchunks) load_B(c + 1);
-        // M = G o decay o dt (row t = this thread), high and remainder
-        {
-            const int t = tid;
+        if (ok && issuer) {
+            pend_G = -1;
+            if (c + 1 < nchunks) load_C(c + 1);   // G and Y2 are done with the C tile
+        }
+        if (ok) {
+            const int t = row;
             const float st = ss2[t];
 #pragma unroll
-            for (int q = 0; q < kQ / 32; ++q) {
+            for (int qi = 0; qi < 2; ++qi) {
+                const int q = grp + 2 * qi;
+                const int ublk = q >> 1;          // which 64-wide u block
+                const int c0 = (q & 1) * 4;       // its first 16-byte chunk in the row
+                if (q > quarter) {
+                    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint32_t off = tc::sw128(t, 8 * (c0 + cc));
+                        *reinterpret_cast<uint4*>(sm + oMh + ublk * kBlk + off) = zero;
+                        *reinterpret_cast<uint4*>(sm + oMl + ublk * kBlk + off) = zero;
+                    }
+                    continue;
+                }
                 float gv[32];
                 tc::tmem_ld32(tmem + lane_base + kColG + 32 * q, gv);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
+                    const float4* dtv = reinterpret_cast<const float4*>(sdt + 32 * q + 8 * cc);
+                    const float4* ssv = reinterpret_cast<const float4*>(ss2 + 32 * q + 8 * cc);
+                    const float4 d0 = dtv[0], d1 = dtv[1], s0 = ssv[0], s1 = ssv[1];
+                    const float du[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+                    const float su[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
                     float v[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int u = 32 * q + 8 * cc + i;
-                        v[i] = u <= t ? gv[8 * cc + i] * sdt[u] * ex2(st - ss2[u]) : 0.f;
+                        const float m = gv[8 * cc + i] * du[i] * ex2(st - su[i]);
+                        v[i] = (q < quarter || u < t) ? m : (u == t ? m + Dh : 0.f);
                     }
-                    const int ublk = (32 * q) / 64;              // which 64-wide u block
-                    const int cch = ((32 * q) % 64) / 8 + cc;     // 16-byte chunk in the row
-                    put8_split(sm + oMh + ublk * kBlk, sm + oMl + ublk * kBlk, t, cch, v);
+                    put8_split(sm + oMh + ublk * kBlk, sm + oMl + ublk * kBlk, t, c0 + cc, v);
                 }
             }
         }
         fence_proxy_async_smem();
         tc::fence_before_sync();
-        ok = !__syncthreads_or(!ok);
+        if (__syncthreads_or(!ok)) break;
         tc::fence_after_sync();
-        if (ok && tid == 0) {
+        if (issuer) {
             // Y = M X: A = M (K-major, K = u over two blocks), B = X MN-major
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
@@ -357,92 +420,77 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                                  part > 0 || k > 0);
                 }
             }
-            // Y2 = C h^T: A = C (K-major, K = n), B = h MN-major (rows n)
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                const uint32_t hb = sbase + (part ? oHl : oHh);
-#pragma unroll
-                for (int k = 0; k < kNs / 16; ++k) {
-                    const uint32_t offa = (k >> 2) * kBlk + (k & 3) * 32;
-                    tc::mma_bf16(tmem + kColY2, tc::desc_sw128(sbase + oC + offa, 16, 1024),
-                                 tc::desc_sw128(hb + k * 2048, 1024, 1024), kIdY,
-                                 part > 0 || k > 0);
-                }
-            }
-            tc::mma_commit(bar_mma);
+            tc::mma_commit(bar_Y);
+            pend_Y = static_cast<int>(ph);
         }
-        ok = ok && mbar_wait_bounded(bar_mma, mma_phase, kPolls);
-        mma_phase ^= 1;
+        // epilogue once S and Y have landed: y = Y + exp(s_t) Y2 (row t, the
+        // group's 32 columns) into the staging tile (w o X is no longer read);
+        // state: h <- exp(s_end) h + S (row n, the group's 32 p)
+        ok = mbar_wait_bounded(bar_S, ph, kPolls) && mbar_wait_bounded(bar_Y, ph, kPolls);
         tc::fence_after_sync();
-        // Y2 is done with the C tile: the next chunk's C can land
-        if (ok && tid == 0 && c + 1 < nchunks) load_C(c + 1);
-        // epilogue: y = Y + exp(s_t) Y2 + D x (row t), in place over x;
-        // state: h <- exp(s_end) h + S (row n = this thread)
-        {
-            const int t = tid;
+        if (ok && issuer) {
+            pend_S = pend_Y = -1;
+            if (c + 1 < nchunks) {   // S is done with B, Y with X
+                load_B(c + 1);
+                load_X(c + 1);
+            }
+        }
+        if (ok) {
+            const int t = row;
             const float et = ex2(ss2[t]);
+            float yv[32], y2[32];
+            tc::tmem_ld32(tmem + lane_base + kColY + 32 * grp, yv);
+            tc::tmem_ld32(tmem + lane_base + kColY2 + 32 * grp, y2);
 #pragma unroll
-            for (int q = 0; q < kP / 32; ++q) {
-                float yv[32], y2[32];
-                tc::tmem_ld32(tmem + lane_base + kColY + 32 * q, yv);
-                tc::tmem_ld32(tmem + lane_base + kColY2 + 32 * q, y2);
+            for (int k = 0; k < 4; ++k) {
+                float o[8];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    float xv[8];
-                    const int ch = 4 * q + cc;
-                    get8(sm + oX, t, ch, xv);
-                    float o[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        o[i] = fmaf(Dh, xv[i], fmaf(et, y2[8 * cc + i], yv[8 * cc + i]));
-                    *reinterpret_cast<uint4*>(sm + oX + tc::sw128(t, 8 * ch)) =
-                        make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
-                                   pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
-                }
+                for (int i = 0; i < 8; ++i) o[i] = fmaf(et, y2[8 * k + i], yv[8 * k + i]);
+                *reinterpret_cast<uint4*>(sm + oWh + tc::sw128(t, 8 * (4 * grp + k))) =
+                    make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
+                               pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
             }
             const float eend = ex2(s_end);
+            float sv[32];
+            tc::tmem_ld32(tmem + lane_base + kColS + 32 * grp, sv);
 #pragma unroll
-            for (int q = 0; q < kP / 32; ++q) {
-                float sv[32];
-                tc::tmem_ld32(tmem + lane_base + kColS + 32 * q, sv);
+            for (int i = 0; i < 32; ++i) h[i] = fmaf(eend, h[i], sv[i]);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) h[32 * q + i] = fmaf(eend, h[32 * q + i], sv[i]);
-            }
-#pragma unroll
-            for (int cc = 0; cc < kP / 8; ++cc) {
+            for (int k = 0; k < 4; ++k) {
                 float v[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = h[8 * cc + i];
-                put8_split(sm + oHh, sm + oHl, tid, cc, v);
+                for (int i = 0; i < 8; ++i) v[i] = h[8 * k + i];
+                put8_split(sm + oHh, sm + oHl, row, 4 * grp + k, v);
             }
         }
         fence_proxy_async_smem();
         tc::fence_before_sync();
-        ok = !__syncthreads_or(!ok);
+        if (__syncthreads_or(!ok)) break;
         tc::fence_after_sync();
-        if (ok && tid == 0) {
-            tma_store_4d(&tm_y, 0, static_cast<int>(hd), t0, static_cast<int>(b), sm + oX);
+        if (issuer) {
+            tma_store_4d(&tm_y, 0, static_cast<int>(hd), t0, static_cast<int>(b), sm + oWh);
             bulk_commit();
-            bulk_wait_read<0>();   // the X tile is reloaded by the next chunk
-            if (c + 1 < nchunks) load_X(c + 1);
         }
-        __syncthreads();
     }
-    if (tid == 0) bulk_wait_all();
+    ok = !__syncthreads_or(!ok);   // every thread leaves the loop at the same barrier
+    if (issuer) bulk_wait_all();
     if (!ok) {
-        if (tid == 0) {
-            // let a load in flight land before the CTA releases its memory
-            // (each tile load still in flight is waited for once more, bounded)
+        if (issuer) {
+            // let the loads and products in flight land before the CTA releases
+            // its memory (each waited for once more, bounded)
             if (pend_B >= 0) mbar_wait_bounded(bar_B, static_cast<uint32_t>(pend_B), kPolls);
             if (pend_C >= 0) mbar_wait_bounded(bar_C, static_cast<uint32_t>(pend_C), kPolls);
             if (pend_X >= 0) mbar_wait_bounded(bar_X, static_cast<uint32_t>(pend_X), kPolls);
+            if (pend_G >= 0) mbar_wait_bounded(bar_G, static_cast<uint32_t>(pend_G), kPolls);
+            if (pend_S >= 0) mbar_wait_bounded(bar_S, static_cast<uint32_t>(pend_S), kPolls);
+            if (pend_Y >= 0) mbar_wait_bounded(bar_Y, static_cast<uint32_t>(pend_Y), kPolls);
             if (a.status) atomicExch(a.status, kStatusTimeout);
         }
     } else if (a.final_state) {
-        const int n = tid;
+        const int n = row;
 #pragma unroll
-        for (int p = 0; p < kP; ++p)
-            a.final_state[(((b * a.H + hd) * kP) + p) * kNs + n] = h[p];
+        for (int i = 0; i < 32; ++i)
+            a.final_state[(((b * a.H + hd) * kP) + 32 * grp + i) * kNs + n] = h[i];
     }
     tc::fence_before_sync();
     __syncthreads();
