@@ -15,7 +15,7 @@
 // before it, ahead of any arithmetic (kRun + 3 independent 16-byte loads in
 // flight per thread) and keeps the window in registers. A CTA is 32 lanes of
 // consecutive channel vectors (a warp's load of one row is 512 contiguous
-// bytes) by 8 warps of consecutive runs; the halo rows a run re-reads were
+// bytes) by 4 warps of consecutive runs; the halo rows a run re-reads were
 // loaded by the warp before it and come from L1/L2. The taps of the CTA's
 // channels are one contiguous block of [channel][K] floats: they are staged
 // through shared memory with coalesced loads (per-lane loads of them would
@@ -29,7 +29,7 @@
 namespace ssm {
 namespace {
 
-constexpr int kConvThreads = 256;
+constexpr int kConvThreads = 128;   // (a launch-shape sweep on b4 L2048 d1536: 128 x 4 per SM best)
 constexpr int kRun = 8;                    // tokens per thread
 constexpr int kHalo = kMaxConvK - 1;       // rows before the run
 
@@ -65,8 +65,25 @@ __device__ __forceinline__ uint4 pack16(const float (&v)[16 / sizeof(T)]) {
     }
 }
 
-template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads, 2) conv1d_silu_kernel(const ConvArgs a) {
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// silu on a pair, with packed FP32 arithmetic: z / (1 + 2^(-z log2 e)); below
+// z = -88 the exponential is inf, its reciprocal 0 and the result -0.
+__device__ __forceinline__ float2 silu2(float2 z) {
+    const float2 s = __fmul2_rn(z, make_float2(-kLog2e, -kLog2e));
+    const float2 d = __ffma2_rn(make_float2(ex2(s.x), ex2(s.y)), make_float2(1.f, 1.f),
+                                make_float2(1.f, 1.f));
+    return __fmul2_rn(z, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+
+template <typename T, int K, int RUN = kRun, int THREADS = kConvThreads, int MINB = 4>
+__global__ void __launch_bounds__(THREADS, MINB) conv1d_silu_kernel(const ConvArgs a) {
+    constexpr int kRun = RUN;
+    constexpr int kConvThreads = THREADS;
     constexpr int VE = 16 / sizeof(T);     // channels per thread
     constexpr int NF = VE * K / 4;         // float4 of taps per lane
     constexpr int NFP = NF + 1;            // padded lane stride in shared memory
@@ -109,6 +126,7 @@ __global__ void __launch_bounds__(kConvThreads, 2) conv1d_silu_kernel(const Conv
     __syncthreads();
     if (!active) return;
 
+    // taps and bias of channel pairs (c, c + 1), for packed FP32 arithmetic
     float tap[VE * K], bias[VE];
 #pragma unroll
     for (int j = 0; j < NF; ++j) {
@@ -122,20 +140,27 @@ __global__ void __launch_bounds__(kConvThreads, 2) conv1d_silu_kernel(const Conv
     }
 #pragma unroll
     for (int i = 0; i < kRun; ++i) {
-        float acc[VE];
+        float2 acc[VE / 2];
 #pragma unroll
-        for (int c = 0; c < VE; ++c) acc[c] = bias[c];
+        for (int c = 0; c < VE / 2; ++c) acc[c] = make_float2(bias[2 * c], bias[2 * c + 1]);
         // tap k multiplies the row K - 1 - k tokens before t (row kHalo + i is t)
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             float v[VE];
             unpack16<T>(raw[kHalo + i - (K - 1) + k], v);
 #pragma unroll
-            for (int c = 0; c < VE; ++c) acc[c] = fmaf(tap[c * K + k], v[c], acc[c]);
+            for (int c = 0; c < VE / 2; ++c)
+                acc[c] = __ffma2_rn(make_float2(tap[2 * c * K + k], tap[(2 * c + 1) * K + k]),
+                                    make_float2(v[2 * c], v[2 * c + 1]), acc[c]);
         }
+        float o[VE];
 #pragma unroll
-        for (int c = 0; c < VE; ++c) acc[c] = silu(acc[c]);
-        if (t0 + i < a.L) *reinterpret_cast<uint4*>(u + (t0 + i) * a.dim) = pack16<T>(acc);
+        for (int c = 0; c < VE / 2; ++c) {
+            const float2 r = silu2(acc[c]);
+            o[2 * c] = r.x;
+            o[2 * c + 1] = r.y;
+        }
+        if (t0 + i < a.L) *reinterpret_cast<uint4*>(u + (t0 + i) * a.dim) = pack16<T>(o);
     }
 }
 

@@ -27,7 +27,7 @@
 namespace ssm {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;                // 3 CTAs (12 warps) per SM at <= 170 registers
 constexpr int kRun = 8;                      // tokens per thread
 constexpr int kRuns = kThreads / 32;         // runs (warps) per CTA
 constexpr int kVE = 4;                       // channels per thread
@@ -65,7 +65,7 @@ __device__ __forceinline__ float dsilu(float p) {
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kThreads) conv1d_silu_bwd_kernel(const ConvBwdArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) conv1d_silu_bwd_kernel(const ConvBwdArgs a) {
     constexpr int NX = kRun + 2 * (K - 1);   // x rows: t0 - K + 1 .. t0 + kRun + K - 2
     constexpr int ND = kRun + K - 1;         // du / dpre rows: t0 .. t0 + kRun + K - 2
     __shared__ float s_part[kRuns][32][kVE * (K + 1)];

@@ -85,6 +85,7 @@ constexpr uint32_t kIdS = tc::idesc_bf16(128, kP, true, true);     // B^T (MN-ma
 constexpr uint32_t kIdY = tc::idesc_bf16(128, kP, false, true);    // M (K-major) X (MN-major)
 
 struct SsdArgs {
+    const void* x;            // [batch, L, H, 64] bf16 (rows of w o X, read directly)
     const void* dt;           // [batch, L, H] bf16
     const float* A;           // [H]
     const float* D;           // [H] or NULL
@@ -100,37 +101,23 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
 }
-__device__ __forceinline__ float bf16_round(float v) {
-    return __bfloat162float(__float2bfloat16_rn(v));
-}
-
 // Row r of a [128 x 64] swizzled block holds 64 values; write 8 of them (one
-// 16-byte chunk, columns 8c .. 8c+7) as bf16 high parts and remainders.
+// 16-byte chunk, columns 8c .. 8c+7) as bf16 high parts and remainders: per
+// pair, the high parts rounded to bf16, widened back, and the remainder
+// v - high (exact in fp32) rounded to bf16.
 __device__ __forceinline__ void put8_split(unsigned char* hi, unsigned char* lo, uint32_t r,
                                            uint32_t c, const float (&v)[8]) {
-    float h[8], l[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        h[i] = bf16_round(v[i]);
-        l[i] = v[i] - h[i];
-    }
-    const uint32_t off = tc::sw128(r, 8 * c);
-    *reinterpret_cast<uint4*>(hi + off) =
-        make_uint4(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]), pack_bf16(h[4], h[5]),
-                   pack_bf16(h[6], h[7]));
-    *reinterpret_cast<uint4*>(lo + off) =
-        make_uint4(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]), pack_bf16(l[4], l[5]),
-                   pack_bf16(l[6], l[7]));
-}
-
-__device__ __forceinline__ void get8(const unsigned char* blk, uint32_t r, uint32_t c, float (&v)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(blk + tc::sw128(r, 8 * c));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t hw[4], lw[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __uint_as_float(w[i] << 16);
-        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        hw[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+        const float2 hf = make_float2(__uint_as_float(hw[i] << 16), __uint_as_float(hw[i] & 0xffff0000u));
+        const float2 l = __ffma2_rn(hf, make_float2(-1.f, -1.f), make_float2(v[2 * i], v[2 * i + 1]));
+        lw[i] = pack_bf16(l.x, l.y);
     }
+    const uint32_t off = tc::sw128(r, 8 * c);
+    *reinterpret_cast<uint4*>(hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* tm, int c0, int c1, int c2,
@@ -255,6 +242,19 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                        : 0.f;
     };
     float dt_next = tid < kQ ? load_dt(0) : 0.f;
+    // this thread's part of x row `row` of chunk c (its group's 32 channels),
+    // for w o X: loaded from global memory a chunk ahead, so that the X tile
+    // is read by Y = M X alone and can be reloaded while the next chunk starts
+    auto load_xrow = [&](int c, uint4 (&xr)[4]) {
+        const int64_t t = int64_t(c) * kQ + row;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(a.x) + ((b * a.L + (t < a.L ? t : 0)) * a.H + hd) * kP +
+            32 * grp);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) xr[k] = t < a.L ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    uint4 xrow[4];
+    load_xrow(0, xrow);
 
     bool ok = true;
     for (int c = 0; c < nchunks; ++c) {
@@ -315,24 +315,28 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             ss2[tid] = cs * A2;   // s_t log2 e
         }
         // (the next write of swarp is a chunk later, after several barriers)
-        ok = mbar_wait_bounded(bar_X, ph, kPolls);
-        if (ok && issuer) pend_X = -1;
         if (__syncthreads_or(!ok)) break;   // ss2 complete
         const float s_end = ss2[kQ - 1];
         // w o X (high and remainder): row u = this thread's row, columns of its
-        // group, w_u = exp(s_end - s_u) dt_u
+        // group, w_u = exp(s_end - s_u) dt_u; then the next chunk's x row
         {
             const int u = row;
             const float w = ex2(s_end - ss2[u]) * sdt[u];
+            const float2 w2 = make_float2(w, w);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int cc = 4 * grp + k;
+                const uint32_t wd[4] = {xrow[k].x, xrow[k].y, xrow[k].z, xrow[k].w};
                 float v[8];
-                get8(sm + oX, u, cc, v);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] *= w;
-                put8_split(sm + oWh, sm + oWl, u, cc, v);
+                for (int i = 0; i < 4; ++i) {
+                    const float2 p = __fmul2_rn(w2, make_float2(__uint_as_float(wd[i] << 16),
+                                                                __uint_as_float(wd[i] & 0xffff0000u)));
+                    v[2 * i] = p.x;
+                    v[2 * i + 1] = p.y;
+                }
+                put8_split(sm + oWh, sm + oWl, u, 4 * grp + k, v);
             }
+            load_xrow(c + 1, xrow);
         }
         fence_proxy_async_smem();
         tc::fence_before_sync();
@@ -385,6 +389,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 }
                 float gv[32];
                 tc::tmem_ld32(tmem + lane_base + kColG + 32 * q, gv);
+                const float2 st2 = make_float2(st, st);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const float4* dtv = reinterpret_cast<const float4*>(sdt + 32 * q + 8 * cc);
@@ -394,10 +399,23 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     const float su[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
                     float v[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int u = 32 * q + 8 * cc + i;
-                        const float m = gv[8 * cc + i] * du[i] * ex2(st - su[i]);
-                        v[i] = (q < quarter || u < t) ? m : (u == t ? m + Dh : 0.f);
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 ds = __ffma2_rn(make_float2(su[2 * i], su[2 * i + 1]),
+                                                     make_float2(-1.f, -1.f), st2);   // s_t - s_u
+                        const float2 e = make_float2(ex2(ds.x), ex2(ds.y));
+                        const float2 m = __fmul2_rn(
+                            __fmul2_rn(make_float2(gv[8 * cc + 2 * i], gv[8 * cc + 2 * i + 1]),
+                                       make_float2(du[2 * i], du[2 * i + 1])),
+                            e);
+                        v[2 * i] = m.x;
+                        v[2 * i + 1] = m.y;
+                    }
+                    if (q == quarter) {   // the diagonal block: zero above, D on the diagonal
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int u = 32 * q + 8 * cc + i;
+                            v[i] = u < t ? v[i] : (u == t ? v[i] + Dh : 0.f);
+                        }
                     }
                     put8_split(sm + oMh + ublk * kBlk, sm + oMl + ublk * kBlk, t, c0 + cc, v);
                 }
@@ -408,7 +426,13 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         if (__syncthreads_or(!ok)) break;
         tc::fence_after_sync();
         if (issuer) {
-            // Y = M X: A = M (K-major, K = u over two blocks), B = X MN-major
+            // Y = M X once the X tile has landed: A = M (K-major, K = u over two
+            // blocks), B = X MN-major
+            ok = mbar_wait_bounded(bar_X, ph, kPolls);
+            if (ok) pend_X = -1;
+            tc::fence_after_sync();
+        }
+        if (issuer && ok) {
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
                 const uint32_t m = sbase + (part ? oMl : oMh);
@@ -422,6 +446,12 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             }
             tc::mma_commit(bar_Y);
             pend_Y = static_cast<int>(ph);
+            // S (issued before M) is done with the B tile: the next chunk's B can land
+            ok = mbar_wait_bounded(bar_S, ph, kPolls);
+            if (ok) {
+                pend_S = -1;
+                if (c + 1 < nchunks) load_B(c + 1);
+            }
         }
         // epilogue once S and Y have landed: y = Y + exp(s_t) Y2 (row t, the
         // group's 32 columns) into the staging tile (w o X is no longer read);
@@ -429,11 +459,8 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         ok = mbar_wait_bounded(bar_S, ph, kPolls) && mbar_wait_bounded(bar_Y, ph, kPolls);
         tc::fence_after_sync();
         if (ok && issuer) {
-            pend_S = pend_Y = -1;
-            if (c + 1 < nchunks) {   // S is done with B, Y with X
-                load_B(c + 1);
-                load_X(c + 1);
-            }
+            pend_Y = -1;
+            if (c + 1 < nchunks) load_X(c + 1);   // Y is done with the X tile
         }
         if (ok) {
             const int t = row;
@@ -539,7 +566,7 @@ cudaError_t launch_ssd(const SsdLaunch& l, cudaStream_t s) {
     if ((e = make_tmap4(&tB, l.B, l.batch, l.L, l.G, kNs)) != cudaSuccess) return e;
     if ((e = make_tmap4(&tC, l.C, l.batch, l.L, l.G, kNs)) != cudaSuccess) return e;
     SsdArgs a{};
-    a.dt = l.dt; a.A = l.A; a.D = l.D; a.dt_bias = l.dt_bias; a.softplus = l.softplus;
+    a.x = l.x; a.dt = l.dt; a.A = l.A; a.D = l.D; a.dt_bias = l.dt_bias; a.softplus = l.softplus;
     a.h0 = l.h0; a.final_state = l.final_state;
     a.batch = l.batch; a.L = l.L; a.H = l.H; a.G = l.G; a.status = l.status;
     ssd_kernel<<<static_cast<unsigned>(l.batch * l.H), kThreads, kSmemBytes, s>>>(tx, tB, tC, ty, a);

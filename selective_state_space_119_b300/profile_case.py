@@ -5,7 +5,7 @@
     python -m selective_state_space_119_b300.profile_case ssd --batch 16 --seqlen 1024 \\
         [--heads 8] [--groups 1] [--calls 3]
     python -m selective_state_space_119_b300.profile_case bcd_train --batch 4 --seqlen 2048 \\
-        --dim 1536 [--calls 3]
+        --dim 1536 [--chunk-len 0] [--calls 3]
 
 The inputs are the seeded workload distributions of ``inputs`` (the scan's
 long-sequence recipe by default: delta log-uniform in [1e-4, 1e-2], gate, D = 1,
@@ -81,10 +81,12 @@ def run_bcd_train(args, torch):
     rng = np.random.default_rng(4)
     dout = _dev(torch, I.store(rng.standard_normal((spec.batch, spec.L, spec.dim)), "bf16"))
     plan = libssm.ssm_scan_plan(spec.batch, spec.L, spec.dim, 16, "bf16",
+                                chunk_len_hint=args.chunk_len,
                                 flags=libssm.SSM_FLAG_BC_PER_CHANNEL)
     print("plan", plan, flush=True)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    kw = dict(D=t["D"], z=t["z"], delta_bias=t["delta_bias"], delta_softplus=True)
+    kw = dict(D=t["D"], z=t["z"], delta_bias=t["delta_bias"], delta_softplus=True,
+              chunk_len_hint=args.chunk_len)
     for i in range(args.calls):
         ev[0].record()
         libssm.ssm_selective_scan_fwd(t["x"], t["delta"], t["A"], B4, C4, **kw)

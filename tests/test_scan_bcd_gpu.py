@@ -60,12 +60,13 @@ def test_bcd_matches_oracle(torch, io, hint):
     G.parity(G.host64(fs), rh, "state", "per-channel final state (%s, hint %d)" % (io, hint))
 
 
-@pytest.mark.parametrize("gate", [True, False])
-def test_bcd_plain_delta_and_h0(torch, gate):
-    spec = I.ScanSpec(1, 130, 136, io="f32", gate=gate, D_kind="none", seed=82)
+@pytest.mark.parametrize("gate,dim", [(True, 136), (False, 136), (True, 132)])
+def test_bcd_plain_delta_and_h0(torch, gate, dim):
+    """dim 132 (fp32) ends half-way through a warp's 8 channels."""
+    spec = I.ScanSpec(1, 130, dim, io="f32", gate=gate, D_kind="none", seed=82)
     inp = I.make_scan_inputs(spec)
     B4, C4 = I.make_bc_per_channel(spec)
-    h0 = np.random.default_rng(83).standard_normal((1, 136, 16)).astype(np.float32)
+    h0 = np.random.default_rng(83).standard_normal((1, dim, 16)).astype(np.float32)
     out, fs = _gpu(inp, B4, C4, False, 32, h0=h0)
     ry, rh = _ref(inp, B4, C4, False, h0=h0)
     G.parity(G.host64(out), ry, "f32", "per-channel y from h0 (gate %s)" % gate)
