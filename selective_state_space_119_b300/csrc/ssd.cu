@@ -19,10 +19,12 @@
 // This kernel runs one CTA per (batch row, head) over the chunks in order,
 // the state in fp32 registers. Per chunk TMA (cp.async.bulk.tensor, 128-byte
 // swizzle) brings the C, B and X tiles; one thread issues the tcgen05.mma
-// products into tensor memory; the CTA's 256 threads form M, w o X and the
+// products into tensor memory; the CTA's 512 threads form M, w o X and the
 // epilogue on the CUDA cores (a thread owns one row of every [Q x .]
-// accumulator, the row of its warp's TMEM lane quarter, and half of its
-// columns: warps w and w + 4 split them). The products are issued as soon as
+// accumulator, the row of its warp's TMEM lane quarter, and a quarter of its
+// columns: warps w, w + 4, w + 8 and w + 12 split them; 16 warps, so that
+// the CUDA-core phases, chains of dependent operations, keep the schedulers
+// busy). The products are issued as soon as
 // their operands are ready, so that the tensor cores work while the CUDA cores
 // do: G = C B^T and Y2 = C h^T as soon as the B and C tiles have landed (during
 // the cumulative sum of dt and w o X), S^T while M is formed; D x rides in M's
@@ -52,7 +54,9 @@ namespace {
 constexpr int kQ = 128;     // tokens per chunk
 constexpr int kP = 64;      // channels per head
 constexpr int kNs = 128;    // state width
-constexpr int kThreads = 256;   // warps w and w + 4 share TMEM lane quarter w mod 4
+constexpr int kThreads = 512;   // warps w, w + 4, w + 8, w + 12 share TMEM lane quarter w mod 4
+constexpr int kGroups = kThreads / 128;   // column groups: a thread owns 64 / kGroups columns
+constexpr int kGC = kP / kGroups;         // 16 columns of P per thread
 constexpr int kIssuer = 128;    // the thread that issues TMA loads and MMAs (warp 4, lane 0)
 constexpr uint32_t kPolls = 1u << 24;
 constexpr uint32_t kStatusTimeout = 7;
@@ -118,6 +122,23 @@ __device__ __forceinline__ void put8_split(unsigned char* hi, unsigned char* lo,
     const uint32_t off = tc::sw128(r, 8 * c);
     *reinterpret_cast<uint4*>(hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     *reinterpret_cast<uint4*>(lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes, waited for in the
+// same statement.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* tm, int c0, int c1, int c2,
@@ -186,20 +207,20 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     const uint32_t tmem = *tm_slot;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;   // this warp's TMEM lanes
 
-    // the state: thread (row n, group g) holds h[p][n] for p = 32 g .. 32 g + 31
+    // the state: thread (row n, group g) holds h[p][n] for p = 16 g .. 16 g + 15
     // (fp32) and writes it as rows n of the MN-major operand [n x p] of C h^T
-    float h[32];
+    float h[kGC];
     {
         const int n = row;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            h[i] = a.h0 ? a.h0[(((b * a.H + hd) * kP) + 32 * grp + i) * kNs + n] : 0.f;
+        for (int i = 0; i < kGC; ++i)
+            h[i] = a.h0 ? a.h0[(((b * a.H + hd) * kP) + kGC * grp + i) * kNs + n] : 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kGC / 8; ++k) {
             float v[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) v[i] = h[8 * k + i];
-            put8_split(sm + oHh, sm + oHl, n, 4 * grp + k, v);
+            put8_split(sm + oHh, sm + oHl, n, (kGC / 8) * grp + k, v);
         }
     }
     // the first chunk's C h^T reads these rows through the async proxy
@@ -242,18 +263,19 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                        : 0.f;
     };
     float dt_next = tid < kQ ? load_dt(0) : 0.f;
-    // this thread's part of x row `row` of chunk c (its group's 32 channels),
+    // this thread's part of x row `row` of chunk c (its group's 16 channels),
     // for w o X: loaded from global memory a chunk ahead, so that the X tile
     // is read by Y = M X alone and can be reloaded while the next chunk starts
-    auto load_xrow = [&](int c, uint4 (&xr)[4]) {
+    auto load_xrow = [&](int c, uint4 (&xr)[kGC / 8]) {
         const int64_t t = int64_t(c) * kQ + row;
         const uint4* src = reinterpret_cast<const uint4*>(
             static_cast<const __nv_bfloat16*>(a.x) + ((b * a.L + (t < a.L ? t : 0)) * a.H + hd) * kP +
-            32 * grp);
+            kGC * grp);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) xr[k] = t < a.L ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
+        for (int k = 0; k < kGC / 8; ++k)
+            xr[k] = t < a.L ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
     };
-    uint4 xrow[4];
+    uint4 xrow[kGC / 8];
     load_xrow(0, xrow);
 
     bool ok = true;
@@ -324,7 +346,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             const float w = ex2(s_end - ss2[u]) * sdt[u];
             const float2 w2 = make_float2(w, w);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < kGC / 8; ++k) {
                 const uint32_t wd[4] = {xrow[k].x, xrow[k].y, xrow[k].z, xrow[k].w};
                 float v[8];
 #pragma unroll
@@ -334,7 +356,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     v[2 * i] = p.x;
                     v[2 * i + 1] = p.y;
                 }
-                put8_split(sm + oWh, sm + oWl, u, 4 * grp + k, v);
+                put8_split(sm + oWh, sm + oWl, u, (kGC / 8) * grp + k, v);
             }
             load_xrow(c + 1, xrow);
         }
@@ -357,13 +379,20 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             }
             tc::mma_commit(bar_S);
             pend_S = static_cast<int>(ph);
+            // once S is done with the B tile, the next chunk's B can land (the
+            // issuer's warp has no M block of its own to form meanwhile)
+            ok = mbar_wait_bounded(bar_S, ph, kPolls);
+            if (ok) {
+                pend_S = -1;
+                if (c + 1 < nchunks) load_B(c + 1);
+            }
         }
         // M = G o decay o dt + D on the diagonal (so that M X carries D x), row
-        // t = this thread's row, high and remainder, while S computes. Warps w
-        // and w + 4 split the 32-column blocks q of rows 32 (w mod 4) ..: the
+        // t = this thread's row, high and remainder, while S computes. Warp w
+        // forms the 32-column block q = w / 4 of rows 32 (w mod 4) ..: the
         // blocks q > w mod 4 lie above the diagonal (zero), q < w mod 4 below it
         // (no mask).
-        ok = mbar_wait_bounded(bar_G, ph, kPolls);
+        ok = ok && mbar_wait_bounded(bar_G, ph, kPolls);
         tc::fence_after_sync();
         if (ok && issuer) {
             pend_G = -1;
@@ -372,9 +401,8 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         if (ok) {
             const int t = row;
             const float st = ss2[t];
-#pragma unroll
-            for (int qi = 0; qi < 2; ++qi) {
-                const int q = grp + 2 * qi;
+            {
+                const int q = grp;
                 const int ublk = q >> 1;          // which 64-wide u block
                 const int c0 = (q & 1) * 4;       // its first 16-byte chunk in the row
                 if (q > quarter) {
@@ -385,8 +413,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                         *reinterpret_cast<uint4*>(sm + oMh + ublk * kBlk + off) = zero;
                         *reinterpret_cast<uint4*>(sm + oMl + ublk * kBlk + off) = zero;
                     }
-                    continue;
-                }
+                } else {
                 float gv[32];
                 tc::tmem_ld32(tmem + lane_base + kColG + 32 * q, gv);
                 const float2 st2 = make_float2(st, st);
@@ -419,6 +446,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     }
                     put8_split(sm + oMh + ublk * kBlk, sm + oMl + ublk * kBlk, t, c0 + cc, v);
                 }
+                }
             }
         }
         fence_proxy_async_smem();
@@ -446,48 +474,42 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             }
             tc::mma_commit(bar_Y);
             pend_Y = static_cast<int>(ph);
-            // S (issued before M) is done with the B tile: the next chunk's B can land
-            ok = mbar_wait_bounded(bar_S, ph, kPolls);
-            if (ok) {
-                pend_S = -1;
-                if (c + 1 < nchunks) load_B(c + 1);
-            }
         }
         // epilogue once S and Y have landed: y = Y + exp(s_t) Y2 (row t, the
-        // group's 32 columns) into the staging tile (w o X is no longer read);
-        // state: h <- exp(s_end) h + S (row n, the group's 32 p)
-        ok = mbar_wait_bounded(bar_S, ph, kPolls) && mbar_wait_bounded(bar_Y, ph, kPolls);
+        // group's 16 columns) into the staging tile (w o X is no longer read);
+        // state: h <- exp(s_end) h + S (row n, the group's 16 p)
+        ok = ok && mbar_wait_bounded(bar_S, ph, kPolls) && mbar_wait_bounded(bar_Y, ph, kPolls);
         tc::fence_after_sync();
         if (ok && issuer) {
-            pend_Y = -1;
+            pend_S = pend_Y = -1;
             if (c + 1 < nchunks) load_X(c + 1);   // Y is done with the X tile
         }
         if (ok) {
             const int t = row;
             const float et = ex2(ss2[t]);
-            float yv[32], y2[32];
-            tc::tmem_ld32(tmem + lane_base + kColY + 32 * grp, yv);
-            tc::tmem_ld32(tmem + lane_base + kColY2 + 32 * grp, y2);
+            float yv[kGC], y2[kGC];
+            tmem_ld16(tmem + lane_base + kColY + kGC * grp, yv);
+            tmem_ld16(tmem + lane_base + kColY2 + kGC * grp, y2);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < kGC / 8; ++k) {
                 float o[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) o[i] = fmaf(et, y2[8 * k + i], yv[8 * k + i]);
-                *reinterpret_cast<uint4*>(sm + oWh + tc::sw128(t, 8 * (4 * grp + k))) =
+                *reinterpret_cast<uint4*>(sm + oWh + tc::sw128(t, 8 * ((kGC / 8) * grp + k))) =
                     make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
                                pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
             }
             const float eend = ex2(s_end);
-            float sv[32];
-            tc::tmem_ld32(tmem + lane_base + kColS + 32 * grp, sv);
+            float sv[kGC];
+            tmem_ld16(tmem + lane_base + kColS + kGC * grp, sv);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] = fmaf(eend, h[i], sv[i]);
+            for (int i = 0; i < kGC; ++i) h[i] = fmaf(eend, h[i], sv[i]);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < kGC / 8; ++k) {
                 float v[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) v[i] = h[8 * k + i];
-                put8_split(sm + oHh, sm + oHl, row, 4 * grp + k, v);
+                put8_split(sm + oHh, sm + oHl, row, (kGC / 8) * grp + k, v);
             }
         }
         fence_proxy_async_smem();
@@ -516,8 +538,8 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     } else if (a.final_state) {
         const int n = row;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            a.final_state[(((b * a.H + hd) * kP) + 32 * grp + i) * kNs + n] = h[i];
+        for (int i = 0; i < kGC; ++i)
+            a.final_state[(((b * a.H + hd) * kP) + kGC * grp + i) * kNs + n] = h[i];
     }
     tc::fence_before_sync();
     __syncthreads();
