@@ -6,6 +6,8 @@
         [--heads 8] [--groups 1] [--calls 3]
     python -m selective_state_space_119_b300.profile_case bcd_train --batch 4 --seqlen 2048 \\
         --dim 1536 [--chunk-len 0] [--calls 3]
+    python -m selective_state_space_119_b300.profile_case conv --batch 4 --seqlen 2048 \\
+        --dim 1536 [--calls 3]
 
 The inputs are the seeded workload distributions of ``inputs`` (the scan's
 long-sequence recipe by default: delta log-uniform in [1e-4, 1e-2], gate, D = 1,
@@ -101,9 +103,31 @@ def run_bcd_train(args, torch):
           flush=True)
 
 
+def run_conv(args, torch):
+    """The input stage (causal conv1d of width 4 + SiLU) and its backward, each
+    call one forward and one backward (du ~ N(0, 1)), bf16."""
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+    rng = np.random.default_rng(6)
+    x = _dev(torch, I.store(rng.standard_normal((args.batch, args.seqlen, args.dim)), "bf16"))
+    du = _dev(torch, I.store(rng.standard_normal((args.batch, args.seqlen, args.dim)), "bf16"))
+    w = _dev(torch, (rng.standard_normal((args.dim, 4)) * 0.5).astype(np.float32))
+    bias = _dev(torch, (rng.standard_normal(args.dim) * 0.1).astype(np.float32))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for i in range(args.calls):
+        ev[0].record()
+        libssm.ssm_causal_conv1d_silu(x, w, bias)
+        ev[1].record()
+        libssm.ssm_causal_conv1d_silu_bwd(x, w, du, conv_b=bias)
+        ev[2].record()
+    torch.cuda.synchronize()
+    print("last call: fwd %.3f ms, bwd %.3f ms (allocations included)"
+          % (ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("kernel", choices=["scan", "ssd", "bcd_train"])
+    ap.add_argument("kernel", choices=["scan", "ssd", "bcd_train", "conv"])
     ap.add_argument("--batch", type=int, required=True)
     ap.add_argument("--seqlen", type=int, required=True)
     ap.add_argument("--dim", type=int, default=5120)
@@ -117,7 +141,8 @@ def main(argv=None):
     import torch
     if not torch.cuda.is_available():
         sys.exit("no CUDA device")
-    {"scan": run_scan, "ssd": run_ssd, "bcd_train": run_bcd_train}[args.kernel](args, torch)
+    {"scan": run_scan, "ssd": run_ssd, "bcd_train": run_bcd_train,
+     "conv": run_conv}[args.kernel](args, torch)
 
 
 if __name__ == "__main__":
