@@ -19,7 +19,6 @@
 // token block) in a fixed order, so the sums do not depend on scheduling.
 #include <cuda_bf16.h>
 
-#include <algorithm>
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -170,13 +169,32 @@ __global__ void __launch_bounds__(kThreads, 3) conv1d_silu_bwd_kernel(const Conv
     }
 }
 
-// dw[d][k] and dbias[d]: the shares of every (batch row, token block) in order.
-__global__ void conv1d_bwd_reduce_kernel(const ConvBwdArgs a, int64_t nblocks, int K) {
+// dw[d][k] and dbias[d]: the shares of every (batch row, token block). A CTA
+// owns 32 outputs; its 8 warps sum the rows q = w, w + 8, w + 16, ... of each
+// (4 running sums each, added in order), and warp 0 adds the 8 slices in
+// order: a fixed order, so the result does not depend on scheduling.
+__global__ void __launch_bounds__(256) conv1d_bwd_reduce_kernel(const ConvBwdArgs a,
+                                                                 int64_t nblocks, int K) {
+    constexpr int kSlices = 8;
+    __shared__ float s_slice[kSlices][32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t n = a.dim * (K + 1);
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
-         i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (i < n) {
+        int64_t q = w;
+        for (; q + 3 * kSlices < nblocks; q += 4 * kSlices) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[j] += a.part[(q + j * kSlices) * n + i];
+        }
+        for (int j = 0; q < nblocks; q += kSlices, ++j) acc[j] += a.part[q * n + i];
+    }
+    s_slice[w][lane] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    __syncthreads();
+    if (w == 0 && i < n) {
         float s = 0.f;
-        for (int64_t q = 0; q < nblocks; ++q) s += a.part[q * n + i];
+#pragma unroll
+        for (int r = 0; r < kSlices; ++r) s += s_slice[r][lane];
         const int64_t d = i / (K + 1), k = i % (K + 1);
         if (k < K)
             a.dw[d * K + k] = s;
@@ -194,7 +212,8 @@ cudaError_t launch_bwd_k(const ConvBwdArgs& a, cudaStream_t s) {
     if (blocks >= (int64_t(1) << 31)) return cudaErrorInvalidConfiguration;
     conv1d_silu_bwd_kernel<T, K><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(a);
     const int64_t n = a.dim * (K + 1);
-    const int64_t rblocks = std::min<int64_t>((n + 255) / 256, 4096);
+    const int64_t rblocks = (n + 31) / 32;
+    if (rblocks >= (int64_t(1) << 31)) return cudaErrorInvalidConfiguration;
     conv1d_bwd_reduce_kernel<<<static_cast<unsigned>(rblocks), 256, 0, s>>>(a, a.batch * RB, K);
     return cudaGetLastError();
 }

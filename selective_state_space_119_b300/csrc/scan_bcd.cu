@@ -27,12 +27,12 @@ namespace ssm {
 namespace {
 
 constexpr int kBcdThreads = 128;    // = the 128-channel tile of configuration 0
-// tokens of loads in flight per lane: the chunk-state pass reads no C (half
-// the bytes per token), so it keeps twice as many tokens in flight; fp32 rows
-// are twice as wide as bf16 ones
+// tokens of loads in flight per lane: the chunk-state and checkpoint passes
+// read no C (half the bytes per token), so they keep twice as many tokens in
+// flight; fp32 rows are twice as wide as bf16 ones
 template <typename T, int MODE>
 struct RingTokens {
-    static constexpr int value = (sizeof(T) == 2 ? 4 : 2) * (MODE == 0 ? 2 : 1);
+    static constexpr int value = (sizeof(T) == 2 ? 4 : 2) * (MODE == 1 ? 1 : 2);
 };
 
 template <typename T, int N>
@@ -90,10 +90,14 @@ struct Slot {
 };
 
 // MODE 1: the output pass (composes the chunk carries, writes y and the final
-// state; with CKPT also the state before every kCkptTokens-th token, for the
-// backward); MODE 0: the chunk-state pass (end state from 0 and sum of dt of
-// every chunk but the last). One lane = one channel.
-template <typename T, int N, int MODE, bool SOFTPLUS, bool GATE, bool CKPT = false>
+// state); MODE 0: the chunk-state pass (end state from 0 and sum of dt of
+// every chunk but the last); MODE 2: the checkpoint pass of the training
+// forward (composes the carries like the output pass, reads what the
+// chunk-state pass reads, and saves the state before every kCkptTokens-th
+// token for the backward). Saving the states from the output pass itself ran
+// 2.4 times slower than the plain output pass; this pass costs one more read of
+// x, delta and B instead. One lane = one channel.
+template <typename T, int N, int MODE, bool SOFTPLUS, bool GATE>
 __global__ void __launch_bounds__(kBcdThreads) scan_bcd_kernel(const ScanArgs a) {
     constexpr bool WITH_C = MODE == 1, WITH_Z = MODE == 1 && GATE;
     using S = Slot<T, N, WITH_C, WITH_Z>;
@@ -114,7 +118,7 @@ __global__ void __launch_bounds__(kBcdThreads) scan_bcd_kernel(const ScanArgs a)
         A2[q] = ch_ok ? __ldg(a.A + dsafe * N + q) * kLog2e : 0.f;
         h[q] = 0.f;
     }
-    if (MODE == 1 && ch_ok) {
+    if (MODE != 0 && ch_ok) {
         if (a.h0) {
 #pragma unroll
             for (int q = 0; q < N; ++q) h[q] = a.h0[(b * a.dim + d) * N + q];
@@ -160,7 +164,7 @@ __global__ void __launch_bounds__(kBcdThreads) scan_bcd_kernel(const ScanArgs a)
             const S cur = ring[u];
             load(ring[u], t + kRing);   // the loads of a later token, in flight meanwhile
             const bool valid = ch_ok && t < t_end;
-            if constexpr (CKPT) {
+            if constexpr (MODE == 2) {
                 if (valid && t % kCkptTokens == 0) {
                     float4* ck = reinterpret_cast<float4*>(
                         a.ckpt + ((b * a.nckpt + t / kCkptTokens) * a.dim + d) * N);
@@ -189,7 +193,7 @@ __global__ void __launch_bounds__(kBcdThreads) scan_bcd_kernel(const ScanArgs a)
                 float y = fmaf(Dd, xv, acc.x + acc.y);
                 if constexpr (GATE) y *= silu(__uint_as_float(cur.z));
                 if (valid) IO<T>::st(og + t * a.dim, y);
-            } else {
+            } else if constexpr (MODE == 0) {
                 dt_sum += dt;
             }
         }
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__(kBcdThreads) scan_bcd_kernel(const ScanArgs a)
 #pragma unroll
             for (int q = 0; q < N; ++q) a.final_state[(b * a.dim + d) * N + q] = h[q];
         }
-    } else {
+    } else if constexpr (MODE == 0) {
         const int64_t idx = (b * (a.nchunks - 1) + k) * a.dim + d;
 #pragma unroll
         for (int q = 0; q < N; ++q) a.ws_H[idx * N + q] = h[q];
@@ -216,11 +220,10 @@ cudaError_t launch_flags(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     if (p.nchunks > 1)
         scan_bcd_kernel<T, N, 0, SOFTPLUS, false>
             <<<static_cast<unsigned>(per_chunk * (p.nchunks - 1)), kBcdThreads, 0, s>>>(a);
+    scan_bcd_kernel<T, N, 1, SOFTPLUS, GATE>
+        <<<static_cast<unsigned>(per_chunk * p.nchunks), kBcdThreads, 0, s>>>(a);
     if (a.ckpt)
-        scan_bcd_kernel<T, N, 1, SOFTPLUS, GATE, true>
-            <<<static_cast<unsigned>(per_chunk * p.nchunks), kBcdThreads, 0, s>>>(a);
-    else
-        scan_bcd_kernel<T, N, 1, SOFTPLUS, GATE>
+        scan_bcd_kernel<T, N, 2, SOFTPLUS, false>
             <<<static_cast<unsigned>(per_chunk * p.nchunks), kBcdThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
