@@ -278,9 +278,12 @@ int ssm_selective_scan_fwd_ckpt(const void* x, const void* delta, const float* A
  * Every gradient is written, not accumulated. Outputs must not overlap inputs,
  * each other or the workspace (SSM_ERR_ALIAS). dims->workspace must hold
  * ssm_scan_bwd_workspace_bytes(dims) bytes (no initial contents needed). The
- * sums over channels, rows and chunks are added in a fixed order: results do
- * not depend on scheduling. seqlen == 0 zeroes dA, dD, ddelta_bias and copies
- * dfinal_state (or zero) to dh0.
+ * backward splits the sequence into L-chunks of its own (enough to fill the
+ * device in one wave; dims->chunk_len_hint, when given, sets them as for the
+ * forward); the checkpoints do not depend on the forward's chunks. The sums
+ * over channels, rows and chunks are added in a fixed order: results do not
+ * depend on scheduling (for a given chunk plan). seqlen == 0 zeroes dA, dD,
+ * ddelta_bias and copies dfinal_state (or zero) to dh0.
  */
 size_t ssm_scan_bwd_workspace_bytes(const ssm_dims* dims);
 int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A, const void* B,

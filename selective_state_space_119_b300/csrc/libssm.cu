@@ -85,7 +85,18 @@ int choose_tile_cfg(int64_t N, int32_t hint) {
     return 0;
 }
 
-int make_plan(const ssm_dims* d, ssm::ScanPlan* p) {
+// purpose: the forward (kPlanFwd) or the backward (kPlanBwd), whose chunk count
+// follows its own rule (below).
+constexpr int kPlanFwd = 0, kPlanBwd = 1;
+// The backward's gradient pass holds three CTAs per SM, and a chunk more costs
+// it little (its reverse-carry pass covers every chunk but the first whatever
+// their number, and composing one more carry is 16 FMAs per channel), so its
+// plan takes as many chunks as fill those slots in one wave (a chunk at least
+// 64 tokens).
+constexpr int64_t kBwdResidentCtas = 3;
+constexpr int64_t kMinBwdChunk = 64;
+
+int make_plan(const ssm_dims* d, ssm::ScanPlan* p, int purpose = kPlanFwd) {
     *p = ssm::ScanPlan{};
     const int64_t batch = d->batch, L = d->seqlen, dim = d->dim, N = d->dstate;
     const int64_t TS = ssm::kScanStageTokens;
@@ -98,6 +109,10 @@ int make_plan(const ssm_dims* d, ssm::ScanPlan* p) {
     int64_t chunk;
     if (d->chunk_len_hint > 0) {
         chunk = d->chunk_len_hint;
+    } else if (purpose == kPlanBwd) {
+        const int64_t k = std::max<int64_t>(
+            1, std::min<int64_t>(kBwdResidentCtas * sms / per_chunk, L / kMinBwdChunk));
+        chunk = (L + k - 1) / k;
     } else if (d->flags & SSM_FLAG_BC_PER_CHANNEL) {
         // per-channel B, C are bound by HBM: split the sequence until about 2.5
         // output CTAs per SM keep enough loads in flight (measured best for
@@ -122,9 +137,12 @@ int make_plan(const ssm_dims* d, ssm::ScanPlan* p) {
             }
         }
     }
-    // whole pipeline stages per chunk, so that only the sequence end is ragged
-    chunk = std::max<int64_t>(TS, (chunk + TS - 1) / TS * TS);
-    chunk = std::min(chunk, (L + TS - 1) / TS * TS);
+    // whole pipeline stages per chunk, so that only the sequence end is ragged;
+    // the backward's chunks need only start on a checkpoint (its blocks are
+    // counted per chunk)
+    const int64_t gran = purpose == kPlanBwd ? ssm::kCkptTokens : TS;
+    chunk = std::max<int64_t>(gran, (chunk + gran - 1) / gran * gran);
+    chunk = std::min(chunk, (L + gran - 1) / gran * gran);
     p->chunk_len = chunk;
     p->nchunks = (L + chunk - 1) / chunk;
     p->ctas = per_chunk * p->nchunks;
@@ -435,7 +453,7 @@ size_t ssm_scan_bwd_workspace_bytes(const ssm_dims* dims) {
     if (check_dims(dims, true) != SSM_OK) return 0;
     if (dims->dstate != 16 || dims->tile_config_hint > 1) return 0;
     ssm::ScanPlan p;
-    if (make_plan(dims, &p) != SSM_OK || p.nchunks == 0) return 0;
+    if (make_plan(dims, &p, kPlanBwd) != SSM_OK || p.nchunks == 0) return 0;
     return bwd_layout(dims, p).bytes;
 }
 
@@ -486,7 +504,7 @@ int ssm_selective_scan_bwd(const void* x, const void* delta, const float* A, con
         if (rc != SSM_OK) return rc;
     }
     ssm::ScanPlan p;
-    rc = make_plan(dims, &p);
+    rc = make_plan(dims, &p, kPlanBwd);
     if (rc != SSM_OK) return rc;
     const BwdLayout lay = bwd_layout(dims, p);
     if (!dims->workspace || dims->workspace_bytes < lay.bytes) return SSM_ERR_WORKSPACE;

@@ -24,8 +24,12 @@
 //
 // The states come from a checkpointing forward (the state before every 8th
 // token, fp32). Per 8-token block, in reverse order, a CTA reloads the block's
-// first state, recomputes the block's 8 states forward into shared memory,
-// then runs the reverse sweep over them. The sequence is split into the same
+// first state, recomputes the block's 8 states forward and keeps those after
+// its even tokens in shared memory, then runs the reverse sweep over odd / even
+// pairs of tokens: an odd token's state is one step of the recurrence from the
+// even one before it (h_t = e^{dt A} h_{t-1} + dt x B, the e^{dt A} that the
+// sweep forms anyway), which halves the shared memory of the states and lets
+// three CTAs share an SM. The sequence is split into the same
 // L-chunks as the forward: a first pass computes, for every chunk but the
 // first, its reverse carry from zero (Q at its first token) and its sum of dt;
 // each chunk of the gradient pass composes the carries of the chunks to its
@@ -73,8 +77,8 @@ struct BwdSmem {
     static constexpr int IN_BYTES = (IN_ELEMS * int(sizeof(T)) + 127) & ~127;
     static constexpr int oIn = 0;
     static constexpr int oBC = 2 * IN_BYTES;                               // fp32 [TB][2N]
-    static constexpr int oHist = oBC + TB * 2 * N * 4;                    // float4 [TB][N/4][128]
-    static constexpr int oRed = oHist + (GRAD ? TB * (N / 4) * kBwdThreads * 16 : 0);  // fp32 [4][TB][32]
+    static constexpr int oHist = oBC + TB * 2 * N * 4;                    // float4 [TB/2][N/4][128]
+    static constexpr int oRed = oHist + (GRAD ? TB / 2 * (N / 4) * kBwdThreads * 16 : 0);  // fp32 [4][TB][32]
     static constexpr int oDt = oRed + (GRAD ? kBwdWarps * TB * 32 * 4 : 0);  // float2 [TB][128]
     static constexpr int oY = oDt + (GRAD ? TB * kBwdThreads * 8 : 0);        // fp32 [TB][128]
     static constexpr int kBytes = oY + (GRAD ? TB * kBwdThreads * 4 : 0);
@@ -171,7 +175,7 @@ __device__ __forceinline__ void stage_block(const BwdArgs& a, T* in, int64_t b, 
 // MODE 0: reverse carry of chunks 1 .. nchunks-1 from zero (Q at the chunk's
 // first token, and its sum of dt). MODE 1: the gradients of one chunk.
 template <typename T, int N, bool SOFTPLUS, bool GATE, int MODE, bool ZOH = false>
-__global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(const BwdArgs a) {
     constexpr int TB = MODE == 1 ? kGradTokens : kCarryTokens;
     using Sm = BwdSmem<T, N, TB, MODE == 1>;
     constexpr int NS = 2, SPL = N / NS;
@@ -327,11 +331,15 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
                     }
                     yp[r] = y2.x + y2.y;
                 }
+                // the states after the even tokens (the sweep forms the odd ones
+                // from them with one step of the recurrence)
+                if ((tt & 1) == 0) {
 #pragma unroll
-                for (int c4 = 0; c4 < N / 4; ++c4) {
-                    const int r = c4 / (SPL / 4), q = (c4 % (SPL / 4)) * 4;
-                    hist[(tt * (N / 4) + c4) * kBwdThreads + tid] =
-                        make_float4(h[r][q], h[r][q + 1], h[r][q + 2], h[r][q + 3]);
+                    for (int c4 = 0; c4 < N / 4; ++c4) {
+                        const int r = c4 / (SPL / 4), q = (c4 % (SPL / 4)) * 4;
+                        hist[((tt >> 1) * (N / 4) + c4) * kBwdThreads + tid] =
+                            make_float4(h[r][q], h[r][q + 1], h[r][q + 2], h[r][q + 3]);
+                    }
                 }
                 // the partner's slot 1 is this lane's channel
                 ys[tt * kBwdThreads + tid] =
@@ -339,9 +347,8 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
             }
         }
 
-        // ---- reverse sweep over the block ----
-#pragma unroll (MODE == 1 ? 2 : 4)
-        for (int tt = TB - 1; tt >= 0; --tt) {
+        // ---- reverse sweep over the block, tokens in odd / even pairs ----
+        auto sweep_token = [&](const int tt, const bool odd) {
             const float* Bt = bcs + tt * 2 * N + j * SPL;
             const float* Ct = Bt + N;
             const float2 gp = lds_pair(in + Sm::kDout + tt * kBwdChannels + pc);
@@ -390,7 +397,8 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
 #pragma unroll
                 for (int c4 = 0; c4 < N / 4; ++c4) {
                     const int r = c4 / (SPL / 4), q = (c4 % (SPL / 4)) * 4;
-                    const float4 v = hist[(tt * (N / 4) + c4) * kBwdThreads + tid];
+                    // the state after token tt (even tt) or after tt - 1 (odd tt)
+                    const float4 v = hist[((tt >> 1) * (N / 4) + c4) * kBwdThreads + tid];
                     hreg[r][q] = v.x; hreg[r][q + 1] = v.y; hreg[r][q + 2] = v.z; hreg[r][q + 3] = v.w;
                 }
                 float dxs[NS], saw[NS], sbe[NS], vals[2 * SPL];
@@ -406,7 +414,14 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
                             const float e = ex2(dt[r] * A2[r][q]);
                             const float m = zoh_m(dt[r], z, e, invA[r][q]);
                             const float xB = xv[r] * Bt[q];
-                            const float wv = fmaf(-xB, m, hreg[r][q]);          // a h_{t-1}
+                            float hq, wv;                                       // h_t, a h_{t-1}
+                            if (odd) {
+                                wv = e * hreg[r][q];
+                                hq = fmaf(xB, m, wv);
+                            } else {
+                                hq = hreg[r][q];
+                                wv = fmaf(-xB, m, hq);
+                            }
                             const float g = fmaf(dy[r], Ct[q], Q[r][q]);        // dLoss/dh_t
                             dx1 = fmaf(g * Bt[q], m, dx1);
                             sa1 = fmaf(g * wv, A2[r][q], sa1);
@@ -414,7 +429,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
                             dA[r][q] = fmaf(g, fmaf(wv, dt[r], xB * dt[r] * dt[r] * phi_prime(z, e)),
                                             dA[r][q]);
                             vals[q] = fmaf(g, xv[r] * m, vals[q]);                // dB
-                            vals[SPL + q] = fmaf(dy[r], hreg[r][q], vals[SPL + q]);  // dC
+                            vals[SPL + q] = fmaf(dy[r], hq, vals[SPL + q]);  // dC
                             Q[r][q] = e * g;
                         }
                         dxs[r] = dx1;
@@ -431,10 +446,17 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
 #pragma unroll
                     for (int q = 0; q < SPL; q += 2) {
                         const float2 B2 = make_float2(Bt[q], Bt[q + 1]);
-                        const float2 h2 = make_float2(hreg[r][q], hreg[r][q + 1]);
                         const float2 A22 = make_float2(A2[r][q], A2[r][q + 1]);
                         const float2 arg = __fmul2_rn(dt2, A22);
-                        const float2 wv = __ffma2_rn(ndtx2, B2, h2);              // a * h_{t-1}
+                        const float2 e2 = make_float2(ex2(arg.x), ex2(arg.y));
+                        float2 h2, wv;                                            // h_t, a * h_{t-1}
+                        if (odd) {
+                            wv = __fmul2_rn(e2, make_float2(hreg[r][q], hreg[r][q + 1]));
+                            h2 = __ffma2_rn(dtx2, B2, wv);
+                        } else {
+                            h2 = make_float2(hreg[r][q], hreg[r][q + 1]);
+                            wv = __ffma2_rn(ndtx2, B2, h2);
+                        }
                         const float2 g = __ffma2_rn(dy2, make_float2(Ct[q], Ct[q + 1]),
                                                     make_float2(Q[r][q], Q[r][q + 1]));  // dLoss/dh_t
                         dxs2 = __ffma2_rn(g, B2, dxs2);
@@ -449,7 +471,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
                         const float2 vc = __ffma2_rn(dy2, h2, make_float2(vals[SPL + q], vals[SPL + q + 1]));
                         vals[SPL + q] = vc.x;                                     // dC
                         vals[SPL + q + 1] = vc.y;
-                        const float2 qn = __fmul2_rn(make_float2(ex2(arg.x), ex2(arg.y)), g);
+                        const float2 qn = __fmul2_rn(e2, g);
                         Q[r][q] = qn.x;
                         Q[r][q + 1] = qn.y;
                     }
@@ -494,6 +516,11 @@ __global__ void __launch_bounds__(kBwdThreads, 2) scan_bwd_kernel(const BwdArgs 
                 }
                 red[(w * TB + tt) * 32 + lane] = vals[0];
             }
+                };
+#pragma unroll (MODE == 1 ? 1 : 2)
+        for (int tp = TB / 2 - 1; tp >= 0; --tp) {
+            sweep_token(2 * tp + 1, true);
+            sweep_token(2 * tp, false);
         }
         if constexpr (MODE == 1) {
             __syncthreads();

@@ -157,8 +157,10 @@ def test_checkpoints_are_prefix_states(torch, hint):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("hint", [0, 64, 96])
+@pytest.mark.parametrize("hint", [0, 40, 64, 96])
 def test_gradients_softplus_gate(torch, io, hint):
+    """hint 40: the forward's chunks are 64 tokens, the backward's 40 (its chunks
+    need only start on a checkpoint)."""
     spec = I.ScanSpec(2, 300, 264, io=io, delta_kind="softplus_bias", A_kind="lognormal",
                       D_kind="uniform", seed=63)
     inp, dout, h0, dfin = _case(spec, 64, with_h0=True, with_dfinal=True)
