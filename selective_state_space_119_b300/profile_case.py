@@ -8,6 +8,8 @@
         --dim 1536 [--chunk-len 0] [--calls 3]
     python -m selective_state_space_119_b300.profile_case conv --batch 4 --seqlen 2048 \\
         --dim 1536 [--calls 3]
+    python -m selective_state_space_119_b300.profile_case train --batch 4 --seqlen 2048 \\
+        --dim 1536 [--A s4d|lognormal] [--calls 3]
 
 The inputs are the seeded workload distributions of ``inputs`` (the scan's
 long-sequence recipe by default: delta log-uniform in [1e-4, 1e-2], gate, D = 1,
@@ -103,6 +105,31 @@ def run_bcd_train(args, torch):
           flush=True)
 
 
+def run_train(args, torch):
+    """Training through the scan with shared B, C on the softplus recipe: each
+    call is one checkpointing forward and one backward (dout ~ N(0, 1))."""
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+    spec = I.ScanSpec(args.batch, args.seqlen, args.dim, io="bf16", delta_kind="softplus_bias",
+                      A_kind=args.A, D_kind="uniform", seed=3)
+    t = {k: _dev(torch, v) for k, v in I.make_scan_inputs(spec).items()}
+    rng = np.random.default_rng(4)
+    dout = _dev(torch, I.store(rng.standard_normal((spec.batch, spec.L, spec.dim)), "bf16"))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    kw = dict(D=t["D"], z=t["z"], delta_bias=t["delta_bias"], delta_softplus=True,
+              chunk_len_hint=args.chunk_len)
+    for i in range(args.calls):
+        ev[0].record()
+        _, _, ck = libssm.ssm_selective_scan_fwd_ckpt(t["x"], t["delta"], t["A"], t["B"], t["C"],
+                                                      **kw)
+        ev[1].record()
+        libssm.ssm_selective_scan_bwd(t["x"], t["delta"], t["A"], t["B"], t["C"], ck, dout, **kw)
+        ev[2].record()
+    torch.cuda.synchronize()
+    print("last call: fwd_ckpt %.3f ms, bwd %.3f ms (allocations included)"
+          % (ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])), flush=True)
+
+
 def run_conv(args, torch):
     """The input stage (causal conv1d of width 4 + SiLU) and its backward, each
     call one forward and one backward (du ~ N(0, 1)), bf16."""
@@ -127,7 +154,7 @@ def run_conv(args, torch):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("kernel", choices=["scan", "ssd", "bcd_train", "conv"])
+    ap.add_argument("kernel", choices=["scan", "ssd", "bcd_train", "conv", "train"])
     ap.add_argument("--batch", type=int, required=True)
     ap.add_argument("--seqlen", type=int, required=True)
     ap.add_argument("--dim", type=int, default=5120)
@@ -142,7 +169,7 @@ def main(argv=None):
     if not torch.cuda.is_available():
         sys.exit("no CUDA device")
     {"scan": run_scan, "ssd": run_ssd, "bcd_train": run_bcd_train,
-     "conv": run_conv}[args.kernel](args, torch)
+     "conv": run_conv, "train": run_train}[args.kernel](args, torch)
 
 
 if __name__ == "__main__":
