@@ -33,8 +33,8 @@
 // in M's diagonal, so the X tile is read by Y alone; M goes to tensor memory
 // (tcgen05.st) and is the A operand of Y = M X from there, which leaves the
 // shared memory for two buffers of B and C tiles: each chunk requests the next
-// chunk's as soon as its own have landed. y is staged in the w o X tile for
-// its TMA store. Operands that the CUDA cores produce (M, w o X and h) are
+// chunk's as soon as its own have landed. y is staged in a tile of its own
+// for its TMA store (which has a chunk's time to read it). Operands that the CUDA cores produce (M, w o X and h) are
 // split into a bf16 high part and a bf16 remainder, two products each, so that
 // every product carries about 16 significant bits more than one bf16 rounding
 // would.
@@ -72,11 +72,12 @@ constexpr int kBlk = kQ * 128;                 // one [128 rows x 64] bf16 block
 constexpr int oC = 0;                          // C tiles of two chunks: rows t, K = n (2 blocks each)
 constexpr int oB = oC + 4 * kBlk;              // B tiles of two chunks: rows u, n (2 blocks each)
 constexpr int oX = oB + 4 * kBlk;              // X tile: rows u, p (1 block)
-constexpr int oWh = oX + kBlk;                 // w o X high: rows u, p; y staged here
+constexpr int oWh = oX + kBlk;                 // w o X high: rows u, p
 constexpr int oWl = oWh + kBlk;
 constexpr int oHh = oWl + kBlk;                // h high: rows n, p
 constexpr int oHl = oHh + kBlk;
-constexpr int oDt = oHl + kBlk;                // dt [Q] f32
+constexpr int oYs = oHl + kBlk;                // y staged for its TMA store: rows t, p
+constexpr int oDt = oYs + kBlk;                // dt [Q] f32
 constexpr int oS2 = oDt + kQ * 4;              // s log2 e [Q] f32
 constexpr int oWs = oS2 + kQ * 4;              // warp partial sums [4] f32
 constexpr int oBar = oWs + 64;                 // 13 mbarriers (loads, products, hand-overs)
@@ -219,7 +220,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     uint64_t* rdy_W = bar_B + 9;   // w o X written
     uint64_t* rdy_M = bar_B + 10;  // M stored to tensor memory
     uint64_t* rdy_E = bar_B + 11;  // epilogue done: y staged, h written, accumulators read
-    uint64_t* free_W = bar_B + 12; // the y store has read the staging tile
+    uint64_t* free_Y = bar_B + 12; // the y store has read the staging tile
     uint32_t* tm_slot = reinterpret_cast<uint32_t*>(sm + oTm);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -238,7 +239,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     if (producer && lane == 0) {
         for (int i = 0; i < 9; ++i) mbar_init(bar_B + i, 1);
         for (int i = 9; i < 12; ++i) mbar_init(bar_B + i, kComputeWarps);
-        mbar_init(free_W, 1);
+        mbar_init(free_Y, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -375,11 +376,11 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 // back once the store has read it
                 ok = mbar_wait_bounded(rdy_E, ph ^ 1u, kPolls);
                 if (!ok) break;
-                tma_store_4d(&tm_y, 0, hh, c * kQ, bb, sm + oWh);
+                tma_store_4d(&tm_y, 0, hh, c * kQ, bb, sm + oYs);
                 bulk_commit();
                 stored = true;
                 bulk_wait_read<0>();
-                mbar_arrive(free_W);
+                mbar_arrive(free_Y);
             }
             if (stored) bulk_wait_all();
             if (!ok) {
@@ -477,8 +478,6 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 ss2[dtok] = cs * A2;   // s_t log2 e
             }
             // (the next write of swarp is a chunk later, after several barriers)
-            // the previous chunk's y store has read its staging tile
-            ok = c == 0 || mbar_wait_bounded(free_W, ph ^ 1u, kPolls);
             if (named_bar_or(1, kCompute, !ok)) {
                 ok = false;
                 break;
@@ -577,7 +576,9 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             // epilogue once S and Y (and Y2) have landed: y = Y + exp(s_t) Y2 (row
             // t, the group's 16 columns) into the staging tile; state: h <-
             // exp(s_end) h + S (row n, the group's 16 p)
-            ok = ok && mbar_wait_bounded(bar_S, ph, kPolls) && mbar_wait_bounded(bar_Y, ph, kPolls);
+            // (and once the previous chunk's y store has read the staging tile)
+            ok = ok && mbar_wait_bounded(bar_S, ph, kPolls) && mbar_wait_bounded(bar_Y, ph, kPolls) &&
+                 (c == 0 || mbar_wait_bounded(free_Y, ph ^ 1u, kPolls));
             ok = __all_sync(0xffffffffu, ok);
             tc::fence_after_sync();
             if (ok) {
@@ -591,7 +592,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     float o[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) o[i] = fmaf(et, y2[8 * k + i], yv[8 * k + i]);
-                    *reinterpret_cast<uint4*>(sm + oWh + tc::sw128(t, 8 * ((kGC / 8) * grp + k))) =
+                    *reinterpret_cast<uint4*>(sm + oYs + tc::sw128(t, 8 * ((kGC / 8) * grp + k))) =
                         make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
                                    pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
                 }
