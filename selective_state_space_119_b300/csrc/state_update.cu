@@ -17,11 +17,11 @@
 // (one 128-bit load and store), so a warp reads and writes 512 contiguous
 // bytes of state per instruction; the state is streamed (read once, written
 // once) with evict-first cache hints. A CTA covers CH_PER_CTA channels of
-// kItems consecutive batch rows (the grid's y index); each lane group handles
-// its channel in all kItems rows, so A, the bias and D are loaded once for
-// them (every row reads the same [dim, N] A), with all loads issued before any
-// arithmetic, to keep enough bytes in flight per SM. The partial C . h sums
-// meet through butterfly shuffles; lane 0 of each group writes y.
+// kItems consecutive batch rows (the grid's y index; one row measured fastest,
+// below); each lane group handles its channel in all kItems rows, so A, the
+// bias and D are loaded once for them, with all loads issued before any
+// arithmetic. The partial C . h sums meet through butterfly shuffles; lane 0 of
+// each group writes y.
 #include <cuda_bf16.h>
 
 #include "ssm_device.cuh"
@@ -31,7 +31,10 @@ namespace ssm {
 namespace {
 
 constexpr int kStepThreads = 256;
-constexpr int kItems = 2;
+// batch rows per lane group (a sweep on b256 d5120 bf16: 1 row 32.8 us, 2 rows
+// 34.8, 4 rows 40.1, 8 rows 61.6: more, smaller CTAs keep more loads in flight
+// than more rows per thread)
+constexpr int kItems = 1;
 
 // NPL consecutive I/O elements widened to fp32 (NPL <= 4; 8-byte aligned for
 // bf16 x 4 and 16-byte aligned for fp32 x 4).
@@ -63,8 +66,9 @@ __device__ __forceinline__ float zoh_m(float dt, float A, float dA) {
     return fabsf(zz) < 0.1f ? dt * p : (dA - 1.f) / A;
 }
 
-template <typename T, int N, bool ZOH, bool BCD>
+template <typename T, int N, bool ZOH, bool BCD, int ITEMS = kItems>
 __global__ void __launch_bounds__(kStepThreads) state_update_kernel(const StepArgs a) {
+    constexpr int kItems = ITEMS;
     constexpr int NPL = N >= 4 ? 4 : N;        // states per lane
     constexpr int LANES = N / NPL;             // lanes per channel (1, 2 or 4)
     constexpr int CH_PER_CTA = kStepThreads / LANES;
