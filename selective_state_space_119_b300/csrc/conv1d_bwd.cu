@@ -63,8 +63,10 @@ __device__ __forceinline__ float dsilu(float p) {
     return s * fmaf(p, 1.f - s, 1.f);
 }
 
-template <typename T, int K>
-__global__ void __launch_bounds__(kThreads, 3) conv1d_silu_bwd_kernel(const ConvBwdArgs a) {
+template <typename T, int K, int RUN = kRun, int THREADS = kThreads, int MINB = 3>
+__global__ void __launch_bounds__(THREADS, MINB) conv1d_silu_bwd_kernel(const ConvBwdArgs a) {
+    constexpr int kRun = RUN;
+    constexpr int kRuns = THREADS / 32;
     constexpr int NX = kRun + 2 * (K - 1);   // x rows: t0 - K + 1 .. t0 + kRun + K - 2
     constexpr int ND = kRun + K - 1;         // du / dpre rows: t0 .. t0 + kRun + K - 2
     __shared__ float s_part[kRuns][32][kVE * (K + 1)];

@@ -10,6 +10,8 @@
         --dim 1536 [--calls 3]
     python -m selective_state_space_119_b300.profile_case train --batch 4 --seqlen 2048 \\
         --dim 1536 [--A s4d|lognormal] [--calls 3]
+    python -m selective_state_space_119_b300.profile_case decode --batch 256 --seqlen 1 \\
+        --dim 5120 [--calls 3]
 
 The inputs are the seeded workload distributions of ``inputs`` (the scan's
 long-sequence recipe by default: delta log-uniform in [1e-4, 1e-2], gate, D = 1,
@@ -130,6 +132,27 @@ def run_train(args, torch):
           % (ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])), flush=True)
 
 
+def run_decode(args, torch):
+    """Decode steps on the recipe of the decode workload (state N(0, 1), one
+    token set per call, --seqlen ignored); every call updates the state."""
+    from selective_state_space_119_b300 import inputs as I
+    from selective_state_space_119_b300 import libssm
+    spec = I.DecodeSpec(args.batch, args.dim, steps=1, seed=7)
+    inp = I.make_decode_inputs(spec)
+    t = {k: _dev(torch, v) for k, v in inp.items()}
+    state = t["state0"].clone()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.calls):
+        e0.record()
+        libssm.ssm_state_update(state, t["x"][0], t["delta"][0], t["A"], t["B"][0], t["C"][0],
+                                D=t.get("D"), z=None if t.get("z") is None else t["z"][0],
+                                delta_bias=t.get("delta_bias"),
+                                delta_softplus=False)
+        e1.record()
+    torch.cuda.synchronize()
+    print("last call %.3f ms (output allocation included)" % e0.elapsed_time(e1), flush=True)
+
+
 def run_conv(args, torch):
     """The input stage (causal conv1d of width 4 + SiLU) and its backward, each
     call one forward and one backward (du ~ N(0, 1)), bf16."""
@@ -154,7 +177,7 @@ def run_conv(args, torch):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("kernel", choices=["scan", "ssd", "bcd_train", "conv", "train"])
+    ap.add_argument("kernel", choices=["scan", "ssd", "bcd_train", "conv", "train", "decode"])
     ap.add_argument("--batch", type=int, required=True)
     ap.add_argument("--seqlen", type=int, required=True)
     ap.add_argument("--dim", type=int, default=5120)
@@ -169,7 +192,7 @@ def main(argv=None):
     if not torch.cuda.is_available():
         sys.exit("no CUDA device")
     {"scan": run_scan, "ssd": run_ssd, "bcd_train": run_bcd_train,
-     "conv": run_conv, "train": run_train}[args.kernel](args, torch)
+     "conv": run_conv, "train": run_train, "decode": run_decode}[args.kernel](args, torch)
 
 
 if __name__ == "__main__":
