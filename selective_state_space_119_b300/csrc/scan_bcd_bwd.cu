@@ -285,6 +285,336 @@ __global__ void __launch_bounds__(kThreads, 3) bcd_grad_kernel(const BwdArgs a) 
     a.pbias[row * a.dim + d] = gbias;
 }
 
+// The gradient pass for bf16 rows, staged through shared memory.
+//
+// The same arithmetic as bcd_grad_kernel, laid out for more warps and with the
+// loads taken off the lanes:
+// - Each 8-token block's B and C rows (32 bytes per channel and token), its x,
+//   delta, z and dout rows and its checkpoint are copied into one of two
+//   shared-memory buffers with 16-byte cp.async, the next block's (in reverse
+//   order) while this one computes, so a block's 80 KB are in flight at once.
+// - Two lanes per channel, 8 states each (256 threads for 128 channels): one
+//   CTA per SM (the buffers take 208 KB) still holds 8 warps, and the sums over
+//   the states (sum_n g B, sum_n g A a h, sum_n C h) take one exchange of the
+//   pair. The per-token scalars (dt, sigmoid(delta + bias), dy, dout silu'(z))
+//   are formed once per channel in a pass over the block.
+// - Only the states after the block's even tokens are kept; the sweep forms an
+//   odd token's state from the even one before it, h_j = e^{dt A} h_{j-1} +
+//   dt x B, the step the recompute took.
+// Requires dim % 8 == 0 and 16-byte aligned rows, which the bf16 entry points
+// check.
+constexpr int kGThreads = 2 * kThreads;              // two lanes per channel
+constexpr int kNH = kN / 2;                          // states per lane
+constexpr int kSRows = kTB * kThreads * kN * 2;      // a block's B (or C) rows, bytes
+constexpr int kSScal = kTB * kThreads * 2;           // a block's x (or delta, z, dout) row set
+constexpr int kSCkpt = kThreads * kN * 4;            // a block's checkpoint
+constexpr int kSOffScal = 2 * kSRows, kSOffCkpt = 2 * kSRows + 4 * kSScal;
+constexpr int kSBuf = kSOffCkpt + kSCkpt;            // one buffer (80 KB)
+constexpr int kSHist = kTB / 2 * 2 * kGThreads * 16; // states after the even tokens
+constexpr int kSTok = kTB * kThreads * 16;           // per token and channel: dt, sig, dy, gz
+constexpr int kStagedSmem = 2 * kSBuf + kSHist + kSTok;
+static_assert(kStagedSmem <= 227 * 1024, "shared memory per CTA");
+static_assert(kThreads == 128 && kTB == 8 && kN == 16, "the copy and lane maps below");
+
+// Byte offset of 16-byte piece `half` (0, 1) of channel ch's row within one
+// token's 128 rows (the two lanes of channel ch read one piece each; lanes of a
+// quarter-warp read 128 consecutive bytes).
+__device__ __forceinline__ int row_piece(int ch, int half) { return ch * 32 + (half << 4); }
+// Byte offset of float4 `part` (0..3) of channel ch's checkpoint: parts rotate
+// with ch / 2 so that the 8 lanes of a quarter-warp reading part 2 half + i
+// of channels ch .. ch + 3 cover all 32 banks.
+__device__ __forceinline__ int ckpt_piece(int ch, int part) {
+    return ch * 64 + ((part ^ ((ch >> 1) & 3)) << 4);
+}
+
+// 16 bytes global -> shared, asynchronously; valid = false writes zeros.
+__device__ __forceinline__ void cp16(void* dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int K>
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(K) : "memory");
+}
+
+// 8 floats -> 8 bf16 (16 bytes)
+__device__ __forceinline__ void st_half(__nv_bfloat16* p, const float2 (&v)[kNH / 2]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = __float22bfloat162_rn(v[i]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <bool SOFTPLUS, bool GATE>
+__global__ void __launch_bounds__(kGThreads, 1) bcd_grad_staged_kernel(const BwdArgs a) {
+    using T = __nv_bfloat16;
+    extern __shared__ __align__(16) unsigned char smem[];
+    float4* hist = reinterpret_cast<float4*>(smem + 2 * kSBuf);          // [kTB/2][2][kGThreads]
+    float4* stok = reinterpret_cast<float4*>(smem + 2 * kSBuf + kSHist); // [kTB][kThreads]
+
+    const int tid = threadIdx.x;
+    const int c = tid >> 1, half = tid & 1;   // this lane: channel c of the tile, states 8 half ..
+    const int64_t lin = blockIdx.x;           // (k * batch + b) * tiles + tile
+    const int64_t tile = lin % a.tiles;
+    const int64_t b = (lin / a.tiles) % a.batch;
+    const int64_t k = lin / (a.tiles * a.batch);
+    const int64_t dbase = tile * kThreads;
+    // lanes past dim (a ragged last tile) compute on zeros and store nothing;
+    // every lane takes part in the copies and the barriers
+    const int nch = a.dim - dbase < kThreads ? static_cast<int>(a.dim - dbase) : kThreads;
+    const bool ch_ok = c < nch;
+    const int64_t d = ch_ok ? dbase + c : dbase;
+    const int64_t t_begin = k * a.chunk_len;
+    const int64_t t_end = min(a.L, t_begin + a.chunk_len);
+    const int q0 = kNH * half;
+
+    // states in pairs (packed FP32 arithmetic): pair p holds states q0 + 2p, q0 + 2p + 1
+    constexpr int kP2 = kNH / 2;
+    float2 A2[kP2], Q[kP2], gA[kP2];
+#pragma unroll
+    for (int p = 0; p < kP2; ++p) {
+        A2[p] = make_float2(__ldg(a.A + d * kN + q0 + 2 * p) * kLog2e,
+                            __ldg(a.A + d * kN + q0 + 2 * p + 1) * kLog2e);
+        Q[p] = (a.dfinal && ch_ok)
+                   ? *reinterpret_cast<const float2*>(a.dfinal + (b * a.dim + d) * kN + q0 + 2 * p)
+                   : make_float2(0.f, 0.f);
+        gA[p] = make_float2(0.f, 0.f);
+    }
+    // dL/dh at the chunk's last token: the carries of the chunks to the right
+    for (int64_t i = a.nchunks - 1; i > k; --i) {
+        const int64_t idx = (b * (a.nchunks - 1) + (i - 1)) * a.dim + d;
+        const float S = a.wsS[idx];
+#pragma unroll
+        for (int p = 0; p < kP2; ++p) {
+            const float2 qc = *reinterpret_cast<const float2*>(a.wsQ + idx * kN + q0 + 2 * p);
+            const float2 e = make_float2(ex2(A2[p].x * S), ex2(A2[p].y * S));
+            Q[p] = __ffma2_rn(e, Q[p], qc);
+        }
+    }
+    const float Dd = a.D ? __ldg(a.D + d) : 0.f;
+    // the scalar pass's channel (tid mod 128) and its bias
+    const int pc = tid & (kThreads - 1);
+    const float pbias = (a.delta_bias && pc < nch) ? __ldg(a.delta_bias + dbase + pc) : 0.f;
+    const int64_t e0 = b * a.L * a.dim + d;
+    T* dxg = static_cast<T*>(a.dx) + e0;
+    T* ddg = static_cast<T*>(a.ddelta) + e0;
+    T* dzg = GATE ? static_cast<T*>(a.dz) + e0 : nullptr;
+    T* dBg = static_cast<T*>(a.dB) + e0 * kN + q0;
+    T* dCg = static_cast<T*>(a.dC) + e0 * kN + q0;
+    float gD = 0.f, gbias = 0.f;
+
+    // the copies of block m (tokens 8m ..) into buffer `buf`: consecutive lanes
+    // take consecutive 16-byte pieces of global memory; rows past the chunk's
+    // end or the last channel read as zeros
+    auto stage = [&](int64_t m, int buf) {
+        unsigned char* base = smem + buf * kSBuf;
+        const int64_t u0 = m * kTB;
+        const int cnt = t_end - u0 < kTB ? static_cast<int>(t_end - u0) : kTB;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const T* g = static_cast<const T*>(which ? a.C : a.B);
+#pragma unroll
+            for (int j = 0; j < kTB; ++j) {
+                const bool valid = j < cnt && c < nch;
+                const T* src = g + (valid ? ((b * a.L + u0 + j) * a.dim + dbase + c) * kN + q0 : 0);
+                cp16(base + which * kSRows + j * (kThreads * 32) + row_piece(c, half), src, valid);
+            }
+        }
+        // x, delta (lanes 0..127) and z, dout (lanes 128..255): channels
+        // 8 (tid mod 16) .. of token (tid mod 128) / 16
+        {
+            const int j = pc >> 4, c8 = (pc & 15) * 8;
+            const bool valid = j < cnt && c8 < nch;
+            const int64_t off = valid ? (b * a.L + u0 + j) * a.dim + dbase + c8 : 0;
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                const int which = 2 * w + (tid >> 7);   // uniform per warp
+                if (!GATE && which == 2) continue;
+                const T* g = static_cast<const T*>(which == 0 ? a.x : which == 1 ? a.delta
+                                                   : which == 2 ? a.z : a.dout);
+                cp16(base + kSOffScal + which * kSScal + (j * kThreads + c8) * 2, g + off, valid);
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const int piece = p * kGThreads + tid, ch = piece >> 2, part = piece & 3;
+            const bool valid = ch < nch;
+            const float* src = a.ckpt + (valid ? ((b * a.nckpt + m) * a.dim + dbase + ch) * kN + part * 4 : 0);
+            cp16(base + kSOffCkpt + ckpt_piece(ch, part), src, valid);
+        }
+        cp_commit();
+    };
+
+    const int64_t m_first = t_begin / kTB, m_last = (t_end - 1) / kTB;
+    stage(m_last, 0);
+    int buf = 0;
+    for (int64_t m = m_last; m >= m_first; --m, buf ^= 1) {
+        const int64_t u0 = m * kTB;
+        const int cnt = t_end - u0 < kTB ? static_cast<int>(t_end - u0) : kTB;
+        if (m > m_first) {
+            stage(m - 1, buf ^ 1);   // in flight while this block computes
+            cp_wait<1>();
+        } else {
+            cp_wait<0>();
+        }
+        __syncthreads();   // every lane's copies of this block have landed
+        const unsigned char* base = smem + buf * kSBuf;
+        const T* xs = reinterpret_cast<const T*>(base + kSOffScal);   // [kTB][kThreads] each
+        const T* ds = xs + kTB * kThreads;
+        const T* zs = ds + kTB * kThreads;
+        const T* gs = zs + kTB * kThreads;
+        // the per-token scalars of channel pc, tokens (tid / 128) + 2 i
+#pragma unroll
+        for (int i = 0; i < kTB / 2; ++i) {
+            const int j = 2 * i + (tid >> 7);
+            const int o = j * kThreads + pc;
+            const float v = __bfloat162float(ds[o]) + pbias;
+            const float dout = __bfloat162float(gs[o]);
+            float4 s;
+            s.x = SOFTPLUS ? softplus(v) : v;
+            s.y = SOFTPLUS ? sigmoid(v) : 1.f;
+            s.z = dout;
+            s.w = 0.f;
+            if constexpr (GATE) {
+                const float zv = __bfloat162float(zs[o]);
+                s.z = dout * silu(zv);
+                s.w = dout * dsilu(zv);
+            }
+            stok[o] = s;
+        }
+        __syncthreads();
+        // this lane's half of channel c's B (which 0) or C (which 1) row of token j
+        auto row = [&](int which, int j, float2 (&v)[kP2]) {
+            const uint4 u = *reinterpret_cast<const uint4*>(base + which * kSRows + j * (kThreads * 32) +
+                                                            row_piece(c, half));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < kP2; ++i)
+                v[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+        };
+        auto e_pair = [&](const float2 A22, const float2 dt2) {
+            const float2 arg = __fmul2_rn(A22, dt2);
+            return make_float2(ex2(arg.x), ex2(arg.y));
+        };
+        // the state before token u0, then forward over the block, the states
+        // after the even tokens kept
+        float2 h[kP2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float4 v = *reinterpret_cast<const float4*>(base + kSOffCkpt + ckpt_piece(c, 2 * half + i));
+            h[2 * i] = make_float2(v.x, v.y);
+            h[2 * i + 1] = make_float2(v.z, v.w);
+        }
+#pragma unroll
+        for (int j = 0; j < kTB; ++j) {
+            if (j < cnt) {
+                const float xv = __bfloat162float(xs[j * kThreads + c]);
+                const float dt = stok[j * kThreads + c].x;
+                float2 bb[kP2];
+                row(0, j, bb);
+                const float2 dt2 = make_float2(dt, dt), dtx2 = make_float2(dt * xv, dt * xv);
+#pragma unroll
+                for (int p = 0; p < kP2; ++p)
+                    h[p] = __ffma2_rn(e_pair(A2[p], dt2), h[p], __fmul2_rn(dtx2, bb[p]));
+                if ((j & 1) == 0) {
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+                        hist[((j >> 1) * 2 + i) * kGThreads + tid] =
+                            make_float4(h[2 * i].x, h[2 * i].y, h[2 * i + 1].x, h[2 * i + 1].y);
+                }
+            }
+        }
+        // one token of the reverse sweep; odd: the kept state is h_{j-1}
+        auto sweep = [&](const int j, const bool odd) {
+            const float xv = __bfloat162float(xs[j * kThreads + c]);
+            const float4 s = stok[j * kThreads + c];
+            const float dt = s.x, dy = s.z;
+            float2 bb[kP2], cc[kP2], hk[kP2];
+            row(0, j, bb);
+            row(1, j, cc);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float4 v = hist[((j >> 1) * 2 + i) * kGThreads + tid];
+                hk[2 * i] = make_float2(v.x, v.y);
+                hk[2 * i + 1] = make_float2(v.z, v.w);
+            }
+            const float dtx = dt * xv;
+            const float2 dt2 = make_float2(dt, dt), dtx2 = make_float2(dtx, dtx),
+                         ndtx2 = make_float2(-dtx, -dtx), dy2 = make_float2(dy, dy);
+            float2 dB[kP2], dC[kP2];
+            float2 sgb2 = make_float2(0.f, 0.f), sga2 = sgb2, y2 = sgb2;
+#pragma unroll
+            for (int p = 0; p < kP2; ++p) {
+                const float2 e = e_pair(A2[p], dt2);
+                float2 hh, ahp;   // h_j and e^{dt A} h_{j-1}
+                if (odd) {
+                    ahp = __fmul2_rn(e, hk[p]);
+                    hh = __ffma2_rn(dtx2, bb[p], ahp);
+                } else {
+                    hh = hk[p];
+                    ahp = __ffma2_rn(ndtx2, bb[p], hh);
+                }
+                const float2 g = __ffma2_rn(dy2, cc[p], Q[p]);
+                const float2 gahp = __fmul2_rn(g, ahp);
+                dC[p] = __fmul2_rn(dy2, hh);
+                dB[p] = __fmul2_rn(g, dtx2);
+                sgb2 = __ffma2_rn(g, bb[p], sgb2);
+                sga2 = __ffma2_rn(gahp, A2[p], sga2);
+                gA[p] = __ffma2_rn(gahp, dt2, gA[p]);
+                Q[p] = __fmul2_rn(e, g);
+                if constexpr (GATE) y2 = __ffma2_rn(cc[p], hh, y2);
+            }
+            float sgb = sgb2.x + sgb2.y, sga = sga2.x + sga2.y, y = y2.x + y2.y;
+            // the pair's sums over all 16 states
+            sgb += __shfl_xor_sync(0xffffffffu, sgb, 1);
+            sga += __shfl_xor_sync(0xffffffffu, sga, 1);
+            if constexpr (GATE) y += __shfl_xor_sync(0xffffffffu, y, 1);
+            if (ch_ok) {
+                const int64_t e = (u0 + j) * a.dim;
+                st_half(dBg + e * kN, dB);
+                st_half(dCg + e * kN, dC);
+                if (half == 0) {
+                    const float ddt = fmaf(xv, sgb, sga * kLn2f);
+                    const float dd = SOFTPLUS ? ddt * s.y : ddt;
+                    IO<T>::st(dxg + e, fmaf(dt, sgb, dy * Dd));
+                    IO<T>::st(ddg + e, dd);
+                    gD = fmaf(dy, xv, gD);
+                    gbias += dd;
+                } else if constexpr (GATE) {
+                    IO<T>::st(dzg + e, s.w * fmaf(Dd, xv, y));
+                }
+            }
+        };
+        for (int j = cnt - 1; j >= 0; --j) {
+            if (j & 1)
+                sweep(j, true);
+            else
+                sweep(j, false);
+        }
+        __syncthreads();   // this buffer and the scalars are free for what follows
+    }
+    if (!ch_ok) return;
+    if (k == 0 && a.dh0) {
+#pragma unroll
+        for (int p = 0; p < kP2; ++p)
+            *reinterpret_cast<float2*>(a.dh0 + (b * a.dim + d) * kN + q0 + 2 * p) = Q[p];
+    }
+    const int64_t prow = b * a.nchunks + k;
+#pragma unroll
+    for (int p = 0; p < kP2; ++p)
+        *reinterpret_cast<float2*>(a.pA + (prow * a.dim + d) * kN + q0 + 2 * p) = gA[p];
+    if (half == 0) {
+        a.pD[prow * a.dim + d] = gD;
+        a.pbias[prow * a.dim + d] = gbias;
+    }
+}
+
 // dA, dD, dbias: the shares of every (batch row, chunk), added in order.
 __global__ void __launch_bounds__(256) bcd_bwd_reduce_kernel(const BwdArgs a) {
     const int64_t nA = a.dim * kN, nd = a.dim;
@@ -317,11 +647,16 @@ cudaError_t launch_flags(const BwdArgs& a, cudaStream_t s) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    constexpr bool kStaged = sizeof(T) == 2;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!done[dev]) {
-            e = cudaFuncSetAttribute(bcd_grad_kernel<T, SOFTPLUS, GATE>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kGradSmem);
+            if constexpr (kStaged)
+                e = cudaFuncSetAttribute(bcd_grad_staged_kernel<SOFTPLUS, GATE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kStagedSmem);
+            else
+                e = cudaFuncSetAttribute(bcd_grad_kernel<T, SOFTPLUS, GATE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kGradSmem);
             if (e != cudaSuccess) return e;
             done[dev] = true;
         }
@@ -330,8 +665,12 @@ cudaError_t launch_flags(const BwdArgs& a, cudaStream_t s) {
     if (a.nchunks > 1)
         bcd_carry_kernel<T, SOFTPLUS, GATE>
             <<<static_cast<unsigned>(per_chunk * (a.nchunks - 1)), kThreads, 0, s>>>(a);
-    bcd_grad_kernel<T, SOFTPLUS, GATE>
-        <<<static_cast<unsigned>(per_chunk * a.nchunks), kThreads, kGradSmem, s>>>(a);
+    if constexpr (kStaged)
+        bcd_grad_staged_kernel<SOFTPLUS, GATE>
+            <<<static_cast<unsigned>(per_chunk * a.nchunks), kGThreads, kStagedSmem, s>>>(a);
+    else
+        bcd_grad_kernel<T, SOFTPLUS, GATE>
+            <<<static_cast<unsigned>(per_chunk * a.nchunks), kThreads, kGradSmem, s>>>(a);
     const int64_t total = a.dim * kN + 2 * a.dim;
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, 148 * 16);
     bcd_bwd_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);

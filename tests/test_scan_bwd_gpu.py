@@ -419,14 +419,18 @@ def test_bcd_gradients_plain_delta(torch, io, gate, D_kind):
                 "per-channel ddelta_bias = sum of ddelta")
 
 
-@pytest.mark.parametrize("L,dim", [(1, 128), (7, 128), (8, 128), (9, 132), (33, 132)])
-def test_bcd_gradients_short_sequences(torch, L, dim):
-    """dim 132 (fp32) ends half-way through a warp's 8 channels."""
-    spec = I.ScanSpec(2, L, dim, io="f32", delta_kind="softplus_bias", seed=97)
+@pytest.mark.parametrize("io,L,dim", [("f32", 1, 128), ("f32", 7, 128), ("f32", 8, 128),
+                                       ("f32", 9, 132), ("f32", 33, 132), ("bf16", 1, 136),
+                                       ("bf16", 7, 136), ("bf16", 9, 136), ("bf16", 33, 256)])
+def test_bcd_gradients_short_sequences(torch, io, L, dim):
+    """dim 132 (fp32) ends half-way through a warp's 8 channels; bf16 runs the
+    staged gradient pass, whose blocks here hold fewer than 8 tokens and whose
+    last channel tile (dim 136) holds 8 channels."""
+    spec = I.ScanSpec(2, L, dim, io=io, delta_kind="softplus_bias", seed=97)
     inp, B4, C4, dout, _, dfin = _bcd_case(spec, 98, with_dfinal=True)
     _, _, _, g = _gpu_train_bcd(inp, B4, C4, True, dout, dfinal=dfin, want_dh0=True)
     ref = _oracle_bcd(inp, B4, C4, True, dout, dfinal=dfin)
-    _check_bcd_grads(g, ref, "f32", "(per-channel, L %d, dim %d)" % (L, dim), dh0=True)
+    _check_bcd_grads(g, ref, io, "(per-channel, %s, L %d, dim %d)" % (io, L, dim), dh0=True)
 
 
 def test_bcd_equal_rows_give_the_shared_gradients(torch):
