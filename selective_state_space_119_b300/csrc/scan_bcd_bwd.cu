@@ -615,6 +615,119 @@ __global__ void __launch_bounds__(kGThreads, 1) bcd_grad_staged_kernel(const Bwd
     }
 }
 
+// The reverse carry for bf16 rows, staged through shared memory: the same
+// recurrence as bcd_carry_kernel. Each 8-token block's C rows and delta, dout
+// and z rows of 64 channels are copied with cp.async, three blocks in flight
+// per CTA; two lanes per channel, 8 states each, and each lane forms its
+// channel's dt and dy itself. 57 KB of shared memory: three CTAs (12 warps)
+// per SM.
+constexpr int kCCh = 64;                               // channels per CTA
+constexpr int kCThreads = 2 * kCCh;
+constexpr int kCStages = 3;
+constexpr int kCRows = kTB * kCCh * kN * 2;            // a block's C rows, bytes
+constexpr int kCScal = kTB * kCCh * 2;                 // a block's delta (dout, z) rows
+constexpr int kCBuf = kCRows + 3 * kCScal;
+constexpr int kCarrySmem = kCStages * kCBuf;
+
+template <bool SOFTPLUS, bool GATE>
+__global__ void __launch_bounds__(kCThreads) bcd_carry_staged_kernel(const BwdArgs a, int64_t ctiles) {
+    using T = __nv_bfloat16;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int tid = threadIdx.x;
+    const int c = tid >> 1, half = tid & 1;
+    const int64_t lin = blockIdx.x;   // ((k - 1) * batch + b) * ctiles + tile
+    const int64_t tile = lin % ctiles;
+    const int64_t b = (lin / ctiles) % a.batch;
+    const int64_t k = 1 + lin / (ctiles * a.batch);
+    const int64_t dbase = tile * kCCh;
+    const int nch = a.dim - dbase < kCCh ? static_cast<int>(a.dim - dbase) : kCCh;
+    const bool ch_ok = c < nch;
+    const int64_t d = ch_ok ? dbase + c : dbase;
+    const int64_t t_begin = k * a.chunk_len;
+    const int64_t t_end = min(a.L, t_begin + a.chunk_len);
+    const int q0 = kNH * half;
+    constexpr int kP2 = kNH / 2;
+
+    float2 A2[kP2], Q[kP2];
+#pragma unroll
+    for (int p = 0; p < kP2; ++p) {
+        A2[p] = make_float2(__ldg(a.A + d * kN + q0 + 2 * p) * kLog2e,
+                            __ldg(a.A + d * kN + q0 + 2 * p + 1) * kLog2e);
+        Q[p] = make_float2(0.f, 0.f);
+    }
+    const float bias = a.delta_bias ? __ldg(a.delta_bias + d) : 0.f;
+
+    auto stage = [&](int64_t m, int buf) {
+        unsigned char* base = smem + buf * kCBuf;
+        const int64_t u0 = m * kTB;
+        const int cnt = t_end - u0 < kTB ? static_cast<int>(t_end - u0) : kTB;
+        const T* Cg = static_cast<const T*>(a.C);
+        // C rows: token j, channel ch, piece h: 8 tokens x 64 channels x 2
+#pragma unroll
+        for (int i = 0; i < kTB * kCCh * 2 / kCThreads; ++i) {
+            const int piece = i * kCThreads + tid, j = piece / (kCCh * 2), r = piece % (kCCh * 2);
+            const int ch = r >> 1, h = r & 1;
+            const bool valid = j < cnt && ch < nch;
+            const T* src = Cg + (valid ? ((b * a.L + u0 + j) * a.dim + dbase + ch) * kN + h * 8 : 0);
+            cp16(base + piece * 16, src, valid);
+        }
+        // delta, dout, z: 3 arrays x 8 tokens x 8 pieces of 8 channels
+        for (int piece = tid; piece < 3 * kTB * (kCCh / 8); piece += kCThreads) {
+            const int which = piece / (kTB * (kCCh / 8)), r = piece % (kTB * (kCCh / 8));
+            if (!GATE && which == 2) continue;
+            const int j = r / (kCCh / 8), c8 = (r % (kCCh / 8)) * 8;
+            const T* g = static_cast<const T*>(which == 0 ? a.delta : which == 1 ? a.dout : a.z);
+            const bool valid = j < cnt && c8 < nch;
+            const T* src = g + (valid ? (b * a.L + u0 + j) * a.dim + dbase + c8 : 0);
+            cp16(base + kCRows + which * kCScal + (j * kCCh + c8) * 2, src, valid);
+        }
+    };
+
+    const int64_t m_first = t_begin / kTB, m_last = (t_end - 1) / kTB;
+    const int64_t nblk = m_last - m_first + 1;
+#pragma unroll
+    for (int s = 0; s < kCStages - 1; ++s) {
+        if (s < nblk) stage(m_last - s, s);
+        cp_commit();
+    }
+    float dt_sum = 0.f;
+    for (int64_t i = 0; i < nblk; ++i) {
+        const int64_t m = m_last - i;
+        if (i + kCStages - 1 < nblk)
+            stage(m - (kCStages - 1), static_cast<int>((i + kCStages - 1) % kCStages));
+        cp_commit();
+        cp_wait<kCStages - 1>();
+        __syncthreads();   // block m's copies (every lane's) have landed
+        const unsigned char* base = smem + (i % kCStages) * kCBuf;
+        const T* dls = reinterpret_cast<const T*>(base + kCRows);
+        const T* gos = dls + kTB * kCCh;
+        const T* zs = gos + kTB * kCCh;
+        const int cnt = t_end - m * kTB < kTB ? static_cast<int>(t_end - m * kTB) : kTB;
+        for (int j = cnt - 1; j >= 0; --j) {
+            float dt = __bfloat162float(dls[j * kCCh + c]) + bias;
+            if constexpr (SOFTPLUS) dt = softplus(dt);
+            float dy = __bfloat162float(gos[j * kCCh + c]);
+            if constexpr (GATE) dy *= silu(__bfloat162float(zs[j * kCCh + c]));
+            const uint4 u = *reinterpret_cast<const uint4*>(base + (j * kCCh + c) * 32 + half * 16);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            const float2 dt2 = make_float2(dt, dt), dy2 = make_float2(dy, dy);
+#pragma unroll
+            for (int p = 0; p < kP2; ++p) {
+                const float2 cc = make_float2(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xffff0000u));
+                const float2 arg = __fmul2_rn(A2[p], dt2);
+                Q[p] = __fmul2_rn(make_float2(ex2(arg.x), ex2(arg.y)), __ffma2_rn(dy2, cc, Q[p]));
+            }
+            dt_sum += dt;
+        }
+        __syncthreads();   // this buffer is refilled two blocks later
+    }
+    if (!ch_ok) return;
+    const int64_t idx = (b * (a.nchunks - 1) + (k - 1)) * a.dim + d;
+#pragma unroll
+    for (int p = 0; p < kP2; ++p) *reinterpret_cast<float2*>(a.wsQ + idx * kN + q0 + 2 * p) = Q[p];
+    if (half == 0) a.wsS[idx] = dt_sum;
+}
+
 // dA, dD, dbias: the shares of every (batch row, chunk), added in order.
 __global__ void __launch_bounds__(256) bcd_bwd_reduce_kernel(const BwdArgs a) {
     const int64_t nA = a.dim * kN, nd = a.dim;
@@ -651,10 +764,13 @@ cudaError_t launch_flags(const BwdArgs& a, cudaStream_t s) {
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!done[dev]) {
-            if constexpr (kStaged)
+            if constexpr (kStaged) {
                 e = cudaFuncSetAttribute(bcd_grad_staged_kernel<SOFTPLUS, GATE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kStagedSmem);
-            else
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(bcd_carry_staged_kernel<SOFTPLUS, GATE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kCarrySmem);
+            } else
                 e = cudaFuncSetAttribute(bcd_grad_kernel<T, SOFTPLUS, GATE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kGradSmem);
             if (e != cudaSuccess) return e;
@@ -662,9 +778,17 @@ cudaError_t launch_flags(const BwdArgs& a, cudaStream_t s) {
         }
     }
     const int64_t per_chunk = a.tiles * a.batch;
-    if (a.nchunks > 1)
-        bcd_carry_kernel<T, SOFTPLUS, GATE>
-            <<<static_cast<unsigned>(per_chunk * (a.nchunks - 1)), kThreads, 0, s>>>(a);
+    if (a.nchunks > 1) {
+        if constexpr (kStaged) {
+            const int64_t ctiles = (a.dim + kCCh - 1) / kCCh;
+            bcd_carry_staged_kernel<SOFTPLUS, GATE>
+                <<<static_cast<unsigned>(ctiles * a.batch * (a.nchunks - 1)), kCThreads, kCarrySmem, s>>>(
+                    a, ctiles);
+        } else {
+            bcd_carry_kernel<T, SOFTPLUS, GATE>
+                <<<static_cast<unsigned>(per_chunk * (a.nchunks - 1)), kThreads, 0, s>>>(a);
+        }
+    }
     if constexpr (kStaged)
         bcd_grad_staged_kernel<SOFTPLUS, GATE>
             <<<static_cast<unsigned>(per_chunk * a.nchunks), kGThreads, kStagedSmem, s>>>(a);

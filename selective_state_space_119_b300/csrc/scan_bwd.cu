@@ -29,21 +29,22 @@
 // pairs of tokens: an odd token's state is one step of the recurrence from the
 // even one before it (h_t = e^{dt A} h_{t-1} + dt x B, the e^{dt A} that the
 // sweep forms anyway), which halves the shared memory of the states and lets
-// three CTAs share an SM. The sequence is split into the same
-// L-chunks as the forward: a first pass computes, for every chunk but the
-// first, its reverse carry from zero (Q at its first token) and its sum of dt;
-// each chunk of the gradient pass composes the carries of the chunks to its
-// right, Q <- exp(A S_i) Q + Q_i, starting from dLoss/dfinal_state.
+// three CTAs share an SM. The sequence is split into L-chunks (the backward's
+// own plan): a first pass (carry16_kernel, one lane per channel) computes, for
+// every chunk but the first, its reverse carry from zero (Q at its first
+// token) and its sum of dt; each chunk of the gradient pass composes the
+// carries of the chunks to its right, Q <- exp(A S_i) Q + Q_i, starting from
+// dLoss/dfinal_state.
 //
-// Layout of the lanes is the forward's: lanes 2p, 2p+1 own channels 2p, 2p+1
-// of a 128-channel tile; lane j of the pair holds states [8j, 8j+8) of both
-// (slot 0 = own channel, slot 1 = partner). dB and dC sum over channels: per
-// token each lane holds 16 partial sums (its 8 states of dB and of dC, both
-// channels added), a 4-step reduce-scatter over the 16 lanes of equal j leaves
-// one warp sum per lane, the 4 warps are added in shared memory, and every
-// 128-channel tile writes its sums to a workspace that a last kernel adds up
-// (no atomics: the result does not depend on scheduling). dA, dD and dbias are
-// summed per CTA in registers and added the same way.
+// The gradient pass's lanes are laid out as the forward's: lanes 2p, 2p+1 own
+// channels 2p, 2p+1 of a 128-channel tile; lane j of the pair holds states
+// [8j, 8j+8) of both (slot 0 = own channel, slot 1 = partner). dB and dC sum
+// over channels: per token each lane holds 16 partial sums (its 8 states of dB
+// and of dC, both channels added), a 4-step reduce-scatter over the 16 lanes
+// of equal j leaves one warp sum per lane, the 4 warps are added in shared
+// memory, and every 128-channel tile writes its sums to a workspace that a last
+// kernel adds up (no atomics: the result does not depend on scheduling). dA,
+// dD and dbias are summed per CTA in registers and added the same way.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -59,12 +60,11 @@ constexpr int kBwdWarps = 4;
 constexpr int kBwdThreads = 32 * kBwdWarps;
 constexpr int kBwdChannels = kBwdThreads;      // one channel per lane
 constexpr int kGradTokens = kCkptTokens;       // tokens per block of the gradient pass (8)
-constexpr int kCarryTokens = 32;               // tokens per block of the reverse-carry pass
 constexpr float kLn2f = 0.6931471805599453f;
 
-// Shared memory of one CTA (N = 16): TB-token blocks; the gradient pass
-// (GRAD) also keeps the block's states, dt and y, and the dB | dC warp sums.
-template <typename T, int N, int TB, bool GRAD>
+// Shared memory of one gradient CTA (N = 16): two staging buffers of TB-token
+// blocks, the block's states, dt and y, and the dB | dC warp sums.
+template <typename T, int N, int TB>
 struct BwdSmem {
     static constexpr int VEC = 16 / sizeof(T);            // elements per 16-byte chunk
     static constexpr int ROWC = kBwdChannels / VEC;       // chunks per token row of a tile
@@ -78,10 +78,10 @@ struct BwdSmem {
     static constexpr int oIn = 0;
     static constexpr int oBC = 2 * IN_BYTES;                               // fp32 [TB][2N]
     static constexpr int oHist = oBC + TB * 2 * N * 4;                    // float4 [TB/2][N/4][128]
-    static constexpr int oRed = oHist + (GRAD ? TB / 2 * (N / 4) * kBwdThreads * 16 : 0);  // fp32 [4][TB][32]
-    static constexpr int oDt = oRed + (GRAD ? kBwdWarps * TB * 32 * 4 : 0);  // float2 [TB][128]
-    static constexpr int oY = oDt + (GRAD ? TB * kBwdThreads * 8 : 0);        // fp32 [TB][128]
-    static constexpr int kBytes = oY + (GRAD ? TB * kBwdThreads * 4 : 0);
+    static constexpr int oRed = oHist + TB / 2 * (N / 4) * kBwdThreads * 16;  // fp32 [4][TB][32]
+    static constexpr int oDt = oRed + kBwdWarps * TB * 32 * 4;  // float2 [TB][128]
+    static constexpr int oY = oDt + TB * kBwdThreads * 8;        // fp32 [TB][128]
+    static constexpr int kBytes = oY + TB * kBwdThreads * 4;
     static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
     static_assert(N == 16, "the backward is built for dstate 16");
 };
@@ -136,12 +136,11 @@ __device__ __forceinline__ void cp_async_wait() {
 // Starts the copies of one block's inputs into shared memory: the [TB x 128]
 // tiles of x, delta, (z,) dout and the TB rows of B and C, as 16-byte
 // asynchronous copies spread over the CTA (rows past the end of the sequence
-// and channels past dim are written as zeros). Tiles the pass does not read
-// are not copied.
-template <typename T, int N, int TB, bool GATE, int MODE>
+// and channels past dim are written as zeros). z is copied only with the gate.
+template <typename T, int N, int TB, bool GATE>
 __device__ __forceinline__ void stage_block(const BwdArgs& a, T* in, int64_t b, int64_t dbase,
                                             int64_t u0, int cnt) {
-    using Sm = BwdSmem<T, N, TB, MODE == 1>;
+    using Sm = BwdSmem<T, N, TB>;
     constexpr int VEC = Sm::VEC, ROWC = Sm::ROWC;
     constexpr int NTILES = 4;
     constexpr int TILE_CHUNKS = TB * ROWC;
@@ -150,8 +149,7 @@ __device__ __forceinline__ void stage_block(const BwdArgs& a, T* in, int64_t b, 
     for (int i = threadIdx.x; i < TOTAL; i += kBwdThreads) {
         if (i < NTILES * TILE_CHUNKS) {
             const int which = i / TILE_CHUNKS, r = i % TILE_CHUNKS;
-            // the state-carry pass reads no x; z only with the gate
-            if ((MODE == 0 && which == 0) || (!GATE && which == 2)) continue;
+            if (!GATE && which == 2) continue;
             const int tt = r / ROWC, c = (r % ROWC) * VEC;
             const void* base = which == 0 ? a.x : which == 1 ? a.delta : which == 2 ? a.z : a.dout;
             const bool valid = tt < cnt && dbase + c < a.dim;
@@ -161,7 +159,6 @@ __device__ __forceinline__ void stage_block(const BwdArgs& a, T* in, int64_t b, 
         } else {
             const int r = i - NTILES * TILE_CHUNKS;
             const int which = r / BC_CHUNKS, e = (r % BC_CHUNKS) * VEC;
-            if (MODE == 0 && which == 0) continue;           // the carry pass needs no B
             const int tt = e / N, n = e % N;
             const bool valid = tt < cnt;
             const T* src = static_cast<const T*>(which ? a.C : a.B) +
@@ -172,12 +169,12 @@ __device__ __forceinline__ void stage_block(const BwdArgs& a, T* in, int64_t b, 
     cp_async_commit();
 }
 
-// MODE 0: reverse carry of chunks 1 .. nchunks-1 from zero (Q at the chunk's
-// first token, and its sum of dt). MODE 1: the gradients of one chunk.
-template <typename T, int N, bool SOFTPLUS, bool GATE, int MODE, bool ZOH = false>
+// The gradients of one chunk (the reverse carries of the chunks to its right
+// come from carry16_kernel).
+template <typename T, int N, bool SOFTPLUS, bool GATE, bool ZOH = false>
 __global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(const BwdArgs a) {
-    constexpr int TB = MODE == 1 ? kGradTokens : kCarryTokens;
-    using Sm = BwdSmem<T, N, TB, MODE == 1>;
+    constexpr int TB = kGradTokens;
+    using Sm = BwdSmem<T, N, TB>;
     constexpr int NS = 2, SPL = N / NS;
     extern __shared__ __align__(128) unsigned char smem[];
     T* const in0 = reinterpret_cast<T*>(smem + Sm::oIn);        // two staging buffers
@@ -191,7 +188,7 @@ __global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(cons
     const int64_t lin = blockIdx.x;   // chunk-major: ((k * batch) + b) * tiles + tile
     const int64_t tile = lin % a.tiles;
     const int64_t b = (lin / a.tiles) % a.batch;
-    const int64_t k = lin / (a.tiles * a.batch) + (MODE == 0 ? 1 : 0);
+    const int64_t k = lin / (a.tiles * a.batch);
     const int64_t t_begin = k * a.chunk_len;
     const int64_t t_end = min(a.L, t_begin + a.chunk_len);
     const int nblk = static_cast<int>((t_end - t_begin + TB - 1) / TB);
@@ -214,7 +211,7 @@ __global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(cons
             Q[r][q] = 0.f;
             dA[r][q] = 0.f;
         }
-        if (MODE == 1 && ch_ok) {
+        if (ch_ok) {
             // the carry entering the chunk from the right: dLoss/dfinal_state,
             // then the chunks nchunks-1 .. k+1 in turn, Q <- exp(A S_i) Q + Q_i
             if (a.dfinal) {
@@ -230,8 +227,8 @@ __global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(cons
             }
         }
     }
-    const float Dd = (MODE == 1 && a.D && ch_ok) ? __ldg(a.D + dsafe) : 0.f;
-    float dD_acc = 0.f, dbias_acc = 0.f, S_acc = 0.f;
+    const float Dd = (a.D && ch_ok) ? __ldg(a.D + dsafe) : 0.f;
+    float dD_acc = 0.f, dbias_acc = 0.f;
     float invA[NS][SPL];   // 1 / A per state (exact zero-order hold only)
     if constexpr (ZOH) {
 #pragma unroll
@@ -246,7 +243,7 @@ __global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(cons
         return static_cast<int>(t_end - u < TB ? t_end - u : TB);
     };
     auto buffer = [&](int blk) { return in0 + (blk & 1) * (Sm::IN_BYTES / int(sizeof(T))); };
-    stage_block<T, N, TB, GATE, MODE>(a, buffer(nblk - 1), b, dbase, block_start(nblk - 1),
+    stage_block<T, N, TB, GATE>(a, buffer(nblk - 1), b, dbase, block_start(nblk - 1),
                                       block_count(nblk - 1));
     for (int blk = nblk - 1; blk >= 0; --blk) {
         const int64_t u0 = block_start(blk);
@@ -254,7 +251,7 @@ __global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(cons
         T* const in = buffer(blk);
         __syncthreads();   // the previous block is done with its buffer, bcs and red
         if (blk > 0) {
-            stage_block<T, N, TB, GATE, MODE>(a, buffer(blk - 1), b, dbase, block_start(blk - 1),
+            stage_block<T, N, TB, GATE>(a, buffer(blk - 1), b, dbase, block_start(blk - 1),
                                               block_count(blk - 1));
             cp_async_wait<1>();   // this thread's copies of the current block have landed
         } else {
@@ -280,7 +277,7 @@ __global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(cons
             dt[1] = __shfl_xor_sync(0xffffffffu, dt[0], 1);
         };
 
-        if constexpr (MODE == 1) {
+        {
             // ---- forward recompute of the block's states from its checkpoint ----
             float h[NS][SPL];
 #pragma unroll
@@ -354,13 +351,10 @@ __global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(cons
             const float2 gp = lds_pair(in + Sm::kDout + tt * kBwdChannels + pc);
             float dy[NS], dt[NS];
             float gate_ds = 1.f;   // silu'(z) of the own channel
-            if constexpr (MODE == 1) {
+            {
                 const float2 dtp = dts[tt * kBwdThreads + tid];
                 dt[0] = dtp.x;
                 dt[1] = dtp.y;
-            } else {
-                float xv[NS];
-                token(tt, dt, xv);
             }
             dy[0] = j ? gp.y : gp.x;
             if constexpr (GATE) {
@@ -371,22 +365,7 @@ __global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(cons
                 dy[0] *= zo * sg;
             }
             dy[1] = __shfl_xor_sync(0xffffffffu, dy[0], 1);   // the partner's channel
-            if constexpr (MODE == 0) {
-#pragma unroll
-                for (int r = 0; r < NS; ++r) {
-                    const float2 dt2 = make_float2(dt[r], dt[r]), dy2 = make_float2(dy[r], dy[r]);
-#pragma unroll
-                    for (int q = 0; q < SPL; q += 2) {
-                        const float2 g = __ffma2_rn(dy2, make_float2(Ct[q], Ct[q + 1]),
-                                                    make_float2(Q[r][q], Q[r][q + 1]));
-                        const float2 arg = __fmul2_rn(dt2, make_float2(A2[r][q], A2[r][q + 1]));
-                        const float2 qn = __fmul2_rn(make_float2(ex2(arg.x), ex2(arg.y)), g);
-                        Q[r][q] = qn.x;
-                        Q[r][q + 1] = qn.y;
-                    }
-                }
-                S_acc += dt[0];
-            } else {
+            {
                 float xv[NS];
                 {
                     const float2 xp = lds_pair(in + Sm::kX + tt * kBwdChannels + pc);
@@ -517,12 +496,12 @@ __global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(cons
                 red[(w * TB + tt) * 32 + lane] = vals[0];
             }
                 };
-#pragma unroll (MODE == 1 ? 1 : 2)
+#pragma unroll 1
         for (int tp = TB / 2 - 1; tp >= 0; --tp) {
             sweep_token(2 * tp + 1, true);
             sweep_token(2 * tp, false);
         }
-        if constexpr (MODE == 1) {
+        {
             __syncthreads();
             // the 4 warps' sums, written as this tile's share of dB | dC
             for (int i = tid; i < TB * 32; i += kBwdThreads) {
@@ -543,27 +522,148 @@ __global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(cons
 #pragma unroll
     for (int r = 0; r < NS; ++r) {
         const int64_t dr = dsafe - j + (j ^ r);
-        if constexpr (MODE == 0) {
-            float* dst = a.wsQ + ((b * (a.nchunks - 1) + (k - 1)) * a.dim + dr) * N + j * SPL;
+        float* dst = a.pA + ((b * a.nchunks + k) * a.dim + dr) * N + j * SPL;
 #pragma unroll
-            for (int q = 0; q < SPL; ++q) dst[q] = Q[r][q];
-        } else {
-            float* dst = a.pA + ((b * a.nchunks + k) * a.dim + dr) * N + j * SPL;
+        for (int q = 0; q < SPL; ++q) dst[q] = dA[r][q];
+        if (k == 0 && a.dh0) {
+            float* h0g = a.dh0 + (b * a.dim + dr) * N + j * SPL;
 #pragma unroll
-            for (int q = 0; q < SPL; ++q) dst[q] = dA[r][q];
-            if (k == 0 && a.dh0) {
-                float* h0g = a.dh0 + (b * a.dim + dr) * N + j * SPL;
-#pragma unroll
-                for (int q = 0; q < SPL; ++q) h0g[q] = Q[r][q];
-            }
+            for (int q = 0; q < SPL; ++q) h0g[q] = Q[r][q];
         }
     }
-    if constexpr (MODE == 0) {
-        a.wsS[(b * (a.nchunks - 1) + (k - 1)) * a.dim + d] = S_acc;
-    } else {
-        a.pD[(b * a.nchunks + k) * a.dim + d] = dD_acc;
-        a.pbias[(b * a.nchunks + k) * a.dim + d] = dbias_acc;
+    a.pD[(b * a.nchunks + k) * a.dim + d] = dD_acc;
+    a.pbias[(b * a.nchunks + k) * a.dim + d] = dbias_acc;
+}
+
+// The reverse carry of chunks 1 .. nchunks-1 from zero, in a layout of its
+// own: one lane per channel holding all 16 states (no partner exchange: the
+// lane forms its own dt and dy, and Q <- e^{dt A} (dy C + Q) needs nothing of
+// another channel), a ring of kCarryStages blocks of kCarryTB tokens of delta,
+// dout (and z) tiles and C rows copied by cp.async, C converted to fp32 once
+// per block. It leaves what the gradient pass composes: Q at the chunk's first
+// token and the chunk's sum of dt. (Two lanes per channel, 8 states each, with
+// twice the warps per SM, measured slower: each lane then repeats the
+// channel's softplus and SiLU.)
+constexpr int kCarryTB = 16;
+constexpr int kCarryStages = 4;
+template <typename T, int N>
+struct CarrySmem {
+    static constexpr int VEC = 16 / sizeof(T);
+    static constexpr int ROWC = kBwdChannels / VEC;        // 16-byte chunks per tile row
+    static constexpr int TILE = kCarryTB * kBwdChannels;   // elements of one [TB][128] tile
+    static constexpr int kDelta = 0, kDout = TILE, kZ = 2 * TILE, kC = 3 * TILE;
+    static constexpr int ELEMS = 3 * TILE + kCarryTB * N;
+    static constexpr int BYTES = (ELEMS * int(sizeof(T)) + 127) & ~127;
+    static constexpr int oCf = kCarryStages * BYTES;        // fp32 C rows [TB][N]
+    static constexpr int kBytes = oCf + kCarryTB * N * 4;
+    static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
+};
+
+template <typename T, int N, bool SOFTPLUS, bool GATE>
+__global__ void __launch_bounds__(kBwdThreads, 4) carry16_kernel(const BwdArgs a) {
+    using Sm = CarrySmem<T, N>;
+    constexpr int VEC = Sm::VEC, ROWC = Sm::ROWC, TB = kCarryTB;
+    extern __shared__ __align__(128) unsigned char smem[];
+    float* cf = reinterpret_cast<float*>(smem + Sm::oCf);
+
+    const int tid = threadIdx.x;
+    const int64_t lin = blockIdx.x;   // chunk-major: (((k - 1) * batch) + b) * tiles + tile
+    const int64_t tile = lin % a.tiles;
+    const int64_t b = (lin / a.tiles) % a.batch;
+    const int64_t k = lin / (a.tiles * a.batch) + 1;
+    const int64_t t_begin = k * a.chunk_len;
+    const int64_t t_end = min(a.L, t_begin + a.chunk_len);
+    const int nblk = static_cast<int>((t_end - t_begin + TB - 1) / TB);
+    const int64_t dbase = tile * kBwdChannels;
+    const int64_t d = dbase + tid;
+    const bool ch_ok = d < a.dim;
+    const int64_t dsafe = ch_ok ? d : 0;
+
+    float A2[N], Q[N];
+#pragma unroll
+    for (int q = 0; q < N; ++q) {
+        A2[q] = __ldg(a.A + dsafe * N + q) * kLog2e;
+        Q[q] = 0.f;
     }
+    const float bias = (a.delta_bias && ch_ok) ? __ldg(a.delta_bias + dsafe) : 0.f;
+
+    // block blk covers tokens t_begin + TB blk ..; blocks are visited last to first
+    auto stage = [&](int blk, int buf) {
+        T* in = reinterpret_cast<T*>(smem + buf * Sm::BYTES);
+        const int64_t u0 = t_begin + static_cast<int64_t>(blk) * TB;
+        const int cnt = static_cast<int>(t_end - u0 < TB ? t_end - u0 : TB);
+        constexpr int TILE_CHUNKS = TB * ROWC, C_CHUNKS = TB * N / VEC;
+        for (int i = tid; i < 3 * TILE_CHUNKS + C_CHUNKS; i += kBwdThreads) {
+            if (i < 3 * TILE_CHUNKS) {
+                const int which = i / TILE_CHUNKS, r = i % TILE_CHUNKS;
+                if (!GATE && which == 2) continue;
+                const int tt = r / ROWC, c = (r % ROWC) * VEC;
+                const void* g = which == 0 ? a.delta : which == 1 ? a.dout : a.z;
+                const bool valid = tt < cnt && dbase + c < a.dim;
+                const T* src = static_cast<const T*>(g) +
+                               (valid ? (b * a.L + u0 + tt) * a.dim + dbase + c : 0);
+                cp_async16(in + which * Sm::TILE + tt * kBwdChannels + c, src, valid);
+            } else {
+                const int e = (i - 3 * TILE_CHUNKS) * VEC, tt = e / N, n = e % N;
+                const bool valid = tt < cnt;
+                const T* src = static_cast<const T*>(a.C) + (valid ? (b * a.L + u0 + tt) * N + n : 0);
+                cp_async16(in + Sm::kC + e, src, valid);
+            }
+        }
+    };
+    // the ring: kCarryStages - 1 blocks ahead, one commit group per block
+#pragma unroll
+    for (int s = 0; s < kCarryStages - 1; ++s) {
+        if (s < nblk) stage(nblk - 1 - s, s);
+        cp_async_commit();
+    }
+    float S_acc = 0.f;
+    for (int i = 0; i < nblk; ++i) {
+        const int blk = nblk - 1 - i;
+        // groups committed: kCarryStages - 1 + i; the i-th (this block's) is complete
+        cp_async_wait<kCarryStages - 2>();
+        __syncthreads();   // every lane's copies of this block landed; the previous block is done
+        // refill the buffer the previous block used
+        if (i + kCarryStages - 1 < nblk)
+            stage(blk - (kCarryStages - 1), (i + kCarryStages - 1) % kCarryStages);
+        cp_async_commit();
+        const T* in = reinterpret_cast<const T*>(smem + (i % kCarryStages) * Sm::BYTES);
+        for (int e = tid; e < TB * N; e += kBwdThreads) cf[e] = to_f(in[Sm::kC + e]);
+        __syncthreads();   // the block's C rows in fp32
+        const int64_t u0 = t_begin + static_cast<int64_t>(blk) * TB;
+        const int cnt = static_cast<int>(t_end - u0 < TB ? t_end - u0 : TB);
+#pragma unroll 2
+        for (int tt = cnt - 1; tt >= 0; --tt) {
+            float dt = to_f(in[Sm::kDelta + tt * kBwdChannels + tid]) + bias;
+            if constexpr (SOFTPLUS) dt = softplus(dt);
+            float dy = to_f(in[Sm::kDout + tt * kBwdChannels + tid]);
+            if constexpr (GATE) dy *= silu(to_f(in[Sm::kZ + tt * kBwdChannels + tid]));
+            const float2 dt2 = make_float2(dt, dt), dy2 = make_float2(dy, dy);
+            const float4* c4 = reinterpret_cast<const float4*>(cf + tt * N);
+#pragma unroll
+            for (int q4 = 0; q4 < N / 4; ++q4) {
+                const float4 cv = c4[q4];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int q = 4 * q4 + 2 * h;
+                    const float2 C2 = h ? make_float2(cv.z, cv.w) : make_float2(cv.x, cv.y);
+                    const float2 g = __ffma2_rn(dy2, C2, make_float2(Q[q], Q[q + 1]));
+                    const float2 arg = __fmul2_rn(dt2, make_float2(A2[q], A2[q + 1]));
+                    const float2 qn = __fmul2_rn(make_float2(ex2(arg.x), ex2(arg.y)), g);
+                    Q[q] = qn.x;
+                    Q[q + 1] = qn.y;
+                }
+            }
+            S_acc += dt;
+        }
+        __syncthreads();   // cf and this block's buffer are free
+    }
+    if (!ch_ok) return;
+    const int64_t idx = (b * (a.nchunks - 1) + (k - 1)) * a.dim + d;
+    float4* dst = reinterpret_cast<float4*>(a.wsQ + idx * N);
+#pragma unroll
+    for (int q = 0; q < N / 4; ++q) dst[q] = make_float4(Q[4 * q], Q[4 * q + 1], Q[4 * q + 2], Q[4 * q + 3]);
+    a.wsS[idx] = S_acc;
 }
 
 // The sums over channel tiles (dB, dC) and over batch rows and chunks (dA, dD,
@@ -601,9 +701,9 @@ __global__ void __launch_bounds__(256) scan_bwd_reduce_kernel(const BwdArgs a) {
     }
 }
 
-template <typename T, int N, bool SOFTPLUS, bool GATE, int MODE, bool ZOH>
-cudaError_t launch_mode(const BwdArgs& a, int64_t ctas, cudaStream_t s) {
-    using Sm = BwdSmem<T, N, MODE == 1 ? kGradTokens : kCarryTokens, MODE == 1>;
+template <typename T, int N, bool SOFTPLUS, bool GATE, bool ZOH>
+cudaError_t launch_grad(const BwdArgs& a, int64_t ctas, cudaStream_t s) {
+    using Sm = BwdSmem<T, N, kGradTokens>;
     static std::mutex mu;
     static bool done[128] = {};
     int dev = 0;
@@ -613,14 +713,37 @@ cudaError_t launch_mode(const BwdArgs& a, int64_t ctas, cudaStream_t s) {
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!done[dev]) {
-            e = cudaFuncSetAttribute(scan_bwd_kernel<T, N, SOFTPLUS, GATE, MODE, ZOH>,
+            e = cudaFuncSetAttribute(scan_bwd_kernel<T, N, SOFTPLUS, GATE, ZOH>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::kBytes);
             if (e != cudaSuccess) return e;
             done[dev] = true;
         }
     }
-    scan_bwd_kernel<T, N, SOFTPLUS, GATE, MODE, ZOH>
+    scan_bwd_kernel<T, N, SOFTPLUS, GATE, ZOH>
         <<<static_cast<unsigned>(ctas), kBwdThreads, Sm::kBytes, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int N, bool SOFTPLUS, bool GATE>
+cudaError_t launch_carry(const BwdArgs& a, cudaStream_t s) {
+    using Sm = CarrySmem<T, N>;
+    static std::mutex mu;
+    static bool done[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            e = cudaFuncSetAttribute(carry16_kernel<T, N, SOFTPLUS, GATE>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::kBytes);
+            if (e != cudaSuccess) return e;
+            done[dev] = true;
+        }
+    }
+    carry16_kernel<T, N, SOFTPLUS, GATE>
+        <<<static_cast<unsigned>(a.tiles * a.batch * (a.nchunks - 1)), kBwdThreads, Sm::kBytes, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -630,12 +753,9 @@ cudaError_t launch_flags(const BwdArgs& a, cudaStream_t s) {
     cudaError_t e;
     // the reverse carries involve only the decay e^{dt A}: one carry pass
     // serves both input terms
-    if (a.nchunks > 1 &&
-        (e = launch_mode<T, N, SOFTPLUS, GATE, 0, false>(a, per_chunk * (a.nchunks - 1), s)) !=
-            cudaSuccess)
-        return e;
-    e = a.zoh ? launch_mode<T, N, SOFTPLUS, GATE, 1, true>(a, per_chunk * a.nchunks, s)
-              : launch_mode<T, N, SOFTPLUS, GATE, 1, false>(a, per_chunk * a.nchunks, s);
+    if (a.nchunks > 1 && (e = launch_carry<T, N, SOFTPLUS, GATE>(a, s)) != cudaSuccess) return e;
+    e = a.zoh ? launch_grad<T, N, SOFTPLUS, GATE, true>(a, per_chunk * a.nchunks, s)
+              : launch_grad<T, N, SOFTPLUS, GATE, false>(a, per_chunk * a.nchunks, s);
     if (e != cudaSuccess) return e;
     const int64_t total = a.batch * a.L * 2 * N + a.dim * N + 2 * a.dim;
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, 148 * 16);
