@@ -616,16 +616,18 @@ __global__ void __launch_bounds__(kGThreads, 1) bcd_grad_staged_kernel(const Bwd
 }
 
 // The reverse carry for bf16 rows, staged through shared memory: the same
-// recurrence as bcd_carry_kernel. Each 8-token block's C rows and delta, dout
+// recurrence as bcd_carry_kernel. Each 4-token block's C rows and delta, dout
 // and z rows of 64 channels are copied with cp.async, three blocks in flight
 // per CTA; two lanes per channel, 8 states each, and each lane forms its
-// channel's dt and dy itself. 57 KB of shared memory: three CTAs (12 warps)
-// per SM.
+// channel's dt and dy itself. 28.5 KB of shared memory: up to seven CTAs per
+// SM, so that a pass of a few CTAs per SM runs in one wave (8-token blocks,
+// 57 KB and three CTAs per SM, left a second, partial wave).
 constexpr int kCCh = 64;                               // channels per CTA
+constexpr int kCTB = 4;                                // tokens per block
 constexpr int kCThreads = 2 * kCCh;
 constexpr int kCStages = 3;
-constexpr int kCRows = kTB * kCCh * kN * 2;            // a block's C rows, bytes
-constexpr int kCScal = kTB * kCCh * 2;                 // a block's delta (dout, z) rows
+constexpr int kCRows = kCTB * kCCh * kN * 2;            // a block's C rows, bytes
+constexpr int kCScal = kCTB * kCCh * 2;                 // a block's delta (dout, z) rows
 constexpr int kCBuf = kCRows + 3 * kCScal;
 constexpr int kCarrySmem = kCStages * kCBuf;
 
@@ -659,12 +661,12 @@ __global__ void __launch_bounds__(kCThreads) bcd_carry_staged_kernel(const BwdAr
 
     auto stage = [&](int64_t m, int buf) {
         unsigned char* base = smem + buf * kCBuf;
-        const int64_t u0 = m * kTB;
-        const int cnt = t_end - u0 < kTB ? static_cast<int>(t_end - u0) : kTB;
+        const int64_t u0 = m * kCTB;
+        const int cnt = t_end - u0 < kCTB ? static_cast<int>(t_end - u0) : kCTB;
         const T* Cg = static_cast<const T*>(a.C);
         // C rows: token j, channel ch, piece h: 8 tokens x 64 channels x 2
 #pragma unroll
-        for (int i = 0; i < kTB * kCCh * 2 / kCThreads; ++i) {
+        for (int i = 0; i < kCTB * kCCh * 2 / kCThreads; ++i) {
             const int piece = i * kCThreads + tid, j = piece / (kCCh * 2), r = piece % (kCCh * 2);
             const int ch = r >> 1, h = r & 1;
             const bool valid = j < cnt && ch < nch;
@@ -672,8 +674,8 @@ __global__ void __launch_bounds__(kCThreads) bcd_carry_staged_kernel(const BwdAr
             cp16(base + piece * 16, src, valid);
         }
         // delta, dout, z: 3 arrays x 8 tokens x 8 pieces of 8 channels
-        for (int piece = tid; piece < 3 * kTB * (kCCh / 8); piece += kCThreads) {
-            const int which = piece / (kTB * (kCCh / 8)), r = piece % (kTB * (kCCh / 8));
+        for (int piece = tid; piece < 3 * kCTB * (kCCh / 8); piece += kCThreads) {
+            const int which = piece / (kCTB * (kCCh / 8)), r = piece % (kCTB * (kCCh / 8));
             if (!GATE && which == 2) continue;
             const int j = r / (kCCh / 8), c8 = (r % (kCCh / 8)) * 8;
             const T* g = static_cast<const T*>(which == 0 ? a.delta : which == 1 ? a.dout : a.z);
@@ -683,7 +685,7 @@ __global__ void __launch_bounds__(kCThreads) bcd_carry_staged_kernel(const BwdAr
         }
     };
 
-    const int64_t m_first = t_begin / kTB, m_last = (t_end - 1) / kTB;
+    const int64_t m_first = t_begin / kCTB, m_last = (t_end - 1) / kCTB;
     const int64_t nblk = m_last - m_first + 1;
 #pragma unroll
     for (int s = 0; s < kCStages - 1; ++s) {
@@ -700,9 +702,9 @@ __global__ void __launch_bounds__(kCThreads) bcd_carry_staged_kernel(const BwdAr
         __syncthreads();   // block m's copies (every lane's) have landed
         const unsigned char* base = smem + (i % kCStages) * kCBuf;
         const T* dls = reinterpret_cast<const T*>(base + kCRows);
-        const T* gos = dls + kTB * kCCh;
-        const T* zs = gos + kTB * kCCh;
-        const int cnt = t_end - m * kTB < kTB ? static_cast<int>(t_end - m * kTB) : kTB;
+        const T* gos = dls + kCTB * kCCh;
+        const T* zs = gos + kCTB * kCCh;
+        const int cnt = t_end - m * kCTB < kCTB ? static_cast<int>(t_end - m * kCTB) : kCTB;
         for (int j = cnt - 1; j >= 0; --j) {
             float dt = __bfloat162float(dls[j * kCCh + c]) + bias;
             if constexpr (SOFTPLUS) dt = softplus(dt);
