@@ -91,7 +91,9 @@ __device__ __forceinline__ void st_row(T* p, const float (&v)[kN]) {
     }
 }
 
-__device__ __forceinline__ float sigmoid(float v) { return 1.f / (1.f + __expf(-v)); }
+// (a fast quotient: the denominator is at least 1; where it exceeds 2^126 the
+// quotient, then 0, is below the smallest normal float anyway)
+__device__ __forceinline__ float sigmoid(float v) { return __fdividef(1.f, 1.f + __expf(-v)); }
 
 // silu'(z) = sigmoid(z) (1 + z (1 - sigmoid(z)))
 __device__ __forceinline__ float dsilu(float z) {

@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(cons
             if constexpr (GATE) {
                 const float2 zp = lds_pair(in + Sm::kZ + tt * kBwdChannels + pc);
                 const float zo = j ? zp.y : zp.x;   // z of the own channel
-                const float sg = 1.f / (1.f + __expf(-zo));
+                const float sg = __fdividef(1.f, 1.f + __expf(-zo));
                 gate_ds = sg * fmaf(zo, 1.f - sg, 1.f);
                 dy[0] *= zo * sg;
             }
@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(cons
                     if constexpr (SOFTPLUS) {
                         const float2 dp = lds_pair(in + Sm::kDelta + tt * kBwdChannels + pc);
                         const float v = (j ? dp.y : dp.x) + bias[0];
-                        dd = ddt / (1.f + __expf(-v));
+                        dd = __fdividef(ddt, 1.f + __expf(-v));
                     }
                     st_io(static_cast<T*>(a.ddelta) + e, dd);
                     if constexpr (GATE)
