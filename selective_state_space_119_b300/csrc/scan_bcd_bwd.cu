@@ -418,14 +418,15 @@ __global__ void __launch_bounds__(kGThreads, 1) bcd_grad_staged_kernel(const Bwd
         unsigned char* base = smem + buf * kSBuf;
         const int64_t u0 = m * kTB;
         const int cnt = t_end - u0 < kTB ? static_cast<int>(t_end - u0) : kTB;
+        const int64_t rstride = a.dim * kN, roff = ((b * a.L + u0) * a.dim + d) * kN + q0;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
             const T* g = static_cast<const T*>(which ? a.C : a.B);
+            const T* src = g + roff;
 #pragma unroll
-            for (int j = 0; j < kTB; ++j) {
-                const bool valid = j < cnt && c < nch;
-                const T* src = g + (valid ? ((b * a.L + u0 + j) * a.dim + dbase + c) * kN + q0 : 0);
-                cp16(base + which * kSRows + j * (kThreads * 32) + row_piece(c, half), src, valid);
+            for (int j = 0; j < kTB; ++j, src += rstride) {
+                const bool valid = j < cnt && ch_ok;
+                cp16(base + which * kSRows + j * (kThreads * 32) + row_piece(c, half), valid ? src : g, valid);
             }
         }
         // x, delta (lanes 0..127) and z, dout (lanes 128..255): channels
@@ -618,45 +619,44 @@ __global__ void __launch_bounds__(kGThreads, 1) bcd_grad_staged_kernel(const Bwd
 }
 
 // The reverse carry for bf16 rows, staged through shared memory: the same
-// recurrence as bcd_carry_kernel. Each 4-token block's C rows and delta, dout
-// and z rows of 64 channels are copied with cp.async, three blocks in flight
-// per CTA; two lanes per channel, 8 states each, and each lane forms its
-// channel's dt and dy itself. 28.5 KB of shared memory: up to seven CTAs per
-// SM, so that a pass of a few CTAs per SM runs in one wave (8-token blocks,
-// 57 KB and three CTAs per SM, left a second, partial wave).
-constexpr int kCCh = 64;                               // channels per CTA
+// recurrence as bcd_carry_kernel, one lane per channel with all 16 states.
+// Each 4-token block's C rows and delta, dout and z rows of 128 channels are
+// copied with cp.async, three blocks in flight per CTA (57 KB of shared
+// memory, three CTAs per SM). A lane reads its channel's C row as two 16-byte
+// pieces whose order alternates every 4 channels, so that the 8 lanes of a
+// quarter-warp cover all 32 banks. (Two lanes per channel, 8 states each,
+// executed three times the instructions per channel and token: each lane
+// repeated the channel's softplus and SiLU.)
+constexpr int kCCh = 128;                              // channels per CTA, one per lane
 constexpr int kCTB = 4;                                // tokens per block
-constexpr int kCThreads = 2 * kCCh;
 constexpr int kCStages = 3;
-constexpr int kCRows = kCTB * kCCh * kN * 2;            // a block's C rows, bytes
-constexpr int kCScal = kCTB * kCCh * 2;                 // a block's delta (dout, z) rows
+constexpr int kCRows = kCTB * kCCh * kN * 2;           // a block's C rows, bytes
+constexpr int kCScal = kCTB * kCCh * 2;                // a block's delta (dout, z) rows
 constexpr int kCBuf = kCRows + 3 * kCScal;
 constexpr int kCarrySmem = kCStages * kCBuf;
 
+__device__ __forceinline__ int crow_piece(int ch, int h) { return ch * 32 + ((h ^ ((ch >> 2) & 1)) << 4); }
+
 template <bool SOFTPLUS, bool GATE>
-__global__ void __launch_bounds__(kCThreads) bcd_carry_staged_kernel(const BwdArgs a, int64_t ctiles) {
+__global__ void __launch_bounds__(kCCh) bcd_carry_staged_kernel(const BwdArgs a, int64_t ctiles) {
     using T = __nv_bfloat16;
     extern __shared__ __align__(16) unsigned char smem[];
     const int tid = threadIdx.x;
-    const int c = tid >> 1, half = tid & 1;
     const int64_t lin = blockIdx.x;   // ((k - 1) * batch + b) * ctiles + tile
     const int64_t tile = lin % ctiles;
     const int64_t b = (lin / ctiles) % a.batch;
     const int64_t k = 1 + lin / (ctiles * a.batch);
     const int64_t dbase = tile * kCCh;
     const int nch = a.dim - dbase < kCCh ? static_cast<int>(a.dim - dbase) : kCCh;
-    const bool ch_ok = c < nch;
-    const int64_t d = ch_ok ? dbase + c : dbase;
+    const bool ch_ok = tid < nch;
+    const int64_t d = ch_ok ? dbase + tid : dbase;
     const int64_t t_begin = k * a.chunk_len;
     const int64_t t_end = min(a.L, t_begin + a.chunk_len);
-    const int q0 = kNH * half;
-    constexpr int kP2 = kNH / 2;
 
-    float2 A2[kP2], Q[kP2];
+    float2 A2[kN / 2], Q[kN / 2];
 #pragma unroll
-    for (int p = 0; p < kP2; ++p) {
-        A2[p] = make_float2(__ldg(a.A + d * kN + q0 + 2 * p) * kLog2e,
-                            __ldg(a.A + d * kN + q0 + 2 * p + 1) * kLog2e);
+    for (int p = 0; p < kN / 2; ++p) {
+        A2[p] = make_float2(__ldg(a.A + d * kN + 2 * p) * kLog2e, __ldg(a.A + d * kN + 2 * p + 1) * kLog2e);
         Q[p] = make_float2(0.f, 0.f);
     }
     const float bias = a.delta_bias ? __ldg(a.delta_bias + d) : 0.f;
@@ -666,17 +666,21 @@ __global__ void __launch_bounds__(kCThreads) bcd_carry_staged_kernel(const BwdAr
         const int64_t u0 = m * kCTB;
         const int cnt = t_end - u0 < kCTB ? static_cast<int>(t_end - u0) : kCTB;
         const T* Cg = static_cast<const T*>(a.C);
-        // C rows: token j, channel ch, piece h: 8 tokens x 64 channels x 2
+        // C rows: lane tid copies piece tid & 1 of channels tid / 2 and 64 + tid / 2
+        // of every token (consecutive lanes, consecutive global bytes)
+        const int h = tid & 1, chp = tid >> 1;
+        const T* rowsrc = Cg + ((b * a.L + u0) * a.dim + dbase) * kN + h * 8;
 #pragma unroll
-        for (int i = 0; i < kCTB * kCCh * 2 / kCThreads; ++i) {
-            const int piece = i * kCThreads + tid, j = piece / (kCCh * 2), r = piece % (kCCh * 2);
-            const int ch = r >> 1, h = r & 1;
-            const bool valid = j < cnt && ch < nch;
-            const T* src = Cg + (valid ? ((b * a.L + u0 + j) * a.dim + dbase + ch) * kN + h * 8 : 0);
-            cp16(base + piece * 16, src, valid);
+        for (int j = 0; j < kCTB; ++j, rowsrc += a.dim * kN) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int ch = half * (kCCh / 2) + chp;
+                const bool valid = j < cnt && ch < nch;
+                cp16(base + j * (kCCh * 32) + crow_piece(ch, h), valid ? rowsrc + ch * kN : Cg, valid);
+            }
         }
-        // delta, dout, z: 3 arrays x 8 tokens x 8 pieces of 8 channels
-        for (int piece = tid; piece < 3 * kCTB * (kCCh / 8); piece += kCThreads) {
+        // delta, dout, z: 3 arrays x 4 tokens x 16 pieces of 8 channels
+        for (int piece = tid; piece < 3 * kCTB * (kCCh / 8); piece += kCCh) {
             const int which = piece / (kCTB * (kCCh / 8)), r = piece % (kCTB * (kCCh / 8));
             if (!GATE && which == 2) continue;
             const int j = r / (kCCh / 8), c8 = (r % (kCCh / 8)) * 8;
@@ -708,15 +712,17 @@ __global__ void __launch_bounds__(kCThreads) bcd_carry_staged_kernel(const BwdAr
         const T* zs = gos + kCTB * kCCh;
         const int cnt = t_end - m * kCTB < kCTB ? static_cast<int>(t_end - m * kCTB) : kCTB;
         for (int j = cnt - 1; j >= 0; --j) {
-            float dt = __bfloat162float(dls[j * kCCh + c]) + bias;
+            float dt = __bfloat162float(dls[j * kCCh + tid]) + bias;
             if constexpr (SOFTPLUS) dt = softplus(dt);
-            float dy = __bfloat162float(gos[j * kCCh + c]);
-            if constexpr (GATE) dy *= silu(__bfloat162float(zs[j * kCCh + c]));
-            const uint4 u = *reinterpret_cast<const uint4*>(base + (j * kCCh + c) * 32 + half * 16);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            float dy = __bfloat162float(gos[j * kCCh + tid]);
+            if constexpr (GATE) dy *= silu(__bfloat162float(zs[j * kCCh + tid]));
+            const unsigned char* rowp = base + j * (kCCh * 32);
+            const uint4 u0v = *reinterpret_cast<const uint4*>(rowp + crow_piece(tid, 0));
+            const uint4 u1v = *reinterpret_cast<const uint4*>(rowp + crow_piece(tid, 1));
+            const uint32_t w[8] = {u0v.x, u0v.y, u0v.z, u0v.w, u1v.x, u1v.y, u1v.z, u1v.w};
             const float2 dt2 = make_float2(dt, dt), dy2 = make_float2(dy, dy);
 #pragma unroll
-            for (int p = 0; p < kP2; ++p) {
+            for (int p = 0; p < kN / 2; ++p) {
                 const float2 cc = make_float2(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xffff0000u));
                 const float2 arg = __fmul2_rn(A2[p], dt2);
                 Q[p] = __fmul2_rn(make_float2(ex2(arg.x), ex2(arg.y)), __ffma2_rn(dy2, cc, Q[p]));
@@ -728,8 +734,8 @@ __global__ void __launch_bounds__(kCThreads) bcd_carry_staged_kernel(const BwdAr
     if (!ch_ok) return;
     const int64_t idx = (b * (a.nchunks - 1) + (k - 1)) * a.dim + d;
 #pragma unroll
-    for (int p = 0; p < kP2; ++p) *reinterpret_cast<float2*>(a.wsQ + idx * kN + q0 + 2 * p) = Q[p];
-    if (half == 0) a.wsS[idx] = dt_sum;
+    for (int p = 0; p < kN / 2; ++p) *reinterpret_cast<float2*>(a.wsQ + idx * kN + 2 * p) = Q[p];
+    a.wsS[idx] = dt_sum;
 }
 
 // dA, dD, dbias: the shares of every (batch row, chunk), added in order.
@@ -786,7 +792,7 @@ cudaError_t launch_flags(const BwdArgs& a, cudaStream_t s) {
         if constexpr (kStaged) {
             const int64_t ctiles = (a.dim + kCCh - 1) / kCCh;
             bcd_carry_staged_kernel<SOFTPLUS, GATE>
-                <<<static_cast<unsigned>(ctiles * a.batch * (a.nchunks - 1)), kCThreads, kCarrySmem, s>>>(
+                <<<static_cast<unsigned>(ctiles * a.batch * (a.nchunks - 1)), kCCh, kCarrySmem, s>>>(
                     a, ctiles);
         } else {
             bcd_carry_kernel<T, SOFTPLUS, GATE>
