@@ -142,29 +142,32 @@ __device__ __forceinline__ void stage_block(const BwdArgs& a, T* in, int64_t b, 
                                             int64_t u0, int cnt) {
     using Sm = BwdSmem<T, N, TB>;
     constexpr int VEC = Sm::VEC, ROWC = Sm::ROWC;
-    constexpr int NTILES = 4;
-    constexpr int TILE_CHUNKS = TB * ROWC;
+    constexpr int RSTEP = kBwdThreads / ROWC;              // rows per pass of the CTA
     constexpr int BC_CHUNKS = TB * N / VEC;                  // per B or C
-    constexpr int TOTAL = NTILES * TILE_CHUNKS + 2 * BC_CHUNKS;
-    for (int i = threadIdx.x; i < TOTAL; i += kBwdThreads) {
-        if (i < NTILES * TILE_CHUNKS) {
-            const int which = i / TILE_CHUNKS, r = i % TILE_CHUNKS;
-            if (!GATE && which == 2) continue;
-            const int tt = r / ROWC, c = (r % ROWC) * VEC;
-            const void* base = which == 0 ? a.x : which == 1 ? a.delta : which == 2 ? a.z : a.dout;
-            const bool valid = tt < cnt && dbase + c < a.dim;
-            const T* src = static_cast<const T*>(base) +
-                           (valid ? (b * a.L + u0 + tt) * a.dim + dbase + c : 0);
-            cp_async16(in + which * Sm::TILE + tt * kBwdChannels + c, src, valid);
-        } else {
-            const int r = i - NTILES * TILE_CHUNKS;
-            const int which = r / BC_CHUNKS, e = (r % BC_CHUNKS) * VEC;
-            const int tt = e / N, n = e % N;
-            const bool valid = tt < cnt;
-            const T* src = static_cast<const T*>(which ? a.C : a.B) +
-                           (valid ? (b * a.L + u0 + tt) * N + n : 0);
-            cp_async16(in + (which ? Sm::kC : Sm::kB) + e, src, valid);
+    static_assert(kBwdThreads % ROWC == 0 && TB % RSTEP == 0, "whole rows per pass");
+    // the tiles: lane tid copies piece tid mod ROWC of rows tid / ROWC, + RSTEP, ...
+    // of each (pointers stepped per row, not recomputed per piece)
+    const int cc = (threadIdx.x % ROWC) * VEC, r0 = threadIdx.x / ROWC;
+    const bool c_ok = dbase + cc < a.dim;
+    const int64_t off = (b * a.L + u0 + r0) * a.dim + dbase + cc;
+#pragma unroll
+    for (int which = 0; which < 4; ++which) {
+        if (!GATE && which == 2) continue;
+        const T* g = static_cast<const T*>(which == 0 ? a.x : which == 1 ? a.delta : which == 2 ? a.z : a.dout);
+        const T* src = g + off;
+#pragma unroll
+        for (int r = r0, i = 0; i < TB / RSTEP; ++i, r += RSTEP, src += RSTEP * a.dim) {
+            const bool valid = r < cnt && c_ok;
+            cp_async16(in + which * Sm::TILE + r * kBwdChannels + cc, valid ? src : g, valid);
         }
+    }
+    // the TB rows of B and C (N values each)
+    for (int i = threadIdx.x; i < 2 * BC_CHUNKS; i += kBwdThreads) {
+        const int which = i / BC_CHUNKS, e = (i % BC_CHUNKS) * VEC;
+        const int tt = e / N, n = e % N;
+        const bool valid = tt < cnt;
+        const T* g = static_cast<const T*>(which ? a.C : a.B);
+        cp_async16(in + (which ? Sm::kC : Sm::kB) + e, valid ? g + (b * a.L + u0 + tt) * N + n : g, valid);
     }
     cp_async_commit();
 }
@@ -592,23 +595,29 @@ __global__ void __launch_bounds__(kBwdThreads, 4) carry16_kernel(const BwdArgs a
         T* in = reinterpret_cast<T*>(smem + buf * Sm::BYTES);
         const int64_t u0 = t_begin + static_cast<int64_t>(blk) * TB;
         const int cnt = static_cast<int>(t_end - u0 < TB ? t_end - u0 : TB);
-        constexpr int TILE_CHUNKS = TB * ROWC, C_CHUNKS = TB * N / VEC;
-        for (int i = tid; i < 3 * TILE_CHUNKS + C_CHUNKS; i += kBwdThreads) {
-            if (i < 3 * TILE_CHUNKS) {
-                const int which = i / TILE_CHUNKS, r = i % TILE_CHUNKS;
-                if (!GATE && which == 2) continue;
-                const int tt = r / ROWC, c = (r % ROWC) * VEC;
-                const void* g = which == 0 ? a.delta : which == 1 ? a.dout : a.z;
-                const bool valid = tt < cnt && dbase + c < a.dim;
-                const T* src = static_cast<const T*>(g) +
-                               (valid ? (b * a.L + u0 + tt) * a.dim + dbase + c : 0);
-                cp_async16(in + which * Sm::TILE + tt * kBwdChannels + c, src, valid);
-            } else {
-                const int e = (i - 3 * TILE_CHUNKS) * VEC, tt = e / N, n = e % N;
-                const bool valid = tt < cnt;
-                const T* src = static_cast<const T*>(a.C) + (valid ? (b * a.L + u0 + tt) * N + n : 0);
-                cp_async16(in + Sm::kC + e, src, valid);
+        constexpr int RSTEP = kBwdThreads / ROWC, C_CHUNKS = TB * N / VEC;
+        static_assert(kBwdThreads % ROWC == 0 && TB % RSTEP == 0, "whole rows per pass");
+        // lane tid copies piece tid mod ROWC of rows tid / ROWC, + RSTEP, ... of
+        // each tile (pointers stepped per row)
+        const int cc = (tid % ROWC) * VEC, r0 = tid / ROWC;
+        const bool c_ok = dbase + cc < a.dim;
+        const int64_t off = (b * a.L + u0 + r0) * a.dim + dbase + cc;
+#pragma unroll
+        for (int which = 0; which < 3; ++which) {
+            if (!GATE && which == 2) continue;
+            const T* g = static_cast<const T*>(which == 0 ? a.delta : which == 1 ? a.dout : a.z);
+            const T* src = g + off;
+#pragma unroll
+            for (int r = r0, k2 = 0; k2 < TB / RSTEP; ++k2, r += RSTEP, src += RSTEP * a.dim) {
+                const bool valid = r < cnt && c_ok;
+                cp_async16(in + which * Sm::TILE + r * kBwdChannels + cc, valid ? src : g, valid);
             }
+        }
+        for (int i = tid; i < C_CHUNKS; i += kBwdThreads) {
+            const int e = i * VEC, tt = e / N, n = e % N;
+            const bool valid = tt < cnt;
+            const T* Cg = static_cast<const T*>(a.C);
+            cp_async16(in + Sm::kC + e, valid ? Cg + (b * a.L + u0 + tt) * N + n : Cg, valid);
         }
     };
     // the ring: kCarryStages - 1 blocks ahead, one commit group per block
