@@ -738,26 +738,43 @@ __global__ void __launch_bounds__(kCCh) bcd_carry_staged_kernel(const BwdArgs a,
     a.wsS[idx] = dt_sum;
 }
 
-// dA, dD, dbias: the shares of every (batch row, chunk), added in order.
+// dA, dD, dbias: the shares of every (batch row, chunk), added in a fixed
+// order. An output is a lane quad's: lane p of the quad adds rows p, p + 4,
+// ..., and two xor exchanges add the four partial sums (the same bits in every
+// lane: float addition commutes). The quads' range, 4 (16 + 2) dim, is a
+// multiple of 32 (dim is a multiple of 4), so a quad is always whole.
 __global__ void __launch_bounds__(256) bcd_bwd_reduce_kernel(const BwdArgs a) {
     const int64_t nA = a.dim * kN, nd = a.dim;
-    const int64_t total = nA + 2 * nd, rows = a.batch * a.nchunks;
+    const int64_t total = 4 * (nA + 2 * nd), rows = a.batch * a.nchunks;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        if (i < nA) {
-            float s = 0.f;
-            for (int64_t r = 0; r < rows; ++r) s += a.pA[r * nA + i];
-            a.dA[i] = s;
+        const int64_t o = i >> 2;
+        const int part = static_cast<int>(i & 3);
+        const float* src;
+        int64_t stride;
+        if (o < nA) {
+            src = a.pA + o;
+            stride = nA;
+        } else if (o < nA + nd) {
+            src = a.pD + (o - nA);
+            stride = nd;
         } else {
-            const int64_t e = i - nA;
-            const bool is_bias = e >= nd;
-            float* out = is_bias ? a.dbias : a.dD;
-            if (!out) continue;
-            const int64_t dd = is_bias ? e - nd : e;
-            const float* part = is_bias ? a.pbias : a.pD;
-            float s = 0.f;
-            for (int64_t r = 0; r < rows; ++r) s += part[r * nd + dd];
-            out[dd] = s;
+            src = a.pbias + (o - nA - nd);
+            stride = nd;
+        }
+        float s = 0.f;
+        for (int64_t r = part; r < rows; r += 4) s += src[r * stride];
+        const unsigned mask = __activemask();
+        s += __shfl_xor_sync(mask, s, 1);
+        s += __shfl_xor_sync(mask, s, 2);
+        if (part == 0) {
+            if (o < nA)
+                a.dA[o] = s;
+            else if (o < nA + nd) {
+                if (a.dD) a.dD[o - nA] = s;
+            } else if (a.dbias) {
+                a.dbias[o - nA - nd] = s;
+            }
         }
     }
 }
@@ -805,7 +822,7 @@ cudaError_t launch_flags(const BwdArgs& a, cudaStream_t s) {
     else
         bcd_grad_kernel<T, SOFTPLUS, GATE>
             <<<static_cast<unsigned>(per_chunk * a.nchunks), kThreads, kGradSmem, s>>>(a);
-    const int64_t total = a.dim * kN + 2 * a.dim;
+    const int64_t total = 4 * (a.dim * kN + 2 * a.dim);
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, 148 * 16);
     bcd_bwd_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
     return cudaGetLastError();

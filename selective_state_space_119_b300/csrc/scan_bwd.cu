@@ -676,11 +676,16 @@ __global__ void __launch_bounds__(kBwdThreads, 4) carry16_kernel(const BwdArgs a
 }
 
 // The sums over channel tiles (dB, dC) and over batch rows and chunks (dA, dD,
-// dbias) of the per-CTA shares, added in a fixed order.
+// dbias) of the per-CTA shares, added in a fixed order. A dB | dC output is
+// one thread's sum over the tiles; a dA, dD or dbias output is a lane quad's:
+// lane p of the quad adds rows p, p + 4, ..., and two xor exchanges add the
+// four partial sums (the same bits in every lane: float addition commutes).
 template <typename T, int N>
 __global__ void __launch_bounds__(256) scan_bwd_reduce_kernel(const BwdArgs a) {
     const int64_t nBC = a.batch * a.L * 2 * N, nA = a.dim * N, nd = a.dim;
-    const int64_t total = nBC + nA + 2 * nd;
+    // nBC and the quads' range are multiples of 32: a warp never straddles
+    // the two, and a quad is always whole
+    const int64_t total = nBC + 4 * (nA + 2 * nd);
     const int64_t rows = a.batch * a.nchunks;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -691,21 +696,35 @@ __global__ void __launch_bounds__(256) scan_bwd_reduce_kernel(const BwdArgs a) {
             for (int64_t tile = 0; tile < a.tiles; ++tile)
                 s += a.pBC[((b * a.tiles + tile) * a.L + t) * (2 * N) + c];
             st_io(static_cast<T*>(c < N ? a.dB : a.dC) + bt * N + (c % N), s);
-        } else if (i < nBC + nA) {
-            const int64_t e = i - nBC;
-            float s = 0.f;
-            for (int64_t r = 0; r < rows; ++r) s += a.pA[r * nA + e];
-            a.dA[e] = s;
         } else {
-            const int64_t e = i - nBC - nA;
-            const bool is_bias = e >= nd;
-            const int64_t dd = is_bias ? e - nd : e;
-            float* out = is_bias ? a.dbias : a.dD;
-            if (!out) continue;
-            const float* part = is_bias ? a.pbias : a.pD;
+            const int64_t q = i - nBC, o = q >> 2;
+            const int part = static_cast<int>(q & 3);
+            const float* src;
+            int64_t stride;
+            if (o < nA) {
+                src = a.pA + o;
+                stride = nA;
+            } else if (o < nA + nd) {
+                src = a.pD + (o - nA);
+                stride = nd;
+            } else {
+                src = a.pbias + (o - nA - nd);
+                stride = nd;
+            }
             float s = 0.f;
-            for (int64_t r = 0; r < rows; ++r) s += part[r * nd + dd];
-            out[dd] = s;
+            for (int64_t r = part; r < rows; r += 4) s += src[r * stride];
+            const unsigned mask = __activemask();
+            s += __shfl_xor_sync(mask, s, 1);
+            s += __shfl_xor_sync(mask, s, 2);
+            if (part == 0) {
+                if (o < nA)
+                    a.dA[o] = s;
+                else if (o < nA + nd) {
+                    if (a.dD) a.dD[o - nA] = s;
+                } else if (a.dbias) {
+                    a.dbias[o - nA - nd] = s;
+                }
+            }
         }
     }
 }
@@ -766,7 +785,7 @@ cudaError_t launch_flags(const BwdArgs& a, cudaStream_t s) {
     e = a.zoh ? launch_grad<T, N, SOFTPLUS, GATE, true>(a, per_chunk * a.nchunks, s)
               : launch_grad<T, N, SOFTPLUS, GATE, false>(a, per_chunk * a.nchunks, s);
     if (e != cudaSuccess) return e;
-    const int64_t total = a.batch * a.L * 2 * N + a.dim * N + 2 * a.dim;
+    const int64_t total = a.batch * a.L * 2 * N + 4 * (a.dim * N + 2 * a.dim);
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, 148 * 16);
     scan_bwd_reduce_kernel<T, N><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
     return cudaGetLastError();
