@@ -27,9 +27,9 @@ namespace ssm {
 namespace {
 
 constexpr int kBcdThreads = 128;    // = the 128-channel tile of configuration 0
-// tokens of loads in flight per lane: the chunk-state and checkpoint passes
-// read no C (half the bytes per token), so they keep twice as many tokens in
-// flight; fp32 rows are twice as wide as bf16 ones
+// tokens of loads in flight per lane: the chunk-state pass reads no C (half
+// the bytes per token), so it keeps twice as many tokens in flight; fp32 rows
+// are twice as wide as bf16 ones
 template <typename T, int MODE>
 struct RingTokens {
     static constexpr int value = (sizeof(T) == 2 ? 4 : 2) * (MODE == 1 ? 1 : 2);
@@ -90,18 +90,23 @@ struct Slot {
 };
 
 // MODE 1: the output pass (composes the chunk carries, writes y and the final
-// state); MODE 0: the chunk-state pass (end state from 0 and sum of dt of
-// every chunk but the last); MODE 2: the checkpoint pass of the training
-// forward (composes the carries like the output pass, reads what the
-// chunk-state pass reads, and saves the state before every kCkptTokens-th
-// token for the backward). Saving the states from the output pass itself ran
-// 2.4 times slower than the plain output pass; this pass costs one more read of
-// x, delta and B instead. One lane = one channel.
-template <typename T, int N, int MODE, bool SOFTPLUS, bool GATE>
+// state; with CKPT, the training forward's, it also saves the state before
+// every kCkptTokens-th token for the backward); MODE 0: the chunk-state pass
+// (end state from 0 and sum of dt of every chunk but the last). One lane = one
+// channel. The saving pass walks whole groups of kCkptTokens tokens, the save
+// at a fixed position of the unrolled group: a save behind a per-token test of
+// the token index split the token body and ran the pass 3x slower, and a
+// separate pass that re-read x, delta and B cost 111 us on b4 L2048 d1536
+// against the 74 us the in-pass saves add.
+template <typename T, int N, int MODE, bool SOFTPLUS, bool GATE, bool CKPT = false>
 __global__ void __launch_bounds__(kBcdThreads) scan_bcd_kernel(const ScanArgs a) {
     constexpr bool WITH_C = MODE == 1, WITH_Z = MODE == 1 && GATE;
     using S = Slot<T, N, WITH_C, WITH_Z>;
     constexpr int kRing = RingTokens<T, MODE>::value;
+    // the token loop walks whole groups of kCkptTokens (the ring reused), so
+    // that a saved state sits at a fixed position of the unrolled group
+    constexpr int kGroup = CKPT ? kCkptTokens : kRing;
+    static_assert(kGroup % kRing == 0, "whole rings per group");
     const int64_t lin = blockIdx.x;   // chunk-major: ((k * batch) + b) * tiles + tile
     const int64_t tile = lin % a.tiles;
     const int64_t b = (lin / a.tiles) % a.batch;
@@ -157,15 +162,16 @@ __global__ void __launch_bounds__(kBcdThreads) scan_bcd_kernel(const ScanArgs a)
     for (int u = 0; u < kRing; ++u) load(ring[u], t_begin + u);
 
     float dt_sum = 0.f;
-    for (int64_t t0 = t_begin; t0 < t_end; t0 += kRing) {
+    for (int64_t t0 = t_begin; t0 < t_end; t0 += kGroup) {
 #pragma unroll
-        for (int u = 0; u < kRing; ++u) {
+        for (int u = 0; u < kGroup; ++u) {
             const int64_t t = t0 + u;
-            const S cur = ring[u];
-            load(ring[u], t + kRing);   // the loads of a later token, in flight meanwhile
+            const S cur = ring[u % kRing];
+            load(ring[u % kRing], t + kRing);   // the loads of a later token, in flight meanwhile
             const bool valid = ch_ok && t < t_end;
-            if constexpr (MODE == 2) {
-                if (valid && t % kCkptTokens == 0) {
+            if constexpr (CKPT) {
+                // chunks start on a checkpoint: t0 is one, the state before token t0
+                if (u == 0 && valid) {
                     float4* ck = reinterpret_cast<float4*>(
                         a.ckpt + ((b * a.nckpt + t / kCkptTokens) * a.dim + d) * N);
 #pragma unroll
@@ -220,10 +226,11 @@ cudaError_t launch_flags(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
     if (p.nchunks > 1)
         scan_bcd_kernel<T, N, 0, SOFTPLUS, false>
             <<<static_cast<unsigned>(per_chunk * (p.nchunks - 1)), kBcdThreads, 0, s>>>(a);
-    scan_bcd_kernel<T, N, 1, SOFTPLUS, GATE>
-        <<<static_cast<unsigned>(per_chunk * p.nchunks), kBcdThreads, 0, s>>>(a);
     if (a.ckpt)
-        scan_bcd_kernel<T, N, 2, SOFTPLUS, false>
+        scan_bcd_kernel<T, N, 1, SOFTPLUS, GATE, true>
+            <<<static_cast<unsigned>(per_chunk * p.nchunks), kBcdThreads, 0, s>>>(a);
+    else
+        scan_bcd_kernel<T, N, 1, SOFTPLUS, GATE>
             <<<static_cast<unsigned>(per_chunk * p.nchunks), kBcdThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
