@@ -74,6 +74,45 @@ def test_input_stage_gradients(torch, io, K, bias, L):
     summed(G.host64(db), ref["dbias"], "dconv_b K %d L %d" % (K, L))
 
 
+@pytest.mark.parametrize("io,K", [("bf16", 4), ("f32", 3)])
+def test_input_stage_gradients_guard_bands(torch, io, K):
+    """dx, dconv_w and dconv_b written into the middle of pattern-filled
+    buffers through the C ABI (a ragged last token tile and channel tile): the
+    bands before and after stay untouched, and the values match the oracle."""
+    import ctypes
+    from selective_state_space_119_b300 import libssm
+    t = torch
+    batch, L, dim = 2, 77, 264
+    x, w, b, du = _case(batch, L, dim, K, io, True, 211 + K)
+    xd, wd, bd, dud = G.dev(x), G.dev(w), G.dev(b), G.dev(du)
+    pad = 4096
+
+    def guarded(n, dtype, fill):
+        big = t.full((pad + n + pad,), fill, dtype=dtype, device="cuda")
+        return big, big[pad:pad + n]
+
+    big_dx, dx = guarded(batch * L * dim, xd.dtype, 3.0)
+    big_dw, dw = guarded(dim * K, t.float32, -5.0)
+    big_db, db = guarded(dim, t.float32, -5.0)
+    code = libssm.SSM_BF16 if io == "bf16" else libssm.SSM_F32
+    dims = libssm.make_dims(batch, L, dim, 16, code)
+    nb = int(libssm.lib.ssm_causal_conv1d_silu_bwd_workspace_bytes(ctypes.byref(dims), K))
+    ws = t.full((nb,), 0x5A, dtype=t.uint8, device="cuda")
+    dims = libssm.make_dims(batch, L, dim, 16, code, ws.data_ptr(), nb)
+    p = lambda v: ctypes.c_void_p(v.data_ptr())
+    rc = libssm.lib.ssm_causal_conv1d_silu_bwd(p(xd), p(wd), p(bd), K, p(dud), p(dx), p(dw), p(db),
+                                               ctypes.byref(dims), None)
+    assert rc == libssm.SSM_OK
+    t.cuda.synchronize()
+    for big, fill, name in ((big_dx, 3.0, "dx"), (big_dw, -5.0, "dconv_w"), (big_db, -5.0, "dconv_b")):
+        assert t.all(big[:pad] == fill) and t.all(big[-pad:] == fill), name + " band written"
+    ref = oracle.causal_conv1d_silu_bwd(I.widen(x), np.asarray(w, np.float64), I.widen(du),
+                                        bias=np.asarray(b, np.float64))
+    elem(G.host64(dx.view(batch, L, dim)), ref["dx"], io, "guarded dx")
+    summed(G.host64(dw.view(dim, K)), ref["dw"], "guarded dconv_w")
+    summed(G.host64(db), ref["dbias"], "guarded dconv_b")
+
+
 def test_input_stage_gradients_full_size(torch):
     """The input-stage benchmark's shapes (batch 4, L 2048, dim 1536, width 4),
     every element of dx and every weight; and bit-identical on a repeat."""
