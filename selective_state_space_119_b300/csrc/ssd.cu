@@ -279,20 +279,17 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 tma_load_4d(sm + oX, &tm_x, 0, hh, c * kQ, bb, bar_X);
                 pend_X = c & 1;
             };
-            load_B(0);
-            load_C(0);
-            load_X(0);
-            for (int c = 0; c < nchunks && ok; ++c) {
-                const uint32_t ph = static_cast<uint32_t>(c & 1);
+            // chunk c's B and C tiles: wait for them, send the next chunk's to
+            // the other buffer (its last readers, the products of chunk c - 1,
+            // have completed) and the tiles after those into L2, then issue
+            // G = C B^T (8 steps of K = 16 over the two 64-wide n blocks). G
+            // needs nothing of the previous chunk's epilogue, so it is issued as
+            // soon as that chunk's products have completed.
+            auto tiles_and_G = [&](int c) -> bool {
                 const int sb = c & 1;
-                const uint32_t oCc = oC + sb * 2 * kBlk, oBc = oB + sb * 2 * kBlk;
-                // this chunk's B and C tiles; then the next chunk's to the other
-                // buffer (its last readers, the previous chunk's products, have
-                // completed) and the tiles after those into L2
                 const uint32_t pb = static_cast<uint32_t>((c >> 1) & 1);
-                ok = mbar_wait_bounded(bar_B + sb, pb, kPolls) &&
-                     mbar_wait_bounded(bar_C + sb, pb, kPolls);
-                if (!ok) break;
+                if (!mbar_wait_bounded(bar_B + sb, pb, kPolls) || !mbar_wait_bounded(bar_C + sb, pb, kPolls))
+                    return false;
                 pend_B[sb] = pend_C[sb] = -1;
                 tc::fence_after_sync();
                 if (c + 1 < nchunks) {
@@ -306,7 +303,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     prefetch_l2_4d(&tm_C, 64, gg, (c + 2) * kQ, bb);
                     prefetch_l2_4d(&tm_x, 0, hh, (c + 1) * kQ, bb);
                 }
-                // G = C B^T: 8 steps of K = 16 over the two 64-wide n blocks
+                const uint32_t oCc = oC + sb * 2 * kBlk, oBc = oB + sb * 2 * kBlk;
 #pragma unroll
                 for (int k = 0; k < kNs / 16; ++k) {
                     const uint32_t off = (k >> 2) * kBlk + (k & 3) * 32;
@@ -314,12 +311,29 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                                  tc::desc_sw128(sbase + oBc + off, 16, 1024), kIdG, k > 0);
                 }
                 tc::mma_commit(bar_G);
-                pend_G = static_cast<int>(ph);
-                // Y2 = C h^T once the previous chunk's epilogue (or the prologue)
-                // has written h: A = C (K-major, K = n), B = h MN-major (rows n)
+                pend_G = c & 1;
+                return true;
+            };
+            load_B(0);
+            load_C(0);
+            load_X(0);
+            ok = tiles_and_G(0);
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const uint32_t ph = static_cast<uint32_t>(c & 1);
+                const int sb = c & 1;
+                const uint32_t oCc = oC + sb * 2 * kBlk, oBc = oB + sb * 2 * kBlk;
+                // the previous chunk's epilogue (or the prologue) has written h
+                // and staged that chunk's y: store y (its read of the staging tile
+                // is awaited once Y2 is issued), then Y2 = C h^T: A = C (K-major,
+                // K = n), B = h MN-major (rows n)
                 ok = mbar_wait_bounded(rdy_E, ph, kPolls);
                 if (!ok) break;
                 tc::fence_after_sync();
+                if (c > 0) {
+                    tma_store_4d(&tm_y, 0, hh, (c - 1) * kQ, bb, sm + oYs);
+                    bulk_commit();
+                    stored = true;
+                }
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
                     const uint32_t hb = sbase + (part ? oHl : oHh);
@@ -330,6 +344,11 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                                      tc::desc_sw128(hb + k * 2048, 1024, 1024), kIdY,
                                      part > 0 || k > 0);
                     }
+                }
+                if (c > 0) {
+                    // hand the staging tile back once the store has read it
+                    bulk_wait_read<0>();
+                    mbar_arrive(free_Y);
                 }
                 // S^T = B^T (w o X) once w o X is written: A = the B tile read
                 // MN-major (M = n over two 64-wide blocks 16 KB apart), B = w o X
@@ -367,20 +386,24 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 }
                 tc::mma_commit(bar_Y);
                 pend_Y = static_cast<int>(ph);
-                // Y is done with the X tile: the next chunk's X can land
+                // the products of this chunk have completed (in issue order): the
+                // X tile, the B, C buffer and G's columns are free for the next
                 ok = mbar_wait_bounded(bar_Y, ph, kPolls);
                 if (!ok) break;
-                pend_G = pend_S = pend_Y = -1;   // (the products complete in issue order)
-                if (c + 1 < nchunks) load_X(c + 1);
-                // the epilogue has staged y: store it, and hand the staging tile
-                // back once the store has read it
-                ok = mbar_wait_bounded(rdy_E, ph ^ 1u, kPolls);
-                if (!ok) break;
-                tma_store_4d(&tm_y, 0, hh, c * kQ, bb, sm + oYs);
-                bulk_commit();
-                stored = true;
-                bulk_wait_read<0>();
-                mbar_arrive(free_Y);
+                pend_G = pend_S = pend_Y = -1;
+                if (c + 1 < nchunks) {
+                    load_X(c + 1);
+                    ok = tiles_and_G(c + 1);
+                }
+            }
+            // the last chunk's y, once its epilogue has staged it
+            if (ok && nchunks > 0) {
+                ok = mbar_wait_bounded(rdy_E, static_cast<uint32_t>(nchunks & 1), kPolls);
+                if (ok) {
+                    tma_store_4d(&tm_y, 0, hh, (nchunks - 1) * kQ, bb, sm + oYs);
+                    bulk_commit();
+                    stored = true;
+                }
             }
             if (stored) bulk_wait_all();
             if (!ok) {
@@ -451,10 +474,14 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         uint4 xrow[kGC / 8];
         load_xrow(0, xrow);
 
-        for (int c = 0; c < nchunks; ++c) {
-            const uint32_t ph = static_cast<uint32_t>(c & 1);
-            // dt of the chunk (0 past the sequence end; loaded a chunk ahead), then
-            // s = A * cumsum(dt), one token per thread of the four dt warps
+        // Phase A of chunk c: dt (0 past the sequence end; loaded a chunk ahead),
+        // s = A * cumsum(dt), one token per thread of the four dt warps, then
+        // w o X (high and remainder) for S^T = B^T (w o X), then the x row of the
+        // chunk after. Every compute warp passes both named barriers whatever
+        // its state (a warp leaving early would hold the others there); the
+        // result is this warp's: false when a wait gave up.
+        float s_end = 0.f;
+        auto phase_a = [&](int c, bool okw) -> bool {
             float cs = 0.f;
             if (dtw >= 0) {
                 float v = 0.f;
@@ -478,13 +505,13 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 ss2[dtok] = cs * A2;   // s_t log2 e
             }
             // (the next write of swarp is a chunk later, after several barriers)
-            if (named_bar_or(1, kCompute, !ok)) {
-                ok = false;
-                break;
-            }
-            const float s_end = ss2[kQ - 1];
-            // w o X (high and remainder): row u = this thread's row, columns of
-            // its group, w_u = exp(s_end - s_u) dt_u; then the next chunk's x row
+            if (named_bar_or(1, kCompute, !okw)) return false;   // the same for every warp
+            s_end = ss2[kQ - 1];
+            // row u = this thread's row, columns of its group, w_u = exp(s_end -
+            // s_u) dt_u, once the previous chunk's S has read the last w o X
+            if (c > 0 &&
+                !__all_sync(0xffffffffu, mbar_wait_bounded(bar_S, static_cast<uint32_t>((c - 1) & 1), kPolls)))
+                return false;
             {
                 const int u = row;
                 const float w = ex2(s_end - ss2[u]) * sdt[u];
@@ -507,17 +534,29 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(rdy_W);
+            return true;
+        };
+
+        // The chunks are software-pipelined: chunk c + 1's phase A runs while
+        // chunk c's Y = M X computes, between chunk c's M and its epilogue.
+        ok = phase_a(0, ok);
+        for (int c = 0; c < nchunks; ++c) {
+            const uint32_t ph = static_cast<uint32_t>(c & 1);
             // M = G o decay o dt + D on the diagonal (so that M X carries D x),
             // row t = this thread's row, high and remainder, while S computes,
             // stored to tensor memory as the A operand of Y = M X. Warp w forms
             // the 32-column block q = w / 4 of rows 32 (w mod 4) ..: blocks
             // q > w mod 4 lie above the diagonal (zero), q < w mod 4 below it (no
-            // mask).
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar_G, ph, kPolls));
+            // mask). (Chunk c - 1's Y, the last reader of M, completed before its
+            // epilogue.)
+            ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(bar_G, ph, kPolls));
             tc::fence_after_sync();
+            // this thread's s_t and s_end of chunk c, for its epilogue after the
+            // next chunk's phase A has overwritten dt and s
+            const float st_c = ss2[row], s_end_c = s_end;
             if (ok) {
                 const int t = row;
-                const float st = ss2[t];
+                const float st = st_c;
                 const int q = grp;
                 uint32_t hw[16], lw[16];
                 if (q > quarter) {
@@ -573,6 +612,12 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 __syncwarp();
                 if (lane == 0) mbar_arrive(rdy_M);
             }
+            // the next chunk's phase A, once every compute warp has read this
+            // chunk's dt and s
+            if (c + 1 < nchunks) {
+                named_bar_sync(1, kCompute);
+                ok = phase_a(c + 1, ok);
+            }
             // epilogue once S and Y (and Y2) have landed: y = Y + exp(s_t) Y2 (row
             // t, the group's 16 columns) into the staging tile; state: h <-
             // exp(s_end) h + S (row n, the group's 16 p)
@@ -583,7 +628,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             tc::fence_after_sync();
             if (ok) {
                 const int t = row;
-                const float et = ex2(ss2[t]);
+                const float et = ex2(st_c);
                 float yv[kGC], y2[kGC];
                 tmem_ld16(tmem + lane_base + kColY + kGC * grp, yv);
                 tmem_ld16(tmem + lane_base + kColY2 + kGC * grp, y2);
@@ -596,7 +641,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                         make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
                                    pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
                 }
-                const float eend = ex2(s_end);
+                const float eend = ex2(s_end_c);
                 float sv[kGC];
                 tmem_ld16(tmem + lane_base + kColS + kGC * grp, sv);
 #pragma unroll
@@ -613,8 +658,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 __syncwarp();
                 if (lane == 0) mbar_arrive(rdy_E);
             }
-            // every compute warp is done with this chunk's dt and s before the
-            // next chunk overwrites them
+            // every compute warp has passed this chunk before the next one starts
             if (named_bar_or(1, kCompute, !ok)) {
                 ok = false;
                 break;
