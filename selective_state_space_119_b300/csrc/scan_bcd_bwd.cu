@@ -16,17 +16,22 @@
 // are formed. dA, dD and dbias sum over batch rows and tokens: every CTA writes
 // its share, and a last kernel adds the shares in a fixed order.
 //
-// Layout: one lane per channel (128 channels per CTA), all 16 states in
-// registers, as in the per-channel forward. The sequence is split into the
-// forward's L-chunks. The carry pass runs the reverse recurrence of every chunk
-// but the first from Q = 0 and keeps its Q at the chunk's first token and its
-// sum of dt; the gradient pass of chunk k starts from dL/dfinal_state and
-// composes the carries of the chunks to its right, Q <- e^{A S_i} Q + Q_i. It
-// then walks its chunk in 8-token blocks from the end: the block's checkpoint
-// (the state before its first token) is reloaded, the block's 8 states are
-// recomputed forward into the lane's own slots of shared memory, and the
-// reverse sweep reads them back. The slots are private to the lane, so the
-// passes need no barrier.
+// The sequence is split into the backward's L-chunks. The carry pass runs the
+// reverse recurrence of every chunk but the first from Q = 0 and keeps its Q
+// at the chunk's first token and its sum of dt; the gradient pass of chunk k
+// starts from dL/dfinal_state and composes the carries of the chunks to its
+// right, Q <- e^{A S_i} Q + Q_i. It then walks its chunk in 8-token blocks from
+// the end: the block's checkpoint (the state before its first token) is
+// reloaded, the block's states are recomputed forward into shared memory, and
+// the reverse sweep reads them back.
+//
+// Two layouts. bf16 rows (the fast path): both passes stage each block's rows
+// through shared memory with cp.async, a block or two ahead (the staged
+// kernels below); the carry has one lane per channel, the gradient pass two (8
+// states each). fp32 rows: one lane per channel, all 16 states in registers,
+// each lane loading its own rows token by token, as in the per-channel forward
+// (bcd_carry_kernel, bcd_grad_kernel); the recomputed states go to the lane's
+// own slots of shared memory, so those passes need no barrier.
 #include <cuda_bf16.h>
 
 #include <algorithm>
