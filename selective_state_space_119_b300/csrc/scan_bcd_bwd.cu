@@ -177,6 +177,8 @@ __global__ void __launch_bounds__(kThreads, 3) bcd_grad_kernel(const BwdArgs a) 
         gA[q] = 0.f;
     }
     // dL/dh at the chunk's last token: the carries of the chunks to the right
+    // (unrolled: their loads do not depend on Q)
+#pragma unroll 4
     for (int64_t i = a.nchunks - 1; i > k; --i) {
         const int64_t idx = (b * (a.nchunks - 1) + (i - 1)) * a.dim + d;
         const float S = a.wsS[idx];
@@ -394,6 +396,8 @@ __global__ void __launch_bounds__(kGThreads, 1) bcd_grad_staged_kernel(const Bwd
         gA[p] = make_float2(0.f, 0.f);
     }
     // dL/dh at the chunk's last token: the carries of the chunks to the right
+    // (unrolled: their loads do not depend on Q)
+#pragma unroll 4
     for (int64_t i = a.nchunks - 1; i > k; --i) {
         const int64_t idx = (b * (a.nchunks - 1) + (i - 1)) * a.dim + d;
         const float S = a.wsS[idx];

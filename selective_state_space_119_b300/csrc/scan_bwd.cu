@@ -221,6 +221,7 @@ __global__ void __launch_bounds__(kBwdThreads, ZOH ? 2 : 3) scan_bwd_kernel(cons
 #pragma unroll
                 for (int q = 0; q < SPL; ++q) Q[r][q] = a.dfinal[(b * a.dim + dr) * N + j * SPL + q];
             }
+#pragma unroll 4
             for (int64_t i = a.nchunks - 1; i > k; --i) {
                 const int64_t idx = (b * (a.nchunks - 1) + (i - 1)) * a.dim + dr;
                 const float S = a.wsS[idx];

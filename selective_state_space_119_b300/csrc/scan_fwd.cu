@@ -332,6 +332,8 @@ scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             for (int q = 0; q < SPL; ++q) h[r][q] = hs[q];
         }
         if (MODE == 1 && k > 0 && ch_ok) {
+            // (unrolled: the carries' loads do not depend on h)
+#pragma unroll 4
             for (int64_t i = 0; i < k; ++i) {
                 const int64_t idx = (b * (a.nchunks - 1) + i) * a.dim + dr;
                 const float S = a.ws_S[idx];
