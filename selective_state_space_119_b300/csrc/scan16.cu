@@ -289,9 +289,6 @@ scan16_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                 }
             }
             // the state entering chunk k: h <- exp(A S_i) h + H_i over chunks 0 .. k-1
-            // (unrolled, so that the loads of several chunks' carries are in flight
-            // at once: they do not depend on h)
-#pragma unroll 4
             for (int64_t i = 0; i < k; ++i) {
                 const int64_t idx = (b * (a.nchunks - 1) + i) * a.dim + dch[c];
                 const float S = a.ws_S[idx];
