@@ -61,7 +61,10 @@ constexpr int kP = 64;      // channels per head
 constexpr int kNs = 128;    // state width
 constexpr int kComputeWarps = 16;         // warps w, w + 4, w + 8, w + 12 share TMEM lane quarter w mod 4
 constexpr int kCompute = 32 * kComputeWarps;
-constexpr int kThreads = kCompute + 32;   // and one producer warp (TMA loads, tensor-core products)
+// and two producer warps: the first issues the TMA loads, G = C B^T, Y = M X and the
+// y stores; the second Y2 = C h^T and S^T = B^T (w o X), so that two threads on two
+// schedulers issue products at once
+constexpr int kThreads = kCompute + 64;
 constexpr int kGroups = kCompute / 128;   // column groups: a thread owns 64 / kGroups columns
 constexpr int kGC = kP / kGroups;         // 16 columns of P per thread
 constexpr uint32_t kPolls = 1u << 24;
@@ -80,7 +83,7 @@ constexpr int oYs = oHl + kBlk;                // y staged for its TMA store: ro
 constexpr int oDt = oYs + kBlk;                // dt [Q] f32
 constexpr int oS2 = oDt + kQ * 4;              // s log2 e [Q] f32
 constexpr int oWs = oS2 + kQ * 4;              // warp partial sums [4] f32
-constexpr int oBar = oWs + 64;                 // 13 mbarriers (loads, products, hand-overs)
+constexpr int oBar = oWs + 64;                 // 14 mbarriers (loads, products, hand-overs)
 constexpr int oTm = oBar + 112;                // TMEM base address
 constexpr int kSmemUsed = oTm + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;   // + alignment slack
@@ -221,10 +224,11 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     uint64_t* rdy_M = bar_B + 10;  // M stored to tensor memory
     uint64_t* rdy_E = bar_B + 11;  // epilogue done: y staged, h written, accumulators read
     uint64_t* free_Y = bar_B + 12; // the y store has read the staging tile
+    uint64_t* bar_D2 = bar_B + 13; // the second producer's abort path
     uint32_t* tm_slot = reinterpret_cast<uint32_t*>(sm + oTm);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool producer = warp == kComputeWarps;
+    const bool producer = warp == kComputeWarps, producer2 = warp == kComputeWarps + 1;
     const int quarter = warp & 3, grp = warp >> 2;
     const int row = 32 * quarter + lane;   // this compute thread's TMEM lane and tile row
     const int64_t b = blockIdx.x / a.H, hd = blockIdx.x % a.H;
@@ -240,6 +244,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         for (int i = 0; i < 9; ++i) mbar_init(bar_B + i, 1);
         for (int i = 9; i < 12; ++i) mbar_init(bar_B + i, kComputeWarps);
         mbar_init(free_Y, 1);
+        mbar_init(bar_D2, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -258,7 +263,7 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             // the barrier phase of each load and product group in flight, -1 for
             // none (the abort path waits for them)
             int pend_B[2] = {-1, -1}, pend_C[2] = {-1, -1};
-            int pend_X = -1, pend_G = -1, pend_S = -1, pend_Y = -1;
+            int pend_X = -1, pend_G = -1, pend_Y = -1;
             bool stored = false;   // a y store is in flight
             auto load_B = [&](int c) {
                 const int sb = c & 1;
@@ -320,61 +325,22 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             ok = tiles_and_G(0);
             for (int c = 0; c < nchunks && ok; ++c) {
                 const uint32_t ph = static_cast<uint32_t>(c & 1);
-                const int sb = c & 1;
-                const uint32_t oCc = oC + sb * 2 * kBlk, oBc = oB + sb * 2 * kBlk;
-                // the previous chunk's epilogue (or the prologue) has written h
-                // and staged that chunk's y: store y (its read of the staging tile
-                // is awaited once Y2 is issued), then Y2 = C h^T: A = C (K-major,
-                // K = n), B = h MN-major (rows n)
-                ok = mbar_wait_bounded(rdy_E, ph, kPolls);
+                // Y = M X once M is in tensor memory and the X tile has landed:
+                // A = M from tensor memory (K = u, 8 columns of packed pairs per
+                // step of 16), B = X MN-major. Every compute warp forms M after the
+                // previous chunk's epilogue, so that epilogue has staged its y by
+                // then: store it (its read of the staging tile is awaited once Y
+                // is issued).
+                ok = mbar_wait_bounded(rdy_M, ph, kPolls) && mbar_wait_bounded(bar_X, ph, kPolls) &&
+                     (c == 0 || mbar_wait_bounded(rdy_E, ph, kPolls));
                 if (!ok) break;
+                pend_X = -1;
                 tc::fence_after_sync();
                 if (c > 0) {
                     tma_store_4d(&tm_y, 0, hh, (c - 1) * kQ, bb, sm + oYs);
                     bulk_commit();
                     stored = true;
                 }
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const uint32_t hb = sbase + (part ? oHl : oHh);
-#pragma unroll
-                    for (int k = 0; k < kNs / 16; ++k) {
-                        const uint32_t offa = (k >> 2) * kBlk + (k & 3) * 32;
-                        tc::mma_bf16(tmem + kColY2, tc::desc_sw128(sbase + oCc + offa, 16, 1024),
-                                     tc::desc_sw128(hb + k * 2048, 1024, 1024), kIdY,
-                                     part > 0 || k > 0);
-                    }
-                }
-                if (c > 0) {
-                    // hand the staging tile back once the store has read it
-                    bulk_wait_read<0>();
-                    mbar_arrive(free_Y);
-                }
-                // S^T = B^T (w o X) once w o X is written: A = the B tile read
-                // MN-major (M = n over two 64-wide blocks 16 KB apart), B = w o X
-                // MN-major; K = u in steps of 16 rows
-                ok = mbar_wait_bounded(rdy_W, ph, kPolls);
-                if (!ok) break;
-                tc::fence_after_sync();
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const uint32_t wx = sbase + (part ? oWl : oWh);
-#pragma unroll
-                    for (int k = 0; k < kQ / 16; ++k) {
-                        const uint32_t off = k * 2048;
-                        tc::mma_bf16(tmem + kColS, tc::desc_sw128(sbase + oBc + off, kBlk, 1024),
-                                     tc::desc_sw128(wx + off, 1024, 1024), kIdS, part > 0 || k > 0);
-                    }
-                }
-                tc::mma_commit(bar_S);
-                pend_S = static_cast<int>(ph);
-                // Y = M X once M is in tensor memory and the X tile has landed:
-                // A = M from tensor memory (K = u, 8 columns of packed pairs per
-                // step of 16), B = X MN-major
-                ok = mbar_wait_bounded(rdy_M, ph, kPolls) && mbar_wait_bounded(bar_X, ph, kPolls);
-                if (!ok) break;
-                pend_X = -1;
-                tc::fence_after_sync();
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
                     const uint32_t am = tmem + (part ? kColMl : kColMh);
@@ -386,11 +352,17 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 }
                 tc::mma_commit(bar_Y);
                 pend_Y = static_cast<int>(ph);
-                // the products of this chunk have completed (in issue order): the
-                // X tile, the B, C buffer and G's columns are free for the next
-                ok = mbar_wait_bounded(bar_Y, ph, kPolls);
+                if (c > 0) {
+                    // hand the staging tile back once the store has read it
+                    bulk_wait_read<0>();
+                    mbar_arrive(free_Y);
+                }
+                // this chunk's products have completed: G and Y (issued here, in
+                // order) and Y2, S (the second producer's): the X tile, the B, C
+                // buffer and G's columns are free for the next
+                ok = mbar_wait_bounded(bar_Y, ph, kPolls) && mbar_wait_bounded(bar_S, ph, kPolls);
                 if (!ok) break;
-                pend_G = pend_S = pend_Y = -1;
+                pend_G = pend_Y = -1;
                 if (c + 1 < nchunks) {
                     load_X(c + 1);
                     ok = tiles_and_G(c + 1);
@@ -419,8 +391,60 @@ ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 }
                 if (pend_X >= 0) mbar_wait_bounded(bar_X, static_cast<uint32_t>(pend_X), kPolls);
                 if (pend_G >= 0) mbar_wait_bounded(bar_G, static_cast<uint32_t>(pend_G), kPolls);
-                if (pend_S >= 0) mbar_wait_bounded(bar_S, static_cast<uint32_t>(pend_S), kPolls);
                 if (pend_Y >= 0) mbar_wait_bounded(bar_Y, static_cast<uint32_t>(pend_Y), kPolls);
+            }
+        }
+    } else if (producer2) {
+        // ---------------- the second producer: Y2 = C h^T and S^T = B^T (w o X) ----------------
+        if (lane == 0) {
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const uint32_t ph = static_cast<uint32_t>(c & 1);
+                const int sb = c & 1;
+                const uint32_t oCc = oC + sb * 2 * kBlk, oBc = oB + sb * 2 * kBlk;
+                const uint32_t pb = static_cast<uint32_t>((c >> 1) & 1);
+                // the chunk's B and C tiles (the first producer reloads a buffer
+                // only after this chunk's S has completed), and h of the previous
+                // chunk's epilogue (or the prologue), which has also read the
+                // previous Y2 and S: Y2 = C h^T, A = C (K-major, K = n), B = h
+                // MN-major (rows n)
+                ok = mbar_wait_bounded(bar_B + sb, pb, kPolls) && mbar_wait_bounded(bar_C + sb, pb, kPolls) &&
+                     mbar_wait_bounded(rdy_E, ph, kPolls);
+                if (!ok) break;
+                tc::fence_after_sync();
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const uint32_t hb = sbase + (part ? oHl : oHh);
+#pragma unroll
+                    for (int k = 0; k < kNs / 16; ++k) {
+                        const uint32_t offa = (k >> 2) * kBlk + (k & 3) * 32;
+                        tc::mma_bf16(tmem + kColY2, tc::desc_sw128(sbase + oCc + offa, 16, 1024),
+                                     tc::desc_sw128(hb + k * 2048, 1024, 1024), kIdY,
+                                     part > 0 || k > 0);
+                    }
+                }
+                // S^T = B^T (w o X) once w o X is written: A = the B tile read
+                // MN-major (M = n over two 64-wide blocks 16 KB apart), B = w o X
+                // MN-major; K = u in steps of 16 rows; the commit covers Y2 too
+                ok = mbar_wait_bounded(rdy_W, ph, kPolls);
+                if (!ok) break;
+                tc::fence_after_sync();
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const uint32_t wx = sbase + (part ? oWl : oWh);
+#pragma unroll
+                    for (int k = 0; k < kQ / 16; ++k) {
+                        const uint32_t off = k * 2048;
+                        tc::mma_bf16(tmem + kColS, tc::desc_sw128(sbase + oBc + off, kBlk, 1024),
+                                     tc::desc_sw128(wx + off, 1024, 1024), kIdS, part > 0 || k > 0);
+                    }
+                }
+                tc::mma_commit(bar_S);
+            }
+            if (!ok) {
+                // let this producer's products in flight complete before the CTA
+                // releases its memory
+                tc::mma_commit(bar_D2);
+                mbar_wait_bounded(bar_D2, 0u, kPolls);
             }
         }
     } else {
