@@ -17,12 +17,13 @@
 //   S  = (w o X)^T B,  w_u = exp(s_Q - s_u) dt_u          (K = Q)
 //   h_out = exp(s_Q) h_in + S
 // This kernel runs one CTA per (batch row, head) over the chunks in order,
-// the state in fp32 registers, with its warps specialised. One producer warp
-// (one thread) requests the TMA tiles (cp.async.bulk.tensor, 128-byte swizzle)
-// and issues the tcgen05.mma products into tensor memory, each group as soon as
-// its operands are ready: G = C B^T once the B and C tiles have landed, Y2 = C
-// h^T once the previous chunk's epilogue has written h, S^T once w o X is
-// written, Y = M X once M is in tensor memory. Sixteen compute warps form dt
+// the state in fp32 registers, with its warps specialised. Two producer warps
+// (one thread each, on two schedulers) issue the tcgen05.mma products into
+// tensor memory, each group as soon as its operands are ready: the first
+// requests the TMA tiles (cp.async.bulk.tensor, 128-byte swizzle) and issues
+// G = C B^T once the B and C tiles have landed and Y = M X once M is in tensor
+// memory; the second Y2 = C h^T once the previous chunk's epilogue has written
+// h and S^T once w o X is written. Sixteen compute warps form dt
 // and its cumulative sum, w o X, M and the epilogue on the CUDA cores (a thread
 // owns one row of every [Q x .] accumulator, the row of its warp's TMEM lane
 // quarter, and a quarter of its columns: warps w, w + 4, w + 8, w + 12 split
@@ -195,8 +196,8 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* tm, int c0, int 
         : "memory");
 }
 
-// (17 warps: one of the four schedulers holds five, so at most 96 registers
-// per thread fit its share of the register file)
+// (18 warps: two of the four schedulers hold five, so at most 96 registers
+// per thread fit their share of the register file)
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
            const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_y,
